@@ -1,0 +1,383 @@
+"""Decode throughput of the GB300 megakernel (one JSON line on rank 0).
+
+Workload (default): the Llama-3.2-1B-shaped decoder at batch 1 -- 16 layers,
+hidden 2048, 32 query / 8 kv heads of 64, SwiGLU FFN 8192, vocab 128256, tied
+LM head, bf16 weights ~N(0, 0.02) from a seed, bf16 KV cache prefilled with
+1024 positions -- decoding greedily: step t feeds the previous step's argmax
+device-to-device and writes cache row 1024 + (t mod 128), so the timed steps
+cycle over the 128-step decode window of the workload.  A step is one launch
+of the persistent kernel over the whole forward pass.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+  python bench.py --impl reference ...   (the CPU oracle on the host cores)
+
+Multi-GPU: replicas only (the path has no exchange step): under torchrun each
+rank decodes its own copy of the workload; value = all ranks' tokens / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tok/s at batch 1 (Llama-1B shape); % of 8 TB/s HBM roofline"
+WINDOW = None  # decode window (steps) of the workload, from the config
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1024)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
+    ap.add_argument("--config", default="llama1b_1k")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ablation", action="store_true", help="also time the per-phase launches")
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def workload_desc(cfg):
+    lo, hi = cfg["prefill"]
+    kv = f"KV prefill {lo}" if lo == hi else f"KV prefill U[{lo},{hi}]"
+    mlp = (f"{cfg['n_experts']} experts x F{cfg['expert_ffn']} top-{cfg['top_k']} + shared "
+           f"F{cfg['shared_ffn']}" if cfg["n_experts"] else f"SwiGLU F{cfg['ffn']}")
+    return (f"{cfg['name']}: {cfg['n_layers']}L H{cfg['hidden']} {cfg['n_q_heads']}q/"
+            f"{cfg['n_kv_heads']}kv d{cfg['head_dim']} {mlp} V{cfg['vocab']}"
+            f"{' tied' if cfg['tied'] else ''}, bf16 weights, batch {cfg['batch']}, {kv}, "
+            f"{cfg['steps']} greedy steps")
+
+
+def step_bytes(cfg, positions, weight_bytes):
+    """Algorithmic HBM bytes of one step: every weight once (routed MoE: the
+    active experts), K and V rows [0, P] read, the new K/V row written, the
+    logits written."""
+    Hkv, d, L, B, V = cfg["n_kv_heads"], cfg["head_dim"], cfg["n_layers"], cfg["batch"], \
+        cfg["vocab"]
+    kv_row = L * Hkv * d * 2 * 2  # K and V, all layers, bytes per position
+    kv = sum((p + 1) * kv_row for p in positions) + B * kv_row
+    return weight_bytes + kv + B * V * 4
+
+
+def kernel_src_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "decode_megakernel_sm_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        j = json.load(open(p))
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def traffic_record(config):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        j = json.load(open(p))
+        e = j.get(config)
+        if e and e.get("kernel_src_sha") == kernel_src_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_uuid=None):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "50"]
+        if device_uuid:
+            cmd += ["-i", device_uuid]
+        try:
+            self.p = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                      text=True)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.p.terminate()
+        out, _ = self.p.communicate(timeout=10)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(cfg, W, ks, vs, lengths, tokens, budget_s=20.0):
+    """The oracle as it stands, on the host cores, on a bounded sample of decode
+    steps of the same workload (at least one step)."""
+    import oracle
+    t0 = time.perf_counter()
+    om = oracle.OracleModel(cfg, W)
+    ko = [oracle._bits(t.cpu()).copy() for t in ks]
+    vo = [oracle._bits(t.cpu()).copy() for t in vs]
+    prep = time.perf_counter() - t0
+    pos = list(lengths)
+    n, t_run = 0, 0.0
+    while True:
+        t1 = time.perf_counter()
+        _, am, _, _ = om.step(ko, vo, tokens, pos)
+        t_run += time.perf_counter() - t1
+        n += 1
+        tokens = [int(a) for a in am]
+        pos = [p + 1 for p in pos]
+        if t_run + t_run / n > budget_s or n >= cfg["steps"]:
+            break
+    B = cfg["batch"]
+    return {"value": n * B / t_run, "unit": "tok/s", "cores": oracle.get_threads(),
+            "kind": "oracle",
+            "sample": f"{n} greedy decode step(s) of the same workload from position "
+                      f"{lengths[0]} ({t_run:.1f} s; host copy of the weights {prep:.1f} s "
+                      f"excluded)"}
+
+
+def run_reference(args, cfg):
+    """--impl reference: the CPU oracle timed on the host cores."""
+    import numpy as np
+    import torch
+    import oracle
+    import synth
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    W = synth.make_weights(cfg, args.seed, "cpu")
+    lengths = synth.make_lengths(cfg, args.seed)
+    ks, vs = synth.make_kv(cfg, lengths, args.seed, "cpu")
+    om = oracle.OracleModel(cfg, W)
+    ko = [oracle._bits(t).copy() for t in ks]
+    vo = [oracle._bits(t).copy() for t in vs]
+    tokens = synth.make_tokens(cfg, args.seed)
+    P0 = list(lengths)
+    t1 = time.perf_counter()
+    om.step(ko, vo, tokens, P0)
+    t_one = time.perf_counter() - t1
+    budget = 120.0
+    k = max(1, min(args.steps, int(budget / max(t_one, 1e-6))))
+    w = min(args.warmup, 1)
+    for i in range(w):
+        om.step(ko, vo, tokens, [p + i for p in P0])
+    t0 = time.perf_counter()
+    toks = tokens
+    for i in range(k):
+        _, am, _, _ = om.step(ko, vo, toks, [p + (i % cfg["steps"]) for p in P0])
+        toks = [int(a) for a in am]
+    el = time.perf_counter() - t0
+    B = cfg["batch"]
+    val = k * B / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "tok/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / k * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": workload_desc(cfg)},
+        "cpu_baseline": {"value": val, "unit": "tok/s", "cores": oracle.get_threads(),
+                         "kind": "oracle",
+                         "sample": f"{k} of {args.steps} requested steps (bounded to ~{budget:.0f}"
+                                   f" s of CPU work), {w} warm-up"},
+        "e2e": {"value": val, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    import synth
+    base = synth.CONFIGS[args.config]
+    cfg = synth.with_cache(base)
+    if args.impl == "reference":
+        run_reference(args, cfg)
+        return
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from decode_megakernel_sm_gb300 import Decoder, MK_ABL_GRAPH, MK_ABL_PDL, MK_ABL_STREAM
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    B, V = cfg["batch"], cfg["vocab"]
+    W = synth.make_weights(cfg, args.seed, dev)
+    lengths = synth.make_lengths(cfg, args.seed)
+    ks, vs = synth.make_kv(cfg, lengths, args.seed, dev)
+    tokens0 = synth.make_tokens(cfg, args.seed)
+    torch.cuda.synchronize()
+    dec = Decoder(cfg, W, ks, vs)
+    dec.build_schedule(B, cfg["max_seq"])
+    info = dec.info()
+    stream = torch.cuda.current_stream()
+    window = cfg["steps"]
+    P0 = torch.tensor(lengths, dtype=torch.int32)
+    pos_table = (P0[None, :] + torch.arange(window, dtype=torch.int32)[:, None]).to(dev)
+    tok0 = torch.tensor(tokens0, dtype=torch.int32, device=dev)
+    am = [torch.empty(B, dtype=torch.int32, device=dev) for _ in range(2)]
+    logits = torch.empty((B, V), dtype=torch.float32, device=dev)
+
+    def run(n, fn=None):
+        for t in range(n):
+            tok = tok0 if t == 0 else am[(t - 1) % 2]
+            if fn is None:
+                dec.step(tok, pos_table[t % window], logits, am[t % 2], stream)
+            else:
+                fn(tok, pos_table[t % window], logits, am[t % 2])
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    run(max(args.warmup, 3))
+    st = dec.sync_status(stream)
+    if st != 0:
+        raise SystemExit(f"device status {st} during warm-up")
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    barrier()
+    clocks = ClockSampler(uuid)
+    time.sleep(0.15)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    run(args.steps)
+    e1.record(stream)
+    barrier()
+    ms = e0.elapsed_time(e1)
+    ck = clocks.stop()
+    st = dec.sync_status(stream)
+    if st != 0:
+        raise SystemExit(f"device status {st} in the timed region")
+    el = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(el, op=dist.ReduceOp.MAX)
+    ms_max = float(el.item())
+    ms_step = ms_max / args.steps
+    value = ws * args.steps * B / (ms_max / 1e3)
+
+    # roofline of the (only) kernel: algorithmic bytes / average launch time
+    per_step = [step_bytes(cfg, [lengths[b] + (t % window) for b in range(B)],
+                           info["weight_bytes_per_step"]) for t in range(args.steps)]
+    alg = sum(per_step) / len(per_step)
+    peak, peak_kind = measured_peak()
+    achieved = alg / (ms / args.steps / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": traffic_record(args.config),
+            "peak_source": peak_kind, "algorithmic_bytes_per_launch": alg,
+            "kernel": "mk::mk_decode_kernel (persistent, 1 launch per step)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "batch": B, "prefill": list(cfg["prefill"]),
+                   "decode_window": window, "parallelism": f"replicas x{ws}",
+                   "l2": "inputs larger than L2 (2.47 GB of weights streamed per step)"},
+        "gpu_launches": args.steps, "roofline": roof, "clocks": ck,
+        "kernel": {"n_sm": info["n_sm"], "ring_stages": info["n_stages"],
+                   "stage_bytes": info["stage_bytes"], "instructions": info["n_instr"],
+                   "attn_splits": info["attn_splits"]},
+    }
+
+    if args.ablation:
+        abl = {}
+        for name, mode in (("stream", MK_ABL_STREAM), ("graph", MK_ABL_GRAPH),
+                           ("pdl", MK_ABL_PDL)):
+            n = min(args.steps, 256)
+            fn = (lambda m: (lambda t, p, lg, a: dec.step_ablation(m, t, p, lg, a, stream)))(mode)
+            run(3, fn)
+            barrier()
+            e0.record(stream)
+            run(n, fn)
+            e1.record(stream)
+            barrier()
+            abl[name] = e0.elapsed_time(e1) / n
+            if dec.sync_status(stream) != 0:
+                abl[name] = None
+        line["ablation_ms_per_step"] = abl
+        line["ablation_launches_per_step"] = info["ablation_launches"]
+
+    if not args.no_e2e:
+        # the public host-buffer call: pinned inputs in, logits + argmax out, every step
+        n = min(args.steps, 256)
+        htok = torch.tensor(tokens0, dtype=torch.int32).pin_memory()
+        hpos = torch.empty(B, dtype=torch.int32).pin_memory()
+        hlg = torch.empty((B, V), dtype=torch.float32).pin_memory()
+        ham = torch.empty(B, dtype=torch.int32).pin_memory()
+        for t in range(3):
+            hpos.copy_(pos_table[t % window].cpu())
+            dec.step_host(htok, hpos, hlg, ham)
+        barrier()
+        host_pos = pos_table.cpu()
+        t0 = time.perf_counter()
+        for t in range(n):
+            hpos.copy_(host_pos[t % window])
+            stt = dec.step_host(htok, hpos, hlg, ham)
+            if stt != 0:
+                raise SystemExit(f"host step status {stt}")
+            htok.copy_(ham)
+        el2 = torch.tensor([time.perf_counter() - t0], dtype=torch.float64, device=dev)
+        if ws > 1:
+            dist.all_reduce(el2, op=dist.ReduceOp.MAX)
+        line["e2e"] = {"value": ws * n * B / float(el2.item()), "unit": "tok/s",
+                       "h2d_bytes_per_step": 2 * B * 4, "d2h_bytes_per_step": B * V * 4 + B * 4,
+                       "steps": n}
+
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, W, ks, vs, lengths, tokens0)
+
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    dec.close()
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,628 @@
+// api.cu -- the C ABI of libmk.so (declared in include/mk.h): handle life
+// cycle, weight packing, schedule upload, the one-launch decode step, the
+// host-buffer step, the per-phase ablation launcher and error reporting.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <new>
+#include <tuple>
+#include <vector>
+
+#include "mk_internal.h"
+
+namespace mk {
+cudaError_t pack_qkv(uint16_t* dst, const void* wq, const void* wk, const void* wv, int H, int Hkv,
+                     int HPG, int D, cudaStream_t s);
+cudaError_t pack_interleave(uint16_t* dst, const void* a, const void* b, long rows, int H,
+                            cudaStream_t s);
+cudaError_t pack_wo(uint16_t* dst, const void* wo, int H, int Hq, int D, cudaStream_t s);
+cudaError_t pack_transpose(uint16_t* dst, const void* src, int R, int C, int batch,
+                           cudaStream_t s);
+
+extern const Variant variant_h256_d64_g2_b1;
+extern const Variant variant_h2048_d64_g4_b1;
+extern const Variant variant_h2048_d64_g4_b8;
+extern const Variant variant_h2048_d128_g4_b1;
+}  // namespace mk
+
+using namespace mk;
+
+struct mk_handle {
+  mk_model_desc d{};
+  int dev = 0, n_sm = 0;
+  const Variant* var = nullptr;
+  int n_stages = 0, smem_bytes = 0;
+  void* packed = nullptr;
+  size_t packed_bytes = 0;
+  std::vector<LayerPtrs> layers_h;
+  LayerPtrs* layers_d = nullptr;
+  const uint16_t *embed = nullptr, *lm_head = nullptr, *final_norm = nullptr;
+  float* rope = nullptr;
+  // schedule and scratch
+  int batch = 0, max_ctx = 0;
+  PlanOut plan;
+  Instr* sched = nullptr;
+  void* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  float *xbuf = nullptr, *qbuf = nullptr, *part = nullptr, *rlog = nullptr, *lm_val = nullptr;
+  int* lm_idx = nullptr;
+  uint32_t* ctr = nullptr;
+  int* err = nullptr;
+  size_t xbuf_bytes = 0, ctr_bytes = 0;
+  std::vector<int> abl_keys;  // ablation launches (keys that own instructions)
+  uint32_t epoch = 0;
+  unsigned long long timeout_ns = 2000000000ull;
+  // host-buffer step
+  cudaStream_t own = nullptr;
+  int32_t *d_tok = nullptr, *d_pos = nullptr, *d_am = nullptr;
+  float* d_logits = nullptr;
+  int* h_err = nullptr;  // pinned [4]
+  // graph-mode ablation cache
+  std::map<std::tuple<const void*, const void*, const void*, const void*, const void*>,
+           cudaGraphExec_t>
+      graphs;
+};
+
+#define CK(x)                                \
+  do {                                       \
+    cudaError_t e_ = (x);                    \
+    if (e_ != cudaSuccess) return MK_ERR_CUDA; \
+  } while (0)
+
+static size_t al256(size_t x) { return (x + 255) / 256 * 256; }
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+static const Variant* pick_variant(const mk_model_desc& d) {
+  const Variant* all[] = {&variant_h256_d64_g2_b1, &variant_h2048_d64_g4_b1,
+                          &variant_h2048_d64_g4_b8, &variant_h2048_d128_g4_b1};
+  const int HPG = d.n_q_heads / d.n_kv_heads;
+  const Variant* best = nullptr;
+  for (const Variant* v : all) {
+    if (v->H != d.hidden || v->D != d.head_dim || v->HPG != HPG) continue;
+    if (v->NB < d.max_batch) continue;
+    if (!best || v->NB < best->NB) best = v;
+  }
+  if (best && d.n_experts > 0 && best->NB != 1) return nullptr;  // MoE routing is per token
+  return best;
+}
+
+static void free_schedule(mk_handle* h) {
+  for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
+  h->graphs.clear();
+  if (h->sched) cudaFree(h->sched);
+  if (h->scratch) cudaFree(h->scratch);
+  h->sched = nullptr;
+  h->scratch = nullptr;
+  if (h->d_tok) cudaFree(h->d_tok);
+  h->d_tok = h->d_pos = h->d_am = nullptr;
+  h->d_logits = nullptr;
+  h->batch = 0;
+}
+
+static void free_all(mk_handle* h) {
+  if (!h) return;
+  free_schedule(h);
+  if (h->packed) cudaFree(h->packed);
+  if (h->layers_d) cudaFree(h->layers_d);
+  if (h->rope) cudaFree(h->rope);
+  if (h->h_err) cudaFreeHost(h->h_err);
+  if (h->own) cudaStreamDestroy(h->own);
+  delete h;
+}
+
+// Packed-buffer sizes (elements) of one layer, in carve order.
+struct LayerSizes {
+  size_t norm, qkv, wo, gu, dT, router, ex_gu, ex_dT, sh_gu, sh_dT;
+};
+
+static LayerSizes layer_sizes(const mk_model_desc& d) {
+  const size_t H = d.hidden, D = d.head_dim, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
+  const size_t HPG = Hq / Hkv;
+  LayerSizes s{};
+  s.norm = H;
+  s.qkv = Hkv * (HPG + 2) * D * H;
+  s.wo = Hq * H * D;
+  if (d.n_experts == 0) {
+    s.gu = 2 * (size_t)d.ffn * H;
+    s.dT = (size_t)d.ffn * H;
+  } else {
+    s.router = (size_t)d.n_experts * H;
+    s.ex_gu = 2 * (size_t)d.n_experts * d.expert_ffn * H;
+    s.ex_dT = (size_t)d.n_experts * d.expert_ffn * H;
+    s.sh_gu = 2 * (size_t)d.shared_ffn * H;
+    s.sh_dT = (size_t)d.shared_ffn * H;
+  }
+  return s;
+}
+
+static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv,
+                       mk_handle* h) {
+  const mk_model_desc& d = *desc;
+  h->d = d;
+  int rc = plan_shape_ok(d);
+  if (rc) return rc;
+  h->var = pick_variant(d);
+  if (!h->var) return MK_ERR_UNSUPPORTED;
+  const int L = d.n_layers, H = d.hidden, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
+  const int D = d.head_dim, HPG = Hq / Hkv;
+  const bool moe = d.n_experts > 0;
+  // ---- argument checks (pointers present and 16-byte aligned)
+  if (!w || !kv || !kv->k || !kv->v || !w->embed || !w->final_norm || !w->attn_norm || !w->wq ||
+      !w->wk || !w->wv || !w->wo || !w->mlp_norm)
+    return MK_ERR_INVALID_ARG;
+  if (!d.tied_lm_head && !w->lm_head) return MK_ERR_INVALID_ARG;
+  if (!moe && (!w->w_gate || !w->w_up || !w->w_down)) return MK_ERR_INVALID_ARG;
+  if (moe && (!w->router || !w->ex_gate || !w->ex_up || !w->ex_down)) return MK_ERR_INVALID_ARG;
+  if (moe && d.shared_ffn > 0 && (!w->sh_gate || !w->sh_up || !w->sh_down))
+    return MK_ERR_INVALID_ARG;
+  auto okp = [](const void* p) { return p && aligned16(p); };
+  if (!okp(w->embed) || !okp(w->final_norm) || (!d.tied_lm_head && !okp(w->lm_head)))
+    return MK_ERR_INVALID_ARG;
+  for (int l = 0; l < L; l++) {
+    if (!okp(w->attn_norm[l]) || !okp(w->wq[l]) || !okp(w->wk[l]) || !okp(w->wv[l]) ||
+        !okp(w->wo[l]) || !okp(w->mlp_norm[l]) || !okp(kv->k[l]) || !okp(kv->v[l]))
+      return MK_ERR_INVALID_ARG;
+    if (!moe && (!okp(w->w_gate[l]) || !okp(w->w_up[l]) || !okp(w->w_down[l])))
+      return MK_ERR_INVALID_ARG;
+    if (moe && (!okp(w->router[l]) || !okp(w->ex_gate[l]) || !okp(w->ex_up[l]) ||
+                !okp(w->ex_down[l])))
+      return MK_ERR_INVALID_ARG;
+    if (moe && d.shared_ffn > 0 &&
+        (!okp(w->sh_gate[l]) || !okp(w->sh_up[l]) || !okp(w->sh_down[l])))
+      return MK_ERR_INVALID_ARG;
+  }
+  // ---- device
+  CK(cudaGetDevice(&h->dev));
+  int optin = 0;
+  CK(cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, h->dev));
+  CK(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->dev));
+  const int K = moe ? d.top_k : 0;
+  int ns = 0;
+  for (int n = 2; n <= 8; n++)
+    if (smem_layout(n, h->var->NB, H, D, HPG, K).total <= optin) ns = n;
+  if (ns < 2) return MK_ERR_UNSUPPORTED;
+  h->n_stages = ns;
+  h->smem_bytes = smem_layout(ns, h->var->NB, H, D, HPG, K).total;
+  CK(cudaFuncSetAttribute(h->var->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                          h->smem_bytes));
+  int per_sm = 0;
+  CK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, h->var->kernel, NTHREADS,
+                                                   h->smem_bytes));
+  if (per_sm < 1) return MK_ERR_UNSUPPORTED;
+  CK(cudaStreamCreateWithFlags(&h->own, cudaStreamNonBlocking));
+  CK(cudaMallocHost(&h->h_err, 4 * sizeof(int)));
+
+  // ---- packed weight buffer
+  const LayerSizes ls = layer_sizes(d);
+  const size_t V = d.vocab;
+  size_t per_layer = 0;
+  for (size_t e : {ls.norm, ls.norm, ls.qkv, ls.wo, ls.gu, ls.dT, ls.router, ls.ex_gu, ls.ex_dT,
+                   ls.sh_gu, ls.sh_dT})
+    per_layer += al256(e * 2);
+  const size_t total = per_layer * L + al256(V * H * 2) * (d.tied_lm_head ? 1 : 2) + al256(H * 2);
+  CK(cudaMalloc(&h->packed, total));
+  h->packed_bytes = total;
+  char* p = (char*)h->packed;
+  auto take = [&](size_t elems) {
+    uint16_t* r = (uint16_t*)p;
+    p += al256(elems * 2);
+    return r;
+  };
+  cudaStream_t s = h->own;
+  h->layers_h.resize(L);
+  for (int l = 0; l < L; l++) {
+    LayerPtrs& lp = h->layers_h[l];
+    std::memset(&lp, 0, sizeof lp);
+    uint16_t* an = take(ls.norm);
+    uint16_t* mn = take(ls.norm);
+    uint16_t* qkv = take(ls.qkv);
+    uint16_t* wo = take(ls.wo);
+    uint16_t* gu = take(ls.gu);
+    uint16_t* dT = take(ls.dT);
+    uint16_t* rt = take(ls.router);
+    uint16_t* egu = take(ls.ex_gu);
+    uint16_t* edT = take(ls.ex_dT);
+    uint16_t* sgu = take(ls.sh_gu);
+    uint16_t* sdT = take(ls.sh_dT);
+    CK(cudaMemcpyAsync(an, w->attn_norm[l], ls.norm * 2, cudaMemcpyDeviceToDevice, s));
+    CK(cudaMemcpyAsync(mn, w->mlp_norm[l], ls.norm * 2, cudaMemcpyDeviceToDevice, s));
+    CK(pack_qkv(qkv, w->wq[l], w->wk[l], w->wv[l], H, Hkv, HPG, D, s));
+    CK(pack_wo(wo, w->wo[l], H, Hq, D, s));
+    if (!moe) {
+      CK(pack_interleave(gu, w->w_gate[l], w->w_up[l], d.ffn, H, s));
+      CK(pack_transpose(dT, w->w_down[l], H, d.ffn, 1, s));
+    } else {
+      CK(cudaMemcpyAsync(rt, w->router[l], ls.router * 2, cudaMemcpyDeviceToDevice, s));
+      CK(pack_interleave(egu, w->ex_gate[l], w->ex_up[l], (long)d.n_experts * d.expert_ffn, H,
+                         s));
+      CK(pack_transpose(edT, w->ex_down[l], H, d.expert_ffn, d.n_experts, s));
+      if (d.shared_ffn > 0) {
+        CK(pack_interleave(sgu, w->sh_gate[l], w->sh_up[l], d.shared_ffn, H, s));
+        CK(pack_transpose(sdT, w->sh_down[l], H, d.shared_ffn, 1, s));
+      }
+    }
+    lp.attn_norm = an;
+    lp.mlp_norm = mn;
+    lp.wqkv = qkv;
+    lp.wo = wo;
+    lp.wgu = moe ? nullptr : gu;
+    lp.wdT = moe ? nullptr : dT;
+    lp.router = moe ? rt : nullptr;
+    lp.ex_gu = moe ? egu : nullptr;
+    lp.ex_dT = moe ? edT : nullptr;
+    lp.sh_gu = moe && d.shared_ffn > 0 ? sgu : nullptr;
+    lp.sh_dT = moe && d.shared_ffn > 0 ? sdT : nullptr;
+    lp.kc = (uint16_t*)kv->k[l];
+    lp.vc = (uint16_t*)kv->v[l];
+  }
+  uint16_t* emb = take(V * H);
+  CK(cudaMemcpyAsync(emb, w->embed, V * H * 2, cudaMemcpyDeviceToDevice, s));
+  h->embed = emb;
+  if (d.tied_lm_head) {
+    h->lm_head = emb;
+  } else {
+    uint16_t* lm = take(V * H);
+    CK(cudaMemcpyAsync(lm, w->lm_head, V * H * 2, cudaMemcpyDeviceToDevice, s));
+    h->lm_head = lm;
+  }
+  uint16_t* fn = take(H);
+  CK(cudaMemcpyAsync(fn, w->final_norm, (size_t)H * 2, cudaMemcpyDeviceToDevice, s));
+  h->final_norm = fn;
+  CK(cudaMalloc(&h->layers_d, sizeof(LayerPtrs) * L));
+  CK(cudaMemcpyAsync(h->layers_d, h->layers_h.data(), sizeof(LayerPtrs) * L,
+                     cudaMemcpyHostToDevice, s));
+  // rotary table: angle p * theta^(-2t/D) evaluated in double, stored fp32
+  std::vector<float> rope((size_t)d.max_seq * D);
+  for (int pp = 0; pp < d.max_seq; pp++)
+    for (int t = 0; t < D / 2; t++) {
+      const double ang = (double)pp * std::pow((double)d.rope_theta, -2.0 * t / (double)D);
+      rope[((size_t)pp * (D / 2) + t) * 2 + 0] = (float)std::cos(ang);
+      rope[((size_t)pp * (D / 2) + t) * 2 + 1] = (float)std::sin(ang);
+    }
+  CK(cudaMalloc(&h->rope, rope.size() * sizeof(float)));
+  CK(cudaMemcpyAsync(h->rope, rope.data(), rope.size() * sizeof(float), cudaMemcpyHostToDevice,
+                     s));
+  CK(cudaStreamSynchronize(s));
+  return MK_OK;
+}
+
+extern "C" int mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv,
+                         mk_handle** out) {
+  if (!out) return MK_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!desc) return MK_ERR_INVALID_ARG;
+  mk_handle* h = new (std::nothrow) mk_handle();
+  if (!h) return MK_ERR_INVALID_ARG;
+  const int rc = create_impl(desc, w, kv, h);
+  if (rc != MK_OK) {
+    free_all(h);
+    cudaGetLastError();
+    return rc;
+  }
+  *out = h;
+  return MK_OK;
+}
+
+// ------------------------------------------------------------- schedule ----
+extern "C" int mk_build_schedule(mk_handle* h, int batch, int max_ctx) {
+  if (!h) return MK_ERR_INVALID_ARG;
+  CK(cudaStreamSynchronize(h->own));
+  free_schedule(h);
+  PlanOut p;
+  int rc = plan_build(h->d, batch, max_ctx, h->n_sm, p);
+  if (rc) return rc;
+  if (plan_verify(h->d, batch, p)) return MK_ERR_SCHEDULE;
+  if (plan_check(p.q.data(), h->n_sm, p.max_pc, p.n_ctr)) return MK_ERR_SCHEDULE;
+  const mk_model_desc& d = h->d;
+  const size_t L = d.n_layers, B = batch, H = d.hidden, Hq = d.n_q_heads, D = d.head_dim;
+  const size_t E = d.n_experts > 0 ? d.n_experts : 1;
+  const size_t sx = al256(2 * 2 * L * B * H * 4), sq = al256(L * B * Hq * D * 4);
+  const size_t sp = al256(L * B * Hq * (size_t)p.splits * (D + 2) * 4);
+  const size_t sr = al256(L * B * E * 4), sl = al256((size_t)p.n_lm * B * 4);
+  const size_t sc = al256((size_t)p.n_ctr * 4), se = 256;
+  const size_t total = sx + sq + sp + sr + 2 * sl + sc + se;
+  CK(cudaMalloc(&h->scratch, total));
+  h->scratch_bytes = total;
+  char* q = (char*)h->scratch;
+  h->xbuf = (float*)q; q += sx;
+  h->qbuf = (float*)q; q += sq;
+  h->part = (float*)q; q += sp;
+  h->rlog = (float*)q; q += sr;
+  h->lm_val = (float*)q; q += sl;
+  h->lm_idx = (int*)q; q += sl;
+  h->ctr = (uint32_t*)q; q += sc;
+  h->err = (int*)q;
+  h->xbuf_bytes = sx;
+  h->ctr_bytes = sc;
+  CK(cudaMemsetAsync(h->scratch, 0, total, h->own));
+  CK(cudaMalloc(&h->sched, p.q.size() * sizeof(Instr)));
+  CK(cudaMemcpyAsync(h->sched, p.q.data(), p.q.size() * sizeof(Instr), cudaMemcpyHostToDevice,
+                     h->own));
+  // staging of the host-buffer step: tokens, positions, argmax, logits
+  const size_t st = al256(B * 4) * 3 + al256(B * (size_t)d.vocab * 4);
+  CK(cudaMalloc(&h->d_tok, st));
+  h->d_pos = (int32_t*)((char*)h->d_tok + al256(B * 4));
+  h->d_am = (int32_t*)((char*)h->d_pos + al256(B * 4));
+  h->d_logits = (float*)((char*)h->d_am + al256(B * 4));
+  std::vector<char> has(L * N_PHASES + 1, 0);
+  for (const Instr& I : p.q) {
+    if (I.op == OP_HALT || I.op == OP_NOP) continue;
+    has[I.op == OP_LMHEAD ? L * N_PHASES : I.layer * N_PHASES + phase_of(I.op)] = 1;
+  }
+  h->abl_keys.clear();
+  for (size_t k = 0; k < has.size(); k++)
+    if (has[k]) h->abl_keys.push_back((int)k);
+  h->plan = std::move(p);
+  h->batch = batch;
+  h->max_ctx = max_ctx;
+  h->epoch = 0;
+  CK(cudaStreamSynchronize(h->own));
+  return MK_OK;
+}
+
+static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_t* pos,
+                            float* logits, int32_t* am) {
+  const mk_model_desc& d = h->d;
+  Globals g;
+  std::memset(&g, 0, sizeof g);
+  g.sched = h->sched;
+  g.layers = h->layers_d;
+  g.embed = h->embed;
+  g.lm_head = h->lm_head;
+  g.final_norm = h->final_norm;
+  g.rope = h->rope;
+  g.xbuf = h->xbuf;
+  g.qbuf = h->qbuf;
+  g.part = h->part;
+  g.rlog = h->rlog;
+  g.lm_val = h->lm_val;
+  g.lm_idx = h->lm_idx;
+  g.ctr = h->ctr;
+  g.err = h->err;
+  g.tokens = tok;
+  g.positions = pos;
+  g.logits = logits;
+  g.argmax = am;
+  g.timeout_ns = h->timeout_ns;
+  g.max_pc = h->plan.max_pc;
+  g.n_sm = h->n_sm;
+  g.n_stages = h->n_stages;
+  g.B = h->batch;
+  g.H = d.hidden;
+  g.Hq = d.n_q_heads;
+  g.Hkv = d.n_kv_heads;
+  g.D = d.head_dim;
+  g.F = d.ffn;
+  g.V = d.vocab;
+  g.L = d.n_layers;
+  g.max_seq = d.max_seq;
+  g.max_ctx = h->max_ctx;
+  g.splits = h->plan.splits;
+  g.E = d.n_experts;
+  g.K = d.n_experts > 0 ? d.top_k : 0;
+  g.Fe = d.expert_ffn;
+  g.Fs = d.shared_ffn;
+  g.eps = d.rms_eps;
+  g.lm_ctr = CtrMap{d.n_kv_heads, d.n_layers}.lm();
+  g.n_lm = h->plan.n_lm;
+  g.sel_key = -1;
+  return g;
+}
+
+static cudaError_t launch_mega(const mk_handle* h, Globals& g, cudaStream_t s) {
+  void* args[] = {&g};
+  return cudaLaunchCooperativeKernel(h->var->kernel, dim3(h->n_sm), dim3(NTHREADS), args,
+                                     (size_t)h->smem_bytes, s);
+}
+
+extern "C" int mk_decode_step(mk_handle* h, const int32_t* d_tokens, const int32_t* d_positions,
+                              float* d_logits, int32_t* d_argmax, void* stream) {
+  if (!h) return MK_ERR_INVALID_ARG;
+  if (!h->sched) return MK_ERR_NOT_READY;
+  if (!d_tokens || !d_positions || !d_logits || !d_argmax) return MK_ERR_INVALID_ARG;
+  Globals g = make_globals(h, d_tokens, d_positions, d_logits, d_argmax);
+  g.epoch = ++h->epoch;
+  g.parity = (int)(g.epoch & 1u);
+  g.zero_next = 1;
+  CK(launch_mega(h, g, (cudaStream_t)stream));
+  return MK_OK;
+}
+
+static void reset_after_error(mk_handle* h) {
+  cudaMemset(h->ctr, 0, h->ctr_bytes);
+  cudaMemset(h->xbuf, 0, h->xbuf_bytes);
+  cudaMemset(h->err, 0, 4 * sizeof(int));
+  cudaDeviceSynchronize();
+  h->epoch = 0;
+}
+
+extern "C" int mk_decode_step_host(mk_handle* h, const int32_t* h_tokens,
+                                   const int32_t* h_positions, float* h_logits,
+                                   int32_t* h_argmax) {
+  if (!h) return MK_ERR_INVALID_ARG;
+  if (!h->sched) return MK_ERR_NOT_READY;
+  if (!h_tokens || !h_positions || !h_argmax) return MK_ERR_INVALID_ARG;
+  const int B = h->batch;
+  for (int b = 0; b < B; b++)
+    if (h_tokens[b] < 0 || h_tokens[b] >= h->d.vocab || h_positions[b] < 0 ||
+        h_positions[b] >= h->max_ctx)
+      return MK_ERR_INVALID_ARG;
+  cudaStream_t s = h->own;
+  CK(cudaMemcpyAsync(h->d_tok, h_tokens, B * 4, cudaMemcpyHostToDevice, s));
+  CK(cudaMemcpyAsync(h->d_pos, h_positions, B * 4, cudaMemcpyHostToDevice, s));
+  Globals g = make_globals(h, h->d_tok, h->d_pos, h->d_logits, h->d_am);
+  g.epoch = ++h->epoch;
+  g.parity = (int)(g.epoch & 1u);
+  g.zero_next = 1;
+  CK(launch_mega(h, g, s));
+  if (h_logits)
+    CK(cudaMemcpyAsync(h_logits, h->d_logits, (size_t)B * h->d.vocab * 4, cudaMemcpyDeviceToHost,
+                       s));
+  CK(cudaMemcpyAsync(h_argmax, h->d_am, B * 4, cudaMemcpyDeviceToHost, s));
+  CK(cudaMemcpyAsync(h->h_err, h->err, 4 * sizeof(int), cudaMemcpyDeviceToHost, s));
+  CK(cudaStreamSynchronize(s));
+  if (h->h_err[0] != 0) {
+    const int code = h->h_err[0];
+    reset_after_error(h);
+    return code;
+  }
+  return MK_OK;
+}
+
+// ------------------------------------------------------------- ablation ----
+static cudaError_t launch_phases(mk_handle* h, Globals g, cudaStream_t s, bool pdl) {
+  for (size_t i = 0; i < h->abl_keys.size(); i++) {
+    g.sel_key = h->abl_keys[i];
+    g.zero_next = g.zero_next && i == 0;
+    g.pdl = pdl ? 1 : 0;
+    void* args[] = {&g};
+    cudaError_t e;
+    if (pdl) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(h->n_sm);
+      cfg.blockDim = dim3(NTHREADS);
+      cfg.dynamicSmemBytes = (size_t)h->smem_bytes;
+      cfg.stream = s;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      at[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      e = cudaLaunchKernelExC(&cfg, h->var->kernel, args);
+    } else {
+      e = cudaLaunchKernel(h->var->kernel, dim3(h->n_sm), dim3(NTHREADS), args,
+                           (size_t)h->smem_bytes, s);
+    }
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+extern "C" int mk_decode_step_ablation(mk_handle* h, int mode, const int32_t* d_tokens,
+                                       const int32_t* d_positions, float* d_logits,
+                                       int32_t* d_argmax, void* stream) {
+  if (!h) return MK_ERR_INVALID_ARG;
+  if (!h->sched) return MK_ERR_NOT_READY;
+  if (!d_tokens || !d_positions || !d_logits || !d_argmax) return MK_ERR_INVALID_ARG;
+  if (mode != MK_ABL_STREAM && mode != MK_ABL_GRAPH && mode != MK_ABL_PDL)
+    return MK_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  Globals g = make_globals(h, d_tokens, d_positions, d_logits, d_argmax);
+  if (mode != MK_ABL_GRAPH) {
+    g.epoch = ++h->epoch;
+    g.parity = (int)(g.epoch & 1u);
+    g.zero_next = 1;
+    CK(launch_phases(h, g, s, mode == MK_ABL_PDL));
+    return MK_OK;
+  }
+  // Graph mode: a self-contained replay -- zero the counters and both
+  // residual sets, then run the step as epoch 1 (parity 1).
+  auto key = std::make_tuple((const void*)d_tokens, (const void*)d_positions, (const void*)d_logits,
+                             (const void*)d_argmax, (const void*)h->sched);
+  auto it = h->graphs.find(key);
+  if (it == h->graphs.end()) {
+    CK(cudaStreamSynchronize(h->own));
+    g.epoch = 1;
+    g.parity = 1;
+    g.zero_next = 0;
+    cudaGraph_t graph = nullptr;
+    CK(cudaStreamBeginCapture(h->own, cudaStreamCaptureModeThreadLocal));
+    cudaError_t e1 = cudaMemsetAsync(h->ctr, 0, h->ctr_bytes, h->own);
+    cudaError_t e2 = cudaMemsetAsync(h->xbuf, 0, h->xbuf_bytes, h->own);
+    cudaError_t e3 = launch_phases(h, g, h->own, false);
+    cudaError_t e4 = cudaStreamEndCapture(h->own, &graph);
+    if (e1 || e2 || e3 || e4) {
+      if (graph) cudaGraphDestroy(graph);
+      cudaGetLastError();
+      return MK_ERR_CUDA;
+    }
+    cudaGraphExec_t exec = nullptr;
+    cudaError_t e5 = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e5 != cudaSuccess) return MK_ERR_CUDA;
+    it = h->graphs.emplace(key, exec).first;
+  }
+  CK(cudaGraphLaunch(it->second, s));
+  h->epoch = 1;  // counters now stand at one step; parity-0 residuals are zero
+  return MK_OK;
+}
+
+// --------------------------------------------------------------- status ----
+extern "C" int mk_sync_status(mk_handle* h, void* stream) {
+  if (!h) return MK_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MK_ERR_CUDA;
+  if (!h->err) return MK_OK;
+  if (cudaMemcpy(h->h_err, h->err, 4 * sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MK_ERR_CUDA;
+  if (h->h_err[0] != 0) {
+    const int code = h->h_err[0];
+    reset_after_error(h);
+    return code;
+  }
+  return MK_OK;
+}
+
+extern "C" int mk_set_wait_timeout(mk_handle* h, uint64_t ns) {
+  if (!h || ns < 1000) return MK_ERR_INVALID_ARG;
+  h->timeout_ns = ns;
+  for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
+  h->graphs.clear();
+  return MK_OK;
+}
+
+extern "C" int mk_get_info(const mk_handle* h, mk_info* out) {
+  if (!h || !out) return MK_ERR_INVALID_ARG;
+  std::memset(out, 0, sizeof *out);
+  out->n_sm = h->n_sm;
+  out->stage_bytes = STAGE_BYTES;
+  out->n_stages = h->n_stages;
+  out->smem_bytes = h->smem_bytes;
+  out->max_pc = h->plan.max_pc;
+  out->n_instr = h->plan.n_instr;
+  out->n_counters = h->plan.n_ctr;
+  out->attn_splits = h->plan.splits;
+  out->launches_per_step = 1;
+  out->ablation_launches = (int)h->abl_keys.size();
+  out->batch = h->batch;
+  out->max_ctx = h->max_ctx;
+  out->packed_bytes = h->packed_bytes;
+  out->scratch_bytes = h->scratch_bytes;
+  out->weight_bytes_per_step = h->plan.weight_bytes;
+  return MK_OK;
+}
+
+extern "C" int mk_debug_drop_instruction(mk_handle* h, int sm, int pc) {
+  if (!h) return MK_ERR_INVALID_ARG;
+  if (!h->sched) return MK_ERR_NOT_READY;
+  if (sm < 0 || sm >= h->n_sm || pc < 0 || pc >= h->plan.max_pc) return MK_ERR_INVALID_ARG;
+  const size_t i = (size_t)sm * h->plan.max_pc + pc;
+  Instr& I = h->plan.q[i];
+  if (I.op == OP_HALT) return MK_ERR_INVALID_ARG;
+  I.op = OP_NOP;
+  CK(cudaMemcpy(h->sched + i, &I, sizeof(Instr), cudaMemcpyHostToDevice));
+  return MK_OK;
+}
+
+extern "C" int mk_destroy(mk_handle* h) {
+  if (!h) return MK_ERR_INVALID_ARG;
+  if (h->own) cudaStreamSynchronize(h->own);
+  free_all(h);
+  return MK_OK;
+}
+
+extern "C" const char* mk_status_string(int status) {
+  switch (status) {
+    case MK_OK: return "ok";
+    case MK_ERR_INVALID_ARG: return "invalid argument";
+    case MK_ERR_CUDA: return "CUDA runtime error";
+    case MK_ERR_UNSUPPORTED: return "unsupported shape (no compiled kernel variant)";
+    case MK_ERR_SCHEDULE: return "schedule failed its deadlock or coverage check";
+    case MK_ERR_TIMEOUT: return "a device wait exceeded its time limit";
+    case MK_ERR_NOT_READY: return "no schedule built";
+    case MK_ERR_DEVICE: return "device reported an internal inconsistency";
+    default: return "unknown status";
+  }
+}

@@ -1,0 +1,958 @@
+// megakernel.cuh -- the persistent decode interpreter for sm_103a.
+//
+// One CTA per SM runs its queue of opcoded instructions in order ("Megakernels:
+// Deleting the Kernel Boundary", section "One launch, one interpreter").
+// The CTA has NCW consumer warps and one producer warp.  The producer walks
+// the same queue ahead of the consumers and issues non-multicast TMA bulk
+// copies (cp.async.bulk) of every instruction's weight rows -- and of the
+// cached K/V rows of attention work items -- into a ring of shared-memory
+// stages guarded by full/empty mbarriers.  Weight loads never wait on a
+// counter, so the ring keeps HBM busy while the consumers wait for the
+// activations of their next instruction; this is the GB300 form of the
+// pages' paged shared memory and load/compute/store/finish overlap (section
+// "Correctness without the free barrier", last paragraph, and the hook
+// template of "One launch, one interpreter").
+//
+// Template parameters: HT hidden size, D head dim, HPG query heads per kv
+// head, NB batch capacity of the compiled variant (rows b >= B are masked).
+#pragma once
+#include "mk_device.cuh"
+
+namespace mk {
+
+template <int HT, int D, int HPG, int NB>
+struct Ctx {
+  float* xn;    // [NB][HT] normalised activation of the current instruction
+  float* yrow;  // [NB][MAX_ROWS] row outputs / attention merge scratch
+  float* hbuf;  // [NB][MAX_COLS] SiLU(gate)*up of an MLP slice
+  float* attn;  // [NB][D] reduced attention output of one head
+  float* red;   // reduction scratch
+  int* tok;     // [NB]
+  int* pos;     // [NB]
+  int* topk;    // [NB][K] routed expert ids
+  float* topw;  // [NB][K] routed expert weights
+  Ring ring;
+  int tid, warp, lane;
+  int pc;
+};
+
+// Residual stream x_j, j in [1, 2L] (x_0 is the embedding row).
+MK_DEV float* xres(const Globals& g, int j, int b) {
+  return g.xbuf + (((size_t)g.parity * 2 * g.L + (size_t)(j - 1)) * g.B + b) * (size_t)g.H;
+}
+
+// The weight / cache byte ranges an instruction streams, in ring order.
+// The producer issues exactly these copies; the consumers consume exactly
+// these stages.  Returns the number of segments (0..2).
+template <int HT, int D>
+MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int* topk, Seg* s) {
+  constexpr uint32_t ROW = HT * 2;
+  constexpr uint32_t RPS = STAGE_BYTES / ROW;
+  const LayerPtrs* Lp = g.layers + (I.op == OP_LMHEAD ? 0 : I.layer);
+  const uint32_t n = I.r1 - I.r0;
+  switch (I.op) {
+    case OP_QKV:
+      s[0] = {(const unsigned char*)(Lp->wqkv + (size_t)I.r0 * HT), nullptr, ROW, n, RPS};
+      return 1;
+    case OP_OPROJ:
+      s[0] = {(const unsigned char*)(Lp->wo + ((size_t)I.g * HT + I.r0) * D), nullptr, D * 2, n,
+              STAGE_BYTES / (D * 2)};
+      return 1;
+    case OP_ROUTER:
+      s[0] = {(const unsigned char*)(Lp->router + (size_t)I.r0 * HT), nullptr, ROW, n, RPS};
+      return 1;
+    case OP_MLP: {
+      const uint16_t *gu, *dT;
+      if (g.E == 0) {
+        gu = Lp->wgu + (size_t)I.r0 * 2 * HT;
+        dT = Lp->wdT + (size_t)I.r0 * HT;
+      } else if (I.flags & F_SHARED) {
+        gu = Lp->sh_gu + (size_t)I.r0 * 2 * HT;
+        dT = Lp->sh_dT + (size_t)I.r0 * HT;
+      } else {
+        const size_t e = (size_t)topk[I.g];
+        gu = Lp->ex_gu + (e * g.Fe + I.r0) * 2 * HT;
+        dT = Lp->ex_dT + (e * g.Fe + I.r0) * HT;
+      }
+      s[0] = {(const unsigned char*)gu, nullptr, ROW, 2 * n, RPS};
+      s[1] = {(const unsigned char*)dT, nullptr, ROW, n, RPS};
+      return 2;
+    }
+    case OP_LMHEAD:
+      s[0] = {(const unsigned char*)(g.lm_head + (size_t)I.r0 * HT), nullptr, ROW, n, RPS};
+      return 1;
+    case OP_ATTN: {
+      // slice s of S over positions [0, P]: [s*C/S, (s+1)*C/S), C = P + 1.
+      // Rows below P come from the cache through the ring; row P (written by
+      // this step's QKV instructions) is read directly after the wait.
+      const int P = pos[I.b];
+      const long C = (long)P + 1;
+      const int p0 = (int)(C * I.r0 / I.r1);
+      const int p1 = (int)(C * (I.r0 + 1) / I.r1);
+      const int pe = p1 < P ? p1 : P;
+      const uint32_t cnt = pe > p0 ? (uint32_t)(pe - p0) : 0u;
+      const size_t base = (((size_t)I.b * g.Hkv + I.g) * g.max_seq + (size_t)p0) * D;
+      s[0] = {(const unsigned char*)(Lp->kc + base), (const unsigned char*)(Lp->vc + base), D * 2,
+              cnt, (STAGE_BYTES / 2) / (D * 2)};
+      return 1;
+    }
+    default:
+      return 0;
+  }
+}
+
+// MoE routing (batch 1): softmax is monotonic, so the top-k by probability
+// are the k largest router logits (lower expert id first on ties); the
+// renormalised weights are exp(l_j - l_max) / sum over the selected i of
+// exp(l_i - l_max).  One warp; every lane returns ids[K] and w[K].
+MK_DEV void route_topk(const float* lg, int E, int K, int lane, int* ids, float* w) {
+  float v[32];
+  uint32_t taken = 0;
+#pragma unroll
+  for (int k = 0; k < 32; k++) {
+    const int e = lane + 32 * k;
+    v[k] = e < E ? __ldcg(lg + e) : -INFINITY;
+  }
+  float top = 0.f, sum = 0.f;
+  for (int j = 0; j < K; j++) {
+    float best = -INFINITY;
+    int bi = 0x7FFFFFFF;
+#pragma unroll
+    for (int k = 0; k < 32; k++) {
+      const int e = lane + 32 * k;
+      if (e < E && !((taken >> k) & 1u) && (v[k] > best || (v[k] == best && e < bi))) {
+        best = v[k];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+      if (ob > best || (ob == best && oi < bi)) {
+        best = ob;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (j == 0) top = best;
+    ids[j] = bi;
+    w[j] = expf(best - top);
+    sum += w[j];
+  }
+  for (int j = 0; j < K; j++) w[j] /= sum;
+}
+
+// ---------------------------------------------------------------- norms ----
+// xn[b][k] = x[b][k] * rsqrt(mean(x^2) + eps) * gain[k] for the residual
+// x_j (j = 0: the embedding row of the token).  All consumer threads.
+template <int HT, int D, int HPG, int NB>
+MK_DEV void norm_into_xn(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const uint16_t* gain) {
+  constexpr int GROUPS = HT / 8;
+  float ss[NB];
+#pragma unroll
+  for (int b = 0; b < NB; b++) ss[b] = 0.f;
+  for (int gi = c.tid; gi < GROUPS; gi += NCT) {
+#pragma unroll
+    for (int b = 0; b < NB; b++) {
+      float v[8];
+      if (b < g.B) {
+        if (j == 0) {
+          const uint4 w = __ldg((const uint4*)(g.embed + (size_t)c.tok[b] * HT) + gi);
+          unpack8(w, v);
+        } else {
+          const float4* p = (const float4*)xres(g, j, b) + 2 * gi;
+          const float4 a0 = __ldcg(p), a1 = __ldcg(p + 1);
+          v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
+          v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; k++) v[k] = 0.f;
+      }
+      float4* o = (float4*)(c.xn + (size_t)b * HT) + 2 * gi;
+      o[0] = make_float4(v[0], v[1], v[2], v[3]);
+      o[1] = make_float4(v[4], v[5], v[6], v[7]);
+#pragma unroll
+      for (int k = 0; k < 8; k++) ss[b] = fmaf(v[k], v[k], ss[b]);
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < NB; b++) {
+    const float t = warp_sum(ss[b]);
+    if (c.lane == 0) c.red[c.warp * NB + b] = t;
+  }
+  consumer_bar();
+  float rs[NB];
+#pragma unroll
+  for (int b = 0; b < NB; b++) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < NCW; w++) t += c.red[w * NB + b];
+    rs[b] = rsqrtf(t / (float)HT + g.eps);
+  }
+  for (int gi = c.tid; gi < GROUPS; gi += NCT) {
+    float gw[8];
+    unpack8(__ldg((const uint4*)gain + gi), gw);
+#pragma unroll
+    for (int b = 0; b < NB; b++) {
+      float4* o = (float4*)(c.xn + (size_t)b * HT) + 2 * gi;
+      float4 a0 = o[0], a1 = o[1];
+      a0.x *= rs[b] * gw[0]; a0.y *= rs[b] * gw[1]; a0.z *= rs[b] * gw[2]; a0.w *= rs[b] * gw[3];
+      a1.x *= rs[b] * gw[4]; a1.y *= rs[b] * gw[5]; a1.z *= rs[b] * gw[6]; a1.w *= rs[b] * gw[7];
+      o[0] = a0;
+      o[1] = a1;
+    }
+  }
+  consumer_bar();
+}
+
+// ----------------------------------------------------------------- GEMV ----
+// Lane l of a warp owns columns {it*256 + l*8 + k}; for NB == 1 its slice of
+// xn lives in registers.
+template <int HT>
+MK_DEV void load_xr(const float* xn, int lane, float (&xr)[HT / 32]) {
+#pragma unroll
+  for (int it = 0; it < HT / 256; it++) {
+    const float4* p = (const float4*)(xn + it * 256 + lane * 8);
+    const float4 a = p[0], b = p[1];
+    xr[it * 8 + 0] = a.x; xr[it * 8 + 1] = a.y; xr[it * 8 + 2] = a.z; xr[it * 8 + 3] = a.w;
+    xr[it * 8 + 4] = b.x; xr[it * 8 + 5] = b.y; xr[it * 8 + 6] = b.z; xr[it * 8 + 7] = b.w;
+  }
+}
+
+// Partial dot of one bf16 row (in shared memory) with the activation(s); the
+// caller reduces across the warp.
+template <int HT, int NB>
+MK_DEV void row_dot(const unsigned char* row, const float (&xr)[HT / 32], const float* xn,
+                    int lane, float (&acc)[NB]) {
+  const uint4* w4 = (const uint4*)row;
+  if constexpr (NB == 1) {
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int it = 0; it < HT / 256; it++) {
+      const uint4 w = w4[it * 32 + lane];
+      const float* x = xr + it * 8;
+      a0 = fmaf(bf_lo(w.x), x[0], a0); a1 = fmaf(bf_hi(w.x), x[1], a1);
+      a0 = fmaf(bf_lo(w.y), x[2], a0); a1 = fmaf(bf_hi(w.y), x[3], a1);
+      a0 = fmaf(bf_lo(w.z), x[4], a0); a1 = fmaf(bf_hi(w.z), x[5], a1);
+      a0 = fmaf(bf_lo(w.w), x[6], a0); a1 = fmaf(bf_hi(w.w), x[7], a1);
+    }
+    acc[0] = a0 + a1;
+  } else {
+#pragma unroll
+    for (int b = 0; b < NB; b++) acc[b] = 0.f;
+#pragma unroll 2
+    for (int it = 0; it < HT / 256; it++) {
+      float wf[8];
+      unpack8(w4[it * 32 + lane], wf);
+#pragma unroll
+      for (int b = 0; b < NB; b++) {
+        const float4* p = (const float4*)(xn + (size_t)b * HT + it * 256 + lane * 8);
+        const float4 x0 = p[0], x1 = p[1];
+        float a = acc[b];
+        a = fmaf(wf[0], x0.x, a); a = fmaf(wf[1], x0.y, a);
+        a = fmaf(wf[2], x0.z, a); a = fmaf(wf[3], x0.w, a);
+        a = fmaf(wf[4], x1.x, a); a = fmaf(wf[5], x1.y, a);
+        a = fmaf(wf[6], x1.z, a); a = fmaf(wf[7], x1.w, a);
+        acc[b] = a;
+      }
+    }
+  }
+}
+
+// Stream the rows of one segment through the ring; warp w computes rows
+// w, w + NCW, ... of each stage and hands (row index, per-sequence dot) to
+// fn on every lane.  Returns false if a wait gave up.
+template <int HT, int D, int HPG, int NB, class Fn>
+MK_DEV bool gemv_rows(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s,
+                      const float (&xr)[HT / 32], Fn&& fn) {
+  for (uint32_t u0 = 0; u0 < s.n; u0 += s.ups) {
+    const uint32_t n = min(s.ups, s.n - u0);
+    if (!c.ring.acquire(g)) return false;
+    const unsigned char* st = c.ring.stage_ptr();
+    for (uint32_t r = c.warp; r < n; r += NCW) {
+      float acc[NB];
+      row_dot<HT, NB>(st + (size_t)r * HT * 2, xr, c.xn, c.lane, acc);
+#pragma unroll
+      for (int b = 0; b < NB; b++) acc[b] = warp_sum(acc[b]);
+      fn(u0 + r, acc);
+    }
+    c.ring.release(c.lane);
+  }
+  return true;
+}
+
+}  // namespace mk
+
+namespace mk {
+
+// ------------------------------------------------- OP_QKV (RMS+QKV+RoPE) ----
+// Rows [r0, r1) of the layer's packed QKV matrix, all inside kv head I.g's
+// group [q heads of the group][k][v]; inside a head, packed rows 2t and 2t+1
+// hold head dims t and t + D/2, so each rotary pair is produced by one SM.
+template <int HT, int D, int HPG, int NB>
+MK_DEV void op_qkv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+  const LayerPtrs& Lp = g.layers[I.layer];
+  if (!(I.flags & F_NORM_CACHED)) norm_into_xn(c, g, 2 * I.layer, Lp.attn_norm);
+  float xr[HT / 32];
+  if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
+  Seg s[2];
+  get_segs<HT, D>(g, I, c.pos, c.topk, s);
+  float* yrow = c.yrow;
+  const int lane = c.lane;
+  gemv_rows(c, g, s[0], xr, [&](uint32_t r, float(&acc)[NB]) {
+    if (lane == 0) {
+#pragma unroll
+      for (int b = 0; b < NB; b++) yrow[b * MAX_ROWS + r] = acc[b];
+    }
+  });
+  consumer_bar();
+  constexpr int GR = (HPG + 2) * D;
+  const uint32_t n = I.r1 - I.r0;
+  for (uint32_t i = 2 * c.tid; i < n; i += 2 * NCT) {
+    const int lr = (int)(I.r0 + i) - (int)I.g * GR;
+    const int hs = lr / D;
+    const int t = (lr % D) >> 1;
+    for (int b = 0; b < g.B && b < NB; b++) {
+      float y0 = yrow[b * MAX_ROWS + i], y1 = yrow[b * MAX_ROWS + i + 1];
+      const int P = c.pos[b];
+      if (hs <= HPG) {  // q heads and k: rotate (t, t + D/2) by P * theta^(-2t/D)
+        const float2 cs = ((const float2*)g.rope)[(size_t)P * (D / 2) + t];
+        const float a = y0 * cs.x - y1 * cs.y;
+        const float bb = y0 * cs.y + y1 * cs.x;
+        y0 = a;
+        y1 = bb;
+      }
+      if (hs < HPG) {
+        float* q = g.qbuf + (((size_t)I.layer * g.B + b) * g.Hq + (size_t)I.g * HPG + hs) * D;
+        q[t] = y0;
+        q[t + D / 2] = y1;
+      } else {
+        uint16_t* row = (hs == HPG ? Lp.kc : Lp.vc) +
+                        (((size_t)b * g.Hkv + I.g) * g.max_seq + (size_t)P) * D;
+        row[t] = to_bf16(y0);
+        row[t + D / 2] = to_bf16(y1);
+      }
+    }
+  }
+  consumer_bar();
+}
+
+// ------------------------------------------ OP_ATTN (split-KV partial) ----
+// Work item (b, kv head g, slice s of S): for the HPG query heads of the
+// group, the partial softmax state over positions [s*C/S, (s+1)*C/S) of
+// [0, P]: running max m, sum l of 2^(score - m) and o = sum 2^(score - m) v,
+// with scores in log2 units (q pre-scaled by log2(e)/sqrt(D)).  Rows stream
+// through the ring K-half / V-half per stage; every slot of LPR lanes handles
+// one position at a time with an online-softmax update, then slots, warps
+// and finally the CTA merge their states.
+constexpr float NEG_BIG = -1e30f;
+
+template <int HT, int D, int HPG, int NB>
+MK_DEV void op_attn(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+  constexpr int LPR = D / 8, SPW = 32 / LPR;
+  const int slot = c.lane / LPR, dsl = c.lane % LPR;
+  const int b = I.b, P = c.pos[b];
+  const LayerPtrs& Lp = g.layers[I.layer];
+  constexpr float QS = (D == 64 ? 0.125f : 0.08838834764831845f) * 1.4426950408889634f;
+  float q[HPG][8], m[HPG], l[HPG], o[HPG][8];
+#pragma unroll
+  for (int h = 0; h < HPG; h++) {
+    const float4* qp = (const float4*)(g.qbuf +
+                                       (((size_t)I.layer * g.B + b) * g.Hq + (size_t)I.g * HPG + h) *
+                                           D +
+                                       dsl * 8);
+    const float4 a0 = __ldcg(qp), a1 = __ldcg(qp + 1);
+    q[h][0] = a0.x * QS; q[h][1] = a0.y * QS; q[h][2] = a0.z * QS; q[h][3] = a0.w * QS;
+    q[h][4] = a1.x * QS; q[h][5] = a1.y * QS; q[h][6] = a1.z * QS; q[h][7] = a1.w * QS;
+    m[h] = NEG_BIG;
+    l[h] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; j++) o[h][j] = 0.f;
+  }
+  auto process = [&](const uint4& kw, const uint4& vw, bool valid) {
+    float kf[8], vf[8], sc[HPG];
+    unpack8(kw, kf);
+    unpack8(vw, vf);
+#pragma unroll
+    for (int h = 0; h < HPG; h++) {
+      float a = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; j++) a = fmaf(q[h][j], kf[j], a);
+      sc[h] = a;
+    }
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1)
+#pragma unroll
+      for (int h = 0; h < HPG; h++) sc[h] += __shfl_xor_sync(0xFFFFFFFFu, sc[h], off);
+    if (valid) {
+#pragma unroll
+      for (int h = 0; h < HPG; h++) {
+        const float mn = fmaxf(m[h], sc[h]);
+        const float cr = exp2f(m[h] - mn), p = exp2f(sc[h] - mn);
+        l[h] = fmaf(l[h], cr, p);
+#pragma unroll
+        for (int j = 0; j < 8; j++) o[h][j] = fmaf(o[h][j], cr, p * vf[j]);
+        m[h] = mn;
+      }
+    }
+  };
+  Seg s[2];
+  get_segs<HT, D>(g, I, c.pos, c.topk, s);
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
+    const uint32_t n = min(s[0].ups, s[0].n - u0);
+    if (!c.ring.acquire(g)) break;
+    const unsigned char* st = c.ring.stage_ptr();
+    for (uint32_t jb = (uint32_t)c.warp * SPW; jb < n; jb += NCW * SPW) {
+      const uint32_t j = jb + slot;
+      const bool valid = j < n;
+      const uint4 kw = valid ? *(const uint4*)(st + (size_t)j * D * 2 + dsl * 16) : zero;
+      const uint4 vw =
+          valid ? *(const uint4*)(st + STAGE_BYTES / 2 + (size_t)j * D * 2 + dsl * 16) : zero;
+      process(kw, vw, valid);
+    }
+    c.ring.release(c.lane);
+  }
+  if (I.r0 + 1 == I.r1 && c.warp == 0) {  // row P, appended by this step's QKV
+    const size_t off = (((size_t)b * g.Hkv + I.g) * g.max_seq + (size_t)P) * D + dsl * 8;
+    const bool valid = slot == 0;
+    const uint4 kw = valid ? __ldcg((const uint4*)(Lp.kc + off)) : zero;
+    const uint4 vw = valid ? __ldcg((const uint4*)(Lp.vc + off)) : zero;
+    process(kw, vw, valid);
+  }
+  // merge the slots of the warp
+#pragma unroll
+  for (int off = LPR; off < 32; off <<= 1) {
+#pragma unroll
+    for (int h = 0; h < HPG; h++) {
+      const float mo = __shfl_xor_sync(0xFFFFFFFFu, m[h], off);
+      const float lo = __shfl_xor_sync(0xFFFFFFFFu, l[h], off);
+      const float mn = fmaxf(m[h], mo);
+      const float fa = exp2f(m[h] - mn), fb = exp2f(mo - mn);
+      l[h] = l[h] * fa + lo * fb;
+#pragma unroll
+      for (int j = 0; j < 8; j++) {
+        const float oo = __shfl_xor_sync(0xFFFFFFFFu, o[h][j], off);
+        o[h][j] = o[h][j] * fa + oo * fb;
+      }
+      m[h] = mn;
+    }
+  }
+  float* sc = c.yrow;  // [NCW][HPG][D + 2]
+  if (slot == 0) {
+#pragma unroll
+    for (int h = 0; h < HPG; h++) {
+      float* p = sc + ((size_t)c.warp * HPG + h) * (D + 2);
+#pragma unroll
+      for (int j = 0; j < 8; j++) p[dsl * 8 + j] = o[h][j];
+      if (dsl == 0) {
+        p[D] = m[h];
+        p[D + 1] = l[h];
+      }
+    }
+  }
+  consumer_bar();
+  for (int t = c.tid; t < HPG * D; t += NCT) {
+    const int h = t / D, dim = t % D;
+    float M = NEG_BIG;
+#pragma unroll
+    for (int w = 0; w < NCW; w++) M = fmaxf(M, sc[(w * HPG + h) * (D + 2) + D]);
+    float Ls = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < NCW; w++) {
+      const float* p = sc + (w * HPG + h) * (D + 2);
+      const float f = exp2f(p[D] - M);
+      Ls = fmaf(p[D + 1], f, Ls);
+      O = fmaf(p[dim], f, O);
+    }
+    float* dst = g.part + ((((size_t)I.layer * g.B + b) * g.Hq + (size_t)I.g * HPG + h) * g.splits +
+                           I.r0) * (D + 2);
+    dst[dim] = O;
+    if (dim == 0) {
+      dst[D] = M;
+      dst[D + 1] = Ls;
+    }
+  }
+  consumer_bar();
+}
+
+// Residual input x_j[b][r] (j = 0: the embedding row of the token).
+MK_DEV float x_in(const Globals& g, int j, const int* tok, int b, int r) {
+  if (j == 0) return bf1(g.embed[(size_t)tok[b] * g.H + r]);
+  return __ldcg(xres(g, j, b) + r);
+}
+
+// --------------------------------- OP_OPROJ (split reduce + O-proj rows) ----
+// Head h's partials are merged (M = max m_s, L = sum l_s 2^(m_s - M),
+// o = sum o_s 2^(m_s - M) / L), then rows [r0, r1) of Wo[:, h*D:(h+1)*D]
+// (packed [Hq][H][D]) are applied and accumulated into x_{2l+1} with float
+// atomics; the head-0 instructions also add the residual x_{2l}.
+template <int HT, int D, int HPG, int NB>
+MK_DEV void op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+  constexpr int LPR = D / 8, SPW = 32 / LPR;
+  const int slot = c.lane / LPR, dsl = c.lane % LPR;
+  const int h = I.g, l = I.layer;
+  for (int t = c.tid; t < NB * D; t += NCT) {
+    const int b = t / D, dim = t % D;
+    if (b < g.B) {
+      const float* base = g.part + (((size_t)l * g.B + b) * g.Hq + h) * g.splits * (D + 2);
+      float M = NEG_BIG;
+      for (int s = 0; s < g.splits; s++) M = fmaxf(M, __ldcg(base + s * (D + 2) + D));
+      float Ls = 0.f, O = 0.f;
+      for (int s = 0; s < g.splits; s++) {
+        const float* p = base + s * (D + 2);
+        const float f = exp2f(__ldcg(p + D) - M);
+        Ls = fmaf(__ldcg(p + D + 1), f, Ls);
+        O = fmaf(__ldcg(p + dim), f, O);
+      }
+      c.attn[b * D + dim] = O / Ls;
+    }
+  }
+  consumer_bar();
+  float a[NB][8];
+#pragma unroll
+  for (int b = 0; b < NB; b++)
+#pragma unroll
+    for (int j = 0; j < 8; j++) a[b][j] = c.attn[b * D + dsl * 8 + j];
+  const bool resid = (I.flags & F_RESIDUAL) != 0;
+  Seg s[2];
+  get_segs<HT, D>(g, I, c.pos, c.topk, s);
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
+    const uint32_t n = min(s[0].ups, s[0].n - u0);
+    if (!c.ring.acquire(g)) break;
+    const unsigned char* st = c.ring.stage_ptr();
+    for (uint32_t jb = (uint32_t)c.warp * SPW; jb < n; jb += NCW * SPW) {
+      const uint32_t j = jb + slot;
+      const bool valid = j < n;
+      float wf[8];
+      unpack8(valid ? *(const uint4*)(st + (size_t)j * D * 2 + dsl * 16) : zero, wf);
+      float y[NB];
+#pragma unroll
+      for (int b = 0; b < NB; b++) {
+        float v = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; k++) v = fmaf(a[b][k], wf[k], v);
+        y[b] = v;
+      }
+#pragma unroll
+      for (int off = LPR / 2; off > 0; off >>= 1)
+#pragma unroll
+        for (int b = 0; b < NB; b++) y[b] += __shfl_xor_sync(0xFFFFFFFFu, y[b], off);
+      if (valid && dsl == 0) {
+        const int r = (int)(I.r0 + u0 + j);
+        for (int b = 0; b < g.B && b < NB; b++) {
+          float v = y[b];
+          if (resid) v += x_in(g, 2 * l, c.tok, b, r);
+          atomicAdd(xres(g, 2 * l + 1, b) + r, v);
+        }
+      }
+    }
+    c.ring.release(c.lane);
+  }
+  consumer_bar();
+}
+
+// ------------------------------------------------- OP_ROUTER (MoE only) ----
+template <int HT, int D, int HPG, int NB>
+MK_DEV void op_router(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+  const LayerPtrs& Lp = g.layers[I.layer];
+  norm_into_xn(c, g, 2 * I.layer + 1, Lp.mlp_norm);
+  float xr[HT / 32];
+  if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
+  Seg s[2];
+  get_segs<HT, D>(g, I, c.pos, c.topk, s);
+  const int lane = c.lane, B = g.B;
+  float* rl = g.rlog + (size_t)I.layer * g.B * g.E + I.r0;
+  const int E = g.E;
+  gemv_rows(c, g, s[0], xr, [&](uint32_t r, float(&acc)[NB]) {
+    if (lane == 0)
+      for (int b = 0; b < B && b < NB; b++) rl[(size_t)b * E + r] = acc[b];
+  });
+  consumer_bar();
+}
+
+// ---------------------------------------- OP_MLP (one FFN column slice) ----
+// h_c = SiLU(gate_c . xn) * (up_c . xn) for the slice's columns c, then
+// x_{2l+2} += sum_c h_c * Wd[:, c] (down stored transposed, one contiguous
+// row per column) with float4 atomics; the instruction also adds x_{2l+1}
+// for its residual rows.  MoE: routed slices scale h by the slot's router
+// weight and read expert topk[slot]'s rows; shared slices use weight 1.
+template <int HT, int D, int HPG, int NB>
+MK_DEV void op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+  const int l = I.layer;
+  const LayerPtrs& Lp = g.layers[l];
+  const bool routed = g.E > 0 && !(I.flags & F_SHARED);
+  if (!(I.flags & F_NORM_CACHED)) norm_into_xn(c, g, 2 * l + 1, Lp.mlp_norm);
+  if (routed) {
+    if (c.warp == 0) route_topk(g.rlog + (size_t)l * g.B * g.E, g.E, g.K, c.lane, c.topk, c.topw);
+    consumer_bar();
+  }
+  const float scale = routed ? c.topw[I.g] : 1.f;
+  float xr[HT / 32];
+  if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
+  Seg s[2];
+  get_segs<HT, D>(g, I, c.pos, c.topk, s);
+  float* yrow = c.yrow;
+  const int lane = c.lane;
+  gemv_rows(c, g, s[0], xr, [&](uint32_t r, float(&acc)[NB]) {
+    if (lane == 0) {
+#pragma unroll
+      for (int b = 0; b < NB; b++) yrow[b * MAX_ROWS + r] = acc[b];
+    }
+  });
+  consumer_bar();
+  const int ncol = (int)(I.r1 - I.r0);
+  for (int t = c.tid; t < NB * ncol; t += NCT) {
+    const int b = t / ncol, j = t % ncol;
+    const float gt = yrow[b * MAX_ROWS + 2 * j], up = yrow[b * MAX_ROWS + 2 * j + 1];
+    c.hbuf[b * MAX_COLS + j] = scale * (gt / (1.f + expf(-gt))) * up;
+  }
+  consumer_bar();
+  constexpr int NG = HT / 8;                   // 8-row groups of the output
+  constexpr int GPT = (NG + NCT - 1) / NCT;    // groups per consumer thread
+  float acc[GPT][NB][8];
+#pragma unroll
+  for (int q = 0; q < GPT; q++)
+#pragma unroll
+    for (int b = 0; b < NB; b++)
+#pragma unroll
+      for (int k = 0; k < 8; k++) acc[q][b][k] = 0.f;
+  for (uint32_t u0 = 0; u0 < s[1].n; u0 += s[1].ups) {
+    const uint32_t n = min(s[1].ups, s[1].n - u0);
+    if (!c.ring.acquire(g)) break;
+    const unsigned char* st = c.ring.stage_ptr();
+    for (uint32_t j = 0; j < n; j++) {
+      float hv[NB];
+#pragma unroll
+      for (int b = 0; b < NB; b++) hv[b] = c.hbuf[b * MAX_COLS + u0 + j];
+#pragma unroll
+      for (int q = 0; q < GPT; q++) {
+        const int k = c.tid + q * NCT;
+        if (k < NG) {
+          float wf[8];
+          unpack8(*(const uint4*)(st + (size_t)j * HT * 2 + k * 16), wf);
+#pragma unroll
+          for (int b = 0; b < NB; b++)
+#pragma unroll
+            for (int e = 0; e < 8; e++) acc[q][b][e] = fmaf(hv[b], wf[e], acc[q][b][e]);
+        }
+      }
+    }
+    c.ring.release(c.lane);
+  }
+  const int rs0 = (int)(I.aux & 0xFFFFu), rs1 = (int)(I.aux >> 16);
+#pragma unroll
+  for (int q = 0; q < GPT; q++) {
+    const int k = c.tid + q * NCT;
+    if (k < NG) {
+      const int r0 = k * 8;
+      for (int b = 0; b < g.B && b < NB; b++) {
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+          v[e] = acc[q][b][e];
+          if (r0 + e >= rs0 && r0 + e < rs1) v[e] += __ldcg(xres(g, 2 * l + 1, b) + r0 + e);
+        }
+        float4* dst = (float4*)(xres(g, 2 * l + 2, b) + r0);
+        atomicAdd(dst, make_float4(v[0], v[1], v[2], v[3]));
+        atomicAdd(dst + 1, make_float4(v[4], v[5], v[6], v[7]));
+      }
+    }
+  }
+  consumer_bar();
+}
+
+// ------------------------------------ OP_LMHEAD (final norm + head rows) ----
+// Logits rows [r0, r1) and this slice's (max, first index); the slice that
+// arrives last on the argmax counter reduces all slices into argmax[b].
+template <int HT, int D, int HPG, int NB>
+MK_DEV void op_lmhead(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+  norm_into_xn(c, g, 2 * g.L, g.final_norm);
+  float xr[HT / 32];
+  if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
+  Seg s[2];
+  get_segs<HT, D>(g, I, c.pos, c.topk, s);
+  float best[NB];
+  int bidx[NB];
+#pragma unroll
+  for (int b = 0; b < NB; b++) {
+    best[b] = -INFINITY;
+    bidx[b] = 0x7FFFFFFF;
+  }
+  const int lane = c.lane, B = g.B, V = g.V;
+  float* logits = g.logits;
+  const uint32_t r0 = I.r0;
+  gemv_rows(c, g, s[0], xr, [&](uint32_t r, float(&acc)[NB]) {
+    if (lane == 0) {
+      const int row = (int)(r0 + r);
+#pragma unroll
+      for (int b = 0; b < NB; b++) {
+        if (b < B) {
+          logits[(size_t)b * V + row] = acc[b];
+          if (acc[b] > best[b] || (acc[b] == best[b] && row < bidx[b])) {
+            best[b] = acc[b];
+            bidx[b] = row;
+          }
+        }
+      }
+    }
+  });
+  float* rv = c.red;
+  int* ri = (int*)(c.red + NCW * NB);
+  if (lane == 0) {
+#pragma unroll
+    for (int b = 0; b < NB; b++) {
+      rv[c.warp * NB + b] = best[b];
+      ri[c.warp * NB + b] = bidx[b];
+    }
+  }
+  consumer_bar();
+  if (c.warp != 0) return;
+  if (lane == 0) {
+    for (int b = 0; b < B && b < NB; b++) {
+      float v = -INFINITY;
+      int ix = 0x7FFFFFFF;
+      for (int w = 0; w < NCW; w++) {
+        const float ov = rv[w * NB + b];
+        const int oi = ri[w * NB + b];
+        if (ov > v || (ov == v && oi < ix)) {
+          v = ov;
+          ix = oi;
+        }
+      }
+      g.lm_val[(size_t)I.aux * B + b] = v;
+      g.lm_idx[(size_t)I.aux * B + b] = ix;
+    }
+  }
+  uint32_t old = 0;
+  if (lane == 0) old = atom_add_acq_rel(g.ctr + g.lm_ctr, 1u);
+  old = __shfl_sync(0xFFFFFFFFu, old, 0);
+  __syncwarp();
+  if (old != g.epoch * (uint32_t)g.n_lm - 1u) return;
+  for (int b = 0; b < B && b < NB; b++) {
+    float v = -INFINITY;
+    int ix = 0x7FFFFFFF;
+    for (int k = lane; k < g.n_lm; k += 32) {
+      const float ov = __ldcg(g.lm_val + (size_t)k * B + b);
+      const int oi = __ldcg(g.lm_idx + (size_t)k * B + b);
+      if (ov > v || (ov == v && oi < ix)) {
+        v = ov;
+        ix = oi;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, ix, o);
+      if (ov > v || (ov == v && oi < ix)) {
+        v = ov;
+        ix = oi;
+      }
+    }
+    if (lane == 0) g.argmax[b] = ix;
+  }
+}
+
+// ------------------------------------------------------------ interpreter ----
+MK_DEV Instr load_instr(const Globals& g, int sm, int pc) {
+  const uint4* p = (const uint4*)(g.sched + (size_t)sm * g.max_pc + pc);
+  const uint4 a = __ldg(p), b = __ldg(p + 1);
+  Instr I;
+  *(uint4*)&I = a;
+  *((uint4*)&I + 1) = b;
+  return I;
+}
+
+MK_DEV bool selected(const Globals& g, const Instr& I) {
+  if (g.sel_key < 0) return true;
+  const int key = I.op == OP_LMHEAD ? g.L * N_PHASES : I.layer * N_PHASES + phase_of(I.op);
+  return key == g.sel_key;
+}
+
+// Producer warp: walks the queue and streams every instruction's segments
+// into the ring (lane 0 issues).  It waits only for free stages -- except
+// that a routed MoE slice needs the router result for its weight addresses.
+// On any error it stops issuing and waits for its copies in flight before
+// the CTA may exit.
+template <int HT, int D, int HPG, int NB>
+MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint32_t empty0,
+                     int* ppos, int* ptopk, float* ptopw, int lane) {
+  const uint64_t pol_w = policy_evict_first();
+  const uint64_t pol_kv = policy_evict_normal();
+  const int ns = g.n_stages;
+  const uint32_t ring_s = smem_u32(ring);
+  uint32_t issued = 0;
+  int st = 0;
+  uint32_t par = 0;
+  bool grid_waited = !g.pdl;
+  int routed_layer = -1;
+  for (int pc = 0; pc < g.max_pc; pc++) {
+    const Instr I = load_instr(g, blockIdx.x, pc);
+    if (I.op == OP_HALT) break;
+    if (I.op == OP_NOP || !selected(g, I)) continue;
+    // every branch below is warp-uniform: lane 0 decides, the warp follows
+    if (__shfl_sync(0xFFFFFFFFu, peek_err(g), 0)) goto drain;
+    const bool routed = I.op == OP_MLP && g.E > 0 && !(I.flags & F_SHARED);
+    if ((I.op == OP_ATTN || routed) && !grid_waited) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      grid_waited = true;
+    }
+    if (I.op == OP_ATTN) {
+      const int P = __shfl_sync(0xFFFFFFFFu, __ldg(g.positions + I.b), 0);
+      if (P < 0 || P >= g.max_ctx) {
+        if (lane == 0) set_err(g, MK_ERR_INVALID_ARG, pc, I.op);
+        goto drain;
+      }
+      if (lane == 0) ppos[I.b] = P;
+    }
+    if (routed && routed_layer != I.layer) {
+      bool ok = true;
+      if (lane == 0) ok = wait_counter(g, I.wait_ctr, g.epoch * I.wait_cnt, pc, I.op);
+      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) goto drain;
+      __syncwarp();
+      route_topk(g.rlog + (size_t)I.layer * g.B * g.E, g.E, g.K, lane, ptopk, ptopw);
+      routed_layer = I.layer;
+    }
+    __syncwarp();
+    Seg s[2];
+    const int nseg = get_segs<HT, D>(g, I, ppos, ptopk, s);
+    for (int k = 0; k < nseg; k++) {
+      for (uint32_t u0 = 0; u0 < s[k].n; u0 += s[k].ups) {
+        const uint32_t n = min(s[k].ups, s[k].n - u0);
+        bool ok = true;
+        if (lane == 0) ok = wait_mbar(g, empty0 + 8u * st, par ^ 1u, true);
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) goto drain;
+        if (lane == 0) {
+          const uint32_t bytes = n * s[k].unit;
+          const uint32_t full = full0 + 8u * st;
+          const uint32_t dst = ring_s + (uint32_t)st * STAGE_BYTES;
+          mbar_expect_tx(full, s[k].src2 ? 2u * bytes : bytes);
+          if (s[k].src2) {
+            bulk_g2s(dst, s[k].src + (size_t)u0 * s[k].unit, bytes, full, pol_kv);
+            bulk_g2s(dst + STAGE_BYTES / 2, s[k].src2 + (size_t)u0 * s[k].unit, bytes, full,
+                     pol_kv);
+          } else {
+            bulk_g2s(dst, s[k].src + (size_t)u0 * s[k].unit, bytes, full, pol_w);
+          }
+        }
+        __syncwarp();
+        issued++;
+        if (++st == ns) {
+          st = 0;
+          par ^= 1u;
+        }
+      }
+    }
+  }
+  return;
+drain:
+  // The latest arming of each stage is among the last ns issued; wait for
+  // those copies to land so that no bulk copy outlives the CTA.
+  if (lane != 0) return;
+  for (uint32_t k = 1; k <= issued && k <= (uint32_t)ns; k++) {
+    const uint32_t j = issued - k;
+    wait_mbar(g, full0 + 8u * (j % (uint32_t)ns), (j / (uint32_t)ns) & 1u, false);
+  }
+}
+
+template <int HT, int D, int HPG, int NB>
+__global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_constant__ Globals g) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const SmemLayout Ls = smem_layout(g.n_stages, NB, HT, D, HPG, g.K);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t full0 = smem_u32(smem + Ls.full), empty0 = smem_u32(smem + Ls.empty);
+  const int KM = g.K > 0 ? g.K : 1;
+  int* misc = (int*)(smem + Ls.misc);
+  int* flag = misc;
+  int* tok = misc + 8;
+  int* pos = tok + NB;
+  int* topk = pos + NB;
+  int* ptopk = topk + NB * KM;
+  float* topw = (float*)(ptopk + NB * KM);
+  float* ptopw = topw + NB * KM;
+  int* ppos = (int*)(ptopw + NB * KM);
+  if (tid == 0) {
+    for (int s = 0; s < g.n_stages; s++) {
+      mbar_init(full0 + 8u * s, 1u);
+      mbar_init(empty0 + 8u * s, (uint32_t)NCW);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    *flag = 0;
+  }
+  __syncthreads();
+
+  if (warp == NCW) {
+    producer<HT, D, HPG, NB>(g, smem + Ls.ring, full0, empty0, ppos, ptopk, ptopw, lane);
+    return;
+  }
+
+  // ---- consumers
+  if (g.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid < g.B && tid < NB) {
+    const int t = g.tokens[tid], p = g.positions[tid];
+    tok[tid] = t;
+    pos[tid] = p;
+    if (t < 0 || t >= g.V || p < 0 || p >= g.max_ctx) *flag = 1;
+  }
+  if (g.zero_next) {  // the residual buffers of the next step's parity
+    const size_t total = (size_t)2 * g.L * g.B * g.H;
+    const size_t a = total * blockIdx.x / gridDim.x, e = total * (blockIdx.x + 1) / gridDim.x;
+    float* nx = g.xbuf + (size_t)(g.parity ^ 1) * total;
+    for (size_t i = a + tid; i < e; i += NCT) nx[i] = 0.f;
+  }
+  consumer_bar();
+  if (*flag) {
+    if (tid == 0) set_err(g, MK_ERR_INVALID_ARG, -1, -1);
+    return;
+  }
+  if (g.pdl && tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  Ctx<HT, D, HPG, NB> c;
+  c.xn = (float*)(smem + Ls.xn);
+  c.yrow = (float*)(smem + Ls.yrow);
+  c.hbuf = (float*)(smem + Ls.hbuf);
+  c.attn = (float*)(smem + Ls.attn);
+  c.red = (float*)(smem + Ls.red);
+  c.tok = tok;
+  c.pos = pos;
+  c.topk = topk;
+  c.topw = topw;
+  c.ring = Ring{smem + Ls.ring, full0, empty0, g.n_stages, 0, 0u};
+  c.tid = tid;
+  c.warp = warp;
+  c.lane = lane;
+  consumer_bar();  // everyone has read *flag before it is reused below
+
+  for (int pc = 0; pc < g.max_pc; pc++) {
+    const Instr I = load_instr(g, blockIdx.x, pc);
+    if (I.op == OP_HALT) break;
+    if (I.op == OP_NOP || !selected(g, I)) continue;
+    c.pc = pc;
+    if (tid == 0) {
+      bool ok = true;
+      if (I.wait_ctr != NO_CTR) ok = wait_counter(g, I.wait_ctr, g.epoch * I.wait_cnt, pc, I.op);
+      if (ok && peek_err(g)) ok = false;
+      *flag = ok ? 0 : 1;
+    }
+    consumer_bar();
+    if (*flag) return;
+    switch (I.op) {
+      case OP_QKV: op_qkv(c, g, I); break;
+      case OP_ATTN: op_attn(c, g, I); break;
+      case OP_OPROJ: op_oproj(c, g, I); break;
+      case OP_ROUTER: op_router(c, g, I); break;
+      case OP_MLP: op_mlp(c, g, I); break;
+      case OP_LMHEAD: op_lmhead(c, g, I); break;
+      default:
+        if (tid == 0) set_err(g, MK_ERR_DEVICE, pc, I.op);
+        consumer_bar();
+        break;
+    }
+    if (tid == 0 && I.sig_ctr != NO_CTR) red_release(g.ctr + I.sig_ctr, 1u);
+  }
+}
+
+}  // namespace mk

@@ -1,0 +1,197 @@
+// mk_device.cuh -- device helpers of the interpreter: inline PTX for mbarriers,
+// bulk copies and release/acquire counters, bounded waits, bf16 unpacking.
+//
+// Counter protocol ("Megakernels: Deleting the Kernel Boundary", section
+// "Correctness without the free barrier"): a producer makes its stores
+// visible device-wide and then increments a counter; a consumer spins until
+// the counter reaches its target.  Here the increment is a release
+// reduction (red.release.gpu) issued by one thread after a CTA barrier, the
+// spin is an acquire load (ld.acquire.gpu), and every spin is bounded by
+// %globaltimer so that a missing producer turns into an error status, never
+// a hung GPU.
+#pragma once
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "mk_internal.h"
+
+namespace mk {
+
+#define MK_DEV __device__ __forceinline__
+
+MK_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+MK_DEV uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+MK_DEV void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+MK_DEV bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+MK_DEV void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+MK_DEV void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+MK_DEV uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+MK_DEV uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Non-multicast bulk copy global -> this CTA's shared memory, completing on
+// the mbarrier's transaction count.  dst, src and bytes are multiples of 16.
+MK_DEV void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                     uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+MK_DEV uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+MK_DEV void red_release(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+MK_DEV uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
+// Barrier among the consumer warps only (the producer warp never joins).
+MK_DEV void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory"); }
+
+MK_DEV float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+MK_DEV float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+MK_DEV float bf1(uint16_t h) { return __uint_as_float(((uint32_t)h) << 16); }
+MK_DEV uint16_t to_bf16(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+
+MK_DEV void unpack8(const uint4& w, float* f) {
+  f[0] = bf_lo(w.x); f[1] = bf_hi(w.x);
+  f[2] = bf_lo(w.y); f[3] = bf_hi(w.y);
+  f[4] = bf_lo(w.z); f[5] = bf_hi(w.z);
+  f[6] = bf_lo(w.w); f[7] = bf_hi(w.w);
+}
+
+MK_DEV float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+MK_DEV int peek_err(const Globals& g) { return *(volatile const int*)g.err; }
+
+MK_DEV void set_err(const Globals& g, int code, int pc, int op) {
+  if (atomicCAS(g.err, 0, code) == 0) {
+    g.err[1] = (int)blockIdx.x;
+    g.err[2] = pc;
+    g.err[3] = op;
+  }
+}
+
+// Spin (acquire) until ctr[idx] has reached `target` (wrap-safe).  Returns
+// false after an error anywhere in the grid or after the time limit.
+MK_DEV bool wait_counter(const Globals& g, uint32_t idx, uint32_t target, int pc, int op) {
+  const uint32_t* p = g.ctr + idx;
+  if ((int32_t)(ld_acquire(p) - target) >= 0) return true;
+  const uint64_t t0 = gtimer();
+  for (uint32_t it = 1;; it++) {
+    if ((int32_t)(ld_acquire(p) - target) >= 0) return true;
+    if ((it & 15) == 0) {
+      if (peek_err(g)) return false;
+      if (gtimer() - t0 > g.timeout_ns) {
+        set_err(g, MK_ERR_TIMEOUT, pc, op);
+        return false;
+      }
+    }
+  }
+}
+
+// Wait for a phase of an mbarrier.  abort_on_err: also give up when the
+// grid has failed (consumers); the producer's drain passes false so that it
+// always waits for its own copies in flight.
+MK_DEV bool wait_mbar(const Globals& g, uint32_t bar, uint32_t parity, bool abort_on_err) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = gtimer();
+  for (uint32_t it = 1;; it++) {
+    if (mbar_try(bar, parity)) return true;
+    if ((it & 63) == 0) {
+      if (abort_on_err && peek_err(g)) return false;
+      if (gtimer() - t0 > g.timeout_ns) {
+        set_err(g, MK_ERR_TIMEOUT, -1, -1);
+        return false;
+      }
+    }
+  }
+}
+
+// One contiguous run of equal-sized units (weight rows, or cache rows of K
+// with the matching V rows in src2) streamed through the ring, `ups` units
+// per stage.  src2 lands in the upper half of the stage.
+struct Seg {
+  const unsigned char* src;
+  const unsigned char* src2;
+  uint32_t unit;
+  uint32_t n;
+  uint32_t ups;
+};
+
+// Ring cursor of one consumer warp.
+struct Ring {
+  unsigned char* base;
+  uint32_t full0, empty0;  // shared addresses of full[0], empty[0]
+  int ns;
+  int st;
+  uint32_t par;
+
+  MK_DEV const unsigned char* stage_ptr() const { return base + (size_t)st * STAGE_BYTES; }
+  // All 32 lanes call; the result is the same on every lane.
+  MK_DEV bool acquire(const Globals& g) {
+    const bool ok = wait_mbar(g, full0 + 8u * st, par, true);
+    return __all_sync(0xFFFFFFFFu, ok);
+  }
+  // All 32 lanes call; lane 0 arrives for the warp.
+  MK_DEV void release(int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8u * st);
+    if (++st == ns) {
+      st = 0;
+      par ^= 1u;
+    }
+  }
+};
+
+}  // namespace mk

@@ -1,0 +1,174 @@
+// mk_internal.h -- records shared by the host planner, the C-ABI layer and the
+// device interpreter.  Plain C++ (no CUDA types) so the planner builds with g++.
+#pragma once
+#include <stddef.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "../../include/mk.h"
+
+#ifdef __CUDACC__
+#define MK_HD __host__ __device__
+#else
+#define MK_HD
+#endif
+
+namespace mk {
+
+// Opcodes of the interpreter ("Megakernels: Deleting the Kernel Boundary",
+// section "One launch, one interpreter", re-cut for GB300: the attention
+// reduce is folded into the O-projection, up/gate and down are one
+// instruction over an FFN column slice, ROUTER serves the MoE MLP).
+enum Op : uint8_t {
+  OP_HALT = 0,
+  OP_QKV = 1,     // RMSNorm + QKV rows + RoPE + KV append
+  OP_ATTN = 2,    // split-KV GQA partial softmax over a slice of positions
+  OP_OPROJ = 3,   // split reduce + O-projection rows of one head + residual
+  OP_MLP = 4,     // RMSNorm + gate/up rows + SiLU*mul + down columns + residual
+  OP_LMHEAD = 5,  // final RMSNorm + LM-head rows + argmax (last arriver)
+  OP_ROUTER = 6,  // MoE: RMSNorm + router rows
+  OP_NOP = 7,     // does nothing (fault-injection stand-in)
+};
+
+// Ablation phases: one launch per (layer, phase).  No instruction waits on a
+// counter signalled by an instruction of its own phase.
+enum Phase : int { PH_QKV = 0, PH_ATTN = 1, PH_OPROJ = 2, PH_ROUTER = 3, PH_MLP = 4, N_PHASES = 5 };
+
+enum Flag : uint8_t {
+  F_RESIDUAL = 1,    // this instruction also adds the residual input for its rows
+  F_NORM_CACHED = 2, // the normalised input left in shared memory is still valid
+  F_SHARED = 4,      // MoE MLP: shared-expert columns (weight 1, no routing)
+};
+
+constexpr uint32_t NO_CTR = 0xFFFFFFFFu;
+
+using Instr = mk_instr;  // 32-byte record, layout fixed by mk.h
+static_assert(sizeof(Instr) == 32, "instruction record must be 32 bytes");
+
+MK_HD inline int phase_of(uint8_t op) {
+  switch (op) {
+    case OP_QKV: return PH_QKV;
+    case OP_ATTN: return PH_ATTN;
+    case OP_OPROJ: return PH_OPROJ;
+    case OP_ROUTER: return PH_ROUTER;
+    default: return PH_MLP;
+  }
+}
+
+// Counter ids: per layer l, base l*stride:
+//   qkv[g] (g < Hkv), attn[g], oproj, mlp, router; then one argmax counter.
+struct CtrMap {
+  int Hkv, L;
+  MK_HD int stride() const { return 2 * Hkv + 3; }
+  MK_HD uint32_t qkv(int l, int g) const { return (uint32_t)(l * stride() + g); }
+  MK_HD uint32_t attn(int l, int g) const { return (uint32_t)(l * stride() + Hkv + g); }
+  MK_HD uint32_t oproj(int l) const { return (uint32_t)(l * stride() + 2 * Hkv); }
+  MK_HD uint32_t mlp(int l) const { return (uint32_t)(l * stride() + 2 * Hkv + 1); }
+  MK_HD uint32_t router(int l) const { return (uint32_t)(l * stride() + 2 * Hkv + 2); }
+  MK_HD uint32_t lm() const { return (uint32_t)(L * stride()); }
+  MK_HD int count() const { return L * stride() + 1; }
+};
+
+// Kernel-shape constants.
+constexpr int NCW = 8;               // consumer warps
+constexpr int NCT = NCW * 32;        // consumer threads
+constexpr int NTHREADS = NCT + 32;   // + one producer warp
+constexpr int STAGE_BYTES = 32768;   // bytes per ring stage
+constexpr int MAX_ROWS = 256;        // rows of one QKV / gate-up / router instruction
+constexpr int MAX_COLS = MAX_ROWS / 2;
+
+// Device pointers of one layer inside the packed weight buffer.
+struct LayerPtrs {
+  const uint16_t* attn_norm;  // [H]
+  const uint16_t* mlp_norm;   // [H]
+  const uint16_t* wqkv;       // [Hkv][(HPG+2)*D][H]; per head rows (t, t+D/2) adjacent
+  const uint16_t* wo;         // [Hq][H][D]
+  const uint16_t* wgu;        // dense: [F][2][H]      (gate row, up row)
+  const uint16_t* wdT;        // dense: [F][H]         (down, transposed)
+  const uint16_t* router;     // MoE:   [E][H]
+  const uint16_t* ex_gu;      // MoE:   [E][Fe][2][H]
+  const uint16_t* ex_dT;      // MoE:   [E][Fe][H]
+  const uint16_t* sh_gu;      // MoE:   [Fs][2][H]
+  const uint16_t* sh_dT;      // MoE:   [Fs][H]
+  uint16_t* kc;               // caller cache [maxB][Hkv][max_seq][D]
+  uint16_t* vc;
+};
+
+// Kernel parameter block (passed by value as __grid_constant__).
+struct Globals {
+  const Instr* sched;
+  const LayerPtrs* layers;
+  const uint16_t* embed;
+  const uint16_t* lm_head;
+  const uint16_t* final_norm;
+  const float* rope;       // [max_seq][D/2][2] (cos, sin)
+  float* xbuf;             // [2][2L][B][H] residual stream, x_1 .. x_2L per parity
+  float* qbuf;             // [L][B][Hq][D]
+  float* part;             // [L][B][Hq][splits][D+2]: o[D], m, l  (log2 domain)
+  float* rlog;             // [L][B][E] router logits
+  float* lm_val;           // [n_lm][B]
+  int* lm_idx;             // [n_lm][B]
+  uint32_t* ctr;           // dependency counters
+  int* err;                // [4]: status, sm, pc, op
+  const int* tokens;
+  const int* positions;
+  float* logits;
+  int* argmax;
+  unsigned long long timeout_ns;
+  int max_pc, n_sm, n_stages;
+  int B, H, Hq, Hkv, D, F, V, L, max_seq, max_ctx, splits;
+  int E, K, Fe, Fs;
+  float eps;
+  uint32_t epoch;          // step number (>= 1); counter targets are epoch * count
+  int parity;              // epoch & 1: which residual buffer set this step uses
+  uint32_t lm_ctr;
+  int n_lm;
+  int sel_key;             // -1: run every instruction; else only key == sel_key (ablation)
+  int zero_next;           // zero the other parity's residual buffers in this launch
+  int pdl;                 // ablation with programmatic dependent launch
+};
+
+// Shared-memory layout (bytes from the dynamic shared memory base).
+struct SmemLayout {
+  int ring, full, empty, xn, yrow, hbuf, attn, red, misc, total;
+};
+
+MK_HD inline SmemLayout smem_layout(int n_stages, int NB, int H, int D, int HPG, int K) {
+  SmemLayout s;
+  int o = 0;
+  s.ring = o;   o += n_stages * STAGE_BYTES;
+  s.full = o;   o += 8 * n_stages;
+  s.empty = o;  o += 8 * n_stages;
+  o = (o + 15) / 16 * 16;
+  s.xn = o;     o += 4 * NB * H;
+  s.yrow = o;
+  int yb = 4 * NB * MAX_ROWS;
+  int mb = 4 * NCW * HPG * (D + 2);
+  o += ((yb > mb ? yb : mb) + 15) / 16 * 16;
+  s.hbuf = o;   o += 4 * NB * MAX_COLS;
+  s.attn = o;   o += 4 * NB * D;
+  s.red = o;    o += 4 * 2 * NCW * NB + 16;
+  s.misc = o;   o += 4 * (8 + 3 * NB + 4 * NB * (K > 0 ? K : 1));
+  s.total = (o + 127) / 128 * 128;
+  return s;
+}
+
+// One compiled instantiation of the interpreter.
+struct Variant {
+  int H, D, HPG, NB;
+  const void* kernel;  // host stub of mk_decode_kernel<H, D, HPG, NB>
+};
+
+// A built schedule: queues [n_sm][max_pc] (HALT-padded) and their statistics.
+struct PlanOut {
+  std::vector<Instr> q;
+  int max_pc = 0, n_ctr = 0, splits = 0, n_lm = 0, n_instr = 0;
+  double max_sm_bytes = 0, mean_sm_bytes = 0, weight_bytes = 0;
+};
+int plan_shape_ok(const mk_model_desc& d);
+int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& out);
+int plan_verify(const mk_model_desc& d, int B, const PlanOut& p);
+int plan_check(const Instr* q, int n_sm, int max_pc, int n_ctr);
+
+}  // namespace mk

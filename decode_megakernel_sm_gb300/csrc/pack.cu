@@ -1,0 +1,99 @@
+// pack.cu -- device-side re-layout of the caller's bf16 weights into the
+// instruction-contiguous layouts the interpreter streams (one run per
+// instruction, one bulk copy per ring stage, no tensor map needed):
+//   QKV   [Hkv][(HPG+2)*D][H]  per kv head: its HPG query heads, then k, then
+//                              v; inside a head, rows 2t / 2t+1 = dims t / t+D/2
+//   Wo    [Hq][H][D]           one head's columns as contiguous 128/256-byte rows
+//   gate/up [F][2][H]          gate row c, then up row c
+//   down  [F][H]               transposed: one contiguous row per FFN column
+#include <cuda_runtime.h>
+
+#include "mk_internal.h"
+
+namespace mk {
+
+__global__ void pack_qkv_kernel(uint4* __restrict__ dst, const uint16_t* __restrict__ wq,
+                                const uint16_t* __restrict__ wk, const uint16_t* __restrict__ wv,
+                                int H, int HPG, int D) {
+  const int p = blockIdx.x;
+  const int GR = (HPG + 2) * D;
+  const int g = p / GR, lr = p % GR, hs = lr / D, e = lr % D;
+  const int dim = (e & 1) ? (e >> 1) + D / 2 : (e >> 1);
+  const uint16_t* src = hs < HPG   ? wq + ((size_t)(g * HPG + hs) * D + dim) * H
+                        : hs == HPG ? wk + ((size_t)g * D + dim) * H
+                                    : wv + ((size_t)g * D + dim) * H;
+  const uint4* s4 = (const uint4*)src;
+  uint4* d4 = dst + (size_t)p * (H / 8);
+  for (int i = threadIdx.x; i < H / 8; i += blockDim.x) d4[i] = s4[i];
+}
+
+// dst row 2c = a row c, dst row 2c+1 = b row c (rows of H elements).
+__global__ void pack_interleave_kernel(uint4* __restrict__ dst, const uint4* __restrict__ a,
+                                       const uint4* __restrict__ b, int H) {
+  const size_t c = blockIdx.x;
+  const int n = H / 8;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    dst[(2 * c) * n + i] = a[c * n + i];
+    dst[(2 * c + 1) * n + i] = b[c * n + i];
+  }
+}
+
+// dst[h][r][:] = wo[r][h*D : (h+1)*D], in 16-byte chunks.
+__global__ void pack_wo_kernel(uint4* __restrict__ dst, const uint4* __restrict__ wo, int H, int Hq,
+                               int D) {
+  const size_t total = (size_t)Hq * H * (D / 8);
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t c8 = i % (D / 8), hr = i / (D / 8);
+    const size_t r = hr % H, h = hr / H;
+    dst[i] = wo[(r * Hq + h) * (D / 8) + c8];
+  }
+}
+
+// Batched transpose of bf16 [R][C] -> [C][R]; blockIdx.z selects the matrix.
+__global__ void transpose_kernel(uint16_t* __restrict__ dst, const uint16_t* __restrict__ src, int R,
+                                 int C) {
+  __shared__ uint16_t tile[32][33];
+  const size_t off = (size_t)blockIdx.z * R * C;
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int k = threadIdx.y; k < 32; k += blockDim.y) {
+    const int r = r0 + k, c = c0 + threadIdx.x;
+    if (r < R && c < C) tile[k][threadIdx.x] = src[off + (size_t)r * C + c];
+  }
+  __syncthreads();
+  for (int k = threadIdx.y; k < 32; k += blockDim.y) {
+    const int c = c0 + k, r = r0 + threadIdx.x;
+    if (r < R && c < C) dst[off + (size_t)c * R + r] = tile[threadIdx.x][k];
+  }
+}
+
+cudaError_t pack_qkv(uint16_t* dst, const void* wq, const void* wk, const void* wv, int H, int Hkv,
+                     int HPG, int D, cudaStream_t s) {
+  pack_qkv_kernel<<<Hkv * (HPG + 2) * D, 128, 0, s>>>((uint4*)dst, (const uint16_t*)wq,
+                                                      (const uint16_t*)wk, (const uint16_t*)wv, H,
+                                                      HPG, D);
+  return cudaGetLastError();
+}
+
+cudaError_t pack_interleave(uint16_t* dst, const void* a, const void* b, long rows, int H,
+                            cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  pack_interleave_kernel<<<(unsigned)rows, 128, 0, s>>>((uint4*)dst, (const uint4*)a,
+                                                       (const uint4*)b, H);
+  return cudaGetLastError();
+}
+
+cudaError_t pack_wo(uint16_t* dst, const void* wo, int H, int Hq, int D, cudaStream_t s) {
+  pack_wo_kernel<<<2048, 256, 0, s>>>((uint4*)dst, (const uint4*)wo, H, Hq, D);
+  return cudaGetLastError();
+}
+
+cudaError_t pack_transpose(uint16_t* dst, const void* src, int R, int C, int batch,
+                           cudaStream_t s) {
+  if (R <= 0 || C <= 0 || batch <= 0) return cudaSuccess;
+  dim3 grid((C + 31) / 32, (R + 31) / 32, batch);
+  transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(dst, (const uint16_t*)src, R, C);
+  return cudaGetLastError();
+}
+
+}  // namespace mk

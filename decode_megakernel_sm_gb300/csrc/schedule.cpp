@@ -1,0 +1,414 @@
+// schedule.cpp -- host-side schedule builder and checker (plain C++, no CUDA).
+//
+// "Megakernels: Deleting the Kernel Boundary", section "One launch, one
+// interpreter": the per-SM instruction queues are computed on the host ahead
+// of time and reused for many forward passes.  Section "Correctness without
+// the free barrier": every dependency is a counter that producers increment
+// and consumers wait on, at a finer grain than a kernel boundary (per kv
+// head after QKV, per kv head after attention, per layer after O-proj/MLP).
+//
+// Balance: every phase is cut into n_sm contiguous row ranges of (nearly)
+// equal bytes, so no SM carries a wave-quantisation tail ("Where the
+// microseconds go": 512 blocks on 148 SMs leave a 68-SM last wave).
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
+#include "mk_internal.h"
+
+namespace mk {
+
+static long cut(long total, int n, int i, int align) {
+  long v = total * (long)i / n;
+  return v / align * align;
+}
+
+int plan_shape_ok(const mk_model_desc& d) {
+  if (d.n_layers <= 0 || d.hidden <= 0 || d.n_q_heads <= 0 || d.n_kv_heads <= 0 ||
+      d.head_dim <= 0 || d.vocab <= 0 || d.max_batch <= 0 || d.max_seq <= 0)
+    return MK_ERR_INVALID_ARG;
+  if (d.n_q_heads % d.n_kv_heads) return MK_ERR_INVALID_ARG;
+  if (!(d.rms_eps >= 0.f) || !(d.rope_theta > 0.f)) return MK_ERR_INVALID_ARG;
+  if (d.n_experts < 0 || d.top_k < 0 || d.expert_ffn < 0 || d.shared_ffn < 0 || d.ffn < 0)
+    return MK_ERR_INVALID_ARG;
+  if (d.n_experts == 0 && d.ffn <= 0) return MK_ERR_INVALID_ARG;
+  if (d.n_experts > 0 && (d.top_k <= 0 || d.top_k > d.n_experts || d.expert_ffn <= 0))
+    return MK_ERR_INVALID_ARG;
+  if (d.hidden % 256 || d.hidden > 16384) return MK_ERR_UNSUPPORTED;
+  if (d.head_dim != 64 && d.head_dim != 128) return MK_ERR_UNSUPPORTED;
+  if (d.n_q_heads / d.n_kv_heads > 8) return MK_ERR_UNSUPPORTED;
+  if (d.n_experts > 1024 || d.top_k > 16) return MK_ERR_UNSUPPORTED;
+  return MK_OK;
+}
+
+int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& out) {
+  int rc = plan_shape_ok(d);
+  if (rc) return rc;
+  if (B <= 0 || B > d.max_batch || max_ctx <= 0 || max_ctx > d.max_seq || n_sm <= 0)
+    return MK_ERR_INVALID_ARG;
+  const int L = d.n_layers, H = d.hidden, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
+  const int D = d.head_dim, HPG = Hq / Hkv, V = d.vocab;
+  const bool moe = d.n_experts > 0;
+  const int GR = (HPG + 2) * D;  // packed QKV rows per kv head
+  const long R = (long)Hkv * GR;
+  CtrMap cm{Hkv, L};
+
+  // split-KV slices per (sequence, kv head): about one work item per SM, at
+  // least 16 positions per slice on average at max_ctx, at most 256 slices.
+  int S = std::max(1, n_sm / (B * Hkv));
+  S = std::min(S, std::max(1, max_ctx / 16));
+  S = std::min(S, 256);
+  const int n_items = B * Hkv * S;
+
+  std::vector<std::vector<Instr>> qs(n_sm);
+  std::vector<double> bytes(n_sm, 0.0);
+  auto mk = [](uint8_t op, int layer) {
+    Instr I;
+    std::memset(&I, 0, sizeof I);
+    I.op = op;
+    I.layer = (uint16_t)layer;
+    I.wait_ctr = NO_CTR;
+    I.sig_ctr = NO_CTR;
+    return I;
+  };
+
+  // MoE virtual FFN: shared-expert columns [0, Fs) then top_k routed slots
+  // of expert_ffn columns each; dense: the ffn columns.
+  const long Fs = moe ? d.shared_ffn : 0;
+  const long Fv = moe ? Fs + (long)d.top_k * d.expert_ffn : d.ffn;
+
+  int n_lm = 0;
+  for (int l = 0; l < L; l++) {
+    // ---- QKV rows
+    for (int i = 0; i < n_sm; i++) {
+      long a = cut(R, n_sm, i, 2), b = cut(R, n_sm, i + 1, 2);
+      if (i == n_sm - 1) b = R;
+      bool first = true;
+      while (a < b) {
+        long g = a / GR;
+        long e = std::min(std::min(b, (g + 1) * GR), a + MAX_ROWS);
+        Instr I = mk(OP_QKV, l);
+        I.g = (uint16_t)g;
+        I.r0 = (uint32_t)a;
+        I.r1 = (uint32_t)e;
+        I.flags = first ? 0 : F_NORM_CACHED;
+        if (l > 0) I.wait_ctr = cm.mlp(l - 1);
+        I.sig_ctr = cm.qkv(l, (int)g);
+        qs[i].push_back(I);
+        bytes[i] += (double)(e - a) * H * 2;
+        first = false;
+        a = e;
+      }
+    }
+    // ---- attention items
+    for (int k = 0; k < n_items; k++) {
+      int sm = (int)((long)k * n_sm / n_items);
+      int b = k / (Hkv * S), g = (k / S) % Hkv, s = k % S;
+      Instr I = mk(OP_ATTN, l);
+      I.b = (uint16_t)b;
+      I.g = (uint16_t)g;
+      I.r0 = (uint32_t)s;
+      I.r1 = (uint32_t)S;
+      I.wait_ctr = cm.qkv(l, g);
+      I.sig_ctr = cm.attn(l, g);
+      qs[sm].push_back(I);
+      bytes[sm] += (double)max_ctx / S * D * 4;
+    }
+    // ---- O-projection: (head, row) space split into n_sm ranges
+    const long OR = (long)Hq * H;
+    for (int i = 0; i < n_sm; i++) {
+      long a = cut(OR, n_sm, i, 1), b = (i == n_sm - 1) ? OR : cut(OR, n_sm, i + 1, 1);
+      while (a < b) {
+        long h = a / H;
+        long e = std::min(b, (h + 1) * H);
+        Instr I = mk(OP_OPROJ, l);
+        I.g = (uint16_t)h;
+        I.r0 = (uint32_t)(a - h * H);
+        I.r1 = (uint32_t)(e - h * H);
+        I.flags = h == 0 ? F_RESIDUAL : 0;
+        I.wait_ctr = cm.attn(l, (int)(h / HPG));
+        I.sig_ctr = cm.oproj(l);
+        qs[i].push_back(I);
+        bytes[i] += (double)(e - a) * D * 2;
+        a = e;
+      }
+    }
+    // ---- MoE router rows
+    if (moe) {
+      const long E = d.n_experts;
+      for (int i = 0; i < n_sm; i++) {
+        long a = cut(E, n_sm, i, 1), b = (i == n_sm - 1) ? E : cut(E, n_sm, i + 1, 1);
+        while (a < b) {
+          long e = std::min(b, a + MAX_ROWS);
+          Instr I = mk(OP_ROUTER, l);
+          I.r0 = (uint32_t)a;
+          I.r1 = (uint32_t)e;
+          I.wait_ctr = cm.oproj(l);
+          I.sig_ctr = cm.router(l);
+          qs[i].push_back(I);
+          bytes[i] += (double)(e - a) * H * 2;
+          a = e;
+        }
+      }
+    }
+    // ---- MLP column slices (dense FFN, or MoE shared + routed slots)
+    std::vector<std::pair<int, size_t>> mlp_at;  // (sm, index in qs[sm])
+    // MoE: every SM takes a slice of the shared columns first (their weights
+    // stream while the router resolves), then a slice of the routed columns.
+    std::vector<std::pair<long, long>> fsegs;
+    if (moe) {
+      if (Fs > 0) fsegs.push_back({0, Fs});
+      fsegs.push_back({Fs, Fv});
+    } else {
+      fsegs.push_back({0, Fv});
+    }
+    for (int i = 0; i < n_sm; i++)
+      for (auto& fs : fsegs) {
+      const long span = fs.second - fs.first;
+      long a = fs.first + cut(span, n_sm, i, 1);
+      long b = fs.first + ((i == n_sm - 1) ? span : cut(span, n_sm, i + 1, 1));
+      while (a < b) {
+        long seg_end = Fv;
+        int slot = -1;
+        if (moe) {
+          if (a < Fs) {
+            seg_end = Fs;
+          } else {
+            slot = (int)((a - Fs) / d.expert_ffn);
+            seg_end = Fs + (long)(slot + 1) * d.expert_ffn;
+          }
+        }
+        long e = std::min(std::min(b, seg_end), a + MAX_COLS);
+        Instr I = mk(OP_MLP, l);
+        if (!moe) {
+          I.r0 = (uint32_t)a;
+          I.r1 = (uint32_t)e;
+          I.wait_ctr = cm.oproj(l);
+        } else if (slot < 0) {
+          I.flags = F_SHARED;
+          I.r0 = (uint32_t)a;
+          I.r1 = (uint32_t)e;
+          I.wait_ctr = cm.oproj(l);
+        } else {
+          long base = Fs + (long)slot * d.expert_ffn;
+          I.g = (uint16_t)slot;
+          I.r0 = (uint32_t)(a - base);
+          I.r1 = (uint32_t)(e - base);
+          I.wait_ctr = cm.router(l);
+        }
+        I.sig_ctr = cm.mlp(l);
+        I.flags |= F_RESIDUAL;
+        qs[i].push_back(I);
+        mlp_at.push_back({i, qs[i].size() - 1});
+        bytes[i] += (double)(e - a) * H * 6;
+        a = e;
+      }
+      }
+    // residual rows [k*H/n, (k+1)*H/n) go to MLP instruction k of this layer
+    const int n_mlp = (int)mlp_at.size();
+    for (int k = 0; k < n_mlp; k++) {
+      Instr& I = qs[mlp_at[k].first][mlp_at[k].second];
+      uint32_t rs0 = (uint32_t)cut(H, n_mlp, k, 1);
+      uint32_t rs1 = (k == n_mlp - 1) ? (uint32_t)H : (uint32_t)cut(H, n_mlp, k + 1, 1);
+      I.aux = rs0 | (rs1 << 16);
+    }
+  }
+  // ---- LM head rows (+ argmax by the last arriver)
+  for (int i = 0; i < n_sm; i++) {
+    long a = cut(V, n_sm, i, 1), b = (i == n_sm - 1) ? V : cut(V, n_sm, i + 1, 1);
+    if (a >= b) continue;
+    Instr I = mk(OP_LMHEAD, L);
+    I.r0 = (uint32_t)a;
+    I.r1 = (uint32_t)b;
+    I.wait_ctr = cm.mlp(L - 1);
+    I.aux = (uint32_t)n_lm++;
+    qs[i].push_back(I);
+    bytes[i] += (double)(b - a) * H * 2;
+  }
+
+  // ---- counter targets: a wait is for every signal of its counter
+  const int n_ctr = cm.count();
+  std::vector<uint32_t> cnt(n_ctr, 0);
+  for (auto& q : qs)
+    for (auto& I : q)
+      if (I.sig_ctr != NO_CTR) cnt[I.sig_ctr]++;
+  for (auto& q : qs)
+    for (auto& I : q)
+      if (I.wait_ctr != NO_CTR) I.wait_cnt = cnt[I.wait_ctr];
+
+  // ---- flatten, HALT-padded
+  size_t mx = 0, total = 0;
+  for (auto& q : qs) {
+    mx = std::max(mx, q.size());
+    total += q.size();
+  }
+  out.max_pc = (int)mx + 1;
+  out.q.assign((size_t)n_sm * out.max_pc, mk(OP_HALT, 0));
+  for (int i = 0; i < n_sm; i++)
+    std::copy(qs[i].begin(), qs[i].end(), out.q.begin() + (size_t)i * out.max_pc);
+  out.n_ctr = n_ctr;
+  out.splits = S;
+  out.n_lm = n_lm;
+  out.n_instr = (int)total;
+  double sum = 0, m = 0;
+  for (double v : bytes) {
+    sum += v;
+    m = std::max(m, v);
+  }
+  out.max_sm_bytes = m;
+  out.mean_sm_bytes = sum / n_sm;
+  const double router_rows = moe ? (double)d.n_experts : 0.0;
+  out.weight_bytes = (double)L * ((double)R * H * 2 + (double)Hq * D * H * 2 +
+                                  router_rows * H * 2 + (double)Fv * H * 6 + 2.0 * H * 2) +
+                     (double)V * H * 2 + (double)H * 2;
+  return MK_OK;
+}
+
+// Coverage check of a built plan: every output row / column / work item of
+// every phase is produced by exactly one instruction, pieces respect the
+// group / pair / size limits the kernel relies on, and every residual row is
+// added exactly once per layer.
+int plan_verify(const mk_model_desc& d, int B, const PlanOut& p) {
+  const int L = d.n_layers, H = d.hidden, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
+  const int D = d.head_dim, HPG = Hq / Hkv, V = d.vocab, GR = (HPG + 2) * D;
+  const bool moe = d.n_experts > 0;
+  const long R = (long)Hkv * GR, Fs = moe ? d.shared_ffn : 0;
+  const long Fv = moe ? Fs + (long)d.top_k * d.expert_ffn : d.ffn;
+  const int S = p.splits;
+  std::vector<uint8_t> qkv((size_t)L * R, 0), att((size_t)L * B * Hkv * S, 0);
+  std::vector<uint8_t> op((size_t)L * Hq * H, 0), mlp((size_t)L * Fv, 0), res((size_t)L * H, 0);
+  std::vector<uint8_t> rt((size_t)L * (moe ? d.n_experts : 1), 0), lm(V, 0), slot(p.n_lm, 0);
+  auto mark = [](std::vector<uint8_t>& v, size_t i) {
+    if (i >= v.size() || v[i]) return false;
+    v[i] = 1;
+    return true;
+  };
+  for (const Instr& I : p.q) {
+    const int l = I.layer;
+    switch (I.op) {
+      case OP_HALT: break;
+      case OP_QKV:
+        if (l >= L || I.r0 >= I.r1 || I.r1 > R || I.r1 - I.r0 > (uint32_t)MAX_ROWS) return 1;
+        if (I.r0 / GR != I.g || (I.r1 - 1) / GR != I.g || (I.r0 % 2) || (I.r1 % 2)) return 2;
+        for (uint32_t r = I.r0; r < I.r1; r++)
+          if (!mark(qkv, (size_t)l * R + r)) return 3;
+        break;
+      case OP_ATTN:
+        if (l >= L || I.b >= B || I.g >= Hkv || (int)I.r1 != S || (int)I.r0 >= S) return 4;
+        if (!mark(att, (((size_t)l * B + I.b) * Hkv + I.g) * S + I.r0)) return 5;
+        break;
+      case OP_OPROJ:
+        if (l >= L || I.g >= Hq || I.r0 >= I.r1 || (int)I.r1 > H) return 6;
+        if (((I.flags & F_RESIDUAL) != 0) != (I.g == 0)) return 7;
+        for (uint32_t r = I.r0; r < I.r1; r++)
+          if (!mark(op, ((size_t)l * Hq + I.g) * H + r)) return 8;
+        break;
+      case OP_ROUTER:
+        if (!moe || l >= L || I.r0 >= I.r1 || (int)I.r1 > d.n_experts ||
+            I.r1 - I.r0 > (uint32_t)MAX_ROWS)
+          return 9;
+        for (uint32_t r = I.r0; r < I.r1; r++)
+          if (!mark(rt, (size_t)l * d.n_experts + r)) return 10;
+        break;
+      case OP_MLP: {
+        if (l >= L || I.r0 >= I.r1 || I.r1 - I.r0 > (uint32_t)MAX_COLS) return 11;
+        long base = 0, width = Fv;
+        if (moe) {
+          if (I.flags & F_SHARED) {
+            width = Fs;
+          } else {
+            if (I.g >= d.top_k) return 12;
+            base = Fs + (long)I.g * d.expert_ffn;
+            width = d.expert_ffn;
+          }
+        }
+        if ((long)I.r1 > width) return 13;
+        for (uint32_t c = I.r0; c < I.r1; c++)
+          if (!mark(mlp, (size_t)l * Fv + base + c)) return 14;
+        uint32_t rs0 = I.aux & 0xFFFF, rs1 = I.aux >> 16;
+        if (rs1 > (uint32_t)H || rs0 > rs1) return 15;
+        for (uint32_t r = rs0; r < rs1; r++)
+          if (!mark(res, (size_t)l * H + r)) return 16;
+        break;
+      }
+      case OP_LMHEAD:
+        if (I.r0 >= I.r1 || (int)I.r1 > V || (int)I.aux >= p.n_lm) return 17;
+        if (!mark(slot, I.aux)) return 18;
+        for (uint32_t r = I.r0; r < I.r1; r++)
+          if (!mark(lm, r)) return 19;
+        break;
+      default:
+        return 20;
+    }
+  }
+  for (auto* v : {&qkv, &att, &op, &mlp, &res, &lm, &slot})
+    for (uint8_t x : *v)
+      if (!x) return 21;
+  if (moe)
+    for (uint8_t x : rt)
+      if (!x) return 22;
+  return 0;
+}
+
+// In-order execution of every queue under the wait semantics: an
+// instruction runs once its counter has received wait_cnt signals.  A
+// deadlock is any state where no queue can advance before all reach HALT.
+int plan_check(const Instr* q, int n_sm, int max_pc, int n_ctr) {
+  if (!q || n_sm <= 0 || max_pc <= 0 || n_ctr <= 0) return MK_ERR_INVALID_ARG;
+  std::vector<int> pc(n_sm, 0);
+  std::vector<uint64_t> cnt(n_ctr, 0);
+  for (;;) {
+    bool progress = false, done = true;
+    for (int s = 0; s < n_sm; s++) {
+      for (;;) {
+        if (pc[s] >= max_pc) break;
+        const Instr& I = q[(size_t)s * max_pc + pc[s]];
+        if (I.op == OP_HALT) break;
+        if (I.wait_ctr != NO_CTR) {
+          if (I.wait_ctr >= (uint32_t)n_ctr) return MK_ERR_SCHEDULE;
+          if (cnt[I.wait_ctr] < I.wait_cnt) break;
+        }
+        if (I.sig_ctr != NO_CTR) {
+          if (I.sig_ctr >= (uint32_t)n_ctr) return MK_ERR_SCHEDULE;
+          cnt[I.sig_ctr]++;
+        }
+        pc[s]++;
+        progress = true;
+      }
+      if (pc[s] < max_pc && q[(size_t)s * max_pc + pc[s]].op != OP_HALT) done = false;
+    }
+    if (done) return MK_OK;
+    if (!progress) return MK_ERR_SCHEDULE;
+  }
+}
+
+}  // namespace mk
+
+extern "C" int mk_plan(const mk_model_desc* desc, int batch, int max_ctx, int n_sm,
+                       mk_plan_stats* stats, mk_instr* out, size_t out_cap) {
+  if (!desc) return MK_ERR_INVALID_ARG;
+  mk::PlanOut p;
+  int rc = mk::plan_build(*desc, batch, max_ctx, n_sm, p);
+  if (rc) return rc;
+  if (mk::plan_verify(*desc, batch, p)) return MK_ERR_SCHEDULE;
+  if (mk::plan_check(p.q.data(), n_sm, p.max_pc, p.n_ctr)) return MK_ERR_SCHEDULE;
+  if (stats) {
+    stats->n_sm = n_sm;
+    stats->max_pc = p.max_pc;
+    stats->n_instr = p.n_instr;
+    stats->n_counters = p.n_ctr;
+    stats->attn_splits = p.splits;
+    stats->n_lm = p.n_lm;
+    stats->max_sm_bytes = p.max_sm_bytes;
+    stats->mean_sm_bytes = p.mean_sm_bytes;
+  }
+  if (out) {
+    if (out_cap < p.q.size()) return MK_ERR_INVALID_ARG;
+    std::memcpy(out, p.q.data(), p.q.size() * sizeof(mk_instr));
+  }
+  return MK_OK;
+}
+
+extern "C" int mk_plan_check(const mk_instr* q, int n_sm, int max_pc, int n_counters) {
+  return mk::plan_check(q, n_sm, max_pc, n_counters);
+}

@@ -1,0 +1,127 @@
+"""Decoder: a thin object over the C ABI that keeps the caller's tensors alive
+and marshals torch CUDA tensors to device pointers.  No arithmetic here."""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import _lib as L
+
+
+def desc_from_config(cfg: dict, max_batch: int, max_seq: int) -> L.mk_model_desc:
+    d = L.mk_model_desc()
+    for n in ("n_layers", "hidden", "n_q_heads", "n_kv_heads", "head_dim", "ffn", "vocab",
+              "n_experts", "top_k", "expert_ffn", "shared_ffn"):
+        setattr(d, n, int(cfg.get(n, 0)))
+    d.rms_eps = float(cfg["rms_eps"])
+    d.rope_theta = float(cfg["rope_theta"])
+    d.tied_lm_head = 1 if cfg.get("tied", True) else 0
+    d.max_batch = int(max_batch)
+    d.max_seq = int(max_seq)
+    return d
+
+
+def _ptr(t, dtype=None):
+    if t is None:
+        return None
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
+        raise ValueError("expected a contiguous CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"expected {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return C.c_void_p(stream.cuda_stream)
+    return C.c_void_p(stream)
+
+
+class Decoder:
+    """One megakernel handle for a model whose weights and KV cache are CUDA tensors.
+
+    weights: dict as produced by ``synth.make_weights`` (bf16, [out][in]);
+    kcache / vcache: per-layer bf16 tensors [max_batch][Hkv][max_seq][head_dim]."""
+
+    def __init__(self, cfg: dict, weights: dict, kcache, vcache):
+        max_batch, _, max_seq, _ = kcache[0].shape
+        self.cfg = cfg
+        self.desc = desc_from_config(cfg, max_batch, max_seq)
+        nl = cfg["n_layers"]
+        bf = torch.bfloat16
+        w = L.mk_weights()
+        w.embed = _ptr(weights["embed"], bf)
+        w.lm_head = _ptr(weights.get("lm_head"), bf)
+        w.final_norm = _ptr(weights["final_norm"], bf)
+        self._arrays = []
+        for name in L.WEIGHT_LISTS:
+            ts = [lw.get(name) for lw in weights["layers"]]
+            if all(t is None for t in ts):
+                continue
+            arr = (C.c_void_p * nl)(*[_ptr(t, bf) for t in ts])
+            self._arrays.append(arr)
+            setattr(w, name, C.cast(arr, C.POINTER(C.c_void_p)))
+        ka = (C.c_void_p * nl)(*[_ptr(t, bf) for t in kcache])
+        va = (C.c_void_p * nl)(*[_ptr(t, bf) for t in vcache])
+        self._arrays += [ka, va]
+        kv = L.mk_kv(C.cast(ka, C.POINTER(C.c_void_p)), C.cast(va, C.POINTER(C.c_void_p)))
+        self.kcache, self.vcache = kcache, vcache  # the library writes row P in place
+        self.h = L.mk_create(self.desc, w, kv)
+        self.batch = 0
+
+    # -- schedule ---------------------------------------------------------
+    def build_schedule(self, batch: int, max_ctx: int):
+        L.mk_build_schedule(self.h, batch, max_ctx)
+        self.batch = batch
+
+    def info(self) -> dict:
+        return L.mk_get_info(self.h)
+
+    def set_wait_timeout(self, ns: int):
+        L.mk_set_wait_timeout(self.h, int(ns))
+
+    def drop_instruction(self, sm: int, pc: int):
+        L.mk_debug_drop_instruction(self.h, sm, pc)
+
+    # -- steps ------------------------------------------------------------
+    def step(self, tokens, positions, logits, argmax, stream=None):
+        """Device-buffer step (asynchronous): int32 tokens/positions [B], fp32 logits
+        [B][V], int32 argmax [B]."""
+        i32 = torch.int32
+        L.mk_decode_step(self.h, _ptr(tokens, i32), _ptr(positions, i32),
+                         _ptr(logits, torch.float32), _ptr(argmax, i32), _stream(stream))
+
+    def step_ablation(self, mode, tokens, positions, logits, argmax, stream=None):
+        i32 = torch.int32
+        L.mk_decode_step_ablation(self.h, mode, _ptr(tokens, i32), _ptr(positions, i32),
+                                  _ptr(logits, torch.float32), _ptr(argmax, i32),
+                                  _stream(stream))
+
+    def step_host(self, tokens, positions, logits, argmax) -> int:
+        """Host-buffer step (synchronous).  Accepts CPU int32 / fp32 tensors (pinned
+        for speed); logits may be None.  Returns the status."""
+        def hp(t, dt):
+            if t is None:
+                return None
+            if t.device.type != "cpu" or t.dtype != dt or not t.is_contiguous():
+                raise ValueError("expected a contiguous CPU tensor of " + str(dt))
+            return t.data_ptr()
+        return L.mk_decode_step_host(self.h, hp(tokens, torch.int32), hp(positions, torch.int32),
+                                     hp(logits, torch.float32), hp(argmax, torch.int32))
+
+    def sync_status(self, stream=None) -> int:
+        return L.mk_sync_status(self.h, _stream(stream))
+
+    def close(self):
+        if self.h:
+            L.mk_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,222 @@
+/*
+ * mk.h -- C ABI of the GB300 decode megakernel library (libmk.so).
+ *
+ * One low-batch transformer decode step runs as ONE persistent CUDA kernel
+ * (one CTA per SM) that interprets a per-SM queue of opcoded instructions,
+ * replaces kernel boundaries with a global-memory counter array, and streams
+ * weights through a TMA bulk-copy shared-memory ring.  The design follows
+ * "Megakernels: Deleting the Kernel Boundary to Win Back Microseconds"
+ * (sections "One launch, one interpreter", "Correctness without the free
+ * barrier"), re-planned for sm_103a.
+ *
+ * Conventions
+ *  - Every pointer named d_* is a CUDA device pointer; h_* is host memory.
+ *  - Weights are bf16 (IEEE binary32 upper halves), row-major [out][in].
+ *  - All calls return MK_OK (0) or a negative MK_ERR_* code; no call aborts
+ *    the process, and no kernel traps: device-side faults in the schedule
+ *    (a wait that never completes) or in the inputs (a token or position
+ *    out of range) set a device error word that mk_sync_status() returns.
+ *  - A handle is not thread-safe; use one handle per host thread.
+ *  - `stream` arguments are cudaStream_t values passed as void* (NULL is the
+ *    legacy default stream).
+ */
+#ifndef MK_H
+#define MK_H
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MK_OK 0
+#define MK_ERR_INVALID_ARG (-1) /* bad pointer, shape, token or position          */
+#define MK_ERR_CUDA (-2)        /* a CUDA runtime call failed                      */
+#define MK_ERR_UNSUPPORTED (-3) /* shape with no compiled kernel variant           */
+#define MK_ERR_SCHEDULE (-4)    /* schedule failed its deadlock / coverage check   */
+#define MK_ERR_TIMEOUT (-5)     /* a device wait ran past its time limit           */
+#define MK_ERR_NOT_READY (-6)   /* mk_build_schedule has not succeeded yet         */
+#define MK_ERR_DEVICE (-7)      /* device reported an internal inconsistency       */
+
+typedef struct mk_handle mk_handle;
+
+/* Decoder shape.  Dense MLP when n_experts == 0 (ffn used); otherwise a
+ * routed MoE MLP with n_experts experts of width expert_ffn, top_k of them
+ * per token, plus an always-on shared expert of width shared_ffn (0: none).
+ * "Gemma 4 TPU megakernel", section "Megakernels for Gemma 4", lists the
+ * router / experts / shared MLP components of that MoE step.             */
+typedef struct {
+  int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
+  float rms_eps, rope_theta;
+  int tied_lm_head;                 /* 1: the LM head is the embedding matrix */
+  int n_experts, top_k, expert_ffn, shared_ffn;
+  int max_batch, max_seq;           /* KV cache capacity (rows per kv head)   */
+} mk_model_desc;
+
+/* Weight pointers (device, bf16).  Per-layer fields are HOST arrays of
+ * n_layers device pointers.  mk_create copies (and re-lays-out) every weight
+ * into a library-owned buffer, so the caller may free its copies after
+ * mk_create returns.  Fields a model does not use may be NULL.
+ *   embed [vocab][hidden], lm_head [vocab][hidden] (NULL when tied),
+ *   final_norm [hidden], attn_norm/mlp_norm [hidden],
+ *   wq [n_q_heads*head_dim][hidden], wk/wv [n_kv_heads*head_dim][hidden],
+ *   wo [hidden][n_q_heads*head_dim],
+ *   dense: w_gate/w_up [ffn][hidden], w_down [hidden][ffn],
+ *   MoE:   router [n_experts][hidden], ex_gate/ex_up [n_experts][expert_ffn][hidden],
+ *          ex_down [n_experts][hidden][expert_ffn],
+ *          sh_gate/sh_up [shared_ffn][hidden], sh_down [hidden][shared_ffn].   */
+typedef struct {
+  const void* embed;
+  const void* lm_head;
+  const void* final_norm;
+  const void* const* attn_norm;
+  const void* const* wq;
+  const void* const* wk;
+  const void* const* wv;
+  const void* const* wo;
+  const void* const* mlp_norm;
+  const void* const* w_gate;
+  const void* const* w_up;
+  const void* const* w_down;
+  const void* const* router;
+  const void* const* ex_gate;
+  const void* const* ex_up;
+  const void* const* ex_down;
+  const void* const* sh_gate;
+  const void* const* sh_up;
+  const void* const* sh_down;
+} mk_weights;
+
+/* KV cache, caller-owned, bf16.  k[l], v[l] (HOST arrays of n_layers device
+ * pointers) each point at [max_batch][n_kv_heads][max_seq][head_dim], 16-byte
+ * aligned.  Rows [0, P) of sequence b must hold the already-rotated keys and
+ * the values of earlier positions; mk_decode_step writes row P in place.
+ * The cache must stay allocated for the life of the handle.               */
+typedef struct {
+  void* const* k;
+  void* const* v;
+} mk_kv;
+
+/* Create a handle on the current CUDA device: validates the shape, selects
+ * the compiled kernel variant (MK_ERR_UNSUPPORTED if none), copies and packs
+ * the weights on the device (synchronous), allocates counters and scratch.
+ * On error *out is NULL and nothing is leaked.                            */
+int mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv, mk_handle** out);
+
+/* Build the per-SM instruction queues for `batch` sequences whose positions
+ * will stay below `max_ctx` (<= max_seq): splits every projection into
+ * byte-balanced row ranges, one split-KV attention work item per
+ * (sequence, kv head, split), assigns counter ids and targets, checks the
+ * queues for deadlock and coverage on the host (MK_ERR_SCHEDULE), uploads
+ * them and zeroes the counters.  Synchronous.  Must precede any step.     */
+int mk_build_schedule(mk_handle* h, int batch, int max_ctx);
+
+/* One decode step, asynchronous on `stream`, one kernel launch.
+ *   d_tokens    [batch] int32: token fed at this step (may alias the d_argmax
+ *               of the previous step);
+ *   d_positions [batch] int32: P, the cache row written by this step; each
+ *               sequence attends to rows [0, P]; must satisfy P < max_ctx;
+ *   d_logits    [batch][vocab] fp32 output;
+ *   d_argmax    [batch] int32 output: first index of the largest logit.
+ * Out-of-range tokens or positions are detected on the device before any
+ * write; the step then writes nothing and mk_sync_status() returns
+ * MK_ERR_INVALID_ARG.                                                     */
+int mk_decode_step(mk_handle* h, const int32_t* d_tokens, const int32_t* d_positions,
+                   float* d_logits, int32_t* d_argmax, void* stream);
+
+/* The same step from HOST buffers: copies h_tokens / h_positions to the
+ * device, runs the step on the handle's own stream, copies logits (may be
+ * NULL to skip) and argmax back, and waits.  Validates tokens and positions
+ * on the host first.                                                       */
+int mk_decode_step_host(mk_handle* h, const int32_t* h_tokens, const int32_t* h_positions,
+                        float* h_logits, int32_t* h_argmax);
+
+/* Ablation: the same instruction bodies, one kernel launch per (layer,
+ * phase) instead of one persistent launch.  "Megakernels: Deleting the
+ * Kernel Boundary", section "Where the microseconds go", describes the
+ * per-operator launch sequence this reproduces.
+ *   mode MK_ABL_STREAM: plain launches on `stream`;
+ *   mode MK_ABL_GRAPH : the same launches captured once into a CUDA graph
+ *                       (cached per argument set) and replayed;
+ *   mode MK_ABL_PDL   : plain launches with programmatic dependent launch,
+ *                       each kernel starts its weight prefetch before
+ *                       waiting on its predecessor.                        */
+#define MK_ABL_STREAM 0
+#define MK_ABL_GRAPH 1
+#define MK_ABL_PDL 2
+int mk_decode_step_ablation(mk_handle* h, int mode, const int32_t* d_tokens,
+                            const int32_t* d_positions, float* d_logits, int32_t* d_argmax,
+                            void* stream);
+
+/* Wait for `stream` and return the device error word (MK_OK if none).  A
+ * non-OK result also resets the counters and scratch so that the next step
+ * starts clean (the KV rows written by the failed step are unspecified).  */
+int mk_sync_status(mk_handle* h, void* stream);
+
+/* Limit, in nanoseconds, of every device-side wait (default 2 s). */
+int mk_set_wait_timeout(mk_handle* h, uint64_t ns);
+
+typedef struct {
+  int n_sm;               /* CTAs of the persistent kernel (= SMs)          */
+  int stage_bytes;        /* bytes per shared-memory ring stage             */
+  int n_stages;           /* ring stages                                    */
+  int smem_bytes;         /* dynamic shared memory per CTA                  */
+  int max_pc;             /* instructions per SM queue (incl. HALT)         */
+  int n_instr;            /* instructions in the schedule                   */
+  int n_counters;         /* counters in the dependency array               */
+  int attn_splits;        /* split-KV slices per (sequence, kv head)        */
+  int launches_per_step;  /* megakernel: 1                                  */
+  int ablation_launches;  /* launches per step in the ablation modes        */
+  int batch, max_ctx;
+  size_t packed_bytes;    /* library-owned weight copy                      */
+  size_t scratch_bytes;   /* counters + activations + partials              */
+  double weight_bytes_per_step; /* weights one step must read (routed MoE: active experts) */
+} mk_info;
+int mk_get_info(const mk_handle* h, mk_info* out);
+
+/* Replace instruction `pc` of SM `sm` by a no-op that neither waits nor
+ * signals -- a fault-injection aid for tests: every instruction waiting on
+ * the dropped one's counter then runs into its time limit and the step
+ * fails with MK_ERR_TIMEOUT instead of hanging.  Undone by the next
+ * mk_build_schedule.                                                       */
+int mk_debug_drop_instruction(mk_handle* h, int sm, int pc);
+
+int mk_destroy(mk_handle* h);
+const char* mk_status_string(int status);
+
+/* ---- host-only planning (no GPU needed) ---------------------------------
+ * The schedule builder and its checker, exposed for inspection and tests.
+ * Instructions are 32-byte records:
+ *   op, flags (u8), layer (u16), b, g (u16), r0, r1, wait_ctr, wait_cnt,
+ *   sig_ctr, aux (u32).  op: 0 HALT, 1 QKV, 2 ATTN, 3 OPROJ, 4 MLP,
+ *   5 LMHEAD, 6 ROUTER, 7 NOP.  wait_ctr / sig_ctr 0xFFFFFFFF: none.      */
+typedef struct {
+  uint8_t op, flags;
+  uint16_t layer;
+  uint16_t b, g;
+  uint32_t r0, r1;
+  uint32_t wait_ctr, wait_cnt;
+  uint32_t sig_ctr, aux;
+} mk_instr;
+
+typedef struct {
+  int n_sm, max_pc, n_instr, n_counters, attn_splits, n_lm;
+  double max_sm_bytes, mean_sm_bytes; /* streamed bytes per SM (weights + KV at max_ctx) */
+} mk_plan_stats;
+
+/* Build the schedule for `n_sm` SMs on the host.  If `out` is non-NULL and
+ * `out_cap` >= n_sm * max_pc records, the queues are written there
+ * ([n_sm][max_pc], HALT-padded).  Returns MK_OK or an MK_ERR_* code.     */
+int mk_plan(const mk_model_desc* desc, int batch, int max_ctx, int n_sm, mk_plan_stats* stats,
+            mk_instr* out, size_t out_cap);
+
+/* Check queues [n_sm][max_pc] against n_counters counters: simulates
+ * in-order execution of every queue under the wait semantics; MK_OK if all
+ * queues run to HALT, MK_ERR_SCHEDULE on a deadlock (some wait can never be
+ * met) or an out-of-range counter id.                                      */
+int mk_plan_check(const mk_instr* q, int n_sm, int max_pc, int n_counters);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,91 @@
+"""Parity harness: run the CUDA decode path and the CPU oracle on the same seeded
+inputs, teacher-forcing the oracle with the GPU's emitted tokens.
+
+Acceptance per step and sequence (the decode contract):
+  * max |logit_gpu - logit_oracle| <= 2e-2 * std(logit_oracle);
+  * argmax_gpu == argmax_oracle wherever the oracle's top-2 margin > 5e-2;
+  * argmax_gpu is exactly the first index of the maximum of the GPU's own logits;
+  * the K/V rows appended at P match the oracle's bf16 rows to one bf16 ulp.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+from decode_megakernel_sm_gb300 import Decoder
+
+TOL = 2e-2
+MARGIN = 5e-2
+
+
+class Run:
+    def __init__(self, cfg: dict, seed: int = 0, max_ctx: int | None = None):
+        cfg = cfg if "max_seq" in cfg else synth.with_cache(cfg)
+        self.cfg = cfg
+        self.W = synth.make_weights(cfg, seed, "cuda")
+        self.lengths = synth.make_lengths(cfg, seed)
+        self.ks, self.vs = synth.make_kv(cfg, self.lengths, seed, "cuda")
+        torch.cuda.synchronize()
+        self.ko = [oracle._bits(t.cpu()).copy() for t in self.ks]
+        self.vo = [oracle._bits(t.cpu()).copy() for t in self.vs]
+        self.om = oracle.OracleModel(cfg, self.W)
+        self.dec = Decoder(cfg, self.W, self.ks, self.vs)
+        self.B = cfg["batch"]
+        self.max_ctx = max_ctx or cfg["max_seq"]
+        self.dec.build_schedule(self.B, self.max_ctx)
+        self.tokens = synth.make_tokens(cfg, seed)
+        self.pos = list(self.lengths)
+        dev = "cuda"
+        self.d_tok = torch.tensor(self.tokens, dtype=torch.int32, device=dev)
+        self.d_pos = torch.tensor(self.pos, dtype=torch.int32, device=dev)
+        self.d_logits = torch.empty((self.B, cfg["vocab"]), dtype=torch.float32, device=dev)
+        self.d_am = torch.empty(self.B, dtype=torch.int32, device=dev)
+        self.worst = 0.0
+
+    def gpu_step(self, mode: str = "mega"):
+        self.d_tok.copy_(torch.tensor(self.tokens, dtype=torch.int32))
+        self.d_pos.copy_(torch.tensor(self.pos, dtype=torch.int32))
+        if mode == "mega":
+            self.dec.step(self.d_tok, self.d_pos, self.d_logits, self.d_am)
+        else:
+            self.dec.step_ablation({"stream": 0, "graph": 1, "pdl": 2}[mode], self.d_tok,
+                                   self.d_pos, self.d_logits, self.d_am)
+        status = self.dec.sync_status()
+        assert status == 0, f"device status {status}"
+        return self.d_logits.cpu().numpy().astype(np.float64), self.d_am.cpu().numpy()
+
+    def check(self, lg, am, lo, ao):
+        for b in range(self.B):
+            std = lo[b].std()
+            d = np.abs(lg[b] - lo[b]).max()
+            self.worst = max(self.worst, d / std)
+            assert d <= TOL * std, f"b={b}: max|dlogit| {d:.3e} > {TOL} * std {std:.3e}"
+            assert am[b] == int(np.argmax(lg[b])), "argmax is not the first max of the logits"
+            s = np.sort(lo[b])
+            if s[-1] - s[-2] > MARGIN:
+                assert am[b] == ao[b], f"b={b}: argmax {am[b]} vs oracle {ao[b]}"
+
+    def check_kv(self):
+        for l in range(self.cfg["n_layers"]):
+            for b in range(self.B):
+                P = self.pos[b]
+                for gpu, ora in ((self.ks[l], self.ko[l]), (self.vs[l], self.vo[l])):
+                    g = gpu[b, :, P, :].float().cpu().numpy()
+                    o = (ora[b, :, P, :].astype(np.uint32) << 16).view(np.float32)
+                    assert np.all(np.abs(g - o) <= 2.0 ** -7 * np.abs(o) + 1e-6), \
+                        f"layer {l} b {b}: appended K/V row differs"
+
+    def step(self, mode: str = "mega", check_kv: bool = True):
+        lg, am = self.gpu_step(mode)
+        lo, ao, _, _ = self.om.step(self.ko, self.vo, self.tokens, self.pos)
+        self.check(lg, am, lo, ao)
+        if check_kv:
+            self.check_kv()
+        self.tokens = [int(a) for a in am]
+        self.pos = [p + 1 for p in self.pos]
+        return lg, am
+
+    def close(self):
+        self.dec.close()

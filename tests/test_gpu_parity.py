@@ -1,0 +1,116 @@
+"""GPU parity of the megakernel against the CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from decode_megakernel_sm_gb300 import MK_ERR_INVALID_ARG, MK_ERR_TIMEOUT, MK_OK
+from tests.harness import Run
+
+pytestmark = pytest.mark.gpu
+
+
+def run_steps(cfg, steps, seed=0, **kw):
+    r = Run(cfg, seed, **kw)
+    try:
+        for _ in range(steps):
+            r.step()
+        return r.worst
+    finally:
+        r.close()
+
+
+def test_tiny_parity_8_steps():
+    run_steps(synth.CONFIGS["tiny"], 8)
+
+
+def test_ragged_small_shape_parity():
+    # 3 kv heads x 2 q heads, FFN and vocab not multiples of anything, 3 layers
+    cfg = synth.custom(n_layers=3, n_q_heads=6, n_kv_heads=3, ffn=1000, vocab=999,
+                       prefill=(37, 37), steps=4)
+    run_steps(cfg, 4, seed=3)
+
+
+def test_position_zero_attends_to_itself_only():
+    run_steps(synth.custom(prefill=(0, 0), steps=3), 3, seed=5)
+
+
+def test_last_position_below_max_ctx():
+    cfg = synth.custom(prefill=(40, 40), steps=1)
+    r = Run(cfg, seed=6, max_ctx=41)  # P = 40 = max_ctx - 1
+    try:
+        r.step()
+        # P = max_ctx is rejected on the device, and the handle recovers
+        r.d_pos.fill_(41)
+        r.dec.step(r.d_tok, r.d_pos, r.d_logits, r.d_am)
+        assert r.dec.sync_status() == MK_ERR_INVALID_ARG
+        r.pos = [40]
+        r.step()
+    finally:
+        r.close()
+
+
+def test_batch8_variant_ragged_lengths():
+    cfg = synth.custom(n_layers=2, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=64, ffn=3000,
+                       vocab=5000, batch=8, prefill=(0, 300), steps=3, rope_theta=5e5)
+    run_steps(cfg, 3, seed=7)
+
+
+def test_llama1b_1k_parity():
+    cfg = synth.CONFIGS["llama1b_1k"]
+    worst = run_steps(cfg, 3, seed=0)
+    print(f"llama1b_1k worst max|dlogit|/std = {worst:.2e}")
+
+
+def test_llama1b_8k_parity():
+    run_steps(synth.CONFIGS["llama1b_8k"], 2, seed=1)
+
+
+def test_ablation_modes_match_megakernel():
+    cfg = synth.custom(n_layers=3, n_q_heads=6, n_kv_heads=3, ffn=1000, vocab=999,
+                       prefill=(20, 20), steps=6)
+    r = Run(cfg, seed=11)
+    try:
+        for mode in ("stream", "graph", "pdl", "mega"):
+            pos0, tok0 = list(r.pos), list(r.tokens)
+            lg_m, am_m = r.gpu_step("mega")
+            lg_a, am_a = r.gpu_step(mode)
+            assert np.array_equal(am_m, am_a), mode
+            assert np.abs(lg_m - lg_a).max() <= 1e-3 * lg_m.std(), mode
+            r.pos, r.tokens = pos0, tok0
+            r.step(mode)  # and against the oracle
+    finally:
+        r.close()
+
+
+def test_missing_producer_times_out_and_recovers():
+    r = Run(synth.CONFIGS["tiny"], seed=2)
+    try:
+        r.dec.set_wait_timeout(50_000_000)  # 50 ms
+        r.dec.drop_instruction(0, 0)  # SM 0's first QKV slice never signals
+        r.dec.step(r.d_tok, r.d_pos, r.d_logits, r.d_am)
+        assert r.dec.sync_status() == MK_ERR_TIMEOUT
+        r.dec.build_schedule(r.B, r.max_ctx)  # restores the dropped instruction
+        r.step()
+        r.step()
+    finally:
+        r.close()
+
+
+def test_host_buffer_step_matches_and_validates():
+    r = Run(synth.CONFIGS["tiny"], seed=4)
+    try:
+        cfg = r.cfg
+        tok = torch.tensor(r.tokens, dtype=torch.int32).pin_memory()
+        pos = torch.tensor(r.pos, dtype=torch.int32).pin_memory()
+        lg = torch.empty((1, cfg["vocab"]), dtype=torch.float32).pin_memory()
+        am = torch.empty(1, dtype=torch.int32).pin_memory()
+        assert r.dec.step_host(tok, pos, lg, am) == MK_OK
+        lo, ao, _, _ = r.om.step(r.ko, r.vo, r.tokens, r.pos)
+        r.check(lg.numpy().astype(np.float64), am.numpy(), lo, ao)
+        bad = torch.tensor([cfg["vocab"]], dtype=torch.int32)
+        assert r.dec.step_host(bad, pos, lg, am) == MK_ERR_INVALID_ARG
+        badp = torch.tensor([r.max_ctx], dtype=torch.int32)
+        assert r.dec.step_host(tok, badp, lg, am) == MK_ERR_INVALID_ARG
+    finally:
+        r.close()

@@ -1,0 +1,176 @@
+"""Host-only tests of libmk.so: exported symbols, the schedule builder and its
+deadlock / coverage checker.  No GPU needed (no compute call is made)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import synth
+from decode_megakernel_sm_gb300 import _lib as L
+from decode_megakernel_sm_gb300.decoder import desc_from_config
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            names |= set(re.findall(r"^(?:int|const char\*)\s+(mk_\w+)\s*\(", src, re.M))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = L.lib()
+    names = declared_symbols()
+    assert len(names) >= 13
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+
+
+def test_status_strings():
+    for s in range(0, -8, -1):
+        assert L.mk_status_string(s) not in ("", "unknown status")
+    assert L.mk_status_string(-99) == "unknown status"
+
+
+def desc(name, **over):
+    cfg = synth.with_cache(dict(synth.CONFIGS[name], **over))
+    return cfg, desc_from_config(cfg, cfg["batch"], cfg["max_seq"])
+
+
+def queues(q, n_sm, max_pc):
+    return [[q[s * max_pc + i] for i in range(max_pc)] for s in range(n_sm)]
+
+
+def independent_coverage(cfg, q, n_sm, max_pc, splits):
+    """Re-derive, in Python, that every unit of work appears exactly once."""
+    Lc, H, Hq, Hkv, D = cfg["n_layers"], cfg["hidden"], cfg["n_q_heads"], cfg["n_kv_heads"], \
+        cfg["head_dim"]
+    B = cfg["batch"]
+    R = Hkv * (Hq // Hkv + 2) * D
+    moe = cfg["n_experts"] > 0
+    Fv = cfg["shared_ffn"] + cfg["top_k"] * cfg["expert_ffn"] if moe else cfg["ffn"]
+    seen = {k: set() for k in ("qkv", "attn", "oproj", "mlp", "res", "lm", "router")}
+    sig = {}
+    for s in range(n_sm):
+        for i in range(max_pc):
+            I = q[s * max_pc + i]
+            if I.op == 0:
+                break
+            if I.sig_ctr != 0xFFFFFFFF:
+                sig[I.sig_ctr] = sig.get(I.sig_ctr, 0) + 1
+            if I.op == 1:
+                for r in range(I.r0, I.r1):
+                    assert (I.layer, r) not in seen["qkv"]
+                    seen["qkv"].add((I.layer, r))
+            elif I.op == 2:
+                key = (I.layer, I.b, I.g, I.r0)
+                assert key not in seen["attn"] and I.r1 == splits
+                seen["attn"].add(key)
+            elif I.op == 3:
+                for r in range(I.r0, I.r1):
+                    seen["oproj"].add((I.layer, I.g, r))
+            elif I.op == 4:
+                base = 0
+                if moe and not (I.flags & 4):
+                    base = cfg["shared_ffn"] + I.g * cfg["expert_ffn"]
+                for c in range(I.r0, I.r1):
+                    assert (I.layer, base + c) not in seen["mlp"]
+                    seen["mlp"].add((I.layer, base + c))
+                for r in range(I.aux & 0xFFFF, I.aux >> 16):
+                    assert (I.layer, r) not in seen["res"]
+                    seen["res"].add((I.layer, r))
+            elif I.op == 5:
+                for r in range(I.r0, I.r1):
+                    assert r not in seen["lm"]
+                    seen["lm"].add(r)
+            elif I.op == 6:
+                for r in range(I.r0, I.r1):
+                    seen["router"].add((I.layer, r))
+    assert len(seen["qkv"]) == Lc * R
+    assert len(seen["attn"]) == Lc * B * Hkv * splits
+    assert len(seen["oproj"]) == Lc * Hq * H
+    assert len(seen["mlp"]) == Lc * Fv
+    assert len(seen["res"]) == Lc * H
+    assert len(seen["lm"]) == cfg["vocab"]
+    assert len(seen["router"]) == (Lc * cfg["n_experts"] if moe else 0)
+    # every wait is for all signals of its counter
+    for s in range(n_sm):
+        for i in range(max_pc):
+            I = q[s * max_pc + i]
+            if I.op == 0:
+                break
+            if I.wait_ctr != 0xFFFFFFFF:
+                assert I.wait_cnt == sig[I.wait_ctr] > 0
+
+
+@pytest.mark.parametrize("name", list(synth.CONFIGS))
+@pytest.mark.parametrize("n_sm", [1, 7, 148, 152])
+def test_plan_covers_all_work_and_is_deadlock_free(name, n_sm):
+    cfg, d = desc(name)
+    st, q = L.mk_plan(d, cfg["batch"], cfg["max_seq"], n_sm)
+    assert st["n_sm"] == n_sm
+    independent_coverage(cfg, q, n_sm, st["max_pc"], st["attn_splits"])
+    assert L.mk_plan_check(q, n_sm, st["max_pc"], st["n_counters"]) == L.MK_OK
+
+
+def test_llama1b_plan_is_byte_balanced():
+    cfg, d = desc("llama1b_1k")
+    st, _ = L.mk_plan(d, 1, cfg["max_seq"], 152, with_queues=False)
+    assert st["max_sm_bytes"] / st["mean_sm_bytes"] < 1.03
+    assert 120 <= st["attn_splits"] * cfg["n_kv_heads"] <= 152
+
+
+def test_checker_rejects_unsatisfiable_wait():
+    cfg, d = desc("tiny")
+    st, q = L.mk_plan(d, 1, cfg["max_seq"], 16)
+    for i in range(len(q)):
+        if q[i].op == 2:  # an attention item: wait one signal more than will ever come
+            q[i].wait_cnt += 1
+            break
+    assert L.mk_plan_check(q, 16, st["max_pc"], st["n_counters"]) == L.MK_ERR_SCHEDULE
+
+
+def test_checker_rejects_cyclic_order():
+    cfg, d = desc("tiny")
+    n_sm = 4
+    st, q = L.mk_plan(d, 1, cfg["max_seq"], n_sm)
+    mp = st["max_pc"]
+    # on SM 0 move a layer-1 QKV (waits on all layer-0 MLP slices) in front of
+    # SM 0's own layer-0 MLP slice: a cycle through SM 0's queue
+    row = [q[i] for i in range(mp)]
+    i_mlp = next(i for i, I in enumerate(row) if I.op == 4 and I.layer == 0)
+    i_qkv = next(i for i, I in enumerate(row) if I.op == 1 and I.layer == 1)
+    saved = L.mk_instr()
+    C.memmove(C.byref(saved), C.byref(q[i_qkv]), C.sizeof(saved))
+    for k in range(i_qkv, i_mlp, -1):
+        C.memmove(C.byref(q[k]), C.byref(q[k - 1]), C.sizeof(saved))
+    C.memmove(C.byref(q[i_mlp]), C.byref(saved), C.sizeof(saved))
+    assert L.mk_plan_check(q, n_sm, mp, st["n_counters"]) == L.MK_ERR_SCHEDULE
+
+
+def test_checker_rejects_bad_counter_id():
+    cfg, d = desc("tiny")
+    st, q = L.mk_plan(d, 1, cfg["max_seq"], 8)
+    q[0].sig_ctr = st["n_counters"] + 5
+    assert L.mk_plan_check(q, 8, st["max_pc"], st["n_counters"]) == L.MK_ERR_SCHEDULE
+
+
+def test_plan_rejects_bad_arguments():
+    cfg, d = desc("tiny")
+    with pytest.raises(L.MkError) as e:
+        L.mk_plan(d, 0, cfg["max_seq"], 8)
+    assert e.value.status == L.MK_ERR_INVALID_ARG
+    with pytest.raises(L.MkError) as e:
+        L.mk_plan(d, 1, cfg["max_seq"] + 1, 8)
+    assert e.value.status == L.MK_ERR_INVALID_ARG
+    with pytest.raises(L.MkError) as e:
+        L.mk_plan(d, 2, cfg["max_seq"], 8)  # batch above max_batch
+    assert e.value.status == L.MK_ERR_INVALID_ARG
+    _, d2 = desc("tiny", head_dim=96)
+    with pytest.raises(L.MkError) as e:
+        L.mk_plan(d2, 1, 64, 8)
+    assert e.value.status == L.MK_ERR_UNSUPPORTED
