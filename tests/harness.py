@@ -74,8 +74,10 @@ class Run:
                 for gpu, ora in ((self.ks[l], self.ko[l]), (self.vs[l], self.vo[l])):
                     g = gpu[b, :, P, :].float().cpu().numpy()
                     o = (ora[b, :, P, :].astype(np.uint32) << 16).view(np.float32)
-                    assert np.all(np.abs(g - o) <= 2.0 ** -7 * np.abs(o) + 1e-6), \
-                        f"layer {l} b {b}: appended K/V row differs"
+                    # one bf16 ulp, plus fp32-vs-fp64 accumulation noise at the row's scale
+                    tol = 2.0 ** -7 * np.abs(o) + 1e-3 * np.sqrt(np.mean(o * o))
+                    assert np.all(np.abs(g - o) <= tol), \
+                        f"layer {l} b {b}: appended K/V row differs by {np.abs(g - o).max()}"
 
     def step(self, mode: str = "mega", check_kv: bool = True):
         lg, am = self.gpu_step(mode)
