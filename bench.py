@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ablation", action="store_true", help="also time the per-phase launches")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--trace", default=None,
+                    help="write a per-instruction timeline of 3 traced steps to this path")
     return ap.parse_args()
 
 
@@ -341,6 +343,18 @@ def main():
                 abl[name] = None
         line["ablation_ms_per_step"] = abl
         line["ablation_launches_per_step"] = info["ablation_launches"]
+
+    if args.trace:
+        from decode_megakernel_sm_gb300.trace import chrome_trace, summarize
+        dec.set_trace(True)
+        run(3)
+        barrier()
+        tr, q, n_sm, max_pc = dec.get_trace()
+        dec.set_trace(False)
+        summ = summarize(tr, q, n_sm, max_pc)
+        chrome_trace(tr, q, n_sm, max_pc, args.trace)
+        with open(args.trace + ".summary.json", "w") as f:
+            json.dump(summ, f, indent=1)
 
     if not args.no_e2e:
         # the public host-buffer call: pinned inputs in, logits + argmax out, every step

@@ -87,6 +87,8 @@ SIGNATURES = {
     "mk_set_wait_timeout": (C.c_int, [C.c_void_p, C.c_uint64]),
     "mk_get_info": (C.c_int, [C.c_void_p, C.POINTER(mk_info)]),
     "mk_debug_drop_instruction": (C.c_int, [C.c_void_p, C.c_int, C.c_int]),
+    "mk_set_trace": (C.c_int, [C.c_void_p, C.c_int]),
+    "mk_get_trace": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.c_size_t]),
     "mk_destroy": (C.c_int, [C.c_void_p]),
     "mk_status_string": (C.c_char_p, [C.c_int]),
     "mk_plan": (C.c_int, [C.POINTER(mk_model_desc), C.c_int, C.c_int, C.c_int,
@@ -169,6 +171,19 @@ def mk_get_info(h) -> dict:
 
 def mk_debug_drop_instruction(h, sm: int, pc: int):
     _check(lib().mk_debug_drop_instruction(h, sm, pc), "mk_debug_drop_instruction")
+
+
+def mk_set_trace(h, on: bool):
+    _check(lib().mk_set_trace(h, 1 if on else 0), "mk_set_trace")
+
+
+def mk_get_trace(h, n_sm: int, max_pc: int):
+    """Returns a numpy uint64 array [n_sm][max_pc][4] of %globaltimer stamps."""
+    import numpy as np
+    out = np.zeros((n_sm, max_pc, 4), np.uint64)
+    _check(lib().mk_get_trace(h, out.ctypes.data_as(C.POINTER(C.c_uint64)), out.size),
+           "mk_get_trace")
+    return out
 
 
 def mk_destroy(h):

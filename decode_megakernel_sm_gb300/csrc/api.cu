@@ -59,6 +59,7 @@ struct mk_handle {
   int32_t *d_tok = nullptr, *d_pos = nullptr, *d_am = nullptr;
   float* d_logits = nullptr;
   int* h_err = nullptr;  // pinned [4]
+  unsigned long long* trace = nullptr;  // [n_sm][max_pc][4] when tracing is on
   // graph-mode ablation cache
   std::map<std::tuple<const void*, const void*, const void*, const void*, const void*>,
            cudaGraphExec_t>
@@ -90,6 +91,8 @@ static const Variant* pick_variant(const mk_model_desc& d) {
 }
 
 static void free_schedule(mk_handle* h) {
+  if (h->trace) cudaFree(h->trace);
+  h->trace = nullptr;
   for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
   h->graphs.clear();
   if (h->sched) cudaFree(h->sched);
@@ -181,7 +184,7 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
   CK(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->dev));
   const int K = moe ? d.top_k : 0;
   int ns = 0;
-  for (int n = 2; n <= 8; n++)
+  for (int n = 2; n <= MAX_STAGES; n++)
     if (smem_layout(n, h->var->NB, H, D, HPG, K).total <= optin) ns = n;
   if (ns < 2) return MK_ERR_UNSUPPORTED;
   h->n_stages = ns;
@@ -409,6 +412,7 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.lm_ctr = CtrMap{d.n_kv_heads, d.n_layers}.lm();
   g.n_lm = h->plan.n_lm;
   g.sel_key = -1;
+  g.trace = h->trace;
   return g;
 }
 
@@ -591,6 +595,35 @@ extern "C" int mk_get_info(const mk_handle* h, mk_info* out) {
   out->packed_bytes = h->packed_bytes;
   out->scratch_bytes = h->scratch_bytes;
   out->weight_bytes_per_step = h->plan.weight_bytes;
+  return MK_OK;
+}
+
+extern "C" int mk_set_trace(mk_handle* h, int on) {
+  if (!h) return MK_ERR_INVALID_ARG;
+  if (!h->sched) return MK_ERR_NOT_READY;
+  CK(cudaStreamSynchronize(h->own));
+  for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
+  h->graphs.clear();
+  if (!on) {
+    if (h->trace) cudaFree(h->trace);
+    h->trace = nullptr;
+    return MK_OK;
+  }
+  if (!h->trace) {
+    const size_t n = (size_t)h->n_sm * h->plan.max_pc * 4;
+    CK(cudaMalloc(&h->trace, n * sizeof(unsigned long long)));
+    CK(cudaMemset(h->trace, 0, n * sizeof(unsigned long long)));
+  }
+  return MK_OK;
+}
+
+extern "C" int mk_get_trace(mk_handle* h, uint64_t* out, size_t n) {
+  if (!h || !out) return MK_ERR_INVALID_ARG;
+  if (!h->trace) return MK_ERR_NOT_READY;
+  const size_t need = (size_t)h->n_sm * h->plan.max_pc * 4;
+  if (n < need) return MK_ERR_INVALID_ARG;
+  CK(cudaDeviceSynchronize());
+  CK(cudaMemcpy(out, h->trace, need * sizeof(uint64_t), cudaMemcpyDeviceToHost));
   return MK_OK;
 }
 

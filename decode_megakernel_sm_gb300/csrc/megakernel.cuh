@@ -494,18 +494,32 @@ MK_DEV void op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   constexpr int LPR = D / 8, SPW = 32 / LPR;
   const int slot = c.lane / LPR, dsl = c.lane % LPR;
   const int h = I.g, l = I.layer;
+  const int S = g.splits;
+  // (m, l) of every slice of every sequence in one parallel round trip ...
+  float* sm_m = c.yrow;
+  float* sm_l = c.yrow + NB * S;
+  for (int t = c.tid; t < g.B * S; t += NCT) {
+    const int b = t / S, s = t % S;
+    const float* p = g.part + ((((size_t)l * g.B + b) * g.Hq + h) * S + s) * (D + 2) + D;
+    sm_m[t] = __ldcg(p);
+    sm_l[t] = __ldcg(p + 1);
+  }
+  consumer_bar();
+  // ... then o[dim] of every slice, eight loads in flight per thread
   for (int t = c.tid; t < NB * D; t += NCT) {
     const int b = t / D, dim = t % D;
     if (b < g.B) {
-      const float* base = g.part + (((size_t)l * g.B + b) * g.Hq + h) * g.splits * (D + 2);
+      const float* base = g.part + (((size_t)l * g.B + b) * g.Hq + h) * S * (D + 2) + dim;
+      const float* mb = sm_m + b * S;
+      const float* lb = sm_l + b * S;
       float M = NEG_BIG;
-      for (int s = 0; s < g.splits; s++) M = fmaxf(M, __ldcg(base + s * (D + 2) + D));
+      for (int s = 0; s < S; s++) M = fmaxf(M, mb[s]);
       float Ls = 0.f, O = 0.f;
-      for (int s = 0; s < g.splits; s++) {
-        const float* p = base + s * (D + 2);
-        const float f = exp2f(__ldcg(p + D) - M);
-        Ls = fmaf(__ldcg(p + D + 1), f, Ls);
-        O = fmaf(__ldcg(p + dim), f, O);
+#pragma unroll 8
+      for (int s = 0; s < S; s++) {
+        const float f = exp2f(mb[s] - M);
+        Ls = fmaf(lb[s], f, Ls);
+        O = fmaf(__ldcg(base + (size_t)s * (D + 2)), f, O);
       }
       c.attn[b * D + dim] = O / Ls;
     }
@@ -826,6 +840,8 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
         if (lane == 0) ok = wait_mbar(g, empty0 + 8u * st, par ^ 1u, true);
         if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) goto drain;
         if (lane == 0) {
+          if (g.trace && k == 0 && u0 == 0)
+            g.trace[((size_t)blockIdx.x * g.max_pc + pc) * 4] = gtimer();
           const uint32_t bytes = n * s[k].unit;
           const uint32_t full = full0 + 8u * st;
           const uint32_t dst = ring_s + (uint32_t)st * STAGE_BYTES;
@@ -926,16 +942,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
   c.lane = lane;
   consumer_bar();  // everyone has read *flag before it is reused below
 
+  Instr next = load_instr(g, blockIdx.x, 0);
   for (int pc = 0; pc < g.max_pc; pc++) {
-    const Instr I = load_instr(g, blockIdx.x, pc);
+    const Instr I = next;
     if (I.op == OP_HALT) break;
+    if (pc + 1 < g.max_pc) next = load_instr(g, blockIdx.x, pc + 1);
     if (I.op == OP_NOP || !selected(g, I)) continue;
     c.pc = pc;
+    unsigned long long tw0 = 0, tw1 = 0;
     if (tid == 0) {
+      if (g.trace) tw0 = gtimer();
       bool ok = true;
       if (I.wait_ctr != NO_CTR) ok = wait_counter(g, I.wait_ctr, g.epoch * I.wait_cnt, pc, I.op);
       if (ok && peek_err(g)) ok = false;
       *flag = ok ? 0 : 1;
+      if (g.trace) tw1 = gtimer();
     }
     consumer_bar();
     if (*flag) return;
@@ -951,7 +972,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
         consumer_bar();
         break;
     }
-    if (tid == 0 && I.sig_ctr != NO_CTR) red_release(g.ctr + I.sig_ctr, 1u);
+    if (tid == 0) {
+      if (g.trace) {
+        unsigned long long* t = g.trace + ((size_t)blockIdx.x * g.max_pc + pc) * 4;
+        t[1] = tw0;
+        t[2] = tw1;
+        t[3] = gtimer();
+      }
+      if (I.sig_ctr != NO_CTR) red_release(g.ctr + I.sig_ctr, 1u);
+    }
   }
 }
 

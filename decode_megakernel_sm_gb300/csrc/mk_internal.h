@@ -74,7 +74,8 @@ struct CtrMap {
 constexpr int NCW = 8;               // consumer warps
 constexpr int NCT = NCW * 32;        // consumer threads
 constexpr int NTHREADS = NCT + 32;   // + one producer warp
-constexpr int STAGE_BYTES = 32768;   // bytes per ring stage
+constexpr int STAGE_BYTES = 16384;   // bytes per ring stage
+constexpr int MAX_STAGES = 16;
 constexpr int MAX_ROWS = 256;        // rows of one QKV / gate-up / router instruction
 constexpr int MAX_COLS = MAX_ROWS / 2;
 
@@ -127,6 +128,7 @@ struct Globals {
   int sel_key;             // -1: run every instruction; else only key == sel_key (ablation)
   int zero_next;           // zero the other parity's residual buffers in this launch
   int pdl;                 // ablation with programmatic dependent launch
+  unsigned long long* trace;  // optional [n_sm][max_pc][4] %globaltimer stamps (NULL: off)
 };
 
 // Shared-memory layout (bytes from the dynamic shared memory base).

@@ -54,10 +54,11 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
   CtrMap cm{Hkv, L};
 
   // split-KV slices per (sequence, kv head): about one work item per SM, at
-  // least 16 positions per slice on average at max_ctx, at most 256 slices.
+  // least 16 positions per slice on average at max_ctx, at most 128 slices
+  // (the O-projection stages every slice's (m, l) in shared memory).
   int S = std::max(1, n_sm / (B * Hkv));
   S = std::min(S, std::max(1, max_ctx / 16));
-  S = std::min(S, 256);
+  S = std::min(S, 128);
   const int n_items = B * Hkv * S;
 
   std::vector<std::vector<Instr>> qs(n_sm);

@@ -83,6 +83,16 @@ class Decoder:
     def set_wait_timeout(self, ns: int):
         L.mk_set_wait_timeout(self.h, int(ns))
 
+    def set_trace(self, on: bool):
+        L.mk_set_trace(self.h, on)
+
+    def get_trace(self):
+        """(stamps [n_sm][max_pc][4], host copy of the queues) of the last traced launch."""
+        info = self.info()
+        tr = L.mk_get_trace(self.h, info["n_sm"], info["max_pc"])
+        _, q = L.mk_plan(self.desc, info["batch"], info["max_ctx"], info["n_sm"])
+        return tr, q, info["n_sm"], info["max_pc"]
+
     def drop_instruction(self, sm: int, pc: int):
         L.mk_debug_drop_instruction(self.h, sm, pc)
 

@@ -1,0 +1,89 @@
+"""Timeline of one traced megakernel launch (see mk_set_trace / mk_get_trace).
+
+Each instruction slot holds four %globaltimer stamps (ns): the producer's
+first bulk copy of the instruction, the consumers' wait start, wait end and
+body end.  `summarize` attributes the step's time the way "Megakernels:
+Deleting the Kernel Boundary", section "What it buys, and where the time
+still goes", breaks down a forward pass: time spent waiting on dependencies
+versus time spent in instruction bodies, per opcode and per layer.
+`chrome_trace` writes the timeline in Chrome trace-event JSON."""
+from __future__ import annotations
+
+import json
+
+import numpy as np
+
+from . import _lib as L
+
+
+def _rows(trace, queues, n_sm, max_pc):
+    t = trace.astype(np.int64)
+    base = None
+    rows = []
+    for s in range(n_sm):
+        for pc in range(max_pc):
+            I = queues[s * max_pc + pc]
+            if I.op == 0:
+                break
+            ts = t[s, pc]
+            if ts[1] == 0 or ts[3] == 0:
+                continue
+            rows.append((s, pc, I.op, I.layer, ts[0], ts[1], ts[2], ts[3]))
+            base = ts[1] if base is None else min(base, ts[1])
+    return rows, base
+
+
+def summarize(trace, queues, n_sm: int, max_pc: int) -> dict:
+    rows, base = _rows(trace, queues, n_sm, max_pc)
+    if not rows:
+        return {}
+    end = max(r[7] for r in rows)
+    by_op = {}
+    for s, pc, op, layer, tp, tw0, tw1, te in rows:
+        d = by_op.setdefault(L.OP_NAMES[op], {"n": 0, "wait_us": 0.0, "body_us": 0.0,
+                                               "max_wait_us": 0.0})
+        d["n"] += 1
+        d["wait_us"] += (tw1 - tw0) / 1e3
+        d["body_us"] += (te - tw1) / 1e3
+        d["max_wait_us"] = max(d["max_wait_us"], (tw1 - tw0) / 1e3)
+    for d in by_op.values():
+        d["mean_wait_us"] = d["wait_us"] / d["n"]
+        d["mean_body_us"] = d["body_us"] / d["n"]
+    # per layer and phase: when the last instruction of the phase finished
+    phase_end = {}
+    for s, pc, op, layer, tp, tw0, tw1, te in rows:
+        k = (layer, L.OP_NAMES[op])
+        phase_end[k] = max(phase_end.get(k, 0), te - base)
+    layers = sorted({k[0] for k in phase_end})
+    per_layer = []
+    prev = 0
+    for l in layers:
+        e = max(v for k, v in phase_end.items() if k[0] == l)
+        per_layer.append({"layer": l, "end_us": e / 1e3, "span_us": (e - prev) / 1e3,
+                          "phases_end_us": {k[1]: v / 1e3 for k, v in phase_end.items()
+                                            if k[0] == l}})
+        prev = e
+    busy = np.zeros(n_sm)
+    waited = np.zeros(n_sm)
+    for s, pc, op, layer, tp, tw0, tw1, te in rows:
+        busy[s] += te - tw1
+        waited[s] += tw1 - tw0
+    return {"step_us": (end - base) / 1e3, "by_op": by_op, "per_layer": per_layer,
+            "mean_sm_body_us": float(busy.mean() / 1e3),
+            "mean_sm_wait_us": float(waited.mean() / 1e3)}
+
+
+def chrome_trace(trace, queues, n_sm: int, max_pc: int, path: str):
+    rows, base = _rows(trace, queues, n_sm, max_pc)
+    ev = []
+    for s, pc, op, layer, tp, tw0, tw1, te in rows:
+        name = f"{L.OP_NAMES[op]} L{layer}"
+        ev.append({"name": "wait " + name, "ph": "X", "pid": 0, "tid": s,
+                   "ts": (tw0 - base) / 1e3, "dur": (tw1 - tw0) / 1e3})
+        ev.append({"name": name, "ph": "X", "pid": 0, "tid": s, "ts": (tw1 - base) / 1e3,
+                   "dur": (te - tw1) / 1e3})
+        if tp:
+            ev.append({"name": "issue " + name, "ph": "i", "pid": 1, "tid": s,
+                       "ts": (tp - base) / 1e3, "s": "t"})
+    with open(path, "w") as f:
+        json.dump({"traceEvents": ev}, f)
