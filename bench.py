@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ablation", action="store_true", help="also time the per-phase launches")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--l2-ahead", type=int, default=None,
+                    help="bytes each SM warms in L2 ahead of its ring (library default if unset)")
     ap.add_argument("--trace", default=None,
                     help="write a per-instruction timeline of 3 traced steps to this path")
     return ap.parse_args()
@@ -250,6 +252,8 @@ def main():
     torch.cuda.synchronize()
     dec = Decoder(cfg, W, ks, vs)
     dec.build_schedule(B, cfg["max_seq"])
+    if args.l2_ahead is not None:
+        dec.set_l2_prefetch(args.l2_ahead)
     info = dec.info()
     stream = torch.cuda.current_stream()
     window = cfg["steps"]

@@ -88,6 +88,7 @@ SIGNATURES = {
     "mk_get_info": (C.c_int, [C.c_void_p, C.POINTER(mk_info)]),
     "mk_debug_drop_instruction": (C.c_int, [C.c_void_p, C.c_int, C.c_int]),
     "mk_set_trace": (C.c_int, [C.c_void_p, C.c_int]),
+    "mk_set_l2_prefetch": (C.c_int, [C.c_void_p, C.c_uint64]),
     "mk_get_trace": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.c_size_t]),
     "mk_destroy": (C.c_int, [C.c_void_p]),
     "mk_status_string": (C.c_char_p, [C.c_int]),
@@ -171,6 +172,10 @@ def mk_get_info(h) -> dict:
 
 def mk_debug_drop_instruction(h, sm: int, pc: int):
     _check(lib().mk_debug_drop_instruction(h, sm, pc), "mk_debug_drop_instruction")
+
+
+def mk_set_l2_prefetch(h, bytes_ahead: int):
+    _check(lib().mk_set_l2_prefetch(h, int(bytes_ahead)), "mk_set_l2_prefetch")
 
 
 def mk_set_trace(h, on: bool):

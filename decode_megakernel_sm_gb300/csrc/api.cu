@@ -54,6 +54,7 @@ struct mk_handle {
   std::vector<int> abl_keys;  // ablation launches (keys that own instructions)
   uint32_t epoch = 0;
   unsigned long long timeout_ns = 2000000000ull;
+  unsigned long long l2_ahead = 512ull << 10;
   // host-buffer step
   cudaStream_t own = nullptr;
   int32_t *d_tok = nullptr, *d_pos = nullptr, *d_am = nullptr;
@@ -413,6 +414,7 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.n_lm = h->plan.n_lm;
   g.sel_key = -1;
   g.trace = h->trace;
+  g.l2_ahead = h->l2_ahead;
   return g;
 }
 
@@ -572,6 +574,14 @@ extern "C" int mk_sync_status(mk_handle* h, void* stream) {
 extern "C" int mk_set_wait_timeout(mk_handle* h, uint64_t ns) {
   if (!h || ns < 1000) return MK_ERR_INVALID_ARG;
   h->timeout_ns = ns;
+  for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
+  h->graphs.clear();
+  return MK_OK;
+}
+
+extern "C" int mk_set_l2_prefetch(mk_handle* h, uint64_t bytes_ahead) {
+  if (!h) return MK_ERR_INVALID_ARG;
+  h->l2_ahead = bytes_ahead;
   for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
   h->graphs.clear();
   return MK_OK;

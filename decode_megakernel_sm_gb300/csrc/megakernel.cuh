@@ -786,6 +786,71 @@ MK_DEV bool selected(const Globals& g, const Instr& I) {
   return key == g.sel_key;
 }
 
+// Second cursor of the producer: walks the same chunk sequence as the ring
+// cursor and warms L2 with each chunk (cp.async.bulk.prefetch.L2) once the
+// ring cursor is within l2_ahead bytes of it.  While the consumers wait on a
+// dependency and the ring is full, HBM keeps streaming the SM's upcoming
+// weights into L2; the ring then refills from L2.  Lane 0 only.
+template <int HT, int D, int NB>
+struct L2Cursor {
+  int pc = 0, k = 0, nseg = 0;
+  uint32_t u0 = 0;
+  unsigned long long bytes = 0;
+  bool done = false;
+  Seg s[2];
+
+  MK_DEV void run(const Globals& g, unsigned long long limit, const int* ptopk, int routed_layer) {
+    while (!done && bytes < limit) {
+      if (k >= nseg) {
+        if (pc >= g.max_pc) {
+          done = true;
+          return;
+        }
+        const Instr I = load_instr(g, blockIdx.x, pc);
+        if (I.op == OP_HALT) {
+          done = true;
+          return;
+        }
+        if (I.op == OP_NOP || !selected(g, I)) {
+          pc++;
+          continue;
+        }
+        const bool routed = I.op == OP_MLP && g.E > 0 && !(I.flags & F_SHARED);
+        if (routed && routed_layer != (int)I.layer) return;  // addresses not known yet
+        int pos[NB];
+        if (I.op == OP_ATTN) {
+          if (g.pdl) {  // positions may still be written by the previous launch
+            pc++;
+            continue;
+          }
+          const int P = __ldg(g.positions + I.b);
+          if (P < 0 || P >= g.max_ctx) {
+            done = true;
+            return;
+          }
+          pos[I.b] = P;
+        }
+        nseg = get_segs<HT, D>(g, I, pos, ptopk, s);
+        k = 0;
+        u0 = 0;
+        pc++;
+        continue;
+      }
+      if (u0 >= s[k].n) {
+        k++;
+        u0 = 0;
+        continue;
+      }
+      const uint32_t n = min(s[k].ups, s[k].n - u0);
+      const uint32_t b = n * s[k].unit;
+      bulk_prefetch_l2(s[k].src + (size_t)u0 * s[k].unit, b);
+      if (s[k].src2) bulk_prefetch_l2(s[k].src2 + (size_t)u0 * s[k].unit, b);
+      bytes += s[k].src2 ? 2ull * b : b;
+      u0 += n;
+    }
+  }
+};
+
 // Producer warp: walks the queue and streams every instruction's segments
 // into the ring (lane 0 issues).  It waits only for free stages -- except
 // that a routed MoE slice needs the router result for its weight addresses.
@@ -803,6 +868,9 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
   uint32_t par = 0;
   bool grid_waited = !g.pdl;
   int routed_layer = -1;
+  unsigned long long issued_bytes = 0;
+  L2Cursor<HT, D, NB> l2;
+  if (lane == 0 && g.l2_ahead) l2.run(g, g.l2_ahead, ptopk, routed_layer);
   for (int pc = 0; pc < g.max_pc; pc++) {
     const Instr I = load_instr(g, blockIdx.x, pc);
     if (I.op == OP_HALT) break;
@@ -829,6 +897,8 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
       __syncwarp();
       route_topk(g.rlog + (size_t)I.layer * g.B * g.E, g.E, g.K, lane, ptopk, ptopw);
       routed_layer = I.layer;
+      __syncwarp();
+      if (lane == 0 && g.l2_ahead) l2.run(g, issued_bytes + g.l2_ahead, ptopk, routed_layer);
     }
     __syncwarp();
     Seg s[2];
@@ -853,6 +923,8 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
           } else {
             bulk_g2s(dst, s[k].src + (size_t)u0 * s[k].unit, bytes, full, pol_w);
           }
+          issued_bytes += s[k].src2 ? 2ull * bytes : bytes;
+          if (g.l2_ahead) l2.run(g, issued_bytes + g.l2_ahead, ptopk, routed_layer);
         }
         __syncwarp();
         issued++;

@@ -74,6 +74,12 @@ MK_DEV void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar
       : "memory");
 }
 
+// Warm L2 with a global range ahead of its bulk copy (no shared memory, no
+// completion tracking).  src and bytes are multiples of 16.
+MK_DEV void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 MK_DEV uint32_t ld_acquire(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

@@ -83,6 +83,9 @@ class Decoder:
     def set_wait_timeout(self, ns: int):
         L.mk_set_wait_timeout(self.h, int(ns))
 
+    def set_l2_prefetch(self, bytes_ahead: int):
+        L.mk_set_l2_prefetch(self.h, bytes_ahead)
+
     def set_trace(self, on: bool):
         L.mk_set_trace(self.h, on)
 

@@ -156,6 +156,12 @@ int mk_sync_status(mk_handle* h, void* stream);
 /* Limit, in nanoseconds, of every device-side wait (default 2 s). */
 int mk_set_wait_timeout(mk_handle* h, uint64_t ns);
 
+/* How far (bytes of each SM's own weight / KV stream) the kernel warms L2
+ * ahead of its shared-memory ring with cp.async.bulk.prefetch.L2; 0 turns
+ * the L2 lookahead off.  Default 512 KiB.  A performance knob only: results
+ * do not depend on it.                                                     */
+int mk_set_l2_prefetch(mk_handle* h, uint64_t bytes_ahead);
+
 typedef struct {
   int n_sm;               /* CTAs of the persistent kernel (= SMs)          */
   int stage_bytes;        /* bytes per shared-memory ring stage             */
