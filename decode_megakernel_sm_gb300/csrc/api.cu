@@ -54,7 +54,7 @@ struct mk_handle {
   std::vector<int> abl_keys;  // ablation launches (keys that own instructions)
   uint32_t epoch = 0;
   unsigned long long timeout_ns = 2000000000ull;
-  unsigned long long l2_ahead = 512ull << 10;
+  unsigned long long l2_ahead = 0;
   // host-buffer step
   cudaStream_t own = nullptr;
   int32_t *d_tok = nullptr, *d_pos = nullptr, *d_am = nullptr;

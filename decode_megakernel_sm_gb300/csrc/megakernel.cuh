@@ -31,10 +31,29 @@ struct Ctx {
   int* pos;     // [NB]
   int* topk;    // [NB][K] routed expert ids
   float* topw;  // [NB][K] routed expert weights
+  int* flag;    // abort flag shared by the consumer warps
   Ring ring;
   int tid, warp, lane;
   int pc;
+  unsigned long long tw0, tw1;  // trace: wait start / end (thread 0)
 };
+
+// The dependency wait of one instruction: thread 0 spins on the counter,
+// then all consumer warps meet; false if the grid has failed.  Every op
+// calls it exactly once, after issuing its dependency-free loads.
+template <int HT, int D, int HPG, int NB>
+MK_DEV bool dep_wait(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+  if (c.tid == 0) {
+    if (g.trace) c.tw0 = gtimer();
+    bool ok = true;
+    if (I.wait_ctr != NO_CTR) ok = wait_counter(g, I.wait_ctr, g.epoch * I.wait_cnt, c.pc, I.op);
+    if (ok && peek_err(g)) ok = false;
+    *c.flag = ok ? 0 : 1;
+    if (g.trace) c.tw1 = gtimer();
+  }
+  consumer_bar();
+  return *c.flag == 0;
+}
 
 // Residual stream x_j, j in [1, 2L] (x_0 is the embedding row).
 MK_DEV float* xres(const Globals& g, int j, int b) {
@@ -145,14 +164,35 @@ MK_DEV void route_topk(const float* lg, int E, int K, int lane, int* ids, float*
 
 // ---------------------------------------------------------------- norms ----
 // xn[b][k] = x[b][k] * rsqrt(mean(x^2) + eps) * gain[k] for the residual
-// x_j (j = 0: the embedding row of the token).  All consumer threads.
+// x_j (j = 0: the embedding row of the token).  The gain slice of each
+// thread is loaded before the dependency wait (norm_gain), the rest after
+// it (norm_apply).  All consumer threads.
+template <int HT>
+struct NormGain {
+  static constexpr int GROUPS = HT / 8;
+  static constexpr int GPT = (GROUPS + NCT - 1) / NCT;
+  uint4 w[GPT];  // 8 packed bf16 gains per 8-column group
+};
+
+template <int HT>
+MK_DEV void norm_gain(NormGain<HT>& ng, const uint16_t* gain, int tid) {
+#pragma unroll
+  for (int q = 0; q < NormGain<HT>::GPT; q++) {
+    const int gi = tid + q * NCT;
+    if (gi < NormGain<HT>::GROUPS) ng.w[q] = __ldg((const uint4*)gain + gi);
+  }
+}
+
 template <int HT, int D, int HPG, int NB>
-MK_DEV void norm_into_xn(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const uint16_t* gain) {
-  constexpr int GROUPS = HT / 8;
+MK_DEV void norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const NormGain<HT>& ng) {
+  constexpr int GROUPS = NormGain<HT>::GROUPS, GPT = NormGain<HT>::GPT;
   float ss[NB];
 #pragma unroll
   for (int b = 0; b < NB; b++) ss[b] = 0.f;
-  for (int gi = c.tid; gi < GROUPS; gi += NCT) {
+#pragma unroll
+  for (int q = 0; q < GPT; q++) {
+    const int gi = c.tid + q * NCT;
+    if (gi >= GROUPS) continue;
 #pragma unroll
     for (int b = 0; b < NB; b++) {
       float v[8];
@@ -191,9 +231,12 @@ MK_DEV void norm_into_xn(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const 
     for (int w = 0; w < NCW; w++) t += c.red[w * NB + b];
     rs[b] = rsqrtf(t / (float)HT + g.eps);
   }
-  for (int gi = c.tid; gi < GROUPS; gi += NCT) {
+#pragma unroll
+  for (int q = 0; q < GPT; q++) {
+    const int gi = c.tid + q * NCT;
+    if (gi >= GROUPS) continue;
     float gw[8];
-    unpack8(__ldg((const uint4*)gain + gi), gw);
+    unpack8(ng.w[q], gw);
 #pragma unroll
     for (int b = 0; b < NB; b++) {
       float4* o = (float4*)(c.xn + (size_t)b * HT) + 2 * gi;
@@ -292,9 +335,30 @@ namespace mk {
 // group [q heads of the group][k][v]; inside a head, packed rows 2t and 2t+1
 // hold head dims t and t + D/2, so each rotary pair is produced by one SM.
 template <int HT, int D, int HPG, int NB>
-MK_DEV void op_qkv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+  static_assert(MAX_ROWS <= 2 * NCT, "one rotary pair per thread");
   const LayerPtrs& Lp = g.layers[I.layer];
-  if (!(I.flags & F_NORM_CACHED)) norm_into_xn(c, g, 2 * I.layer, Lp.attn_norm);
+  const bool cached = (I.flags & F_NORM_CACHED) != 0;
+  NormGain<HT> ng;
+  if (!cached) norm_gain(ng, Lp.attn_norm, c.tid);
+  // this thread's rotary pair: head slot hs, dims (t, t + D/2), and its
+  // cos/sin at P -- none of it depends on the wait
+  constexpr int GR = (HPG + 2) * D;
+  const uint32_t n = I.r1 - I.r0;
+  const uint32_t i = 2u * (uint32_t)c.tid;
+  int hs = 0, t = 0;
+  float2 cs[NB];
+  if (i < n) {
+    const int lr = (int)(I.r0 + i) - (int)I.g * GR;
+    hs = lr / D;
+    t = (lr % D) >> 1;
+    if (hs <= HPG)
+#pragma unroll
+      for (int b = 0; b < NB; b++)
+        if (b < g.B) cs[b] = ((const float2*)g.rope)[(size_t)c.pos[b] * (D / 2) + t];
+  }
+  if (!dep_wait(c, g, I)) return false;
+  if (!cached) norm_apply(c, g, 2 * I.layer, ng);
   float xr[HT / 32];
   if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
   Seg s[2];
@@ -308,19 +372,15 @@ MK_DEV void op_qkv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
     }
   });
   consumer_bar();
-  constexpr int GR = (HPG + 2) * D;
-  const uint32_t n = I.r1 - I.r0;
-  for (uint32_t i = 2 * c.tid; i < n; i += 2 * NCT) {
-    const int lr = (int)(I.r0 + i) - (int)I.g * GR;
-    const int hs = lr / D;
-    const int t = (lr % D) >> 1;
-    for (int b = 0; b < g.B && b < NB; b++) {
+  if (i < n) {
+#pragma unroll
+    for (int b = 0; b < NB; b++) {
+      if (b >= g.B) break;
       float y0 = yrow[b * MAX_ROWS + i], y1 = yrow[b * MAX_ROWS + i + 1];
       const int P = c.pos[b];
       if (hs <= HPG) {  // q heads and k: rotate (t, t + D/2) by P * theta^(-2t/D)
-        const float2 cs = ((const float2*)g.rope)[(size_t)P * (D / 2) + t];
-        const float a = y0 * cs.x - y1 * cs.y;
-        const float bb = y0 * cs.y + y1 * cs.x;
+        const float a = y0 * cs[b].x - y1 * cs[b].y;
+        const float bb = y0 * cs[b].y + y1 * cs[b].x;
         y0 = a;
         y1 = bb;
       }
@@ -337,6 +397,7 @@ MK_DEV void op_qkv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
     }
   }
   consumer_bar();
+  return true;
 }
 
 // ------------------------------------------ OP_ATTN (split-KV partial) ----
@@ -350,11 +411,21 @@ MK_DEV void op_qkv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
 constexpr float NEG_BIG = -1e30f;
 
 template <int HT, int D, int HPG, int NB>
-MK_DEV void op_attn(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+MK_DEV bool op_attn(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   constexpr int LPR = D / 8, SPW = 32 / LPR;
   const int slot = c.lane / LPR, dsl = c.lane % LPR;
   const int b = I.b, P = c.pos[b];
   const LayerPtrs& Lp = g.layers[I.layer];
+  const bool last = I.r0 + 1 == I.r1 && c.warp == 0;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  if (!dep_wait(c, g, I)) return false;
+  // row P (appended by this step's QKV) is fetched together with q
+  uint4 kP = zero, vP = zero;
+  if (last && slot == 0) {
+    const size_t off = (((size_t)b * g.Hkv + I.g) * g.max_seq + (size_t)P) * D + dsl * 8;
+    kP = __ldcg((const uint4*)(Lp.kc + off));
+    vP = __ldcg((const uint4*)(Lp.vc + off));
+  }
   constexpr float QS = (D == 64 ? 0.125f : 0.08838834764831845f) * 1.4426950408889634f;
   float q[HPG][8], m[HPG], l[HPG], o[HPG][8];
 #pragma unroll
@@ -400,7 +471,6 @@ MK_DEV void op_attn(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   };
   Seg s[2];
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
-  const uint4 zero = make_uint4(0, 0, 0, 0);
   for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
     const uint32_t n = min(s[0].ups, s[0].n - u0);
     if (!c.ring.acquire(g)) break;
@@ -415,13 +485,7 @@ MK_DEV void op_attn(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
     }
     c.ring.release(c.lane);
   }
-  if (I.r0 + 1 == I.r1 && c.warp == 0) {  // row P, appended by this step's QKV
-    const size_t off = (((size_t)b * g.Hkv + I.g) * g.max_seq + (size_t)P) * D + dsl * 8;
-    const bool valid = slot == 0;
-    const uint4 kw = valid ? __ldcg((const uint4*)(Lp.kc + off)) : zero;
-    const uint4 vw = valid ? __ldcg((const uint4*)(Lp.vc + off)) : zero;
-    process(kw, vw, valid);
-  }
+  if (last) process(kP, vP, slot == 0);
   // merge the slots of the warp
 #pragma unroll
   for (int off = LPR; off < 32; off <<= 1) {
@@ -476,6 +540,7 @@ MK_DEV void op_attn(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
     }
   }
   consumer_bar();
+  return true;
 }
 
 // Residual input x_j[b][r] (j = 0: the embedding row of the token).
@@ -490,39 +555,53 @@ MK_DEV float x_in(const Globals& g, int j, const int* tok, int b, int r) {
 // (packed [Hq][H][D]) are applied and accumulated into x_{2l+1} with float
 // atomics; the head-0 instructions also add the residual x_{2l}.
 template <int HT, int D, int HPG, int NB>
-MK_DEV void op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   constexpr int LPR = D / 8, SPW = 32 / LPR;
+  constexpr int SG = (NCT / (NB * D)) > 0 ? NCT / (NB * D) : 1;  // slice groups per (b, dim)
   const int slot = c.lane / LPR, dsl = c.lane % LPR;
   const int h = I.g, l = I.layer;
   const int S = g.splits;
-  // (m, l) of every slice of every sequence in one parallel round trip ...
-  float* sm_m = c.yrow;
-  float* sm_l = c.yrow + NB * S;
-  for (int t = c.tid; t < g.B * S; t += NCT) {
-    const int b = t / S, s = t % S;
-    const float* p = g.part + ((((size_t)l * g.B + b) * g.Hq + h) * S + s) * (D + 2) + D;
-    sm_m[t] = __ldcg(p);
-    sm_l[t] = __ldcg(p + 1);
+  if (!dep_wait(c, g, I)) return false;
+  // Work item (b, dim, sg) merges slices sg, sg + SG, ... -- all its loads
+  // are independent, so the whole combine costs about one L2 round trip.
+  float* pm = c.yrow;                    // [NB][SG][D] partial max
+  float* pl = pm + NB * SG * D;          // partial sum
+  float* po = pl + NB * SG * D;          // partial o
+  for (int it = c.tid; it < NB * SG * D; it += NCT) {
+    const int dim = it % D, sg = (it / D) % SG, b = it / (D * SG);
+    float M = NEG_BIG, Ls = 0.f, O = 0.f;
+    if (b < g.B) {
+      const float* base = g.part + (((size_t)l * g.B + b) * g.Hq + h) * S * (D + 2);
+#pragma unroll 4
+      for (int s = sg; s < S; s += SG) {
+        const float* p = base + (size_t)s * (D + 2);
+        const float ms = __ldcg(p + D), ls = __ldcg(p + D + 1), os = __ldcg(p + dim);
+        const float mn = fmaxf(M, ms);
+        const float fa = exp2f(M - mn), fb = exp2f(ms - mn);
+        Ls = Ls * fa + ls * fb;
+        O = O * fa + os * fb;
+        M = mn;
+      }
+    }
+    pm[it] = M;
+    pl[it] = Ls;
+    po[it] = O;
   }
   consumer_bar();
-  // ... then o[dim] of every slice, eight loads in flight per thread
-  for (int t = c.tid; t < NB * D; t += NCT) {
-    const int b = t / D, dim = t % D;
-    if (b < g.B) {
-      const float* base = g.part + (((size_t)l * g.B + b) * g.Hq + h) * S * (D + 2) + dim;
-      const float* mb = sm_m + b * S;
-      const float* lb = sm_l + b * S;
-      float M = NEG_BIG;
-      for (int s = 0; s < S; s++) M = fmaxf(M, mb[s]);
-      float Ls = 0.f, O = 0.f;
-#pragma unroll 8
-      for (int s = 0; s < S; s++) {
-        const float f = exp2f(mb[s] - M);
-        Ls = fmaf(lb[s], f, Ls);
-        O = fmaf(__ldcg(base + (size_t)s * (D + 2)), f, O);
-      }
-      c.attn[b * D + dim] = O / Ls;
+  for (int it = c.tid; it < NB * D; it += NCT) {
+    const int b = it / D, dim = it % D;
+    float M = NEG_BIG;
+#pragma unroll
+    for (int sg = 0; sg < SG; sg++) M = fmaxf(M, pm[(b * SG + sg) * D + dim]);
+    float Ls = 0.f, O = 0.f;
+#pragma unroll
+    for (int sg = 0; sg < SG; sg++) {
+      const int k = (b * SG + sg) * D + dim;
+      const float f = exp2f(pm[k] - M);
+      Ls = fmaf(pl[k], f, Ls);
+      O = fmaf(po[k], f, O);
     }
+    c.attn[b * D + dim] = b < g.B ? O / Ls : 0.f;
   }
   consumer_bar();
   float a[NB][8];
@@ -567,13 +646,17 @@ MK_DEV void op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
     c.ring.release(c.lane);
   }
   consumer_bar();
+  return true;
 }
 
 // ------------------------------------------------- OP_ROUTER (MoE only) ----
 template <int HT, int D, int HPG, int NB>
-MK_DEV void op_router(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+MK_DEV bool op_router(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   const LayerPtrs& Lp = g.layers[I.layer];
-  norm_into_xn(c, g, 2 * I.layer + 1, Lp.mlp_norm);
+  NormGain<HT> ng;
+  norm_gain(ng, Lp.mlp_norm, c.tid);
+  if (!dep_wait(c, g, I)) return false;
+  norm_apply(c, g, 2 * I.layer + 1, ng);
   float xr[HT / 32];
   if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
   Seg s[2];
@@ -586,6 +669,7 @@ MK_DEV void op_router(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
       for (int b = 0; b < B && b < NB; b++) rl[(size_t)b * E + r] = acc[b];
   });
   consumer_bar();
+  return true;
 }
 
 // ---------------------------------------- OP_MLP (one FFN column slice) ----
@@ -595,11 +679,15 @@ MK_DEV void op_router(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
 // for its residual rows.  MoE: routed slices scale h by the slot's router
 // weight and read expert topk[slot]'s rows; shared slices use weight 1.
 template <int HT, int D, int HPG, int NB>
-MK_DEV void op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   const int l = I.layer;
   const LayerPtrs& Lp = g.layers[l];
   const bool routed = g.E > 0 && !(I.flags & F_SHARED);
-  if (!(I.flags & F_NORM_CACHED)) norm_into_xn(c, g, 2 * l + 1, Lp.mlp_norm);
+  const bool cached = (I.flags & F_NORM_CACHED) != 0;
+  NormGain<HT> ng;
+  if (!cached) norm_gain(ng, Lp.mlp_norm, c.tid);
+  if (!dep_wait(c, g, I)) return false;
+  if (!cached) norm_apply(c, g, 2 * l + 1, ng);
   if (routed) {
     if (c.warp == 0) route_topk(g.rlog + (size_t)l * g.B * g.E, g.E, g.K, c.lane, c.topk, c.topw);
     consumer_bar();
@@ -677,14 +765,18 @@ MK_DEV void op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
     }
   }
   consumer_bar();
+  return true;
 }
 
 // ------------------------------------ OP_LMHEAD (final norm + head rows) ----
 // Logits rows [r0, r1) and this slice's (max, first index); the slice that
 // arrives last on the argmax counter reduces all slices into argmax[b].
 template <int HT, int D, int HPG, int NB>
-MK_DEV void op_lmhead(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
-  norm_into_xn(c, g, 2 * g.L, g.final_norm);
+MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+  NormGain<HT> ng;
+  norm_gain(ng, g.final_norm, c.tid);
+  if (!dep_wait(c, g, I)) return false;
+  norm_apply(c, g, 2 * g.L, ng);
   float xr[HT / 32];
   if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
   Seg s[2];
@@ -724,7 +816,7 @@ MK_DEV void op_lmhead(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
     }
   }
   consumer_bar();
-  if (c.warp != 0) return;
+  if (c.warp != 0) return true;
   if (lane == 0) {
     for (int b = 0; b < B && b < NB; b++) {
       float v = -INFINITY;
@@ -745,7 +837,7 @@ MK_DEV void op_lmhead(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   if (lane == 0) old = atom_add_acq_rel(g.ctr + g.lm_ctr, 1u);
   old = __shfl_sync(0xFFFFFFFFu, old, 0);
   __syncwarp();
-  if (old != g.epoch * (uint32_t)g.n_lm - 1u) return;
+  if (old != g.epoch * (uint32_t)g.n_lm - 1u) return true;
   for (int b = 0; b < B && b < NB; b++) {
     float v = -INFINITY;
     int ix = 0x7FFFFFFF;
@@ -768,6 +860,7 @@ MK_DEV void op_lmhead(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
     }
     if (lane == 0) g.argmax[b] = ix;
   }
+  return true;
 }
 
 // ------------------------------------------------------------ interpreter ----
@@ -1012,6 +1105,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
   c.tid = tid;
   c.warp = warp;
   c.lane = lane;
+  c.flag = flag;
+  c.tw0 = c.tw1 = 0;
   consumer_bar();  // everyone has read *flag before it is reused below
 
   Instr next = load_instr(g, blockIdx.x, 0);
@@ -1021,34 +1116,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
     if (pc + 1 < g.max_pc) next = load_instr(g, blockIdx.x, pc + 1);
     if (I.op == OP_NOP || !selected(g, I)) continue;
     c.pc = pc;
-    unsigned long long tw0 = 0, tw1 = 0;
-    if (tid == 0) {
-      if (g.trace) tw0 = gtimer();
-      bool ok = true;
-      if (I.wait_ctr != NO_CTR) ok = wait_counter(g, I.wait_ctr, g.epoch * I.wait_cnt, pc, I.op);
-      if (ok && peek_err(g)) ok = false;
-      *flag = ok ? 0 : 1;
-      if (g.trace) tw1 = gtimer();
-    }
-    consumer_bar();
-    if (*flag) return;
+    bool ok;
     switch (I.op) {
-      case OP_QKV: op_qkv(c, g, I); break;
-      case OP_ATTN: op_attn(c, g, I); break;
-      case OP_OPROJ: op_oproj(c, g, I); break;
-      case OP_ROUTER: op_router(c, g, I); break;
-      case OP_MLP: op_mlp(c, g, I); break;
-      case OP_LMHEAD: op_lmhead(c, g, I); break;
+      case OP_QKV: ok = op_qkv(c, g, I); break;
+      case OP_ATTN: ok = op_attn(c, g, I); break;
+      case OP_OPROJ: ok = op_oproj(c, g, I); break;
+      case OP_ROUTER: ok = op_router(c, g, I); break;
+      case OP_MLP: ok = op_mlp(c, g, I); break;
+      case OP_LMHEAD: ok = op_lmhead(c, g, I); break;
       default:
         if (tid == 0) set_err(g, MK_ERR_DEVICE, pc, I.op);
-        consumer_bar();
+        ok = false;
         break;
     }
+    if (!ok) return;
     if (tid == 0) {
       if (g.trace) {
         unsigned long long* t = g.trace + ((size_t)blockIdx.x * g.max_pc + pc) * 4;
-        t[1] = tw0;
-        t[2] = tw1;
+        t[1] = c.tw0;
+        t[2] = c.tw1;
         t[3] = gtimer();
       }
       if (I.sig_ctr != NO_CTR) red_release(g.ctr + I.sig_ctr, 1u);

@@ -80,10 +80,21 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
 
   int n_lm = 0;
   for (int l = 0; l < L; l++) {
-    // ---- QKV rows
+    // ---- QKV rows: with at least one SM per kv head, every SM works inside
+    // one group (so no SM runs two pieces); otherwise contiguous ranges.
     for (int i = 0; i < n_sm; i++) {
-      long a = cut(R, n_sm, i, 2), b = cut(R, n_sm, i + 1, 2);
-      if (i == n_sm - 1) b = R;
+      long a, b;
+      if (n_sm >= Hkv) {
+        const int g = (int)((long)i * Hkv / n_sm);
+        const long s0 = ((long)g * n_sm + Hkv - 1) / Hkv;   // first SM of group g
+        const long s1 = ((long)(g + 1) * n_sm + Hkv - 1) / Hkv;
+        const int m = (int)(s1 - s0), k = (int)(i - s0);
+        a = (long)g * GR + cut(GR, m, k, 2);
+        b = (long)g * GR + (k == m - 1 ? GR : cut(GR, m, k + 1, 2));
+      } else {
+        a = cut(R, n_sm, i, 2);
+        b = (i == n_sm - 1) ? R : cut(R, n_sm, i + 1, 2);
+      }
       bool first = true;
       while (a < b) {
         long g = a / GR;
@@ -115,10 +126,22 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
       qs[sm].push_back(I);
       bytes[sm] += (double)max_ctx / S * D * 4;
     }
-    // ---- O-projection: (head, row) space split into n_sm ranges
+    // ---- O-projection: with at least one SM per query head every SM takes
+    // rows of a single head; otherwise the (head, row) space is cut evenly.
     const long OR = (long)Hq * H;
     for (int i = 0; i < n_sm; i++) {
-      long a = cut(OR, n_sm, i, 1), b = (i == n_sm - 1) ? OR : cut(OR, n_sm, i + 1, 1);
+      long a, b;
+      if (n_sm >= Hq) {
+        const int h = (int)((long)i * Hq / n_sm);
+        const long s0 = ((long)h * n_sm + Hq - 1) / Hq;
+        const long s1 = ((long)(h + 1) * n_sm + Hq - 1) / Hq;
+        const int m = (int)(s1 - s0), k = (int)(i - s0);
+        a = (long)h * H + cut(H, m, k, 1);
+        b = (long)h * H + (k == m - 1 ? H : cut(H, m, k + 1, 1));
+      } else {
+        a = cut(OR, n_sm, i, 1);
+        b = (i == n_sm - 1) ? OR : cut(OR, n_sm, i + 1, 1);
+      }
       while (a < b) {
         long h = a / H;
         long e = std::min(b, (h + 1) * H);

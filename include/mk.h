@@ -158,7 +158,7 @@ int mk_set_wait_timeout(mk_handle* h, uint64_t ns);
 
 /* How far (bytes of each SM's own weight / KV stream) the kernel warms L2
  * ahead of its shared-memory ring with cp.async.bulk.prefetch.L2; 0 turns
- * the L2 lookahead off.  Default 512 KiB.  A performance knob only: results
+ * the L2 lookahead off (the default).  A performance knob only: results
  * do not depend on it.                                                     */
 int mk_set_l2_prefetch(mk_handle* h, uint64_t bytes_ahead);
 
