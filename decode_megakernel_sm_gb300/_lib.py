@@ -183,9 +183,9 @@ def mk_set_trace(h, on: bool):
 
 
 def mk_get_trace(h, n_sm: int, max_pc: int):
-    """Returns a numpy uint64 array [n_sm][max_pc][4] of %globaltimer stamps."""
+    """Returns a numpy uint64 array [n_sm][max_pc][8] of %globaltimer stamps."""
     import numpy as np
-    out = np.zeros((n_sm, max_pc, 4), np.uint64)
+    out = np.zeros((n_sm, max_pc, 8), np.uint64)
     _check(lib().mk_get_trace(h, out.ctypes.data_as(C.POINTER(C.c_uint64)), out.size),
            "mk_get_trace")
     return out

@@ -60,7 +60,7 @@ struct mk_handle {
   int32_t *d_tok = nullptr, *d_pos = nullptr, *d_am = nullptr;
   float* d_logits = nullptr;
   int* h_err = nullptr;  // pinned [4]
-  unsigned long long* trace = nullptr;  // [n_sm][max_pc][4] when tracing is on
+  unsigned long long* trace = nullptr;  // [n_sm][max_pc][8] when tracing is on
   // graph-mode ablation cache
   std::map<std::tuple<const void*, const void*, const void*, const void*, const void*>,
            cudaGraphExec_t>
@@ -620,7 +620,7 @@ extern "C" int mk_set_trace(mk_handle* h, int on) {
     return MK_OK;
   }
   if (!h->trace) {
-    const size_t n = (size_t)h->n_sm * h->plan.max_pc * 4;
+    const size_t n = (size_t)h->n_sm * h->plan.max_pc * 8;
     CK(cudaMalloc(&h->trace, n * sizeof(unsigned long long)));
     CK(cudaMemset(h->trace, 0, n * sizeof(unsigned long long)));
   }
@@ -630,7 +630,7 @@ extern "C" int mk_set_trace(mk_handle* h, int on) {
 extern "C" int mk_get_trace(mk_handle* h, uint64_t* out, size_t n) {
   if (!h || !out) return MK_ERR_INVALID_ARG;
   if (!h->trace) return MK_ERR_NOT_READY;
-  const size_t need = (size_t)h->n_sm * h->plan.max_pc * 4;
+  const size_t need = (size_t)h->n_sm * h->plan.max_pc * 8;
   if (n < need) return MK_ERR_INVALID_ARG;
   CK(cudaDeviceSynchronize());
   CK(cudaMemcpy(out, h->trace, need * sizeof(uint64_t), cudaMemcpyDeviceToHost));

@@ -36,6 +36,10 @@ struct Ctx {
   int tid, warp, lane;
   int pc;
   unsigned long long tw0, tw1;  // trace: wait start / end (thread 0)
+  unsigned long long tm[2];     // trace: after the prologue phase, after the ring loop
+  MK_DEV void mark(const Globals& g, int k) {
+    if (g.trace && tid == 0) tm[k] = gtimer();
+  }
 };
 
 // The dependency wait of one instruction: thread 0 spins on the counter,
@@ -359,6 +363,7 @@ MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   }
   if (!dep_wait(c, g, I)) return false;
   if (!cached) norm_apply(c, g, 2 * I.layer, ng);
+  c.mark(g, 0);
   float xr[HT / 32];
   if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
   Seg s[2];
@@ -371,6 +376,7 @@ MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
       for (int b = 0; b < NB; b++) yrow[b * MAX_ROWS + r] = acc[b];
     }
   });
+  c.mark(g, 1);
   consumer_bar();
   if (i < n) {
 #pragma unroll
@@ -469,6 +475,7 @@ MK_DEV bool op_attn(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
       }
     }
   };
+  c.mark(g, 0);
   Seg s[2];
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
   for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
@@ -486,6 +493,7 @@ MK_DEV bool op_attn(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
     c.ring.release(c.lane);
   }
   if (last) process(kP, vP, slot == 0);
+  c.mark(g, 1);
   // merge the slots of the warp
 #pragma unroll
   for (int off = LPR; off < 32; off <<= 1) {
@@ -603,6 +611,7 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
     }
     c.attn[b * D + dim] = b < g.B ? O / Ls : 0.f;
   }
+  c.mark(g, 0);
   consumer_bar();
   float a[NB][8];
 #pragma unroll
@@ -645,6 +654,7 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
     }
     c.ring.release(c.lane);
   }
+  c.mark(g, 1);
   consumer_bar();
   return true;
 }
@@ -688,6 +698,7 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   if (!cached) norm_gain(ng, Lp.mlp_norm, c.tid);
   if (!dep_wait(c, g, I)) return false;
   if (!cached) norm_apply(c, g, 2 * l + 1, ng);
+  c.mark(g, 0);
   if (routed) {
     if (c.warp == 0) route_topk(g.rlog + (size_t)l * g.B * g.E, g.E, g.K, c.lane, c.topk, c.topw);
     consumer_bar();
@@ -745,6 +756,7 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
     }
     c.ring.release(c.lane);
   }
+  c.mark(g, 1);
   const int rs0 = (int)(I.aux & 0xFFFFu), rs1 = (int)(I.aux >> 16);
 #pragma unroll
   for (int q = 0; q < GPT; q++) {
@@ -777,6 +789,7 @@ MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   norm_gain(ng, g.final_norm, c.tid);
   if (!dep_wait(c, g, I)) return false;
   norm_apply(c, g, 2 * g.L, ng);
+  c.mark(g, 0);
   float xr[HT / 32];
   if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
   Seg s[2];
@@ -880,10 +893,12 @@ MK_DEV bool selected(const Globals& g, const Instr& I) {
 }
 
 // Second cursor of the producer: walks the same chunk sequence as the ring
-// cursor and warms L2 with each chunk (cp.async.bulk.prefetch.L2) once the
-// ring cursor is within l2_ahead bytes of it.  While the consumers wait on a
-// dependency and the ring is full, HBM keeps streaming the SM's upcoming
-// weights into L2; the ring then refills from L2.  Lane 0 only.
+// cursor and warms L2 with each chunk once the ring cursor is within
+// l2_ahead bytes of it.  While the consumers wait on a dependency and the
+// ring is full, HBM keeps streaming the SM's upcoming weights into L2; the
+// ring then refills from L2.  The prefetches are per-line LSU prefetches
+// spread over the producer warp's 32 lanes (the TMA engine stays free for
+// the ring copies); every lane runs the cursor in lockstep.
 template <int HT, int D, int NB>
 struct L2Cursor {
   int pc = 0, k = 0, nseg = 0;
@@ -936,8 +951,11 @@ struct L2Cursor {
       }
       const uint32_t n = min(s[k].ups, s[k].n - u0);
       const uint32_t b = n * s[k].unit;
-      bulk_prefetch_l2(s[k].src + (size_t)u0 * s[k].unit, b);
-      if (s[k].src2) bulk_prefetch_l2(s[k].src2 + (size_t)u0 * s[k].unit, b);
+      const int lane = threadIdx.x & 31;
+      for (uint32_t off = (uint32_t)lane * 128u; off < b; off += 32u * 128u) {
+        prefetch_l2_line(s[k].src + (size_t)u0 * s[k].unit + off);
+        if (s[k].src2) prefetch_l2_line(s[k].src2 + (size_t)u0 * s[k].unit + off);
+      }
       bytes += s[k].src2 ? 2ull * b : b;
       u0 += n;
     }
@@ -963,7 +981,7 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
   int routed_layer = -1;
   unsigned long long issued_bytes = 0;
   L2Cursor<HT, D, NB> l2;
-  if (lane == 0 && g.l2_ahead) l2.run(g, g.l2_ahead, ptopk, routed_layer);
+  if (g.l2_ahead) l2.run(g, g.l2_ahead, ptopk, routed_layer);
   for (int pc = 0; pc < g.max_pc; pc++) {
     const Instr I = load_instr(g, blockIdx.x, pc);
     if (I.op == OP_HALT) break;
@@ -991,7 +1009,7 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
       route_topk(g.rlog + (size_t)I.layer * g.B * g.E, g.E, g.K, lane, ptopk, ptopw);
       routed_layer = I.layer;
       __syncwarp();
-      if (lane == 0 && g.l2_ahead) l2.run(g, issued_bytes + g.l2_ahead, ptopk, routed_layer);
+      if (g.l2_ahead) l2.run(g, issued_bytes + g.l2_ahead, ptopk, routed_layer);
     }
     __syncwarp();
     Seg s[2];
@@ -1004,7 +1022,7 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
         if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) goto drain;
         if (lane == 0) {
           if (g.trace && k == 0 && u0 == 0)
-            g.trace[((size_t)blockIdx.x * g.max_pc + pc) * 4] = gtimer();
+            g.trace[((size_t)blockIdx.x * g.max_pc + pc) * 8] = gtimer();
           const uint32_t bytes = n * s[k].unit;
           const uint32_t full = full0 + 8u * st;
           const uint32_t dst = ring_s + (uint32_t)st * STAGE_BYTES;
@@ -1016,9 +1034,9 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
           } else {
             bulk_g2s(dst, s[k].src + (size_t)u0 * s[k].unit, bytes, full, pol_w);
           }
-          issued_bytes += s[k].src2 ? 2ull * bytes : bytes;
-          if (g.l2_ahead) l2.run(g, issued_bytes + g.l2_ahead, ptopk, routed_layer);
         }
+        issued_bytes += (s[k].src2 ? 2ull : 1ull) * n * s[k].unit;
+        if (g.l2_ahead) l2.run(g, issued_bytes + g.l2_ahead, ptopk, routed_layer);
         __syncwarp();
         issued++;
         if (++st == ns) {
@@ -1107,6 +1125,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
   c.lane = lane;
   c.flag = flag;
   c.tw0 = c.tw1 = 0;
+  c.tm[0] = c.tm[1] = 0;
   consumer_bar();  // everyone has read *flag before it is reused below
 
   Instr next = load_instr(g, blockIdx.x, 0);
@@ -1132,10 +1151,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
     if (!ok) return;
     if (tid == 0) {
       if (g.trace) {
-        unsigned long long* t = g.trace + ((size_t)blockIdx.x * g.max_pc + pc) * 4;
+        unsigned long long* t = g.trace + ((size_t)blockIdx.x * g.max_pc + pc) * 8;
         t[1] = c.tw0;
         t[2] = c.tw1;
-        t[3] = gtimer();
+        t[3] = c.tm[0];
+        t[4] = c.tm[1];
+        t[5] = gtimer();
       }
       if (I.sig_ctr != NO_CTR) red_release(g.ctr + I.sig_ctr, 1u);
     }

@@ -128,7 +128,7 @@ struct Globals {
   int sel_key;             // -1: run every instruction; else only key == sel_key (ablation)
   int zero_next;           // zero the other parity's residual buffers in this launch
   int pdl;                 // ablation with programmatic dependent launch
-  unsigned long long* trace;  // optional [n_sm][max_pc][4] %globaltimer stamps (NULL: off)
+  unsigned long long* trace;  // optional [n_sm][max_pc][8] %globaltimer stamps (NULL: off)
   unsigned long long l2_ahead;  // bytes of the SM's stream warmed in L2 ahead of the ring (0: off)
 };
 

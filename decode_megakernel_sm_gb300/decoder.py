@@ -90,7 +90,7 @@ class Decoder:
         L.mk_set_trace(self.h, on)
 
     def get_trace(self):
-        """(stamps [n_sm][max_pc][4], host copy of the queues) of the last traced launch."""
+        """(stamps [n_sm][max_pc][8], host copy of the queues) of the last traced launch."""
         info = self.info()
         tr = L.mk_get_trace(self.h, info["n_sm"], info["max_pc"])
         _, q = L.mk_plan(self.desc, info["batch"], info["max_ctx"], info["n_sm"])
