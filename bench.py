@@ -151,6 +151,12 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def _to_host(W):
+    return {k: (None if v is None else
+                [{n: t.cpu() for n, t in lw.items()} for lw in v] if k == "layers" else v.cpu())
+            for k, v in W.items()}
+
+
 def cpu_baseline(cfg, W, ks, vs, lengths, tokens, budget_s=20.0):
     """The oracle as it stands, on the host cores, on a bounded sample of decode
     steps of the same workload (at least one step)."""
@@ -251,6 +257,11 @@ def main():
     tokens0 = synth.make_tokens(cfg, args.seed)
     torch.cuda.synchronize()
     dec = Decoder(cfg, W, ks, vs)
+    # the library holds its own packed copy: keep only a host copy (for the CPU
+    # baseline) and free the device one
+    want_cpu = rank == 0 and ws == 1 and not args.no_cpu_baseline
+    W = _to_host(W) if want_cpu else None
+    torch.cuda.empty_cache()
     dec.build_schedule(B, cfg["max_seq"])
     if args.l2_ahead is not None:
         dec.set_l2_prefetch(args.l2_ahead)

@@ -611,6 +611,15 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
     }
     c.attn[b * D + dim] = b < g.B ? O / Ls : 0.f;
   }
+  const bool resid = (I.flags & F_RESIDUAL) != 0;
+  float* xr_s = c.xn;  // residual rows of this slice, [NB][nr] with nr <= H (head-0 slices)
+  if (resid) {
+    const int nr = (int)(I.r1 - I.r0);
+    for (int t = c.tid; t < NB * nr; t += NCT) {
+      const int b = t / nr, r = t % nr;
+      xr_s[t] = b < g.B ? x_in(g, 2 * l, c.tok, b, (int)I.r0 + r) : 0.f;
+    }
+  }
   c.mark(g, 0);
   consumer_bar();
   float a[NB][8];
@@ -618,10 +627,10 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   for (int b = 0; b < NB; b++)
 #pragma unroll
     for (int j = 0; j < 8; j++) a[b][j] = c.attn[b * D + dsl * 8 + j];
-  const bool resid = (I.flags & F_RESIDUAL) != 0;
   Seg s[2];
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
   const uint4 zero = make_uint4(0, 0, 0, 0);
+  const int nr = (int)(I.r1 - I.r0);
   for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
     const uint32_t n = min(s[0].ups, s[0].n - u0);
     if (!c.ring.acquire(g)) break;
@@ -647,7 +656,7 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
         const int r = (int)(I.r0 + u0 + j);
         for (int b = 0; b < g.B && b < NB; b++) {
           float v = y[b];
-          if (resid) v += x_in(g, 2 * l, c.tok, b, r);
+          if (resid) v += xr_s[b * nr + (r - (int)I.r0)];
           atomicAdd(xres(g, 2 * l + 1, b) + r, v);
         }
       }
@@ -893,12 +902,14 @@ MK_DEV bool selected(const Globals& g, const Instr& I) {
 }
 
 // Second cursor of the producer: walks the same chunk sequence as the ring
-// cursor and warms L2 with each chunk once the ring cursor is within
-// l2_ahead bytes of it.  While the consumers wait on a dependency and the
-// ring is full, HBM keeps streaming the SM's upcoming weights into L2; the
-// ring then refills from L2.  The prefetches are per-line LSU prefetches
-// spread over the producer warp's 32 lanes (the TMA engine stays free for
-// the ring copies); every lane runs the cursor in lockstep.
+// cursor.  Only while the ring is full (the consumers are waiting on a
+// dependency and the producer is blocked) does it warm L2 with the chunks
+// that lie up to l2_ahead bytes beyond the ring cursor, so that HBM keeps
+// streaming the SM's upcoming weights during the wait and the ring then
+// refills from L2; chunks the ring has already issued are skipped.  The
+// prefetches are per-line LSU prefetches spread over the producer warp's 32
+// lanes (the TMA engine stays free for the ring copies); every lane runs the
+// cursor in lockstep.
 template <int HT, int D, int NB>
 struct L2Cursor {
   int pc = 0, k = 0, nseg = 0;
@@ -907,8 +918,11 @@ struct L2Cursor {
   bool done = false;
   Seg s[2];
 
-  MK_DEV void run(const Globals& g, unsigned long long limit, const int* ptopk, int routed_layer) {
-    while (!done && bytes < limit) {
+  // Advance over chunks ending at or before `from` without prefetching, then
+  // prefetch at most `budget` chunks that start below `limit`.
+  MK_DEV void run(const Globals& g, unsigned long long limit, unsigned long long from,
+                  const int* ptopk, int routed_layer, int budget) {
+    while (!done && bytes < limit && budget > 0) {
       if (k >= nseg) {
         if (pc >= g.max_pc) {
           done = true;
@@ -951,12 +965,16 @@ struct L2Cursor {
       }
       const uint32_t n = min(s[k].ups, s[k].n - u0);
       const uint32_t b = n * s[k].unit;
-      const int lane = threadIdx.x & 31;
-      for (uint32_t off = (uint32_t)lane * 128u; off < b; off += 32u * 128u) {
-        prefetch_l2_line(s[k].src + (size_t)u0 * s[k].unit + off);
-        if (s[k].src2) prefetch_l2_line(s[k].src2 + (size_t)u0 * s[k].unit + off);
+      const unsigned long long cb = s[k].src2 ? 2ull * b : b;
+      if (bytes + cb > from) {
+        const int lane = threadIdx.x & 31;
+        for (uint32_t off = (uint32_t)lane * 128u; off < b; off += 32u * 128u) {
+          prefetch_l2_line(s[k].src + (size_t)u0 * s[k].unit + off);
+          if (s[k].src2) prefetch_l2_line(s[k].src2 + (size_t)u0 * s[k].unit + off);
+        }
+        budget--;
       }
-      bytes += s[k].src2 ? 2ull * b : b;
+      bytes += cb;
       u0 += n;
     }
   }
@@ -981,7 +999,6 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
   int routed_layer = -1;
   unsigned long long issued_bytes = 0;
   L2Cursor<HT, D, NB> l2;
-  if (g.l2_ahead) l2.run(g, g.l2_ahead, ptopk, routed_layer);
   for (int pc = 0; pc < g.max_pc; pc++) {
     const Instr I = load_instr(g, blockIdx.x, pc);
     if (I.op == OP_HALT) break;
@@ -1008,8 +1025,6 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
       __syncwarp();
       route_topk(g.rlog + (size_t)I.layer * g.B * g.E, g.E, g.K, lane, ptopk, ptopw);
       routed_layer = I.layer;
-      __syncwarp();
-      if (g.l2_ahead) l2.run(g, issued_bytes + g.l2_ahead, ptopk, routed_layer);
     }
     __syncwarp();
     Seg s[2];
@@ -1017,9 +1032,28 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
     for (int k = 0; k < nseg; k++) {
       for (uint32_t u0 = 0; u0 < s[k].n; u0 += s[k].ups) {
         const uint32_t n = min(s[k].ups, s[k].n - u0);
-        bool ok = true;
-        if (lane == 0) ok = wait_mbar(g, empty0 + 8u * st, par ^ 1u, true);
-        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) goto drain;
+        // wait for a free stage; while the ring is full, warm L2 ahead
+        const uint32_t empty = empty0 + 8u * st;
+        if (!__shfl_sync(0xFFFFFFFFu, mbar_try(empty, par ^ 1u), 0)) {
+          const uint64_t t0 = gtimer();
+          for (uint32_t it = 1;; it++) {
+            if (g.l2_ahead)
+              l2.run(g, issued_bytes + g.l2_ahead, issued_bytes, ptopk, routed_layer, 1);
+            if (__shfl_sync(0xFFFFFFFFu, mbar_try(empty, par ^ 1u), 0)) break;
+            if ((it & 63) == 0) {
+              int bad = 0;
+              if (lane == 0) {
+                if (peek_err(g)) {
+                  bad = 1;
+                } else if (gtimer() - t0 > g.timeout_ns) {
+                  set_err(g, MK_ERR_TIMEOUT, pc, I.op);
+                  bad = 1;
+                }
+              }
+              if (__shfl_sync(0xFFFFFFFFu, bad, 0)) goto drain;
+            }
+          }
+        }
         if (lane == 0) {
           if (g.trace && k == 0 && u0 == 0)
             g.trace[((size_t)blockIdx.x * g.max_pc + pc) * 8] = gtimer();
@@ -1036,7 +1070,6 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
           }
         }
         issued_bytes += (s[k].src2 ? 2ull : 1ull) * n * s[k].unit;
-        if (g.l2_ahead) l2.run(g, issued_bytes + g.l2_ahead, ptopk, routed_layer);
         __syncwarp();
         issued++;
         if (++st == ns) {

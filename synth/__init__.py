@@ -38,6 +38,13 @@ CONFIGS = {
         name="llama1b_b8", n_layers=16, hidden=2048, n_q_heads=32, n_kv_heads=8, head_dim=64,
         ffn=8192, vocab=128256, rms_eps=1e-5, rope_theta=5e5, tied=True, n_experts=0, top_k=0,
         expert_ffn=0, shared_ffn=0, batch=8, prefill=(512, 2048), steps=64),
+    # A small case of the same kernel for detailed profiler captures: four
+    # layers of the Llama-1B shape and a 32000-row head (about 620 MB of bf16
+    # weights, well above the 129 MB L2).
+    "llama1b_4l": dict(
+        name="llama1b_4l", n_layers=4, hidden=2048, n_q_heads=32, n_kv_heads=8, head_dim=64,
+        ffn=8192, vocab=32000, rms_eps=1e-5, rope_theta=5e5, tied=True, n_experts=0, top_k=0,
+        expert_ffn=0, shared_ffn=0, batch=1, prefill=(1024, 1024), steps=128),
     "moe": dict(
         name="moe", n_layers=24, hidden=2048, n_q_heads=16, n_kv_heads=4, head_dim=128, ffn=0,
         vocab=65536, rms_eps=1e-5, rope_theta=5e5, tied=False, n_experts=128, top_k=8,
