@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--l2-ahead", type=int, default=None,
                     help="bytes each SM warms in L2 ahead of its ring (library default if unset)")
+    ap.add_argument("--kc", type=int, default=None,
+                    help="partial copies of each residual vector (library default if unset)")
     ap.add_argument("--trace", default=None,
                     help="write a per-instruction timeline of 3 traced steps to this path")
     return ap.parse_args()
@@ -262,6 +264,8 @@ def main():
     want_cpu = rank == 0 and ws == 1 and not args.no_cpu_baseline
     W = _to_host(W) if want_cpu else None
     torch.cuda.empty_cache()
+    if args.kc is not None:
+        dec.set_residual_copies(args.kc)
     dec.build_schedule(B, cfg["max_seq"])
     if args.l2_ahead is not None:
         dec.set_l2_prefetch(args.l2_ahead)

@@ -89,6 +89,7 @@ SIGNATURES = {
     "mk_debug_drop_instruction": (C.c_int, [C.c_void_p, C.c_int, C.c_int]),
     "mk_set_trace": (C.c_int, [C.c_void_p, C.c_int]),
     "mk_set_l2_prefetch": (C.c_int, [C.c_void_p, C.c_uint64]),
+    "mk_set_residual_copies": (C.c_int, [C.c_void_p, C.c_int]),
     "mk_get_trace": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.c_size_t]),
     "mk_destroy": (C.c_int, [C.c_void_p]),
     "mk_status_string": (C.c_char_p, [C.c_int]),
@@ -176,6 +177,10 @@ def mk_debug_drop_instruction(h, sm: int, pc: int):
 
 def mk_set_l2_prefetch(h, bytes_ahead: int):
     _check(lib().mk_set_l2_prefetch(h, int(bytes_ahead)), "mk_set_l2_prefetch")
+
+
+def mk_set_residual_copies(h, copies: int):
+    _check(lib().mk_set_residual_copies(h, int(copies)), "mk_set_residual_copies")
 
 
 def mk_set_trace(h, on: bool):

@@ -55,6 +55,7 @@ struct mk_handle {
   uint32_t epoch = 0;
   unsigned long long timeout_ns = 2000000000ull;
   unsigned long long l2_ahead = 0;
+  int kc = 4;  // partial copies of each residual vector
   // host-buffer step
   cudaStream_t own = nullptr;
   int32_t *d_tok = nullptr, *d_pos = nullptr, *d_am = nullptr;
@@ -323,7 +324,7 @@ extern "C" int mk_build_schedule(mk_handle* h, int batch, int max_ctx) {
   const mk_model_desc& d = h->d;
   const size_t L = d.n_layers, B = batch, H = d.hidden, Hq = d.n_q_heads, D = d.head_dim;
   const size_t E = d.n_experts > 0 ? d.n_experts : 1;
-  const size_t sx = al256(2 * 2 * L * B * H * 4), sq = al256(L * B * Hq * D * 4);
+  const size_t sx = al256(2 * 2 * L * (size_t)h->kc * B * H * 4), sq = al256(L * B * Hq * D * 4);
   const size_t sp = al256(L * B * Hq * (size_t)p.splits * (D + 2) * 4);
   const size_t sr = al256(L * B * E * 4), sl = al256((size_t)p.n_lm * B * 4);
   const size_t sc = al256((size_t)p.n_ctr * 4), se = 256;
@@ -409,6 +410,7 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.K = d.n_experts > 0 ? d.top_k : 0;
   g.Fe = d.expert_ffn;
   g.Fs = d.shared_ffn;
+  g.kc = h->kc;
   g.eps = d.rms_eps;
   g.lm_ctr = CtrMap{d.n_kv_heads, d.n_layers}.lm();
   g.n_lm = h->plan.n_lm;
@@ -576,6 +578,12 @@ extern "C" int mk_set_wait_timeout(mk_handle* h, uint64_t ns) {
   h->timeout_ns = ns;
   for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
   h->graphs.clear();
+  return MK_OK;
+}
+
+extern "C" int mk_set_residual_copies(mk_handle* h, int copies) {
+  if (!h || copies < 1 || copies > 8) return MK_ERR_INVALID_ARG;
+  h->kc = copies;
   return MK_OK;
 }
 

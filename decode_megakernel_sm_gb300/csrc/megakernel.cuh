@@ -59,9 +59,24 @@ MK_DEV bool dep_wait(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   return *c.flag == 0;
 }
 
-// Residual stream x_j, j in [1, 2L] (x_0 is the embedding row).
-MK_DEV float* xres(const Globals& g, int j, int b) {
-  return g.xbuf + (((size_t)g.parity * 2 * g.L + (size_t)(j - 1)) * g.B + b) * (size_t)g.H;
+// Residual stream x_j, j in [1, 2L] (x_0 is the embedding row), held as
+// g.kc partial copies that add up to x_j: an SM accumulates its atomics into
+// copy (SM index mod kc), which spreads the contention on each L2 line over
+// kc lines; readers sum the copies.
+MK_DEV float* xres(const Globals& g, int j, int b, int copy = 0) {
+  return g.xbuf +
+         ((((size_t)g.parity * 2 * g.L + (size_t)(j - 1)) * g.kc + copy) * g.B + b) * (size_t)g.H;
+}
+
+MK_DEV float* xres_mine(const Globals& g, int j, int b) {
+  return xres(g, j, b, (int)(blockIdx.x % (unsigned)g.kc));
+}
+
+// x_j[b][r], summed over the copies.
+MK_DEV float xres_sum(const Globals& g, int j, int b, int r) {
+  float v = 0.f;
+  for (int c = 0; c < g.kc; c++) v += __ldcg(xres(g, j, b, c) + r);
+  return v;
 }
 
 // The weight / cache byte ranges an instruction streams, in ring order.
@@ -205,10 +220,14 @@ MK_DEV void norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const No
           const uint4 w = __ldg((const uint4*)(g.embed + (size_t)c.tok[b] * HT) + gi);
           unpack8(w, v);
         } else {
-          const float4* p = (const float4*)xres(g, j, b) + 2 * gi;
-          const float4 a0 = __ldcg(p), a1 = __ldcg(p + 1);
-          v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
-          v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+#pragma unroll
+          for (int k = 0; k < 8; k++) v[k] = 0.f;
+          for (int cp = 0; cp < g.kc; cp++) {
+            const float4* p = (const float4*)xres(g, j, b, cp) + 2 * gi;
+            const float4 a0 = __ldcg(p), a1 = __ldcg(p + 1);
+            v[0] += a0.x; v[1] += a0.y; v[2] += a0.z; v[3] += a0.w;
+            v[4] += a1.x; v[5] += a1.y; v[6] += a1.z; v[7] += a1.w;
+          }
         }
       } else {
 #pragma unroll
@@ -318,7 +337,9 @@ MK_DEV bool gemv_rows(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s,
     const uint32_t n = min(s.ups, s.n - u0);
     if (!c.ring.acquire(g)) return false;
     const unsigned char* st = c.ring.stage_ptr();
-    for (uint32_t r = c.warp; r < n; r += NCW) {
+    // segment row u0 + r goes to warp (u0 + r) mod NCW, so a short segment
+    // spreads its rows over all warps rather than over one stage's worth
+    for (uint32_t r = (uint32_t)(c.warp + NCW - (int)(u0 % NCW)) % NCW; r < n; r += NCW) {
       float acc[NB];
       row_dot<HT, NB>(st + (size_t)r * HT * 2, xr, c.xn, c.lane, acc);
 #pragma unroll
@@ -554,7 +575,7 @@ MK_DEV bool op_attn(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
 // Residual input x_j[b][r] (j = 0: the embedding row of the token).
 MK_DEV float x_in(const Globals& g, int j, const int* tok, int b, int r) {
   if (j == 0) return bf1(g.embed[(size_t)tok[b] * g.H + r]);
-  return __ldcg(xres(g, j, b) + r);
+  return xres_sum(g, j, b, r);
 }
 
 // --------------------------------- OP_OPROJ (split reduce + O-proj rows) ----
@@ -657,7 +678,7 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
         for (int b = 0; b < g.B && b < NB; b++) {
           float v = y[b];
           if (resid) v += xr_s[b * nr + (r - (int)I.r0)];
-          atomicAdd(xres(g, 2 * l + 1, b) + r, v);
+          atomicAdd(xres_mine(g, 2 * l + 1, b) + r, v);
         }
       }
     }
@@ -777,9 +798,9 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
 #pragma unroll
         for (int e = 0; e < 8; e++) {
           v[e] = acc[q][b][e];
-          if (r0 + e >= rs0 && r0 + e < rs1) v[e] += __ldcg(xres(g, 2 * l + 1, b) + r0 + e);
+          if (r0 + e >= rs0 && r0 + e < rs1) v[e] += xres_sum(g, 2 * l + 1, b, r0 + e);
         }
-        float4* dst = (float4*)(xres(g, 2 * l + 2, b) + r0);
+        float4* dst = (float4*)(xres_mine(g, 2 * l + 2, b) + r0);
         atomicAdd(dst, make_float4(v[0], v[1], v[2], v[3]));
         atomicAdd(dst + 1, make_float4(v[4], v[5], v[6], v[7]));
       }
@@ -1130,7 +1151,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
     if (t < 0 || t >= g.V || p < 0 || p >= g.max_ctx) *flag = 1;
   }
   if (g.zero_next) {  // the residual buffers of the next step's parity
-    const size_t total = (size_t)2 * g.L * g.B * g.H;
+    const size_t total = (size_t)2 * g.L * g.kc * g.B * g.H;
     const size_t a = total * blockIdx.x / gridDim.x, e = total * (blockIdx.x + 1) / gridDim.x;
     float* nx = g.xbuf + (size_t)(g.parity ^ 1) * total;
     for (size_t i = a + tid; i < e; i += NCT) nx[i] = 0.f;

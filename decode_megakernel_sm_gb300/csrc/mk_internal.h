@@ -104,7 +104,7 @@ struct Globals {
   const uint16_t* lm_head;
   const uint16_t* final_norm;
   const float* rope;       // [max_seq][D/2][2] (cos, sin)
-  float* xbuf;             // [2][2L][B][H] residual stream, x_1 .. x_2L per parity
+  float* xbuf;             // [2][2L][kc][B][H] residual stream x_1 .. x_2L, kc partial copies
   float* qbuf;             // [L][B][Hq][D]
   float* part;             // [L][B][Hq][splits][D+2]: o[D], m, l  (log2 domain)
   float* rlog;             // [L][B][E] router logits
@@ -120,6 +120,7 @@ struct Globals {
   int max_pc, n_sm, n_stages;
   int B, H, Hq, Hkv, D, F, V, L, max_seq, max_ctx, splits;
   int E, K, Fe, Fs;
+  int kc;                  // partial copies of each residual vector (1..8)
   float eps;
   uint32_t epoch;          // step number (>= 1); counter targets are epoch * count
   int parity;              // epoch & 1: which residual buffer set this step uses

@@ -83,6 +83,10 @@ class Decoder:
     def set_wait_timeout(self, ns: int):
         L.mk_set_wait_timeout(self.h, int(ns))
 
+    def set_residual_copies(self, copies: int):
+        """Takes effect at the next build_schedule."""
+        L.mk_set_residual_copies(self.h, copies)
+
     def set_l2_prefetch(self, bytes_ahead: int):
         L.mk_set_l2_prefetch(self.h, bytes_ahead)
 
