@@ -55,7 +55,7 @@ struct mk_handle {
   uint32_t epoch = 0;
   unsigned long long timeout_ns = 2000000000ull;
   unsigned long long l2_ahead = 0;
-  int kc = 4;  // partial copies of each residual vector
+  int kc = 1;  // partial copies of each residual vector
   // host-buffer step
   cudaStream_t own = nullptr;
   int32_t *d_tok = nullptr, *d_pos = nullptr, *d_am = nullptr;

@@ -678,7 +678,7 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
         for (int b = 0; b < g.B && b < NB; b++) {
           float v = y[b];
           if (resid) v += xr_s[b * nr + (r - (int)I.r0)];
-          atomicAdd(xres_mine(g, 2 * l + 1, b) + r, v);
+          red_add_f32(xres_mine(g, 2 * l + 1, b) + r, v);
         }
       }
     }
@@ -800,9 +800,9 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
           v[e] = acc[q][b][e];
           if (r0 + e >= rs0 && r0 + e < rs1) v[e] += xres_sum(g, 2 * l + 1, b, r0 + e);
         }
-        float4* dst = (float4*)(xres_mine(g, 2 * l + 2, b) + r0);
-        atomicAdd(dst, make_float4(v[0], v[1], v[2], v[3]));
-        atomicAdd(dst + 1, make_float4(v[4], v[5], v[6], v[7]));
+        float* dst = xres_mine(g, 2 * l + 2, b) + r0;
+        red_add_v4f32(dst, v[0], v[1], v[2], v[3]);
+        red_add_v4f32(dst + 4, v[4], v[5], v[6], v[7]);
       }
     }
   }

@@ -162,7 +162,7 @@ int mk_set_wait_timeout(mk_handle* h, uint64_t ns);
  * do not depend on it.                                                     */
 int mk_set_l2_prefetch(mk_handle* h, uint64_t bytes_ahead);
 
-/* Number of partial copies (1..8, default 4) that each residual-stream
+/* Number of partial copies (1..8, default 1) that each residual-stream
  * vector is accumulated into: SM i adds its float atomics into copy
  * i mod copies and readers sum the copies, which spreads the atomic traffic
  * of the O-projection and MLP slices over more L2 lines.  Takes effect at
