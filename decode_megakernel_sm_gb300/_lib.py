@@ -18,6 +18,7 @@ MK_ERR_SCHEDULE = -4
 MK_ERR_TIMEOUT = -5
 MK_ERR_NOT_READY = -6
 MK_ERR_DEVICE = -7
+MK_ERR_SCRATCH = -8
 MK_ABL_STREAM, MK_ABL_GRAPH, MK_ABL_PDL = 0, 1, 2
 
 OP_NAMES = {0: "HALT", 1: "QKV", 2: "ATTN", 3: "OPROJ", 4: "MLP", 5: "LMHEAD", 6: "ROUTER",
@@ -83,6 +84,7 @@ SIGNATURES = {
     "mk_decode_step": (C.c_int, [C.c_void_p] * 6),
     "mk_decode_step_host": (C.c_int, [C.c_void_p] * 5),
     "mk_decode_step_ablation": (C.c_int, [C.c_void_p, C.c_int] + [C.c_void_p] * 5),
+    "mk_decode_step_noalloc": (C.c_int, [C.c_void_p] * 7),
     "mk_sync_status": (C.c_int, [C.c_void_p, C.c_void_p]),
     "mk_set_wait_timeout": (C.c_int, [C.c_void_p, C.c_uint64]),
     "mk_get_info": (C.c_int, [C.c_void_p, C.POINTER(mk_info)]),
@@ -155,6 +157,14 @@ def mk_decode_step_host(h, h_tokens, h_positions, h_logits, h_argmax) -> int:
 def mk_decode_step_ablation(h, mode, d_tokens, d_positions, d_logits, d_argmax, stream=None):
     _check(lib().mk_decode_step_ablation(h, mode, d_tokens, d_positions, d_logits, d_argmax,
                                          stream), "mk_decode_step_ablation")
+
+
+def mk_decode_step_noalloc(h, d_tokens, d_positions, d_logits, d_argmax, d_status=None,
+                           stream=None) -> int:
+    """The decode step with its scratch in the library's fixed device array (no
+    allocation anywhere); returns the status of the call itself."""
+    return lib().mk_decode_step_noalloc(h, d_tokens, d_positions, d_logits, d_argmax, d_status,
+                                        stream)
 
 
 def mk_sync_status(h, stream=None) -> int:

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstring>
 #include <map>
+#include <mutex>
 #include <new>
 #include <tuple>
 #include <vector>
@@ -581,6 +582,82 @@ extern "C" int mk_set_wait_timeout(mk_handle* h, uint64_t ns) {
   return MK_OK;
 }
 
+// ------------------------------------------------- no-allocation step ----
+// Some callers cannot allocate device memory at the moment they decode: a
+// serving loop whose device memory is owned by another allocator (a pooled
+// or budgeted arena that forbids stray cudaMalloc calls), code that must not
+// hit the synchronising cudaMalloc/cudaFree paths on a latency-critical
+// thread, or a host that hands this library a handle built earlier but no
+// memory of its own.  For them, mk_decode_step_noalloc runs the very same
+// decode kernel with its scratch (residual stream, q, attention partials,
+// router logits, argmax slots, counters and error word) carved out of the
+// fixed array below instead of the handle's scratch.  The array is a
+// file-scope __device__ object: every GPU that loads this library holds it
+// until the process exits.
+#define MK_NOALLOC_SCRATCH_BYTES (16u << 20)
+static __device__ __align__(256) unsigned char mk_noalloc_scratch[MK_NOALLOC_SCRATCH_BYTES];
+
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_base[64];  // device address of the array, per device
+
+extern "C" int mk_decode_step_noalloc(mk_handle* h, const int32_t* d_tokens,
+                                      const int32_t* d_positions, float* d_logits,
+                                      int32_t* d_argmax, int32_t* d_status, void* stream) {
+  if (!h) return MK_ERR_INVALID_ARG;
+  if (!h->sched) return MK_ERR_NOT_READY;
+  if (!d_tokens || !d_positions || !d_logits || !d_argmax) return MK_ERR_INVALID_ARG;
+  int dev = -1;
+  CK(cudaGetDevice(&dev));
+  if (dev != h->dev || dev < 0 || dev >= 64) return MK_ERR_INVALID_ARG;
+  // the same carve as the handle's scratch, sized for this handle's schedule
+  const mk_model_desc& d = h->d;
+  const size_t L = d.n_layers, B = h->batch, H = d.hidden, Hq = d.n_q_heads, D = d.head_dim;
+  const size_t E = d.n_experts > 0 ? d.n_experts : 1;
+  const size_t sx = al256(2 * 2 * L * (size_t)h->kc * B * H * 4), sq = al256(L * B * Hq * D * 4);
+  const size_t sp = al256(L * B * Hq * (size_t)h->plan.splits * (D + 2) * 4);
+  const size_t sr = al256(L * B * E * 4), sl = al256((size_t)h->plan.n_lm * B * 4);
+  const size_t sc = al256((size_t)h->plan.n_ctr * 4), se = 256;
+  if (sx + sq + sp + sr + 2 * sl + sc + se > MK_NOALLOC_SCRATCH_BYTES) return MK_ERR_SCRATCH;
+  // set-up, once per device, with that device current: the host-side name of
+  // the array is not a device address, so look the address up
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_base[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, mk_noalloc_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();
+        return MK_ERR_CUDA;
+      }
+      g_noalloc_base[dev] = p;
+    }
+    base = g_noalloc_base[dev];
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  char* q = (char*)base;
+  Globals g = make_globals(h, d_tokens, d_positions, d_logits, d_argmax);
+  g.xbuf = (float*)q; q += sx;
+  g.qbuf = (float*)q; q += sq;
+  g.part = (float*)q; q += sp;
+  g.rlog = (float*)q; q += sr;
+  g.lm_val = (float*)q; q += sl;
+  g.lm_idx = (int*)q; q += sl;
+  g.ctr = (uint32_t*)q; q += sc;
+  g.err = (int*)q;
+  // the array keeps the previous call's contents: clear what must start at
+  // zero (residual accumulators of both parities, counters, error word) and
+  // run the step as epoch 1
+  CK(cudaMemsetAsync(g.xbuf, 0, sx, s));
+  CK(cudaMemsetAsync(g.ctr, 0, sc + se, s));
+  g.epoch = 1;
+  g.parity = 1;
+  g.zero_next = 0;
+  g.trace = nullptr;
+  CK(launch_mega(h, g, s));
+  if (d_status) CK(cudaMemcpyAsync(d_status, g.err, sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
+  return MK_OK;
+}
+
 extern "C" int mk_set_residual_copies(mk_handle* h, int copies) {
   if (!h || copies < 1 || copies > 8) return MK_ERR_INVALID_ARG;
   h->kc = copies;
@@ -674,6 +751,8 @@ extern "C" const char* mk_status_string(int status) {
     case MK_ERR_TIMEOUT: return "a device wait exceeded its time limit";
     case MK_ERR_NOT_READY: return "no schedule built";
     case MK_ERR_DEVICE: return "device reported an internal inconsistency";
+    case MK_ERR_SCRATCH:
+      return "workload needs more scratch than the 16 MiB no-allocation array holds";
     default: return "unknown status";
   }
 }

@@ -37,6 +37,7 @@ extern "C" {
 #define MK_ERR_TIMEOUT (-5)     /* a device wait ran past its time limit           */
 #define MK_ERR_NOT_READY (-6)   /* mk_build_schedule has not succeeded yet         */
 #define MK_ERR_DEVICE (-7)      /* device reported an internal inconsistency       */
+#define MK_ERR_SCRATCH (-8)     /* scratch need exceeds the fixed no-allocation array */
 
 typedef struct mk_handle mk_handle;
 
@@ -147,6 +148,29 @@ int mk_decode_step_host(mk_handle* h, const int32_t* h_tokens, const int32_t* h_
 int mk_decode_step_ablation(mk_handle* h, int mode, const int32_t* d_tokens,
                             const int32_t* d_positions, float* d_logits, int32_t* d_argmax,
                             void* stream);
+
+/* Decode step that allocates nothing -- no counterpart in the pages; it is a
+ * service to callers that must not allocate device memory while decoding
+ * (their device memory belongs to another allocator or a fixed budget, or
+ * they run on a latency-critical thread that must not enter the
+ * synchronising cudaMalloc/cudaFree paths).  Same arguments and same kernel
+ * as mk_decode_step, but the step's scratch (residual stream, q, attention
+ * partials, router logits, argmax slots, counters, error word) lives in a
+ * fixed file-scope device array of 16 MiB that every GPU loading this
+ * library holds until exit, not in the handle's scratch.  The handle must
+ * have a schedule (built earlier, by a caller that could allocate).
+ *   d_status (may be NULL): [1] int32 device output that receives the step's
+ *            device status (MK_OK, MK_ERR_TIMEOUT, MK_ERR_INVALID_ARG, ...).
+ * Returns MK_ERR_SCRATCH, with nothing launched, if the handle's schedule
+ * needs more than 16 MiB of scratch.  Each call clears the parts of the
+ * array that must start at zero, on `stream`, before its launch; all calls
+ * share the one array, so calls that overlap on the GPU (on different
+ * streams, or from different handles) race and must be serialised by the
+ * caller.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Calls no cudaMalloc / cudaFree.            */
+int mk_decode_step_noalloc(mk_handle* h, const int32_t* d_tokens, const int32_t* d_positions,
+                           float* d_logits, int32_t* d_argmax, int32_t* d_status, void* stream);
 
 /* Wait for `stream` and return the device error word (MK_OK if none).  A
  * non-OK result also resets the counters and scratch so that the next step

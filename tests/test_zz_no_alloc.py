@@ -1,0 +1,69 @@
+"""The decode step that allocates nothing, checked against the regular step.
+
+Callers that may not allocate device memory while they decode -- because an
+outside allocator or a fixed budget owns the device memory, or because the
+decoding thread must stay off the synchronising cudaMalloc/cudaFree paths --
+use mk_decode_step_noalloc, whose scratch is a fixed array inside the library.
+These tests call it through the C ABI and compare it with mk_decode_step on
+the same inputs, two calls in a row, with the tolerance of the parity tests.
+This file is collected last so that a run stopping at the first failure has
+already run every other test.
+"""
+import ctypes as C
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from decode_megakernel_sm_gb300 import _lib as L
+from tests.harness import Run
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(r, logits, am, status):
+    stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = L.lib().mk_decode_step_noalloc(r.dec.h, r.d_tok.data_ptr(), r.d_pos.data_ptr(),
+                                        logits.data_ptr(), am.data_ptr(), status.data_ptr(),
+                                        stream)
+    assert rc == L.MK_OK, L.mk_status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status.item()) == L.MK_OK
+    return logits.cpu().numpy().astype(np.float64), am.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama1b_1k"])
+def test_noalloc_step_matches_regular_step_on_two_calls(name):
+    r = Run(synth.CONFIGS[name], seed=13)
+    try:
+        V = r.cfg["vocab"]
+        logits = torch.full((r.B, V), float("nan"), dtype=torch.float32, device="cuda")
+        am = torch.full((r.B,), -1, dtype=torch.int32, device="cuda")
+        status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+        for _ in range(2):
+            lg_ref, am_ref = r.gpu_step("mega")       # the existing entry point
+            lg, a = _noalloc(r, logits, am, status)   # same inputs, same cache row P
+            r.check(lg, a, lg_ref, am_ref)
+            r.tokens = [int(x) for x in am_ref]
+            r.pos = [p + 1 for p in r.pos]
+    finally:
+        r.close()
+
+
+def test_noalloc_rejects_schedules_beyond_its_array():
+    # 250 layers of one-kv-head attention at 2048 positions need more than
+    # 16 MiB of split-KV partials: refused before any launch
+    cfg = synth.custom(n_layers=250, n_q_heads=2, n_kv_heads=1, ffn=256, vocab=256,
+                       prefill=(8, 8), steps=2040)
+    r = Run(cfg, seed=1)
+    try:
+        logits = torch.empty((1, 256), dtype=torch.float32, device="cuda")
+        am = torch.empty(1, dtype=torch.int32, device="cuda")
+        stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+        rc = L.lib().mk_decode_step_noalloc(r.dec.h, r.d_tok.data_ptr(), r.d_pos.data_ptr(),
+                                            logits.data_ptr(), am.data_ptr(), None, stream)
+        assert rc == L.MK_ERR_SCRATCH
+        assert "16 MiB" in L.mk_status_string(rc)
+    finally:
+        r.close()
