@@ -89,6 +89,7 @@ SIGNATURES = {
     "mk_set_wait_timeout": (C.c_int, [C.c_void_p, C.c_uint64]),
     "mk_get_info": (C.c_int, [C.c_void_p, C.POINTER(mk_info)]),
     "mk_debug_drop_instruction": (C.c_int, [C.c_void_p, C.c_int, C.c_int]),
+    "mk_get_routes": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32), C.c_size_t]),
     "mk_set_trace": (C.c_int, [C.c_void_p, C.c_int]),
     "mk_set_l2_prefetch": (C.c_int, [C.c_void_p, C.c_uint64]),
     "mk_set_residual_copies": (C.c_int, [C.c_void_p, C.c_int]),
@@ -179,6 +180,15 @@ def mk_get_info(h) -> dict:
     info = mk_info()
     _check(lib().mk_get_info(h, C.byref(info)), "mk_get_info")
     return {n: getattr(info, n) for n, _ in mk_info._fields_}
+
+
+def mk_get_routes(h, n_layers: int, top_k: int):
+    """Expert ids chosen at the last step, numpy int32 [n_layers][top_k]."""
+    import numpy as np
+    out = np.zeros((n_layers, top_k), np.int32)
+    _check(lib().mk_get_routes(h, out.ctypes.data_as(C.POINTER(C.c_int32)), out.size),
+           "mk_get_routes")
+    return out
 
 
 def mk_debug_drop_instruction(h, sm: int, pc: int):

@@ -49,6 +49,7 @@ struct mk_handle {
   size_t scratch_bytes = 0;
   float *xbuf = nullptr, *qbuf = nullptr, *part = nullptr, *rlog = nullptr, *lm_val = nullptr;
   int* lm_idx = nullptr;
+  int* routes = nullptr;
   uint32_t* ctr = nullptr;
   int* err = nullptr;
   size_t xbuf_bytes = 0, ctr_bytes = 0;
@@ -329,7 +330,8 @@ extern "C" int mk_build_schedule(mk_handle* h, int batch, int max_ctx) {
   const size_t sp = al256(L * B * Hq * (size_t)p.splits * (D + 2) * 4);
   const size_t sr = al256(L * B * E * 4), sl = al256((size_t)p.n_lm * B * 4);
   const size_t sc = al256((size_t)p.n_ctr * 4), se = 256;
-  const size_t total = sx + sq + sp + sr + 2 * sl + sc + se;
+  const size_t sroute = al256(L * (size_t)(d.top_k > 0 ? d.top_k : 1) * 4);
+  const size_t total = sx + sq + sp + sr + 2 * sl + sc + se + sroute;
   CK(cudaMalloc(&h->scratch, total));
   h->scratch_bytes = total;
   char* q = (char*)h->scratch;
@@ -340,7 +342,8 @@ extern "C" int mk_build_schedule(mk_handle* h, int batch, int max_ctx) {
   h->lm_val = (float*)q; q += sl;
   h->lm_idx = (int*)q; q += sl;
   h->ctr = (uint32_t*)q; q += sc;
-  h->err = (int*)q;
+  h->err = (int*)q; q += se;
+  h->routes = (int*)q;
   h->xbuf_bytes = sx;
   h->ctr_bytes = sc;
   CK(cudaMemsetAsync(h->scratch, 0, total, h->own));
@@ -384,6 +387,7 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.qbuf = h->qbuf;
   g.part = h->part;
   g.rlog = h->rlog;
+  g.routes = h->routes;
   g.lm_val = h->lm_val;
   g.lm_idx = h->lm_idx;
   g.ctr = h->ctr;
@@ -719,6 +723,17 @@ extern "C" int mk_get_trace(mk_handle* h, uint64_t* out, size_t n) {
   if (n < need) return MK_ERR_INVALID_ARG;
   CK(cudaDeviceSynchronize());
   CK(cudaMemcpy(out, h->trace, need * sizeof(uint64_t), cudaMemcpyDeviceToHost));
+  return MK_OK;
+}
+
+extern "C" int mk_get_routes(mk_handle* h, int32_t* out, size_t n) {
+  if (!h || !out) return MK_ERR_INVALID_ARG;
+  if (!h->sched) return MK_ERR_NOT_READY;
+  if (h->d.n_experts == 0) return MK_ERR_UNSUPPORTED;
+  const size_t need = (size_t)h->d.n_layers * h->d.top_k;
+  if (n < need) return MK_ERR_INVALID_ARG;
+  CK(cudaDeviceSynchronize());
+  CK(cudaMemcpy(out, h->routes, need * sizeof(int32_t), cudaMemcpyDeviceToHost));
   return MK_OK;
 }
 

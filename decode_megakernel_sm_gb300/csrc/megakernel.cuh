@@ -730,7 +730,11 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   if (!cached) norm_apply(c, g, 2 * l + 1, ng);
   c.mark(g, 0);
   if (routed) {
-    if (c.warp == 0) route_topk(g.rlog + (size_t)l * g.B * g.E, g.E, g.K, c.lane, c.topk, c.topw);
+    if (c.warp == 0) {
+      route_topk(g.rlog + (size_t)l * g.B * g.E, g.E, g.K, c.lane, c.topk, c.topw);
+      // record the choice (every routed slice writes the same ids)
+      if (c.lane < g.K) g.routes[(size_t)l * g.K + c.lane] = c.topk[c.lane];
+    }
     consumer_bar();
   }
   const float scale = routed ? c.topw[I.g] : 1.f;

@@ -108,6 +108,7 @@ struct Globals {
   float* qbuf;             // [L][B][Hq][D]
   float* part;             // [L][B][Hq][splits][D+2]: o[D], m, l  (log2 domain)
   float* rlog;             // [L][B][E] router logits
+  int* routes;             // [L][K] expert ids chosen at the last step (MoE, batch 1)
   float* lm_val;           // [n_lm][B]
   int* lm_idx;             // [n_lm][B]
   uint32_t* ctr;           // dependency counters

@@ -100,6 +100,10 @@ class Decoder:
         _, q = L.mk_plan(self.desc, info["batch"], info["max_ctx"], info["n_sm"])
         return tr, q, info["n_sm"], info["max_pc"]
 
+    def routes(self):
+        """MoE: expert ids chosen at the last step, [n_layers][top_k]."""
+        return L.mk_get_routes(self.h, self.cfg["n_layers"], self.cfg["top_k"])
+
     def drop_instruction(self, sm: int, pc: int):
         L.mk_debug_drop_instruction(self.h, sm, pc)
 

@@ -211,6 +211,12 @@ typedef struct {
 } mk_info;
 int mk_get_info(const mk_handle* h, mk_info* out);
 
+/* MoE only: the expert ids the router chose at the most recent step,
+ * [n_layers][top_k] int32 in selection order (largest router logit first,
+ * lower id first on ties; "Gemma 4 TPU megakernel", section "Megakernels
+ * for Gemma 4", component "Router").  Waits for the device.  n = capacity. */
+int mk_get_routes(mk_handle* h, int32_t* out, size_t n);
+
 /* Replace instruction `pc` of SM `sm` by a no-op that neither waits nor
  * signals -- a fault-injection aid for tests: every instruction waiting on
  * the dropped one's counter then runs into its time limit and the step

@@ -66,6 +66,25 @@ def test_llama1b_8k_parity():
     run_steps(synth.CONFIGS["llama1b_8k"], 2, seed=1)
 
 
+def test_moe_small_parity():
+    # MoE variant (hidden 2048, head_dim 128, 4 q heads per kv head) at a reduced
+    # size: 16 experts, top-4, shared expert, ragged FFN widths
+    cfg = synth.custom(n_layers=3, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn=0,
+                       vocab=3001, tied=False, n_experts=16, top_k=4, expert_ffn=200,
+                       shared_ffn=500, rope_theta=5e5, prefill=(70, 70), steps=4)
+    run_steps(cfg, 4, seed=21)
+
+
+def test_moe_full_config_parity():
+    r = Run(synth.CONFIGS["moe"], seed=0)
+    try:
+        for _ in range(2):
+            r.step()
+        print(f"moe worst max|dlogit|/std = {r.worst:.2e}, near ties {r.near_ties}")
+    finally:
+        r.close()
+
+
 def test_ablation_modes_match_megakernel():
     cfg = synth.custom(n_layers=3, n_q_heads=6, n_kv_heads=3, ffn=1000, vocab=999,
                        prefill=(20, 20), steps=6)
