@@ -48,6 +48,7 @@ struct mk_handle {
   void* scratch = nullptr;
   size_t scratch_bytes = 0;
   float *xbuf = nullptr, *qbuf = nullptr, *part = nullptr, *rlog = nullptr, *lm_val = nullptr;
+  float* hglob = nullptr;
   int* lm_idx = nullptr;
   int* routes = nullptr;
   uint32_t* ctr = nullptr;
@@ -240,7 +241,10 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
     CK(pack_wo(wo, w->wo[l], H, Hq, D, s));
     if (!moe) {
       CK(pack_interleave(gu, w->w_gate[l], w->w_up[l], d.ffn, H, s));
-      CK(pack_transpose(dT, w->w_down[l], H, d.ffn, 1, s));
+      if (mlp_split(d))  // the down rows are streamed as they are
+        CK(cudaMemcpyAsync(dT, w->w_down[l], ls.dT * 2, cudaMemcpyDeviceToDevice, s));
+      else
+        CK(pack_transpose(dT, w->w_down[l], H, d.ffn, 1, s));
     } else {
       CK(cudaMemcpyAsync(rt, w->router[l], ls.router * 2, cudaMemcpyDeviceToDevice, s));
       CK(pack_interleave(egu, w->ex_gate[l], w->ex_up[l], (long)d.n_experts * d.expert_ffn, H,
@@ -331,7 +335,8 @@ extern "C" int mk_build_schedule(mk_handle* h, int batch, int max_ctx) {
   const size_t sr = al256(L * B * E * 4), sl = al256((size_t)p.n_lm * B * 4);
   const size_t sc = al256((size_t)p.n_ctr * 4), se = 256;
   const size_t sroute = al256(L * (size_t)(d.top_k > 0 ? d.top_k : 1) * 4);
-  const size_t total = sx + sq + sp + sr + 2 * sl + sc + se + sroute;
+  const size_t sh = al256(L * B * (size_t)(d.ffn > 0 ? d.ffn : 1) * 4);
+  const size_t total = sx + sq + sp + sr + 2 * sl + sc + se + sroute + sh;
   CK(cudaMalloc(&h->scratch, total));
   h->scratch_bytes = total;
   char* q = (char*)h->scratch;
@@ -343,7 +348,8 @@ extern "C" int mk_build_schedule(mk_handle* h, int batch, int max_ctx) {
   h->lm_idx = (int*)q; q += sl;
   h->ctr = (uint32_t*)q; q += sc;
   h->err = (int*)q; q += se;
-  h->routes = (int*)q;
+  h->routes = (int*)q; q += sroute;
+  h->hglob = (float*)q;
   h->xbuf_bytes = sx;
   h->ctr_bytes = sc;
   CK(cudaMemsetAsync(h->scratch, 0, total, h->own));
@@ -387,6 +393,7 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.qbuf = h->qbuf;
   g.part = h->part;
   g.rlog = h->rlog;
+  g.hglob = h->hglob;
   g.routes = h->routes;
   g.lm_val = h->lm_val;
   g.lm_idx = h->lm_idx;
@@ -621,7 +628,8 @@ extern "C" int mk_decode_step_noalloc(mk_handle* h, const int32_t* d_tokens,
   const size_t sp = al256(L * B * Hq * (size_t)h->plan.splits * (D + 2) * 4);
   const size_t sr = al256(L * B * E * 4), sl = al256((size_t)h->plan.n_lm * B * 4);
   const size_t sc = al256((size_t)h->plan.n_ctr * 4), se = 256;
-  if (sx + sq + sp + sr + 2 * sl + sc + se > MK_NOALLOC_SCRATCH_BYTES) return MK_ERR_SCRATCH;
+  const size_t sh = al256(L * B * (size_t)(d.ffn > 0 ? d.ffn : 1) * 4);
+  if (sx + sq + sp + sr + 2 * sl + sc + se + sh > MK_NOALLOC_SCRATCH_BYTES) return MK_ERR_SCRATCH;
   // set-up, once per device, with that device current: the host-side name of
   // the array is not a device address, so look the address up
   void* base = nullptr;
@@ -647,7 +655,8 @@ extern "C" int mk_decode_step_noalloc(mk_handle* h, const int32_t* d_tokens,
   g.lm_val = (float*)q; q += sl;
   g.lm_idx = (int*)q; q += sl;
   g.ctr = (uint32_t*)q; q += sc;
-  g.err = (int*)q;
+  g.err = (int*)q; q += se;
+  g.hglob = (float*)q;
   // the array keeps the previous call's contents: clear what must start at
   // zero (residual accumulators of both parities, counters, error word) and
   // run the step as epoch 1

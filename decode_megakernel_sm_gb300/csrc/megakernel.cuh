@@ -119,6 +119,13 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
     case OP_LMHEAD:
       s[0] = {(const unsigned char*)(g.lm_head + (size_t)I.r0 * HT), nullptr, ROW, n, RPS};
       return 1;
+    case OP_MLP_UP:
+      s[0] = {(const unsigned char*)(Lp->wgu + (size_t)I.r0 * 2 * HT), nullptr, ROW, 2 * n, RPS};
+      return 1;
+    case OP_MLP_DOWN:  // rows of the row-major [H][F] down projection
+      s[0] = {(const unsigned char*)(Lp->wdT + (size_t)I.r0 * g.F), nullptr, (uint32_t)g.F * 2, n,
+              STAGE_BYTES / ((uint32_t)g.F * 2)};
+      return 1;
     case OP_ATTN: {
       // slice s of S over positions [0, P]: [s*C/S, (s+1)*C/S), C = P + 1.
       // Rows below P come from the cache through the ring; row P (written by
@@ -814,6 +821,114 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   return true;
 }
 
+// ------------------------------------- OP_MLP_UP (gate/up column slice) ----
+// h_c = SiLU(gate_c . xn) * (up_c . xn) for the slice's FFN columns, written
+// to the layer's h vector in global memory for the down instructions.
+template <int HT, int D, int HPG, int NB>
+MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+  const int l = I.layer;
+  const LayerPtrs& Lp = g.layers[l];
+  const bool cached = (I.flags & F_NORM_CACHED) != 0;
+  NormGain<HT> ng;
+  if (!cached) norm_gain(ng, Lp.mlp_norm, c.tid);
+  if (!dep_wait(c, g, I)) return false;
+  if (!cached) norm_apply(c, g, 2 * l + 1, ng);
+  c.mark(g, 0);
+  float xr[HT / 32];
+  if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
+  Seg s[2];
+  get_segs<HT, D>(g, I, c.pos, c.topk, s);
+  float* yrow = c.yrow;
+  const int lane = c.lane;
+  gemv_rows(c, g, s[0], xr, [&](uint32_t r, float(&acc)[NB]) {
+    if (lane == 0) {
+#pragma unroll
+      for (int b = 0; b < NB; b++) yrow[b * MAX_ROWS + r] = acc[b];
+    }
+  });
+  c.mark(g, 1);
+  consumer_bar();
+  const int ncol = (int)(I.r1 - I.r0);
+  for (int t = c.tid; t < NB * ncol; t += NCT) {
+    const int b = t / ncol, j = t % ncol;
+    if (b < g.B) {
+      const float gt = yrow[b * MAX_ROWS + 2 * j], up = yrow[b * MAX_ROWS + 2 * j + 1];
+      g.hglob[((size_t)l * g.B + b) * g.F + I.r0 + j] = (gt / (1.f + expf(-gt))) * up;
+    }
+  }
+  consumer_bar();
+  return true;
+}
+
+// --------------------------------------- OP_MLP_DOWN (down rows, batch 1) ----
+// Rows [r0, r1) of x_{2l+2} = x_{2l+1} + Wd h: each consumer thread holds
+// its 16-byte chunks of h in registers and dots them with the same chunks of
+// every down row streamed through the ring; per-warp partials meet in shared
+// memory.  Plain stores: no atomics, no other SM touches these rows.
+template <int HT, int D, int HPG, int NB>
+MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+  if constexpr (NB != 1) {
+    if (c.tid == 0) set_err(g, MK_ERR_DEVICE, c.pc, I.op);
+    return false;
+  } else {
+    constexpr int CPT = (STAGE_BYTES / 16 + NCT - 1) / NCT;  // h chunks per thread
+    const int l = I.layer, F = g.F, nch = F / 8;
+    const int nrows = (int)(I.r1 - I.r0);
+    if (!dep_wait(c, g, I)) return false;
+    float h[CPT][8];
+    const float* hp = g.hglob + (size_t)l * F;
+#pragma unroll
+    for (int q = 0; q < CPT; q++) {
+      const int k = c.tid + q * NCT;
+      if (k < nch) {
+        const float4 a = __ldcg((const float4*)(hp + (size_t)k * 8));
+        const float4 b = __ldcg((const float4*)(hp + (size_t)k * 8) + 1);
+        h[q][0] = a.x; h[q][1] = a.y; h[q][2] = a.z; h[q][3] = a.w;
+        h[q][4] = b.x; h[q][5] = b.y; h[q][6] = b.z; h[q][7] = b.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; e++) h[q][e] = 0.f;
+      }
+    }
+    const float res = c.tid < nrows ? xres_sum(g, 2 * l + 1, 0, (int)I.r0 + c.tid) : 0.f;
+    c.mark(g, 0);
+    float* part = c.yrow;  // [NCW][MAX_DOWN_ROWS]
+    Seg s[2];
+    get_segs<HT, D>(g, I, c.pos, c.topk, s);
+    for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
+      const uint32_t n = min(s[0].ups, s[0].n - u0);
+      if (!c.ring.acquire(g)) break;
+      const unsigned char* st = c.ring.stage_ptr();
+      for (uint32_t j = 0; j < n; j++) {
+        float acc = 0.f;
+#pragma unroll
+        for (int q = 0; q < CPT; q++) {
+          const int k = c.tid + q * NCT;
+          if (k < nch) {
+            float w[8];
+            unpack8(*(const uint4*)(st + (size_t)j * F * 2 + (size_t)k * 16), w);
+#pragma unroll
+            for (int e = 0; e < 8; e++) acc = fmaf(w[e], h[q][e], acc);
+          }
+        }
+        acc = warp_sum(acc);
+        if (c.lane == 0) part[c.warp * MAX_DOWN_ROWS + u0 + j] = acc;
+      }
+      c.ring.release(c.lane);
+    }
+    c.mark(g, 1);
+    consumer_bar();
+    if (c.tid < nrows) {
+      float y = 0.f;
+#pragma unroll
+      for (int w = 0; w < NCW; w++) y += part[w * MAX_DOWN_ROWS + c.tid];
+      xres(g, 2 * l + 2, 0)[I.r0 + c.tid] = res + y;
+    }
+    consumer_bar();
+    return true;
+  }
+}
+
 // ------------------------------------ OP_LMHEAD (final norm + head rows) ----
 // Logits rows [r0, r1) and this slice's (max, first index); the slice that
 // arrives last on the argmax counter reduces all slices into argmax[b].
@@ -1200,6 +1315,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
       case OP_OPROJ: ok = op_oproj(c, g, I); break;
       case OP_ROUTER: ok = op_router(c, g, I); break;
       case OP_MLP: ok = op_mlp(c, g, I); break;
+      case OP_MLP_UP: ok = op_mlp_up(c, g, I); break;
+      case OP_MLP_DOWN: ok = op_mlp_down(c, g, I); break;
       case OP_LMHEAD: ok = op_lmhead(c, g, I); break;
       default:
         if (tid == 0) set_err(g, MK_ERR_DEVICE, pc, I.op);

@@ -29,11 +29,15 @@ enum Op : uint8_t {
   OP_LMHEAD = 5,  // final RMSNorm + LM-head rows + argmax (last arriver)
   OP_ROUTER = 6,  // MoE: RMSNorm + router rows
   OP_NOP = 7,     // does nothing (fault-injection stand-in)
+  OP_MLP_UP = 8,  // RMSNorm + gate/up rows + SiLU*mul of an FFN column slice -> h (split MLP)
+  OP_MLP_DOWN = 9,  // down-projection rows over the whole h + residual (split MLP)
 };
 
 // Ablation phases: one launch per (layer, phase).  No instruction waits on a
 // counter signalled by an instruction of its own phase.
-enum Phase : int { PH_QKV = 0, PH_ATTN = 1, PH_OPROJ = 2, PH_ROUTER = 3, PH_MLP = 4, N_PHASES = 5 };
+enum Phase : int {
+  PH_QKV = 0, PH_ATTN = 1, PH_OPROJ = 2, PH_ROUTER = 3, PH_MLP = 4, PH_DOWN = 5, N_PHASES = 6
+};
 
 enum Flag : uint8_t {
   F_RESIDUAL = 1,    // this instruction also adds the residual input for its rows
@@ -52,20 +56,22 @@ MK_HD inline int phase_of(uint8_t op) {
     case OP_ATTN: return PH_ATTN;
     case OP_OPROJ: return PH_OPROJ;
     case OP_ROUTER: return PH_ROUTER;
+    case OP_MLP_DOWN: return PH_DOWN;
     default: return PH_MLP;
   }
 }
 
 // Counter ids: per layer l, base l*stride:
-//   qkv[g] (g < Hkv), attn[g], oproj, mlp, router; then one argmax counter.
+//   qkv[g] (g < Hkv), attn[g], oproj, mlp, router, mlp_up; then one argmax counter.
 struct CtrMap {
   int Hkv, L;
-  MK_HD int stride() const { return 2 * Hkv + 3; }
+  MK_HD int stride() const { return 2 * Hkv + 4; }
   MK_HD uint32_t qkv(int l, int g) const { return (uint32_t)(l * stride() + g); }
   MK_HD uint32_t attn(int l, int g) const { return (uint32_t)(l * stride() + Hkv + g); }
   MK_HD uint32_t oproj(int l) const { return (uint32_t)(l * stride() + 2 * Hkv); }
   MK_HD uint32_t mlp(int l) const { return (uint32_t)(l * stride() + 2 * Hkv + 1); }
   MK_HD uint32_t router(int l) const { return (uint32_t)(l * stride() + 2 * Hkv + 2); }
+  MK_HD uint32_t mlp_up(int l) const { return (uint32_t)(l * stride() + 2 * Hkv + 3); }
   MK_HD uint32_t lm() const { return (uint32_t)(L * stride()); }
   MK_HD int count() const { return L * stride() + 1; }
 };
@@ -78,6 +84,14 @@ constexpr int STAGE_BYTES = 16384;   // bytes per ring stage
 constexpr int MAX_STAGES = 16;
 constexpr int MAX_ROWS = 256;        // rows of one QKV / gate-up / router instruction
 constexpr int MAX_COLS = MAX_ROWS / 2;
+constexpr int MAX_DOWN_ROWS = 64;    // output rows of one split-MLP down instruction
+
+// Dense batch-1 models run the MLP as two ops (gate/up column slices, then
+// row-split down projection over the whole h) when one down row fits a ring
+// stage; otherwise one fused op per FFN column slice with float atomics.
+inline bool mlp_split(const mk_model_desc& d) {
+  return d.n_experts == 0 && d.max_batch == 1 && d.ffn % 8 == 0 && d.ffn * 2 <= STAGE_BYTES;
+}
 
 // Device pointers of one layer inside the packed weight buffer.
 struct LayerPtrs {
@@ -86,7 +100,7 @@ struct LayerPtrs {
   const uint16_t* wqkv;       // [Hkv][(HPG+2)*D][H]; per head rows (t, t+D/2) adjacent
   const uint16_t* wo;         // [Hq][H][D]
   const uint16_t* wgu;        // dense: [F][2][H]      (gate row, up row)
-  const uint16_t* wdT;        // dense: [F][H]         (down, transposed)
+  const uint16_t* wdT;        // dense: down, [F][H] transposed (fused MLP) or [H][F] (split MLP)
   const uint16_t* router;     // MoE:   [E][H]
   const uint16_t* ex_gu;      // MoE:   [E][Fe][2][H]
   const uint16_t* ex_dT;      // MoE:   [E][Fe][H]
@@ -108,6 +122,7 @@ struct Globals {
   float* qbuf;             // [L][B][Hq][D]
   float* part;             // [L][B][Hq][splits][D+2]: o[D], m, l  (log2 domain)
   float* rlog;             // [L][B][E] router logits
+  float* hglob;            // [L][B][F] SiLU(gate)*up (split MLP)
   int* routes;             // [L][K] expert ids chosen at the last step (MoE, batch 1)
   float* lm_val;           // [n_lm][B]
   int* lm_idx;             // [n_lm][B]

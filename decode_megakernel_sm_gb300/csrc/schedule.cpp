@@ -175,6 +175,42 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
         }
       }
     }
+    // ---- split MLP (dense, batch 1): gate/up column slices, then down rows
+    if (mlp_split(d)) {
+      const long F = d.ffn;
+      for (int i = 0; i < n_sm; i++) {
+        long a = cut(F, n_sm, i, 1), b = (i == n_sm - 1) ? F : cut(F, n_sm, i + 1, 1);
+        bool first = true;
+        while (a < b) {
+          const long e = std::min(b, a + MAX_COLS);
+          Instr I = mk(OP_MLP_UP, l);
+          I.r0 = (uint32_t)a;
+          I.r1 = (uint32_t)e;
+          I.flags = first ? 0 : F_NORM_CACHED;
+          I.wait_ctr = cm.oproj(l);
+          I.sig_ctr = cm.mlp_up(l);
+          qs[i].push_back(I);
+          bytes[i] += (double)(e - a) * H * 4;
+          first = false;
+          a = e;
+        }
+      }
+      for (int i = 0; i < n_sm; i++) {
+        long a = cut(H, n_sm, i, 1), b = (i == n_sm - 1) ? H : cut(H, n_sm, i + 1, 1);
+        while (a < b) {
+          const long e = std::min(b, a + MAX_DOWN_ROWS);
+          Instr I = mk(OP_MLP_DOWN, l);
+          I.r0 = (uint32_t)a;
+          I.r1 = (uint32_t)e;
+          I.wait_ctr = cm.mlp_up(l);
+          I.sig_ctr = cm.mlp(l);
+          qs[i].push_back(I);
+          bytes[i] += (double)(e - a) * F * 2;
+          a = e;
+        }
+      }
+      continue;
+    }
     // ---- MLP column slices (dense FFN, or MoE shared + routed slots)
     std::vector<std::pair<int, size_t>> mlp_at;  // (sm, index in qs[sm])
     // MoE: every SM takes a slice of the shared columns first (their weights
@@ -355,6 +391,20 @@ int plan_verify(const mk_model_desc& d, int B, const PlanOut& p) {
           if (!mark(res, (size_t)l * H + r)) return 16;
         break;
       }
+      case OP_MLP_UP:
+        if (!mlp_split(d) || l >= L || I.r0 >= I.r1 || I.r1 - I.r0 > (uint32_t)MAX_COLS ||
+            (long)I.r1 > Fv)
+          return 23;
+        for (uint32_t c = I.r0; c < I.r1; c++)
+          if (!mark(mlp, (size_t)l * Fv + c)) return 24;
+        break;
+      case OP_MLP_DOWN:
+        if (!mlp_split(d) || l >= L || I.r0 >= I.r1 || (int)I.r1 > H ||
+            I.r1 - I.r0 > (uint32_t)MAX_DOWN_ROWS)
+          return 25;
+        for (uint32_t r = I.r0; r < I.r1; r++)
+          if (!mark(res, (size_t)l * H + r)) return 26;
+        break;
       case OP_LMHEAD:
         if (I.r0 >= I.r1 || (int)I.r1 > V || (int)I.aux >= p.n_lm) return 17;
         if (!mark(slot, I.aux)) return 18;

@@ -242,8 +242,9 @@ const char* mk_status_string(int status);
  * The schedule builder and its checker, exposed for inspection and tests.
  * Instructions are 32-byte records:
  *   op, flags (u8), layer (u16), b, g (u16), r0, r1, wait_ctr, wait_cnt,
- *   sig_ctr, aux (u32).  op: 0 HALT, 1 QKV, 2 ATTN, 3 OPROJ, 4 MLP,
- *   5 LMHEAD, 6 ROUTER, 7 NOP.  wait_ctr / sig_ctr 0xFFFFFFFF: none.      */
+ *   sig_ctr, aux (u32).  op: 0 HALT, 1 QKV, 2 ATTN, 3 OPROJ, 4 MLP (fused
+ *   column slice), 5 LMHEAD, 6 ROUTER, 7 NOP, 8 MLP_UP (gate/up column
+ *   slice), 9 MLP_DOWN (down rows).  wait_ctr / sig_ctr 0xFFFFFFFF: none.  */
 typedef struct {
   uint8_t op, flags;
   uint16_t layer;

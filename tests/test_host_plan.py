@@ -83,6 +83,15 @@ def independent_coverage(cfg, q, n_sm, max_pc, splits):
                 for r in range(I.aux & 0xFFFF, I.aux >> 16):
                     assert (I.layer, r) not in seen["res"]
                     seen["res"].add((I.layer, r))
+            elif I.op == 8:  # gate/up column slice of the split MLP
+                for c in range(I.r0, I.r1):
+                    assert (I.layer, c) not in seen["mlp"]
+                    seen["mlp"].add((I.layer, c))
+            elif I.op == 9:  # down rows of the split MLP (own their residual)
+                assert I.r1 - I.r0 <= 64
+                for r in range(I.r0, I.r1):
+                    assert (I.layer, r) not in seen["res"]
+                    seen["res"].add((I.layer, r))
             elif I.op == 5:
                 for r in range(I.r0, I.r1):
                     assert r not in seen["lm"]
@@ -117,6 +126,15 @@ def test_plan_covers_all_work_and_is_deadlock_free(name, n_sm):
     assert L.mk_plan_check(q, n_sm, st["max_pc"], st["n_counters"]) == L.MK_OK
 
 
+def test_split_mlp_is_used_for_dense_batch1_only():
+    for name, split in (("llama1b_1k", True), ("tiny", True), ("llama1b_b8", False), ("moe", False)):
+        cfg, d = desc(name)
+        st, q = L.mk_plan(d, cfg["batch"], cfg["max_seq"], 152)
+        ops = {q[i].op for i in range(152 * st["max_pc"])}
+        assert (8 in ops and 9 in ops and 4 not in ops) == split, name
+        assert (4 in ops) == (not split), name
+
+
 def test_llama1b_plan_is_byte_balanced():
     cfg, d = desc("llama1b_1k")
     st, _ = L.mk_plan(d, 1, cfg["max_seq"], 152, with_queues=False)
@@ -139,10 +157,11 @@ def test_checker_rejects_cyclic_order():
     n_sm = 4
     st, q = L.mk_plan(d, 1, cfg["max_seq"], n_sm)
     mp = st["max_pc"]
-    # on SM 0 move a layer-1 QKV (waits on all layer-0 MLP slices) in front of
-    # SM 0's own layer-0 MLP slice: a cycle through SM 0's queue
+    # on SM 0 move a layer-1 QKV (waits on all of layer 0's MLP) in front of
+    # SM 0's own layer-0 MLP instruction: a cycle through SM 0's queue
     row = [q[i] for i in range(mp)]
-    i_mlp = next(i for i, I in enumerate(row) if I.op == 4 and I.layer == 0)
+    # the instruction signalling layer 0's MLP counter: fused slice (4) or down rows (9)
+    i_mlp = next(i for i, I in enumerate(row) if I.op in (4, 9) and I.layer == 0)
     i_qkv = next(i for i, I in enumerate(row) if I.op == 1 and I.layer == 1)
     saved = L.mk_instr()
     C.memmove(C.byref(saved), C.byref(q[i_qkv]), C.sizeof(saved))
