@@ -21,7 +21,7 @@ MK_ERR_DEVICE = -7
 MK_ERR_SCRATCH = -8
 MK_ABL_STREAM, MK_ABL_GRAPH, MK_ABL_PDL = 0, 1, 2
 
-OP_NAMES = {0: "HALT", 1: "QKV", 2: "ATTN", 3: "OPROJ", 4: "MLP", 5: "LMHEAD", 6: "ROUTER",
+OP_NAMES = {0: "HALT", 1: "QKV", 2: "ATTN", 3: "OPROJ", 4: "MLP", 5: "LMHEAD", 6: "ROUTER", 8: "MLP_UP", 9: "MLP_DOWN",
             7: "NOP"}
 
 
