@@ -48,6 +48,9 @@ def parse():
                     help="bytes each SM warms in L2 ahead of its ring (library default if unset)")
     ap.add_argument("--kc", type=int, default=None,
                     help="partial copies of each residual vector (library default if unset)")
+    ap.add_argument("--hold", type=int, default=None,
+                    help="hold-policy mask (library default if unset)")
+    ap.add_argument("--hold-prefetch", type=int, default=256 << 10)
     ap.add_argument("--trace", default=None,
                     help="write a per-instruction timeline of 3 traced steps to this path")
     return ap.parse_args()
@@ -266,6 +269,8 @@ def main():
     torch.cuda.empty_cache()
     if args.kc is not None:
         dec.set_residual_copies(args.kc)
+    if args.hold is not None:
+        dec.set_hold_policy(args.hold, args.hold_prefetch)
     dec.build_schedule(B, cfg["max_seq"])
     if args.l2_ahead is not None:
         dec.set_l2_prefetch(args.l2_ahead)

@@ -59,6 +59,8 @@ struct mk_handle {
   unsigned long long timeout_ns = 2000000000ull;
   unsigned long long l2_ahead = 0;
   int kc = 1;  // partial copies of each residual vector
+  unsigned hold_mask = DEFAULT_HOLD;
+  unsigned hold_prefetch = 256u << 10;
   // host-buffer step
   cudaStream_t own = nullptr;
   int32_t *d_tok = nullptr, *d_pos = nullptr, *d_am = nullptr;
@@ -323,7 +325,7 @@ extern "C" int mk_build_schedule(mk_handle* h, int batch, int max_ctx) {
   CK(cudaStreamSynchronize(h->own));
   free_schedule(h);
   PlanOut p;
-  int rc = plan_build(h->d, batch, max_ctx, h->n_sm, p);
+  int rc = plan_build(h->d, batch, max_ctx, h->n_sm, p, h->hold_mask);
   if (rc) return rc;
   if (plan_verify(h->d, batch, p)) return MK_ERR_SCHEDULE;
   if (plan_check(p.q.data(), h->n_sm, p.max_pc, p.n_ctr)) return MK_ERR_SCHEDULE;
@@ -429,6 +431,7 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.sel_key = -1;
   g.trace = h->trace;
   g.l2_ahead = h->l2_ahead;
+  g.hold_prefetch = h->hold_prefetch;
   return g;
 }
 
@@ -668,6 +671,13 @@ extern "C" int mk_decode_step_noalloc(mk_handle* h, const int32_t* d_tokens,
   g.trace = nullptr;
   CK(launch_mega(h, g, s));
   if (d_status) CK(cudaMemcpyAsync(d_status, g.err, sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
+  return MK_OK;
+}
+
+extern "C" int mk_set_hold_policy(mk_handle* h, unsigned mask, uint64_t prefetch_bytes) {
+  if (!h || mask > 63u || prefetch_bytes > (64ull << 20)) return MK_ERR_INVALID_ARG;
+  h->hold_mask = mask;
+  h->hold_prefetch = (unsigned)prefetch_bytes;
   return MK_OK;
 }
 

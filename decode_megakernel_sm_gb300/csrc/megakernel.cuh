@@ -1127,7 +1127,7 @@ struct L2Cursor {
 // the CTA may exit.
 template <int HT, int D, int HPG, int NB>
 MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint32_t empty0,
-                     int* ppos, int* ptopk, float* ptopw, int lane) {
+                     int* ppos, int* ptopk, float* ptopw, const int* done, int lane) {
   const uint64_t pol_w = policy_evict_first();
   const uint64_t pol_kv = policy_evict_normal();
   const int ns = g.n_stages;
@@ -1137,6 +1137,7 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
   uint32_t par = 0;
   bool grid_waited = !g.pdl;
   int routed_layer = -1;
+  int seq = 0;  // instructions of this launch before the current one (consumer order)
   unsigned long long issued_bytes = 0;
   L2Cursor<HT, D, NB> l2;
   for (int pc = 0; pc < g.max_pc; pc++) {
@@ -1169,6 +1170,37 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
     __syncwarp();
     Seg s[2];
     const int nseg = get_segs<HT, D>(g, I, ppos, ptopk, s);
+    const int my_seq = seq++;
+    if (I.flags & F_HOLD) {
+      // warm L2 with (the start of) this instruction's data -- prefetches do
+      // not slow the consumers' release fences -- then wait until the
+      // consumers have finished every earlier instruction of this launch
+      if (lane == 0) {
+        unsigned long long left = g.hold_prefetch;
+        for (int k = 0; k < nseg && left; k++)
+          for (uint32_t u0 = 0; u0 < s[k].n && left; u0 += s[k].ups) {
+            const uint32_t b = min(s[k].ups, s[k].n - u0) * s[k].unit;
+            bulk_prefetch_l2(s[k].src + (size_t)u0 * s[k].unit, b);
+            if (s[k].src2) bulk_prefetch_l2(s[k].src2 + (size_t)u0 * s[k].unit, b);
+            left = left > b ? left - b : 0;
+          }
+      }
+      int bad = 0;
+      if (lane == 0) {
+        const uint64_t t0 = gtimer();
+        for (uint32_t it = 1; *(volatile int*)done < my_seq; it++) {
+          if ((it & 63) == 0) {
+            if (peek_err(g)) { bad = 1; break; }
+            if (gtimer() - t0 > g.timeout_ns) {
+              set_err(g, MK_ERR_TIMEOUT, pc, I.op);
+              bad = 1;
+              break;
+            }
+          }
+        }
+      }
+      if (__shfl_sync(0xFFFFFFFFu, bad, 0)) goto drain;
+    }
     for (int k = 0; k < nseg; k++) {
       for (uint32_t u0 = 0; u0 < s[k].n; u0 += s[k].ups) {
         const uint32_t n = min(s[k].ups, s[k].n - u0);
@@ -1253,11 +1285,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *flag = 0;
+    misc[1] = 0;  // instructions the consumers have finished (read by the producer)
   }
   __syncthreads();
 
   if (warp == NCW) {
-    producer<HT, D, HPG, NB>(g, smem + Ls.ring, full0, empty0, ppos, ptopk, ptopw, lane);
+    producer<HT, D, HPG, NB>(g, smem + Ls.ring, full0, empty0, ppos, ptopk, ptopw, misc + 1,
+                             lane);
     return;
   }
 
@@ -1301,6 +1335,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
   c.tm[0] = c.tm[1] = 0;
   consumer_bar();  // everyone has read *flag before it is reused below
 
+  int finished = 0;
   Instr next = load_instr(g, blockIdx.x, 0);
   for (int pc = 0; pc < g.max_pc; pc++) {
     const Instr I = next;
@@ -1334,6 +1369,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
         t[5] = gtimer();
       }
       if (I.sig_ctr != NO_CTR) red_release(g.ctr + I.sig_ctr, 1u);
+      *(volatile int*)(misc + 1) = ++finished;
     }
   }
 }

@@ -43,7 +43,19 @@ enum Flag : uint8_t {
   F_RESIDUAL = 1,    // this instruction also adds the residual input for its rows
   F_NORM_CACHED = 2, // the normalised input left in shared memory is still valid
   F_SHARED = 4,      // MoE MLP: shared-expert columns (weight 1, no routing)
+  F_HOLD = 8,        // producer: warm L2 with this instruction's data, then issue its ring
+                     // copies only after the consumers released every earlier instruction
 };
+
+// Which instructions the planner marks F_HOLD (first of a run of the op on
+// an SM).  A release fence drains the SM's bulk copies in flight, so an
+// instruction whose predecessor ends with a fence on the critical path does
+// better to fetch through L2 after that fence than to have its copies in
+// flight during it.
+enum HoldBit : unsigned {
+  HOLD_QKV = 1, HOLD_ATTN = 2, HOLD_OPROJ = 4, HOLD_MLP = 8, HOLD_DOWN = 16, HOLD_LM = 32,
+};
+constexpr unsigned DEFAULT_HOLD = HOLD_DOWN | HOLD_QKV | HOLD_LM;
 
 constexpr uint32_t NO_CTR = 0xFFFFFFFFu;
 
@@ -147,6 +159,7 @@ struct Globals {
   int pdl;                 // ablation with programmatic dependent launch
   unsigned long long* trace;  // optional [n_sm][max_pc][8] %globaltimer stamps (NULL: off)
   unsigned long long l2_ahead;  // bytes of the SM's stream warmed in L2 ahead of the ring (0: off)
+  unsigned hold_prefetch;       // bytes of a held instruction warmed in L2 before its copies
 };
 
 // Shared-memory layout (bytes from the dynamic shared memory base).
@@ -187,7 +200,8 @@ struct PlanOut {
   double max_sm_bytes = 0, mean_sm_bytes = 0, weight_bytes = 0;
 };
 int plan_shape_ok(const mk_model_desc& d);
-int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& out);
+int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& out,
+               unsigned hold_mask = DEFAULT_HOLD);
 int plan_verify(const mk_model_desc& d, int B, const PlanOut& p);
 int plan_check(const Instr* q, int n_sm, int max_pc, int n_ctr);
 

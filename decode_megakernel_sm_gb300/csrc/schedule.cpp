@@ -41,7 +41,8 @@ int plan_shape_ok(const mk_model_desc& d) {
   return MK_OK;
 }
 
-int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& out) {
+int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& out,
+               unsigned hold_mask) {
   int rc = plan_shape_ok(d);
   if (rc) return rc;
   if (B <= 0 || B > d.max_batch || max_ctx <= 0 || max_ctx > d.max_seq || n_sm <= 0)
@@ -285,6 +286,24 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
     qs[i].push_back(I);
     bytes[i] += (double)(b - a) * H * 2;
   }
+
+  // ---- hold marks: the first instruction of each run of a held op on an SM
+  auto hold_bit = [](uint8_t op) -> unsigned {
+    switch (op) {
+      case OP_QKV: return HOLD_QKV;
+      case OP_ATTN: return HOLD_ATTN;
+      case OP_OPROJ: return HOLD_OPROJ;
+      case OP_MLP: case OP_MLP_UP: case OP_ROUTER: return HOLD_MLP;
+      case OP_MLP_DOWN: return HOLD_DOWN;
+      case OP_LMHEAD: return HOLD_LM;
+      default: return 0;
+    }
+  };
+  for (auto& q : qs)
+    for (size_t k = 1; k < q.size(); k++)
+      if ((hold_mask & hold_bit(q[k].op)) &&
+          (q[k - 1].op != q[k].op || q[k - 1].layer != q[k].layer))
+        q[k].flags |= F_HOLD;
 
   // ---- counter targets: a wait is for every signal of its counter
   const int n_ctr = cm.count();

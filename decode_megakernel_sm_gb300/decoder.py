@@ -87,6 +87,10 @@ class Decoder:
         """Takes effect at the next build_schedule."""
         L.mk_set_residual_copies(self.h, copies)
 
+    def set_hold_policy(self, mask: int, prefetch_bytes: int = 256 << 10):
+        """Takes effect at the next build_schedule."""
+        L.mk_set_hold_policy(self.h, mask, prefetch_bytes)
+
     def set_l2_prefetch(self, bytes_ahead: int):
         L.mk_set_l2_prefetch(self.h, bytes_ahead)
 
