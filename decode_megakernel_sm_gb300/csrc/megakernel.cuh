@@ -1326,7 +1326,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
   c.pos = pos;
   c.topk = topk;
   c.topw = topw;
-  c.ring = Ring{smem + Ls.ring, full0, empty0, g.n_stages, 0, 0u};
+  c.ring = Ring{smem + Ls.ring, full0, empty0, g.n_stages, 0, 0u, 0ull, g.trace != nullptr};
   c.tid = tid;
   c.warp = warp;
   c.lane = lane;
@@ -1367,6 +1367,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
         t[3] = c.tm[0];
         t[4] = c.tm[1];
         t[5] = gtimer();
+        t[6] = c.ring.waited;  // warp 0's time blocked on ring data during this instruction
+        c.ring.waited = 0;
       }
       if (I.sig_ctr != NO_CTR) red_release(g.ctr + I.sig_ctr, 1u);
       *(volatile int*)(misc + 1) = ++finished;

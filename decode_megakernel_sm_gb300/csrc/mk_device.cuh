@@ -199,11 +199,20 @@ struct Ring {
   int ns;
   int st;
   uint32_t par;
+  unsigned long long waited;  // ns spent blocked in acquire (measured only when tracing)
+  bool timed;
 
   MK_DEV const unsigned char* stage_ptr() const { return base + (size_t)st * STAGE_BYTES; }
   // All 32 lanes call; the result is the same on every lane.
   MK_DEV bool acquire(const Globals& g) {
-    const bool ok = wait_mbar(g, full0 + 8u * st, par, true);
+    bool ok;
+    if (timed && !mbar_try(full0 + 8u * st, par)) {
+      const uint64_t t0 = gtimer();
+      ok = wait_mbar(g, full0 + 8u * st, par, true);
+      waited += gtimer() - t0;
+    } else {
+      ok = wait_mbar(g, full0 + 8u * st, par, true);
+    }
     return __all_sync(0xFFFFFFFFu, ok);
   }
   // All 32 lanes call; lane 0 arrives for the warp.

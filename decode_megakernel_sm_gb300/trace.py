@@ -31,7 +31,7 @@ def _rows(trace, queues, n_sm, max_pc):
                 continue
             m0 = ts[3] if ts[3] >= ts[2] else ts[2]
             m1 = ts[4] if ts[4] >= m0 else m0
-            rows.append((s, pc, I.op, I.layer, ts[0], ts[1], ts[2], ts[5], m0, m1))
+            rows.append((s, pc, I.op, I.layer, ts[0], ts[1], ts[2], ts[5], m0, m1, ts[6]))
             base = ts[1] if base is None else min(base, ts[1])
     return rows, base
 
@@ -42,10 +42,12 @@ def summarize(trace, queues, n_sm: int, max_pc: int) -> dict:
         return {}
     end = max(r[7] for r in rows)
     by_op = {}
-    for s, pc, op, layer, tp, tw0, tw1, te, m0, m1 in rows:
+    for s, pc, op, layer, tp, tw0, tw1, te, m0, m1, rw in rows:
         d = by_op.setdefault(L.OP_NAMES[op], {"n": 0, "wait_us": 0.0, "body_us": 0.0,
                                                "max_wait_us": 0.0, "prologue_us": 0.0,
-                                               "ring_us": 0.0, "epilogue_us": 0.0})
+                                               "ring_us": 0.0, "epilogue_us": 0.0,
+                                               "ring_data_wait_us": 0.0})
+        d["ring_data_wait_us"] += rw / 1e3
         d["n"] += 1
         d["wait_us"] += (tw1 - tw0) / 1e3
         d["body_us"] += (te - tw1) / 1e3
@@ -54,11 +56,11 @@ def summarize(trace, queues, n_sm: int, max_pc: int) -> dict:
         d["epilogue_us"] += (te - m1) / 1e3
         d["max_wait_us"] = max(d["max_wait_us"], (tw1 - tw0) / 1e3)
     for d in by_op.values():
-        for k in ("wait", "body", "prologue", "ring", "epilogue"):
+        for k in ("wait", "body", "prologue", "ring", "epilogue", "ring_data_wait"):
             d[f"mean_{k}_us"] = d[f"{k}_us"] / d["n"]
     # per layer and phase: when the last instruction of the phase finished
     phase_end = {}
-    for s, pc, op, layer, tp, tw0, tw1, te, m0, m1 in rows:
+    for s, pc, op, layer, tp, tw0, tw1, te, m0, m1, rw in rows:
         k = (layer, L.OP_NAMES[op])
         phase_end[k] = max(phase_end.get(k, 0), te - base)
     layers = sorted({k[0] for k in phase_end})
@@ -72,7 +74,7 @@ def summarize(trace, queues, n_sm: int, max_pc: int) -> dict:
         prev = e
     busy = np.zeros(n_sm)
     waited = np.zeros(n_sm)
-    for s, pc, op, layer, tp, tw0, tw1, te, m0, m1 in rows:
+    for s, pc, op, layer, tp, tw0, tw1, te, m0, m1, rw in rows:
         busy[s] += te - tw1
         waited[s] += tw1 - tw0
     return {"step_us": (end - base) / 1e3, "by_op": by_op, "per_layer": per_layer,
@@ -83,7 +85,7 @@ def summarize(trace, queues, n_sm: int, max_pc: int) -> dict:
 def chrome_trace(trace, queues, n_sm: int, max_pc: int, path: str):
     rows, base = _rows(trace, queues, n_sm, max_pc)
     ev = []
-    for s, pc, op, layer, tp, tw0, tw1, te, m0, m1 in rows:
+    for s, pc, op, layer, tp, tw0, tw1, te, m0, m1, rw in rows:
         name = f"{L.OP_NAMES[op]} L{layer}"
         ev.append({"name": "wait " + name, "ph": "X", "pid": 0, "tid": s,
                    "ts": (tw0 - base) / 1e3, "dur": (tw1 - tw0) / 1e3})
