@@ -89,7 +89,7 @@ struct CtrMap {
 };
 
 // Kernel-shape constants.
-constexpr int NCW = 8;               // consumer warps
+constexpr int NCW = 7;               // consumer warps (8 warps per CTA: two per scheduler partition, 255 registers)
 constexpr int NCT = NCW * 32;        // consumer threads
 constexpr int NTHREADS = NCT + 32;   // + one producer warp
 constexpr int STAGE_BYTES = 16384;   // bytes per ring stage
