@@ -206,7 +206,7 @@ struct Ring {
   // All 32 lanes call; the result is the same on every lane.
   MK_DEV bool acquire(const Globals& g) {
     bool ok;
-    if (timed && !mbar_try(full0 + 8u * st, par)) {
+    if (timed) {  // try_wait itself may suspend the thread, so time the whole wait
       const uint64_t t0 = gtimer();
       ok = wait_mbar(g, full0 + 8u * st, par, true);
       waited += gtimer() - t0;
