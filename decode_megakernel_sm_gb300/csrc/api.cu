@@ -212,7 +212,7 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
 
   // ---- packed weight buffer
   const LayerSizes ls = layer_sizes(d);
-  const size_t V = d.vocab, Vp = (V + 15) / 16 * 16;
+  const size_t V = d.vocab, Vp = (V + 7) / 8 * 8;
   size_t per_layer = 0;
   for (size_t e : {ls.norm, ls.norm, ls.qkv, ls.wo, ls.gu, ls.dT, ls.router, ls.ex_gu, ls.ex_dT,
                    ls.sh_gu, ls.sh_dT})
@@ -432,7 +432,7 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.D = d.head_dim;
   g.F = d.ffn;
   g.V = d.vocab;
-  g.Vp = (d.vocab + 15) / 16 * 16;
+  g.Vp = (d.vocab + 7) / 8 * 8;
   g.L = d.n_layers;
   g.max_seq = d.max_seq;
   g.max_ctx = h->max_ctx;

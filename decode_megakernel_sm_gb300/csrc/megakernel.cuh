@@ -86,12 +86,12 @@ template <int HT, int D>
 MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int* topk, Seg* s) {
   constexpr uint32_t ROW = HT * 2;
   constexpr uint32_t RPS = STAGE_BYTES / ROW;
-  // tiled GEMV matrices: units are tiles of 16 rows x KG columns
-  constexpr int KG = HT < 512 ? HT : 512, NKG = HT / KG;
-  constexpr uint32_t TE = TILE_ROWS * KG, TB = 2 * TE, TPS = STAGE_BYTES / TB;
+  // tiled GEMV matrices: units are tiles of 8 rows x KG columns
+  constexpr int KG = HT < 1024 ? HT : 1024, NKG = HT / KG;
+  constexpr uint32_t TE = 8 * KG, TB = 2 * TE, TPS = STAGE_BYTES / TB;
   auto tiles = [&](const uint16_t* base, uint32_t row0, uint32_t rows) -> Seg {
-    return Seg{(const unsigned char*)(base + (size_t)(row0 / TILE_ROWS) * NKG * TE), nullptr, TB,
-               rows / TILE_ROWS * NKG, TPS};
+    return Seg{(const unsigned char*)(base + (size_t)(row0 / 8) * NKG * TE), nullptr, TB,
+               rows / 8 * NKG, TPS};
   };
   const LayerPtrs* Lp = g.layers + (I.op == OP_LMHEAD ? 0 : I.layer);
   const uint32_t n = I.r1 - I.r0;
@@ -290,54 +290,45 @@ MK_DEV void norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const No
 
 // ----------------------------------------------------------------- GEMV ----
 // y[b][row] = W[row] . xn[b] on the tensor cores: mma.sync m16n8k16 with
-//   A = 16 weight rows x 16 columns of a tile, loaded with ldmatrix.x4,
-//   B = the activation: batch 1 -- column 0 its bf16-high part, column 1 its
-//       bf16-low remainder (so the product keeps ~16 bits of xn); batch > 1
-//       -- column g sequence g, once with the high parts and once (a second
-//       MMA into the same accumulators) with the low remainders,
-// so D[row][0] + D[row][1] (batch 1) or D[row][g] (batch > 1) = y.  Each warp
-// owns a fixed set of k-steps of every K group; its B fragments stay in
-// registers for the whole instruction; the warps' per-tile partial sums meet
-// in shared memory (yrow, zeroed by the op before its dependency wait).
-template <int HT, int NB>
-struct BFrag {
-  static constexpr int KG = HT < 512 ? HT : 512;
+//   A = the activation, rows g = bf16-high part of sequence g, rows g + 8 =
+//       its bf16-low remainder (so the product keeps ~16 bits of xn),
+//   B = 8 weight rows x 16 columns of a tile, loaded with ldmatrix,
+// D[g][n] + D[g+8][n] = y[g][row n].  Each warp owns a fixed set of k-steps
+// of every K group, its A fragments stay in registers for the whole
+// instruction; per-tile partial sums of the warps meet in shared memory
+// (yrow, zeroed by the op before its dependency wait).
+template <int HT>
+struct AFrag {
+  static constexpr int KG = HT < 1024 ? HT : 1024;
   static constexpr int NKG = HT / KG;
   static constexpr int KSTEPS = KG / 16;
   static constexpr int SLOTS = (KSTEPS + NCW - 1) / NCW;
-  static constexpr int NR = NB > 1 ? 4 : 2;  // registers per k-step
-  uint32_t b[NKG][SLOTS][NR];
+  uint32_t a[NKG][SLOTS][4];
 };
 
 template <int HT, int NB>
-MK_DEV void build_bfrag(BFrag<HT, NB>& f, const float* xn, int B, int warp, int lane) {
-  using F = BFrag<HT, NB>;
+MK_DEV void build_afrag(AFrag<HT>& f, const float* xn, int B, int warp, int lane) {
+  using F = AFrag<HT>;
   const int gq = lane >> 2, t = lane & 3;
+  const bool live = gq < NB && gq < B;
 #pragma unroll
   for (int kk = 0; kk < F::NKG; kk++)
 #pragma unroll
     for (int sl = 0; sl < F::SLOTS; sl++) {
       const int ks = warp + sl * NCW;
-#pragma unroll
-      for (int r = 0; r < F::NR; r++) f.b[kk][sl][r] = 0u;
-      const bool live = ks < F::KSTEPS && (NB == 1 ? gq < 2 : gq < B);
-      if (!live) continue;
-      const int seq = NB == 1 ? 0 : gq;
-      const float* x = xn + (size_t)seq * HT + kk * F::KG + ks * 16 + 2 * t;
-      uint16_t h0, l0, h1, l1, h8, l8, h9, l9;
-      split_bf16(x[0], h0, l0);
-      split_bf16(x[1], h1, l1);
-      split_bf16(x[8], h8, l8);
-      split_bf16(x[9], h9, l9);
-      if constexpr (NB == 1) {
-        const bool hi = gq == 0;  // column 0: high parts, column 1: low parts
-        f.b[kk][sl][0] = hi ? pack2(h0, h1) : pack2(l0, l1);
-        f.b[kk][sl][1] = hi ? pack2(h8, h9) : pack2(l8, l9);
+      if (live && ks < F::KSTEPS) {
+        const float* x = xn + (size_t)gq * HT + kk * F::KG + ks * 16 + 2 * t;
+        uint16_t h0, l0, h1, l1, h2, l2, h3, l3;
+        split_bf16(x[0], h0, l0);
+        split_bf16(x[1], h1, l1);
+        split_bf16(x[8], h2, l2);
+        split_bf16(x[9], h3, l3);
+        f.a[kk][sl][0] = pack2(h0, h1);
+        f.a[kk][sl][1] = pack2(l0, l1);
+        f.a[kk][sl][2] = pack2(h2, h3);
+        f.a[kk][sl][3] = pack2(l2, l3);
       } else {
-        f.b[kk][sl][0] = pack2(h0, h1);
-        f.b[kk][sl][1] = pack2(h8, h9);
-        f.b[kk][sl][2] = pack2(l0, l1);
-        f.b[kk][sl][3] = pack2(l8, l9);
+        f.a[kk][sl][0] = f.a[kk][sl][1] = f.a[kk][sl][2] = f.a[kk][sl][3] = 0u;
       }
     }
 }
@@ -354,15 +345,14 @@ MK_DEV void zero_yrow(Ctx<HT, D, HPG, NB>& c, int nrows) {
 // gave up.
 template <int HT, int D, int HPG, int NB>
 MK_DEV bool gemv_tiles(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s,
-                       const BFrag<HT, NB>& f) {
-  using F = BFrag<HT, NB>;
-  constexpr uint32_t TB = 2 * TILE_ROWS * F::KG;
+                       const AFrag<HT>& f) {
+  using F = AFrag<HT>;
+  constexpr uint32_t TB = 16 * F::KG;
   const int gq = c.lane >> 2, t = c.lane & 3;
-  // this lane's ldmatrix.x4 row within a k-step: matrices (rows 0-7 | 8-15)
-  // x (chunk 2ks | 2ks+1), 16 bytes per row, 16 rows per chunk
-  const uint32_t ld_off =
-      ((uint32_t)((c.lane >> 4) & 1) * 16u + (uint32_t)((c.lane >> 3) & 1) * 8u +
-       (uint32_t)(c.lane & 7)) * 16u;
+  const bool live = gq < NB && gq < g.B;
+  // this lane's ldmatrix row within a k-step: chunk 2ks (lanes 0-7) or 2ks+1
+  // (lanes 8-15), row lane % 8; a chunk of 8 rows is 128 bytes
+  const uint32_t ld_off = ((uint32_t)((c.lane >> 3) & 1) * 8u + (uint32_t)(c.lane & 7)) * 16u;
   for (uint32_t u0 = 0; u0 < s.n; u0 += s.ups) {
     const uint32_t n = min(s.ups, s.n - u0);
     if (!c.ring.acquire(g)) return false;
@@ -378,49 +368,27 @@ MK_DEV bool gemv_tiles(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s,
 #pragma unroll
       for (int kk = 0; kk < F::NKG; kk++) {
         if ((uint32_t)kk != kg) continue;
-        uint32_t a[F::SLOTS][4];
+        uint32_t b[F::SLOTS][2];
 #pragma unroll
         for (int sl = 0; sl < F::SLOTS; sl++) {
           const int ks = c.warp + sl * NCW;
-          if (ks < F::KSTEPS) {
-            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(a[sl][0]), "=r"(a[sl][1]), "=r"(a[sl][2]), "=r"(a[sl][3])
-                         : "r"(tile + (uint32_t)ks * 512u + ld_off));
-          }
+          if (ks < F::KSTEPS) ldmatrix_x2(tile + (uint32_t)ks * 256u + ld_off, b[sl][0], b[sl][1]);
         }
 #pragma unroll
         for (int sl = 0; sl < F::SLOTS; sl++) {
           const int ks = c.warp + sl * NCW;
-          if (ks < F::KSTEPS) {
-            float* dq = d[sl & 3];
-            mma_bf16_16816(dq[0], dq[1], dq[2], dq[3], a[sl][0], a[sl][1], a[sl][2], a[sl][3],
-                           f.b[kk][sl][0], f.b[kk][sl][1]);
-            if constexpr (NB > 1)
-              mma_bf16_16816(dq[0], dq[1], dq[2], dq[3], a[sl][0], a[sl][1], a[sl][2], a[sl][3],
-                             f.b[kk][sl][2], f.b[kk][sl][3]);
-          }
+          if (ks < F::KSTEPS)
+            mma_bf16_16816(d[sl & 3][0], d[sl & 3][1], d[sl & 3][2], d[sl & 3][3],
+                           f.a[kk][sl][0], f.a[kk][sl][1], f.a[kk][sl][2], f.a[kk][sl][3],
+                           b[sl][0], b[sl][1]);
         }
       }
-      float v[4];
-#pragma unroll
-      for (int e = 0; e < 4; e++) v[e] = (d[0][e] + d[1][e]) + (d[2][e] + d[3][e]);
-      float* y = c.yrow + rb * TILE_ROWS + gq;
-      if constexpr (NB == 1) {
-        // D[row g][0] + D[row g][1] on the lanes with t == 0
-        if (t == 0) {
-          atomicAdd(y, v[0] + v[1]);
-          atomicAdd(y + 8, v[2] + v[3]);
-        }
-      } else {
-        // D[row][seq 2t], D[row][seq 2t + 1] for rows g and g + 8
-        if (2 * t < g.B) {
-          atomicAdd(y + (2 * t) * MAX_ROWS, v[0]);
-          atomicAdd(y + (2 * t) * MAX_ROWS + 8, v[2]);
-        }
-        if (2 * t + 1 < g.B) {
-          atomicAdd(y + (2 * t + 1) * MAX_ROWS, v[1]);
-          atomicAdd(y + (2 * t + 1) * MAX_ROWS + 8, v[3]);
-        }
+      if (live) {
+        float* y = c.yrow + gq * MAX_ROWS + rb * 8 + 2 * t;
+        atomicAdd(y, (d[0][0] + d[1][0]) + (d[2][0] + d[3][0]) + (d[0][2] + d[1][2]) +
+                         (d[2][2] + d[3][2]));
+        atomicAdd(y + 1, (d[0][1] + d[1][1]) + (d[2][1] + d[3][1]) + (d[0][3] + d[1][3]) +
+                             (d[2][3] + d[3][3]));
       }
     }
     c.ring.release(c.lane);
@@ -463,8 +431,8 @@ MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   if (!dep_wait(c, g, I)) return false;
   if (!cached) norm_apply(c, g, 2 * I.layer, ng);
   c.mark(g, 0);
-  BFrag<HT, NB> f;
-  build_bfrag<HT, NB>(f, c.xn, g.B, c.warp, c.lane);
+  AFrag<HT> f;
+  build_afrag<HT, NB>(f, c.xn, g.B, c.warp, c.lane);
   Seg s[2];
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
   gemv_tiles(c, g, s[0], f);
@@ -771,8 +739,8 @@ MK_DEV bool op_router(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   zero_yrow(c, nr);
   if (!dep_wait(c, g, I)) return false;
   norm_apply(c, g, 2 * I.layer + 1, ng);
-  BFrag<HT, NB> f;
-  build_bfrag<HT, NB>(f, c.xn, g.B, c.warp, c.lane);
+  AFrag<HT> f;
+  build_afrag<HT, NB>(f, c.xn, g.B, c.warp, c.lane);
   Seg s[2];
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
   gemv_tiles(c, g, s[0], f);
@@ -811,8 +779,8 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
     consumer_bar();
   }
   const float scale = routed ? c.topw[I.g] : 1.f;
-  BFrag<HT, NB> f;
-  build_bfrag<HT, NB>(f, c.xn, g.B, c.warp, c.lane);
+  AFrag<HT> f;
+  build_afrag<HT, NB>(f, c.xn, g.B, c.warp, c.lane);
   Seg s[2];
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
   gemv_tiles(c, g, s[0], f);
@@ -895,8 +863,8 @@ MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   if (!dep_wait(c, g, I)) return false;
   if (!cached) norm_apply(c, g, 2 * l + 1, ng);
   c.mark(g, 0);
-  BFrag<HT, NB> f;
-  build_bfrag<HT, NB>(f, c.xn, g.B, c.warp, c.lane);
+  AFrag<HT> f;
+  build_afrag<HT, NB>(f, c.xn, g.B, c.warp, c.lane);
   Seg s[2];
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
   gemv_tiles(c, g, s[0], f);
@@ -997,8 +965,8 @@ MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   if (!dep_wait(c, g, I)) return false;
   if (!cached) norm_apply(c, g, 2 * g.L, ng);
   c.mark(g, 0);
-  BFrag<HT, NB> f;
-  build_bfrag<HT, NB>(f, c.xn, g.B, c.warp, c.lane);
+  AFrag<HT> f;
+  build_afrag<HT, NB>(f, c.xn, g.B, c.warp, c.lane);
   Seg s[2];
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
   gemv_tiles(c, g, s[0], f);

@@ -106,17 +106,16 @@ inline bool mlp_split(const mk_model_desc& d) {
 }
 
 // Tiled layout of the matrices the GEMV streams (QKV, gate/up, router, LM
-// head): tiles of 16 rows x KG columns, KG = min(K, 512) so that one tile is
+// head): tiles of 8 rows x KG columns, KG = min(K, 1024) so that one tile is
 // at most one 16 KiB ring stage; tiles run row block major, then K group;
-// inside a tile the 16-byte chunks run chunk major, then row, so rows 0-7
-// and rows 8-15 of one chunk are each 128 contiguous bytes (conflict-free
-// ldmatrix 8x8 matrices).  Element (row, col) of an R x K matrix sits at
-//   ((row/16 * (K/KG) + col/KG) * 16 * KG) + ((col%KG)/8 * 16 + row%16) * 8 + col%8.
-constexpr int TILE_ROWS = 16;
-MK_HD inline int tile_kg(int K) { return K < 512 ? K : 512; }
+// inside a tile the 16-byte chunks run chunk major, then row, so the eight
+// rows of one chunk are 128 contiguous bytes (one conflict-free ldmatrix
+// 8x8 matrix).  Element (row, col) of an R x K matrix sits at
+//   ((row/8 * (K/KG) + col/KG) * 8 * KG) + ((col%KG)/8 * 8 + row%8) * 8 + col%8.
+MK_HD inline int tile_kg(int K) { return K < 1024 ? K : 1024; }
 MK_HD inline size_t tiled_offset(size_t row, size_t col, int K) {
   const size_t kg = (size_t)tile_kg(K), nkg = (size_t)K / kg;
-  return ((row / 16) * nkg + col / kg) * 16 * kg + ((col % kg) / 8 * 16 + row % 16) * 8 + col % 8;
+  return ((row / 8) * nkg + col / kg) * 8 * kg + ((col % kg) / 8 * 8 + row % 8) * 8 + col % 8;
 }
 
 // Device pointers of one layer inside the packed weight buffer.
@@ -141,7 +140,7 @@ struct Globals {
   const Instr* sched;
   const LayerPtrs* layers;
   const uint16_t* embed;     // the tiled LM head when tied, else tiled [Vp][H]
-  const uint16_t* lm_head;   // tiled [Vp][H], Vp = vocab rounded up to 16 (zero rows)
+  const uint16_t* lm_head;   // tiled [Vp][H], Vp = vocab rounded up to 8 (zero rows)
   const uint16_t* final_norm;
   const float* rope;       // [max_seq][D/2][2] (cos, sin)
   float* xbuf;             // [2][2L][kc][B][H] residual stream x_1 .. x_2L, kc partial copies
@@ -161,7 +160,7 @@ struct Globals {
   unsigned long long timeout_ns;
   int max_pc, n_sm, n_stages;
   int B, H, Hq, Hkv, D, F, V, L, max_seq, max_ctx, splits;
-  int Vp;                  // LM-head rows rounded up to 16 (tiled layout)
+  int Vp;                  // LM-head rows rounded up to 8 (tiled layout)
   int E, K, Fe, Fs;
   int kc;                  // partial copies of each residual vector (1..8)
   float eps;
