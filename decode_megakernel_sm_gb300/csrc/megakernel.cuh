@@ -361,34 +361,25 @@ MK_DEV bool gemv_tiles(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s,
       const uint32_t T = u0 + j;
       const uint32_t rb = T / F::NKG, kg = T % F::NKG;
       const uint32_t tile = st + j * TB;
-      // four independent accumulator sets keep the MMA chain short
-      float d[4][4];
-#pragma unroll
-      for (int q = 0; q < 4; q++) d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.f;
+      float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
 #pragma unroll
       for (int kk = 0; kk < F::NKG; kk++) {
         if ((uint32_t)kk != kg) continue;
-        uint32_t b[F::SLOTS][2];
 #pragma unroll
         for (int sl = 0; sl < F::SLOTS; sl++) {
           const int ks = c.warp + sl * NCW;
-          if (ks < F::KSTEPS) ldmatrix_x2(tile + (uint32_t)ks * 256u + ld_off, b[sl][0], b[sl][1]);
-        }
-#pragma unroll
-        for (int sl = 0; sl < F::SLOTS; sl++) {
-          const int ks = c.warp + sl * NCW;
-          if (ks < F::KSTEPS)
-            mma_bf16_16816(d[sl & 3][0], d[sl & 3][1], d[sl & 3][2], d[sl & 3][3],
-                           f.a[kk][sl][0], f.a[kk][sl][1], f.a[kk][sl][2], f.a[kk][sl][3],
-                           b[sl][0], b[sl][1]);
+          if (ks < F::KSTEPS) {
+            uint32_t b0, b1;
+            ldmatrix_x2(tile + (uint32_t)ks * 256u + ld_off, b0, b1);
+            mma_bf16_16816(d0, d1, d2, d3, f.a[kk][sl][0], f.a[kk][sl][1], f.a[kk][sl][2],
+                           f.a[kk][sl][3], b0, b1);
+          }
         }
       }
       if (live) {
         float* y = c.yrow + gq * MAX_ROWS + rb * 8 + 2 * t;
-        atomicAdd(y, (d[0][0] + d[1][0]) + (d[2][0] + d[3][0]) + (d[0][2] + d[1][2]) +
-                         (d[2][2] + d[3][2]));
-        atomicAdd(y + 1, (d[0][1] + d[1][1]) + (d[2][1] + d[3][1]) + (d[0][3] + d[1][3]) +
-                             (d[2][3] + d[3][3]));
+        atomicAdd(y, d0 + d2);
+        atomicAdd(y + 1, d1 + d3);
       }
     }
     c.ring.release(c.lane);
