@@ -3,7 +3,6 @@
 // host-buffer step, the per-phase ablation launcher and error reporting.
 #include <cuda_runtime.h>
 
-#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <map>
@@ -22,8 +21,6 @@ cudaError_t pack_interleave(uint16_t* dst, const void* a, const void* b, long ro
 cudaError_t pack_wo(uint16_t* dst, const void* wo, int H, int Hq, int D, cudaStream_t s);
 cudaError_t pack_transpose(uint16_t* dst, const void* src, int R, int C, int batch,
                            cudaStream_t s);
-cudaError_t pack_retile(uint16_t* dst, const void* src, int R, int Rp, int K, int batch,
-                        cudaStream_t s);
 
 extern const Variant variant_h256_d64_g2_b1;
 extern const Variant variant_h2048_d64_g4_b1;
@@ -40,7 +37,6 @@ struct mk_handle {
   int n_stages = 0, smem_bytes = 0;
   void* packed = nullptr;
   size_t packed_bytes = 0;
-  void* pack_tmp = nullptr;  // row-major staging while packing (freed by mk_create)
   std::vector<LayerPtrs> layers_h;
   LayerPtrs* layers_d = nullptr;
   const uint16_t *embed = nullptr, *lm_head = nullptr, *final_norm = nullptr;
@@ -120,7 +116,6 @@ static void free_all(mk_handle* h) {
   if (!h) return;
   free_schedule(h);
   if (h->packed) cudaFree(h->packed);
-  if (h->pack_tmp) cudaFree(h->pack_tmp);
   if (h->layers_d) cudaFree(h->layers_d);
   if (h->rope) cudaFree(h->rope);
   if (h->h_err) cudaFreeHost(h->h_err);
@@ -212,17 +207,13 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
 
   // ---- packed weight buffer
   const LayerSizes ls = layer_sizes(d);
-  const size_t V = d.vocab, Vp = (V + 7) / 8 * 8;
+  const size_t V = d.vocab;
   size_t per_layer = 0;
   for (size_t e : {ls.norm, ls.norm, ls.qkv, ls.wo, ls.gu, ls.dT, ls.router, ls.ex_gu, ls.ex_dT,
                    ls.sh_gu, ls.sh_dT})
     per_layer += al256(e * 2);
-  const size_t total = per_layer * L + al256(Vp * H * 2) * (d.tied_lm_head ? 1 : 2) + al256(H * 2);
+  const size_t total = per_layer * L + al256(V * H * 2) * (d.tied_lm_head ? 1 : 2) + al256(H * 2);
   CK(cudaMalloc(&h->packed, total));
-  // GEMV matrices are assembled row-major in a staging buffer, then retiled
-  size_t tmp_elems = std::max(ls.qkv, std::max(ls.gu, std::max(ls.ex_gu, ls.sh_gu)));
-  CK(cudaMalloc(&h->pack_tmp, tmp_elems * 2));
-  uint16_t* tmp = (uint16_t*)h->pack_tmp;
   h->packed_bytes = total;
   char* p = (char*)h->packed;
   auto take = [&](size_t elems) {
@@ -248,26 +239,21 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
     uint16_t* sdT = take(ls.sh_dT);
     CK(cudaMemcpyAsync(an, w->attn_norm[l], ls.norm * 2, cudaMemcpyDeviceToDevice, s));
     CK(cudaMemcpyAsync(mn, w->mlp_norm[l], ls.norm * 2, cudaMemcpyDeviceToDevice, s));
-    const int R = Hkv * (HPG + 2) * D;
-    CK(pack_qkv(tmp, w->wq[l], w->wk[l], w->wv[l], H, Hkv, HPG, D, s));
-    CK(pack_retile(qkv, tmp, R, R, H, 1, s));
+    CK(pack_qkv(qkv, w->wq[l], w->wk[l], w->wv[l], H, Hkv, HPG, D, s));
     CK(pack_wo(wo, w->wo[l], H, Hq, D, s));
     if (!moe) {
-      CK(pack_interleave(tmp, w->w_gate[l], w->w_up[l], d.ffn, H, s));
-      CK(pack_retile(gu, tmp, 2 * d.ffn, 2 * d.ffn, H, 1, s));
+      CK(pack_interleave(gu, w->w_gate[l], w->w_up[l], d.ffn, H, s));
       if (mlp_split(d))  // the down rows are streamed as they are
         CK(cudaMemcpyAsync(dT, w->w_down[l], ls.dT * 2, cudaMemcpyDeviceToDevice, s));
       else
         CK(pack_transpose(dT, w->w_down[l], H, d.ffn, 1, s));
     } else {
-      CK(pack_retile(rt, w->router[l], d.n_experts, d.n_experts, H, 1, s));
-      CK(pack_interleave(tmp, w->ex_gate[l], w->ex_up[l], (long)d.n_experts * d.expert_ffn, H,
+      CK(cudaMemcpyAsync(rt, w->router[l], ls.router * 2, cudaMemcpyDeviceToDevice, s));
+      CK(pack_interleave(egu, w->ex_gate[l], w->ex_up[l], (long)d.n_experts * d.expert_ffn, H,
                          s));
-      CK(pack_retile(egu, tmp, 2 * d.expert_ffn, 2 * d.expert_ffn, H, d.n_experts, s));
       CK(pack_transpose(edT, w->ex_down[l], H, d.expert_ffn, d.n_experts, s));
       if (d.shared_ffn > 0) {
-        CK(pack_interleave(tmp, w->sh_gate[l], w->sh_up[l], d.shared_ffn, H, s));
-        CK(pack_retile(sgu, tmp, 2 * d.shared_ffn, 2 * d.shared_ffn, H, 1, s));
+        CK(pack_interleave(sgu, w->sh_gate[l], w->sh_up[l], d.shared_ffn, H, s));
         CK(pack_transpose(sdT, w->sh_down[l], H, d.shared_ffn, 1, s));
       }
     }
@@ -285,14 +271,14 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
     lp.kc = (uint16_t*)kv->k[l];
     lp.vc = (uint16_t*)kv->v[l];
   }
-  uint16_t* emb = take(Vp * H);
-  CK(pack_retile(emb, w->embed, (int)V, (int)Vp, H, 1, s));
+  uint16_t* emb = take(V * H);
+  CK(cudaMemcpyAsync(emb, w->embed, V * H * 2, cudaMemcpyDeviceToDevice, s));
   h->embed = emb;
   if (d.tied_lm_head) {
     h->lm_head = emb;
   } else {
-    uint16_t* lm = take(Vp * H);
-    CK(pack_retile(lm, w->lm_head, (int)V, (int)Vp, H, 1, s));
+    uint16_t* lm = take(V * H);
+    CK(cudaMemcpyAsync(lm, w->lm_head, V * H * 2, cudaMemcpyDeviceToDevice, s));
     h->lm_head = lm;
   }
   uint16_t* fn = take(H);
@@ -313,8 +299,6 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
   CK(cudaMemcpyAsync(h->rope, rope.data(), rope.size() * sizeof(float), cudaMemcpyHostToDevice,
                      s));
   CK(cudaStreamSynchronize(s));
-  cudaFree(h->pack_tmp);
-  h->pack_tmp = nullptr;
   return MK_OK;
 }
 
@@ -432,7 +416,6 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.D = d.head_dim;
   g.F = d.ffn;
   g.V = d.vocab;
-  g.Vp = (d.vocab + 7) / 8 * 8;
   g.L = d.n_layers;
   g.max_seq = d.max_seq;
   g.max_ctx = h->max_ctx;

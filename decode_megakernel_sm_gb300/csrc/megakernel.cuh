@@ -86,48 +86,41 @@ template <int HT, int D>
 MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int* topk, Seg* s) {
   constexpr uint32_t ROW = HT * 2;
   constexpr uint32_t RPS = STAGE_BYTES / ROW;
-  // tiled GEMV matrices: units are tiles of 8 rows x KG columns
-  constexpr int KG = HT < 1024 ? HT : 1024, NKG = HT / KG;
-  constexpr uint32_t TE = 8 * KG, TB = 2 * TE, TPS = STAGE_BYTES / TB;
-  auto tiles = [&](const uint16_t* base, uint32_t row0, uint32_t rows) -> Seg {
-    return Seg{(const unsigned char*)(base + (size_t)(row0 / 8) * NKG * TE), nullptr, TB,
-               rows / 8 * NKG, TPS};
-  };
   const LayerPtrs* Lp = g.layers + (I.op == OP_LMHEAD ? 0 : I.layer);
   const uint32_t n = I.r1 - I.r0;
   switch (I.op) {
     case OP_QKV:
-      s[0] = tiles(Lp->wqkv, I.r0, n);
+      s[0] = {(const unsigned char*)(Lp->wqkv + (size_t)I.r0 * HT), nullptr, ROW, n, RPS};
       return 1;
     case OP_OPROJ:
       s[0] = {(const unsigned char*)(Lp->wo + ((size_t)I.g * HT + I.r0) * D), nullptr, D * 2, n,
               STAGE_BYTES / (D * 2)};
       return 1;
     case OP_ROUTER:
-      s[0] = tiles(Lp->router, I.r0, n);
+      s[0] = {(const unsigned char*)(Lp->router + (size_t)I.r0 * HT), nullptr, ROW, n, RPS};
       return 1;
     case OP_MLP: {
       const uint16_t *gu, *dT;
       if (g.E == 0) {
-        gu = Lp->wgu;
+        gu = Lp->wgu + (size_t)I.r0 * 2 * HT;
         dT = Lp->wdT + (size_t)I.r0 * HT;
       } else if (I.flags & F_SHARED) {
-        gu = Lp->sh_gu;
+        gu = Lp->sh_gu + (size_t)I.r0 * 2 * HT;
         dT = Lp->sh_dT + (size_t)I.r0 * HT;
       } else {
         const size_t e = (size_t)topk[I.g];
-        gu = Lp->ex_gu + e * 2 * g.Fe * HT;
+        gu = Lp->ex_gu + (e * g.Fe + I.r0) * 2 * HT;
         dT = Lp->ex_dT + (e * g.Fe + I.r0) * HT;
       }
-      s[0] = tiles(gu, 2 * I.r0, 2 * n);
+      s[0] = {(const unsigned char*)gu, nullptr, ROW, 2 * n, RPS};
       s[1] = {(const unsigned char*)dT, nullptr, ROW, n, RPS};
       return 2;
     }
     case OP_LMHEAD:
-      s[0] = tiles(g.lm_head, I.r0, n);
+      s[0] = {(const unsigned char*)(g.lm_head + (size_t)I.r0 * HT), nullptr, ROW, n, RPS};
       return 1;
     case OP_MLP_UP:
-      s[0] = tiles(Lp->wgu, 2 * I.r0, 2 * n);
+      s[0] = {(const unsigned char*)(Lp->wgu + (size_t)I.r0 * 2 * HT), nullptr, ROW, 2 * n, RPS};
       return 1;
     case OP_MLP_DOWN:  // rows of the row-major [H][F] down projection
       s[0] = {(const unsigned char*)(Lp->wdT + (size_t)I.r0 * g.F), nullptr, (uint32_t)g.F * 2, n,
@@ -231,8 +224,7 @@ MK_DEV void norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const No
       float v[8];
       if (b < g.B) {
         if (j == 0) {
-          const uint4 w =
-              __ldg((const uint4*)(g.embed + tiled_offset((size_t)c.tok[b], (size_t)gi * 8, HT)));
+          const uint4 w = __ldg((const uint4*)(g.embed + (size_t)c.tok[b] * HT) + gi);
           unpack8(w, v);
         } else {
 #pragma unroll
@@ -289,98 +281,77 @@ MK_DEV void norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const No
 }
 
 // ----------------------------------------------------------------- GEMV ----
-// y[b][row] = W[row] . xn[b] on the tensor cores: mma.sync m16n8k16 with
-//   A = the activation, rows g = bf16-high part of sequence g, rows g + 8 =
-//       its bf16-low remainder (so the product keeps ~16 bits of xn),
-//   B = 8 weight rows x 16 columns of a tile, loaded with ldmatrix,
-// D[g][n] + D[g+8][n] = y[g][row n].  Each warp owns a fixed set of k-steps
-// of every K group, its A fragments stay in registers for the whole
-// instruction; per-tile partial sums of the warps meet in shared memory
-// (yrow, zeroed by the op before its dependency wait).
+// Lane l of a warp owns columns {it*256 + l*8 + k}; for NB == 1 its slice of
+// xn lives in registers.
 template <int HT>
-struct AFrag {
-  static constexpr int KG = HT < 1024 ? HT : 1024;
-  static constexpr int NKG = HT / KG;
-  static constexpr int KSTEPS = KG / 16;
-  static constexpr int SLOTS = (KSTEPS + NCW - 1) / NCW;
-  uint32_t a[NKG][SLOTS][4];
-};
+MK_DEV void load_xr(const float* xn, int lane, float (&xr)[HT / 32]) {
+#pragma unroll
+  for (int it = 0; it < HT / 256; it++) {
+    const float4* p = (const float4*)(xn + it * 256 + lane * 8);
+    const float4 a = p[0], b = p[1];
+    xr[it * 8 + 0] = a.x; xr[it * 8 + 1] = a.y; xr[it * 8 + 2] = a.z; xr[it * 8 + 3] = a.w;
+    xr[it * 8 + 4] = b.x; xr[it * 8 + 5] = b.y; xr[it * 8 + 6] = b.z; xr[it * 8 + 7] = b.w;
+  }
+}
 
+// Partial dot of one bf16 row (in shared memory) with the activation(s); the
+// caller reduces across the warp.
 template <int HT, int NB>
-MK_DEV void build_afrag(AFrag<HT>& f, const float* xn, int B, int warp, int lane) {
-  using F = AFrag<HT>;
-  const int gq = lane >> 2, t = lane & 3;
-  const bool live = gq < NB && gq < B;
+MK_DEV void row_dot(const unsigned char* row, const float (&xr)[HT / 32], const float* xn,
+                    int lane, float (&acc)[NB]) {
+  const uint4* w4 = (const uint4*)row;
+  if constexpr (NB == 1) {
+    float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-  for (int kk = 0; kk < F::NKG; kk++)
+    for (int it = 0; it < HT / 256; it++) {
+      const uint4 w = w4[it * 32 + lane];
+      const float* x = xr + it * 8;
+      a0 = fmaf(bf_lo(w.x), x[0], a0); a1 = fmaf(bf_hi(w.x), x[1], a1);
+      a0 = fmaf(bf_lo(w.y), x[2], a0); a1 = fmaf(bf_hi(w.y), x[3], a1);
+      a0 = fmaf(bf_lo(w.z), x[4], a0); a1 = fmaf(bf_hi(w.z), x[5], a1);
+      a0 = fmaf(bf_lo(w.w), x[6], a0); a1 = fmaf(bf_hi(w.w), x[7], a1);
+    }
+    acc[0] = a0 + a1;
+  } else {
 #pragma unroll
-    for (int sl = 0; sl < F::SLOTS; sl++) {
-      const int ks = warp + sl * NCW;
-      if (live && ks < F::KSTEPS) {
-        const float* x = xn + (size_t)gq * HT + kk * F::KG + ks * 16 + 2 * t;
-        uint16_t h0, l0, h1, l1, h2, l2, h3, l3;
-        split_bf16(x[0], h0, l0);
-        split_bf16(x[1], h1, l1);
-        split_bf16(x[8], h2, l2);
-        split_bf16(x[9], h3, l3);
-        f.a[kk][sl][0] = pack2(h0, h1);
-        f.a[kk][sl][1] = pack2(l0, l1);
-        f.a[kk][sl][2] = pack2(h2, h3);
-        f.a[kk][sl][3] = pack2(l2, l3);
-      } else {
-        f.a[kk][sl][0] = f.a[kk][sl][1] = f.a[kk][sl][2] = f.a[kk][sl][3] = 0u;
+    for (int b = 0; b < NB; b++) acc[b] = 0.f;
+#pragma unroll 2
+    for (int it = 0; it < HT / 256; it++) {
+      float wf[8];
+      unpack8(w4[it * 32 + lane], wf);
+#pragma unroll
+      for (int b = 0; b < NB; b++) {
+        const float4* p = (const float4*)(xn + (size_t)b * HT + it * 256 + lane * 8);
+        const float4 x0 = p[0], x1 = p[1];
+        float a = acc[b];
+        a = fmaf(wf[0], x0.x, a); a = fmaf(wf[1], x0.y, a);
+        a = fmaf(wf[2], x0.z, a); a = fmaf(wf[3], x0.w, a);
+        a = fmaf(wf[4], x1.x, a); a = fmaf(wf[5], x1.y, a);
+        a = fmaf(wf[6], x1.z, a); a = fmaf(wf[7], x1.w, a);
+        acc[b] = a;
       }
     }
+  }
 }
 
-// Zero y rows [0, nrows) of every sequence slot (before the dependency wait,
-// whose barrier orders it before the accumulation).
-template <int HT, int D, int HPG, int NB>
-MK_DEV void zero_yrow(Ctx<HT, D, HPG, NB>& c, int nrows) {
-  for (int i = c.tid; i < NB * nrows; i += NCT) c.yrow[(i / nrows) * MAX_ROWS + i % nrows] = 0.f;
-}
-
-// Stream the tiles of one segment through the ring and accumulate
-// y[b][row - first row of the segment] into c.yrow.  Returns false if a wait
-// gave up.
-template <int HT, int D, int HPG, int NB>
-MK_DEV bool gemv_tiles(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s,
-                       const AFrag<HT>& f) {
-  using F = AFrag<HT>;
-  constexpr uint32_t TB = 16 * F::KG;
-  const int gq = c.lane >> 2, t = c.lane & 3;
-  const bool live = gq < NB && gq < g.B;
-  // this lane's ldmatrix row within a k-step: chunk 2ks (lanes 0-7) or 2ks+1
-  // (lanes 8-15), row lane % 8; a chunk of 8 rows is 128 bytes
-  const uint32_t ld_off = ((uint32_t)((c.lane >> 3) & 1) * 8u + (uint32_t)(c.lane & 7)) * 16u;
+// Stream the rows of one segment through the ring; warp w computes rows
+// w, w + NCW, ... of each stage and hands (row index, per-sequence dot) to
+// fn on every lane.  Returns false if a wait gave up.
+template <int HT, int D, int HPG, int NB, class Fn>
+MK_DEV bool gemv_rows(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s,
+                      const float (&xr)[HT / 32], Fn&& fn) {
   for (uint32_t u0 = 0; u0 < s.n; u0 += s.ups) {
     const uint32_t n = min(s.ups, s.n - u0);
     if (!c.ring.acquire(g)) return false;
-    const uint32_t st = smem_u32(c.ring.stage_ptr());
-    for (uint32_t j = 0; j < n; j++) {
-      const uint32_t T = u0 + j;
-      const uint32_t rb = T / F::NKG, kg = T % F::NKG;
-      const uint32_t tile = st + j * TB;
-      float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+    const unsigned char* st = c.ring.stage_ptr();
+    // segment row u0 + r goes to warp (u0 + r) mod NCW, so a short segment
+    // spreads its rows over all warps rather than over one stage's worth
+    for (uint32_t r = (uint32_t)(c.warp + NCW - (int)(u0 % NCW)) % NCW; r < n; r += NCW) {
+      float acc[NB];
+      row_dot<HT, NB>(st + (size_t)r * HT * 2, xr, c.xn, c.lane, acc);
 #pragma unroll
-      for (int kk = 0; kk < F::NKG; kk++) {
-        if ((uint32_t)kk != kg) continue;
-#pragma unroll
-        for (int sl = 0; sl < F::SLOTS; sl++) {
-          const int ks = c.warp + sl * NCW;
-          if (ks < F::KSTEPS) {
-            uint32_t b0, b1;
-            ldmatrix_x2(tile + (uint32_t)ks * 256u + ld_off, b0, b1);
-            mma_bf16_16816(d0, d1, d2, d3, f.a[kk][sl][0], f.a[kk][sl][1], f.a[kk][sl][2],
-                           f.a[kk][sl][3], b0, b1);
-          }
-        }
-      }
-      if (live) {
-        float* y = c.yrow + gq * MAX_ROWS + rb * 8 + 2 * t;
-        atomicAdd(y, d0 + d2);
-        atomicAdd(y + 1, d1 + d3);
-      }
+      for (int b = 0; b < NB; b++) acc[b] = warp_sum(acc[b]);
+      fn(u0 + r, acc);
     }
     c.ring.release(c.lane);
   }
@@ -418,18 +389,23 @@ MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
       for (int b = 0; b < NB; b++)
         if (b < g.B) cs[b] = ((const float2*)g.rope)[(size_t)c.pos[b] * (D / 2) + t];
   }
-  zero_yrow(c, (int)n);
   if (!dep_wait(c, g, I)) return false;
   if (!cached) norm_apply(c, g, 2 * I.layer, ng);
   c.mark(g, 0);
-  AFrag<HT> f;
-  build_afrag<HT, NB>(f, c.xn, g.B, c.warp, c.lane);
+  float xr[HT / 32];
+  if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
   Seg s[2];
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
-  gemv_tiles(c, g, s[0], f);
+  float* yrow = c.yrow;
+  const int lane = c.lane;
+  gemv_rows(c, g, s[0], xr, [&](uint32_t r, float(&acc)[NB]) {
+    if (lane == 0) {
+#pragma unroll
+      for (int b = 0; b < NB; b++) yrow[b * MAX_ROWS + r] = acc[b];
+    }
+  });
   c.mark(g, 1);
   consumer_bar();
-  const float* yrow = c.yrow;
   if (i < n) {
 #pragma unroll
     for (int b = 0; b < NB; b++) {
@@ -605,7 +581,7 @@ MK_DEV bool op_attn(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
 
 // Residual input x_j[b][r] (j = 0: the embedding row of the token).
 MK_DEV float x_in(const Globals& g, int j, const int* tok, int b, int r) {
-  if (j == 0) return bf1(g.embed[tiled_offset((size_t)tok[b], (size_t)r, g.H)]);
+  if (j == 0) return bf1(g.embed[(size_t)tok[b] * g.H + r]);
   return xres_sum(g, j, b, r);
 }
 
@@ -726,19 +702,19 @@ MK_DEV bool op_router(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   const LayerPtrs& Lp = g.layers[I.layer];
   NormGain<HT> ng;
   norm_gain(ng, Lp.mlp_norm, c.tid);
-  const int nr = (int)(I.r1 - I.r0);
-  zero_yrow(c, nr);
   if (!dep_wait(c, g, I)) return false;
   norm_apply(c, g, 2 * I.layer + 1, ng);
-  AFrag<HT> f;
-  build_afrag<HT, NB>(f, c.xn, g.B, c.warp, c.lane);
+  float xr[HT / 32];
+  if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
   Seg s[2];
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
-  gemv_tiles(c, g, s[0], f);
-  consumer_bar();
+  const int lane = c.lane, B = g.B;
   float* rl = g.rlog + (size_t)I.layer * g.B * g.E + I.r0;
-  for (int t = c.tid; t < g.B * nr; t += NCT)
-    rl[(size_t)(t / nr) * g.E + t % nr] = c.yrow[(t / nr) * MAX_ROWS + t % nr];
+  const int E = g.E;
+  gemv_rows(c, g, s[0], xr, [&](uint32_t r, float(&acc)[NB]) {
+    if (lane == 0)
+      for (int b = 0; b < B && b < NB; b++) rl[(size_t)b * E + r] = acc[b];
+  });
   consumer_bar();
   return true;
 }
@@ -757,7 +733,6 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   const bool cached = (I.flags & F_NORM_CACHED) != 0;
   NormGain<HT> ng;
   if (!cached) norm_gain(ng, Lp.mlp_norm, c.tid);
-  zero_yrow(c, 2 * (int)(I.r1 - I.r0));
   if (!dep_wait(c, g, I)) return false;
   if (!cached) norm_apply(c, g, 2 * l + 1, ng);
   c.mark(g, 0);
@@ -770,13 +745,19 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
     consumer_bar();
   }
   const float scale = routed ? c.topw[I.g] : 1.f;
-  AFrag<HT> f;
-  build_afrag<HT, NB>(f, c.xn, g.B, c.warp, c.lane);
+  float xr[HT / 32];
+  if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
   Seg s[2];
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
-  gemv_tiles(c, g, s[0], f);
+  float* yrow = c.yrow;
+  const int lane = c.lane;
+  gemv_rows(c, g, s[0], xr, [&](uint32_t r, float(&acc)[NB]) {
+    if (lane == 0) {
+#pragma unroll
+      for (int b = 0; b < NB; b++) yrow[b * MAX_ROWS + r] = acc[b];
+    }
+  });
   consumer_bar();
-  const float* yrow = c.yrow;
   const int ncol = (int)(I.r1 - I.r0);
   for (int t = c.tid; t < NB * ncol; t += NCT) {
     const int b = t / ncol, j = t % ncol;
@@ -850,18 +831,23 @@ MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   const bool cached = (I.flags & F_NORM_CACHED) != 0;
   NormGain<HT> ng;
   if (!cached) norm_gain(ng, Lp.mlp_norm, c.tid);
-  zero_yrow(c, 2 * (int)(I.r1 - I.r0));
   if (!dep_wait(c, g, I)) return false;
   if (!cached) norm_apply(c, g, 2 * l + 1, ng);
   c.mark(g, 0);
-  AFrag<HT> f;
-  build_afrag<HT, NB>(f, c.xn, g.B, c.warp, c.lane);
+  float xr[HT / 32];
+  if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
   Seg s[2];
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
-  gemv_tiles(c, g, s[0], f);
+  float* yrow = c.yrow;
+  const int lane = c.lane;
+  gemv_rows(c, g, s[0], xr, [&](uint32_t r, float(&acc)[NB]) {
+    if (lane == 0) {
+#pragma unroll
+      for (int b = 0; b < NB; b++) yrow[b * MAX_ROWS + r] = acc[b];
+    }
+  });
   c.mark(g, 1);
   consumer_bar();
-  const float* yrow = c.yrow;
   const int ncol = (int)(I.r1 - I.r0);
   for (int t = c.tid; t < NB * ncol; t += NCT) {
     const int b = t / ncol, j = t % ncol;
@@ -948,24 +934,15 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I
 // arrives last on the argmax counter reduces all slices into argmax[b].
 template <int HT, int D, int HPG, int NB>
 MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
-  const bool cached = (I.flags & F_NORM_CACHED) != 0;
   NormGain<HT> ng;
-  if (!cached) norm_gain(ng, g.final_norm, c.tid);
-  const int nr = (int)(I.r1 - I.r0);
-  zero_yrow(c, nr);
+  norm_gain(ng, g.final_norm, c.tid);
   if (!dep_wait(c, g, I)) return false;
-  if (!cached) norm_apply(c, g, 2 * g.L, ng);
+  norm_apply(c, g, 2 * g.L, ng);
   c.mark(g, 0);
-  AFrag<HT> f;
-  build_afrag<HT, NB>(f, c.xn, g.B, c.warp, c.lane);
+  float xr[HT / 32];
+  if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
   Seg s[2];
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
-  gemv_tiles(c, g, s[0], f);
-  c.mark(g, 1);
-  consumer_bar();
-  // logits of this piece (rows past the vocabulary are tile padding) and its
-  // (max, first index) per sequence
-  const int lane = c.lane, B = g.B, V = g.V;
   float best[NB];
   int bidx[NB];
 #pragma unroll
@@ -973,33 +950,24 @@ MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
     best[b] = -INFINITY;
     bidx[b] = 0x7FFFFFFF;
   }
-  for (int r = c.tid; r < nr; r += NCT) {
-    const int row = (int)I.r0 + r;
-    if (row >= V) break;
+  const int lane = c.lane, B = g.B, V = g.V;
+  float* logits = g.logits;
+  const uint32_t r0 = I.r0;
+  gemv_rows(c, g, s[0], xr, [&](uint32_t r, float(&acc)[NB]) {
+    if (lane == 0) {
+      const int row = (int)(r0 + r);
 #pragma unroll
-    for (int b = 0; b < NB; b++) {
-      if (b < B) {
-        const float v = c.yrow[b * MAX_ROWS + r];
-        g.logits[(size_t)b * V + row] = v;
-        if (v > best[b] || (v == best[b] && row < bidx[b])) {
-          best[b] = v;
-          bidx[b] = row;
+      for (int b = 0; b < NB; b++) {
+        if (b < B) {
+          logits[(size_t)b * V + row] = acc[b];
+          if (acc[b] > best[b] || (acc[b] == best[b] && row < bidx[b])) {
+            best[b] = acc[b];
+            bidx[b] = row;
+          }
         }
       }
     }
-  }
-#pragma unroll
-  for (int b = 0; b < NB; b++) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, best[b], o);
-      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bidx[b], o);
-      if (ov > best[b] || (ov == best[b] && oi < bidx[b])) {
-        best[b] = ov;
-        bidx[b] = oi;
-      }
-    }
-  }
+  });
   float* rv = c.red;
   int* ri = (int*)(c.red + NCW * NB);
   if (lane == 0) {

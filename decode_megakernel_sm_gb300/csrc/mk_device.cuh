@@ -129,37 +129,6 @@ MK_DEV void unpack8(const uint4& w, float* f) {
   f[6] = bf_lo(w.w); f[7] = bf_hi(w.w);
 }
 
-// ---- tensor-core GEMV helpers (mma.sync m16n8k16, bf16 in, fp32 accumulate)
-// Two 8x8 b16 matrices from shared memory; lanes 0-7 address the rows of the
-// first, lanes 8-15 the rows of the second.
-MK_DEV void ldmatrix_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
-               : "=r"(r0), "=r"(r1)
-               : "r"(addr));
-}
-
-// d += A(16x16, row-major) * B(16x8, column-major)
-MK_DEV void mma_bf16_16816(float& d0, float& d1, float& d2, float& d3, uint32_t a0, uint32_t a1,
-                           uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi): two bf16 operands that
-// carry about 16 significant bits of x into the tensor core.
-MK_DEV void split_bf16(float x, uint16_t& hi, uint16_t& lo) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(x);
-  hi = __bfloat16_as_ushort(h);
-  lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
-}
-
-MK_DEV uint32_t pack2(uint16_t first, uint16_t second) {
-  return (uint32_t)first | ((uint32_t)second << 16);
-}
-
 MK_DEV float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);

@@ -105,31 +105,18 @@ inline bool mlp_split(const mk_model_desc& d) {
   return d.n_experts == 0 && d.max_batch == 1 && d.ffn % 8 == 0 && d.ffn * 2 <= STAGE_BYTES;
 }
 
-// Tiled layout of the matrices the GEMV streams (QKV, gate/up, router, LM
-// head): tiles of 8 rows x KG columns, KG = min(K, 1024) so that one tile is
-// at most one 16 KiB ring stage; tiles run row block major, then K group;
-// inside a tile the 16-byte chunks run chunk major, then row, so the eight
-// rows of one chunk are 128 contiguous bytes (one conflict-free ldmatrix
-// 8x8 matrix).  Element (row, col) of an R x K matrix sits at
-//   ((row/8 * (K/KG) + col/KG) * 8 * KG) + ((col%KG)/8 * 8 + row%8) * 8 + col%8.
-MK_HD inline int tile_kg(int K) { return K < 1024 ? K : 1024; }
-MK_HD inline size_t tiled_offset(size_t row, size_t col, int K) {
-  const size_t kg = (size_t)tile_kg(K), nkg = (size_t)K / kg;
-  return ((row / 8) * nkg + col / kg) * 8 * kg + ((col % kg) / 8 * 8 + row % 8) * 8 + col % 8;
-}
-
 // Device pointers of one layer inside the packed weight buffer.
 struct LayerPtrs {
   const uint16_t* attn_norm;  // [H]
   const uint16_t* mlp_norm;   // [H]
-  const uint16_t* wqkv;       // tiled [Hkv*(HPG+2)*D][H]; per head rows (t, t+D/2) adjacent
+  const uint16_t* wqkv;       // [Hkv][(HPG+2)*D][H]; per head rows (t, t+D/2) adjacent
   const uint16_t* wo;         // [Hq][H][D]
-  const uint16_t* wgu;        // dense: tiled [2F][H]  (gate row c at 2c, up row at 2c+1)
+  const uint16_t* wgu;        // dense: [F][2][H]      (gate row, up row)
   const uint16_t* wdT;        // dense: down, [F][H] transposed (fused MLP) or [H][F] (split MLP)
-  const uint16_t* router;     // MoE:   tiled [E][H]
-  const uint16_t* ex_gu;      // MoE:   [E] x tiled [2Fe][H]
+  const uint16_t* router;     // MoE:   [E][H]
+  const uint16_t* ex_gu;      // MoE:   [E][Fe][2][H]
   const uint16_t* ex_dT;      // MoE:   [E][Fe][H]
-  const uint16_t* sh_gu;      // MoE:   tiled [2Fs][H]
+  const uint16_t* sh_gu;      // MoE:   [Fs][2][H]
   const uint16_t* sh_dT;      // MoE:   [Fs][H]
   uint16_t* kc;               // caller cache [maxB][Hkv][max_seq][D]
   uint16_t* vc;
@@ -139,8 +126,8 @@ struct LayerPtrs {
 struct Globals {
   const Instr* sched;
   const LayerPtrs* layers;
-  const uint16_t* embed;     // the tiled LM head when tied, else tiled [Vp][H]
-  const uint16_t* lm_head;   // tiled [Vp][H], Vp = vocab rounded up to 8 (zero rows)
+  const uint16_t* embed;
+  const uint16_t* lm_head;
   const uint16_t* final_norm;
   const float* rope;       // [max_seq][D/2][2] (cos, sin)
   float* xbuf;             // [2][2L][kc][B][H] residual stream x_1 .. x_2L, kc partial copies
@@ -160,7 +147,6 @@ struct Globals {
   unsigned long long timeout_ns;
   int max_pc, n_sm, n_stages;
   int B, H, Hq, Hkv, D, F, V, L, max_seq, max_ctx, splits;
-  int Vp;                  // LM-head rows rounded up to 8 (tiled layout)
   int E, K, Fe, Fs;
   int kc;                  // partial copies of each residual vector (1..8)
   float eps;

@@ -67,30 +67,6 @@ __global__ void transpose_kernel(uint16_t* __restrict__ dst, const uint16_t* __r
   }
 }
 
-// Row-major [R][K] -> tiled layout (see tiled_offset), one 16-byte chunk per
-// thread; rows R..Rp-1 of the destination are zero.  batch matrices of R x K
-// follow each other in both buffers (source stride R*K, destination Rp*K).
-__global__ void retile_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int R, int Rp,
-                              int K, int batch) {
-  const size_t chunks = (size_t)Rp * (K / 8);
-  const size_t total = chunks * batch;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const size_t m = i / chunks, j = i % chunks;
-    const size_t row = j / (K / 8), col = (j % (K / 8)) * 8;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (row < (size_t)R) v = src[m * ((size_t)R * K / 8) + j];
-    dst[m * ((size_t)Rp * K / 8) + tiled_offset(row, col, K) / 8] = v;
-  }
-}
-
-cudaError_t pack_retile(uint16_t* dst, const void* src, int R, int Rp, int K, int batch,
-                        cudaStream_t s) {
-  if (R <= 0 || K <= 0 || batch <= 0) return cudaSuccess;
-  retile_kernel<<<4096, 256, 0, s>>>((uint4*)dst, (const uint4*)src, R, Rp, K, batch);
-  return cudaGetLastError();
-}
-
 cudaError_t pack_qkv(uint16_t* dst, const void* wq, const void* wk, const void* wv, int H, int Hkv,
                      int HPG, int D, cudaStream_t s) {
   pack_qkv_kernel<<<Hkv * (HPG + 2) * D, 128, 0, s>>>((uint4*)dst, (const uint16_t*)wq,

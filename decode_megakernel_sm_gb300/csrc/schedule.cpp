@@ -35,11 +35,6 @@ int plan_shape_ok(const mk_model_desc& d) {
   if (d.n_experts > 0 && (d.top_k <= 0 || d.top_k > d.n_experts || d.expert_ffn <= 0))
     return MK_ERR_INVALID_ARG;
   if (d.hidden % 256 || d.hidden > 16384) return MK_ERR_UNSUPPORTED;
-  // tiled GEMV layout: 8-row tiles of min(hidden, 1024) columns
-  if (d.hidden > 1024 && d.hidden % 1024) return MK_ERR_UNSUPPORTED;
-  if (d.n_experts == 0 && d.ffn % 4) return MK_ERR_UNSUPPORTED;
-  if (d.n_experts > 0 && (d.n_experts % 8 || d.expert_ffn % 4 || d.shared_ffn % 4))
-    return MK_ERR_UNSUPPORTED;
   if (d.head_dim != 64 && d.head_dim != 128) return MK_ERR_UNSUPPORTED;
   if (d.n_q_heads / d.n_kv_heads > 8) return MK_ERR_UNSUPPORTED;
   if (d.n_experts > 1024 || d.top_k > 16) return MK_ERR_UNSUPPORTED;
@@ -95,11 +90,11 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
         const long s0 = ((long)g * n_sm + Hkv - 1) / Hkv;   // first SM of group g
         const long s1 = ((long)(g + 1) * n_sm + Hkv - 1) / Hkv;
         const int m = (int)(s1 - s0), k = (int)(i - s0);
-        a = (long)g * GR + cut(GR, m, k, 8);
-        b = (long)g * GR + (k == m - 1 ? GR : cut(GR, m, k + 1, 8));
+        a = (long)g * GR + cut(GR, m, k, 2);
+        b = (long)g * GR + (k == m - 1 ? GR : cut(GR, m, k + 1, 2));
       } else {
-        a = cut(R, n_sm, i, 8);
-        b = (i == n_sm - 1) ? R : cut(R, n_sm, i + 1, 8);
+        a = cut(R, n_sm, i, 2);
+        b = (i == n_sm - 1) ? R : cut(R, n_sm, i + 1, 2);
       }
       bool first = true;
       while (a < b) {
@@ -167,7 +162,7 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
     if (moe) {
       const long E = d.n_experts;
       for (int i = 0; i < n_sm; i++) {
-        long a = cut(E, n_sm, i, 8), b = (i == n_sm - 1) ? E : cut(E, n_sm, i + 1, 8);
+        long a = cut(E, n_sm, i, 1), b = (i == n_sm - 1) ? E : cut(E, n_sm, i + 1, 1);
         while (a < b) {
           long e = std::min(b, a + MAX_ROWS);
           Instr I = mk(OP_ROUTER, l);
@@ -185,7 +180,7 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
     if (mlp_split(d)) {
       const long F = d.ffn;
       for (int i = 0; i < n_sm; i++) {
-        long a = cut(F, n_sm, i, 4), b = (i == n_sm - 1) ? F : cut(F, n_sm, i + 1, 4);
+        long a = cut(F, n_sm, i, 1), b = (i == n_sm - 1) ? F : cut(F, n_sm, i + 1, 1);
         bool first = true;
         while (a < b) {
           const long e = std::min(b, a + MAX_COLS);
@@ -231,8 +226,8 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
     for (int i = 0; i < n_sm; i++)
       for (auto& fs : fsegs) {
       const long span = fs.second - fs.first;
-      long a = fs.first + cut(span, n_sm, i, 4);
-      long b = fs.first + ((i == n_sm - 1) ? span : cut(span, n_sm, i + 1, 4));
+      long a = fs.first + cut(span, n_sm, i, 1);
+      long b = fs.first + ((i == n_sm - 1) ? span : cut(span, n_sm, i + 1, 1));
       while (a < b) {
         long seg_end = Fv;
         int slot = -1;
@@ -279,25 +274,17 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
       I.aux = rs0 | (rs1 << 16);
     }
   }
-  // ---- LM head rows over the 8-row-padded vocabulary, in pieces of at most
-  // MAX_ROWS rows (+ argmax by the last arriver)
-  const long Vp = (V + 7) / 8 * 8;
+  // ---- LM head rows (+ argmax by the last arriver)
   for (int i = 0; i < n_sm; i++) {
-    long a = cut(Vp, n_sm, i, 8), b = (i == n_sm - 1) ? Vp : cut(Vp, n_sm, i + 1, 8);
-    bool first = true;
-    while (a < b) {
-      const long e = std::min(b, a + MAX_ROWS);
-      Instr I = mk(OP_LMHEAD, L);
-      I.r0 = (uint32_t)a;
-      I.r1 = (uint32_t)e;
-      I.flags = first ? 0 : F_NORM_CACHED;
-      I.wait_ctr = cm.mlp(L - 1);
-      I.aux = (uint32_t)n_lm++;
-      qs[i].push_back(I);
-      bytes[i] += (double)(e - a) * H * 2;
-      first = false;
-      a = e;
-    }
+    long a = cut(V, n_sm, i, 1), b = (i == n_sm - 1) ? V : cut(V, n_sm, i + 1, 1);
+    if (a >= b) continue;
+    Instr I = mk(OP_LMHEAD, L);
+    I.r0 = (uint32_t)a;
+    I.r1 = (uint32_t)b;
+    I.wait_ctr = cm.mlp(L - 1);
+    I.aux = (uint32_t)n_lm++;
+    qs[i].push_back(I);
+    bytes[i] += (double)(b - a) * H * 2;
   }
 
   // ---- hold marks: the first instruction of each run of a held op on an SM
@@ -369,8 +356,7 @@ int plan_verify(const mk_model_desc& d, int B, const PlanOut& p) {
   const int S = p.splits;
   std::vector<uint8_t> qkv((size_t)L * R, 0), att((size_t)L * B * Hkv * S, 0);
   std::vector<uint8_t> op((size_t)L * Hq * H, 0), mlp((size_t)L * Fv, 0), res((size_t)L * H, 0);
-  const size_t Vp = ((size_t)V + 7) / 8 * 8;
-  std::vector<uint8_t> rt((size_t)L * (moe ? d.n_experts : 1), 0), lm(Vp, 0), slot(p.n_lm, 0);
+  std::vector<uint8_t> rt((size_t)L * (moe ? d.n_experts : 1), 0), lm(V, 0), slot(p.n_lm, 0);
   auto mark = [](std::vector<uint8_t>& v, size_t i) {
     if (i >= v.size() || v[i]) return false;
     v[i] = 1;
@@ -382,7 +368,7 @@ int plan_verify(const mk_model_desc& d, int B, const PlanOut& p) {
       case OP_HALT: break;
       case OP_QKV:
         if (l >= L || I.r0 >= I.r1 || I.r1 > R || I.r1 - I.r0 > (uint32_t)MAX_ROWS) return 1;
-        if (I.r0 / GR != I.g || (I.r1 - 1) / GR != I.g || (I.r0 % 8) || (I.r1 % 8)) return 2;
+        if (I.r0 / GR != I.g || (I.r1 - 1) / GR != I.g || (I.r0 % 2) || (I.r1 % 2)) return 2;
         for (uint32_t r = I.r0; r < I.r1; r++)
           if (!mark(qkv, (size_t)l * R + r)) return 3;
         break;
@@ -398,15 +384,13 @@ int plan_verify(const mk_model_desc& d, int B, const PlanOut& p) {
         break;
       case OP_ROUTER:
         if (!moe || l >= L || I.r0 >= I.r1 || (int)I.r1 > d.n_experts ||
-            I.r1 - I.r0 > (uint32_t)MAX_ROWS || (I.r0 % 8) || (I.r1 % 8))
+            I.r1 - I.r0 > (uint32_t)MAX_ROWS)
           return 9;
         for (uint32_t r = I.r0; r < I.r1; r++)
           if (!mark(rt, (size_t)l * d.n_experts + r)) return 10;
         break;
       case OP_MLP: {
-        if (l >= L || I.r0 >= I.r1 || I.r1 - I.r0 > (uint32_t)MAX_COLS || (I.r0 % 4) ||
-            (I.r1 % 4))
-          return 11;
+        if (l >= L || I.r0 >= I.r1 || I.r1 - I.r0 > (uint32_t)MAX_COLS) return 11;
         long base = 0, width = Fv;
         if (moe) {
           if (I.flags & F_SHARED) {
@@ -428,7 +412,7 @@ int plan_verify(const mk_model_desc& d, int B, const PlanOut& p) {
       }
       case OP_MLP_UP:
         if (!mlp_split(d) || l >= L || I.r0 >= I.r1 || I.r1 - I.r0 > (uint32_t)MAX_COLS ||
-            (long)I.r1 > Fv || (I.r0 % 4) || (I.r1 % 4))
+            (long)I.r1 > Fv)
           return 23;
         for (uint32_t c = I.r0; c < I.r1; c++)
           if (!mark(mlp, (size_t)l * Fv + c)) return 24;
@@ -441,9 +425,7 @@ int plan_verify(const mk_model_desc& d, int B, const PlanOut& p) {
           if (!mark(res, (size_t)l * H + r)) return 26;
         break;
       case OP_LMHEAD:
-        if (I.r0 >= I.r1 || I.r1 > Vp || (int)I.aux >= p.n_lm || (I.r0 % 8) || (I.r1 % 8) ||
-            I.r1 - I.r0 > (uint32_t)MAX_ROWS)
-          return 17;
+        if (I.r0 >= I.r1 || (int)I.r1 > V || (int)I.aux >= p.n_lm) return 17;
         if (!mark(slot, I.aux)) return 18;
         for (uint32_t r = I.r0; r < I.r1; r++)
           if (!mark(lm, r)) return 19;

@@ -104,7 +104,7 @@ def independent_coverage(cfg, q, n_sm, max_pc, splits):
     assert len(seen["oproj"]) == Lc * Hq * H
     assert len(seen["mlp"]) == Lc * Fv
     assert len(seen["res"]) == Lc * H
-    assert len(seen["lm"]) == (cfg["vocab"] + 7) // 8 * 8  # tiled head: vocab padded to 8 rows
+    assert len(seen["lm"]) == cfg["vocab"]
     assert len(seen["router"]) == (Lc * cfg["n_experts"] if moe else 0)
     # every wait is for all signals of its counter
     for s in range(n_sm):
