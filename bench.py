@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--hold", type=int, default=None,
                     help="hold-policy mask (library default if unset)")
     ap.add_argument("--hold-prefetch", type=int, default=256 << 10)
+    ap.add_argument("--stage-bytes", type=int, default=None,
+                    help="ring stage size in bytes (default: the library's)")
     ap.add_argument("--trace", default=None,
                     help="write a per-instruction timeline of 3 traced steps to this path")
     return ap.parse_args()
@@ -271,6 +273,8 @@ def main():
         dec.set_residual_copies(args.kc)
     if args.hold is not None:
         dec.set_hold_policy(args.hold, args.hold_prefetch)
+    if args.stage_bytes is not None:
+        dec.set_stage_bytes(args.stage_bytes)
     dec.build_schedule(B, cfg["max_seq"])
     if args.l2_ahead is not None:
         dec.set_l2_prefetch(args.l2_ahead)

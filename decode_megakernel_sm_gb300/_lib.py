@@ -93,6 +93,7 @@ SIGNATURES = {
     "mk_set_trace": (C.c_int, [C.c_void_p, C.c_int]),
     "mk_set_l2_prefetch": (C.c_int, [C.c_void_p, C.c_uint64]),
     "mk_set_residual_copies": (C.c_int, [C.c_void_p, C.c_int]),
+    "mk_set_stage_bytes": (C.c_int, [C.c_void_p, C.c_int]),
     "mk_set_hold_policy": (C.c_int, [C.c_void_p, C.c_uint, C.c_uint64]),
     "mk_get_trace": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.c_size_t]),
     "mk_destroy": (C.c_int, [C.c_void_p]),
@@ -202,6 +203,10 @@ def mk_set_l2_prefetch(h, bytes_ahead: int):
 
 def mk_set_residual_copies(h, copies: int):
     _check(lib().mk_set_residual_copies(h, int(copies)), "mk_set_residual_copies")
+
+
+def mk_set_stage_bytes(h, stage_bytes: int):
+    _check(lib().mk_set_stage_bytes(h, int(stage_bytes)), "mk_set_stage_bytes")
 
 
 def mk_set_hold_policy(h, mask: int, prefetch_bytes: int):

@@ -35,6 +35,7 @@ struct mk_handle {
   int dev = 0, n_sm = 0;
   const Variant* var = nullptr;
   int n_stages = 0, smem_bytes = 0;
+  int stage_bytes = DEFAULT_STAGE_BYTES;
   void* packed = nullptr;
   size_t packed_bytes = 0;
   std::vector<LayerPtrs> layers_h;
@@ -148,6 +149,31 @@ static LayerSizes layer_sizes(const mk_model_desc& d) {
   return s;
 }
 
+// Ring depth for `stage_bytes`: as many stages (2..MAX_STAGES) as the
+// opt-in shared memory holds next to the fixed buffers; sets the kernel's
+// dynamic shared-memory size and checks that one CTA still fits per SM.
+static int size_ring(mk_handle* h, int stage_bytes) {
+  const mk_model_desc& d = h->d;
+  const int K = d.n_experts > 0 ? d.top_k : 0;
+  const int HPG = d.n_q_heads / d.n_kv_heads;
+  int optin = 0;
+  CK(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->dev));
+  int ns = 0;
+  for (int n = 2; n <= MAX_STAGES; n++)
+    if (smem_layout(n, stage_bytes, h->var->NB, d.hidden, d.head_dim, HPG, K).total <= optin)
+      ns = n;
+  if (ns < 2) return MK_ERR_UNSUPPORTED;
+  const int bytes = smem_layout(ns, stage_bytes, h->var->NB, d.hidden, d.head_dim, HPG, K).total;
+  CK(cudaFuncSetAttribute(h->var->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+  int per_sm = 0;
+  CK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, h->var->kernel, NTHREADS, bytes));
+  if (per_sm < 1) return MK_ERR_UNSUPPORTED;
+  h->stage_bytes = stage_bytes;
+  h->n_stages = ns;
+  h->smem_bytes = bytes;
+  return MK_OK;
+}
+
 static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv,
                        mk_handle* h) {
   const mk_model_desc& d = *desc;
@@ -186,22 +212,11 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
   }
   // ---- device
   CK(cudaGetDevice(&h->dev));
-  int optin = 0;
   CK(cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, h->dev));
-  CK(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->dev));
-  const int K = moe ? d.top_k : 0;
-  int ns = 0;
-  for (int n = 2; n <= MAX_STAGES; n++)
-    if (smem_layout(n, h->var->NB, H, D, HPG, K).total <= optin) ns = n;
-  if (ns < 2) return MK_ERR_UNSUPPORTED;
-  h->n_stages = ns;
-  h->smem_bytes = smem_layout(ns, h->var->NB, H, D, HPG, K).total;
-  CK(cudaFuncSetAttribute(h->var->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                          h->smem_bytes));
-  int per_sm = 0;
-  CK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, h->var->kernel, NTHREADS,
-                                                   h->smem_bytes));
-  if (per_sm < 1) return MK_ERR_UNSUPPORTED;
+  {
+    const int st = size_ring(h, h->stage_bytes);
+    if (st != MK_OK) return st;
+  }
   CK(cudaStreamCreateWithFlags(&h->own, cudaStreamNonBlocking));
   CK(cudaMallocHost(&h->h_err, 4 * sizeof(int)));
 
@@ -409,6 +424,7 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.max_pc = h->plan.max_pc;
   g.n_sm = h->n_sm;
   g.n_stages = h->n_stages;
+  g.stage_bytes = h->stage_bytes;
   g.B = h->batch;
   g.H = d.hidden;
   g.Hq = d.n_q_heads;
@@ -681,6 +697,21 @@ extern "C" int mk_set_hold_policy(mk_handle* h, unsigned mask, uint64_t prefetch
   return MK_OK;
 }
 
+extern "C" int mk_set_stage_bytes(mk_handle* h, int stage_bytes) {
+  if (!h || stage_bytes < STAGE_UNIT || stage_bytes > MAX_STAGE_BYTES ||
+      stage_bytes % STAGE_UNIT != 0)
+    return MK_ERR_INVALID_ARG;
+  const int old = h->stage_bytes;
+  const int st = size_ring(h, stage_bytes);
+  if (st != MK_OK) {
+    size_ring(h, old);
+    return st;
+  }
+  for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
+  h->graphs.clear();
+  return MK_OK;
+}
+
 extern "C" int mk_set_residual_copies(mk_handle* h, int copies) {
   if (!h || copies < 1 || copies > 8) return MK_ERR_INVALID_ARG;
   h->kc = copies;
@@ -699,7 +730,7 @@ extern "C" int mk_get_info(const mk_handle* h, mk_info* out) {
   if (!h || !out) return MK_ERR_INVALID_ARG;
   std::memset(out, 0, sizeof *out);
   out->n_sm = h->n_sm;
-  out->stage_bytes = STAGE_BYTES;
+  out->stage_bytes = h->stage_bytes;
   out->n_stages = h->n_stages;
   out->smem_bytes = h->smem_bytes;
   out->max_pc = h->plan.max_pc;

@@ -85,7 +85,8 @@ MK_DEV float xres_sum(const Globals& g, int j, int b, int r) {
 template <int HT, int D>
 MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int* topk, Seg* s) {
   constexpr uint32_t ROW = HT * 2;
-  constexpr uint32_t RPS = STAGE_BYTES / ROW;
+  const uint32_t SBY = (uint32_t)g.stage_bytes;
+  const uint32_t RPS = SBY / ROW;
   const LayerPtrs* Lp = g.layers + (I.op == OP_LMHEAD ? 0 : I.layer);
   const uint32_t n = I.r1 - I.r0;
   switch (I.op) {
@@ -94,7 +95,7 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
       return 1;
     case OP_OPROJ:
       s[0] = {(const unsigned char*)(Lp->wo + ((size_t)I.g * HT + I.r0) * D), nullptr, D * 2, n,
-              STAGE_BYTES / (D * 2)};
+              SBY / (D * 2)};
       return 1;
     case OP_ROUTER:
       s[0] = {(const unsigned char*)(Lp->router + (size_t)I.r0 * HT), nullptr, ROW, n, RPS};
@@ -124,7 +125,7 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
       return 1;
     case OP_MLP_DOWN:  // rows of the row-major [H][F] down projection
       s[0] = {(const unsigned char*)(Lp->wdT + (size_t)I.r0 * g.F), nullptr, (uint32_t)g.F * 2, n,
-              STAGE_BYTES / ((uint32_t)g.F * 2)};
+              SBY / ((uint32_t)g.F * 2)};
       return 1;
     case OP_ATTN: {
       // slice s of S over positions [0, P]: [s*C/S, (s+1)*C/S), C = P + 1.
@@ -138,7 +139,7 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
       const uint32_t cnt = pe > p0 ? (uint32_t)(pe - p0) : 0u;
       const size_t base = (((size_t)I.b * g.Hkv + I.g) * g.max_seq + (size_t)p0) * D;
       s[0] = {(const unsigned char*)(Lp->kc + base), (const unsigned char*)(Lp->vc + base), D * 2,
-              cnt, (STAGE_BYTES / 2) / (D * 2)};
+              cnt, (SBY / 2) / (D * 2)};
       return 1;
     }
     default:
@@ -301,17 +302,21 @@ MK_DEV void row_dot(const unsigned char* row, const float (&xr)[HT / 32], const 
                     int lane, float (&acc)[NB]) {
   const uint4* w4 = (const uint4*)row;
   if constexpr (NB == 1) {
-    float a0 = 0.f, a1 = 0.f;
+    // eight independent chains (one per element of a 16-byte chunk): the
+    // dependent-FMA depth is HT/256 instead of HT/64
+    float a[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) a[k] = 0.f;
 #pragma unroll
     for (int it = 0; it < HT / 256; it++) {
       const uint4 w = w4[it * 32 + lane];
       const float* x = xr + it * 8;
-      a0 = fmaf(bf_lo(w.x), x[0], a0); a1 = fmaf(bf_hi(w.x), x[1], a1);
-      a0 = fmaf(bf_lo(w.y), x[2], a0); a1 = fmaf(bf_hi(w.y), x[3], a1);
-      a0 = fmaf(bf_lo(w.z), x[4], a0); a1 = fmaf(bf_hi(w.z), x[5], a1);
-      a0 = fmaf(bf_lo(w.w), x[6], a0); a1 = fmaf(bf_hi(w.w), x[7], a1);
+      a[0] = fmaf(bf_lo(w.x), x[0], a[0]); a[1] = fmaf(bf_hi(w.x), x[1], a[1]);
+      a[2] = fmaf(bf_lo(w.y), x[2], a[2]); a[3] = fmaf(bf_hi(w.y), x[3], a[3]);
+      a[4] = fmaf(bf_lo(w.z), x[4], a[4]); a[5] = fmaf(bf_hi(w.z), x[5], a[5]);
+      a[6] = fmaf(bf_lo(w.w), x[6], a[6]); a[7] = fmaf(bf_hi(w.w), x[7], a[7]);
     }
-    acc[0] = a0 + a1;
+    acc[0] = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
   } else {
 #pragma unroll
     for (int b = 0; b < NB; b++) acc[b] = 0.f;
@@ -340,6 +345,8 @@ MK_DEV void row_dot(const unsigned char* row, const float (&xr)[HT / 32], const 
 template <int HT, int D, int HPG, int NB, class Fn>
 MK_DEV bool gemv_rows(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s,
                       const float (&xr)[HT / 32], Fn&& fn) {
+  float pend = 0.f;  // NB == 1: this lane's partial of the row not yet reduced
+  int prow = -1;
   for (uint32_t u0 = 0; u0 < s.n; u0 += s.ups) {
     const uint32_t n = min(s.ups, s.n - u0);
     if (!c.ring.acquire(g)) return false;
@@ -348,12 +355,28 @@ MK_DEV bool gemv_rows(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s,
     // spreads its rows over all warps rather than over one stage's worth
     for (uint32_t r = (uint32_t)(c.warp + NCW - (int)(u0 % NCW)) % NCW; r < n; r += NCW) {
       float acc[NB];
-      row_dot<HT, NB>(st + (size_t)r * HT * 2, xr, c.xn, c.lane, acc);
+      if constexpr (NB == 1) {
+        // the previous row's cross-lane sum is issued in the same block as
+        // this row's loads and FMAs, so its shuffle latency hides behind them
+        float prev[1] = {warp_sum(pend)};
+        row_dot<HT, NB>(st + (size_t)r * HT * 2, xr, c.xn, c.lane, acc);
+        if (prow >= 0) fn((uint32_t)prow, prev);
+        pend = acc[0];
+        prow = (int)(u0 + r);
+      } else {
+        row_dot<HT, NB>(st + (size_t)r * HT * 2, xr, c.xn, c.lane, acc);
 #pragma unroll
-      for (int b = 0; b < NB; b++) acc[b] = warp_sum(acc[b]);
-      fn(u0 + r, acc);
+        for (int b = 0; b < NB; b++) acc[b] = warp_sum(acc[b]);
+        fn(u0 + r, acc);
+      }
     }
     c.ring.release(c.lane);
+  }
+  if constexpr (NB == 1) {
+    if (prow >= 0) {
+      float last[1] = {warp_sum(pend)};
+      fn((uint32_t)prow, last);
+    }
   }
   return true;
 }
@@ -515,7 +538,7 @@ MK_DEV bool op_attn(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
       const bool valid = j < n;
       const uint4 kw = valid ? *(const uint4*)(st + (size_t)j * D * 2 + dsl * 16) : zero;
       const uint4 vw =
-          valid ? *(const uint4*)(st + STAGE_BYTES / 2 + (size_t)j * D * 2 + dsl * 16) : zero;
+          valid ? *(const uint4*)(st + c.ring.sb / 2 + (size_t)j * D * 2 + dsl * 16) : zero;
       process(kw, vw, valid);
     }
     c.ring.release(c.lane);
@@ -650,46 +673,124 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   }
   c.mark(g, 0);
   consumer_bar();
+  Seg s[2];
+  get_segs<HT, D>(g, I, c.pos, c.topk, s);
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  const int nr = (int)(I.r1 - I.r0);
+  if constexpr (NB == 1) {
+    // One lane per Wo row: the lane dots its row's D columns with the head's
+    // attention output (registers for D = 64, shared-memory broadcasts for
+    // D = 128), so there is no cross-lane reduction, and a warp's 32
+    // consecutive rows leave as one coalesced reduction.  The packed rows are
+    // chunk-swizzled (chunk k of row r at slot k ^ (r & 7)), which keeps the
+    // 32 lanes' row reads free of bank conflicts.
+    constexpr int CPR = D / 8;
+    constexpr bool REG = D <= 64;
+    float av[REG ? D : 1];
+    if constexpr (REG) {
+#pragma unroll
+      for (int k = 0; k < D / 4; k++) {
+        const float4 t = ((const float4*)c.attn)[k];
+        av[4 * k] = t.x; av[4 * k + 1] = t.y; av[4 * k + 2] = t.z; av[4 * k + 3] = t.w;
+      }
+    }
+    float* dst = xres_mine(g, 2 * l + 1, 0);
+    uint32_t bc = 0;  // 32-row blocks of earlier stages (round-robin offset)
+    for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
+      const uint32_t n = min(s[0].ups, s[0].n - u0);
+      if (!c.ring.acquire(g)) break;
+      const unsigned char* st = c.ring.stage_ptr();
+      const uint32_t nblk = (n + 31) / 32;
+      for (uint32_t blk = (uint32_t)(c.warp + NCW - (int)(bc % NCW)) % NCW; blk < nblk;
+           blk += NCW) {
+        const uint32_t j = blk * 32 + (uint32_t)c.lane;
+        const bool valid = j < n;
+        const uint32_t row = I.r0 + u0 + j;
+        const unsigned char* rp = st + (size_t)j * D * 2;
+        float a[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) a[e] = 0.f;
+#pragma unroll
+        for (int k = 0; k < CPR; k++) {
+          const uint4 w = valid ? *(const uint4*)(rp + ((k ^ (row & 7u)) * 16)) : zero;
+          float wf[8];
+          unpack8(w, wf);
+          float xv[8];
+          if constexpr (REG) {
+#pragma unroll
+            for (int e = 0; e < 8; e++) xv[e] = av[k * 8 + e];
+          } else {
+            const float4 x0 = ((const float4*)c.attn)[2 * k], x1 = ((const float4*)c.attn)[2 * k + 1];
+            xv[0] = x0.x; xv[1] = x0.y; xv[2] = x0.z; xv[3] = x0.w;
+            xv[4] = x1.x; xv[5] = x1.y; xv[6] = x1.z; xv[7] = x1.w;
+          }
+#pragma unroll
+          for (int e = 0; e < 8; e++) a[e] = fmaf(wf[e], xv[e], a[e]);
+        }
+        if (valid) {
+          float v = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+          if (resid) v += xr_s[row - I.r0];
+          red_add_f32(dst + row, v);
+        }
+      }
+      bc += nblk;
+      c.ring.release(c.lane);
+    }
+  } else {
   float a[NB][8];
 #pragma unroll
   for (int b = 0; b < NB; b++)
 #pragma unroll
     for (int j = 0; j < 8; j++) a[b][j] = c.attn[b * D + dsl * 8 + j];
-  Seg s[2];
-  get_segs<HT, D>(g, I, c.pos, c.topk, s);
-  const uint4 zero = make_uint4(0, 0, 0, 0);
-  const int nr = (int)(I.r1 - I.r0);
   for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
     const uint32_t n = min(s[0].ups, s[0].n - u0);
     if (!c.ring.acquire(g)) break;
     const unsigned char* st = c.ring.stage_ptr();
-    for (uint32_t jb = (uint32_t)c.warp * SPW; jb < n; jb += NCW * SPW) {
-      const uint32_t j = jb + slot;
-      const bool valid = j < n;
-      float wf[8];
-      unpack8(valid ? *(const uint4*)(st + (size_t)j * D * 2 + dsl * 16) : zero, wf);
-      float y[NB];
+    // two passes of SPW rows per iteration: independent loads, FMA chains
+    // and shuffles, so each warp keeps two rows' latencies in flight
+    constexpr uint32_t STEP = NCW * SPW;
+    for (uint32_t jb = (uint32_t)c.warp * SPW; jb < n; jb += 2 * STEP) {
+      float y[2][NB];
 #pragma unroll
-      for (int b = 0; b < NB; b++) {
-        float v = 0.f;
+      for (int p = 0; p < 2; p++) {
+        const uint32_t j = jb + p * STEP + slot;
+        const uint32_t key = (I.r0 + u0 + j) & 7u;  // chunk swizzle of this row
+        float wf[8];
+        unpack8(j < n ? *(const uint4*)(st + (size_t)j * D * 2 + ((dsl ^ key) * 16)) : zero, wf);
 #pragma unroll
-        for (int k = 0; k < 8; k++) v = fmaf(a[b][k], wf[k], v);
-        y[b] = v;
+        for (int b = 0; b < NB; b++) {
+          float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+          for (int k = 0; k < 8; k += 2) {
+            v0 = fmaf(a[b][k], wf[k], v0);
+            v1 = fmaf(a[b][k + 1], wf[k + 1], v1);
+          }
+          y[p][b] = v0 + v1;
+        }
       }
 #pragma unroll
       for (int off = LPR / 2; off > 0; off >>= 1)
 #pragma unroll
-        for (int b = 0; b < NB; b++) y[b] += __shfl_xor_sync(0xFFFFFFFFu, y[b], off);
-      if (valid && dsl == 0) {
-        const int r = (int)(I.r0 + u0 + j);
-        for (int b = 0; b < g.B && b < NB; b++) {
-          float v = y[b];
-          if (resid) v += xr_s[b * nr + (r - (int)I.r0)];
-          red_add_f32(xres_mine(g, 2 * l + 1, b) + r, v);
+        for (int p = 0; p < 2; p++)
+#pragma unroll
+          for (int b = 0; b < NB; b++) y[p][b] += __shfl_xor_sync(0xFFFFFFFFu, y[p][b], off);
+      if (dsl == 0) {
+#pragma unroll
+        for (int p = 0; p < 2; p++) {
+          const uint32_t j = jb + p * STEP + slot;
+          if (j < n) {
+            const int r = (int)(I.r0 + u0 + j);
+            for (int b = 0; b < g.B && b < NB; b++) {
+              float v = y[p][b];
+              if (resid) v += xr_s[b * nr + (r - (int)I.r0)];
+              red_add_f32(xres_mine(g, 2 * l + 1, b) + r, v);
+            }
+          }
         }
       }
     }
     c.ring.release(c.lane);
+  }
   }
   c.mark(g, 1);
   consumer_bar();
@@ -871,7 +972,7 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I
     if (c.tid == 0) set_err(g, MK_ERR_DEVICE, c.pc, I.op);
     return false;
   } else {
-    constexpr int CPT = (STAGE_BYTES / 16 + NCT - 1) / NCT;  // h chunks per thread
+    constexpr int CPT = (DOWN_ROW_MAX / 16 + NCT - 1) / NCT;  // h chunks per thread
     const int l = I.layer, F = g.F, nch = F / 8;
     const int nrows = (int)(I.r1 - I.r0);
     if (!dep_wait(c, g, I)) return false;
@@ -893,6 +994,9 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I
     const float res = c.tid < nrows ? xres_sum(g, 2 * l + 1, 0, (int)I.r0 + c.tid) : 0.f;
     c.mark(g, 0);
     float* part = c.yrow;  // [NCW][MAX_DOWN_ROWS]
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    float pend = 0.f;
+    int prow = -1;
     Seg s[2];
     get_segs<HT, D>(g, I, c.pos, c.topk, s);
     for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
@@ -900,21 +1004,33 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I
       if (!c.ring.acquire(g)) break;
       const unsigned char* st = c.ring.stage_ptr();
       for (uint32_t j = 0; j < n; j++) {
-        float acc = 0.f;
+        const float prev = warp_sum(pend);  // overlaps this row's FMAs
+        float a[CPT];
 #pragma unroll
         for (int q = 0; q < CPT; q++) {
           const int k = c.tid + q * NCT;
-          if (k < nch) {
-            float w[8];
-            unpack8(*(const uint4*)(st + (size_t)j * F * 2 + (size_t)k * 16), w);
+          float w[8];
+          unpack8(k < nch ? *(const uint4*)(st + (size_t)j * F * 2 + (size_t)k * 16) : zero, w);
+          float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; e++) acc = fmaf(w[e], h[q][e], acc);
+          for (int e = 0; e < 8; e += 2) {
+            a0 = fmaf(w[e], h[q][e], a0);
+            a1 = fmaf(w[e + 1], h[q][e + 1], a1);
           }
+          a[q] = a0 + a1;
         }
-        acc = warp_sum(acc);
-        if (c.lane == 0) part[c.warp * MAX_DOWN_ROWS + u0 + j] = acc;
+        if (prow >= 0 && c.lane == 0) part[c.warp * MAX_DOWN_ROWS + prow] = prev;
+        float t = 0.f;
+#pragma unroll
+        for (int q = 0; q < CPT; q++) t += a[q];
+        pend = t;
+        prow = (int)(u0 + j);
       }
       c.ring.release(c.lane);
+    }
+    if (prow >= 0) {
+      const float last = warp_sum(pend);
+      if (c.lane == 0) part[c.warp * MAX_DOWN_ROWS + prow] = last;
     }
     c.mark(g, 1);
     consumer_bar();
@@ -1231,11 +1347,11 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
             g.trace[((size_t)blockIdx.x * g.max_pc + pc) * 8] = gtimer();
           const uint32_t bytes = n * s[k].unit;
           const uint32_t full = full0 + 8u * st;
-          const uint32_t dst = ring_s + (uint32_t)st * STAGE_BYTES;
+          const uint32_t dst = ring_s + (uint32_t)st * (uint32_t)g.stage_bytes;
           mbar_expect_tx(full, s[k].src2 ? 2u * bytes : bytes);
           if (s[k].src2) {
             bulk_g2s(dst, s[k].src + (size_t)u0 * s[k].unit, bytes, full, pol_kv);
-            bulk_g2s(dst + STAGE_BYTES / 2, s[k].src2 + (size_t)u0 * s[k].unit, bytes, full,
+            bulk_g2s(dst + (uint32_t)g.stage_bytes / 2, s[k].src2 + (size_t)u0 * s[k].unit, bytes, full,
                      pol_kv);
           } else {
             bulk_g2s(dst, s[k].src + (size_t)u0 * s[k].unit, bytes, full, pol_w);
@@ -1265,7 +1381,7 @@ drain:
 template <int HT, int D, int HPG, int NB>
 __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_constant__ Globals g) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  const SmemLayout Ls = smem_layout(g.n_stages, NB, HT, D, HPG, g.K);
+  const SmemLayout Ls = smem_layout(g.n_stages, g.stage_bytes, NB, HT, D, HPG, g.K);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t full0 = smem_u32(smem + Ls.full), empty0 = smem_u32(smem + Ls.empty);
   const int KM = g.K > 0 ? g.K : 1;
@@ -1326,7 +1442,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
   c.pos = pos;
   c.topk = topk;
   c.topw = topw;
-  c.ring = Ring{smem + Ls.ring, full0, empty0, g.n_stages, 0, 0u, 0ull, g.trace != nullptr};
+  c.ring = Ring{smem + Ls.ring, full0, empty0, g.n_stages, 0, 0u, 0ull, g.trace != nullptr,
+                (uint32_t)g.stage_bytes};
   c.tid = tid;
   c.warp = warp;
   c.lane = lane;

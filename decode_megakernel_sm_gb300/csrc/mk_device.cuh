@@ -201,8 +201,9 @@ struct Ring {
   uint32_t par;
   unsigned long long waited;  // ns spent blocked in acquire (measured only when tracing)
   bool timed;
+  uint32_t sb;  // bytes per stage
 
-  MK_DEV const unsigned char* stage_ptr() const { return base + (size_t)st * STAGE_BYTES; }
+  MK_DEV const unsigned char* stage_ptr() const { return base + (size_t)st * sb; }
   // All 32 lanes call; the result is the same on every lane.
   MK_DEV bool acquire(const Globals& g) {
     bool ok;

@@ -92,8 +92,14 @@ struct CtrMap {
 constexpr int NCW = 7;               // consumer warps (8 warps per CTA: two per scheduler partition, 255 registers)
 constexpr int NCT = NCW * 32;        // consumer threads
 constexpr int NTHREADS = NCT + 32;   // + one producer warp
-constexpr int STAGE_BYTES = 16384;   // bytes per ring stage
+// Ring stages are a runtime size: a multiple of STAGE_UNIT up to
+// MAX_STAGE_BYTES (bigger stages hold more rows, so all consumer warps have a
+// row in every stage and the per-stage barrier cost is spread wider).
+constexpr int STAGE_UNIT = 16384;
+constexpr int MAX_STAGE_BYTES = 65536;
+constexpr int DEFAULT_STAGE_BYTES = 16384;
 constexpr int MAX_STAGES = 16;
+constexpr int DOWN_ROW_MAX = 16384;  // bytes of one down row (F <= 8192) in the split MLP
 constexpr int MAX_ROWS = 256;        // rows of one QKV / gate-up / router instruction
 constexpr int MAX_COLS = MAX_ROWS / 2;
 constexpr int MAX_DOWN_ROWS = 64;    // output rows of one split-MLP down instruction
@@ -102,7 +108,7 @@ constexpr int MAX_DOWN_ROWS = 64;    // output rows of one split-MLP down instru
 // row-split down projection over the whole h) when one down row fits a ring
 // stage; otherwise one fused op per FFN column slice with float atomics.
 inline bool mlp_split(const mk_model_desc& d) {
-  return d.n_experts == 0 && d.max_batch == 1 && d.ffn % 8 == 0 && d.ffn * 2 <= STAGE_BYTES;
+  return d.n_experts == 0 && d.max_batch == 1 && d.ffn % 8 == 0 && d.ffn * 2 <= DOWN_ROW_MAX;
 }
 
 // Device pointers of one layer inside the packed weight buffer.
@@ -146,6 +152,7 @@ struct Globals {
   int* argmax;
   unsigned long long timeout_ns;
   int max_pc, n_sm, n_stages;
+  int stage_bytes;  // bytes per ring stage (multiple of STAGE_UNIT)
   int B, H, Hq, Hkv, D, F, V, L, max_seq, max_ctx, splits;
   int E, K, Fe, Fs;
   int kc;                  // partial copies of each residual vector (1..8)
@@ -167,10 +174,11 @@ struct SmemLayout {
   int ring, full, empty, xn, yrow, hbuf, attn, red, misc, total;
 };
 
-MK_HD inline SmemLayout smem_layout(int n_stages, int NB, int H, int D, int HPG, int K) {
+MK_HD inline SmemLayout smem_layout(int n_stages, int stage_bytes, int NB, int H, int D, int HPG,
+                                     int K) {
   SmemLayout s;
   int o = 0;
-  s.ring = o;   o += n_stages * STAGE_BYTES;
+  s.ring = o;   o += n_stages * stage_bytes;
   s.full = o;   o += 8 * n_stages;
   s.empty = o;  o += 8 * n_stages;
   o = (o + 15) / 16 * 16;

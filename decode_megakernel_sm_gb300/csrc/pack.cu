@@ -3,7 +3,10 @@
 // instruction, one bulk copy per ring stage, no tensor map needed):
 //   QKV   [Hkv][(HPG+2)*D][H]  per kv head: its HPG query heads, then k, then
 //                              v; inside a head, rows 2t / 2t+1 = dims t / t+D/2
-//   Wo    [Hq][H][D]           one head's columns as contiguous 128/256-byte rows
+//   Wo    [Hq][H][D]           one head's columns as contiguous 128/256-byte rows;
+//                              16-byte chunk c of row r sits at slot c ^ (r & 7),
+//                              so 8 consecutive rows read chunk c from 8
+//                              different shared-memory bank groups
 //   gate/up [F][2][H]          gate row c, then up row c
 //   down  [F][H]               transposed: one contiguous row per FFN column
 #include <cuda_runtime.h>
@@ -38,14 +41,15 @@ __global__ void pack_interleave_kernel(uint4* __restrict__ dst, const uint4* __r
   }
 }
 
-// dst[h][r][:] = wo[r][h*D : (h+1)*D], in 16-byte chunks.
+// dst[h][r][c ^ (r & 7)] = wo[r][h*D + 8c : h*D + 8c + 8] (16-byte chunks c).
 __global__ void pack_wo_kernel(uint4* __restrict__ dst, const uint4* __restrict__ wo, int H, int Hq,
                                int D) {
   const size_t total = (size_t)Hq * H * (D / 8);
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (size_t)gridDim.x * blockDim.x) {
-    const size_t c8 = i % (D / 8), hr = i / (D / 8);
+    const size_t slot = i % (D / 8), hr = i / (D / 8);
     const size_t r = hr % H, h = hr / H;
+    const size_t c8 = slot ^ (r & 7);
     dst[i] = wo[(r * Hq + h) * (D / 8) + c8];
   }
 }

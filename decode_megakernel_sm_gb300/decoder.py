@@ -87,6 +87,10 @@ class Decoder:
         """Takes effect at the next build_schedule."""
         L.mk_set_residual_copies(self.h, copies)
 
+    def set_stage_bytes(self, stage_bytes: int):
+        """Ring stage size (16, 32, 48 or 64 KiB); takes effect at the next step."""
+        L.mk_set_stage_bytes(self.h, stage_bytes)
+
     def set_hold_policy(self, mask: int, prefetch_bytes: int = 256 << 10):
         """Takes effect at the next build_schedule."""
         L.mk_set_hold_policy(self.h, mask, prefetch_bytes)

@@ -186,6 +186,16 @@ int mk_set_wait_timeout(mk_handle* h, uint64_t ns);
  * do not depend on it.                                                     */
 int mk_set_l2_prefetch(mk_handle* h, uint64_t bytes_ahead);
 
+/* Bytes per shared-memory ring stage: 16384, 32768, 49152 or 65536
+ * (default 16384).  The ring holds as many stages (2..16) as the device's
+ * opt-in shared memory allows next to the kernel's fixed buffers.  Bigger
+ * stages hold more weight rows, so every consumer warp has rows in each
+ * stage; smaller stages give a deeper ring.  Results do not depend on it.
+ * Call between steps (not while a step is in flight on another stream);
+ * drops the cached ablation graphs.  MK_ERR_INVALID_ARG for other sizes,
+ * MK_ERR_UNSUPPORTED if two stages no longer fit (the old size is kept). */
+int mk_set_stage_bytes(mk_handle* h, int stage_bytes);
+
 /* Number of partial copies (1..8, default 1) that each residual-stream
  * vector is accumulated into: SM i adds its float atomics into copy
  * i mod copies and readers sum the copies, which spreads the atomic traffic

@@ -31,6 +31,24 @@ def test_ragged_small_shape_parity():
     run_steps(cfg, 4, seed=3)
 
 
+@pytest.mark.parametrize("sb", [32768, 49152, 65536])
+def test_ring_stage_sizes(sb):
+    # the same ragged shape with every larger stage size: more rows, more
+    # cache positions and more down rows per stage, results unchanged
+    cfg = synth.custom(n_layers=3, n_q_heads=6, n_kv_heads=3, ffn=1000, vocab=999,
+                       prefill=(300, 300), steps=3)
+    run_steps(cfg, 3, seed=9, stage_bytes=sb)
+
+
+def test_llama1b_large_stages():
+    r = Run(synth.CONFIGS["llama1b_1k"], seed=3, stage_bytes=65536)
+    try:
+        r.step()
+        r.step()
+    finally:
+        r.close()
+
+
 def test_position_zero_attends_to_itself_only():
     run_steps(synth.custom(prefill=(0, 0), steps=3), 3, seed=5)
 
