@@ -30,6 +30,55 @@ extern const Variant variant_h2048_d128_g4_b1;
 
 using namespace mk;
 
+// Per-schedule device scratch, carved from one allocation (or from the
+// library's fixed array on the no-alloc path).  The tagged block holds the
+// words that carry a step tag; it must read as tag 0 (never a valid epoch)
+// whenever a step is about to run with an epoch that earlier contents may
+// already carry.
+struct Scratch {
+  float *xbuf, *qbuf, *part, *rlog, *lm_val;
+  int *lm_idx, *routes, *err;
+  uint32_t* ctr;
+  float* hglob;             // SiLU(gate)*up (split MLP)
+  TagWord* xt;              // tagged block: x_{2l+2} (split MLP)
+  size_t xbuf_bytes, ctr_bytes, tag_bytes, total;
+};
+
+static size_t al256(size_t n) { return (n + 255) / 256 * 256; }
+
+// Sizes (and, when base != nullptr, pointers) of the scratch for one schedule.
+static Scratch carve_scratch(const mk_model_desc& d, size_t B, size_t kc, size_t splits,
+                             size_t n_lm, size_t n_ctr, char* base) {
+  const size_t L = d.n_layers, H = d.hidden, Hq = d.n_q_heads, D = d.head_dim;
+  const size_t E = d.n_experts > 0 ? d.n_experts : 1;
+  const size_t F = d.ffn > 0 ? d.ffn : 1;
+  const size_t sx = al256(2 * 2 * L * kc * B * H * 4), sq = al256(L * B * Hq * D * 4);
+  const size_t sp = al256(L * B * Hq * splits * (D + 2) * 4);
+  const size_t sr = al256(L * B * E * 4), sl = al256(n_lm * B * 4);
+  const size_t sc = al256(n_ctr * 4), se = 256;
+  const size_t sroute = al256(L * (size_t)(d.top_k > 0 ? d.top_k : 1) * 4);
+  const size_t sxt = al256(L * B * H * 8), sh = al256(L * B * F * 4);
+  Scratch s{};
+  s.xbuf_bytes = sx;
+  s.ctr_bytes = sc;
+  s.tag_bytes = sxt;
+  s.total = sx + sq + sp + sr + 2 * sl + sc + se + sroute + sh + sxt;
+  if (!base) return s;
+  char* q = base;
+  s.xbuf = (float*)q; q += sx;
+  s.qbuf = (float*)q; q += sq;
+  s.part = (float*)q; q += sp;
+  s.rlog = (float*)q; q += sr;
+  s.lm_val = (float*)q; q += sl;
+  s.lm_idx = (int*)q; q += sl;
+  s.ctr = (uint32_t*)q; q += sc;
+  s.err = (int*)q; q += se;
+  s.routes = (int*)q; q += sroute;
+  s.hglob = (float*)q; q += sh;
+  s.xt = (TagWord*)q;
+  return s;
+}
+
 struct mk_handle {
   mk_model_desc d{};
   int dev = 0, n_sm = 0;
@@ -48,13 +97,7 @@ struct mk_handle {
   Instr* sched = nullptr;
   void* scratch = nullptr;
   size_t scratch_bytes = 0;
-  float *xbuf = nullptr, *qbuf = nullptr, *part = nullptr, *rlog = nullptr, *lm_val = nullptr;
-  float* hglob = nullptr;
-  int* lm_idx = nullptr;
-  int* routes = nullptr;
-  uint32_t* ctr = nullptr;
-  int* err = nullptr;
-  size_t xbuf_bytes = 0, ctr_bytes = 0;
+  Scratch sc{};
   std::vector<int> abl_keys;  // ablation launches (keys that own instructions)
   uint32_t epoch = 0;
   unsigned long long timeout_ns = 2000000000ull;
@@ -80,7 +123,6 @@ struct mk_handle {
     if (e_ != cudaSuccess) return MK_ERR_CUDA; \
   } while (0)
 
-static size_t al256(size_t x) { return (x + 255) / 256 * 256; }
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -345,30 +387,11 @@ extern "C" int mk_build_schedule(mk_handle* h, int batch, int max_ctx) {
   if (plan_verify(h->d, batch, p)) return MK_ERR_SCHEDULE;
   if (plan_check(p.q.data(), h->n_sm, p.max_pc, p.n_ctr)) return MK_ERR_SCHEDULE;
   const mk_model_desc& d = h->d;
-  const size_t L = d.n_layers, B = batch, H = d.hidden, Hq = d.n_q_heads, D = d.head_dim;
-  const size_t E = d.n_experts > 0 ? d.n_experts : 1;
-  const size_t sx = al256(2 * 2 * L * (size_t)h->kc * B * H * 4), sq = al256(L * B * Hq * D * 4);
-  const size_t sp = al256(L * B * Hq * (size_t)p.splits * (D + 2) * 4);
-  const size_t sr = al256(L * B * E * 4), sl = al256((size_t)p.n_lm * B * 4);
-  const size_t sc = al256((size_t)p.n_ctr * 4), se = 256;
-  const size_t sroute = al256(L * (size_t)(d.top_k > 0 ? d.top_k : 1) * 4);
-  const size_t sh = al256(L * B * (size_t)(d.ffn > 0 ? d.ffn : 1) * 4);
-  const size_t total = sx + sq + sp + sr + 2 * sl + sc + se + sroute + sh;
+  const size_t L = d.n_layers, B = batch;
+  const size_t total = carve_scratch(d, B, h->kc, p.splits, p.n_lm, p.n_ctr, nullptr).total;
   CK(cudaMalloc(&h->scratch, total));
   h->scratch_bytes = total;
-  char* q = (char*)h->scratch;
-  h->xbuf = (float*)q; q += sx;
-  h->qbuf = (float*)q; q += sq;
-  h->part = (float*)q; q += sp;
-  h->rlog = (float*)q; q += sr;
-  h->lm_val = (float*)q; q += sl;
-  h->lm_idx = (int*)q; q += sl;
-  h->ctr = (uint32_t*)q; q += sc;
-  h->err = (int*)q; q += se;
-  h->routes = (int*)q; q += sroute;
-  h->hglob = (float*)q;
-  h->xbuf_bytes = sx;
-  h->ctr_bytes = sc;
+  h->sc = carve_scratch(d, B, h->kc, p.splits, p.n_lm, p.n_ctr, (char*)h->scratch);
   CK(cudaMemsetAsync(h->scratch, 0, total, h->own));
   CK(cudaMalloc(&h->sched, p.q.size() * sizeof(Instr)));
   CK(cudaMemcpyAsync(h->sched, p.q.data(), p.q.size() * sizeof(Instr), cudaMemcpyHostToDevice,
@@ -406,16 +429,17 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.lm_head = h->lm_head;
   g.final_norm = h->final_norm;
   g.rope = h->rope;
-  g.xbuf = h->xbuf;
-  g.qbuf = h->qbuf;
-  g.part = h->part;
-  g.rlog = h->rlog;
-  g.hglob = h->hglob;
-  g.routes = h->routes;
-  g.lm_val = h->lm_val;
-  g.lm_idx = h->lm_idx;
-  g.ctr = h->ctr;
-  g.err = h->err;
+  g.xbuf = h->sc.xbuf;
+  g.qbuf = h->sc.qbuf;
+  g.part = h->sc.part;
+  g.rlog = h->sc.rlog;
+  g.xt = h->sc.xt;
+  g.hglob = h->sc.hglob;
+  g.routes = h->sc.routes;
+  g.lm_val = h->sc.lm_val;
+  g.lm_idx = h->sc.lm_idx;
+  g.ctr = h->sc.ctr;
+  g.err = h->sc.err;
   g.tokens = tok;
   g.positions = pos;
   g.logits = logits;
@@ -441,6 +465,7 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.Fe = d.expert_ffn;
   g.Fs = d.shared_ffn;
   g.kc = h->kc;
+  g.xtag = mlp_split(d) ? 1 : 0;
   g.eps = d.rms_eps;
   g.lm_ctr = CtrMap{d.n_kv_heads, d.n_layers}.lm();
   g.n_lm = h->plan.n_lm;
@@ -471,9 +496,10 @@ extern "C" int mk_decode_step(mk_handle* h, const int32_t* d_tokens, const int32
 }
 
 static void reset_after_error(mk_handle* h) {
-  cudaMemset(h->ctr, 0, h->ctr_bytes);
-  cudaMemset(h->xbuf, 0, h->xbuf_bytes);
-  cudaMemset(h->err, 0, 4 * sizeof(int));
+  cudaMemset(h->sc.ctr, 0, h->sc.ctr_bytes);
+  cudaMemset(h->sc.xbuf, 0, h->sc.xbuf_bytes);
+  cudaMemset(h->sc.xt, 0, h->sc.tag_bytes);  // the next step is epoch 1 again
+  cudaMemset(h->sc.err, 0, 4 * sizeof(int));
   cudaDeviceSynchronize();
   h->epoch = 0;
 }
@@ -501,7 +527,7 @@ extern "C" int mk_decode_step_host(mk_handle* h, const int32_t* h_tokens,
     CK(cudaMemcpyAsync(h_logits, h->d_logits, (size_t)B * h->d.vocab * 4, cudaMemcpyDeviceToHost,
                        s));
   CK(cudaMemcpyAsync(h_argmax, h->d_am, B * 4, cudaMemcpyDeviceToHost, s));
-  CK(cudaMemcpyAsync(h->h_err, h->err, 4 * sizeof(int), cudaMemcpyDeviceToHost, s));
+  CK(cudaMemcpyAsync(h->h_err, h->sc.err, 4 * sizeof(int), cudaMemcpyDeviceToHost, s));
   CK(cudaStreamSynchronize(s));
   if (h->h_err[0] != 0) {
     const int code = h->h_err[0];
@@ -569,8 +595,10 @@ extern "C" int mk_decode_step_ablation(mk_handle* h, int mode, const int32_t* d_
     g.zero_next = 0;
     cudaGraph_t graph = nullptr;
     CK(cudaStreamBeginCapture(h->own, cudaStreamCaptureModeThreadLocal));
-    cudaError_t e1 = cudaMemsetAsync(h->ctr, 0, h->ctr_bytes, h->own);
-    cudaError_t e2 = cudaMemsetAsync(h->xbuf, 0, h->xbuf_bytes, h->own);
+    cudaError_t e1 = cudaMemsetAsync(h->sc.ctr, 0, h->sc.ctr_bytes, h->own);
+    cudaError_t e2 = cudaMemsetAsync(h->sc.xbuf, 0, h->sc.xbuf_bytes, h->own);
+    // every replay runs as epoch 1: clear the previous replay's step tags
+    if (!e2) e2 = cudaMemsetAsync(h->sc.xt, 0, h->sc.tag_bytes, h->own);
     cudaError_t e3 = launch_phases(h, g, h->own, false);
     cudaError_t e4 = cudaStreamEndCapture(h->own, &graph);
     if (e1 || e2 || e3 || e4) {
@@ -593,8 +621,8 @@ extern "C" int mk_decode_step_ablation(mk_handle* h, int mode, const int32_t* d_
 extern "C" int mk_sync_status(mk_handle* h, void* stream) {
   if (!h) return MK_ERR_INVALID_ARG;
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MK_ERR_CUDA;
-  if (!h->err) return MK_OK;
-  if (cudaMemcpy(h->h_err, h->err, 4 * sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (!h->sc.err) return MK_OK;
+  if (cudaMemcpy(h->h_err, h->sc.err, 4 * sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
     return MK_ERR_CUDA;
   if (h->h_err[0] != 0) {
     const int code = h->h_err[0];
@@ -641,14 +669,9 @@ extern "C" int mk_decode_step_noalloc(mk_handle* h, const int32_t* d_tokens,
   if (dev != h->dev || dev < 0 || dev >= 64) return MK_ERR_INVALID_ARG;
   // the same carve as the handle's scratch, sized for this handle's schedule
   const mk_model_desc& d = h->d;
-  const size_t L = d.n_layers, B = h->batch, H = d.hidden, Hq = d.n_q_heads, D = d.head_dim;
-  const size_t E = d.n_experts > 0 ? d.n_experts : 1;
-  const size_t sx = al256(2 * 2 * L * (size_t)h->kc * B * H * 4), sq = al256(L * B * Hq * D * 4);
-  const size_t sp = al256(L * B * Hq * (size_t)h->plan.splits * (D + 2) * 4);
-  const size_t sr = al256(L * B * E * 4), sl = al256((size_t)h->plan.n_lm * B * 4);
-  const size_t sc = al256((size_t)h->plan.n_ctr * 4), se = 256;
-  const size_t sh = al256(L * B * (size_t)(d.ffn > 0 ? d.ffn : 1) * 4);
-  if (sx + sq + sp + sr + 2 * sl + sc + se + sh > MK_NOALLOC_SCRATCH_BYTES) return MK_ERR_SCRATCH;
+  const size_t need =
+      carve_scratch(d, h->batch, h->kc, h->plan.splits, h->plan.n_lm, h->plan.n_ctr, nullptr).total;
+  if (need > MK_NOALLOC_SCRATCH_BYTES) return MK_ERR_SCRATCH;
   // set-up, once per device, with that device current: the host-side name of
   // the array is not a device address, so look the address up
   void* base = nullptr;
@@ -665,22 +688,25 @@ extern "C" int mk_decode_step_noalloc(mk_handle* h, const int32_t* d_tokens,
     base = g_noalloc_base[dev];
   }
   cudaStream_t s = (cudaStream_t)stream;
-  char* q = (char*)base;
+  const Scratch sc =
+      carve_scratch(d, h->batch, h->kc, h->plan.splits, h->plan.n_lm, h->plan.n_ctr, (char*)base);
   Globals g = make_globals(h, d_tokens, d_positions, d_logits, d_argmax);
-  g.xbuf = (float*)q; q += sx;
-  g.qbuf = (float*)q; q += sq;
-  g.part = (float*)q; q += sp;
-  g.rlog = (float*)q; q += sr;
-  g.lm_val = (float*)q; q += sl;
-  g.lm_idx = (int*)q; q += sl;
-  g.ctr = (uint32_t*)q; q += sc;
-  g.err = (int*)q; q += se;
-  g.hglob = (float*)q;
+  g.xbuf = sc.xbuf;
+  g.qbuf = sc.qbuf;
+  g.part = sc.part;
+  g.rlog = sc.rlog;
+  g.lm_val = sc.lm_val;
+  g.lm_idx = sc.lm_idx;
+  g.ctr = sc.ctr;
+  g.err = sc.err;
+  g.xt = sc.xt;
+  g.hglob = sc.hglob;
   // the array keeps the previous call's contents: clear what must start at
-  // zero (residual accumulators of both parities, counters, error word) and
-  // run the step as epoch 1
-  CK(cudaMemsetAsync(g.xbuf, 0, sx, s));
-  CK(cudaMemsetAsync(g.ctr, 0, sc + se, s));
+  // zero (residual accumulators of both parities, counters, error word, step
+  // tags) and run the step as epoch 1
+  CK(cudaMemsetAsync(g.xbuf, 0, sc.xbuf_bytes, s));
+  CK(cudaMemsetAsync(g.ctr, 0, sc.ctr_bytes + 256, s));
+  CK(cudaMemsetAsync(g.xt, 0, sc.tag_bytes, s));
   g.epoch = 1;
   g.parity = 1;
   g.zero_next = 0;
@@ -783,7 +809,7 @@ extern "C" int mk_get_routes(mk_handle* h, int32_t* out, size_t n) {
   const size_t need = (size_t)h->d.n_layers * h->d.top_k;
   if (n < need) return MK_ERR_INVALID_ARG;
   CK(cudaDeviceSynchronize());
-  CK(cudaMemcpy(out, h->routes, need * sizeof(int32_t), cudaMemcpyDeviceToHost));
+  CK(cudaMemcpy(out, h->sc.routes, need * sizeof(int32_t), cudaMemcpyDeviceToHost));
   return MK_OK;
 }
 

@@ -31,7 +31,8 @@ struct Ctx {
   int* pos;     // [NB]
   int* topk;    // [NB][K] routed expert ids
   float* topw;  // [NB][K] routed expert weights
-  int* flag;    // abort flag shared by the consumer warps
+  int* flag;    // [0] abort flag of the dependency wait, [2] a tagged-input poll failed
+                // (both shared by the consumer warps; [1] belongs to the producer)
   Ring ring;
   int tid, warp, lane;
   int pc;
@@ -50,9 +51,12 @@ MK_DEV bool dep_wait(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   if (c.tid == 0) {
     if (g.trace) c.tw0 = gtimer();
     bool ok = true;
-    if (I.wait_ctr != NO_CTR) ok = wait_counter(g, I.wait_ctr, g.epoch * I.wait_cnt, c.pc, I.op);
+    if (!(I.flags & F_TAG_WAIT)) {
+      if (I.wait_ctr != NO_CTR) ok = wait_counter(g, I.wait_ctr, g.epoch * I.wait_cnt, c.pc, I.op);
+    }  // F_TAG_WAIT: the op polls its tagged inputs itself
     if (ok && peek_err(g)) ok = false;
     *c.flag = ok ? 0 : 1;
+    c.flag[2] = 0;
     if (g.trace) c.tw1 = gtimer();
   }
   consumer_bar();
@@ -211,8 +215,23 @@ MK_DEV void norm_gain(NormGain<HT>& ng, const uint16_t* gain, int tid) {
 }
 
 template <int HT, int D, int HPG, int NB>
-MK_DEV void norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const NormGain<HT>& ng) {
+MK_DEV bool norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const NormGain<HT>& ng) {
   constexpr int GROUPS = NormGain<HT>::GROUPS, GPT = NormGain<HT>::GPT;
+  // split MLP: x_{2l+2} (j even, j > 0) arrives as tagged words from the
+  // down rows' owners; each thread polls its own 8-element groups
+  const bool tagged = g.xtag && j > 0 && (j & 1) == 0;
+  bool ok = true;
+  if constexpr (NB == 1) {
+    if (tagged) {  // this thread's groups, polled together straight into xn
+      uint32_t valid = 0;
+#pragma unroll
+      for (int q = 0; q < GPT; q++)
+        if (c.tid + q * NCT < GROUPS) valid |= 1u << q;
+      ok = poll_tag_groups_to<GPT, 4>(g, g.xt + (size_t)(j / 2 - 1) * HT + 8 * c.tid,
+                                      (size_t)NCT * 8, valid, g.epoch, c.xn + 8 * c.tid, NCT * 8,
+                                      c.pc, OP_QKV);
+    }
+  }
   float ss[NB];
 #pragma unroll
   for (int b = 0; b < NB; b++) ss[b] = 0.f;
@@ -227,6 +246,11 @@ MK_DEV void norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const No
         if (j == 0) {
           const uint4 w = __ldg((const uint4*)(g.embed + (size_t)c.tok[b] * HT) + gi);
           unpack8(w, v);
+        } else if (tagged) {  // polled into xn above (batch 1 only: the split MLP)
+          const float4* p = (const float4*)(c.xn + (size_t)b * HT) + 2 * gi;
+          const float4 a0 = p[0], a1 = p[1];
+          v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
+          v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
         } else {
 #pragma unroll
           for (int k = 0; k < 8; k++) v[k] = 0.f;
@@ -253,7 +277,9 @@ MK_DEV void norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const No
     const float t = warp_sum(ss[b]);
     if (c.lane == 0) c.red[c.warp * NB + b] = t;
   }
+  if (!ok) c.flag[2] = 1;  // read by every consumer thread after the barrier
   consumer_bar();
+  if (c.flag[2]) return false;
   float rs[NB];
 #pragma unroll
   for (int b = 0; b < NB; b++) {
@@ -279,6 +305,7 @@ MK_DEV void norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const No
     }
   }
   consumer_bar();
+  return true;
 }
 
 // ----------------------------------------------------------------- GEMV ----
@@ -413,7 +440,7 @@ MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
         if (b < g.B) cs[b] = ((const float2*)g.rope)[(size_t)c.pos[b] * (D / 2) + t];
   }
   if (!dep_wait(c, g, I)) return false;
-  if (!cached) norm_apply(c, g, 2 * I.layer, ng);
+  if (!cached && !norm_apply(c, g, 2 * I.layer, ng)) return false;
   c.mark(g, 0);
   float xr[HT / 32];
   if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
@@ -666,13 +693,26 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   float* xr_s = c.xn;  // residual rows of this slice, [NB][nr] with nr <= H (head-0 slices)
   if (resid) {
     const int nr = (int)(I.r1 - I.r0);
+    const bool tagged = g.xtag && l > 0;  // x_{2l} from the down rows' owners
+    bool okr = true;
     for (int t = c.tid; t < NB * nr; t += NCT) {
       const int b = t / nr, r = t % nr;
-      xr_s[t] = b < g.B ? x_in(g, 2 * l, c.tok, b, (int)I.r0 + r) : 0.f;
+      float v = 0.f;
+      if (b < g.B) {
+        if (tagged) {
+          const TagWord* p = g.xt + ((size_t)(l - 1) * g.B + b) * g.H + I.r0 + r;
+          if (!poll_tag1(g, p, g.epoch, v, c.pc, I.op)) okr = false;
+        } else {
+          v = x_in(g, 2 * l, c.tok, b, (int)I.r0 + r);
+        }
+      }
+      xr_s[t] = v;
     }
+    if (!okr) c.flag[2] = 1;
   }
   c.mark(g, 0);
   consumer_bar();
+  if (c.flag[2]) return false;
   Seg s[2];
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
   const uint4 zero = make_uint4(0, 0, 0, 0);
@@ -804,7 +844,7 @@ MK_DEV bool op_router(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   NormGain<HT> ng;
   norm_gain(ng, Lp.mlp_norm, c.tid);
   if (!dep_wait(c, g, I)) return false;
-  norm_apply(c, g, 2 * I.layer + 1, ng);
+  if (!norm_apply(c, g, 2 * I.layer + 1, ng)) return false;
   float xr[HT / 32];
   if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
   Seg s[2];
@@ -835,7 +875,7 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   NormGain<HT> ng;
   if (!cached) norm_gain(ng, Lp.mlp_norm, c.tid);
   if (!dep_wait(c, g, I)) return false;
-  if (!cached) norm_apply(c, g, 2 * l + 1, ng);
+  if (!cached && !norm_apply(c, g, 2 * l + 1, ng)) return false;
   c.mark(g, 0);
   if (routed) {
     if (c.warp == 0) {
@@ -933,7 +973,7 @@ MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   NormGain<HT> ng;
   if (!cached) norm_gain(ng, Lp.mlp_norm, c.tid);
   if (!dep_wait(c, g, I)) return false;
-  if (!cached) norm_apply(c, g, 2 * l + 1, ng);
+  if (!cached && !norm_apply(c, g, 2 * l + 1, ng)) return false;
   c.mark(g, 0);
   float xr[HT / 32];
   if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
@@ -1038,7 +1078,7 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I
       float y = 0.f;
 #pragma unroll
       for (int w = 0; w < NCW; w++) y += part[w * MAX_DOWN_ROWS + c.tid];
-      xres(g, 2 * l + 2, 0)[I.r0 + c.tid] = res + y;
+      st_tag(g.xt + (size_t)l * g.B * g.H + I.r0 + c.tid, res + y, g.epoch);
     }
     consumer_bar();
     return true;
@@ -1053,7 +1093,7 @@ MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   NormGain<HT> ng;
   norm_gain(ng, g.final_norm, c.tid);
   if (!dep_wait(c, g, I)) return false;
-  norm_apply(c, g, 2 * g.L, ng);
+  if (!norm_apply(c, g, 2 * g.L, ng)) return false;
   c.mark(g, 0);
   float xr[HT / 32];
   if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
@@ -1487,7 +1527,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
         t[6] = c.ring.waited;  // warp 0's time blocked on ring data during this instruction
         c.ring.waited = 0;
       }
-      if (I.sig_ctr != NO_CTR) red_release(g.ctr + I.sig_ctr, 1u);
+      if (I.sig_ctr != NO_CTR) {
+        if (I.flags & F_RELAXED_SIG)
+          red_relaxed(g.ctr + I.sig_ctr, 1u);
+        else
+          red_release(g.ctr + I.sig_ctr, 1u);
+      }
+      if (g.trace) g.trace[((size_t)blockIdx.x * g.max_pc + pc) * 8 + 7] = gtimer();
       *(volatile int*)(misc + 1) = ++finished;
     }
   }

@@ -103,6 +103,18 @@ MK_DEV uint32_t ld_acquire(const uint32_t* p) {
   return v;
 }
 
+MK_DEV uint32_t ld_relaxed(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// A reduction with no release semantics: it orders nothing before it, and
+// so does not wait for this SM's outstanding memory operations.
+MK_DEV void red_relaxed(uint32_t* p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 MK_DEV void red_release(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -145,14 +157,110 @@ MK_DEV void set_err(const Globals& g, int code, int pc, int op) {
   }
 }
 
-// Spin (acquire) until ctr[idx] has reached `target` (wrap-safe).  Returns
-// false after an error anywhere in the grid or after the time limit.
-MK_DEV bool wait_counter(const Globals& g, uint32_t idx, uint32_t target, int pc, int op) {
-  const uint32_t* p = g.ctr + idx;
-  if ((int32_t)(ld_acquire(p) - target) >= 0) return true;
+// ---- tagged words --------------------------------------------------------
+// A value produced by exactly one writer per step travels as a 64-bit word
+// {f32 value, u32 tag}, tag = the step's epoch, written with one relaxed
+// 64-bit store.  Aligned 64-bit accesses are single-copy atomic, so a
+// reader that sees this step's tag sees the value stored with it: the writer
+// needs no release fence, and the reader needs no counter round trip before
+// it loads the data -- it polls the data itself.
+MK_DEV void st_tag(TagWord* p, float v, uint32_t tag) {
+  const unsigned long long w = ((unsigned long long)tag << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+
+MK_DEV void ld_tag2(const TagWord* p, TagWord& a, TagWord& b) {
+  unsigned long long x, y;
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(x), "=l"(y) : "l"(p) : "memory");
+  a = TagWord{(uint32_t)x, (uint32_t)(x >> 32)};
+  b = TagWord{(uint32_t)y, (uint32_t)(y >> 32)};
+}
+
+MK_DEV TagWord ld_tag1(const TagWord* p) {
+  unsigned long long x;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(x) : "l"(p) : "memory");
+  return TagWord{(uint32_t)x, (uint32_t)(x >> 32)};
+}
+
+// G groups of NP tagged pairs, group q at p + q * stride (in words); only
+// the groups whose bit is set in `valid` are read, and their values land in
+// memory (shared memory, as a rule): group q's 2*NP floats at
+// dst + q * dst_stride.  Every first read is issued before any tag is
+// checked, so a thread's whole input costs one round trip once the last
+// writer has stored; only stale pairs are re-read.  Bounded like every
+// wait: false if the grid has failed or the deadline passed (then the
+// error word is set).
+template <int G, int NP>
+MK_DEV bool poll_tag_groups_to(const Globals& g, const TagWord* p, size_t stride, uint32_t valid,
+                               uint32_t tag, float* dst, int dst_stride, int pc, int op) {
+  static_assert(G * NP <= 32, "one bit per pair");
+  uint32_t miss = 0;
+#pragma unroll
+  for (int q = 0; q < G; q++)
+#pragma unroll
+    for (int i = 0; i < NP; i++) {
+      if (valid & (1u << q)) {
+        TagWord a, b;
+        ld_tag2(p + q * stride + 2 * i, a, b);
+        dst[q * dst_stride + 2 * i] = __uint_as_float(a.bits);
+        dst[q * dst_stride + 2 * i + 1] = __uint_as_float(b.bits);
+        if (a.tag != tag || b.tag != tag) miss |= 1u << (q * NP + i);
+      }
+    }
+  if (miss == 0) return true;
   const uint64_t t0 = gtimer();
   for (uint32_t it = 1;; it++) {
-    if ((int32_t)(ld_acquire(p) - target) >= 0) return true;
+    for (int k = 0; k < G * NP; k++) {
+      const uint32_t bit = 1u << k;
+      if (miss & bit) {
+        const int q = k / NP, i = k % NP;
+        TagWord a, b;
+        ld_tag2(p + q * stride + 2 * i, a, b);
+        dst[q * dst_stride + 2 * i] = __uint_as_float(a.bits);
+        dst[q * dst_stride + 2 * i + 1] = __uint_as_float(b.bits);
+        if (a.tag == tag && b.tag == tag) miss &= ~bit;
+      }
+    }
+    if (miss == 0) return true;
+    if ((it & 15) == 0) {
+      if (peek_err(g)) return false;
+      if (gtimer() - t0 > g.timeout_ns) {
+        set_err(g, MK_ERR_TIMEOUT, pc, op);
+        return false;
+      }
+    }
+  }
+}
+
+// One tagged float, polled the same way.
+MK_DEV bool poll_tag1(const Globals& g, const TagWord* p, uint32_t tag, float& v, int pc, int op) {
+  TagWord a = ld_tag1(p);
+  if (a.tag != tag) {
+    const uint64_t t0 = gtimer();
+    for (uint32_t it = 1; (a = ld_tag1(p)).tag != tag; it++) {
+      if ((it & 15) == 0) {
+        if (peek_err(g)) return false;
+        if (gtimer() - t0 > g.timeout_ns) {
+          set_err(g, MK_ERR_TIMEOUT, pc, op);
+          return false;
+        }
+      }
+    }
+  }
+  v = __uint_as_float(a.bits);
+  return true;
+}
+
+// Spin (acquire) until ctr[idx] has reached `target` (wrap-safe).  Returns
+// false after an error anywhere in the grid or after the time limit.
+template <bool ACQUIRE = true>
+MK_DEV bool wait_counter(const Globals& g, uint32_t idx, uint32_t target, int pc, int op) {
+  const uint32_t* p = g.ctr + idx;
+  auto ld = [](const uint32_t* a) { return ACQUIRE ? ld_acquire(a) : ld_relaxed(a); };
+  if ((int32_t)(ld(p) - target) >= 0) return true;
+  const uint64_t t0 = gtimer();
+  for (uint32_t it = 1;; it++) {
+    if ((int32_t)(ld(p) - target) >= 0) return true;
     if ((it & 15) == 0) {
       if (peek_err(g)) return false;
       if (gtimer() - t0 > g.timeout_ns) {

@@ -45,6 +45,10 @@ enum Flag : uint8_t {
   F_SHARED = 4,      // MoE MLP: shared-expert columns (weight 1, no routing)
   F_HOLD = 8,        // producer: warm L2 with this instruction's data, then issue its ring
                      // copies only after the consumers released every earlier instruction
+  F_TAG_WAIT = 16,   // inputs arrive as tagged words: poll them, not the wait counter
+                     // (which still models the dependency for the schedule checker)
+  F_RELAXED_SIG = 32,// every consumer polls tagged outputs: signal with a relaxed reduction,
+                     // which does not wait for this SM's earlier memory operations
 };
 
 // Which instructions the planner marks F_HOLD (first of a run of the op on
@@ -128,6 +132,13 @@ struct LayerPtrs {
   uint16_t* vc;
 };
 
+// A value that one writer produces once per step, with that step's tag
+// (the epoch); read and written as one aligned 64-bit word.
+struct alignas(8) TagWord {
+  uint32_t bits;  // the f32 value's bits
+  uint32_t tag;   // epoch of the step that wrote it (0: never written)
+};
+
 // Kernel parameter block (passed by value as __grid_constant__).
 struct Globals {
   const Instr* sched;
@@ -141,6 +152,7 @@ struct Globals {
   float* part;             // [L][B][Hq][splits][D+2]: o[D], m, l  (log2 domain)
   float* rlog;             // [L][B][E] router logits
   float* hglob;            // [L][B][F] SiLU(gate)*up (split MLP)
+  TagWord* xt;             // [L][B][H] tagged x_{2l+2} (split MLP: written once, by row owners)
   int* routes;             // [L][K] expert ids chosen at the last step (MoE, batch 1)
   float* lm_val;           // [n_lm][B]
   int* lm_idx;             // [n_lm][B]
@@ -157,7 +169,9 @@ struct Globals {
   int E, K, Fe, Fs;
   int kc;                  // partial copies of each residual vector (1..8)
   float eps;
-  uint32_t epoch;          // step number (>= 1); counter targets are epoch * count
+  uint32_t epoch;          // step number (>= 1); counter targets are epoch * count, and
+                           // tagged words written in this step carry tag == epoch
+  int xtag;                // x_{2l+2} lives in xt (split MLP) rather than in xbuf
   int parity;              // epoch & 1: which residual buffer set this step uses
   uint32_t lm_ctr;
   int n_lm;

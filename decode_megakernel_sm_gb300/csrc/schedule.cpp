@@ -106,6 +106,8 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
         I.r1 = (uint32_t)e;
         I.flags = first ? 0 : F_NORM_CACHED;
         if (l > 0) I.wait_ctr = cm.mlp(l - 1);
+        // split MLP: the previous layer's down rows arrive as tagged words
+        if (l > 0 && mlp_split(d)) I.flags |= F_TAG_WAIT;
         I.sig_ctr = cm.qkv(l, (int)g);
         qs[i].push_back(I);
         bytes[i] += (double)(e - a) * H * 2;
@@ -203,6 +205,9 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
           Instr I = mk(OP_MLP_DOWN, l);
           I.r0 = (uint32_t)a;
           I.r1 = (uint32_t)e;
+          // its rows of x_{2l+2} leave as tagged words, polled by their
+          // consumers: the signal needs no release
+          I.flags = F_RELAXED_SIG;
           I.wait_ctr = cm.mlp_up(l);
           I.sig_ctr = cm.mlp(l);
           qs[i].push_back(I);
@@ -282,6 +287,7 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
     I.r0 = (uint32_t)a;
     I.r1 = (uint32_t)b;
     I.wait_ctr = cm.mlp(L - 1);
+    if (mlp_split(d)) I.flags |= F_TAG_WAIT;
     I.aux = (uint32_t)n_lm++;
     qs[i].push_back(I);
     bytes[i] += (double)(b - a) * H * 2;
@@ -312,8 +318,9 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
     for (auto& I : q)
       if (I.sig_ctr != NO_CTR) cnt[I.sig_ctr]++;
   for (auto& q : qs)
-    for (auto& I : q)
+    for (auto& I : q) {
       if (I.wait_ctr != NO_CTR) I.wait_cnt = cnt[I.wait_ctr];
+    }
 
   // ---- flatten, HALT-padded
   size_t mx = 0, total = 0;
@@ -362,6 +369,27 @@ int plan_verify(const mk_model_desc& d, int B, const PlanOut& p) {
     v[i] = 1;
     return true;
   };
+  const CtrMap cm{Hkv, L};
+  // signals per counter, and whether any signaller of it signals without
+  // release (F_RELAXED_SIG): such a counter orders no data, so only waiters
+  // that poll tagged inputs may use it
+  std::vector<uint32_t> sig_count(p.n_ctr, 0);
+  std::vector<uint8_t> silent(p.n_ctr, 0);
+  for (const Instr& I : p.q) {
+    if (I.op == OP_HALT || I.sig_ctr == NO_CTR) continue;
+    if (I.sig_ctr >= (uint32_t)p.n_ctr) return 28;
+    sig_count[I.sig_ctr]++;
+    if (I.flags & F_RELAXED_SIG) silent[I.sig_ctr] = 1;
+  }
+  for (const Instr& I : p.q) {
+    if (I.op == OP_HALT) continue;
+    const bool tag_wait = (I.flags & F_TAG_WAIT) != 0;
+    // only these consumers poll tagged inputs, and only in the split MLP
+    if (tag_wait && !(mlp_split(d) && (I.op == OP_QKV || I.op == OP_LMHEAD))) return 29;
+    if ((I.flags & F_RELAXED_SIG) && !(mlp_split(d) && I.op == OP_MLP_DOWN)) return 29;
+    if (!tag_wait && I.wait_ctr != NO_CTR && I.wait_ctr < (uint32_t)p.n_ctr && silent[I.wait_ctr])
+      return 30;
+  }
   for (const Instr& I : p.q) {
     const int l = I.layer;
     switch (I.op) {
@@ -444,12 +472,17 @@ int plan_verify(const mk_model_desc& d, int B, const PlanOut& p) {
 }
 
 // In-order execution of every queue under the wait semantics: an
-// instruction runs once its counter has received wait_cnt signals.  A
-// deadlock is any state where no queue can advance before all reach HALT.
+// instruction runs once its counter has received wait_cnt signals.  Two
+// counts are kept per counter: every signal, which is what a consumer of
+// tagged inputs (F_TAG_WAIT) waits for, and the release signals only (not
+// F_RELAXED_SIG), the only ones that order the data a plain counter wait
+// then reads -- a plain wait that needs a relaxed signal never completes
+// here.  A deadlock is any state where no queue can advance before all
+// reach HALT.
 int plan_check(const Instr* q, int n_sm, int max_pc, int n_ctr) {
   if (!q || n_sm <= 0 || max_pc <= 0 || n_ctr <= 0) return MK_ERR_INVALID_ARG;
   std::vector<int> pc(n_sm, 0);
-  std::vector<uint64_t> cnt(n_ctr, 0);
+  std::vector<uint64_t> cnt(n_ctr, 0), dev(n_ctr, 0);
   for (;;) {
     bool progress = false, done = true;
     for (int s = 0; s < n_sm; s++) {
@@ -457,13 +490,15 @@ int plan_check(const Instr* q, int n_sm, int max_pc, int n_ctr) {
         if (pc[s] >= max_pc) break;
         const Instr& I = q[(size_t)s * max_pc + pc[s]];
         if (I.op == OP_HALT) break;
+        const bool tag_wait = (I.flags & F_TAG_WAIT) != 0;
         if (I.wait_ctr != NO_CTR) {
           if (I.wait_ctr >= (uint32_t)n_ctr) return MK_ERR_SCHEDULE;
-          if (cnt[I.wait_ctr] < I.wait_cnt) break;
+          if ((tag_wait ? cnt : dev)[I.wait_ctr] < I.wait_cnt) break;
         }
         if (I.sig_ctr != NO_CTR) {
           if (I.sig_ctr >= (uint32_t)n_ctr) return MK_ERR_SCHEDULE;
           cnt[I.sig_ctr]++;
+          if (!(I.flags & F_RELAXED_SIG)) dev[I.sig_ctr]++;
         }
         pc[s]++;
         progress = true;

@@ -3,7 +3,8 @@
 Each instruction slot holds %globaltimer stamps (ns): the producer's first
 bulk copy of the instruction, the consumers' wait start and end, the end of
 the op's prologue phase (norm / split combine), the end of its ring loop and
-the body end (a missing mid stamp falls back to the previous one).  `summarize` attributes the step's time the way "Megakernels:
+the body end, and the moment the completion signal (a release reduction)
+retired (a missing mid stamp falls back to the previous one).  `summarize` attributes the step's time the way "Megakernels:
 Deleting the Kernel Boundary", section "What it buys, and where the time
 still goes", breaks down a forward pass: time spent waiting on dependencies
 versus time spent in instruction bodies, per opcode and per layer.
@@ -31,7 +32,8 @@ def _rows(trace, queues, n_sm, max_pc):
                 continue
             m0 = ts[3] if ts[3] >= ts[2] else ts[2]
             m1 = ts[4] if ts[4] >= m0 else m0
-            rows.append((s, pc, I.op, I.layer, ts[0], ts[1], ts[2], ts[5], m0, m1, ts[6]))
+            rows.append((s, pc, I.op, I.layer, ts[0], ts[1], ts[2], ts[5], m0, m1, ts[6],
+                         ts[7] if ts[7] >= ts[5] else ts[5]))
             base = ts[1] if base is None else min(base, ts[1])
     return rows, base
 
@@ -42,7 +44,7 @@ def summarize(trace, queues, n_sm: int, max_pc: int) -> dict:
         return {}
     end = max(r[7] for r in rows)
     by_op = {}
-    for s, pc, op, layer, tp, tw0, tw1, te, m0, m1, rw in rows:
+    for s, pc, op, layer, tp, tw0, tw1, te, m0, m1, rw, tsig in rows:
         d = by_op.setdefault(L.OP_NAMES[op], {"n": 0, "wait_us": 0.0, "body_us": 0.0,
                                                "max_wait_us": 0.0, "prologue_us": 0.0,
                                                "ring_us": 0.0, "epilogue_us": 0.0,
@@ -60,7 +62,7 @@ def summarize(trace, queues, n_sm: int, max_pc: int) -> dict:
             d[f"mean_{k}_us"] = d[f"{k}_us"] / d["n"]
     # per layer and phase: when the last instruction of the phase finished
     phase_end = {}
-    for s, pc, op, layer, tp, tw0, tw1, te, m0, m1, rw in rows:
+    for s, pc, op, layer, tp, tw0, tw1, te, m0, m1, rw, tsig in rows:
         k = (layer, L.OP_NAMES[op])
         phase_end[k] = max(phase_end.get(k, 0), te - base)
     layers = sorted({k[0] for k in phase_end})
@@ -74,7 +76,7 @@ def summarize(trace, queues, n_sm: int, max_pc: int) -> dict:
         prev = e
     busy = np.zeros(n_sm)
     waited = np.zeros(n_sm)
-    for s, pc, op, layer, tp, tw0, tw1, te, m0, m1, rw in rows:
+    for s, pc, op, layer, tp, tw0, tw1, te, m0, m1, rw, tsig in rows:
         busy[s] += te - tw1
         waited[s] += tw1 - tw0
     return {"step_us": (end - base) / 1e3, "by_op": by_op, "per_layer": per_layer,
@@ -85,12 +87,14 @@ def summarize(trace, queues, n_sm: int, max_pc: int) -> dict:
 def chrome_trace(trace, queues, n_sm: int, max_pc: int, path: str):
     rows, base = _rows(trace, queues, n_sm, max_pc)
     ev = []
-    for s, pc, op, layer, tp, tw0, tw1, te, m0, m1, rw in rows:
+    for s, pc, op, layer, tp, tw0, tw1, te, m0, m1, rw, tsig in rows:
         name = f"{L.OP_NAMES[op]} L{layer}"
         ev.append({"name": "wait " + name, "ph": "X", "pid": 0, "tid": s,
                    "ts": (tw0 - base) / 1e3, "dur": (tw1 - tw0) / 1e3})
         ev.append({"name": name, "ph": "X", "pid": 0, "tid": s, "ts": (tw1 - base) / 1e3,
-                   "dur": (te - tw1) / 1e3})
+                   "dur": (te - tw1) / 1e3,
+                   "args": {"prologue_end": (m0 - base) / 1e3, "ring_end": (m1 - base) / 1e3,
+                            "signal_done": (tsig - base) / 1e3}})
         if tp:
             ev.append({"name": "issue " + name, "ph": "i", "pid": 1, "tid": s,
                        "ts": (tp - base) / 1e3, "s": "t"})

@@ -252,7 +252,10 @@ int mk_debug_drop_instruction(mk_handle* h, int sm, int pc);
  * first bulk copy of the instruction, [1] the consumers' wait start, [2]
  * wait end, [3] end of the op's prologue phase (norm / split combine), [4]
  * end of its ring loop, [5] body end, [6] nanoseconds warp 0 spent waiting
- * for ring data during the instruction, [7] unused (0).  Slots of instructions that did not run keep their old values.
+ * for ring data during the instruction, [7] the moment the instruction's
+ * completion signal (a release reduction, which first waits for the SM's
+ * earlier memory operations) retired.  Slots of instructions that did not
+ * run keep their old values.
  * mk_set_trace(h, 1) allocates the buffer (after mk_build_schedule; a new
  * schedule turns tracing off); mk_get_trace waits for the device and copies
  * the n_sm * max_pc * 8 values to `out` (n = capacity in values).         */

@@ -193,3 +193,29 @@ def test_plan_rejects_bad_arguments():
     with pytest.raises(L.MkError) as e:
         L.mk_plan(d2, 1, 64, 8)
     assert e.value.status == L.MK_ERR_UNSUPPORTED
+
+
+def test_split_mlp_residual_hop_is_tagged():
+    # dense batch 1: the down rows publish x_{2l+2} as tagged words and signal
+    # without release; its readers (next QKV, LM head) poll the words
+    cfg, d = desc("llama1b_1k")
+    st, q = L.mk_plan(d, 1, cfg["max_seq"], 152)
+    n = 152 * st["max_pc"]
+    ops = [q[i] for i in range(n) if q[i].op != 0]
+    F_TAG_WAIT, F_RELAXED_SIG = 16, 32
+    assert all(I.flags & F_RELAXED_SIG for I in ops if I.op == 9)
+    assert all(I.flags & F_TAG_WAIT for I in ops if I.op == 5)
+    assert all(bool(I.flags & F_TAG_WAIT) == (I.layer > 0) for I in ops if I.op == 1)
+    assert not any(I.flags & (F_TAG_WAIT | F_RELAXED_SIG) for I in ops if I.op in (2, 3, 8))
+
+
+def test_checker_rejects_plain_wait_on_relaxed_signals():
+    # relaxed signals order no data: a consumer that waits on such a counter
+    # and then reads untagged data could read stale values, so the checker
+    # counts only release signals for plain waits and reports the deadlock
+    cfg, d = desc("tiny")
+    st, q = L.mk_plan(d, 1, cfg["max_seq"], 8)
+    assert L.mk_plan_check(q, 8, st["max_pc"], st["n_counters"]) == L.MK_OK
+    i = next(i for i in range(len(q)) if q[i].op == 1 and q[i].layer == 1)
+    q[i].flags &= ~16
+    assert L.mk_plan_check(q, 8, st["max_pc"], st["n_counters"]) == L.MK_ERR_SCHEDULE
