@@ -59,7 +59,9 @@ enum Flag : uint8_t {
 enum HoldBit : unsigned {
   HOLD_QKV = 1, HOLD_ATTN = 2, HOLD_OPROJ = 4, HOLD_MLP = 8, HOLD_DOWN = 16, HOLD_LM = 32,
 };
-constexpr unsigned DEFAULT_HOLD = HOLD_DOWN | HOLD_QKV | HOLD_LM;
+// Default: none.  The down rows' signal is relaxed (tagged outputs), and the
+// remaining fences cost less than the prefetch a hold would give up.
+constexpr unsigned DEFAULT_HOLD = 0;
 
 constexpr uint32_t NO_CTR = 0xFFFFFFFFu;
 

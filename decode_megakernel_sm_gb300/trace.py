@@ -38,6 +38,41 @@ def _rows(trace, queues, n_sm, max_pc):
     return rows, base
 
 
+# Consecutive phases of a layer (the split MLP; a fused MLP shows up as MLP).
+_CHAIN = ("QKV", "ATTN", "OPROJ", "MLP_UP", "MLP_DOWN")
+
+
+def _hops(rows) -> dict:
+    """Per dependency hop, averaged over the inner layers: from the moment
+    the producing phase's last instruction ended its body to the end of the
+    consuming instructions' prologues (min / median / max over the
+    consumers), and the consumers' median time from prologue end to body
+    end.  The hop covers the producer's completion signal, its propagation,
+    the consumer's wait and the loading of the phase's input vector."""
+    by = {}
+    for s, pc, op, layer, tp, tw0, tw1, te, m0, m1, rw, tsig in rows:
+        by.setdefault((layer, L.OP_NAMES[op]), []).append((te, m0))
+    layers = sorted({k[0] for k in by if k[1] in _CHAIN})
+    out = {}
+    pairs = [(a, b, 0) for a, b in zip(_CHAIN, _CHAIN[1:])] + [(_CHAIN[-1], _CHAIN[0], 1)]
+    for a, b, dl in pairs:
+        lat, body = [], []
+        for l in layers[1:-1]:
+            pa, pb = by.get((l, a)), by.get((l + dl, b))
+            if not pa or not pb:
+                continue
+            last = max(t for t, _ in pa)
+            pe = np.array([m for _, m in pb], dtype=np.float64)
+            lat.append(((pe.min() - last), np.median(pe) - last, pe.max() - last))
+            body.append(float(np.median([t - m for t, m in pb])))
+        if lat:
+            v = np.array(lat).mean(axis=0) / 1e3
+            out[f"{a}->{b}"] = {"min_us": float(v[0]), "median_us": float(v[1]),
+                                "max_us": float(v[2]),
+                                "consumer_ring_and_epilogue_us": float(np.mean(body)) / 1e3}
+    return out
+
+
 def summarize(trace, queues, n_sm: int, max_pc: int) -> dict:
     rows, base = _rows(trace, queues, n_sm, max_pc)
     if not rows:
@@ -80,6 +115,7 @@ def summarize(trace, queues, n_sm: int, max_pc: int) -> dict:
         busy[s] += te - tw1
         waited[s] += tw1 - tw0
     return {"step_us": (end - base) / 1e3, "by_op": by_op, "per_layer": per_layer,
+            "hops": _hops(rows),
             "mean_sm_body_us": float(busy.mean() / 1e3),
             "mean_sm_wait_us": float(waited.mean() / 1e3)}
 

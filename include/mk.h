@@ -212,7 +212,7 @@ int mk_set_residual_copies(mk_handle* h, int copies);
  * are "held": the producer first warms L2 with up to `prefetch_bytes` of the
  * instruction's data (L2 prefetches do not slow fences), then issues the
  * ring copies only after the consumers have finished every earlier
- * instruction.  Default mask 49 (QKV, down rows, LM head), 256 KiB.  Takes
+ * instruction.  Default mask 0 (nothing held), 256 KiB.  Takes
  * effect at the next mk_build_schedule.  Results do not depend on it.     */
 int mk_set_hold_policy(mk_handle* h, unsigned mask, uint64_t prefetch_bytes);
 
