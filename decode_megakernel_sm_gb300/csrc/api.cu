@@ -19,6 +19,7 @@ cudaError_t pack_qkv(uint16_t* dst, const void* wq, const void* wk, const void* 
 cudaError_t pack_interleave(uint16_t* dst, const void* a, const void* b, long rows, int H,
                             cudaStream_t s);
 cudaError_t pack_wo(uint16_t* dst, const void* wo, int H, int Hq, int D, cudaStream_t s);
+cudaError_t pack_rows(uint16_t* dst, const void* src, long rows, int H, cudaStream_t s);
 cudaError_t pack_transpose(uint16_t* dst, const void* src, int R, int C, int batch,
                            cudaStream_t s);
 
@@ -305,7 +306,7 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
       else
         CK(pack_transpose(dT, w->w_down[l], H, d.ffn, 1, s));
     } else {
-      CK(cudaMemcpyAsync(rt, w->router[l], ls.router * 2, cudaMemcpyDeviceToDevice, s));
+      CK(pack_rows(rt, w->router[l], d.n_experts, H, s));
       CK(pack_interleave(egu, w->ex_gate[l], w->ex_up[l], (long)d.n_experts * d.expert_ffn, H,
                          s));
       CK(pack_transpose(edT, w->ex_down[l], H, d.expert_ffn, d.n_experts, s));
@@ -329,13 +330,13 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
     lp.vc = (uint16_t*)kv->v[l];
   }
   uint16_t* emb = take(V * H);
-  CK(cudaMemcpyAsync(emb, w->embed, V * H * 2, cudaMemcpyDeviceToDevice, s));
+  CK(pack_rows(emb, w->embed, (long)V, H, s));
   h->embed = emb;
   if (d.tied_lm_head) {
     h->lm_head = emb;
   } else {
     uint16_t* lm = take(V * H);
-    CK(cudaMemcpyAsync(lm, w->lm_head, V * H * 2, cudaMemcpyDeviceToDevice, s));
+    CK(pack_rows(lm, w->lm_head, (long)V, H, s));
     h->lm_head = lm;
   }
   uint16_t* fn = take(H);

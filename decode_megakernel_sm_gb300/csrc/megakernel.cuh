@@ -95,37 +95,42 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
   const uint32_t n = I.r1 - I.r0;
   switch (I.op) {
     case OP_QKV:
-      s[0] = {(const unsigned char*)(Lp->wqkv + (size_t)I.r0 * HT), nullptr, ROW, n, RPS};
+      s[0] = {(const unsigned char*)(Lp->wqkv + (size_t)I.r0 * HT), nullptr, ROW, n, RPS, I.r0};
       return 1;
     case OP_OPROJ:
       s[0] = {(const unsigned char*)(Lp->wo + ((size_t)I.g * HT + I.r0) * D), nullptr, D * 2, n,
               SBY / (D * 2)};
       return 1;
     case OP_ROUTER:
-      s[0] = {(const unsigned char*)(Lp->router + (size_t)I.r0 * HT), nullptr, ROW, n, RPS};
+      s[0] = {(const unsigned char*)(Lp->router + (size_t)I.r0 * HT), nullptr, ROW, n, RPS, I.r0};
       return 1;
     case OP_MLP: {
       const uint16_t *gu, *dT;
+      uint32_t row0;  // first gate/up row, the swizzle key of the packed tensor
       if (g.E == 0) {
         gu = Lp->wgu + (size_t)I.r0 * 2 * HT;
         dT = Lp->wdT + (size_t)I.r0 * HT;
+        row0 = 2 * I.r0;
       } else if (I.flags & F_SHARED) {
         gu = Lp->sh_gu + (size_t)I.r0 * 2 * HT;
         dT = Lp->sh_dT + (size_t)I.r0 * HT;
+        row0 = 2 * I.r0;
       } else {
         const size_t e = (size_t)topk[I.g];
         gu = Lp->ex_gu + (e * g.Fe + I.r0) * 2 * HT;
         dT = Lp->ex_dT + (e * g.Fe + I.r0) * HT;
+        row0 = (uint32_t)(2 * (e * g.Fe + I.r0));
       }
-      s[0] = {(const unsigned char*)gu, nullptr, ROW, 2 * n, RPS};
+      s[0] = {(const unsigned char*)gu, nullptr, ROW, 2 * n, RPS, row0};
       s[1] = {(const unsigned char*)dT, nullptr, ROW, n, RPS};
       return 2;
     }
     case OP_LMHEAD:
-      s[0] = {(const unsigned char*)(g.lm_head + (size_t)I.r0 * HT), nullptr, ROW, n, RPS};
+      s[0] = {(const unsigned char*)(g.lm_head + (size_t)I.r0 * HT), nullptr, ROW, n, RPS, I.r0};
       return 1;
     case OP_MLP_UP:
-      s[0] = {(const unsigned char*)(Lp->wgu + (size_t)I.r0 * 2 * HT), nullptr, ROW, 2 * n, RPS};
+      s[0] = {(const unsigned char*)(Lp->wgu + (size_t)I.r0 * 2 * HT), nullptr, ROW, 2 * n, RPS,
+              2 * I.r0};
       return 1;
     case OP_MLP_DOWN:  // rows of the row-major [H][F] down projection
       s[0] = {(const unsigned char*)(Lp->wdT + (size_t)I.r0 * g.F), nullptr, (uint32_t)g.F * 2, n,
@@ -244,7 +249,8 @@ MK_DEV bool norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const No
       float v[8];
       if (b < g.B) {
         if (j == 0) {
-          const uint4 w = __ldg((const uint4*)(g.embed + (size_t)c.tok[b] * HT) + gi);
+          // embedding rows are chunk-swizzled by token id
+          const uint4 w = __ldg((const uint4*)(g.embed + (size_t)c.tok[b] * HT) + (gi ^ (c.tok[b] & 7)));
           unpack8(w, v);
         } else if (tagged) {  // polled into xn above (batch 1 only: the split MLP)
           const float4* p = (const float4*)(c.xn + (size_t)b * HT) + 2 * gi;
@@ -326,8 +332,11 @@ MK_DEV void load_xr(const float* xn, int lane, float (&xr)[HT / 32]) {
 // caller reduces across the warp.
 template <int HT, int NB>
 MK_DEV void row_dot(const unsigned char* row, const float (&xr)[HT / 32], const float* xn,
-                    int lane, float (&acc)[NB]) {
+                    int lane, int key, float (&acc)[NB]) {
+  // the row is chunk-swizzled: this lane's chunk it*32 + lane sits at slot
+  // it*32 + (lane ^ key), key = row index & 7
   const uint4* w4 = (const uint4*)row;
+  const int sl = lane ^ key;
   if constexpr (NB == 1) {
     // eight independent chains (one per element of a 16-byte chunk): the
     // dependent-FMA depth is HT/256 instead of HT/64
@@ -336,7 +345,7 @@ MK_DEV void row_dot(const unsigned char* row, const float (&xr)[HT / 32], const 
     for (int k = 0; k < 8; k++) a[k] = 0.f;
 #pragma unroll
     for (int it = 0; it < HT / 256; it++) {
-      const uint4 w = w4[it * 32 + lane];
+      const uint4 w = w4[it * 32 + sl];
       const float* x = xr + it * 8;
       a[0] = fmaf(bf_lo(w.x), x[0], a[0]); a[1] = fmaf(bf_hi(w.x), x[1], a[1]);
       a[2] = fmaf(bf_lo(w.y), x[2], a[2]); a[3] = fmaf(bf_hi(w.y), x[3], a[3]);
@@ -350,7 +359,7 @@ MK_DEV void row_dot(const unsigned char* row, const float (&xr)[HT / 32], const 
 #pragma unroll 2
     for (int it = 0; it < HT / 256; it++) {
       float wf[8];
-      unpack8(w4[it * 32 + lane], wf);
+      unpack8(w4[it * 32 + sl], wf);
 #pragma unroll
       for (int b = 0; b < NB; b++) {
         const float4* p = (const float4*)(xn + (size_t)b * HT + it * 256 + lane * 8);
@@ -386,12 +395,14 @@ MK_DEV bool gemv_rows(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s,
         // the previous row's cross-lane sum is issued in the same block as
         // this row's loads and FMAs, so its shuffle latency hides behind them
         float prev[1] = {warp_sum(pend)};
-        row_dot<HT, NB>(st + (size_t)r * HT * 2, xr, c.xn, c.lane, acc);
+        row_dot<HT, NB>(st + (size_t)r * HT * 2, xr, c.xn, c.lane, (int)((s.row0 + u0 + r) & 7u),
+                        acc);
         if (prow >= 0) fn((uint32_t)prow, prev);
         pend = acc[0];
         prow = (int)(u0 + r);
       } else {
-        row_dot<HT, NB>(st + (size_t)r * HT * 2, xr, c.xn, c.lane, acc);
+        row_dot<HT, NB>(st + (size_t)r * HT * 2, xr, c.xn, c.lane, (int)((s.row0 + u0 + r) & 7u),
+                        acc);
 #pragma unroll
         for (int b = 0; b < NB; b++) acc[b] = warp_sum(acc[b]);
         fn(u0 + r, acc);
@@ -631,7 +642,8 @@ MK_DEV bool op_attn(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
 
 // Residual input x_j[b][r] (j = 0: the embedding row of the token).
 MK_DEV float x_in(const Globals& g, int j, const int* tok, int b, int r) {
-  if (j == 0) return bf1(g.embed[(size_t)tok[b] * g.H + r]);
+  if (j == 0)  // embedding rows are chunk-swizzled by token id
+    return bf1(g.embed[(size_t)tok[b] * g.H + ((((r >> 3) ^ (tok[b] & 7)) << 3) | (r & 7))]);
   return xres_sum(g, j, b, r);
 }
 

@@ -298,6 +298,7 @@ struct Seg {
   uint32_t unit;
   uint32_t n;
   uint32_t ups;
+  uint32_t row0;  // swizzled GEMV matrices: index of the first row in its tensor (key = row & 7)
 };
 
 // Ring cursor of one consumer warp.

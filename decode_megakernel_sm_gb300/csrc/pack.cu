@@ -1,6 +1,12 @@
 // pack.cu -- device-side re-layout of the caller's bf16 weights into the
 // instruction-contiguous layouts the interpreter streams (one run per
-// instruction, one bulk copy per ring stage, no tensor map needed):
+// instruction, one bulk copy per ring stage, no tensor map needed).
+// Every matrix whose rows are dotted with the normalised activation (QKV,
+// gate/up, router, experts, embedding / LM head) is chunk-swizzled: 16-byte
+// chunk i of row p sits at slot i ^ (p & 7), so 8 consecutive rows read at
+// the same column offset land in 8 different shared-memory bank groups
+// (ldmatrix over 8 rows is conflict-free; a lane that walks one row just
+// XORs its chunk index).
 //   QKV   [Hkv][(HPG+2)*D][H]  per kv head: its HPG query heads, then k, then
 //                              v; inside a head, rows 2t / 2t+1 = dims t / t+D/2
 //   Wo    [Hq][H][D]           one head's columns as contiguous 128/256-byte rows;
@@ -27,18 +33,26 @@ __global__ void pack_qkv_kernel(uint4* __restrict__ dst, const uint16_t* __restr
                                     : wv + ((size_t)g * D + dim) * H;
   const uint4* s4 = (const uint4*)src;
   uint4* d4 = dst + (size_t)p * (H / 8);
-  for (int i = threadIdx.x; i < H / 8; i += blockDim.x) d4[i] = s4[i];
+  for (int i = threadIdx.x; i < H / 8; i += blockDim.x) d4[i ^ (p & 7)] = s4[i];
 }
 
-// dst row 2c = a row c, dst row 2c+1 = b row c (rows of H elements).
+// dst row 2c = a row c, dst row 2c+1 = b row c (rows of H elements), swizzled.
 __global__ void pack_interleave_kernel(uint4* __restrict__ dst, const uint4* __restrict__ a,
                                        const uint4* __restrict__ b, int H) {
   const size_t c = blockIdx.x;
   const int n = H / 8;
+  const int k0 = (int)((2 * c) & 7), k1 = (int)((2 * c + 1) & 7);
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    dst[(2 * c) * n + i] = a[c * n + i];
-    dst[(2 * c + 1) * n + i] = b[c * n + i];
+    dst[(2 * c) * n + (i ^ k0)] = a[c * n + i];
+    dst[(2 * c + 1) * n + (i ^ k1)] = b[c * n + i];
   }
+}
+
+// dst row r = src row r (rows of H elements), swizzled.
+__global__ void pack_rows_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int H) {
+  const size_t r = blockIdx.x;
+  const int n = H / 8;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) dst[r * n + (i ^ (int)(r & 7))] = src[r * n + i];
 }
 
 // dst[h][r][c ^ (r & 7)] = wo[r][h*D + 8c : h*D + 8c + 8] (16-byte chunks c).
@@ -84,6 +98,12 @@ cudaError_t pack_interleave(uint16_t* dst, const void* a, const void* b, long ro
   if (rows <= 0) return cudaSuccess;
   pack_interleave_kernel<<<(unsigned)rows, 128, 0, s>>>((uint4*)dst, (const uint4*)a,
                                                        (const uint4*)b, H);
+  return cudaGetLastError();
+}
+
+cudaError_t pack_rows(uint16_t* dst, const void* src, long rows, int H, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  pack_rows_kernel<<<(unsigned)rows, 128, 0, s>>>((uint4*)dst, (const uint4*)src, H);
   return cudaGetLastError();
 }
 
