@@ -25,6 +25,7 @@ struct Ctx {
   float* xn;    // [NB][HT] normalised activation of the current instruction
   float* yrow;  // [NB][MAX_ROWS] row outputs / attention merge scratch
   float* hbuf;  // [NB][MAX_COLS] SiLU(gate)*up of an MLP slice
+  float* mpart; // NB > 1: [NCW][MMA_FLUSH][NB] per-warp partial sums of the batched GEMV
   float* attn;  // [NB][D] reduced attention output of one head
   float* red;   // reduction scratch
   int* tok;     // [NB]
@@ -208,10 +209,12 @@ struct NormGain {
   static constexpr int GROUPS = HT / 8;
   static constexpr int GPT = (GROUPS + NCT - 1) / NCT;
   uint4 w[GPT];  // 8 packed bf16 gains per 8-column group
+  const uint16_t* src;  // the gain vector (batched variants read it per column)
 };
 
 template <int HT>
 MK_DEV void norm_gain(NormGain<HT>& ng, const uint16_t* gain, int tid) {
+  ng.src = gain;
 #pragma unroll
   for (int q = 0; q < NormGain<HT>::GPT; q++) {
     const int gi = tid + q * NCT;
@@ -219,8 +222,127 @@ MK_DEV void norm_gain(NormGain<HT>& ng, const uint16_t* gain, int tid) {
   }
 }
 
+// RMSNorm for the batched variants (NB = 8), straight into the tensor-core
+// A-fragment layout the batched GEMV reads.  Pass 1: thread t takes columns
+// k = t + q*NCT of all 8 sequences and stores each column k-major (32 bytes;
+// adjacent lanes write adjacent columns, so the stores do not conflict),
+// summing squares on the way.  Pass 2 scales column k by gain[k] / rms(x_b).
+// Pass 3 turns every 16-column k-tile (512 bytes, k-major) into its 32 lanes'
+// fragments in place: lane 4g + t holds bf16 hi / lo of sequence g at
+// columns 2t, 2t+1 and 2t+8, 2t+9.
+template <int HT, int D, int HPG, int NB>
+MK_DEV bool norm_apply_batched(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j,
+                               const uint16_t* gain) {
+  static_assert(NB == 8, "k-tile blocks of 16 columns x 8 sequences");
+  constexpr int KPT = (HT + NCT - 1) / NCT;  // columns per thread
+  constexpr int CH = 5;                      // columns whose loads are in flight together
+  float ss[NB];
+#pragma unroll
+  for (int b = 0; b < NB; b++) ss[b] = 0.f;
+  // the per-sequence source rows (and the case) are fixed for the whole pass,
+  // so the column loop below is a straight run of independent loads
+  const bool emb = j == 0;
+  const float* xb[NB];
+  int tk[NB];
+#pragma unroll
+  for (int b = 0; b < NB; b++) {
+    const bool live = b < g.B;
+    tk[b] = live ? c.tok[b] : 0;
+    xb[b] = (!emb && live) ? xres(g, j, b, 0) : nullptr;
+  }
+#pragma unroll
+  for (int q0 = 0; q0 < KPT; q0 += CH) {
+    float v[CH][NB];
+#pragma unroll
+    for (int u = 0; u < CH; u++) {
+      const int k = c.tid + (q0 + u) * NCT;
+      const bool kin = q0 + u < KPT && k < HT;
+#pragma unroll
+      for (int b = 0; b < NB; b++) {
+        float x = 0.f;
+        if (kin && b < g.B) {
+          if (emb)  // embedding rows are chunk-swizzled by token id
+            x = bf1(__ldg(g.embed + (size_t)tk[b] * HT + ((((k >> 3) ^ (tk[b] & 7)) << 3) | (k & 7))));
+          else
+            x = __ldcg(xb[b] + k);
+        }
+        v[u][b] = x;
+      }
+    }
+    if (g.kc > 1 && !emb) {  // further partial copies of the residual vector
+      for (int cp = 1; cp < g.kc; cp++)
+#pragma unroll
+        for (int u = 0; u < CH; u++) {
+          const int k = c.tid + (q0 + u) * NCT;
+#pragma unroll
+          for (int b = 0; b < NB; b++)
+            if (q0 + u < KPT && k < HT && b < g.B) v[u][b] += __ldcg(xres(g, j, b, cp) + k);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < CH; u++) {
+      const int k = c.tid + (q0 + u) * NCT;
+      if (q0 + u < KPT && k < HT) {
+        st_shared_f4(c.xn + (size_t)k * NB, v[u][0], v[u][1], v[u][2], v[u][3]);
+        st_shared_f4(c.xn + (size_t)k * NB + 4, v[u][4], v[u][5], v[u][6], v[u][7]);
+#pragma unroll
+        for (int b = 0; b < NB; b++) ss[b] = fmaf(v[u][b], v[u][b], ss[b]);
+      }
+    }
+  }
+  float gw[KPT];
+#pragma unroll
+  for (int q = 0; q < KPT; q++) {
+    const int k = c.tid + q * NCT;
+    gw[q] = k < HT ? bf1(__ldg(gain + k)) : 0.f;
+  }
+#pragma unroll
+  for (int b = 0; b < NB; b++) {
+    const float t = warp_sum(ss[b]);
+    if (c.lane == 0) c.red[c.warp * NB + b] = t;
+  }
+  consumer_bar();
+  float rs[NB];
+#pragma unroll
+  for (int b = 0; b < NB; b++) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < NCW; w++) t += c.red[w * NB + b];
+    rs[b] = rsqrtf(t / (float)HT + g.eps);
+  }
+#pragma unroll
+  for (int q = 0; q < KPT; q++) {
+    const int k = c.tid + q * NCT;
+    if (k < HT) {
+      float4* o = (float4*)(c.xn + (size_t)k * NB);
+      float4 a0 = o[0], a1 = o[1];
+      a0.x *= rs[0] * gw[q]; a0.y *= rs[1] * gw[q]; a0.z *= rs[2] * gw[q]; a0.w *= rs[3] * gw[q];
+      a1.x *= rs[4] * gw[q]; a1.y *= rs[5] * gw[q]; a1.z *= rs[6] * gw[q]; a1.w *= rs[7] * gw[q];
+      o[0] = a0;
+      o[1] = a1;
+    }
+  }
+  consumer_bar();
+  const int gq = c.lane >> 2, tq = c.lane & 3;
+  for (int kt = c.warp; kt < HT / 16; kt += NCW) {
+    const float* blk = c.xn + (size_t)kt * 16 * NB;
+    const float v0 = blk[(2 * tq) * NB + gq], v1 = blk[(2 * tq + 1) * NB + gq];
+    const float v2 = blk[(2 * tq + 8) * NB + gq], v3 = blk[(2 * tq + 9) * NB + gq];
+    uint4 f;
+    split2(v0, v1, f.x, f.y);
+    split2(v2, v3, f.z, f.w);
+    __syncwarp();
+    ((uint4*)c.xn)[(size_t)kt * 32 + c.lane] = f;
+  }
+  consumer_bar();
+  return true;
+}
+
 template <int HT, int D, int HPG, int NB>
 MK_DEV bool norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const NormGain<HT>& ng) {
+  if constexpr (NB > 1) {
+    return norm_apply_batched(c, g, j, ng.src);
+  } else {
   constexpr int GROUPS = NormGain<HT>::GROUPS, GPT = NormGain<HT>::GPT;
   // split MLP: x_{2l+2} (j even, j > 0) arrives as tagged words from the
   // down rows' owners; each thread polls its own 8-element groups
@@ -244,39 +366,52 @@ MK_DEV bool norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const No
   for (int q = 0; q < GPT; q++) {
     const int gi = c.tid + q * NCT;
     if (gi >= GROUPS) continue;
+    // every sequence's loads of this group first, then the shared-memory
+    // stores: the stores may alias (as far as the compiler can tell) and
+    // would otherwise hold each next load back by a whole round trip
+    float v[NB][8];
 #pragma unroll
     for (int b = 0; b < NB; b++) {
-      float v[8];
       if (b < g.B) {
         if (j == 0) {
           // embedding rows are chunk-swizzled by token id
-          const uint4 w = __ldg((const uint4*)(g.embed + (size_t)c.tok[b] * HT) + (gi ^ (c.tok[b] & 7)));
-          unpack8(w, v);
+          const uint4 w =
+              __ldg((const uint4*)(g.embed + (size_t)c.tok[b] * HT) + (gi ^ (c.tok[b] & 7)));
+          unpack8(w, v[b]);
         } else if (tagged) {  // polled into xn above (batch 1 only: the split MLP)
           const float4* p = (const float4*)(c.xn + (size_t)b * HT) + 2 * gi;
           const float4 a0 = p[0], a1 = p[1];
-          v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
-          v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+          v[b][0] = a0.x; v[b][1] = a0.y; v[b][2] = a0.z; v[b][3] = a0.w;
+          v[b][4] = a1.x; v[b][5] = a1.y; v[b][6] = a1.z; v[b][7] = a1.w;
+        } else if (g.kc == 1) {
+          const float4* p = (const float4*)xres(g, j, b, 0) + 2 * gi;
+          const float4 a0 = __ldcg(p), a1 = __ldcg(p + 1);
+          v[b][0] = a0.x; v[b][1] = a0.y; v[b][2] = a0.z; v[b][3] = a0.w;
+          v[b][4] = a1.x; v[b][5] = a1.y; v[b][6] = a1.z; v[b][7] = a1.w;
         } else {
 #pragma unroll
-          for (int k = 0; k < 8; k++) v[k] = 0.f;
+          for (int k = 0; k < 8; k++) v[b][k] = 0.f;
           for (int cp = 0; cp < g.kc; cp++) {
             const float4* p = (const float4*)xres(g, j, b, cp) + 2 * gi;
             const float4 a0 = __ldcg(p), a1 = __ldcg(p + 1);
-            v[0] += a0.x; v[1] += a0.y; v[2] += a0.z; v[3] += a0.w;
-            v[4] += a1.x; v[5] += a1.y; v[6] += a1.z; v[7] += a1.w;
+            v[b][0] += a0.x; v[b][1] += a0.y; v[b][2] += a0.z; v[b][3] += a0.w;
+            v[b][4] += a1.x; v[b][5] += a1.y; v[b][6] += a1.z; v[b][7] += a1.w;
           }
         }
       } else {
 #pragma unroll
-        for (int k = 0; k < 8; k++) v[k] = 0.f;
+        for (int k = 0; k < 8; k++) v[b][k] = 0.f;
       }
-      float4* o = (float4*)(c.xn + (size_t)b * HT) + 2 * gi;
-      o[0] = make_float4(v[0], v[1], v[2], v[3]);
-      o[1] = make_float4(v[4], v[5], v[6], v[7]);
-#pragma unroll
-      for (int k = 0; k < 8; k++) ss[b] = fmaf(v[k], v[k], ss[b]);
     }
+    {
+      float4* o = (float4*)c.xn + 2 * gi;
+      o[0] = make_float4(v[0][0], v[0][1], v[0][2], v[0][3]);
+      o[1] = make_float4(v[0][4], v[0][5], v[0][6], v[0][7]);
+    }
+#pragma unroll
+    for (int b = 0; b < NB; b++)
+#pragma unroll
+      for (int k = 0; k < 8; k++) ss[b] = fmaf(v[b][k], v[b][k], ss[b]);
   }
 #pragma unroll
   for (int b = 0; b < NB; b++) {
@@ -300,18 +435,18 @@ MK_DEV bool norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const No
     if (gi >= GROUPS) continue;
     float gw[8];
     unpack8(ng.w[q], gw);
-#pragma unroll
-    for (int b = 0; b < NB; b++) {
-      float4* o = (float4*)(c.xn + (size_t)b * HT) + 2 * gi;
+    {
+      float4* o = (float4*)c.xn + 2 * gi;
       float4 a0 = o[0], a1 = o[1];
-      a0.x *= rs[b] * gw[0]; a0.y *= rs[b] * gw[1]; a0.z *= rs[b] * gw[2]; a0.w *= rs[b] * gw[3];
-      a1.x *= rs[b] * gw[4]; a1.y *= rs[b] * gw[5]; a1.z *= rs[b] * gw[6]; a1.w *= rs[b] * gw[7];
+      a0.x *= rs[0] * gw[0]; a0.y *= rs[0] * gw[1]; a0.z *= rs[0] * gw[2]; a0.w *= rs[0] * gw[3];
+      a1.x *= rs[0] * gw[4]; a1.y *= rs[0] * gw[5]; a1.z *= rs[0] * gw[6]; a1.w *= rs[0] * gw[7];
       o[0] = a0;
       o[1] = a1;
     }
   }
   consumer_bar();
   return true;
+  }
 }
 
 // ----------------------------------------------------------------- GEMV ----
@@ -337,7 +472,8 @@ MK_DEV void row_dot(const unsigned char* row, const float (&xr)[HT / 32], const 
   // it*32 + (lane ^ key), key = row index & 7
   const uint4* w4 = (const uint4*)row;
   const int sl = lane ^ key;
-  if constexpr (NB == 1) {
+  static_assert(NB == 1, "batched variants use the tensor-core GEMV");
+  {
     // eight independent chains (one per element of a 16-byte chunk): the
     // dependent-FMA depth is HT/256 instead of HT/64
     float a[8];
@@ -353,27 +489,9 @@ MK_DEV void row_dot(const unsigned char* row, const float (&xr)[HT / 32], const 
       a[6] = fmaf(bf_lo(w.w), x[6], a[6]); a[7] = fmaf(bf_hi(w.w), x[7], a[7]);
     }
     acc[0] = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
-  } else {
-#pragma unroll
-    for (int b = 0; b < NB; b++) acc[b] = 0.f;
-#pragma unroll 2
-    for (int it = 0; it < HT / 256; it++) {
-      float wf[8];
-      unpack8(w4[it * 32 + sl], wf);
-#pragma unroll
-      for (int b = 0; b < NB; b++) {
-        const float4* p = (const float4*)(xn + (size_t)b * HT + it * 256 + lane * 8);
-        const float4 x0 = p[0], x1 = p[1];
-        float a = acc[b];
-        a = fmaf(wf[0], x0.x, a); a = fmaf(wf[1], x0.y, a);
-        a = fmaf(wf[2], x0.z, a); a = fmaf(wf[3], x0.w, a);
-        a = fmaf(wf[4], x1.x, a); a = fmaf(wf[5], x1.y, a);
-        a = fmaf(wf[6], x1.z, a); a = fmaf(wf[7], x1.w, a);
-        acc[b] = a;
-      }
-    }
   }
 }
+
 
 // Stream the rows of one segment through the ring; warp w computes rows
 // w, w + NCW, ... of each stage and hands (row index, per-sequence dot) to
@@ -419,6 +537,101 @@ MK_DEV bool gemv_rows(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s,
   return true;
 }
 
+// Batched GEMV on the tensor cores (NB > 1): y[b][row] = sum_k W[row][k] x[b][k]
+// with mma.sync m16n8k16 (bf16 in, f32 accumulate), A = the activations and
+// B = 8 weight rows.  A's rows 0..7 hold bf16(x[b]) and rows 8..15 the bf16 of
+// the remainder x[b] - bf16(x[b]); the two halves' products are added, so the
+// activation keeps about 16 mantissa bits; the A fragments are built once per
+// normalisation, in shared memory (norm_apply).  The k range is split over the
+// consumer warps: warp w reads only its k-tile pairs of every ring stage, 8
+// rows at a time with ldmatrix (rows are chunk-swizzled, so the 8 row reads
+// hit 8 bank groups), with the matching A fragments.  Per-warp
+// partial sums meet in shared memory every MMA_FLUSH rows, where fe(row, b,
+// y) receives each output once.  Every warp runs the same loop and barriers;
+// a warp whose ring wait gave up stops touching the ring (it neither reads
+// nor releases stages) and the failure is broadcast, so all return alike.
+template <int HT, int D, int HPG, int NB, class Fe>
+MK_DEV bool gemv_rows_mma(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s, Fe&& fe) {
+  static_assert(NB > 1 && NB <= 8, "one m16n8k16 A tile holds up to 8 sequences");
+  static_assert(NCT % NB == 0 && (NB & (NB - 1)) == 0, "a thread's outputs share one sequence");
+  static_assert(MAX_STAGE_BYTES / (HT * 2) <= MMA_FLUSH, "a stage's rows fit one flush window");
+  static_assert(NB == 8, "the fragment layout packs 8 sequences per k-tile");
+  constexpr int NPAIR = HT / 32;  // pairs of 16-column k-tiles
+  constexpr int PPW = (NPAIR + NCW - 1) / NCW;
+  const int p0 = c.warp * NPAIR / NCW, np = (c.warp + 1) * NPAIR / NCW - p0;
+  const int gq = c.lane >> 2, tq = c.lane & 3;
+  // A fragments of k-tile kt: ((uint4*)xn)[kt * 32 + lane], built by norm_apply
+  const uint4* af = (const uint4*)c.xn + c.lane;
+  float* part = c.mpart;
+  bool bad = false;
+  uint32_t prow0 = 0, pending = 0;  // rows held in part since the last flush
+  const uint32_t li = (uint32_t)c.lane & 7u, lm = (uint32_t)c.lane >> 3;
+  for (uint32_t u0 = 0; u0 < s.n; u0 += s.ups) {
+    const uint32_t n = min(s.ups, s.n - u0);
+    if (!bad && !c.ring.acquire(g)) bad = true;
+    if (!bad) {
+      const uint32_t sbase = smem_u32(c.ring.stage_ptr());
+      for (uint32_t nt = 0; nt < n; nt += 8) {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t rr = nt + li < n ? nt + li : nt;  // rows past the stage repeat row nt
+        const uint32_t key = (s.row0 + u0 + rr) & 7u;
+        const uint32_t rowaddr = sbase + rr * (uint32_t)(HT * 2);
+#pragma unroll
+        for (int pp = 0; pp < PPW; pp++) {
+          if (pp < np) {
+            const uint32_t ch = (uint32_t)(p0 + pp) * 4u + lm;  // 16-byte chunk of this lane's matrix
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(rowaddr + ((ch ^ key) << 4), b0, b1, b2, b3);
+            const uint4 fa = af[(size_t)(p0 + pp) * 64], fb = af[(size_t)(p0 + pp) * 64 + 32];
+            const uint32_t a0[4] = {fa.x, fa.y, fa.z, fa.w}, a1[4] = {fb.x, fb.y, fb.z, fb.w};
+            mma_16816(d, a0, b0, b1);
+            mma_16816(d, a1, b2, b3);
+          }
+        }
+        // d[0], d[1]: hi products of sequence gq, rows nt + 2tq, +1; d[2], d[3]: lo
+        const uint32_t r = nt + 2u * (uint32_t)tq;
+        float* pw = part + ((size_t)c.warp * MMA_FLUSH + (u0 + r - prow0)) * NB + gq;
+        if (gq < NB && r < n) pw[0] = d[0] + d[2];
+        if (gq < NB && r + 1 < n) pw[NB] = d[1] + d[3];
+      }
+      c.ring.release(c.lane);
+    }
+    pending += n;
+    if (u0 + s.ups >= s.n || pending + s.ups > (uint32_t)MMA_FLUSH) {
+      consumer_bar();
+      for (int it = c.tid; it < (int)pending * NB; it += NCT) {
+        const int r = it / NB, b = it % NB;
+        float y = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; w++) y += part[((size_t)w * MMA_FLUSH + r) * NB + b];
+        if (b < g.B) fe(prow0 + (uint32_t)r, b, y);
+      }
+      consumer_bar();
+      prow0 += pending;
+      pending = 0;
+    }
+  }
+  if (bad) c.flag[2] = 1;
+  consumer_bar();
+  return c.flag[2] == 0;
+}
+
+// The GEMV of the row-dotted matrices: fe(row, b, y) is called exactly once
+// per output.  Batch 1 runs on the FP32 pipes (lane 0 of the row's warp
+// calls fe); batched variants run on the tensor cores.
+template <int HT, int D, int HPG, int NB, class Fe>
+MK_DEV bool gemv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s,
+                 const float (&xr)[HT / 32], Fe&& fe) {
+  if constexpr (NB > 1) {
+    return gemv_rows_mma(c, g, s, fe);
+  } else {
+    const int lane = c.lane;
+    return gemv_rows(c, g, s, xr, [&](uint32_t r, float(&acc)[NB]) {
+      if (lane == 0) fe(r, 0, acc[0]);
+    });
+  }
+}
+
 }  // namespace mk
 
 namespace mk {
@@ -459,12 +672,7 @@ MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
   float* yrow = c.yrow;
   const int lane = c.lane;
-  gemv_rows(c, g, s[0], xr, [&](uint32_t r, float(&acc)[NB]) {
-    if (lane == 0) {
-#pragma unroll
-      for (int b = 0; b < NB; b++) yrow[b * MAX_ROWS + r] = acc[b];
-    }
-  });
+  gemv(c, g, s[0], xr, [&](uint32_t r, int b, float y) { yrow[b * MAX_ROWS + r] = y; });
   c.mark(g, 1);
   consumer_bar();
   if (i < n) {
@@ -707,18 +915,29 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
     const int nr = (int)(I.r1 - I.r0);
     const bool tagged = g.xtag && l > 0;  // x_{2l} from the down rows' owners
     bool okr = true;
-    for (int t = c.tid; t < NB * nr; t += NCT) {
-      const int b = t / nr, r = t % nr;
-      float v = 0.f;
-      if (b < g.B) {
-        if (tagged) {
+    if (tagged) {
+      for (int t = c.tid; t < NB * nr; t += NCT) {
+        const int b = t / nr, r = t % nr;
+        float v = 0.f;
+        if (b < g.B) {
           const TagWord* p = g.xt + ((size_t)(l - 1) * g.B + b) * g.H + I.r0 + r;
           if (!poll_tag1(g, p, g.epoch, v, c.pc, I.op)) okr = false;
-        } else {
-          v = x_in(g, 2 * l, c.tok, b, (int)I.r0 + r);
         }
+        xr_s[t] = v;
       }
-      xr_s[t] = v;
+    } else {
+      // eight rows' loads in flight before their shared-memory stores
+      for (int t0 = c.tid; t0 < NB * nr; t0 += 8 * NCT) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+          const int t = t0 + u * NCT, b = t / nr, r = t % nr;
+          v[u] = t < NB * nr && b < g.B ? x_in(g, 2 * l, c.tok, b, (int)I.r0 + r) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; u++)
+          if (t0 + u * NCT < NB * nr) xr_s[t0 + u * NCT] = v[u];
+      }
     }
     if (!okr) c.flag[2] = 1;
   }
@@ -864,10 +1083,7 @@ MK_DEV bool op_router(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   const int lane = c.lane, B = g.B;
   float* rl = g.rlog + (size_t)I.layer * g.B * g.E + I.r0;
   const int E = g.E;
-  gemv_rows(c, g, s[0], xr, [&](uint32_t r, float(&acc)[NB]) {
-    if (lane == 0)
-      for (int b = 0; b < B && b < NB; b++) rl[(size_t)b * E + r] = acc[b];
-  });
+  gemv(c, g, s[0], xr, [&](uint32_t r, int b, float y) { rl[(size_t)b * E + r] = y; });
   consumer_bar();
   return true;
 }
@@ -904,12 +1120,7 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
   float* yrow = c.yrow;
   const int lane = c.lane;
-  gemv_rows(c, g, s[0], xr, [&](uint32_t r, float(&acc)[NB]) {
-    if (lane == 0) {
-#pragma unroll
-      for (int b = 0; b < NB; b++) yrow[b * MAX_ROWS + r] = acc[b];
-    }
-  });
+  gemv(c, g, s[0], xr, [&](uint32_t r, int b, float y) { yrow[b * MAX_ROWS + r] = y; });
   consumer_bar();
   const int ncol = (int)(I.r1 - I.r0);
   for (int t = c.tid; t < NB * ncol; t += NCT) {
@@ -993,12 +1204,7 @@ MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
   float* yrow = c.yrow;
   const int lane = c.lane;
-  gemv_rows(c, g, s[0], xr, [&](uint32_t r, float(&acc)[NB]) {
-    if (lane == 0) {
-#pragma unroll
-      for (int b = 0; b < NB; b++) yrow[b * MAX_ROWS + r] = acc[b];
-    }
-  });
+  gemv(c, g, s[0], xr, [&](uint32_t r, int b, float y) { yrow[b * MAX_ROWS + r] = y; });
   c.mark(g, 1);
   consumer_bar();
   const int ncol = (int)(I.r1 - I.r0);
@@ -1111,39 +1317,37 @@ MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
   Seg s[2];
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
-  float best[NB];
-  int bidx[NB];
-#pragma unroll
-  for (int b = 0; b < NB; b++) {
-    best[b] = -INFINITY;
-    bidx[b] = 0x7FFFFFFF;
-  }
+  // each thread only ever sees one sequence, b = tid % NB (both GEMV paths);
+  // it keeps that sequence's best (value, lowest row) of this slice
+  float best = -INFINITY;
+  int bidx = 0x7FFFFFFF;
   const int lane = c.lane, B = g.B, V = g.V;
   float* logits = g.logits;
   const uint32_t r0 = I.r0;
-  gemv_rows(c, g, s[0], xr, [&](uint32_t r, float(&acc)[NB]) {
-    if (lane == 0) {
-      const int row = (int)(r0 + r);
-#pragma unroll
-      for (int b = 0; b < NB; b++) {
-        if (b < B) {
-          logits[(size_t)b * V + row] = acc[b];
-          if (acc[b] > best[b] || (acc[b] == best[b] && row < bidx[b])) {
-            best[b] = acc[b];
-            bidx[b] = row;
-          }
-        }
-      }
+  gemv(c, g, s[0], xr, [&](uint32_t r, int b, float y) {
+    const int row = (int)(r0 + r);
+    logits[(size_t)b * V + row] = y;
+    if (y > best || (y == best && row < bidx)) {
+      best = y;
+      bidx = row;
     }
   });
+  // lanes with equal lane % NB hold the same sequence: reduce them into
+  // lanes 0 .. NB-1, one per sequence
+#pragma unroll
+  for (int o = NB; o < 32; o <<= 1) {
+    const float ov = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+    const int oi = __shfl_xor_sync(0xFFFFFFFFu, bidx, o);
+    if (ov > best || (ov == best && oi < bidx)) {
+      best = ov;
+      bidx = oi;
+    }
+  }
   float* rv = c.red;
   int* ri = (int*)(c.red + NCW * NB);
-  if (lane == 0) {
-#pragma unroll
-    for (int b = 0; b < NB; b++) {
-      rv[c.warp * NB + b] = best[b];
-      ri[c.warp * NB + b] = bidx[b];
-    }
+  if (lane < NB) {
+    rv[c.warp * NB + lane] = best;
+    ri[c.warp * NB + lane] = bidx;
   }
   consumer_bar();
   if (c.warp != 0) return true;
@@ -1488,6 +1692,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
   c.xn = (float*)(smem + Ls.xn);
   c.yrow = (float*)(smem + Ls.yrow);
   c.hbuf = (float*)(smem + Ls.hbuf);
+  c.mpart = (float*)(smem + Ls.mpart);
   c.attn = (float*)(smem + Ls.attn);
   c.red = (float*)(smem + Ls.red);
   c.tok = tok;

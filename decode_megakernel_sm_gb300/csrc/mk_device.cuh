@@ -134,6 +134,43 @@ MK_DEV float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 MK_DEV float bf1(uint16_t h) { return __uint_as_float(((uint32_t)h) << 16); }
 MK_DEV uint16_t to_bf16(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
 
+// Shared-memory store that the compiler does not treat as touching other
+// memory, so global loads around it may still be issued early (ordering
+// against later shared-memory reads comes from the barrier between them).
+MK_DEV void st_shared_f4(const void* p, float a, float b, float c, float d) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(p)), "f"(a), "f"(b),
+               "f"(c), "f"(d));
+}
+
+// Two floats as bf16x2 pairs: hi = bf16(v) (nearest), lo = bf16(v - hi), so
+// hi + lo carries ~16 mantissa bits of v (lower column in the low half).
+MK_DEV void split2(float v0, float v1, uint32_t& hi, uint32_t& lo) {
+  const uint16_t h0 = to_bf16(v0), h1 = to_bf16(v1);
+  const uint16_t l0 = to_bf16(v0 - bf1(h0)), l1 = to_bf16(v1 - bf1(h1));
+  hi = (uint32_t)h0 | ((uint32_t)h1 << 16);
+  lo = (uint32_t)l0 | ((uint32_t)l1 << 16);
+}
+
+// Four 8x8 b16 matrices from shared memory; lane 8m + i gives row i of
+// matrix m, and register m receives this lane's pair of matrix m (row
+// lane / 4, columns 2 (lane % 4), +1).
+MK_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+// d += A (16x16 bf16, row-major fragment a) x B (16x8 bf16, column-major
+// fragment b0, b1), f32 accumulate.
+MK_DEV void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 MK_DEV void unpack8(const uint4& w, float* f) {
   f[0] = bf_lo(w.x); f[1] = bf_hi(w.x);
   f[2] = bf_lo(w.y); f[3] = bf_hi(w.y);

@@ -109,6 +109,7 @@ constexpr int DOWN_ROW_MAX = 16384;  // bytes of one down row (F <= 8192) in the
 constexpr int MAX_ROWS = 256;        // rows of one QKV / gate-up / router instruction
 constexpr int MAX_COLS = MAX_ROWS / 2;
 constexpr int MAX_DOWN_ROWS = 64;    // output rows of one split-MLP down instruction
+constexpr int MMA_FLUSH = 32;        // batched GEMV: rows per cross-warp sum of partials
 
 // Dense batch-1 models run the MLP as two ops (gate/up column slices, then
 // row-split down projection over the whole h) when one down row fits a ring
@@ -187,7 +188,7 @@ struct Globals {
 
 // Shared-memory layout (bytes from the dynamic shared memory base).
 struct SmemLayout {
-  int ring, full, empty, xn, yrow, hbuf, attn, red, misc, total;
+  int ring, full, empty, xn, yrow, hbuf, attn, red, misc, mpart, total;
 };
 
 MK_HD inline SmemLayout smem_layout(int n_stages, int stage_bytes, int NB, int H, int D, int HPG,
@@ -207,6 +208,8 @@ MK_HD inline SmemLayout smem_layout(int n_stages, int stage_bytes, int NB, int H
   s.attn = o;   o += 4 * NB * D;
   s.red = o;    o += 4 * 2 * NCW * NB + 16;
   s.misc = o;   o += 4 * (8 + 3 * NB + 4 * NB * (K > 0 ? K : 1));
+  o = (o + 15) / 16 * 16;
+  s.mpart = o;  o += NB > 1 ? 4 * NCW * MMA_FLUSH * NB : 0;  // batched GEMV partial sums
   s.total = (o + 127) / 128 * 128;
   return s;
 }
