@@ -158,25 +158,30 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
 }
 
 // MoE routing (batch 1): softmax is monotonic, so the top-k by probability
-// are the k largest router logits (lower expert id first on ties); the
-// renormalised weights are exp(l_j - l_max) / sum over the selected i of
-// exp(l_i - l_max).  One warp; every lane returns ids[K] and w[K].
+// are the k largest router logits (lower expert id first on ties); their
+// probabilities renormalised over the k chosen are exp(l - l_max) / sum.
+// One warp: lane l holds logits l, l + 32, ... (E <= 32 * RT_VPL, all in
+// registers; every loop has a fixed trip count).  Each round takes the warp's
+// best remaining (value, id) with shuffles and the owner lane marks it taken.
+// Lane 0 writes ids[0..K) and w[0..K).
+constexpr int RT_VPL = 8;
 MK_DEV void route_topk(const float* lg, int E, int K, int lane, int* ids, float* w) {
-  float v[32];
-  uint32_t taken = 0;
+  float v[RT_VPL];
 #pragma unroll
-  for (int k = 0; k < 32; k++) {
+  for (int k = 0; k < RT_VPL; k++) {
     const int e = lane + 32 * k;
     v[k] = e < E ? __ldcg(lg + e) : -INFINITY;
   }
+  uint32_t taken = 0;
   float top = 0.f, sum = 0.f;
   for (int j = 0; j < K; j++) {
     float best = -INFINITY;
     int bi = 0x7FFFFFFF;
 #pragma unroll
-    for (int k = 0; k < 32; k++) {
+    for (int k = 0; k < RT_VPL; k++) {
       const int e = lane + 32 * k;
-      if (e < E && !((taken >> k) & 1u) && (v[k] > best || (v[k] == best && e < bi))) {
+      const bool ok = e < E && !((taken >> k) & 1u);
+      if (ok && (v[k] > best || (v[k] == best && e < bi))) {
         best = v[k];
         bi = e;
       }
@@ -190,13 +195,18 @@ MK_DEV void route_topk(const float* lg, int E, int K, int lane, int* ids, float*
         bi = oi;
       }
     }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if ((bi & 31) == lane) taken |= 1u << ((bi >> 5) & (RT_VPL - 1));
     if (j == 0) top = best;
-    ids[j] = bi;
-    w[j] = expf(best - top);
-    sum += w[j];
+    const float p = expf(best - top);
+    sum += p;
+    if (lane == 0) {
+      ids[j] = bi;
+      w[j] = p;
+    }
   }
-  for (int j = 0; j < K; j++) w[j] /= sum;
+  if (lane == 0)
+    for (int j = 0; j < K; j++) w[j] /= sum;
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------- norms ----

@@ -37,7 +37,7 @@ int plan_shape_ok(const mk_model_desc& d) {
   if (d.hidden % 256 || d.hidden > 16384) return MK_ERR_UNSUPPORTED;
   if (d.head_dim != 64 && d.head_dim != 128) return MK_ERR_UNSUPPORTED;
   if (d.n_q_heads / d.n_kv_heads > 8) return MK_ERR_UNSUPPORTED;
-  if (d.n_experts > 1024 || d.top_k > 16) return MK_ERR_UNSUPPORTED;
+  if (d.n_experts > 256 || d.top_k > 16) return MK_ERR_UNSUPPORTED;  // 8 router logits per lane
   return MK_OK;
 }
 

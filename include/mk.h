@@ -45,7 +45,8 @@ typedef struct mk_handle mk_handle;
  * routed MoE MLP with n_experts experts of width expert_ffn, top_k of them
  * per token, plus an always-on shared expert of width shared_ffn (0: none).
  * "Gemma 4 TPU megakernel", section "Megakernels for Gemma 4", lists the
- * router / experts / shared MLP components of that MoE step.             */
+ * router / experts / shared MLP components of that MoE step.  Supported:
+ * n_experts <= 256, top_k <= 16 (MK_ERR_UNSUPPORTED otherwise).          */
 typedef struct {
   int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
   float rms_eps, rope_theta;
