@@ -39,6 +39,7 @@ using namespace mk;
 struct Scratch {
   float *xbuf, *qbuf, *part, *rlog, *lm_val;
   int *lm_idx, *routes, *err;
+  float* rweight;
   uint32_t* ctr;
   float* hglob;             // SiLU(gate)*up (split MLP)
   TagWord* xt;              // tagged block: x_{2l+2} (split MLP)
@@ -57,13 +58,13 @@ static Scratch carve_scratch(const mk_model_desc& d, size_t B, size_t kc, size_t
   const size_t sp = al256(L * B * Hq * splits * (D + 2) * 4);
   const size_t sr = al256(L * B * E * 4), sl = al256(n_lm * B * 4);
   const size_t sc = al256(n_ctr * 4), se = 256;
-  const size_t sroute = al256(L * (size_t)(d.top_k > 0 ? d.top_k : 1) * 4);
+  const size_t sroute = al256(L * (size_t)(d.top_k > 0 ? d.top_k : 1) * 4);  // ids, then weights
   const size_t sxt = al256(L * B * H * 8), sh = al256(L * B * F * 4);
   Scratch s{};
   s.xbuf_bytes = sx;
   s.ctr_bytes = sc;
   s.tag_bytes = sxt;
-  s.total = sx + sq + sp + sr + 2 * sl + sc + se + sroute + sh + sxt;
+  s.total = sx + sq + sp + sr + 2 * sl + sc + se + 2 * sroute + sh + sxt;
   if (!base) return s;
   char* q = base;
   s.xbuf = (float*)q; q += sx;
@@ -75,6 +76,7 @@ static Scratch carve_scratch(const mk_model_desc& d, size_t B, size_t kc, size_t
   s.ctr = (uint32_t*)q; q += sc;
   s.err = (int*)q; q += se;
   s.routes = (int*)q; q += sroute;
+  s.rweight = (float*)q; q += sroute;
   s.hglob = (float*)q; q += sh;
   s.xt = (TagWord*)q;
   return s;
@@ -437,6 +439,7 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.xt = h->sc.xt;
   g.hglob = h->sc.hglob;
   g.routes = h->sc.routes;
+  g.rweight = h->sc.rweight;
   g.lm_val = h->sc.lm_val;
   g.lm_idx = h->sc.lm_idx;
   g.ctr = h->sc.ctr;

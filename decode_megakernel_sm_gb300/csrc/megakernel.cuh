@@ -157,58 +157,6 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
   }
 }
 
-// MoE routing (batch 1): softmax is monotonic, so the top-k by probability
-// are the k largest router logits (lower expert id first on ties); their
-// probabilities renormalised over the k chosen are exp(l - l_max) / sum.
-// One warp: lane l holds logits l, l + 32, ... (E <= 32 * RT_VPL, all in
-// registers; every loop has a fixed trip count).  Each round takes the warp's
-// best remaining (value, id) with shuffles and the owner lane marks it taken.
-// Lane 0 writes ids[0..K) and w[0..K).
-constexpr int RT_VPL = 8;
-MK_DEV void route_topk(const float* lg, int E, int K, int lane, int* ids, float* w) {
-  float v[RT_VPL];
-#pragma unroll
-  for (int k = 0; k < RT_VPL; k++) {
-    const int e = lane + 32 * k;
-    v[k] = e < E ? __ldcg(lg + e) : -INFINITY;
-  }
-  uint32_t taken = 0;
-  float top = 0.f, sum = 0.f;
-  for (int j = 0; j < K; j++) {
-    float best = -INFINITY;
-    int bi = 0x7FFFFFFF;
-#pragma unroll
-    for (int k = 0; k < RT_VPL; k++) {
-      const int e = lane + 32 * k;
-      const bool ok = e < E && !((taken >> k) & 1u);
-      if (ok && (v[k] > best || (v[k] == best && e < bi))) {
-        best = v[k];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-      if (ob > best || (ob == best && oi < bi)) {
-        best = ob;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << ((bi >> 5) & (RT_VPL - 1));
-    if (j == 0) top = best;
-    const float p = expf(best - top);
-    sum += p;
-    if (lane == 0) {
-      ids[j] = bi;
-      w[j] = p;
-    }
-  }
-  if (lane == 0)
-    for (int j = 0; j < K; j++) w[j] /= sum;
-  __syncwarp();
-}
-
 // ---------------------------------------------------------------- norms ----
 // xn[b][k] = x[b][k] * rsqrt(mean(x^2) + eps) * gain[k] for the residual
 // x_j (j = 0: the embedding row of the token).  The gain slice of each
@@ -1090,11 +1038,55 @@ MK_DEV bool op_router(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
   Seg s[2];
   get_segs<HT, D>(g, I, c.pos, c.topk, s);
-  const int lane = c.lane, B = g.B;
   float* rl = g.rlog + (size_t)I.layer * g.B * g.E + I.r0;
   const int E = g.E;
   gemv(c, g, s[0], xr, [&](uint32_t r, int b, float y) { rl[(size_t)b * E + r] = y; });
   consumer_bar();
+  // Every router instruction of the layer arrives once; the last to arrive
+  // ranks all E logits and publishes the routing, then signals the router
+  // counter once for all of them (I.aux of them).  Softmax is monotonic, so
+  // the top-K by probability are the K largest logits; rank i = number of
+  // logits above logit i, equal ones with a lower id counting as above.
+  // Weights are the probabilities renormalised over the K chosen,
+  // exp(l - l_max) / sum.  Batch 1 (sequence 0).
+  int* arrived = c.flag + 3;
+  if (c.tid == 0)
+    *arrived = (int)atom_add_acq_rel(g.ctr + CtrMap{g.Hkv, g.L}.router_arrive(I.layer), 1u);
+  consumer_bar();
+  if ((uint32_t)*arrived != g.epoch * I.aux - 1u) return true;
+  float* ys = c.yrow;               // [E <= 256] logits
+  int* sel = (int*)(c.yrow + 256);  // [K <= 16] ids by rank
+  float* sv = c.yrow + 256 + 16;    // [K] their logits
+  const float* lg = g.rlog + (size_t)I.layer * g.B * g.E;
+  for (int i = c.tid; i < E; i += NCT) ys[i] = __ldcg(lg + i);
+  if (c.tid < g.K) {
+    sel[c.tid] = 0;
+    sv[c.tid] = -INFINITY;
+  }
+  consumer_bar();
+  for (int i = c.tid; i < E; i += NCT) {
+    const float li = ys[i];
+    int rank = 0;
+    for (int j = 0; j < E; j++) {
+      const float lj = ys[j];
+      rank += (lj > li || (lj == li && j < i)) ? 1 : 0;
+    }
+    if (rank < g.K) {
+      sel[rank] = i;
+      sv[rank] = li;
+    }
+  }
+  consumer_bar();
+  if (c.tid == 0) {
+    const float top = sv[0];
+    float sum = 0.f;
+    for (int r = 0; r < g.K; r++) sum += expf(sv[r] - top);
+    for (int r = 0; r < g.K; r++) {
+      g.routes[(size_t)I.layer * g.K + r] = sel[r];
+      g.rweight[(size_t)I.layer * g.K + r] = expf(sv[r] - top) / sum;
+    }
+    red_release(g.ctr + I.sig_ctr, I.aux);
+  }
   return true;
 }
 
@@ -1115,11 +1107,11 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   if (!dep_wait(c, g, I)) return false;
   if (!cached && !norm_apply(c, g, 2 * l + 1, ng)) return false;
   c.mark(g, 0);
-  if (routed) {
-    if (c.warp == 0) {
-      route_topk(g.rlog + (size_t)l * g.B * g.E, g.E, g.K, c.lane, c.topk, c.topw);
-      // record the choice (every routed slice writes the same ids)
-      if (c.lane < g.K) g.routes[(size_t)l * g.K + c.lane] = c.topk[c.lane];
+  if (routed) {  // the routing this layer's last router published (ids clamped to [0, E))
+    if (c.warp == 0 && c.lane < g.K) {
+      const int e = __ldcg(g.routes + (size_t)l * g.K + c.lane);
+      c.topk[c.lane] = min(max(e, 0), g.E - 1);
+      c.topw[c.lane] = __ldcg(g.rweight + (size_t)l * g.K + c.lane);
     }
     consumer_bar();
   }
@@ -1546,7 +1538,12 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
       if (lane == 0) ok = wait_counter(g, I.wait_ctr, g.epoch * I.wait_cnt, pc, I.op);
       if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) goto drain;
       __syncwarp();
-      route_topk(g.rlog + (size_t)I.layer * g.B * g.E, g.E, g.K, lane, ptopk, ptopw);
+      if (lane < g.K) {  // the routing published by the layer's last router
+        const int e = __ldcg(g.routes + (size_t)I.layer * g.K + lane);
+        ptopk[lane] = min(max(e, 0), g.E - 1);
+        ptopw[lane] = __ldcg(g.rweight + (size_t)I.layer * g.K + lane);
+      }
+      __syncwarp();
       routed_layer = I.layer;
     }
     __syncwarp();
@@ -1754,7 +1751,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
         t[6] = c.ring.waited;  // warp 0's time blocked on ring data during this instruction
         c.ring.waited = 0;
       }
-      if (I.sig_ctr != NO_CTR) {
+      if (I.sig_ctr != NO_CTR && I.op != OP_ROUTER) {  // routers: the last arriver signals
         if (I.flags & F_RELAXED_SIG)
           red_relaxed(g.ctr + I.sig_ctr, 1u);
         else

@@ -83,13 +83,16 @@ MK_HD inline int phase_of(uint8_t op) {
 //   qkv[g] (g < Hkv), attn[g], oproj, mlp, router, mlp_up; then one argmax counter.
 struct CtrMap {
   int Hkv, L;
-  MK_HD int stride() const { return 2 * Hkv + 4; }
+  MK_HD int stride() const { return 2 * Hkv + 5; }
   MK_HD uint32_t qkv(int l, int g) const { return (uint32_t)(l * stride() + g); }
   MK_HD uint32_t attn(int l, int g) const { return (uint32_t)(l * stride() + Hkv + g); }
   MK_HD uint32_t oproj(int l) const { return (uint32_t)(l * stride() + 2 * Hkv); }
   MK_HD uint32_t mlp(int l) const { return (uint32_t)(l * stride() + 2 * Hkv + 1); }
   MK_HD uint32_t router(int l) const { return (uint32_t)(l * stride() + 2 * Hkv + 2); }
   MK_HD uint32_t mlp_up(int l) const { return (uint32_t)(l * stride() + 2 * Hkv + 3); }
+  // router instructions arriving (not a dependency: the last arriver ranks
+  // the logits, then signals router(l) on behalf of all of them)
+  MK_HD uint32_t router_arrive(int l) const { return (uint32_t)(l * stride() + 2 * Hkv + 4); }
   MK_HD uint32_t lm() const { return (uint32_t)(L * stride()); }
   MK_HD int count() const { return L * stride() + 1; }
 };
@@ -156,7 +159,8 @@ struct Globals {
   float* rlog;             // [L][B][E] router logits
   float* hglob;            // [L][B][F] SiLU(gate)*up (split MLP)
   TagWord* xt;             // [L][B][H] tagged x_{2l+2} (split MLP: written once, by row owners)
-  int* routes;             // [L][K] expert ids chosen at the last step (MoE, batch 1)
+  int* routes;             // [L][K] expert ids of the current step (MoE, batch 1), by rank
+  float* rweight;          // [L][K] their router probabilities renormalised over the K chosen
   float* lm_val;           // [n_lm][B]
   int* lm_idx;             // [n_lm][B]
   uint32_t* ctr;           // dependency counters

@@ -37,7 +37,8 @@ int plan_shape_ok(const mk_model_desc& d) {
   if (d.hidden % 256 || d.hidden > 16384) return MK_ERR_UNSUPPORTED;
   if (d.head_dim != 64 && d.head_dim != 128) return MK_ERR_UNSUPPORTED;
   if (d.n_q_heads / d.n_kv_heads > 8) return MK_ERR_UNSUPPORTED;
-  if (d.n_experts > 256 || d.top_k > 16) return MK_ERR_UNSUPPORTED;  // 8 router logits per lane
+  // the last router of a layer ranks up to 256 logits in shared memory
+  if (d.n_experts > 256 || d.top_k > 16) return MK_ERR_UNSUPPORTED;
   return MK_OK;
 }
 
@@ -160,9 +161,11 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
         a = e;
       }
     }
-    // ---- MoE router rows
+    // ---- MoE router rows; aux of each router instruction = how many there
+    // are in the layer (the last to arrive signals the counter for all)
     if (moe) {
       const long E = d.n_experts;
+      std::vector<std::pair<int, size_t>> routers;
       for (int i = 0; i < n_sm; i++) {
         long a = cut(E, n_sm, i, 1), b = (i == n_sm - 1) ? E : cut(E, n_sm, i + 1, 1);
         while (a < b) {
@@ -173,10 +176,12 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
           I.wait_ctr = cm.oproj(l);
           I.sig_ctr = cm.router(l);
           qs[i].push_back(I);
+          routers.push_back({i, qs[i].size() - 1});
           bytes[i] += (double)(e - a) * H * 2;
           a = e;
         }
       }
+      for (auto& rp : routers) qs[rp.first][rp.second].aux = (uint32_t)routers.size();
     }
     // ---- split MLP (dense, batch 1): gate/up column slices, then down rows
     if (mlp_split(d)) {
@@ -416,6 +421,8 @@ int plan_verify(const mk_model_desc& d, int B, const PlanOut& p) {
           return 9;
         for (uint32_t r = I.r0; r < I.r1; r++)
           if (!mark(rt, (size_t)l * d.n_experts + r)) return 10;
+        // the last router to arrive signals for all: aux = their number
+        if (I.sig_ctr != cm.router(l) || I.aux == 0 || I.aux != sig_count[I.sig_ctr]) return 31;
         break;
       case OP_MLP: {
         if (l >= L || I.r0 >= I.r1 || I.r1 - I.r0 > (uint32_t)MAX_COLS) return 11;

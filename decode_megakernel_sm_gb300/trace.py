@@ -130,7 +130,8 @@ def chrome_trace(trace, queues, n_sm: int, max_pc: int, path: str):
         ev.append({"name": name, "ph": "X", "pid": 0, "tid": s, "ts": (tw1 - base) / 1e3,
                    "dur": (te - tw1) / 1e3,
                    "args": {"prologue_end": (m0 - base) / 1e3, "ring_end": (m1 - base) / 1e3,
-                            "signal_done": (tsig - base) / 1e3}})
+                            "signal_done": (tsig - base) / 1e3,
+                            "ring_data_wait_us": rw / 1e3}})
         if tp:
             ev.append({"name": "issue " + name, "ph": "i", "pid": 1, "tid": s,
                        "ts": (tp - base) / 1e3, "s": "t"})
