@@ -20,6 +20,7 @@ cudaError_t pack_interleave(uint16_t* dst, const void* a, const void* b, long ro
                             cudaStream_t s);
 cudaError_t pack_wo(uint16_t* dst, const void* wo, int H, int Hq, int D, cudaStream_t s);
 cudaError_t pack_rows(uint16_t* dst, const void* src, long rows, int H, cudaStream_t s);
+cudaError_t pack_down_tiles(uint16_t* dst, const void* src, int H, int F, cudaStream_t s);
 cudaError_t pack_transpose(uint16_t* dst, const void* src, int R, int C, int batch,
                            cudaStream_t s);
 
@@ -59,7 +60,10 @@ static Scratch carve_scratch(const mk_model_desc& d, size_t B, size_t kc, size_t
   const size_t sr = al256(L * B * E * 4), sl = al256(n_lm * B * 4);
   const size_t sc = al256(n_ctr * 4), se = 256;
   const size_t sroute = al256(L * (size_t)(d.top_k > 0 ? d.top_k : 1) * 4);  // ids, then weights
-  const size_t sxt = al256(L * B * H * 8), sh = al256(L * B * F * 4);
+  // h: batch-1 split [L][B][F] floats; batched split [L][F/16][32] A-fragment
+  // words of 16 bytes (8 sequences x 4 bytes per column)
+  const size_t hB = mlp_split_batched(d) ? 8 : B;
+  const size_t sxt = al256(L * B * H * 8), sh = al256(L * hB * F * 4);
   Scratch s{};
   s.xbuf_bytes = sx;
   s.ctr_bytes = sc;
@@ -305,6 +309,8 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
       CK(pack_interleave(gu, w->w_gate[l], w->w_up[l], d.ffn, H, s));
       if (mlp_split(d))  // the down rows are streamed as they are
         CK(cudaMemcpyAsync(dT, w->w_down[l], ls.dT * 2, cudaMemcpyDeviceToDevice, s));
+      else if (mlp_split_batched(d))  // tiles of 8 rows x BD_KC columns
+        CK(pack_down_tiles(dT, w->w_down[l], H, d.ffn, s));
       else
         CK(pack_transpose(dT, w->w_down[l], H, d.ffn, 1, s));
     } else {
@@ -470,6 +476,7 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.Fs = d.shared_ffn;
   g.kc = h->kc;
   g.xtag = mlp_split(d) ? 1 : 0;
+  g.bsplit = mlp_split_batched(d) ? 1 : 0;
   g.eps = d.rms_eps;
   g.lm_ctr = CtrMap{d.n_kv_heads, d.n_layers}.lm();
   g.n_lm = h->plan.n_lm;

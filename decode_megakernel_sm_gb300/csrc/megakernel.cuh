@@ -133,7 +133,14 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
       s[0] = {(const unsigned char*)(Lp->wgu + (size_t)I.r0 * 2 * HT), nullptr, ROW, 2 * n, RPS,
               2 * I.r0};
       return 1;
-    case OP_MLP_DOWN:  // rows of the row-major [H][F] down projection
+    case OP_MLP_DOWN:
+      if (g.bsplit) {  // tiles of 8 rows x BD_KC columns, rows [r0, r1) in whole tiles
+        const uint32_t nkc = (uint32_t)g.F / BD_KC, tile = 8u * BD_KC * 2u;
+        s[0] = {(const unsigned char*)(Lp->wdT + (size_t)(I.r0 / 8) * nkc * 8 * BD_KC), nullptr,
+                tile, (n / 8) * nkc, SBY / tile};
+        return 1;
+      }
+      // rows of the row-major [H][F] down projection
       s[0] = {(const unsigned char*)(Lp->wdT + (size_t)I.r0 * g.F), nullptr, (uint32_t)g.F * 2, n,
               SBY / ((uint32_t)g.F * 2)};
       return 1;
@@ -1210,11 +1217,38 @@ MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   c.mark(g, 1);
   consumer_bar();
   const int ncol = (int)(I.r1 - I.r0);
-  for (int t = c.tid; t < NB * ncol; t += NCT) {
-    const int b = t / ncol, j = t % ncol;
-    if (b < g.B) {
-      const float gt = yrow[b * MAX_ROWS + 2 * j], up = yrow[b * MAX_ROWS + 2 * j + 1];
-      g.hglob[((size_t)l * g.B + b) * g.F + I.r0 + j] = (gt / (1.f + expf(-gt))) * up;
+  if constexpr (NB > 1) {
+    // h into shared memory (0 for sequences past the batch), then out as the
+    // down rows' tensor-core A fragments, one 16-byte word per (16-column
+    // k-tile, lane 4g + t): bf16 hi / lo of sequence g at columns 2t, 2t+1
+    // and 2t+8, 2t+9 of the k-tile (the slice is whole k-tiles)
+    float* hs = c.hbuf;  // [NB][MAX_COLS]
+    for (int t = c.tid; t < NB * ncol; t += NCT) {
+      const int b = t / ncol, j = t % ncol;
+      float h = 0.f;
+      if (b < g.B) {
+        const float gt = yrow[b * MAX_ROWS + 2 * j], up = yrow[b * MAX_ROWS + 2 * j + 1];
+        h = (gt / (1.f + expf(-gt))) * up;
+      }
+      hs[b * MAX_COLS + j] = h;
+    }
+    consumer_bar();
+    uint4* hf = (uint4*)g.hglob + ((size_t)l * (g.F / 16) + I.r0 / 16) * 32;
+    for (int it = c.tid; it < (ncol / 16) * 32; it += NCT) {
+      const int kt = it / 32, ln = it % 32, gq = ln >> 2, tq = ln & 3;
+      const float* hp = hs + gq * MAX_COLS + kt * 16 + 2 * tq;
+      uint4 f;
+      split2(hp[0], hp[1], f.x, f.y);
+      split2(hp[8], hp[9], f.z, f.w);
+      hf[it] = f;
+    }
+  } else {
+    for (int t = c.tid; t < NB * ncol; t += NCT) {
+      const int b = t / ncol, j = t % ncol;
+      if (b < g.B) {
+        const float gt = yrow[b * MAX_ROWS + 2 * j], up = yrow[b * MAX_ROWS + 2 * j + 1];
+        g.hglob[((size_t)l * g.B + b) * g.F + I.r0 + j] = (gt / (1.f + expf(-gt))) * up;
+      }
     }
   }
   consumer_bar();
@@ -1229,8 +1263,95 @@ MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
 template <int HT, int D, int HPG, int NB>
 MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   if constexpr (NB != 1) {
-    if (c.tid == 0) set_err(g, MK_ERR_DEVICE, c.pc, I.op);
-    return false;
+    // Batched (8 sequences): rows [r0, r1) in blocks of 8, each block's down
+    // weights streamed as F / BD_KC tiles of 8 rows x BD_KC columns.  Tensor
+    // cores with A = h (fragments written by the gate/up slices) and B = the
+    // tile's 8 rows (ldmatrix, chunk-swizzled).  A tile's 32 k-tile pairs are
+    // split over the warps; each warp loads the A fragments of the next tile
+    // from L2 while it computes the current one.  Per-warp partial sums meet
+    // in shared memory at the end; each row has one writer (plain stores).
+    static_assert(NB == 8, "fragments of 8 sequences");
+    constexpr int NPT = BD_KC / 32;              // k-tile pairs per tile
+    constexpr int PPW = (NPT + NCW - 1) / NCW;   // pairs per warp, at most
+    const int l = I.layer, nkc = g.F / BD_KC;
+    const int nrows = (int)(I.r1 - I.r0), nrb = nrows / 8, ntiles = nrb * nkc;
+    if (!dep_wait(c, g, I)) return false;
+    float* res = c.yrow;  // [nrows][NB] residual rows x_{2l+1}
+    for (int t = c.tid; t < nrows * NB; t += NCT) {
+      const int r = t / NB, b = t % NB;
+      res[t] = b < g.B ? xres_sum(g, 2 * l + 1, b, (int)I.r0 + r) : 0.f;
+    }
+    c.mark(g, 0);
+    const int p0 = c.warp * NPT / NCW, np = (c.warp + 1) * NPT / NCW - p0;
+    const int gq = c.lane >> 2, tq = c.lane & 3;
+    const uint4* hf = (const uint4*)g.hglob + (size_t)l * (g.F / 16) * 32 + c.lane;
+    uint4 ac[PPW][2], an[PPW][2];
+    auto load_a = [&](int idx, uint4(&a)[PPW][2]) {
+      const int kt0 = (idx % nkc) * (BD_KC / 16);
+#pragma unroll
+      for (int pp = 0; pp < PPW; pp++)
+        if (pp < np) {
+          const int kt = kt0 + 2 * (p0 + pp);
+          a[pp][0] = __ldcg(hf + (size_t)kt * 32);
+          a[pp][1] = __ldcg(hf + (size_t)(kt + 1) * 32);
+        }
+    };
+    load_a(0, ac);
+    float* part = c.xn;  // [NCW][8 blocks][8 rows][NB]
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint32_t li = (uint32_t)c.lane & 7u, lm = (uint32_t)c.lane >> 3;
+    Seg s[2];
+    get_segs<HT, D>(g, I, c.pos, c.topk, s);
+    bool bad = false;
+    int idx = 0;
+    for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
+      const uint32_t n = min(s[0].ups, s[0].n - u0);
+      if (!bad && !c.ring.acquire(g)) bad = true;
+      if (bad) continue;
+      const uint32_t sbase = smem_u32(c.ring.stage_ptr());
+      for (uint32_t j = 0; j < n; j++, idx++) {
+        if (idx + 1 < ntiles) load_a(idx + 1, an);
+        const uint32_t rowaddr = sbase + j * (8u * BD_KC * 2u) + li * (BD_KC * 2u);
+#pragma unroll
+        for (int pp = 0; pp < PPW; pp++) {
+          if (pp < np) {
+            const uint32_t ch = (uint32_t)(p0 + pp) * 4u + lm;
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(rowaddr + ((ch ^ li) << 4), b0, b1, b2, b3);
+            const uint32_t a0[4] = {ac[pp][0].x, ac[pp][0].y, ac[pp][0].z, ac[pp][0].w};
+            const uint32_t a1[4] = {ac[pp][1].x, ac[pp][1].y, ac[pp][1].z, ac[pp][1].w};
+            mma_16816(d, a0, b0, b1);
+            mma_16816(d, a1, b2, b3);
+          }
+        }
+        if (idx % nkc == nkc - 1) {  // the block's last tile: hi + lo sums of rows 2tq, 2tq+1
+          float* pw = part + ((size_t)(c.warp * 8 + idx / nkc) * 8) * NB + gq;
+          pw[(2 * tq) * NB] = d[0] + d[2];
+          pw[(2 * tq + 1) * NB] = d[1] + d[3];
+#pragma unroll
+          for (int e = 0; e < 4; e++) d[e] = 0.f;
+        }
+#pragma unroll
+        for (int pp = 0; pp < PPW; pp++) {
+          ac[pp][0] = an[pp][0];
+          ac[pp][1] = an[pp][1];
+        }
+      }
+      c.ring.release(c.lane);
+    }
+    c.mark(g, 1);
+    if (bad) c.flag[2] = 1;
+    consumer_bar();
+    if (c.flag[2]) return false;
+    for (int t = c.tid; t < nrows * NB; t += NCT) {
+      const int r = t / NB, b = t % NB;
+      float y = 0.f;
+#pragma unroll
+      for (int w = 0; w < NCW; w++) y += part[((size_t)(w * 8 + r / 8) * 8 + r % 8) * NB + b];
+      if (b < g.B) xres(g, 2 * l + 2, b, 0)[I.r0 + r] = res[t] + y;
+    }
+    consumer_bar();
+    return true;
   } else {
     constexpr int CPT = (DOWN_ROW_MAX / 16 + NCT - 1) / NCT;  // h chunks per thread
     const int l = I.layer, F = g.F, nch = F / 8;

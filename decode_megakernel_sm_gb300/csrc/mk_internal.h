@@ -106,7 +106,7 @@ constexpr int NTHREADS = NCT + 32;   // + one producer warp
 // row in every stage and the per-stage barrier cost is spread wider).
 constexpr int STAGE_UNIT = 16384;
 constexpr int MAX_STAGE_BYTES = 65536;
-constexpr int DEFAULT_STAGE_BYTES = 16384;
+constexpr int DEFAULT_STAGE_BYTES = 32768;
 constexpr int MAX_STAGES = 16;
 constexpr int DOWN_ROW_MAX = 16384;  // bytes of one down row (F <= 8192) in the split MLP
 constexpr int MAX_ROWS = 256;        // rows of one QKV / gate-up / router instruction
@@ -117,6 +117,15 @@ constexpr int MMA_FLUSH = 32;        // batched GEMV: rows per cross-warp sum of
 // Dense batch-1 models run the MLP as two ops (gate/up column slices, then
 // row-split down projection over the whole h) when one down row fits a ring
 // stage; otherwise one fused op per FFN column slice with float atomics.
+// Batched split MLP (dense, 2..8 sequences): gate/up column slices (multiples
+// of 16 columns) write h in tensor-core A-fragment form; the down rows are
+// owned in blocks of 8 and stream the down weights as tiles of 8 rows x
+// BD_KC columns (8 KB), so no SM reduces into another's rows.
+constexpr int BD_KC = 512;
+MK_HD inline bool mlp_split_batched(const mk_model_desc& d) {
+  return d.n_experts == 0 && d.max_batch > 1 && d.max_batch <= 8 && d.ffn % BD_KC == 0;
+}
+
 inline bool mlp_split(const mk_model_desc& d) {
   return d.n_experts == 0 && d.max_batch == 1 && d.ffn % 8 == 0 && d.ffn * 2 <= DOWN_ROW_MAX;
 }
@@ -179,6 +188,7 @@ struct Globals {
   uint32_t epoch;          // step number (>= 1); counter targets are epoch * count, and
                            // tagged words written in this step carry tag == epoch
   int xtag;                // x_{2l+2} lives in xt (split MLP) rather than in xbuf
+  int bsplit;              // batched split MLP (hglob holds h as A fragments)
   int parity;              // epoch & 1: which residual buffer set this step uses
   uint32_t lm_ctr;
   int n_lm;

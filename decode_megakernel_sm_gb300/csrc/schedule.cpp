@@ -184,10 +184,14 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
       for (auto& rp : routers) qs[rp.first][rp.second].aux = (uint32_t)routers.size();
     }
     // ---- split MLP (dense, batch 1): gate/up column slices, then down rows
-    if (mlp_split(d)) {
-      const long F = d.ffn;
+    if (mlp_split(d) || mlp_split_batched(d)) {
+      // batched: gate/up slices in whole 16-column k-tiles of h, down rows in
+      // whole 8-row weight tiles
+      const bool bat = mlp_split_batched(d);
+      const long F = d.ffn, cu = bat ? 16 : 1, ru = bat ? 8 : 1;
       for (int i = 0; i < n_sm; i++) {
-        long a = cut(F, n_sm, i, 1), b = (i == n_sm - 1) ? F : cut(F, n_sm, i + 1, 1);
+        long a = cut(F / cu, n_sm, i, 1) * cu;
+        long b = (i == n_sm - 1) ? F : cut(F / cu, n_sm, i + 1, 1) * cu;
         bool first = true;
         while (a < b) {
           const long e = std::min(b, a + MAX_COLS);
@@ -204,15 +208,16 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
         }
       }
       for (int i = 0; i < n_sm; i++) {
-        long a = cut(H, n_sm, i, 1), b = (i == n_sm - 1) ? H : cut(H, n_sm, i + 1, 1);
+        long a = cut(H / ru, n_sm, i, 1) * ru;
+        long b = (i == n_sm - 1) ? H : cut(H / ru, n_sm, i + 1, 1) * ru;
         while (a < b) {
           const long e = std::min(b, a + MAX_DOWN_ROWS);
           Instr I = mk(OP_MLP_DOWN, l);
           I.r0 = (uint32_t)a;
           I.r1 = (uint32_t)e;
-          // its rows of x_{2l+2} leave as tagged words, polled by their
-          // consumers: the signal needs no release
-          I.flags = F_RELAXED_SIG;
+          // batch 1: its rows of x_{2l+2} leave as tagged words, polled by
+          // their consumers, so the signal needs no release
+          I.flags = bat ? 0 : F_RELAXED_SIG;
           I.wait_ctr = cm.mlp_up(l);
           I.sig_ctr = cm.mlp(l);
           qs[i].push_back(I);
@@ -446,16 +451,18 @@ int plan_verify(const mk_model_desc& d, int B, const PlanOut& p) {
         break;
       }
       case OP_MLP_UP:
-        if (!mlp_split(d) || l >= L || I.r0 >= I.r1 || I.r1 - I.r0 > (uint32_t)MAX_COLS ||
-            (long)I.r1 > Fv)
+        if (!(mlp_split(d) || mlp_split_batched(d)) || l >= L || I.r0 >= I.r1 ||
+            I.r1 - I.r0 > (uint32_t)MAX_COLS || (long)I.r1 > Fv)
           return 23;
+        if (mlp_split_batched(d) && ((I.r0 % 16) || (I.r1 % 16))) return 23;
         for (uint32_t c = I.r0; c < I.r1; c++)
           if (!mark(mlp, (size_t)l * Fv + c)) return 24;
         break;
       case OP_MLP_DOWN:
-        if (!mlp_split(d) || l >= L || I.r0 >= I.r1 || (int)I.r1 > H ||
+        if (!(mlp_split(d) || mlp_split_batched(d)) || l >= L || I.r0 >= I.r1 || (int)I.r1 > H ||
             I.r1 - I.r0 > (uint32_t)MAX_DOWN_ROWS)
           return 25;
+        if (mlp_split_batched(d) && ((I.r0 % 8) || (I.r1 % 8))) return 25;
         for (uint32_t r = I.r0; r < I.r1; r++)
           if (!mark(res, (size_t)l * H + r)) return 26;
         break;

@@ -31,7 +31,7 @@ def test_ragged_small_shape_parity():
     run_steps(cfg, 4, seed=3)
 
 
-@pytest.mark.parametrize("sb", [32768, 49152, 65536])
+@pytest.mark.parametrize("sb", [16384, 49152, 65536])
 def test_ring_stage_sizes(sb):
     # the same ragged shape with every larger stage size: more rows, more
     # cache positions and more down rows per stage, results unchanged
@@ -72,6 +72,15 @@ def test_batch8_variant_ragged_lengths():
     cfg = synth.custom(n_layers=2, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=64, ffn=3000,
                        vocab=5000, batch=8, prefill=(0, 300), steps=3, rope_theta=5e5)
     run_steps(cfg, 3, seed=7)
+
+
+@pytest.mark.parametrize("batch", [8, 5])
+def test_batched_split_mlp(batch):
+    # batch > 1 with an FFN of whole 512-column tiles: gate/up slices write h
+    # as tensor-core fragments, row-owned down tiles (batch 5: padded rows)
+    cfg = synth.custom(n_layers=2, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=64, ffn=2048,
+                       vocab=5000, batch=batch, prefill=(0, 300), steps=3, rope_theta=5e5)
+    run_steps(cfg, 3, seed=17)
 
 
 def test_llama1b_1k_parity():

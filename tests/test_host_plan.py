@@ -126,8 +126,9 @@ def test_plan_covers_all_work_and_is_deadlock_free(name, n_sm):
     assert L.mk_plan_check(q, n_sm, st["max_pc"], st["n_counters"]) == L.MK_OK
 
 
-def test_split_mlp_is_used_for_dense_batch1_only():
-    for name, split in (("llama1b_1k", True), ("tiny", True), ("llama1b_b8", False), ("moe", False)):
+def test_split_mlp_is_used_for_dense_models():
+    # batch 1, and batches of up to 8 whose FFN is whole 512-column tiles
+    for name, split in (("llama1b_1k", True), ("tiny", True), ("llama1b_b8", True), ("moe", False)):
         cfg, d = desc(name)
         st, q = L.mk_plan(d, cfg["batch"], cfg["max_seq"], 152)
         ops = {q[i].op for i in range(152 * st["max_pc"])}
@@ -219,3 +220,12 @@ def test_checker_rejects_plain_wait_on_relaxed_signals():
     i = next(i for i in range(len(q)) if q[i].op == 1 and q[i].layer == 1)
     q[i].flags &= ~16
     assert L.mk_plan_check(q, 8, st["max_pc"], st["n_counters"]) == L.MK_ERR_SCHEDULE
+
+
+def test_batched_split_mlp_cuts_whole_tiles():
+    cfg, d = desc("llama1b_b8")
+    st, q = L.mk_plan(d, cfg["batch"], cfg["max_seq"], 152)
+    ops = [q[i] for i in range(152 * st["max_pc"]) if q[i].op in (8, 9)]
+    assert all(I.r0 % 16 == 0 and I.r1 % 16 == 0 for I in ops if I.op == 8)
+    assert all(I.r0 % 8 == 0 and I.r1 % 8 == 0 and I.r1 - I.r0 <= 64 for I in ops if I.op == 9)
+    assert not any(I.flags & (16 | 32) for I in ops)  # no tagged hops at batch > 1
