@@ -205,6 +205,8 @@ static int size_ring(mk_handle* h, int stage_bytes) {
   const mk_model_desc& d = h->d;
   const int K = d.n_experts > 0 ? d.top_k : 0;
   const int HPG = d.n_q_heads / d.n_kv_heads;
+  // batched split down: a stage carries a weight unit and its h fragments
+  if (mlp_split_batched(d) && stage_bytes < 2 * BD_ROWS * BD_KC * 2) return MK_ERR_UNSUPPORTED;
   int optin = 0;
   CK(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->dev));
   int ns = 0;
@@ -309,7 +311,7 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
       CK(pack_interleave(gu, w->w_gate[l], w->w_up[l], d.ffn, H, s));
       if (mlp_split(d))  // the down rows are streamed as they are
         CK(cudaMemcpyAsync(dT, w->w_down[l], ls.dT * 2, cudaMemcpyDeviceToDevice, s));
-      else if (mlp_split_batched(d))  // tiles of 8 rows x BD_KC columns
+      else if (mlp_split_batched(d))  // units of BD_ROWS rows x BD_KC columns
         CK(pack_down_tiles(dT, w->w_down[l], H, d.ffn, s));
       else
         CK(pack_transpose(dT, w->w_down[l], H, d.ffn, 1, s));

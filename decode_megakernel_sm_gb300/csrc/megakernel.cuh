@@ -134,10 +134,13 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
               2 * I.r0};
       return 1;
     case OP_MLP_DOWN:
-      if (g.bsplit) {  // tiles of 8 rows x BD_KC columns, rows [r0, r1) in whole tiles
-        const uint32_t nkc = (uint32_t)g.F / BD_KC, tile = 8u * BD_KC * 2u;
-        s[0] = {(const unsigned char*)(Lp->wdT + (size_t)(I.r0 / 8) * nkc * 8 * BD_KC), nullptr,
-                tile, (n / 8) * nkc, SBY / tile};
+      if (g.bsplit) {
+        // BD_ROWS rows; per chunk of BD_KC columns, the weight unit (lower
+        // half of a stage) and that chunk's h fragments (upper half)
+        const uint32_t nkc = (uint32_t)g.F / BD_KC, unit = BD_ROWS * BD_KC * 2u;
+        s[0] = {(const unsigned char*)(Lp->wdT + (size_t)(I.r0 / BD_ROWS) * nkc * BD_ROWS * BD_KC),
+                (const unsigned char*)g.hglob + (size_t)I.layer * (g.F / 16) * 512, unit, nkc,
+                (SBY / 2) / unit};
         return 1;
       }
       // rows of the row-major [H][F] down projection
@@ -1242,6 +1245,8 @@ MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
       split2(hp[8], hp[9], f.z, f.w);
       hf[it] = f;
     }
+    // the down instructions copy these fragments with the bulk-copy engine
+    asm volatile("fence.proxy.async.global;" ::: "memory");
   } else {
     for (int t = c.tid; t < NB * ncol; t += NCT) {
       const int b = t / ncol, j = t % ncol;
@@ -1263,91 +1268,71 @@ MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
 template <int HT, int D, int HPG, int NB>
 MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   if constexpr (NB != 1) {
-    // Batched (8 sequences): rows [r0, r1) in blocks of 8, each block's down
-    // weights streamed as F / BD_KC tiles of 8 rows x BD_KC columns.  Tensor
-    // cores with A = h (fragments written by the gate/up slices) and B = the
-    // tile's 8 rows (ldmatrix, chunk-swizzled).  A tile's 32 k-tile pairs are
-    // split over the warps; each warp loads the A fragments of the next tile
-    // from L2 while it computes the current one.  Per-warp partial sums meet
-    // in shared memory at the end; each row has one writer (plain stores).
+    // Batched (8 sequences): BD_ROWS rows.  Each ring stage holds, per
+    // chunk of BD_KC columns, the rows' weight unit (lower half, chunk
+    // q of unit row i at slot q ^ (i & 7)) and the chunk's h fragments
+    // (upper half) as the gate/up slices wrote them.  Tensor cores: A = h
+    // (rows 0-7 the hi parts of 8 sequences, rows 8-15 the lo parts), B =
+    // 8 weight rows (ldmatrix); a chunk's BD_KC / 16 k-tiles are split over
+    // the warps.  Per-warp partial sums meet in shared memory at the end;
+    // each row has one writer (plain stores).
     static_assert(NB == 8, "fragments of 8 sequences");
-    constexpr int NPT = BD_KC / 32;              // k-tile pairs per tile
-    constexpr int PPW = (NPT + NCW - 1) / NCW;   // pairs per warp, at most
-    const int l = I.layer, nkc = g.F / BD_KC;
-    const int nrows = (int)(I.r1 - I.r0), nrb = nrows / 8, ntiles = nrb * nkc;
+    constexpr int KT = BD_KC / 16;                        // k-tiles per chunk
+    constexpr uint32_t UNIT = BD_ROWS * BD_KC * 2u;       // bytes of a weight unit
+    const int l = I.layer;
     if (!dep_wait(c, g, I)) return false;
-    float* res = c.yrow;  // [nrows][NB] residual rows x_{2l+1}
-    for (int t = c.tid; t < nrows * NB; t += NCT) {
+    float* res = c.yrow;  // [BD_ROWS][NB] residual rows x_{2l+1}
+    for (int t = c.tid; t < BD_ROWS * NB; t += NCT) {
       const int r = t / NB, b = t % NB;
       res[t] = b < g.B ? xres_sum(g, 2 * l + 1, b, (int)I.r0 + r) : 0.f;
     }
     c.mark(g, 0);
-    const int p0 = c.warp * NPT / NCW, np = (c.warp + 1) * NPT / NCW - p0;
+    const int kt0 = c.warp * KT / NCW, kt1 = (c.warp + 1) * KT / NCW;
     const int gq = c.lane >> 2, tq = c.lane & 3;
-    const uint4* hf = (const uint4*)g.hglob + (size_t)l * (g.F / 16) * 32 + c.lane;
-    uint4 ac[PPW][2], an[PPW][2];
-    auto load_a = [&](int idx, uint4(&a)[PPW][2]) {
-      const int kt0 = (idx % nkc) * (BD_KC / 16);
-#pragma unroll
-      for (int pp = 0; pp < PPW; pp++)
-        if (pp < np) {
-          const int kt = kt0 + 2 * (p0 + pp);
-          a[pp][0] = __ldcg(hf + (size_t)kt * 32);
-          a[pp][1] = __ldcg(hf + (size_t)(kt + 1) * 32);
-        }
-    };
-    load_a(0, ac);
-    float* part = c.xn;  // [NCW][8 blocks][8 rows][NB]
-    float d[4] = {0.f, 0.f, 0.f, 0.f};
-    const uint32_t li = (uint32_t)c.lane & 7u, lm = (uint32_t)c.lane >> 3;
+    // ldmatrix lanes: matrix m = lane / 8 is rows 8 (m / 2) .. +7, k half m % 2
+    const uint32_t li = (uint32_t)c.lane & 7u, mi = (uint32_t)c.lane >> 3;
+    const uint32_t roff = (li + 8u * (mi >> 1)) * (BD_KC * 2u);
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
     Seg s[2];
     get_segs<HT, D>(g, I, c.pos, c.topk, s);
+    const uint32_t SB = (uint32_t)g.stage_bytes;
     bool bad = false;
-    int idx = 0;
     for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
       const uint32_t n = min(s[0].ups, s[0].n - u0);
       if (!bad && !c.ring.acquire(g)) bad = true;
       if (bad) continue;
-      const uint32_t sbase = smem_u32(c.ring.stage_ptr());
-      for (uint32_t j = 0; j < n; j++, idx++) {
-        if (idx + 1 < ntiles) load_a(idx + 1, an);
-        const uint32_t rowaddr = sbase + j * (8u * BD_KC * 2u) + li * (BD_KC * 2u);
-#pragma unroll
-        for (int pp = 0; pp < PPW; pp++) {
-          if (pp < np) {
-            const uint32_t ch = (uint32_t)(p0 + pp) * 4u + lm;
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(rowaddr + ((ch ^ li) << 4), b0, b1, b2, b3);
-            const uint32_t a0[4] = {ac[pp][0].x, ac[pp][0].y, ac[pp][0].z, ac[pp][0].w};
-            const uint32_t a1[4] = {ac[pp][1].x, ac[pp][1].y, ac[pp][1].z, ac[pp][1].w};
-            mma_16816(d, a0, b0, b1);
-            mma_16816(d, a1, b2, b3);
-          }
-        }
-        if (idx % nkc == nkc - 1) {  // the block's last tile: hi + lo sums of rows 2tq, 2tq+1
-          float* pw = part + ((size_t)(c.warp * 8 + idx / nkc) * 8) * NB + gq;
-          pw[(2 * tq) * NB] = d[0] + d[2];
-          pw[(2 * tq + 1) * NB] = d[1] + d[3];
-#pragma unroll
-          for (int e = 0; e < 4; e++) d[e] = 0.f;
-        }
-#pragma unroll
-        for (int pp = 0; pp < PPW; pp++) {
-          ac[pp][0] = an[pp][0];
-          ac[pp][1] = an[pp][1];
+      const uint32_t wb = smem_u32(c.ring.stage_ptr());
+      const unsigned char* hb = c.ring.stage_ptr() + SB / 2 + c.lane * 16;
+      for (uint32_t j = 0; j < n; j++) {
+        const uint32_t wu = wb + j * UNIT + roff;
+        for (int kt = kt0; kt < kt1; kt++) {
+          const uint4 af = *(const uint4*)(hb + j * UNIT + kt * 512);
+          const uint32_t a[4] = {af.x, af.y, af.z, af.w};
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(wu + ((((uint32_t)(2 * kt) + (mi & 1u)) ^ li) << 4), b0, b1, b2, b3);
+          mma_16816(d0, a, b0, b1);
+          mma_16816(d1, a, b2, b3);
         }
       }
       c.ring.release(c.lane);
     }
     c.mark(g, 1);
+    float* part = c.xn;  // [NCW][BD_ROWS][NB]: hi + lo sums of rows 2tq, 2tq+1 (+8)
+    {
+      float* pw = part + (size_t)c.warp * BD_ROWS * NB + gq;
+      pw[(2 * tq) * NB] = d0[0] + d0[2];
+      pw[(2 * tq + 1) * NB] = d0[1] + d0[3];
+      pw[(8 + 2 * tq) * NB] = d1[0] + d1[2];
+      pw[(9 + 2 * tq) * NB] = d1[1] + d1[3];
+    }
     if (bad) c.flag[2] = 1;
     consumer_bar();
     if (c.flag[2]) return false;
-    for (int t = c.tid; t < nrows * NB; t += NCT) {
+    for (int t = c.tid; t < BD_ROWS * NB; t += NCT) {
       const int r = t / NB, b = t % NB;
       float y = 0.f;
 #pragma unroll
-      for (int w = 0; w < NCW; w++) y += part[((size_t)(w * 8 + r / 8) * 8 + r % 8) * NB + b];
+      for (int w = 0; w < NCW; w++) y += part[(size_t)w * BD_ROWS * NB + t];
       if (b < g.B) xres(g, 2 * l + 2, b, 0)[I.r0 + r] = res[t] + y;
     }
     consumer_bar();
@@ -1700,6 +1685,89 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
         }
       }
       if (__shfl_sync(0xFFFFFFFFu, bad, 0)) goto drain;
+    }
+    if (I.op == OP_MLP_DOWN && g.bsplit) {
+      // Each stage's weight unit is copied as soon as the stage is free; its
+      // h fragments, written by other SMs' gate/up slices, follow once the
+      // gate/up counter shows them complete.  The stage's full barrier
+      // expects both halves from the first arming on.
+      const Seg& S = s[0];
+      const uint32_t SB = (uint32_t)g.stage_bytes;
+      const uint32_t nst = (S.n + S.ups - 1) / S.ups;
+      uint32_t wi = 0, hi = 0;  // stages whose weights / h fragments are issued
+      bool dep = false;
+      int bad = 0;
+      const uint64_t t0 = gtimer();
+      auto stage_of = [&](uint32_t j, uint32_t& stg, uint32_t& p) {
+        const uint32_t a = (uint32_t)st + j;
+        stg = a % (uint32_t)ns;
+        p = par ^ ((a / (uint32_t)ns) & 1u);
+      };
+      auto issue = [&](uint32_t j, const unsigned char* src, uint32_t off, uint64_t pol) {
+        uint32_t stg, p;
+        stage_of(j, stg, p);
+        const uint32_t u0 = j * S.ups, bytes = min(S.ups, S.n - u0) * S.unit;
+        bulk_g2s(ring_s + stg * SB + off, src + (size_t)u0 * S.unit, bytes, full0 + 8u * stg, pol);
+      };
+      auto issue_h = [&](uint32_t j) {
+        if (lane == 0) issue(j, S.src2, SB / 2, pol_kv);
+      };
+      for (uint32_t it = 1; hi < nst; it++) {
+        bool moved = false;
+        if (wi < nst && wi < hi + (uint32_t)ns) {
+          uint32_t stg, p;
+          stage_of(wi, stg, p);
+          if (__shfl_sync(0xFFFFFFFFu, mbar_try(empty0 + 8u * stg, p ^ 1u), 0)) {
+            if (lane == 0) {
+              if (g.trace && wi == 0) g.trace[((size_t)blockIdx.x * g.max_pc + pc) * 8] = gtimer();
+              const uint32_t u0 = wi * S.ups, bytes = min(S.ups, S.n - u0) * S.unit;
+              mbar_expect_tx(full0 + 8u * stg, 2u * bytes);
+              issue(wi, S.src, 0, pol_w);
+            }
+            wi++;
+            moved = true;
+          }
+        }
+        if (!dep) {
+          int ok = 0;
+          if (lane == 0) {
+            ok = (int32_t)(ld_acquire(g.ctr + I.wait_ctr) - g.epoch * I.wait_cnt) >= 0;
+            // the fragments were written through the generic proxy
+            if (ok) asm volatile("fence.proxy.async.global;" ::: "memory");
+          }
+          dep = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        }
+        if (dep && hi < wi) {
+          issue_h(hi++);
+          moved = true;
+        }
+        if (!moved && (it & 63) == 0) {
+          if (lane == 0) {
+            if (peek_err(g)) {
+              bad = 1;
+            } else if (gtimer() - t0 > g.timeout_ns) {
+              set_err(g, MK_ERR_TIMEOUT, pc, I.op);
+              bad = 1;
+            }
+          }
+          bad = __shfl_sync(0xFFFFFFFFu, bad, 0);
+          if (bad) break;
+        }
+        __syncwarp();
+      }
+      // on failure, complete the armed stages with whatever the fragment
+      // buffer holds (the step has failed) so that every copy can be drained
+      while (hi < wi) issue_h(hi++);
+      __syncwarp();
+      issued += wi;
+      issued_bytes += 2ull * S.n * S.unit;
+      for (uint32_t j = 0; j < wi; j++)
+        if (++st == ns) {
+          st = 0;
+          par ^= 1u;
+        }
+      if (bad) goto drain;
+      continue;
     }
     for (int k = 0; k < nseg; k++) {
       for (uint32_t u0 = 0; u0 < s[k].n; u0 += s[k].ups) {

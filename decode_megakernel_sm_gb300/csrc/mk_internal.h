@@ -118,12 +118,15 @@ constexpr int MMA_FLUSH = 32;        // batched GEMV: rows per cross-warp sum of
 // row-split down projection over the whole h) when one down row fits a ring
 // stage; otherwise one fused op per FFN column slice with float atomics.
 // Batched split MLP (dense, 2..8 sequences): gate/up column slices (multiples
-// of 16 columns) write h in tensor-core A-fragment form; the down rows are
-// owned in blocks of 8 and stream the down weights as tiles of 8 rows x
-// BD_KC columns (8 KB), so no SM reduces into another's rows.
+// of 16 columns) write h in tensor-core A-fragment form; a down instruction
+// owns BD_ROWS rows and streams, per chunk of BD_KC columns, that chunk's h
+// fragments (16 KB) next to its weight unit of BD_ROWS x BD_KC (16 KB), so
+// no SM reduces into another's rows.  Needs ring stages of at least 32 KB.
 constexpr int BD_KC = 512;
+constexpr int BD_ROWS = 16;
 MK_HD inline bool mlp_split_batched(const mk_model_desc& d) {
-  return d.n_experts == 0 && d.max_batch > 1 && d.max_batch <= 8 && d.ffn % BD_KC == 0;
+  return d.n_experts == 0 && d.max_batch > 1 && d.max_batch <= 8 && d.ffn % BD_KC == 0 &&
+         d.hidden % BD_ROWS == 0;
 }
 
 inline bool mlp_split(const mk_model_desc& d) {

@@ -101,18 +101,18 @@ cudaError_t pack_interleave(uint16_t* dst, const void* a, const void* b, long ro
   return cudaGetLastError();
 }
 
-// Down projection [H][F] as tiles of 8 rows x BD_KC columns, tile (rb, kc)
-// at ((rb * (F / BD_KC) + kc) * 8) rows of BD_KC; inside a tile, 16-byte
-// chunk q of tile row i sits at slot q ^ i.
+// Down projection [H][F] as units of BD_ROWS rows x BD_KC columns, unit
+// (rb, kc) at ((rb * (F / BD_KC) + kc) * BD_ROWS) rows of BD_KC; inside a
+// unit, 16-byte chunk q of unit row i sits at slot q ^ (i & 7).
 __global__ void pack_down_tiles_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int F) {
   const int nkc = F / BD_KC, cpr = BD_KC / 8;
   const size_t r = blockIdx.x / nkc;
   const int kc = (int)(blockIdx.x % nkc);
-  const size_t rb = r / 8;
-  const int i = (int)(r % 8);
-  uint4* d = dst + ((rb * nkc + kc) * 8 + i) * cpr;
+  const size_t rb = r / BD_ROWS;
+  const int i = (int)(r % BD_ROWS);
+  uint4* d = dst + ((rb * nkc + kc) * BD_ROWS + i) * cpr;
   const uint4* sr = src + r * (F / 8) + (size_t)kc * cpr;
-  for (int q = threadIdx.x; q < cpr; q += blockDim.x) d[q ^ i] = sr[q];
+  for (int q = threadIdx.x; q < cpr; q += blockDim.x) d[q ^ (i & 7)] = sr[q];
 }
 
 cudaError_t pack_down_tiles(uint16_t* dst, const void* src, int H, int F, cudaStream_t s) {

@@ -186,9 +186,9 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
     // ---- split MLP (dense, batch 1): gate/up column slices, then down rows
     if (mlp_split(d) || mlp_split_batched(d)) {
       // batched: gate/up slices in whole 16-column k-tiles of h, down rows in
-      // whole 8-row weight tiles
+      // units of BD_ROWS rows
       const bool bat = mlp_split_batched(d);
-      const long F = d.ffn, cu = bat ? 16 : 1, ru = bat ? 8 : 1;
+      const long F = d.ffn, cu = bat ? 16 : 1, ru = bat ? BD_ROWS : 1;
       for (int i = 0; i < n_sm; i++) {
         long a = cut(F / cu, n_sm, i, 1) * cu;
         long b = (i == n_sm - 1) ? F : cut(F / cu, n_sm, i + 1, 1) * cu;
@@ -211,7 +211,7 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
         long a = cut(H / ru, n_sm, i, 1) * ru;
         long b = (i == n_sm - 1) ? H : cut(H / ru, n_sm, i + 1, 1) * ru;
         while (a < b) {
-          const long e = std::min(b, a + MAX_DOWN_ROWS);
+          const long e = std::min(b, a + (bat ? (long)BD_ROWS : (long)MAX_DOWN_ROWS));
           Instr I = mk(OP_MLP_DOWN, l);
           I.r0 = (uint32_t)a;
           I.r1 = (uint32_t)e;
@@ -462,7 +462,8 @@ int plan_verify(const mk_model_desc& d, int B, const PlanOut& p) {
         if (!(mlp_split(d) || mlp_split_batched(d)) || l >= L || I.r0 >= I.r1 || (int)I.r1 > H ||
             I.r1 - I.r0 > (uint32_t)MAX_DOWN_ROWS)
           return 25;
-        if (mlp_split_batched(d) && ((I.r0 % 8) || (I.r1 % 8))) return 25;
+        if (mlp_split_batched(d) && ((I.r0 % BD_ROWS) || I.r1 - I.r0 != (uint32_t)BD_ROWS))
+          return 25;
         for (uint32_t r = I.r0; r < I.r1; r++)
           if (!mark(res, (size_t)l * H + r)) return 26;
         break;

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import synth
-from decode_megakernel_sm_gb300 import MK_ERR_INVALID_ARG, MK_ERR_TIMEOUT, MK_OK
+from decode_megakernel_sm_gb300 import MK_ERR_INVALID_ARG, MK_ERR_TIMEOUT, MK_ERR_UNSUPPORTED, MK_OK, MkError
 from tests.harness import Run
 
 pytestmark = pytest.mark.gpu
@@ -74,13 +74,36 @@ def test_batch8_variant_ragged_lengths():
     run_steps(cfg, 3, seed=7)
 
 
+def _bsplit_cfg(batch):
+    return synth.custom(n_layers=2, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=64,
+                        ffn=2048, vocab=5000, batch=batch, prefill=(0, 300), steps=3,
+                        rope_theta=5e5)
+
+
 @pytest.mark.parametrize("batch", [8, 5])
 def test_batched_split_mlp(batch):
-    # batch > 1 with an FFN of whole 512-column tiles: gate/up slices write h
-    # as tensor-core fragments, row-owned down tiles (batch 5: padded rows)
-    cfg = synth.custom(n_layers=2, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=64, ffn=2048,
-                       vocab=5000, batch=batch, prefill=(0, 300), steps=3, rope_theta=5e5)
-    run_steps(cfg, 3, seed=17)
+    # batch > 1 with an FFN of whole 512-column chunks: gate/up slices write h
+    # as tensor-core fragments, 16-row down units stream them next to their
+    # weights (batch 5: padded rows)
+    run_steps(_bsplit_cfg(batch), 3, seed=17)
+
+
+@pytest.mark.parametrize("sb", [49152, 65536])
+def test_batched_split_mlp_stage_sizes(sb):
+    # 48 KiB: one weight unit + its fragments per stage (8 KB idle per
+    # half); 64 KiB: two of each
+    run_steps(_bsplit_cfg(8), 3, seed=19, stage_bytes=sb)
+
+
+def test_batched_split_mlp_refuses_16k_stages():
+    r = Run(_bsplit_cfg(8), seed=2)
+    try:
+        with pytest.raises(MkError) as e:
+            r.dec.set_stage_bytes(16384)
+        assert e.value.status == MK_ERR_UNSUPPORTED
+        r.step()  # the old stage size is kept
+    finally:
+        r.close()
 
 
 def test_llama1b_1k_parity():

@@ -227,5 +227,8 @@ def test_batched_split_mlp_cuts_whole_tiles():
     st, q = L.mk_plan(d, cfg["batch"], cfg["max_seq"], 152)
     ops = [q[i] for i in range(152 * st["max_pc"]) if q[i].op in (8, 9)]
     assert all(I.r0 % 16 == 0 and I.r1 % 16 == 0 for I in ops if I.op == 8)
-    assert all(I.r0 % 8 == 0 and I.r1 % 8 == 0 and I.r1 - I.r0 <= 64 for I in ops if I.op == 9)
+    # down instructions own exactly 16 rows (one weight unit per column chunk)
+    down = [I for I in ops if I.op == 9]
+    assert all(I.r0 % 16 == 0 and I.r1 - I.r0 == 16 for I in down)
+    assert sorted(I.r0 for I in down if I.layer == 0) == list(range(0, cfg["hidden"], 16))
     assert not any(I.flags & (16 | 32) for I in ops)  # no tagged hops at batch > 1
