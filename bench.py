@@ -50,7 +50,8 @@ def parse():
                     help="partial copies of each residual vector (library default if unset)")
     ap.add_argument("--hold", type=int, default=None,
                     help="hold-policy mask (library default if unset)")
-    ap.add_argument("--hold-prefetch", type=int, default=256 << 10)
+    ap.add_argument("--hold-early", type=int, default=128 << 10,
+                    help="bytes of a held instruction's copies issued early (with --hold)")
     ap.add_argument("--stage-bytes", type=int, default=None,
                     help="ring stage size in bytes (default: the library's)")
     ap.add_argument("--trace", default=None,
@@ -272,7 +273,7 @@ def main():
     if args.kc is not None:
         dec.set_residual_copies(args.kc)
     if args.hold is not None:
-        dec.set_hold_policy(args.hold, args.hold_prefetch)
+        dec.set_hold_policy(args.hold, args.hold_early)
     if args.stage_bytes is not None:
         dec.set_stage_bytes(args.stage_bytes)
     dec.build_schedule(B, cfg["max_seq"])

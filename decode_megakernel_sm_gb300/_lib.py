@@ -209,8 +209,8 @@ def mk_set_stage_bytes(h, stage_bytes: int):
     _check(lib().mk_set_stage_bytes(h, int(stage_bytes)), "mk_set_stage_bytes")
 
 
-def mk_set_hold_policy(h, mask: int, prefetch_bytes: int):
-    _check(lib().mk_set_hold_policy(h, int(mask), int(prefetch_bytes)), "mk_set_hold_policy")
+def mk_set_hold_policy(h, mask: int, early_bytes: int):
+    _check(lib().mk_set_hold_policy(h, int(mask), int(early_bytes)), "mk_set_hold_policy")
 
 
 def mk_set_trace(h, on: bool):

@@ -111,7 +111,7 @@ struct mk_handle {
   unsigned long long l2_ahead = 0;
   int kc = 1;  // partial copies of each residual vector
   unsigned hold_mask = DEFAULT_HOLD;
-  unsigned hold_prefetch = 256u << 10;
+  unsigned hold_early = DEFAULT_HOLD_EARLY;
   // host-buffer step
   cudaStream_t own = nullptr;
   int32_t *d_tok = nullptr, *d_pos = nullptr, *d_am = nullptr;
@@ -485,7 +485,7 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.sel_key = -1;
   g.trace = h->trace;
   g.l2_ahead = h->l2_ahead;
-  g.hold_prefetch = h->hold_prefetch;
+  g.hold_early = h->hold_early;
   return g;
 }
 
@@ -729,10 +729,10 @@ extern "C" int mk_decode_step_noalloc(mk_handle* h, const int32_t* d_tokens,
   return MK_OK;
 }
 
-extern "C" int mk_set_hold_policy(mk_handle* h, unsigned mask, uint64_t prefetch_bytes) {
-  if (!h || mask > 63u || prefetch_bytes > (64ull << 20)) return MK_ERR_INVALID_ARG;
+extern "C" int mk_set_hold_policy(mk_handle* h, unsigned mask, uint64_t early_bytes) {
+  if (!h || mask > 63u || early_bytes > (64ull << 20)) return MK_ERR_INVALID_ARG;
   h->hold_mask = mask;
-  h->hold_prefetch = (unsigned)prefetch_bytes;
+  h->hold_early = (unsigned)early_bytes;
   return MK_OK;
 }
 

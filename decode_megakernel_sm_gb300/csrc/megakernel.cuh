@@ -52,10 +52,11 @@ MK_DEV bool dep_wait(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   if (c.tid == 0) {
     if (g.trace) c.tw0 = gtimer();
     bool ok = true;
+    // a met counter means complete inputs; errors elsewhere in the grid
+    // surface in this and the later bounded waits (no extra L2 round trip)
     if (!(I.flags & F_TAG_WAIT)) {
       if (I.wait_ctr != NO_CTR) ok = wait_counter(g, I.wait_ctr, g.epoch * I.wait_cnt, c.pc, I.op);
     }  // F_TAG_WAIT: the op polls its tagged inputs itself
-    if (ok && peek_err(g)) ok = false;
     *c.flag = ok ? 0 : 1;
     c.flag[2] = 0;
     if (g.trace) c.tw1 = gtimer();
@@ -1587,10 +1588,9 @@ struct L2Cursor {
       const uint32_t b = n * s[k].unit;
       const unsigned long long cb = s[k].src2 ? 2ull * b : b;
       if (bytes + cb > from) {
-        const int lane = threadIdx.x & 31;
-        for (uint32_t off = (uint32_t)lane * 128u; off < b; off += 32u * 128u) {
-          prefetch_l2_line(s[k].src + (size_t)u0 * s[k].unit + off);
-          if (s[k].src2) prefetch_l2_line(s[k].src2 + (size_t)u0 * s[k].unit + off);
+        if ((threadIdx.x & 31) == 0) {
+          bulk_prefetch_l2(s[k].src + (size_t)u0 * s[k].unit, b);
+          if (s[k].src2) bulk_prefetch_l2(s[k].src2 + (size_t)u0 * s[k].unit, b);
         }
         budget--;
       }
@@ -1601,10 +1601,12 @@ struct L2Cursor {
 };
 
 // Producer warp: walks the queue and streams every instruction's segments
-// into the ring (lane 0 issues).  It waits only for free stages -- except
-// that a routed MoE slice needs the router result for its weight addresses.
-// On any error it stops issuing and waits for its copies in flight before
-// the CTA may exit.
+// into the ring (lane 0 issues).  It waits for free stages, and besides:
+// a routed MoE slice needs the router result for its weight addresses, a
+// batched down unit's activation half needs the gate/up counter, and a held
+// instruction issues its later stages only once the consumers have finished
+// the instructions before it.  On any error it stops issuing and waits for
+// its copies in flight before the CTA may exit.
 template <int HT, int D, int HPG, int NB>
 MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint32_t empty0,
                      int* ppos, int* ptopk, float* ptopw, const int* done, int lane) {
@@ -1625,7 +1627,7 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
     if (I.op == OP_HALT) break;
     if (I.op == OP_NOP || !selected(g, I)) continue;
     // every branch below is warp-uniform: lane 0 decides, the warp follows
-    if (__shfl_sync(0xFFFFFFFFu, peek_err(g), 0)) goto drain;
+    // (errors elsewhere in the grid are seen in the bounded waits below)
     const bool routed = I.op == OP_MLP && g.E > 0 && !(I.flags & F_SHARED);
     if ((I.op == OP_ATTN || routed) && !grid_waited) {
       asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -1656,36 +1658,12 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
     Seg s[2];
     const int nseg = get_segs<HT, D>(g, I, ppos, ptopk, s);
     const int my_seq = seq++;
-    if (I.flags & F_HOLD) {
-      // warm L2 with (the start of) this instruction's data -- prefetches do
-      // not slow the consumers' release fences -- then wait until the
-      // consumers have finished every earlier instruction of this launch
-      if (lane == 0) {
-        unsigned long long left = g.hold_prefetch;
-        for (int k = 0; k < nseg && left; k++)
-          for (uint32_t u0 = 0; u0 < s[k].n && left; u0 += s[k].ups) {
-            const uint32_t b = min(s[k].ups, s[k].n - u0) * s[k].unit;
-            bulk_prefetch_l2(s[k].src + (size_t)u0 * s[k].unit, b);
-            if (s[k].src2) bulk_prefetch_l2(s[k].src2 + (size_t)u0 * s[k].unit, b);
-            left = left > b ? left - b : 0;
-          }
-      }
-      int bad = 0;
-      if (lane == 0) {
-        const uint64_t t0 = gtimer();
-        for (uint32_t it = 1; *(volatile int*)done < my_seq; it++) {
-          if ((it & 63) == 0) {
-            if (peek_err(g)) { bad = 1; break; }
-            if (gtimer() - t0 > g.timeout_ns) {
-              set_err(g, MK_ERR_TIMEOUT, pc, I.op);
-              bad = 1;
-              break;
-            }
-          }
-        }
-      }
-      if (__shfl_sync(0xFFFFFFFFu, bad, 0)) goto drain;
-    }
+    // a held instruction: stages from hold_k on wait until the consumers
+    // have finished (and signalled) every earlier instruction of this launch
+    const uint32_t hold_k =
+        (I.flags & F_HOLD) ? (uint32_t)(g.hold_early / (unsigned)g.stage_bytes) : 0xFFFFFFFFu;
+    auto held_back = [&]() { return *(volatile const int*)done < my_seq; };
+    uint32_t nst_i = 0;  // stages of this instruction issued so far
     if (I.op == OP_MLP_DOWN && g.bsplit) {
       // Each stage's weight unit is copied as soon as the stage is free; its
       // h fragments, written by other SMs' gate/up slices, follow once the
@@ -1714,7 +1692,8 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
       };
       for (uint32_t it = 1; hi < nst; it++) {
         bool moved = false;
-        if (wi < nst && wi < hi + (uint32_t)ns) {
+        const bool wfree = wi < hold_k || !__shfl_sync(0xFFFFFFFFu, held_back(), 0);
+        if (wi < nst && wi < hi + (uint32_t)ns && wfree) {
           uint32_t stg, p;
           stage_of(wi, stg, p);
           if (__shfl_sync(0xFFFFFFFFu, mbar_try(empty0 + 8u * stg, p ^ 1u), 0)) {
@@ -1772,6 +1751,26 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
     for (int k = 0; k < nseg; k++) {
       for (uint32_t u0 = 0; u0 < s[k].n; u0 += s[k].ups) {
         const uint32_t n = min(s[k].ups, s[k].n - u0);
+        if (nst_i++ == hold_k) {
+          int bad = 0;
+          if (lane == 0) {
+            const uint64_t t0 = gtimer();
+            for (uint32_t it = 1; held_back(); it++) {
+              if ((it & 63) == 0) {
+                if (peek_err(g)) {
+                  bad = 1;
+                  break;
+                }
+                if (gtimer() - t0 > g.timeout_ns) {
+                  set_err(g, MK_ERR_TIMEOUT, pc, I.op);
+                  bad = 1;
+                  break;
+                }
+              }
+            }
+          }
+          if (__shfl_sync(0xFFFFFFFFu, bad, 0)) goto drain;
+        }
         // wait for a free stage; while the ring is full, warm L2 ahead
         const uint32_t empty = empty0 + 8u * st;
         if (!__shfl_sync(0xFFFFFFFFu, mbar_try(empty, par ^ 1u), 0)) {

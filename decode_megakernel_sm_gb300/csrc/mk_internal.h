@@ -43,8 +43,8 @@ enum Flag : uint8_t {
   F_RESIDUAL = 1,    // this instruction also adds the residual input for its rows
   F_NORM_CACHED = 2, // the normalised input left in shared memory is still valid
   F_SHARED = 4,      // MoE MLP: shared-expert columns (weight 1, no routing)
-  F_HOLD = 8,        // producer: warm L2 with this instruction's data, then issue its ring
-                     // copies only after the consumers released every earlier instruction
+  F_HOLD = 8,        // producer: issue at most hold_early bytes of this instruction's ring
+                     // copies before the consumers have finished every earlier instruction
   F_TAG_WAIT = 16,   // inputs arrive as tagged words: poll them, not the wait counter
                      // (which still models the dependency for the schedule checker)
   F_RELAXED_SIG = 32,// every consumer polls tagged outputs: signal with a relaxed reduction,
@@ -52,16 +52,19 @@ enum Flag : uint8_t {
 };
 
 // Which instructions the planner marks F_HOLD (first of a run of the op on
-// an SM).  A release fence drains the SM's bulk copies in flight, so an
-// instruction whose predecessor ends with a fence on the critical path does
-// better to fetch through L2 after that fence than to have its copies in
-// flight during it.
+// an SM).  A release fence waits for every memory operation the SM has in
+// flight -- bulk copies and L2 prefetches included -- so the next
+// instruction's copies issued in the last microseconds before a fence sit
+// on the critical path.  A held instruction gets its first hold_early bytes
+// of copies early (they land before the fence) and the rest right after the
+// previous instruction's signal, while the dependency hop runs.
 enum HoldBit : unsigned {
   HOLD_QKV = 1, HOLD_ATTN = 2, HOLD_OPROJ = 4, HOLD_MLP = 8, HOLD_DOWN = 16, HOLD_LM = 32,
 };
-// Default: none.  The down rows' signal is relaxed (tagged outputs), and the
-// remaining fences cost less than the prefetch a hold would give up.
-constexpr unsigned DEFAULT_HOLD = 0;
+// Default: the gate/up and down instructions, whose predecessors (O-proj and
+// gate/up) end with the fences that have the most copies in flight behind them.
+constexpr unsigned DEFAULT_HOLD = HOLD_MLP | HOLD_DOWN;
+constexpr unsigned DEFAULT_HOLD_EARLY = 128u << 10;
 
 constexpr uint32_t NO_CTR = 0xFFFFFFFFu;
 
@@ -200,7 +203,8 @@ struct Globals {
   int pdl;                 // ablation with programmatic dependent launch
   unsigned long long* trace;  // optional [n_sm][max_pc][8] %globaltimer stamps (NULL: off)
   unsigned long long l2_ahead;  // bytes of the SM's stream warmed in L2 ahead of the ring (0: off)
-  unsigned hold_prefetch;       // bytes of a held instruction warmed in L2 before its copies
+  unsigned hold_early;          // bytes of a held instruction's copies issued before the
+                                // consumers finish the previous instruction (whole stages)
 };
 
 // Shared-memory layout (bytes from the dynamic shared memory base).

@@ -91,9 +91,9 @@ class Decoder:
         """Ring stage size (16, 32, 48 or 64 KiB); takes effect at the next step."""
         L.mk_set_stage_bytes(self.h, stage_bytes)
 
-    def set_hold_policy(self, mask: int, prefetch_bytes: int = 256 << 10):
+    def set_hold_policy(self, mask: int, early_bytes: int = 128 << 10):
         """Takes effect at the next build_schedule."""
-        L.mk_set_hold_policy(self.h, mask, prefetch_bytes)
+        L.mk_set_hold_policy(self.h, mask, early_bytes)
 
     def set_l2_prefetch(self, bytes_ahead: int):
         L.mk_set_l2_prefetch(self.h, bytes_ahead)

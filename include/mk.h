@@ -207,18 +207,19 @@ int mk_set_stage_bytes(mk_handle* h, int stage_bytes);
  * the next mk_build_schedule.  Results agree to float rounding.            */
 int mk_set_residual_copies(mk_handle* h, int copies);
 
-/* Fetch policy at instruction boundaries.  A release fence waits for the
- * SM's bulk copies still in flight, so when an SM streams the next
- * instruction's data during the fence that ends the current one, the fence
- * (and every SM waiting on it) is slowed.  Instructions of the ops in `mask`
- * (bits: 1 QKV, 2 attention, 4 O-projection, 8 MLP gate/up or fused MLP or
- * router, 16 MLP down rows, 32 LM head) that follow another op on their SM
- * are "held": the producer first warms L2 with up to `prefetch_bytes` of the
- * instruction's data (L2 prefetches do not slow fences), then issues the
- * ring copies only after the consumers have finished every earlier
- * instruction.  Default mask 0 (nothing held), 256 KiB.  Takes
- * effect at the next mk_build_schedule.  Results do not depend on it.     */
-int mk_set_hold_policy(mk_handle* h, unsigned mask, uint64_t prefetch_bytes);
+/* Fetch policy at instruction boundaries.  A release fence waits for every
+ * memory operation the SM has in flight (bulk copies and L2 prefetches
+ * included), so ring copies of the next instruction issued just before the
+ * fence that ends the current one slow that fence, and every SM waiting on
+ * it.  Instructions of the ops in `mask` (bits: 1 QKV, 2 attention,
+ * 4 O-projection, 8 MLP gate/up or fused MLP or router, 16 MLP down rows,
+ * 32 LM head) that follow another op on their SM are "held": the producer
+ * issues their first `early_bytes` of ring copies (whole stages; 0: none) as
+ * usual and the rest only after the consumers have finished, and signalled,
+ * every earlier instruction.  Default mask 24 (gate/up and down), 128 KiB.
+ * Takes effect at the next mk_build_schedule.  Results do not depend on it.
+ * MK_ERR_INVALID_ARG for mask > 63 or early_bytes > 64 MiB.               */
+int mk_set_hold_policy(mk_handle* h, unsigned mask, uint64_t early_bytes);
 
 typedef struct {
   int n_sm;               /* CTAs of the persistent kernel (= SMs)          */

@@ -27,7 +27,7 @@ ROUTE_TIE = 1e-4
 
 class Run:
     def __init__(self, cfg: dict, seed: int = 0, max_ctx: int | None = None,
-                 stage_bytes: int | None = None):
+                 stage_bytes: int | None = None, hold: tuple | None = None):
         cfg = cfg if "max_seq" in cfg else synth.with_cache(cfg)
         self.cfg = cfg
         self.W = synth.make_weights(cfg, seed, "cuda")
@@ -40,6 +40,8 @@ class Run:
         self.dec = Decoder(cfg, self.W, self.ks, self.vs)
         if stage_bytes is not None:
             self.dec.set_stage_bytes(stage_bytes)
+        if hold is not None:
+            self.dec.set_hold_policy(*hold)
         self.B = cfg["batch"]
         self.max_ctx = max_ctx or cfg["max_seq"]
         self.dec.build_schedule(self.B, self.max_ctx)

@@ -40,6 +40,20 @@ def test_ring_stage_sizes(sb):
     run_steps(cfg, 3, seed=9, stage_bytes=sb)
 
 
+@pytest.mark.parametrize("mask,early", [(63, 0), (63, 16384), (24, 1 << 20)])
+def test_hold_policies(mask, early):
+    # every op held with no early stage or with one, and the default ops
+    # with every stage early: the producer's extra waits change no result
+    cfg = synth.custom(n_layers=3, n_q_heads=6, n_kv_heads=3, ffn=1000, vocab=999,
+                       prefill=(300, 300), steps=3)
+    run_steps(cfg, 3, seed=11, hold=(mask, early))
+
+
+def test_batched_split_mlp_held():
+    # the batched down units gate their weight halves on the hold as well
+    run_steps(_bsplit_cfg(8), 3, seed=23, hold=(63, 0))
+
+
 def test_llama1b_large_stages():
     r = Run(synth.CONFIGS["llama1b_1k"], seed=3, stage_bytes=65536)
     try:
@@ -116,13 +130,21 @@ def test_llama1b_8k_parity():
     run_steps(synth.CONFIGS["llama1b_8k"], 2, seed=1)
 
 
-def test_moe_small_parity():
+def _moe_small_cfg():
     # MoE variant (hidden 2048, head_dim 128, 4 q heads per kv head) at a reduced
     # size: 16 experts, top-4, shared expert, ragged FFN widths
-    cfg = synth.custom(n_layers=3, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn=0,
-                       vocab=3001, tied=False, n_experts=16, top_k=4, expert_ffn=200,
-                       shared_ffn=500, rope_theta=5e5, prefill=(70, 70), steps=4)
-    run_steps(cfg, 4, seed=21)
+    return synth.custom(n_layers=3, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn=0,
+                        vocab=3001, tied=False, n_experts=16, top_k=4, expert_ffn=200,
+                        shared_ffn=500, rope_theta=5e5, prefill=(70, 70), steps=4)
+
+
+def test_moe_small_parity():
+    run_steps(_moe_small_cfg(), 4, seed=21)
+
+
+def test_moe_small_held():
+    # routers, shared and routed slices all held, no early stage
+    run_steps(_moe_small_cfg(), 3, seed=22, hold=(63, 0))
 
 
 def test_moe_full_config_parity():

@@ -232,3 +232,16 @@ def test_batched_split_mlp_cuts_whole_tiles():
     assert all(I.r0 % 16 == 0 and I.r1 - I.r0 == 16 for I in down)
     assert sorted(I.r0 for I in down if I.layer == 0) == list(range(0, cfg["hidden"], 16))
     assert not any(I.flags & (16 | 32) for I in ops)  # no tagged hops at batch > 1
+
+
+def test_default_hold_marks_gate_up_and_down():
+    # the default fetch policy holds the first gate/up and the first down
+    # instruction of each layer on every SM, and nothing else
+    cfg, d = desc("llama1b_1k")
+    st, q = L.mk_plan(d, 1, cfg["max_seq"], 152)
+    mp = st["max_pc"]
+    for sm in range(152):
+        run = [q[sm * mp + k] for k in range(mp) if q[sm * mp + k].op != 0]
+        for k, I in enumerate(run):
+            first = k > 0 and (run[k - 1].op != I.op or run[k - 1].layer != I.layer)
+            assert bool(I.flags & 8) == (first and I.op in (8, 9)), (sm, k, I.op)
