@@ -348,7 +348,8 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "batch": B, "prefill": list(cfg["prefill"]),
                    "decode_window": window, "parallelism": f"replicas x{ws}",
-                   "l2": "inputs larger than L2 (2.47 GB of weights streamed per step)"},
+                   "l2": "inputs larger than L2 (%.2f GB of weights streamed per step)"
+                         % (info["weight_bytes_per_step"] / 1e9)},
         "gpu_launches": args.steps, "roofline": roof, "clocks": ck,
         "kernel": {"n_sm": info["n_sm"], "ring_stages": info["n_stages"],
                    "stage_bytes": info["stage_bytes"], "instructions": info["n_instr"],

@@ -14,7 +14,10 @@
 //                              so 8 consecutive rows read chunk c from 8
 //                              different shared-memory bank groups
 //   gate/up [F][2][H]          gate row c, then up row c
-//   down  [F][H]               transposed: one contiguous row per FFN column
+//   down  dense batch 1: [H][F] as given (one contiguous row per output row);
+//         2..8 sequences, F a multiple of 512: units of 16 rows x 512 columns,
+//         16-byte chunk q of unit row i at slot q ^ (i & 7);
+//         otherwise [F][H], transposed (one contiguous row per FFN column)
 #include <cuda_runtime.h>
 
 #include "mk_internal.h"
