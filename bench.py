@@ -5,8 +5,11 @@ hidden 2048, 32 query / 8 kv heads of 64, SwiGLU FFN 8192, vocab 128256, tied
 LM head, bf16 weights ~N(0, 0.02) from a seed, bf16 KV cache prefilled with
 1024 positions -- decoding greedily: step t feeds the previous step's argmax
 device-to-device and writes cache row 1024 + (t mod 128), so the timed steps
-cycle over the 128-step decode window of the workload.  A step is one launch
-of the persistent kernel over the whole forward pass.
+cycle over the 128-step decode window of the workload.  A step is one pass
+of the persistent kernel over the whole forward pass; by default one launch
+runs 16 such steps back to back (mk_decode_steps: each step decodes the
+previous step's argmax on the device), --multi-step 0 launches once per step.
+The end-to-end figure goes through the host-buffer call, one step per call.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
   python bench.py --impl reference ...   (the CPU oracle on the host cores)
@@ -43,6 +46,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ablation", action="store_true", help="also time the per-phase launches")
+    ap.add_argument("--multi-step", type=int, default=None,
+                    help="greedy steps per launch (mk_decode_steps); 0: one launch per step; "
+                         "default 16 when it divides the decode window and --steps")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--l2-ahead", type=int, default=None,
                     help="bytes each SM warms in L2 ahead of its ring (library default if unset)")
@@ -50,6 +56,11 @@ def parse():
                     help="partial copies of each residual vector (library default if unset)")
     ap.add_argument("--hold", type=int, default=None,
                     help="hold-policy mask (library default if unset)")
+    ap.add_argument("--pollers", type=int, default=None,
+                    help="warps polling each dependency counter (library default if unset)")
+    ap.add_argument("--poll-stagger", type=int, default=0, help="ns between pollers (with --pollers)")
+    ap.add_argument("--ring-depth", type=int, default=None,
+                    help="at most this many ring stages (library default if unset)")
     ap.add_argument("--hold-early", type=int, default=128 << 10,
                     help="bytes of a held instruction's copies issued early (with --hold)")
     ap.add_argument("--stage-bytes", type=int, default=None,
@@ -105,13 +116,13 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
-def traffic_record(config):
+def traffic_record(config, steps_per_launch=1):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources."""
+    the current kernel sources with this many steps per launch."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         j = json.load(open(p))
-        e = j.get(config)
+        e = j.get(config if steps_per_launch == 1 else f"{config}@{steps_per_launch}")
         if e and e.get("kernel_src_sha") == kernel_src_hash():
             return float(e["dram_bytes_per_launch"])
     except Exception:
@@ -272,6 +283,10 @@ def main():
     torch.cuda.empty_cache()
     if args.kc is not None:
         dec.set_residual_copies(args.kc)
+    if args.pollers is not None:
+        dec.set_poll_policy(args.pollers, args.poll_stagger)
+    if args.ring_depth is not None:
+        dec.set_ring_depth(args.ring_depth)
     if args.hold is not None:
         dec.set_hold_policy(args.hold, args.hold_early)
     if args.stage_bytes is not None:
@@ -288,7 +303,21 @@ def main():
     am = [torch.empty(B, dtype=torch.int32, device=dev) for _ in range(2)]
     logits = torch.empty((B, V), dtype=torch.float32, device=dev)
 
+    ns = args.multi_step
+    if ns is None:
+        ns = 16 if window % 16 == 0 and args.steps % 16 == 0 else 0
+    if ns:
+        if ns < 1 or window % ns or args.steps % ns:
+            raise SystemExit(f"--multi-step {ns} must divide the decode window ({window}) "
+                             f"and --steps ({args.steps})")
+        am_ms = [torch.empty((ns, B), dtype=torch.int32, device=dev) for _ in range(2)]
+
     def run(n, fn=None):
+        if ns and fn is None:  # launches of ns steps, each fed the last argmax of the one before
+            for k in range((n + ns - 1) // ns):
+                tok = tok0 if k == 0 else am_ms[(k - 1) % 2][ns - 1]
+                dec.steps(tok, pos_table[(k * ns) % window], ns, logits, am_ms[k % 2], stream)
+            return
         for t in range(n):
             tok = tok0 if t == 0 else am[(t - 1) % 2]
             if fn is None:
@@ -337,10 +366,12 @@ def main():
     alg = sum(per_step) / len(per_step)
     peak, peak_kind = measured_peak()
     achieved = alg / (ms / args.steps / 1e3) / 1e9
+    spl = ns if ns else 1  # steps per launch
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": traffic_record(args.config),
-            "peak_source": peak_kind, "algorithmic_bytes_per_launch": alg,
-            "kernel": "mk::mk_decode_kernel (persistent, 1 launch per step)"}
+            "frac": achieved / peak,
+            "traffic": traffic_record(args.config, spl),
+            "peak_source": peak_kind, "algorithmic_bytes_per_launch": alg * spl,
+            "kernel": "mk::mk_decode_kernel (persistent, %d step(s) per launch)" % spl}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws, "steps": args.steps,
@@ -350,7 +381,7 @@ def main():
                    "decode_window": window, "parallelism": f"replicas x{ws}",
                    "l2": "inputs larger than L2 (%.2f GB of weights streamed per step)"
                          % (info["weight_bytes_per_step"] / 1e9)},
-        "gpu_launches": args.steps, "roofline": roof, "clocks": ck,
+        "gpu_launches": args.steps // ns if ns else args.steps, "roofline": roof, "clocks": ck,
         "kernel": {"n_sm": info["n_sm"], "ring_stages": info["n_stages"],
                    "stage_bytes": info["stage_bytes"], "instructions": info["n_instr"],
                    "attn_splits": info["attn_splits"]},

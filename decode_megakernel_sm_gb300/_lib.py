@@ -82,6 +82,8 @@ SIGNATURES = {
                             C.POINTER(C.c_void_p)]),
     "mk_build_schedule": (C.c_int, [C.c_void_p, C.c_int, C.c_int]),
     "mk_decode_step": (C.c_int, [C.c_void_p] * 6),
+    "mk_decode_steps": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
+                                  C.c_void_p, C.c_void_p]),
     "mk_decode_step_host": (C.c_int, [C.c_void_p] * 5),
     "mk_decode_step_ablation": (C.c_int, [C.c_void_p, C.c_int] + [C.c_void_p] * 5),
     "mk_decode_step_noalloc": (C.c_int, [C.c_void_p] * 7),
@@ -94,6 +96,8 @@ SIGNATURES = {
     "mk_set_l2_prefetch": (C.c_int, [C.c_void_p, C.c_uint64]),
     "mk_set_residual_copies": (C.c_int, [C.c_void_p, C.c_int]),
     "mk_set_stage_bytes": (C.c_int, [C.c_void_p, C.c_int]),
+    "mk_set_ring_depth": (C.c_int, [C.c_void_p, C.c_int]),
+    "mk_set_poll_policy": (C.c_int, [C.c_void_p, C.c_int, C.c_uint]),
     "mk_set_hold_policy": (C.c_int, [C.c_void_p, C.c_uint, C.c_uint64]),
     "mk_get_trace": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.c_size_t]),
     "mk_destroy": (C.c_int, [C.c_void_p]),
@@ -152,6 +156,11 @@ def mk_decode_step(h, d_tokens, d_positions, d_logits, d_argmax, stream=None):
            "mk_decode_step")
 
 
+def mk_decode_steps(h, d_tokens, d_positions, n_steps: int, d_logits, d_argmax, stream=None):
+    _check(lib().mk_decode_steps(h, d_tokens, d_positions, int(n_steps), d_logits, d_argmax,
+                                 stream), "mk_decode_steps")
+
+
 def mk_decode_step_host(h, h_tokens, h_positions, h_logits, h_argmax) -> int:
     """Host-buffer step; returns the status (device errors are statuses, not raises)."""
     return lib().mk_decode_step_host(h, h_tokens, h_positions, h_logits, h_argmax)
@@ -203,6 +212,14 @@ def mk_set_l2_prefetch(h, bytes_ahead: int):
 
 def mk_set_residual_copies(h, copies: int):
     _check(lib().mk_set_residual_copies(h, int(copies)), "mk_set_residual_copies")
+
+
+def mk_set_poll_policy(h, pollers: int, stagger_ns: int):
+    _check(lib().mk_set_poll_policy(h, int(pollers), int(stagger_ns)), "mk_set_poll_policy")
+
+
+def mk_set_ring_depth(h, max_stages: int):
+    _check(lib().mk_set_ring_depth(h, int(max_stages)), "mk_set_ring_depth")
 
 
 def mk_set_stage_bytes(h, stage_bytes: int):

@@ -92,6 +92,7 @@ struct mk_handle {
   const Variant* var = nullptr;
   int n_stages = 0, smem_bytes = 0;
   int stage_bytes = DEFAULT_STAGE_BYTES;
+  int max_stages = 0;  // 0: as many as fit
   void* packed = nullptr;
   size_t packed_bytes = 0;
   std::vector<LayerPtrs> layers_h;
@@ -108,6 +109,8 @@ struct mk_handle {
   std::vector<int> abl_keys;  // ablation launches (keys that own instructions)
   uint32_t epoch = 0;
   unsigned long long timeout_ns = 2000000000ull;
+  int n_pollers = 1;
+  unsigned poll_stagger_ns = 0;
   unsigned long long l2_ahead = 0;
   int kc = 1;  // partial copies of each residual vector
   unsigned hold_mask = DEFAULT_HOLD;
@@ -210,7 +213,8 @@ static int size_ring(mk_handle* h, int stage_bytes) {
   int optin = 0;
   CK(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->dev));
   int ns = 0;
-  for (int n = 2; n <= MAX_STAGES; n++)
+  const int cap = h->max_stages > 0 ? h->max_stages : MAX_STAGES;
+  for (int n = 2; n <= cap; n++)
     if (smem_layout(n, stage_bytes, h->var->NB, d.hidden, d.head_dim, HPG, K).total <= optin)
       ns = n;
   if (ns < 2) return MK_ERR_UNSUPPORTED;
@@ -457,6 +461,8 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.logits = logits;
   g.argmax = am;
   g.timeout_ns = h->timeout_ns;
+  g.n_pollers = h->n_pollers;
+  g.poll_stagger_ns = h->poll_stagger_ns;
   g.max_pc = h->plan.max_pc;
   g.n_sm = h->n_sm;
   g.n_stages = h->n_stages;
@@ -481,6 +487,8 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.bsplit = mlp_split_batched(d) ? 1 : 0;
   g.eps = d.rms_eps;
   g.lm_ctr = CtrMap{d.n_kv_heads, d.n_layers}.lm();
+  g.lm_done_ctr = CtrMap{d.n_kv_heads, d.n_layers}.lm_done();
+  g.n_steps = 1;
   g.n_lm = h->plan.n_lm;
   g.sel_key = -1;
   g.trace = h->trace;
@@ -502,7 +510,20 @@ extern "C" int mk_decode_step(mk_handle* h, const int32_t* d_tokens, const int32
   if (!d_tokens || !d_positions || !d_logits || !d_argmax) return MK_ERR_INVALID_ARG;
   Globals g = make_globals(h, d_tokens, d_positions, d_logits, d_argmax);
   g.epoch = ++h->epoch;
-  g.parity = (int)(g.epoch & 1u);
+  g.zero_next = 1;
+  CK(launch_mega(h, g, (cudaStream_t)stream));
+  return MK_OK;
+}
+
+extern "C" int mk_decode_steps(mk_handle* h, const int32_t* d_tokens, const int32_t* d_positions,
+                               int n_steps, float* d_logits, int32_t* d_argmax, void* stream) {
+  if (!h) return MK_ERR_INVALID_ARG;
+  if (!h->sched) return MK_ERR_NOT_READY;
+  if (!d_tokens || !d_positions || !d_logits || !d_argmax || n_steps < 1) return MK_ERR_INVALID_ARG;
+  Globals g = make_globals(h, d_tokens, d_positions, d_logits, d_argmax);
+  g.epoch = h->epoch + 1;
+  h->epoch += (uint32_t)n_steps;
+  g.n_steps = n_steps;
   g.zero_next = 1;
   CK(launch_mega(h, g, (cudaStream_t)stream));
   return MK_OK;
@@ -533,7 +554,6 @@ extern "C" int mk_decode_step_host(mk_handle* h, const int32_t* h_tokens,
   CK(cudaMemcpyAsync(h->d_pos, h_positions, B * 4, cudaMemcpyHostToDevice, s));
   Globals g = make_globals(h, h->d_tok, h->d_pos, h->d_logits, h->d_am);
   g.epoch = ++h->epoch;
-  g.parity = (int)(g.epoch & 1u);
   g.zero_next = 1;
   CK(launch_mega(h, g, s));
   if (h_logits)
@@ -554,7 +574,6 @@ extern "C" int mk_decode_step_host(mk_handle* h, const int32_t* h_tokens,
 static cudaError_t launch_phases(mk_handle* h, Globals g, cudaStream_t s, bool pdl) {
   for (size_t i = 0; i < h->abl_keys.size(); i++) {
     g.sel_key = h->abl_keys[i];
-    g.zero_next = g.zero_next && i == 0;
     g.pdl = pdl ? 1 : 0;
     void* args[] = {&g};
     cudaError_t e;
@@ -591,7 +610,6 @@ extern "C" int mk_decode_step_ablation(mk_handle* h, int mode, const int32_t* d_
   Globals g = make_globals(h, d_tokens, d_positions, d_logits, d_argmax);
   if (mode != MK_ABL_GRAPH) {
     g.epoch = ++h->epoch;
-    g.parity = (int)(g.epoch & 1u);
     g.zero_next = 1;
     CK(launch_phases(h, g, s, mode == MK_ABL_PDL));
     return MK_OK;
@@ -604,7 +622,6 @@ extern "C" int mk_decode_step_ablation(mk_handle* h, int mode, const int32_t* d_
   if (it == h->graphs.end()) {
     CK(cudaStreamSynchronize(h->own));
     g.epoch = 1;
-    g.parity = 1;
     g.zero_next = 0;
     cudaGraph_t graph = nullptr;
     CK(cudaStreamBeginCapture(h->own, cudaStreamCaptureModeThreadLocal));
@@ -721,7 +738,6 @@ extern "C" int mk_decode_step_noalloc(mk_handle* h, const int32_t* d_tokens,
   CK(cudaMemsetAsync(g.ctr, 0, sc.ctr_bytes + 256, s));
   CK(cudaMemsetAsync(g.xt, 0, sc.tag_bytes, s));
   g.epoch = 1;
-  g.parity = 1;
   g.zero_next = 0;
   g.trace = nullptr;
   CK(launch_mega(h, g, s));
@@ -733,6 +749,30 @@ extern "C" int mk_set_hold_policy(mk_handle* h, unsigned mask, uint64_t early_by
   if (!h || mask > 63u || early_bytes > (64ull << 20)) return MK_ERR_INVALID_ARG;
   h->hold_mask = mask;
   h->hold_early = (unsigned)early_bytes;
+  return MK_OK;
+}
+
+extern "C" int mk_set_poll_policy(mk_handle* h, int pollers, unsigned stagger_ns) {
+  if (!h || pollers < 1 || pollers > NCW || stagger_ns > 100000u) return MK_ERR_INVALID_ARG;
+  h->n_pollers = pollers;
+  h->poll_stagger_ns = stagger_ns;
+  for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
+  h->graphs.clear();
+  return MK_OK;
+}
+
+extern "C" int mk_set_ring_depth(mk_handle* h, int max_stages) {
+  if (!h || max_stages < 0 || max_stages == 1 || max_stages > MAX_STAGES) return MK_ERR_INVALID_ARG;
+  const int old = h->max_stages;
+  h->max_stages = max_stages;
+  const int st = size_ring(h, h->stage_bytes);
+  if (st != MK_OK) {
+    h->max_stages = old;
+    size_ring(h, h->stage_bytes);
+    return st;
+  }
+  for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
+  h->graphs.clear();
   return MK_OK;
 }
 

@@ -32,11 +32,14 @@ struct Ctx {
   int* pos;     // [NB]
   int* topk;    // [NB][K] routed expert ids
   float* topw;  // [NB][K] routed expert weights
-  int* flag;    // [0] abort flag of the dependency wait, [2] a tagged-input poll failed
+  int* flag;    // [0] bad launch input, [2] a tagged-input poll failed, [3] / [4] key of
+                // the instruction whose counter was seen / whose wait failed
                 // (both shared by the consumer warps; [1] belongs to the producer)
   Ring ring;
   int tid, warp, lane;
   int pc;
+  int step;         // step of this launch (0 .. n_steps - 1)
+  uint32_t epoch;   // g.epoch + step: counter targets, tags, residual parity
   unsigned long long tw0, tw1;  // trace: wait start / end (thread 0)
   unsigned long long tm[2];     // trace: after the prologue phase, after the ring loop
   MK_DEV void mark(const Globals& g, int k) {
@@ -49,39 +52,45 @@ struct Ctx {
 // calls it exactly once, after issuing its dependency-free loads.
 template <int HT, int D, int HPG, int NB>
 MK_DEV bool dep_wait(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+  // the first lanes of n_pollers warps poll the counter, staggered (flag[3]:
+  // key of the instruction whose counter was seen; flag[4]: key of a failed
+  // wait).  A met counter means complete inputs; errors elsewhere in the
+  // grid surface in this and the later bounded waits (no extra L2 round
+  // trip).  F_TAG_WAIT: the op polls its tagged inputs itself.
+  const int key = c.pc + 1;
+  if (c.tid == 0 && g.trace) c.tw0 = gtimer();
+  if (!(I.flags & F_TAG_WAIT) && I.wait_ctr != NO_CTR && c.lane == 0 && c.warp < g.n_pollers) {
+    if (!poll_counter_shared(g, I.wait_ctr, c.epoch * I.wait_cnt,
+                             (uint64_t)c.warp * g.poll_stagger_ns, c.flag + 3, key, c.pc, I.op))
+      ((volatile int*)c.flag)[4] = key;
+  }
   if (c.tid == 0) {
-    if (g.trace) c.tw0 = gtimer();
-    bool ok = true;
-    // a met counter means complete inputs; errors elsewhere in the grid
-    // surface in this and the later bounded waits (no extra L2 round trip)
-    if (!(I.flags & F_TAG_WAIT)) {
-      if (I.wait_ctr != NO_CTR) ok = wait_counter(g, I.wait_ctr, g.epoch * I.wait_cnt, c.pc, I.op);
-    }  // F_TAG_WAIT: the op polls its tagged inputs itself
-    *c.flag = ok ? 0 : 1;
     c.flag[2] = 0;
     if (g.trace) c.tw1 = gtimer();
   }
   consumer_bar();
-  return *c.flag == 0;
+  return ((volatile int*)c.flag)[4] != key;
 }
 
 // Residual stream x_j, j in [1, 2L] (x_0 is the embedding row), held as
 // g.kc partial copies that add up to x_j: an SM accumulates its atomics into
 // copy (SM index mod kc), which spreads the contention on each L2 line over
 // kc lines; readers sum the copies.
-MK_DEV float* xres(const Globals& g, int j, int b, int copy = 0) {
+// The buffers alternate with the step's parity (epoch & 1): a step zeroes
+// the other parity's copies for the next one.
+MK_DEV float* xres(const Globals& g, uint32_t ep, int j, int b, int copy = 0) {
   return g.xbuf +
-         ((((size_t)g.parity * 2 * g.L + (size_t)(j - 1)) * g.kc + copy) * g.B + b) * (size_t)g.H;
+         ((((size_t)(ep & 1u) * 2 * g.L + (size_t)(j - 1)) * g.kc + copy) * g.B + b) * (size_t)g.H;
 }
 
-MK_DEV float* xres_mine(const Globals& g, int j, int b) {
-  return xres(g, j, b, (int)(blockIdx.x % (unsigned)g.kc));
+MK_DEV float* xres_mine(const Globals& g, uint32_t ep, int j, int b) {
+  return xres(g, ep, j, b, (int)(blockIdx.x % (unsigned)g.kc));
 }
 
 // x_j[b][r], summed over the copies.
-MK_DEV float xres_sum(const Globals& g, int j, int b, int r) {
+MK_DEV float xres_sum(const Globals& g, uint32_t ep, int j, int b, int r) {
   float v = 0.f;
-  for (int c = 0; c < g.kc; c++) v += __ldcg(xres(g, j, b, c) + r);
+  for (int c = 0; c < g.kc; c++) v += __ldcg(xres(g, ep, j, b, c) + r);
   return v;
 }
 
@@ -217,7 +226,7 @@ MK_DEV bool norm_apply_batched(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j,
   for (int b = 0; b < NB; b++) {
     const bool live = b < g.B;
     tk[b] = live ? c.tok[b] : 0;
-    xb[b] = (!emb && live) ? xres(g, j, b, 0) : nullptr;
+    xb[b] = (!emb && live) ? xres(g, c.epoch, j, b, 0) : nullptr;
   }
 #pragma unroll
   for (int q0 = 0; q0 < KPT; q0 += CH) {
@@ -245,7 +254,7 @@ MK_DEV bool norm_apply_batched(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j,
           const int k = c.tid + (q0 + u) * NCT;
 #pragma unroll
           for (int b = 0; b < NB; b++)
-            if (q0 + u < KPT && k < HT && b < g.B) v[u][b] += __ldcg(xres(g, j, b, cp) + k);
+            if (q0 + u < KPT && k < HT && b < g.B) v[u][b] += __ldcg(xres(g, c.epoch, j, b, cp) + k);
         }
     }
 #pragma unroll
@@ -324,7 +333,7 @@ MK_DEV bool norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const No
       for (int q = 0; q < GPT; q++)
         if (c.tid + q * NCT < GROUPS) valid |= 1u << q;
       ok = poll_tag_groups_to<GPT, 4>(g, g.xt + (size_t)(j / 2 - 1) * HT + 8 * c.tid,
-                                      (size_t)NCT * 8, valid, g.epoch, c.xn + 8 * c.tid, NCT * 8,
+                                      (size_t)NCT * 8, valid, c.epoch, c.xn + 8 * c.tid, NCT * 8,
                                       c.pc, OP_QKV);
     }
   }
@@ -353,7 +362,7 @@ MK_DEV bool norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const No
           v[b][0] = a0.x; v[b][1] = a0.y; v[b][2] = a0.z; v[b][3] = a0.w;
           v[b][4] = a1.x; v[b][5] = a1.y; v[b][6] = a1.z; v[b][7] = a1.w;
         } else if (g.kc == 1) {
-          const float4* p = (const float4*)xres(g, j, b, 0) + 2 * gi;
+          const float4* p = (const float4*)xres(g, c.epoch, j, b, 0) + 2 * gi;
           const float4 a0 = __ldcg(p), a1 = __ldcg(p + 1);
           v[b][0] = a0.x; v[b][1] = a0.y; v[b][2] = a0.z; v[b][3] = a0.w;
           v[b][4] = a1.x; v[b][5] = a1.y; v[b][6] = a1.z; v[b][7] = a1.w;
@@ -361,7 +370,7 @@ MK_DEV bool norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const No
 #pragma unroll
           for (int k = 0; k < 8; k++) v[b][k] = 0.f;
           for (int cp = 0; cp < g.kc; cp++) {
-            const float4* p = (const float4*)xres(g, j, b, cp) + 2 * gi;
+            const float4* p = (const float4*)xres(g, c.epoch, j, b, cp) + 2 * gi;
             const float4 a0 = __ldcg(p), a1 = __ldcg(p + 1);
             v[b][0] += a0.x; v[b][1] += a0.y; v[b][2] += a0.z; v[b][3] += a0.w;
             v[b][4] += a1.x; v[b][5] += a1.y; v[b][6] += a1.z; v[b][7] += a1.w;
@@ -818,10 +827,10 @@ MK_DEV bool op_attn(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
 }
 
 // Residual input x_j[b][r] (j = 0: the embedding row of the token).
-MK_DEV float x_in(const Globals& g, int j, const int* tok, int b, int r) {
+MK_DEV float x_in(const Globals& g, uint32_t ep, int j, const int* tok, int b, int r) {
   if (j == 0)  // embedding rows are chunk-swizzled by token id
     return bf1(g.embed[(size_t)tok[b] * g.H + ((((r >> 3) ^ (tok[b] & 7)) << 3) | (r & 7))]);
-  return xres_sum(g, j, b, r);
+  return xres_sum(g, ep, j, b, r);
 }
 
 // --------------------------------- OP_OPROJ (split reduce + O-proj rows) ----
@@ -890,7 +899,7 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
         float v = 0.f;
         if (b < g.B) {
           const TagWord* p = g.xt + ((size_t)(l - 1) * g.B + b) * g.H + I.r0 + r;
-          if (!poll_tag1(g, p, g.epoch, v, c.pc, I.op)) okr = false;
+          if (!poll_tag1(g, p, c.epoch, v, c.pc, I.op)) okr = false;
         }
         xr_s[t] = v;
       }
@@ -901,7 +910,7 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
 #pragma unroll
         for (int u = 0; u < 8; u++) {
           const int t = t0 + u * NCT, b = t / nr, r = t % nr;
-          v[u] = t < NB * nr && b < g.B ? x_in(g, 2 * l, c.tok, b, (int)I.r0 + r) : 0.f;
+          v[u] = t < NB * nr && b < g.B ? x_in(g, c.epoch, 2 * l, c.tok, b, (int)I.r0 + r) : 0.f;
         }
 #pragma unroll
         for (int u = 0; u < 8; u++)
@@ -934,7 +943,7 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
         av[4 * k] = t.x; av[4 * k + 1] = t.y; av[4 * k + 2] = t.z; av[4 * k + 3] = t.w;
       }
     }
-    float* dst = xres_mine(g, 2 * l + 1, 0);
+    float* dst = xres_mine(g, c.epoch, 2 * l + 1, 0);
     uint32_t bc = 0;  // 32-row blocks of earlier stages (round-robin offset)
     for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
       const uint32_t n = min(s[0].ups, s[0].n - u0);
@@ -1023,7 +1032,7 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
             for (int b = 0; b < g.B && b < NB; b++) {
               float v = y[p][b];
               if (resid) v += xr_s[b * nr + (r - (int)I.r0)];
-              red_add_f32(xres_mine(g, 2 * l + 1, b) + r, v);
+              red_add_f32(xres_mine(g, c.epoch, 2 * l + 1, b) + r, v);
             }
           }
         }
@@ -1064,7 +1073,7 @@ MK_DEV bool op_router(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   if (c.tid == 0)
     *arrived = (int)atom_add_acq_rel(g.ctr + CtrMap{g.Hkv, g.L}.router_arrive(I.layer), 1u);
   consumer_bar();
-  if ((uint32_t)*arrived != g.epoch * I.aux - 1u) return true;
+  if ((uint32_t)*arrived != c.epoch * I.aux - 1u) return true;
   float* ys = c.yrow;               // [E <= 256] logits
   int* sel = (int*)(c.yrow + 256);  // [K <= 16] ids by rank
   float* sv = c.yrow + 256 + 16;    // [K] their logits
@@ -1186,9 +1195,9 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
 #pragma unroll
         for (int e = 0; e < 8; e++) {
           v[e] = acc[q][b][e];
-          if (r0 + e >= rs0 && r0 + e < rs1) v[e] += xres_sum(g, 2 * l + 1, b, r0 + e);
+          if (r0 + e >= rs0 && r0 + e < rs1) v[e] += xres_sum(g, c.epoch, 2 * l + 1, b, r0 + e);
         }
-        float* dst = xres_mine(g, 2 * l + 2, b) + r0;
+        float* dst = xres_mine(g, c.epoch, 2 * l + 2, b) + r0;
         red_add_v4f32(dst, v[0], v[1], v[2], v[3]);
         red_add_v4f32(dst + 4, v[4], v[5], v[6], v[7]);
       }
@@ -1285,7 +1294,7 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I
     float* res = c.yrow;  // [BD_ROWS][NB] residual rows x_{2l+1}
     for (int t = c.tid; t < BD_ROWS * NB; t += NCT) {
       const int r = t / NB, b = t % NB;
-      res[t] = b < g.B ? xres_sum(g, 2 * l + 1, b, (int)I.r0 + r) : 0.f;
+      res[t] = b < g.B ? xres_sum(g, c.epoch, 2 * l + 1, b, (int)I.r0 + r) : 0.f;
     }
     c.mark(g, 0);
     const int kt0 = c.warp * KT / NCW, kt1 = (c.warp + 1) * KT / NCW;
@@ -1334,7 +1343,7 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I
       float y = 0.f;
 #pragma unroll
       for (int w = 0; w < NCW; w++) y += part[(size_t)w * BD_ROWS * NB + t];
-      if (b < g.B) xres(g, 2 * l + 2, b, 0)[I.r0 + r] = res[t] + y;
+      if (b < g.B) xres(g, c.epoch, 2 * l + 2, b, 0)[I.r0 + r] = res[t] + y;
     }
     consumer_bar();
     return true;
@@ -1358,7 +1367,7 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I
         for (int e = 0; e < 8; e++) h[q][e] = 0.f;
       }
     }
-    const float res = c.tid < nrows ? xres_sum(g, 2 * l + 1, 0, (int)I.r0 + c.tid) : 0.f;
+    const float res = c.tid < nrows ? xres_sum(g, c.epoch, 2 * l + 1, 0, (int)I.r0 + c.tid) : 0.f;
     c.mark(g, 0);
     float* part = c.yrow;  // [NCW][MAX_DOWN_ROWS]
     const uint4 zero = make_uint4(0, 0, 0, 0);
@@ -1405,7 +1414,7 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I
       float y = 0.f;
 #pragma unroll
       for (int w = 0; w < NCW; w++) y += part[w * MAX_DOWN_ROWS + c.tid];
-      st_tag(g.xt + (size_t)l * g.B * g.H + I.r0 + c.tid, res + y, g.epoch);
+      st_tag(g.xt + (size_t)l * g.B * g.H + I.r0 + c.tid, res + y, c.epoch);
     }
     consumer_bar();
     return true;
@@ -1417,6 +1426,16 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I
 // arrives last on the argmax counter reduces all slices into argmax[b].
 template <int HT, int D, int HPG, int NB>
 MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+  if (g.zero_next) {
+    // this slice's share of the next step's residual buffers (the other
+    // parity): every step of this and earlier launches that read them is
+    // done, and the next step accumulates into them only after the argmax
+    // counter below, which waits for every LM head slice
+    const size_t total = (size_t)2 * g.L * g.kc * g.B * g.H;
+    const size_t a = total * I.aux / (size_t)g.n_lm, e = total * (I.aux + 1) / (size_t)g.n_lm;
+    float* nx = g.xbuf + (size_t)((c.epoch + 1u) & 1u) * total;
+    for (size_t i = a + c.tid; i < e; i += NCT) nx[i] = 0.f;
+  }
   NormGain<HT> ng;
   norm_gain(ng, g.final_norm, c.tid);
   if (!dep_wait(c, g, I)) return false;
@@ -1480,7 +1499,7 @@ MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   if (lane == 0) old = atom_add_acq_rel(g.ctr + g.lm_ctr, 1u);
   old = __shfl_sync(0xFFFFFFFFu, old, 0);
   __syncwarp();
-  if (old != g.epoch * (uint32_t)g.n_lm - 1u) return true;
+  if (old != c.epoch * (uint32_t)g.n_lm - 1u) return true;
   for (int b = 0; b < B && b < NB; b++) {
     float v = -INFINITY;
     int ix = 0x7FFFFFFF;
@@ -1501,8 +1520,12 @@ MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
         ix = oi;
       }
     }
-    if (lane == 0) g.argmax[b] = ix;
+    if (lane == 0) g.argmax[(size_t)c.step * B + b] = ix;
   }
+  // every SM is done with this step once its argmax is out: a multi-step
+  // launch starts the next step behind this signal
+  __syncwarp();
+  if (lane == 0) red_release(g.ctr + g.lm_done_ctr, 1u);
   return true;
 }
 
@@ -1622,9 +1645,20 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
   int seq = 0;  // instructions of this launch before the current one (consumer order)
   unsigned long long issued_bytes = 0;
   L2Cursor<HT, D, NB> l2;
-  for (int pc = 0; pc < g.max_pc; pc++) {
-    const Instr I = load_instr(g, blockIdx.x, pc);
-    if (I.op == OP_HALT) break;
+  int t = 0;               // step of this launch: the queue runs once per step
+  uint32_t ep = g.epoch;   // its epoch
+  bool step_ready = true;  // this step's copies may read rows written by earlier steps
+  for (int pc = 0;; pc++) {
+    Instr I;
+    if (pc < g.max_pc) I = load_instr(g, blockIdx.x, pc);
+    if (pc >= g.max_pc || I.op == OP_HALT) {
+      if (++t >= g.n_steps) break;
+      pc = -1;
+      ep = g.epoch + (uint32_t)t;
+      routed_layer = -1;
+      step_ready = false;
+      continue;
+    }
     if (I.op == OP_NOP || !selected(g, I)) continue;
     // every branch below is warp-uniform: lane 0 decides, the warp follows
     // (errors elsewhere in the grid are seen in the bounded waits below)
@@ -1633,8 +1667,20 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
       asm volatile("griddepcontrol.wait;" ::: "memory");
       grid_waited = true;
     }
+    if (I.op == OP_ATTN && !step_ready) {
+      // the cache rows that earlier steps of this launch appended come
+      // through the ring: wait until the previous step is done (its argmax
+      // is out), then order their generic stores before the bulk copies
+      bool ok = true;
+      if (lane == 0) {
+        ok = wait_counter(g, g.lm_done_ctr, ep - 1u, pc, I.op);
+        if (ok) asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) goto drain;
+      step_ready = true;
+    }
     if (I.op == OP_ATTN) {
-      const int P = __shfl_sync(0xFFFFFFFFu, __ldg(g.positions + I.b), 0);
+      const int P = __shfl_sync(0xFFFFFFFFu, __ldg(g.positions + I.b), 0) + t;
       if (P < 0 || P >= g.max_ctx) {
         if (lane == 0) set_err(g, MK_ERR_INVALID_ARG, pc, I.op);
         goto drain;
@@ -1643,7 +1689,7 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
     }
     if (routed && routed_layer != I.layer) {
       bool ok = true;
-      if (lane == 0) ok = wait_counter(g, I.wait_ctr, g.epoch * I.wait_cnt, pc, I.op);
+      if (lane == 0) ok = wait_counter(g, I.wait_ctr, ep * I.wait_cnt, pc, I.op);
       if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) goto drain;
       __syncwarp();
       if (lane < g.K) {  // the routing published by the layer's last router
@@ -1710,7 +1756,7 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
         if (!dep) {
           int ok = 0;
           if (lane == 0) {
-            ok = (int32_t)(ld_acquire(g.ctr + I.wait_ctr) - g.epoch * I.wait_cnt) >= 0;
+            ok = (int32_t)(ld_acquire(g.ctr + I.wait_ctr) - ep * I.wait_cnt) >= 0;
             // the fragments were written through the generic proxy
             if (ok) asm volatile("fence.proxy.async.global;" ::: "memory");
           }
@@ -1853,6 +1899,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *flag = 0;
     misc[1] = 0;  // instructions the consumers have finished (read by the producer)
+    misc[3] = misc[4] = 0;  // dependency-wait keys (never 0 once in use)
   }
   __syncthreads();
 
@@ -1864,25 +1911,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
 
   // ---- consumers
   if (g.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (tid < g.B && tid < NB) {
-    const int t = g.tokens[tid], p = g.positions[tid];
-    tok[tid] = t;
-    pos[tid] = p;
-    if (t < 0 || t >= g.V || p < 0 || p >= g.max_ctx) *flag = 1;
-  }
-  if (g.zero_next) {  // the residual buffers of the next step's parity
-    const size_t total = (size_t)2 * g.L * g.kc * g.B * g.H;
-    const size_t a = total * blockIdx.x / gridDim.x, e = total * (blockIdx.x + 1) / gridDim.x;
-    float* nx = g.xbuf + (size_t)(g.parity ^ 1) * total;
-    for (size_t i = a + tid; i < e; i += NCT) nx[i] = 0.f;
-  }
-  consumer_bar();
-  if (*flag) {
-    if (tid == 0) set_err(g, MK_ERR_INVALID_ARG, -1, -1);
-    return;
-  }
-  if (g.pdl && tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
   Ctx<HT, D, HPG, NB> c;
   c.xn = (float*)(smem + Ls.xn);
   c.yrow = (float*)(smem + Ls.yrow);
@@ -1902,53 +1930,78 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
   c.flag = flag;
   c.tw0 = c.tw1 = 0;
   c.tm[0] = c.tm[1] = 0;
-  consumer_bar();  // everyone has read *flag before it is reused below
 
   int finished = 0;
-  Instr next = load_instr(g, blockIdx.x, 0);
-  for (int pc = 0; pc < g.max_pc; pc++) {
-    const Instr I = next;
-    if (I.op == OP_HALT) break;
-    if (pc + 1 < g.max_pc) next = load_instr(g, blockIdx.x, pc + 1);
-    if (I.op == OP_NOP || !selected(g, I)) continue;
-    c.pc = pc;
-    bool ok;
-    switch (I.op) {
-      case OP_QKV: ok = op_qkv(c, g, I); break;
-      case OP_ATTN: ok = op_attn(c, g, I); break;
-      case OP_OPROJ: ok = op_oproj(c, g, I); break;
-      case OP_ROUTER: ok = op_router(c, g, I); break;
-      case OP_MLP: ok = op_mlp(c, g, I); break;
-      case OP_MLP_UP: ok = op_mlp_up(c, g, I); break;
-      case OP_MLP_DOWN: ok = op_mlp_down(c, g, I); break;
-      case OP_LMHEAD: ok = op_lmhead(c, g, I); break;
-      default:
-        if (tid == 0) set_err(g, MK_ERR_DEVICE, pc, I.op);
-        ok = false;
-        break;
+  for (int step = 0; step < g.n_steps; step++) {
+    c.step = step;
+    c.epoch = g.epoch + (uint32_t)step;
+    if (step > 0) {
+      // step t decodes step t - 1's argmax, once every SM is done with
+      // step t - 1 (its argmax is out)
+      if (tid == 0) *flag = wait_counter(g, g.lm_done_ctr, c.epoch - 1u, -1, OP_LMHEAD) ? 0 : 2;
+      consumer_bar();
+      if (*flag) return;  // the error word is set
     }
-    if (!ok) return;
-    if (tid == 0) {
-      if (g.trace) {
-        unsigned long long* t = g.trace + ((size_t)blockIdx.x * g.max_pc + pc) * 8;
-        t[1] = c.tw0;
-        t[2] = c.tw1;
-        t[3] = c.tm[0];
-        t[4] = c.tm[1];
-        t[5] = gtimer();
-        t[6] = c.ring.waited;  // warp 0's time blocked on ring data during this instruction
-        c.ring.waited = 0;
-      }
-      if (I.sig_ctr != NO_CTR && I.op != OP_ROUTER) {  // routers: the last arriver signals
-        if (I.flags & F_RELAXED_SIG)
-          red_relaxed(g.ctr + I.sig_ctr, 1u);
-        else
-          red_release(g.ctr + I.sig_ctr, 1u);
-      }
-      if (g.trace) g.trace[((size_t)blockIdx.x * g.max_pc + pc) * 8 + 7] = gtimer();
-      *(volatile int*)(misc + 1) = ++finished;
+    if (tid < g.B && tid < NB) {
+      const int t = step == 0 ? g.tokens[tid] : __ldcg(g.argmax + (size_t)(step - 1) * g.B + tid);
+      const int p = g.positions[tid] + step;
+      tok[tid] = t;
+      pos[tid] = p;
+      if (t < 0 || t >= g.V || p < 0 || p >= g.max_ctx) *flag = 1;
     }
-  }
+    consumer_bar();
+    if (*flag) {
+      if (tid == 0) set_err(g, MK_ERR_INVALID_ARG, -1, -1);
+      return;
+    }
+    if (step == 0 && g.pdl && tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    consumer_bar();  // everyone has read *flag before it is reused
+
+    Instr next = load_instr(g, blockIdx.x, 0);
+    for (int pc = 0; pc < g.max_pc; pc++) {
+      const Instr I = next;
+      if (I.op == OP_HALT) break;
+      if (pc + 1 < g.max_pc) next = load_instr(g, blockIdx.x, pc + 1);
+      if (I.op == OP_NOP || !selected(g, I)) continue;
+      c.pc = pc;
+      bool ok;
+      switch (I.op) {
+        case OP_QKV: ok = op_qkv(c, g, I); break;
+        case OP_ATTN: ok = op_attn(c, g, I); break;
+        case OP_OPROJ: ok = op_oproj(c, g, I); break;
+        case OP_ROUTER: ok = op_router(c, g, I); break;
+        case OP_MLP: ok = op_mlp(c, g, I); break;
+        case OP_MLP_UP: ok = op_mlp_up(c, g, I); break;
+        case OP_MLP_DOWN: ok = op_mlp_down(c, g, I); break;
+        case OP_LMHEAD: ok = op_lmhead(c, g, I); break;
+        default:
+          if (tid == 0) set_err(g, MK_ERR_DEVICE, pc, I.op);
+          ok = false;
+          break;
+      }
+      if (!ok) return;
+      if (tid == 0) {
+        if (g.trace) {
+          unsigned long long* t = g.trace + ((size_t)blockIdx.x * g.max_pc + pc) * 8;
+          t[1] = c.tw0;
+          t[2] = c.tw1;
+          t[3] = c.tm[0];
+          t[4] = c.tm[1];
+          t[5] = gtimer();
+          t[6] = c.ring.waited;  // warp 0's time blocked on ring data during this instruction
+          c.ring.waited = 0;
+        }
+        if (I.sig_ctr != NO_CTR && I.op != OP_ROUTER) {  // routers: the last arriver signals
+          if (I.flags & F_RELAXED_SIG)
+            red_relaxed(g.ctr + I.sig_ctr, 1u);
+          else
+            red_release(g.ctr + I.sig_ctr, 1u);
+        }
+        if (g.trace) g.trace[((size_t)blockIdx.x * g.max_pc + pc) * 8 + 7] = gtimer();
+        *(volatile int*)(misc + 1) = ++finished;
+      }
+    }
+  }  // steps
 }
 
 }  // namespace mk

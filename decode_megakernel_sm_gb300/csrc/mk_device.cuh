@@ -315,6 +315,35 @@ MK_DEV bool wait_counter(const Globals& g, uint32_t idx, uint32_t target, int pc
   }
 }
 
+// One of several staggered pollers of a counter (one lane per warp): it
+// starts after `delay_ns` and stops as soon as any poller has seen the
+// counter at `target` (the shared word `seen` then holds `key`).  Each poll
+// is an L2 round trip, so n pollers spaced a fraction of a round trip apart
+// see the counter complete that much sooner than one.  The poller that
+// sees it has acquired; the others are ordered after it by the CTA barrier
+// that follows.  Bounded like every wait.
+MK_DEV bool poll_counter_shared(const Globals& g, uint32_t idx, uint32_t target, uint64_t delay_ns,
+                                volatile int* seen, int key, int pc, int op) {
+  const uint32_t* p = g.ctr + idx;
+  const uint64_t t0 = gtimer();
+  while (delay_ns && gtimer() - t0 < delay_ns)
+    if (*seen == key) return true;
+  for (uint32_t it = 1;; it++) {
+    if (*seen == key) return true;
+    if ((int32_t)(ld_acquire(p) - target) >= 0) {
+      *seen = key;
+      return true;
+    }
+    if ((it & 15) == 0) {
+      if (peek_err(g)) return false;
+      if (gtimer() - t0 > g.timeout_ns) {
+        set_err(g, MK_ERR_TIMEOUT, pc, op);
+        return false;
+      }
+    }
+  }
+}
+
 // Wait for a phase of an mbarrier.  abort_on_err: also give up when the
 // grid has failed (consumers); the producer's drain passes false so that it
 // always waits for its own copies in flight.

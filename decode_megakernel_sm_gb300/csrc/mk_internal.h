@@ -97,7 +97,10 @@ struct CtrMap {
   // the logits, then signals router(l) on behalf of all of them)
   MK_HD uint32_t router_arrive(int l) const { return (uint32_t)(l * stride() + 2 * Hkv + 4); }
   MK_HD uint32_t lm() const { return (uint32_t)(L * stride()); }
-  MK_HD int count() const { return L * stride() + 1; }
+  // one signal per step, by the LM head's last arriver once the step's
+  // argmax is written: a multi-step launch starts step t + 1 behind it
+  MK_HD uint32_t lm_done() const { return (uint32_t)(L * stride() + 1); }
+  MK_HD int count() const { return L * stride() + 2; }
 };
 
 // Kernel-shape constants.
@@ -185,6 +188,8 @@ struct Globals {
   float* logits;
   int* argmax;
   unsigned long long timeout_ns;
+  int n_pollers;           // warps that poll a dependency counter (1..NCW)
+  unsigned poll_stagger_ns;// delay between the pollers' first polls
   int max_pc, n_sm, n_stages;
   int stage_bytes;  // bytes per ring stage (multiple of STAGE_UNIT)
   int B, H, Hq, Hkv, D, F, V, L, max_seq, max_ctx, splits;
@@ -195,11 +200,13 @@ struct Globals {
                            // tagged words written in this step carry tag == epoch
   int xtag;                // x_{2l+2} lives in xt (split MLP) rather than in xbuf
   int bsplit;              // batched split MLP (hglob holds h as A fragments)
-  int parity;              // epoch & 1: which residual buffer set this step uses
   uint32_t lm_ctr;
+  uint32_t lm_done_ctr;     // signalled once per step after the argmax is written
+  int n_steps;              // greedy decode steps in this launch (1: one step)
   int n_lm;
   int sel_key;             // -1: run every instruction; else only key == sel_key (ablation)
-  int zero_next;           // zero the other parity's residual buffers in this launch
+  int zero_next;           // the LM head slices zero the next step's residual buffers (the
+                           // other parity, epoch + 1 & 1) while they wait for their input
   int pdl;                 // ablation with programmatic dependent launch
   unsigned long long* trace;  // optional [n_sm][max_pc][8] %globaltimer stamps (NULL: off)
   unsigned long long l2_ahead;  // bytes of the SM's stream warmed in L2 ahead of the ring (0: off)

@@ -91,6 +91,14 @@ class Decoder:
         """Ring stage size (16, 32, 48 or 64 KiB); takes effect at the next step."""
         L.mk_set_stage_bytes(self.h, stage_bytes)
 
+    def set_poll_policy(self, pollers: int, stagger_ns: int):
+        """Warps polling each dependency counter, and their stagger."""
+        L.mk_set_poll_policy(self.h, pollers, stagger_ns)
+
+    def set_ring_depth(self, max_stages: int):
+        """At most max_stages ring stages (0: as many as fit)."""
+        L.mk_set_ring_depth(self.h, max_stages)
+
     def set_hold_policy(self, mask: int, early_bytes: int = 128 << 10):
         """Takes effect at the next build_schedule."""
         L.mk_set_hold_policy(self.h, mask, early_bytes)
@@ -122,6 +130,16 @@ class Decoder:
         i32 = torch.int32
         L.mk_decode_step(self.h, _ptr(tokens, i32), _ptr(positions, i32),
                          _ptr(logits, torch.float32), _ptr(argmax, i32), _stream(stream))
+
+    def steps(self, tokens, positions, n_steps, logits, argmax, stream=None):
+        """n_steps greedy steps in one launch (asynchronous): int32 tokens/positions [B]
+        for the first step, fp32 logits [B][V] of the last step, int32 argmax
+        [n_steps][B] of every step."""
+        i32 = torch.int32
+        if argmax.numel() < n_steps * len(tokens):
+            raise ValueError("argmax needs n_steps x batch entries")
+        L.mk_decode_steps(self.h, _ptr(tokens, i32), _ptr(positions, i32), n_steps,
+                          _ptr(logits, torch.float32), _ptr(argmax, i32), _stream(stream))
 
     def step_ablation(self, mode, tokens, positions, logits, argmax, stream=None):
         i32 = torch.int32

@@ -126,6 +126,22 @@ int mk_build_schedule(mk_handle* h, int batch, int max_ctx);
 int mk_decode_step(mk_handle* h, const int32_t* d_tokens, const int32_t* d_positions,
                    float* d_logits, int32_t* d_argmax, void* stream);
 
+/* n_steps greedy decode steps in one launch ("Megakernels: Deleting the
+ * Kernel Boundary", ranked next step: the argmax feeds the next step's
+ * embedding on the device).  Step 0 decodes d_tokens at d_positions; step
+ * t > 0 decodes step t - 1's argmax at d_positions + t.  The queues run once
+ * per step; step t begins once every SM is done with step t - 1, and the
+ * producer streams step t's first weights while step t - 1's LM head runs.
+ *   d_argmax  [n_steps][batch] int32 output: the argmax of every step;
+ *   d_logits  [batch][vocab] fp32 output: the logits of the last step.
+ * Requires d_positions[b] + n_steps - 1 < max_ctx (checked on the device
+ * before each step: MK_ERR_INVALID_ARG at mk_sync_status(), nothing written
+ * for that step and the ones after it).  Asynchronous, one kernel launch.
+ * Equivalent to n_steps calls of mk_decode_step, each fed the previous
+ * argmax; results agree to float rounding.                                */
+int mk_decode_steps(mk_handle* h, const int32_t* d_tokens, const int32_t* d_positions,
+                    int n_steps, float* d_logits, int32_t* d_argmax, void* stream);
+
 /* The same step from HOST buffers: copies h_tokens / h_positions to the
  * device, runs the step on the handle's own stream, copies logits (may be
  * NULL to skip) and argmax back, and waits.  Validates tokens and positions
@@ -199,6 +215,22 @@ int mk_set_l2_prefetch(mk_handle* h, uint64_t bytes_ahead);
  * stages carry 16 KB of weights next to 16 KB of activations (the old size
  * is kept).                                                                */
 int mk_set_stage_bytes(mk_handle* h, int stage_bytes);
+
+/* At most `max_stages` ring stages (2..16; 0, the default: as many as the
+ * opt-in shared memory holds).  Fewer stages keep fewer bytes in flight per
+ * SM, which shortens the queues every L2 access waits in while HBM streams.
+ * A performance knob only: results do not depend on it.  Call between
+ * steps; drops the cached ablation graphs.  MK_ERR_INVALID_ARG for 1 or out
+ * of range (the old depth is kept).                                        */
+int mk_set_ring_depth(mk_handle* h, int max_stages);
+
+/* How an SM waits for a dependency counter: `pollers` warps (1..7) each
+ * poll it, the k-th starting k * stagger_ns after the first, and all stop
+ * once one has seen it complete.  A poll is an L2 round trip; staggered
+ * pollers see the counter complete sooner after the last signal.  Takes
+ * effect at the next step.  Results do not depend on it.
+ * MK_ERR_INVALID_ARG for other pollers or stagger_ns > 100000.            */
+int mk_set_poll_policy(mk_handle* h, int pollers, unsigned stagger_ns);
 
 /* Number of partial copies (1..8, default 1) that each residual-stream
  * vector is accumulated into: SM i adds its float atomics into copy

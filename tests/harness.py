@@ -78,17 +78,20 @@ class Run:
             if s[-1] - s[-2] > MARGIN:
                 assert am[b] == ao[b], f"b={b}: argmax {am[b]} vs oracle {ao[b]}"
 
-    def check_kv(self):
+    def check_kv(self, back: int = 0):
+        """The K/V rows appended at the current positions (and the `back`
+        positions before them)."""
         for l in range(self.cfg["n_layers"]):
             for b in range(self.B):
-                P = self.pos[b]
-                for gpu, ora in ((self.ks[l], self.ko[l]), (self.vs[l], self.vo[l])):
-                    g = gpu[b, :, P, :].float().cpu().numpy()
-                    o = (ora[b, :, P, :].astype(np.uint32) << 16).view(np.float32)
-                    # one bf16 ulp, plus fp32-vs-fp64 accumulation noise at the row's scale
-                    tol = 2.0 ** -7 * np.abs(o) + 1e-3 * np.sqrt(np.mean(o * o))
-                    assert np.all(np.abs(g - o) <= tol), \
-                        f"layer {l} b {b}: appended K/V row differs by {np.abs(g - o).max()}"
+                for P in range(self.pos[b] - back, self.pos[b] + 1):
+                    for gpu, ora in ((self.ks[l], self.ko[l]), (self.vs[l], self.vo[l])):
+                        g = gpu[b, :, P, :].float().cpu().numpy()
+                        o = (ora[b, :, P, :].astype(np.uint32) << 16).view(np.float32)
+                        # one bf16 ulp, plus fp32-vs-fp64 accumulation noise at the row's scale
+                        tol = 2.0 ** -7 * np.abs(o) + 1e-3 * np.sqrt(np.mean(o * o))
+                        assert np.all(np.abs(g - o) <= tol), \
+                            f"layer {l} b {b} row {P}: appended K/V row differs by " \
+                            f"{np.abs(g - o).max()}"
 
     def step(self, mode: str = "mega", check_kv: bool = True):
         lg, am = self.gpu_step(mode)
@@ -118,6 +121,38 @@ class Run:
             assert sorted(rid[l, 0]) == sorted(gpu_ids[l]), \
                 f"layer {l}: experts {sorted(gpu_ids[l])} vs oracle {sorted(rid[l, 0])}"
         return lo, ao
+
+    def multi_step(self, n: int, oracle: bool = True):
+        """n greedy steps in one launch.  With `oracle`: teacher-force the
+        oracle with the GPU's argmax of every step, check each step's argmax
+        where the oracle's top-2 margin is clear, then the last step's logits
+        and every appended K/V row.  Returns (logits of the last step,
+        argmax [n][B])."""
+        self.d_tok.copy_(torch.tensor(self.tokens, dtype=torch.int32))
+        self.d_pos.copy_(torch.tensor(self.pos, dtype=torch.int32))
+        d_am = torch.full((n, self.B), -1, dtype=torch.int32, device="cuda")
+        self.dec.steps(self.d_tok, self.d_pos, n, self.d_logits, d_am)
+        status = self.dec.sync_status()
+        assert status == 0, f"device status {status}"
+        lg = self.d_logits.cpu().numpy().astype(np.float64)
+        am = d_am.cpu().numpy()
+        if oracle:
+            for t in range(n):
+                lo, ao, _, _ = self.om.step(self.ko, self.vo, self.tokens, self.pos)
+                for b in range(self.B):
+                    s = np.sort(lo[b])
+                    if s[-1] - s[-2] > MARGIN:
+                        assert am[t][b] == ao[b], f"step {t} b={b}: argmax {am[t][b]} vs oracle {ao[b]}"
+                if t < n - 1:
+                    self.tokens = [int(a) for a in am[t]]
+                    self.pos = [p + 1 for p in self.pos]
+            self.check(lg, am[n - 1], lo, ao)
+            self.check_kv(back=n - 1)
+        else:
+            self.pos = [p + n - 1 for p in self.pos]
+        self.tokens = [int(a) for a in am[n - 1]]
+        self.pos = [p + 1 for p in self.pos]
+        return lg, am
 
     def close(self):
         self.dec.close()

@@ -49,6 +49,27 @@ def test_hold_policies(mask, early):
     run_steps(cfg, 3, seed=11, hold=(mask, early))
 
 
+def test_shallow_ring_and_staggered_pollers():
+    # two ring stages, and four warps polling each counter 100 ns apart:
+    # neither changes a result
+    cfg = synth.custom(n_layers=3, n_q_heads=6, n_kv_heads=3, ffn=1000, vocab=999,
+                       prefill=(300, 300), steps=3)
+    r = Run(cfg, seed=13)
+    try:
+        r.dec.set_ring_depth(2)
+        r.dec.set_poll_policy(4, 100)
+        for _ in range(3):
+            r.step()
+        for bad in ((0, 0), (8, 0), (1, 200000)):
+            with pytest.raises(MkError):
+                r.dec.set_poll_policy(*bad)
+        with pytest.raises(MkError):
+            r.dec.set_ring_depth(1)
+        r.step()  # the previous settings are kept
+    finally:
+        r.close()
+
+
 def test_batched_split_mlp_held():
     # the batched down units gate their weight halves on the hold as well
     run_steps(_bsplit_cfg(8), 3, seed=23, hold=(63, 0))
