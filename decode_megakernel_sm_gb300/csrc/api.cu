@@ -56,7 +56,7 @@ static Scratch carve_scratch(const mk_model_desc& d, size_t B, size_t kc, size_t
   const size_t E = d.n_experts > 0 ? d.n_experts : 1;
   const size_t F = d.ffn > 0 ? d.ffn : 1;
   const size_t sx = al256(2 * 2 * L * kc * B * H * 4), sq = al256(L * B * Hq * D * 4);
-  const size_t sp = al256(L * B * Hq * splits * (D + 2) * 4);
+  const size_t sp = al256(L * B * Hq * splits * part_stride((int)D) * 4);
   const size_t sr = al256(L * B * E * 4), sl = al256(n_lm * B * 4);
   const size_t sc = al256(n_ctr * 4), se = 256;
   const size_t sroute = al256(L * (size_t)(d.top_k > 0 ? d.top_k : 1) * 4);  // ids, then weights
@@ -488,6 +488,7 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.eps = d.rms_eps;
   g.lm_ctr = CtrMap{d.n_kv_heads, d.n_layers}.lm();
   g.lm_done_ctr = CtrMap{d.n_kv_heads, d.n_layers}.lm_done();
+  g.part_staged = part_staged(h->plan.splits, h->var->NB, d.head_dim) ? 1 : 0;
   g.n_steps = 1;
   g.n_lm = h->plan.n_lm;
   g.sel_key = -1;

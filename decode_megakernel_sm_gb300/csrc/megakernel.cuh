@@ -108,10 +108,23 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
     case OP_QKV:
       s[0] = {(const unsigned char*)(Lp->wqkv + (size_t)I.r0 * HT), nullptr, ROW, n, RPS, I.r0};
       return 1;
-    case OP_OPROJ:
-      s[0] = {(const unsigned char*)(Lp->wo + ((size_t)I.g * HT + I.r0) * D), nullptr, D * 2, n,
-              SBY / (D * 2)};
+    case OP_OPROJ: {
+      // rows of Wo; with staged partials (heads of 128+ dims), first head
+      // I.g's split-KV partials of every sequence, copied in by the consumers
+      // once attention is done (one stage)
+      const Seg wo = {(const unsigned char*)(Lp->wo + ((size_t)I.g * HT + I.r0) * D), nullptr,
+                      D * 2, n, SBY / (D * 2)};
+      if constexpr (D >= 128) {
+        if (g.part_staged) {
+          const uint32_t pb = (uint32_t)(g.B * g.splits * part_stride(D) * 4);
+          s[0] = {(const unsigned char*)g.part, nullptr, 16u, pb / 16u, SBY / 16u, SEG_CFILL};
+          s[1] = wo;
+          return 2;
+        }
+      }
+      s[0] = wo;
       return 1;
+    }
     case OP_ROUTER:
       s[0] = {(const unsigned char*)(Lp->router + (size_t)I.r0 * HT), nullptr, ROW, n, RPS, I.r0};
       return 1;
@@ -815,7 +828,7 @@ MK_DEV bool op_attn(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
       O = fmaf(p[dim], f, O);
     }
     float* dst = g.part + ((((size_t)I.layer * g.B + b) * g.Hq + (size_t)I.g * HPG + h) * g.splits +
-                           I.r0) * (D + 2);
+                           I.r0) * part_stride(D);
     dst[dim] = O;
     if (dim == 0) {
       dst[D] = M;
@@ -833,45 +846,10 @@ MK_DEV float x_in(const Globals& g, uint32_t ep, int j, const int* tok, int b, i
   return xres_sum(g, ep, j, b, r);
 }
 
-// --------------------------------- OP_OPROJ (split reduce + O-proj rows) ----
-// Head h's partials are merged (M = max m_s, L = sum l_s 2^(m_s - M),
-// o = sum o_s 2^(m_s - M) / L), then rows [r0, r1) of Wo[:, h*D:(h+1)*D]
-// (packed [Hq][H][D]) are applied and accumulated into x_{2l+1} with float
-// atomics; the head-0 instructions also add the residual x_{2l}.
-template <int HT, int D, int HPG, int NB>
-MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
-  constexpr int LPR = D / 8, SPW = 32 / LPR;
-  constexpr int SG = (NCT / (NB * D)) > 0 ? NCT / (NB * D) : 1;  // slice groups per (b, dim)
-  const int slot = c.lane / LPR, dsl = c.lane % LPR;
-  const int h = I.g, l = I.layer;
-  const int S = g.splits;
-  if (!dep_wait(c, g, I)) return false;
-  // Work item (b, dim, sg) merges slices sg, sg + SG, ... -- all its loads
-  // are independent, so the whole combine costs about one L2 round trip.
-  float* pm = c.yrow;                    // [NB][SG][D] partial max
-  float* pl = pm + NB * SG * D;          // partial sum
-  float* po = pl + NB * SG * D;          // partial o
-  for (int it = c.tid; it < NB * SG * D; it += NCT) {
-    const int dim = it % D, sg = (it / D) % SG, b = it / (D * SG);
-    float M = NEG_BIG, Ls = 0.f, O = 0.f;
-    if (b < g.B) {
-      const float* base = g.part + (((size_t)l * g.B + b) * g.Hq + h) * S * (D + 2);
-#pragma unroll 4
-      for (int s = sg; s < S; s += SG) {
-        const float* p = base + (size_t)s * (D + 2);
-        const float ms = __ldcg(p + D), ls = __ldcg(p + D + 1), os = __ldcg(p + dim);
-        const float mn = fmaxf(M, ms);
-        const float fa = exp2f(M - mn), fb = exp2f(ms - mn);
-        Ls = Ls * fa + ls * fb;
-        O = O * fa + os * fb;
-        M = mn;
-      }
-    }
-    pm[it] = M;
-    pl[it] = Ls;
-    po[it] = O;
-  }
-  consumer_bar();
+// The SG partial merges of each (b, dim) of one head into its attention
+// output (c.attn).  All consumer threads.
+template <int D, int NB, int SG, class C>
+MK_DEV void merge_heads(C& c, const Globals& g, const float* pm, const float* pl, const float* po) {
   for (int it = c.tid; it < NB * D; it += NCT) {
     const int b = it / D, dim = it % D;
     float M = NEG_BIG;
@@ -886,6 +864,73 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
       O = fmaf(po[k], f, O);
     }
     c.attn[b * D + dim] = b < g.B ? O / Ls : 0.f;
+  }
+}
+
+// --------------------------------- OP_OPROJ (split reduce + O-proj rows) ----
+// Head h's partials are merged (M = max m_s, L = sum l_s 2^(m_s - M),
+// o = sum o_s 2^(m_s - M) / L), then rows [r0, r1) of Wo[:, h*D:(h+1)*D]
+// (packed [Hq][H][D]) are applied and accumulated into x_{2l+1} with float
+// atomics; the head-0 instructions also add the residual x_{2l}.
+template <int HT, int D, int HPG, int NB>
+MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+  constexpr int LPR = D / 8, SPW = 32 / LPR;
+  constexpr int SG = (NCT / (NB * D)) > 0 ? NCT / (NB * D) : 1;  // slice groups per (b, dim)
+  const int slot = c.lane / LPR, dsl = c.lane % LPR;
+  const int h = I.g, l = I.layer;
+  const int S = g.splits;
+  constexpr int PS = part_stride(D);  // partial record stride
+  if (!dep_wait(c, g, I)) return false;
+  Seg s[2];
+  bool staged = false;
+  float* pm = c.yrow;                    // [NB][SG][D] partial max
+  float* pl = pm + NB * SG * D;          // partial sum
+  float* po = pl + NB * SG * D;          // partial o
+  if constexpr (D >= 128) {
+    // heads of 128+ dims, many slices: the head's partials of every
+    // sequence land in the instruction's first ring stage, one bulk copy per
+    // sequence, issued now that attention is done (the producer armed the
+    // stage; every earlier stage is released); the residual loads below
+    // overlap them
+    staged = g.part_staged != 0;
+    if (staged) {
+      get_segs<HT, D>(g, I, c.pos, c.topk, s);
+      if (c.tid == 0) {
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // written by generic stores
+        const uint64_t pol = policy_evict_normal();
+        const uint32_t blk = (uint32_t)(S * PS * 4);
+        for (int b = 0; b < g.B; b++)
+          bulk_g2s(smem_u32(c.ring.ahead_ptr(0)) + (uint32_t)b * blk,
+                   g.part + (((size_t)l * g.B + b) * g.Hq + h) * S * PS, blk, c.ring.ahead_full(0),
+                   pol);
+      }
+    }
+  }
+  if (!staged) {
+    // Work item (b, dim, sg) merges slices sg, sg + SG, ... straight from L2;
+    // all its loads are independent (about one round trip per four slices)
+    for (int it = c.tid; it < NB * SG * D; it += NCT) {
+      const int dim = it % D, sg = (it / D) % SG, b = it / (D * SG);
+      float M = NEG_BIG, Ls = 0.f, O = 0.f;
+      if (b < g.B) {
+        const float* base = g.part + (((size_t)l * g.B + b) * g.Hq + h) * S * PS;
+#pragma unroll 4
+        for (int s2 = sg; s2 < S; s2 += SG) {
+          const float* p = base + (size_t)s2 * PS;
+          const float ms = __ldcg(p + D), ls = __ldcg(p + D + 1), os = __ldcg(p + dim);
+          const float mn = fmaxf(M, ms);
+          const float fa = exp2f(M - mn), fb = exp2f(ms - mn);
+          Ls = Ls * fa + ls * fb;
+          O = O * fa + os * fb;
+          M = mn;
+        }
+      }
+      pm[it] = M;
+      pl[it] = Ls;
+      po[it] = O;
+    }
+    consumer_bar();
+    merge_heads<D, NB, SG>(c, g, pm, pl, po);
   }
   const bool resid = (I.flags & F_RESIDUAL) != 0;
   float* xr_s = c.xn;  // residual rows of this slice, [NB][nr] with nr <= H (head-0 slices)
@@ -919,11 +964,42 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
     }
     if (!okr) c.flag[2] = 1;
   }
+  if constexpr (D >= 128) {
+    if (staged) {  // the same merge from the stage, once the copies land
+      if (c.ring.acquire(g)) {
+        const float* part = (const float*)c.ring.stage_ptr();
+        for (int it = c.tid; it < NB * SG * D; it += NCT) {
+          const int dim = it % D, sg = (it / D) % SG, b = it / (D * SG);
+          float M = NEG_BIG, Ls = 0.f, O = 0.f;
+          if (b < g.B) {
+            const float* base = part + (size_t)b * S * PS;
+            for (int s2 = sg; s2 < S; s2 += SG) {
+              const float* p = base + (size_t)s2 * PS;
+              const float ms = p[D], ls = p[D + 1], os = p[dim];
+              const float mn = fmaxf(M, ms);
+              const float fa = exp2f(M - mn), fb = exp2f(ms - mn);
+              Ls = Ls * fa + ls * fb;
+              O = O * fa + os * fb;
+              M = mn;
+            }
+          }
+          pm[it] = M;
+          pl[it] = Ls;
+          po[it] = O;
+        }
+        c.ring.release(c.lane);
+      } else {
+        c.flag[2] = 1;
+      }
+      consumer_bar();
+      merge_heads<D, NB, SG>(c, g, pm, pl, po);
+    }
+  }
   c.mark(g, 0);
   consumer_bar();
   if (c.flag[2]) return false;
-  Seg s[2];
-  get_segs<HT, D>(g, I, c.pos, c.topk, s);
+  if (!staged) get_segs<HT, D>(g, I, c.pos, c.topk, s);
+  const Seg& wseg = s[staged ? 1 : 0];  // the Wo rows
   const uint4 zero = make_uint4(0, 0, 0, 0);
   const int nr = (int)(I.r1 - I.r0);
   if constexpr (NB == 1) {
@@ -945,8 +1021,8 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
     }
     float* dst = xres_mine(g, c.epoch, 2 * l + 1, 0);
     uint32_t bc = 0;  // 32-row blocks of earlier stages (round-robin offset)
-    for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
-      const uint32_t n = min(s[0].ups, s[0].n - u0);
+    for (uint32_t u0 = 0; u0 < wseg.n; u0 += wseg.ups) {
+      const uint32_t n = min(wseg.ups, wseg.n - u0);
       if (!c.ring.acquire(g)) break;
       const unsigned char* st = c.ring.stage_ptr();
       const uint32_t nblk = (n + 31) / 32;
@@ -991,8 +1067,8 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   for (int b = 0; b < NB; b++)
 #pragma unroll
     for (int j = 0; j < 8; j++) a[b][j] = c.attn[b * D + dsl * 8 + j];
-  for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
-    const uint32_t n = min(s[0].ups, s[0].n - u0);
+  for (uint32_t u0 = 0; u0 < wseg.n; u0 += wseg.ups) {
+    const uint32_t n = min(wseg.ups, wseg.n - u0);
     if (!c.ring.acquire(g)) break;
     const unsigned char* st = c.ring.stage_ptr();
     // two passes of SPW rows per iteration: independent loads, FMA chains
@@ -1610,7 +1686,7 @@ struct L2Cursor {
       const uint32_t n = min(s[k].ups, s[k].n - u0);
       const uint32_t b = n * s[k].unit;
       const unsigned long long cb = s[k].src2 ? 2ull * b : b;
-      if (bytes + cb > from) {
+      if (bytes + cb > from && !s[k].cfill()) {
         if ((threadIdx.x & 31) == 0) {
           bulk_prefetch_l2(s[k].src + (size_t)u0 * s[k].unit, b);
           if (s[k].src2) bulk_prefetch_l2(s[k].src2 + (size_t)u0 * s[k].unit, b);
@@ -1846,7 +1922,9 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
           const uint32_t full = full0 + 8u * st;
           const uint32_t dst = ring_s + (uint32_t)st * (uint32_t)g.stage_bytes;
           mbar_expect_tx(full, s[k].src2 ? 2u * bytes : bytes);
-          if (s[k].src2) {
+          if (s[k].cfill()) {
+            // the consumers copy this stage in after their dependency wait
+          } else if (s[k].src2) {
             bulk_g2s(dst, s[k].src + (size_t)u0 * s[k].unit, bytes, full, pol_kv);
             bulk_g2s(dst + (uint32_t)g.stage_bytes / 2, s[k].src2 + (size_t)u0 * s[k].unit, bytes, full,
                      pol_kv);

@@ -365,13 +365,18 @@ MK_DEV bool wait_mbar(const Globals& g, uint32_t bar, uint32_t parity, bool abor
 // One contiguous run of equal-sized units (weight rows, or cache rows of K
 // with the matching V rows in src2) streamed through the ring, `ups` units
 // per stage.  src2 lands in the upper half of the stage.
+constexpr uint32_t SEG_CFILL = 0x80000000u;
+
 struct Seg {
   const unsigned char* src;
   const unsigned char* src2;
   uint32_t unit;
   uint32_t n;
   uint32_t ups;
-  uint32_t row0;  // swizzled GEMV matrices: index of the first row in its tensor (key = row & 7)
+  uint32_t row0;  // swizzled GEMV matrices: index of the first row in its tensor (key = row & 7);
+                  // SEG_CFILL set: an input of this step, whose stages the producer only arms
+                  // and the consumers fill once their dependency wait has passed
+  MK_DEV bool cfill() const { return (row0 & SEG_CFILL) != 0; }
 };
 
 // Ring cursor of one consumer warp.
@@ -386,6 +391,9 @@ struct Ring {
   uint32_t sb;  // bytes per stage
 
   MK_DEV const unsigned char* stage_ptr() const { return base + (size_t)st * sb; }
+  // the stage j places ahead of the cursor, and its full barrier
+  MK_DEV unsigned char* ahead_ptr(int j) const { return base + (size_t)((st + j) % ns) * sb; }
+  MK_DEV uint32_t ahead_full(int j) const { return full0 + 8u * (uint32_t)((st + j) % ns); }
   // All 32 lanes call; the result is the same on every lane.
   MK_DEV bool acquire(const Globals& g) {
     bool ok;

@@ -118,6 +118,21 @@ constexpr int DOWN_ROW_MAX = 16384;  // bytes of one down row (F <= 8192) in the
 constexpr int MAX_ROWS = 256;        // rows of one QKV / gate-up / router instruction
 constexpr int MAX_COLS = MAX_ROWS / 2;
 constexpr int MAX_DOWN_ROWS = 64;    // output rows of one split-MLP down instruction
+// One split-KV partial record: o[D], m, l; for heads of 128+ dims padded to
+// 16 bytes, so that an O-projection instruction can copy its head's partials
+// of every sequence in one bulk copy per sequence (they must then fit the
+// smallest ring stage).
+MK_HD inline constexpr int part_stride(int D) { return D >= 128 ? D + 4 : D + 2; }
+// The O-projection merges each (sequence, dim) of its head over the S slices
+// with SG = NCT / (NB * D) threads, four slices' loads at a time.  For heads
+// of 128 or more dims (one thread per dim), beyond two such rounds of L2
+// round trips it copies the partials into a ring stage first (one bulk copy
+// per sequence) and merges them from shared memory.  Smaller heads merge
+// straight from L2: there the staged variant measured slower.
+MK_HD inline bool part_staged(int S, int NB, int D) {
+  const int sg = NCT / (NB * D) > 0 ? NCT / (NB * D) : 1;
+  return D >= 128 && S > 8 * sg;
+}
 constexpr int MMA_FLUSH = 32;        // batched GEMV: rows per cross-warp sum of partials
 
 // Dense batch-1 models run the MLP as two ops (gate/up column slices, then
@@ -173,7 +188,7 @@ struct Globals {
   const float* rope;       // [max_seq][D/2][2] (cos, sin)
   float* xbuf;             // [2][2L][kc][B][H] residual stream x_1 .. x_2L, kc partial copies
   float* qbuf;             // [L][B][Hq][D]
-  float* part;             // [L][B][Hq][splits][D+2]: o[D], m, l  (log2 domain)
+  float* part;             // [L][B][Hq][splits][part_stride(D)]: o[D], m, l (log2 domain)
   float* rlog;             // [L][B][E] router logits
   float* hglob;            // [L][B][F] SiLU(gate)*up (split MLP)
   TagWord* xt;             // [L][B][H] tagged x_{2l+2} (split MLP: written once, by row owners)
@@ -202,6 +217,7 @@ struct Globals {
   int bsplit;              // batched split MLP (hglob holds h as A fragments)
   uint32_t lm_ctr;
   uint32_t lm_done_ctr;     // signalled once per step after the argmax is written
+  int part_staged;          // O-projection: partials through a ring stage (part_staged())
   int n_steps;              // greedy decode steps in this launch (1: one step)
   int n_lm;
   int sel_key;             // -1: run every instruction; else only key == sel_key (ablation)

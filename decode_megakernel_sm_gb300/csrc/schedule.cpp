@@ -56,11 +56,13 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
   CtrMap cm{Hkv, L};
 
   // split-KV slices per (sequence, kv head): about one work item per SM, at
-  // least 16 positions per slice on average at max_ctx, at most 128 slices
-  // (the O-projection stages every slice's (m, l) in shared memory).
+  // least 16 positions per slice on average at max_ctx, and few enough that
+  // one head's partials of every sequence fit the smallest ring stage (the
+  // O-projection copies them in with one bulk copy per sequence).
   int S = std::max(1, n_sm / (B * Hkv));
   S = std::min(S, std::max(1, max_ctx / 16));
-  S = std::min(S, 128);
+  S = std::min(S, STAGE_UNIT / (B * part_stride(D) * 4));
+  if (S < 1) return MK_ERR_UNSUPPORTED;
   const int n_items = B * Hkv * S;
 
   std::vector<std::vector<Instr>> qs(n_sm);
@@ -371,6 +373,8 @@ int plan_verify(const mk_model_desc& d, int B, const PlanOut& p) {
   const long R = (long)Hkv * GR, Fs = moe ? d.shared_ffn : 0;
   const long Fv = moe ? Fs + (long)d.top_k * d.expert_ffn : d.ffn;
   const int S = p.splits;
+  // one head's partials of every sequence fill at most the smallest ring stage
+  if (S < 1 || (long)B * S * part_stride(D) * 4 > STAGE_UNIT) return 32;
   std::vector<uint8_t> qkv((size_t)L * R, 0), att((size_t)L * B * Hkv * S, 0);
   std::vector<uint8_t> op((size_t)L * Hq * H, 0), mlp((size_t)L * Fv, 0), res((size_t)L * H, 0);
   std::vector<uint8_t> rt((size_t)L * (moe ? d.n_experts : 1), 0), lm(V, 0), slot(p.n_lm, 0);

@@ -75,6 +75,16 @@ def test_batched_split_mlp_held():
     run_steps(_bsplit_cfg(8), 3, seed=23, hold=(63, 0))
 
 
+def test_staged_partials_many_slices():
+    # heads of 128 dims at 2000 positions: 31 split-KV slices, so the
+    # O-projection copies its partials into a ring stage before merging them
+    # (with 16 KiB stages they fill the stage to within 16 bytes)
+    cfg = synth.custom(n_layers=2, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=128,
+                       ffn=2048, vocab=3000, prefill=(2000, 2000), steps=3, rope_theta=5e5)
+    run_steps(cfg, 3, seed=41)
+    run_steps(cfg, 2, seed=42, stage_bytes=16384)
+
+
 def test_llama1b_large_stages():
     r = Run(synth.CONFIGS["llama1b_1k"], seed=3, stage_bytes=65536)
     try:

@@ -52,9 +52,10 @@ def test_noalloc_step_matches_regular_step_on_two_calls(name):
 
 
 def test_noalloc_rejects_schedules_beyond_its_array():
-    # 250 layers of one-kv-head attention at 2048 positions need more than
-    # 16 MiB of split-KV partials: refused before any launch
-    cfg = synth.custom(n_layers=250, n_q_heads=2, n_kv_heads=1, ffn=256, vocab=256,
+    # 400 layers of 4 query heads, each head split into 60 slices at 2048
+    # positions: about 26 MB of split-KV partials, more than the 16 MiB
+    # array holds -- refused before any launch
+    cfg = synth.custom(n_layers=400, n_q_heads=4, n_kv_heads=2, ffn=256, vocab=256,
                        prefill=(8, 8), steps=2040)
     r = Run(cfg, seed=1)
     try:
