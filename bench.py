@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--pollers", type=int, default=None,
                     help="warps polling each dependency counter (library default if unset)")
     ap.add_argument("--poll-stagger", type=int, default=0, help="ns between pollers (with --pollers)")
+    ap.add_argument("--paged", type=int, default=0,
+                    help="paged KV cache with blocks of this many rows (0: contiguous)")
     ap.add_argument("--ring-depth", type=int, default=None,
                     help="at most this many ring stages (library default if unset)")
     ap.add_argument("--hold-early", type=int, default=128 << 10,
@@ -84,7 +86,8 @@ def workload_desc(cfg):
            f"F{cfg['shared_ffn']}" if cfg["n_experts"] else f"SwiGLU F{cfg['ffn']}")
     return (f"{cfg['name']}: {cfg['n_layers']}L H{cfg['hidden']} {cfg['n_q_heads']}q/"
             f"{cfg['n_kv_heads']}kv d{cfg['head_dim']} {mlp} V{cfg['vocab']}"
-            f"{' tied' if cfg['tied'] else ''}, bf16 weights, batch {cfg['batch']}, {kv}, "
+            f"{' tied' if cfg['tied'] else ''}, bf16 weights, batch {cfg['batch']}, {kv}"
+            f"{' in blocks of %d rows (paged)' % cfg['kv_pages'] if cfg.get('kv_pages') else ''}, "
             f"{cfg['steps']} greedy steps")
 
 
@@ -275,7 +278,13 @@ def main():
     ks, vs = synth.make_kv(cfg, lengths, args.seed, dev)
     tokens0 = synth.make_tokens(cfg, args.seed)
     torch.cuda.synchronize()
-    dec = Decoder(cfg, W, ks, vs)
+    if args.paged:  # the same rows in shuffled blocks of a pool, through a block table
+        pk, pv, table = synth.paged_pools(ks, vs, args.paged, args.seed)
+        dec = Decoder(cfg, W, pk, pv, max_batch=B, max_seq=cfg["max_seq"])
+        dec.set_kv_pages(args.paged, table)
+        cfg = dict(cfg, kv_pages=args.paged)
+    else:
+        dec = Decoder(cfg, W, ks, vs)
     # the library holds its own packed copy: keep only a host copy (for the CPU
     # baseline) and free the device one
     want_cpu = rank == 0 and ws == 1 and not args.no_cpu_baseline

@@ -93,6 +93,8 @@ struct mk_handle {
   int n_stages = 0, smem_bytes = 0;
   int stage_bytes = DEFAULT_STAGE_BYTES;
   int max_stages = 0;  // 0: as many as fit
+  int kv_block = 0, kv_blocks = 0, kv_stride = 0;  // paged KV cache (0: contiguous)
+  const int32_t* kv_table = nullptr;
   void* packed = nullptr;
   size_t packed_bytes = 0;
   std::vector<LayerPtrs> layers_h;
@@ -489,6 +491,10 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.lm_ctr = CtrMap{d.n_kv_heads, d.n_layers}.lm();
   g.lm_done_ctr = CtrMap{d.n_kv_heads, d.n_layers}.lm_done();
   g.part_staged = part_staged(h->plan.splits, h->var->NB, d.head_dim) ? 1 : 0;
+  g.kv_block = h->kv_block;
+  g.kv_blocks = h->kv_blocks;
+  g.kv_table = h->kv_table;
+  g.kv_stride = h->kv_stride;
   g.n_steps = 1;
   g.n_lm = h->plan.n_lm;
   g.sel_key = -1;
@@ -757,6 +763,26 @@ extern "C" int mk_set_poll_policy(mk_handle* h, int pollers, unsigned stagger_ns
   if (!h || pollers < 1 || pollers > NCW || stagger_ns > 100000u) return MK_ERR_INVALID_ARG;
   h->n_pollers = pollers;
   h->poll_stagger_ns = stagger_ns;
+  for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
+  h->graphs.clear();
+  return MK_OK;
+}
+
+extern "C" int mk_set_kv_pages(mk_handle* h, int block, int n_blocks, const int32_t* d_table,
+                               int table_stride) {
+  if (!h) return MK_ERR_INVALID_ARG;
+  if (block == 0) {  // back to the contiguous cache
+    h->kv_block = h->kv_blocks = h->kv_stride = 0;
+    h->kv_table = nullptr;
+  } else {
+    if (block < 16 || block > 4096 || (block & (block - 1)) || n_blocks < 1 || !d_table ||
+        table_stride < 1 || (long)table_stride * block < h->d.max_seq)
+      return MK_ERR_INVALID_ARG;
+    h->kv_block = block;
+    h->kv_blocks = n_blocks;
+    h->kv_table = d_table;
+    h->kv_stride = table_stride;
+  }
   for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
   h->graphs.clear();
   return MK_OK;

@@ -683,10 +683,14 @@ MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
         q[t] = y0;
         q[t + D / 2] = y1;
       } else {
-        uint16_t* row = (hs == HPG ? Lp.kc : Lp.vc) +
-                        (((size_t)b * g.Hkv + I.g) * g.max_seq + (size_t)P) * D;
-        row[t] = to_bf16(y0);
-        row[t + D / 2] = to_bf16(y1);
+        const long long off = kv_row(g, b, I.g, P);
+        if (off < 0) {
+          set_err(g, MK_ERR_INVALID_ARG, c.pc, I.op);  // a block outside the pool
+        } else {
+          uint16_t* row = (hs == HPG ? Lp.kc : Lp.vc) + off;
+          row[t] = to_bf16(y0);
+          row[t + D / 2] = to_bf16(y1);
+        }
       }
     }
   }
@@ -716,9 +720,11 @@ MK_DEV bool op_attn(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   // row P (appended by this step's QKV) is fetched together with q
   uint4 kP = zero, vP = zero;
   if (last && slot == 0) {
-    const size_t off = (((size_t)b * g.Hkv + I.g) * g.max_seq + (size_t)P) * D + dsl * 8;
-    kP = __ldcg((const uint4*)(Lp.kc + off));
-    vP = __ldcg((const uint4*)(Lp.vc + off));
+    const long long off = kv_row(g, b, I.g, P);
+    if (off >= 0) {  // (a bad block was reported by the append)
+      kP = __ldcg((const uint4*)(Lp.kc + off + dsl * 8));
+      vP = __ldcg((const uint4*)(Lp.vc + off + dsl * 8));
+    }
   }
   constexpr float QS = (D == 64 ? 0.125f : 0.08838834764831845f) * 1.4426950408889634f;
   float q[HPG][8], m[HPG], l[HPG], o[HPG][8];
@@ -1686,7 +1692,7 @@ struct L2Cursor {
       const uint32_t n = min(s[k].ups, s[k].n - u0);
       const uint32_t b = n * s[k].unit;
       const unsigned long long cb = s[k].src2 ? 2ull * b : b;
-      if (bytes + cb > from && !s[k].cfill()) {
+      if (bytes + cb > from && !s[k].cfill() && !(g.kv_block && s[k].src2)) {
         if ((threadIdx.x & 31) == 0) {
           bulk_prefetch_l2(s[k].src + (size_t)u0 * s[k].unit, b);
           if (s[k].src2) bulk_prefetch_l2(s[k].src2 + (size_t)u0 * s[k].unit, b);
@@ -1924,6 +1930,25 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
           mbar_expect_tx(full, s[k].src2 ? 2u * bytes : bytes);
           if (s[k].cfill()) {
             // the consumers copy this stage in after their dependency wait
+          } else if (s[k].src2 && g.kv_block && I.op == OP_ATTN) {
+            // paged cache: the stage's rows, one copy per block piece (K in
+            // the lower half, V in the upper)
+            const LayerPtrs* Lp = g.layers + I.layer;
+            const int P = ppos[I.b];
+            const int p0 = (int)((long)(P + 1) * I.r0 / I.r1) + (int)u0;
+            for (int r = p0; r < p0 + (int)n;) {
+              const int re = min(p0 + (int)n, (r / g.kv_block + 1) * g.kv_block);
+              long long off = kv_row(g, I.b, I.g, r);
+              if (off < 0) {  // a block outside the pool: fail the step, still fill the stage
+                set_err(g, MK_ERR_INVALID_ARG, pc, I.op);
+                off = 0;
+              }
+              const uint32_t pb = (uint32_t)(re - r) * (uint32_t)(D * 2);
+              const uint32_t at = (uint32_t)(r - p0) * (uint32_t)(D * 2);
+              bulk_g2s(dst + at, Lp->kc + off, pb, full, pol_kv);
+              bulk_g2s(dst + (uint32_t)g.stage_bytes / 2 + at, Lp->vc + off, pb, full, pol_kv);
+              r = re;
+            }
           } else if (s[k].src2) {
             bulk_g2s(dst, s[k].src + (size_t)u0 * s[k].unit, bytes, full, pol_kv);
             bulk_g2s(dst + (uint32_t)g.stage_bytes / 2, s[k].src2 + (size_t)u0 * s[k].unit, bytes, full,

@@ -201,6 +201,21 @@ MK_DEV void set_err(const Globals& g, int code, int pc, int op) {
   }
 }
 
+// ---- KV cache rows -------------------------------------------------------
+// Element offset of cache row p of (sequence b, kv head h): contiguous
+// [B][Hkv][max_seq][D], or paged -- block kv_table[b][p / blk] of the pool
+// [blocks][Hkv][blk][D] (the layout keeps a block's rows of one kv head
+// contiguous, one bulk copy per block).  -1 if the table names a block
+// outside the pool (the caller turns that into MK_ERR_INVALID_ARG).
+MK_DEV long long kv_row(const Globals& g, int b, int h, int p) {
+  if (g.kv_block == 0) return (((long long)b * g.Hkv + h) * g.max_seq + p) * g.D;
+  const int j = p / g.kv_block;
+  if (j >= g.kv_stride) return -1;
+  const int blk = __ldg(g.kv_table + (size_t)b * g.kv_stride + j);
+  if (blk < 0 || blk >= g.kv_blocks) return -1;
+  return (((long long)blk * g.Hkv + h) * g.kv_block + (p - j * g.kv_block)) * g.D;
+}
+
 // ---- tagged words --------------------------------------------------------
 // A value produced by exactly one writer per step travels as a 64-bit word
 // {f32 value, u32 tag}, tag = the step's epoch, written with one relaxed

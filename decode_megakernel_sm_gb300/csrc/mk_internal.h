@@ -218,6 +218,10 @@ struct Globals {
   uint32_t lm_ctr;
   uint32_t lm_done_ctr;     // signalled once per step after the argmax is written
   int part_staged;          // O-projection: partials through a ring stage (part_staged())
+  int kv_block;             // 0: KV cache [B][Hkv][max_seq][D]; else paged, blocks of kv_block rows:
+  int kv_blocks;            //   pool [kv_blocks][Hkv][kv_block][D], block of (b, j) =
+  const int* kv_table;      //   kv_table[b * kv_stride + j]
+  int kv_stride;
   int n_steps;              // greedy decode steps in this launch (1: one step)
   int n_lm;
   int sel_key;             // -1: run every instruction; else only key == sel_key (ablation)

@@ -46,8 +46,11 @@ class Decoder:
     weights: dict as produced by ``synth.make_weights`` (bf16, [out][in]);
     kcache / vcache: per-layer bf16 tensors [max_batch][Hkv][max_seq][head_dim]."""
 
-    def __init__(self, cfg: dict, weights: dict, kcache, vcache):
-        max_batch, _, max_seq, _ = kcache[0].shape
+    def __init__(self, cfg: dict, weights: dict, kcache, vcache, max_batch=None, max_seq=None):
+        """kcache / vcache may also be paged pools [n_blocks][Hkv][block][head_dim]:
+        then pass max_batch and max_seq, and call set_kv_pages before the first step."""
+        if max_batch is None or max_seq is None:
+            max_batch, _, max_seq, _ = kcache[0].shape
         self.cfg = cfg
         self.desc = desc_from_config(cfg, max_batch, max_seq)
         nl = cfg["n_layers"]
@@ -94,6 +97,17 @@ class Decoder:
     def set_poll_policy(self, pollers: int, stagger_ns: int):
         """Warps polling each dependency counter, and their stagger."""
         L.mk_set_poll_policy(self.h, pollers, stagger_ns)
+
+    def set_kv_pages(self, block: int, table):
+        """Paged KV cache: table is an int32 CUDA tensor [max_batch][stride] of block ids
+        into the pools given at construction (block 0: back to contiguous)."""
+        if block == 0:
+            L.mk_set_kv_pages(self.h, 0, 0, None, 0)
+            self._kv_table = None
+            return
+        n_blocks = self.kcache[0].shape[0]
+        L.mk_set_kv_pages(self.h, block, n_blocks, _ptr(table, torch.int32), table.shape[1])
+        self._kv_table = table  # kept alive: the kernel reads it every step
 
     def set_ring_depth(self, max_stages: int):
         """At most max_stages ring stages (0: as many as fit)."""

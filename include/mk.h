@@ -105,6 +105,23 @@ typedef struct {
  * On error *out is NULL and nothing is leaked.                            */
 int mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv, mk_handle** out);
 
+/* Paged KV cache (the survey's "paged KV cache" next step; the blocks of
+ * vLLM-style serving).  From the next step on, kv->k[l] / kv->v[l] given to
+ * mk_create point at pools [n_blocks][n_kv_heads][block][head_dim] (bf16,
+ * 16-byte aligned), and cache row p of sequence b lives in block
+ * d_table[b * table_stride + p / block] at row p % block.  d_table is a
+ * caller-owned device int32 array [max_batch][table_stride]; the caller may
+ * rewrite it between steps (e.g. to give a growing sequence a new block), and
+ * it must name a block for every row a step reads or writes (rows [0, P],
+ * and [0, P + n_steps - 1] for mk_decode_steps).  A block id outside
+ * [0, n_blocks) fails the step with MK_ERR_INVALID_ARG at mk_sync_status().
+ * block: a power of two, 16..4096; table_stride * block >= max_seq.
+ * block == 0 returns to the contiguous cache.  Results are the same as with
+ * the contiguous cache holding the same rows.  MK_ERR_INVALID_ARG
+ * otherwise.                                                               */
+int mk_set_kv_pages(mk_handle* h, int block, int n_blocks, const int32_t* d_table,
+                    int table_stride);
+
 /* Build the per-SM instruction queues for `batch` sequences whose positions
  * will stay below `max_ctx` (<= max_seq): splits every projection into
  * byte-balanced row ranges, one split-KV attention work item per

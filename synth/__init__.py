@@ -34,6 +34,12 @@ CONFIGS = {
         name="llama1b_8k", n_layers=16, hidden=2048, n_q_heads=32, n_kv_heads=8, head_dim=64,
         ffn=8192, vocab=128256, rms_eps=1e-5, rope_theta=5e5, tied=True, n_experts=0, top_k=0,
         expert_ffn=0, shared_ffn=0, batch=1, prefill=(8192, 8192), steps=128),
+    # long-context decode (the paged / long-context next step): a 32K cache,
+    # where the attention's share of the bytes passes a third
+    "llama1b_32k": dict(
+        name="llama1b_32k", n_layers=16, hidden=2048, n_q_heads=32, n_kv_heads=8, head_dim=64,
+        ffn=8192, vocab=128256, rms_eps=1e-5, rope_theta=5e5, tied=True, n_experts=0, top_k=0,
+        expert_ffn=0, shared_ffn=0, batch=1, prefill=(32768, 32768), steps=128),
     "llama1b_b8": dict(
         name="llama1b_b8", n_layers=16, hidden=2048, n_q_heads=32, n_kv_heads=8, head_dim=64,
         ffn=8192, vocab=128256, rms_eps=1e-5, rope_theta=5e5, tied=True, n_experts=0, top_k=0,
@@ -58,6 +64,30 @@ def with_cache(cfg: dict, extra_steps: int = 0) -> dict:
     need = cfg["prefill"][1] + cfg["steps"] + extra_steps
     c["max_seq"] = int((need + 63) // 64 * 64)
     return c
+
+
+def paged_pools(ks, vs, block: int, seed: int, spare: int = 5):
+    """The rows of contiguous caches ks[l] / vs[l] ([B][Hkv][S][D]) as pools
+    [n_blocks][Hkv][block][D] at shuffled block ids, and the int32 block table
+    [B][ceil(S / block)] that addresses them (plus `spare` unused blocks)."""
+    B, Hkv, S, D = ks[0].shape
+    nb = -(-S // block)
+    n_blocks = B * nb + spare
+    perm = torch.randperm(n_blocks, generator=torch.Generator().manual_seed(seed + 99))
+    table = perm[:B * nb].reshape(B, nb).to(torch.int32)
+    pk, pv = [], []
+    for kt, vt in zip(ks, vs):
+        pool_k = torch.zeros((n_blocks, Hkv, block, D), dtype=kt.dtype, device=kt.device)
+        pool_v = torch.zeros_like(pool_k)
+        for b in range(B):
+            for j in range(nb):
+                rows = slice(j * block, min(S, (j + 1) * block))
+                n = rows.stop - rows.start
+                pool_k[int(table[b, j]), :, :n] = kt[b, :, rows]
+                pool_v[int(table[b, j]), :, :n] = vt[b, :, rows]
+        pk.append(pool_k)
+        pv.append(pool_v)
+    return pk, pv, table.to(ks[0].device)
 
 
 def custom(**kw) -> dict:

@@ -27,7 +27,8 @@ ROUTE_TIE = 1e-4
 
 class Run:
     def __init__(self, cfg: dict, seed: int = 0, max_ctx: int | None = None,
-                 stage_bytes: int | None = None, hold: tuple | None = None):
+                 stage_bytes: int | None = None, hold: tuple | None = None,
+                 paged: int | None = None):
         cfg = cfg if "max_seq" in cfg else synth.with_cache(cfg)
         self.cfg = cfg
         self.W = synth.make_weights(cfg, seed, "cuda")
@@ -37,7 +38,17 @@ class Run:
         self.ko = [oracle._bits(t.cpu()).copy() for t in self.ks]
         self.vo = [oracle._bits(t.cpu()).copy() for t in self.vs]
         self.om = oracle.OracleModel(cfg, self.W)
-        self.dec = Decoder(cfg, self.W, self.ks, self.vs)
+        self.paged = paged
+        if paged:
+            # the same rows in pools of `paged`-row blocks, at shuffled block
+            # ids (plus a few spare blocks), addressed through a block table
+            B, Hkv, S, D = self.ks[0].shape
+            pk, pv, self.table = synth.paged_pools(self.ks, self.vs, paged, seed)
+            self.pk, self.pv = pk, pv
+            self.dec = Decoder(cfg, self.W, pk, pv, max_batch=B, max_seq=S)
+            self.dec.set_kv_pages(paged, self.table)
+        else:
+            self.dec = Decoder(cfg, self.W, self.ks, self.vs)
         if stage_bytes is not None:
             self.dec.set_stage_bytes(stage_bytes)
         if hold is not None:
@@ -84,14 +95,22 @@ class Run:
         for l in range(self.cfg["n_layers"]):
             for b in range(self.B):
                 for P in range(self.pos[b] - back, self.pos[b] + 1):
-                    for gpu, ora in ((self.ks[l], self.ko[l]), (self.vs[l], self.vo[l])):
-                        g = gpu[b, :, P, :].float().cpu().numpy()
+                    for kind, ora in ((0, self.ko[l]), (1, self.vo[l])):
+                        g = self.gpu_row(l, kind, b, P)
                         o = (ora[b, :, P, :].astype(np.uint32) << 16).view(np.float32)
                         # one bf16 ulp, plus fp32-vs-fp64 accumulation noise at the row's scale
                         tol = 2.0 ** -7 * np.abs(o) + 1e-3 * np.sqrt(np.mean(o * o))
                         assert np.all(np.abs(g - o) <= tol), \
                             f"layer {l} b {b} row {P}: appended K/V row differs by " \
                             f"{np.abs(g - o).max()}"
+
+    def gpu_row(self, l: int, kind: int, b: int, P: int):
+        """Cache row P of sequence b, all kv heads ([Hkv][D] fp32), as the GPU holds it."""
+        if self.paged:
+            pool = (self.pk, self.pv)[kind][l]
+            blk = int(self.table[b, P // self.paged])
+            return pool[blk, :, P % self.paged, :].float().cpu().numpy()
+        return (self.ks, self.vs)[kind][l][b, :, P, :].float().cpu().numpy()
 
     def step(self, mode: str = "mega", check_kv: bool = True):
         lg, am = self.gpu_step(mode)
