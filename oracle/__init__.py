@@ -50,7 +50,18 @@ _WFIELDS = ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "
 
 class OrcWeights(C.Structure):
     _fields_ = [("embed", C.c_void_p), ("lm_head", C.c_void_p), ("final_norm", C.c_void_p)] + \
-               [(n, C.POINTER(C.c_void_p)) for n in _WFIELDS]
+               [(n, C.POINTER(C.c_void_p)) for n in _WFIELDS] + [("q8", C.c_void_p)]
+
+
+class OrcQmat(C.Structure):
+    _fields_ = [("codes", C.c_void_p), ("scales", C.c_void_p)]
+
+
+_QFIELDS = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+
+
+class OrcQ8(C.Structure):
+    _fields_ = [(n, C.POINTER(OrcQmat)) for n in _QFIELDS] + [("lm_head", OrcQmat)]
 
 
 def lib():
@@ -80,6 +91,8 @@ def lib():
             L.orc_router_topk.argtypes = [dp, C.c_int, C.c_int, ip, dp]
             L.orc_argmax.restype = C.c_int
             L.orc_argmax.argtypes = [dp, C.c_int]
+            L.orc_quantize_rows_int8.argtypes = [u16p, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
+            L.orc_gemv_q8.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, dp, dp]
             L.orc_decode_step.restype = C.c_int
             L.orc_decode_step.argtypes = [C.POINTER(OrcConfig), C.POINTER(OrcWeights),
                                           C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
@@ -135,6 +148,28 @@ def gemv(W_bits, x):
     x = f64(x)
     y = np.empty(rows)
     lib().orc_gemv(_u16(W_bits), rows, cols, _dp(x), _dp(y))
+    return y
+
+
+def quantize_rows_int8(W_bits):
+    """Per-row int8 codes [rows][cols] (int8) and scales [rows] (float32) of a
+    bf16 matrix given as uint16 bits."""
+    W = np.ascontiguousarray(W_bits, np.uint16)
+    rows, cols = W.shape
+    q = np.empty((rows, cols), np.int8)
+    s = np.empty(rows, np.float32)
+    lib().orc_quantize_rows_int8(_u16(W), rows, cols, q.ctypes.data_as(C.c_void_p),
+                                 s.ctypes.data_as(C.c_void_p))
+    return q, s
+
+
+def gemv_q8(codes, scales, x):
+    q = np.ascontiguousarray(codes, np.int8)
+    s = np.ascontiguousarray(scales, np.float32)
+    xx = f64(x)
+    y = np.empty(q.shape[0])
+    lib().orc_gemv_q8(q.ctypes.data_as(C.c_void_p), s.ctypes.data_as(C.c_void_p), q.shape[0],
+                      q.shape[1], _dp(xx), _dp(y))
     return y
 
 
@@ -209,9 +244,11 @@ class OracleModel:
     """Holds host copies of the weights and runs ``orc_decode_step``.
 
     ``weights`` is the dict produced by ``synth.make_weights`` (bf16 tensors
-    on any device are accepted; they are copied to host once)."""
+    on any device are accepted; they are copied to host once).  ``int8``:
+    quantise every streamed matrix with ``orc_quantize_rows_int8`` and decode
+    with the int8 weights (dense models)."""
 
-    def __init__(self, cfg: dict, weights: dict):
+    def __init__(self, cfg: dict, weights: dict, int8: bool = False):
         self.cfg = cfg
         self._keep = []
         c = OrcConfig()
@@ -236,7 +273,26 @@ class OracleModel:
                 arr[l] = None if t is None else self._host(t).ctypes.data
             self._keep.append(arr)
             setattr(w, n, C.cast(arr, C.POINTER(C.c_void_p)))
+        w.q8 = None
+        if int8:
+            assert cfg.get("n_experts", 0) == 0, "int8 weights: dense models"
+            q8 = OrcQ8()
+            for n in _QFIELDS:
+                mats = (OrcQmat * L)()
+                for l in range(L):
+                    mats[l] = self._qmat(weights["layers"][l][n])
+                self._keep.append(mats)
+                setattr(q8, n, C.cast(mats, C.POINTER(OrcQmat)))
+            lm = weights["embed"] if weights.get("lm_head") is None else weights["lm_head"]
+            q8.lm_head = self._qmat(lm)
+            self._keep.append(q8)
+            w.q8 = C.addressof(q8)
         self.w = w
+
+    def _qmat(self, t):
+        q, s = quantize_rows_int8(self._host(t))
+        self._keep += [q, s]
+        return OrcQmat(q.ctypes.data, s.ctypes.data)
 
     def _host(self, t):
         if not isinstance(t, np.ndarray):

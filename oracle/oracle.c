@@ -107,6 +107,46 @@ void orc_gemv(const uint16_t* W, int rows, int cols, const double* x, double* y)
   }
 }
 
+/* Per-row int8 quantisation ([G4] "What's next": INT8 weights).  Reading:
+ * one symmetric scale per output row, the largest magnitude mapped to 127,
+ * round half to even. */
+void orc_quantize_rows_int8(const uint16_t* W, int rows, int cols, int8_t* codes, float* scales) {
+  for (int r = 0; r < rows; r++) {
+    const uint16_t* w = W + (size_t)r * (size_t)cols;
+    float m = 0.0f;
+    for (int k = 0; k < cols; k++) {
+      float a = fabsf((float)orc_bf16_to_f64(w[k]));
+      if (a > m) m = a;
+    }
+    float s = m > 0.0f ? m / 127.0f : 0.0f;
+    for (int k = 0; k < cols; k++) {
+      long q = 0;
+      if (s > 0.0f) {
+        float t = (float)orc_bf16_to_f64(w[k]) / s;
+        q = lrintf(t); /* the default rounding mode: nearest, ties to even */
+        if (q > 127) q = 127;
+        if (q < -127) q = -127;
+      }
+      codes[(size_t)r * (size_t)cols + k] = (int8_t)q;
+    }
+    scales[r] = s;
+  }
+}
+
+void orc_gemv_q8(const int8_t* codes, const float* scales, int rows, int cols, const double* x,
+                 double* y) {
+  int nt = orc_get_threads();
+  (void)nt;
+#pragma omp parallel for schedule(static) num_threads(nt)
+  for (int r = 0; r < rows; r++) {
+    const int8_t* q = codes + (size_t)r * (size_t)cols;
+    const double s = (double)scales[r];
+    double acc = 0.0;
+    for (int k = 0; k < cols; k++) acc += ((double)q[k] * s) * x[k];
+    y[r] = acc;
+  }
+}
+
 /* [MK] op list "attention": softmax(q K^T / sqrt(d)) V over the cached rows. */
 void orc_attention(const double* q, const uint16_t* K, const uint16_t* V, int n_pos, int d,
                    double* out) {
@@ -239,6 +279,15 @@ int orc_argmax(const double* v, int n) {
   return best;
 }
 
+/* The GEMV of one streamed matrix: bf16 W, or its int8 form m when m is set. */
+static void gemv_w(const uint16_t* W, const orc_qmat* m, int rows, int cols, const double* x,
+                   double* y) {
+  if (m)
+    orc_gemv_q8(m->codes, m->scales, rows, cols, x, y);
+  else
+    orc_gemv(W, rows, cols, x, y);
+}
+
 static uint16_t* cache_row(uint16_t* base, const orc_config* c, int b, int g, int pos) {
   size_t idx = (((size_t)b * c->n_kv_heads + g) * (size_t)c->max_seq + (size_t)pos) *
                (size_t)c->head_dim;
@@ -265,6 +314,8 @@ int orc_decode_step(const orc_config* cfg, const orc_weights* w, uint16_t* const
   }
   const int group = Hq / Hkv;
   const int moe = cfg->n_experts > 0;
+  const orc_q8* q8 = w->q8;
+  if (q8 && moe) return -1; /* int8 weights: dense models only */
   double* x = (double*)malloc(sizeof(double) * (size_t)H);
   double* xn = (double*)malloc(sizeof(double) * (size_t)H);
   double* q = (double*)malloc(sizeof(double) * (size_t)Hq * d);
@@ -286,9 +337,9 @@ int orc_decode_step(const orc_config* cfg, const orc_weights* w, uint16_t* const
     for (int l = 0; l < L; l++) {
       /* OP_RMS_QKV_ROPE */
       orc_rmsnorm(x, w->attn_norm[l], H, cfg->rms_eps, xn);
-      orc_gemv(w->wq[l], Hq * d, H, xn, q);
-      orc_gemv(w->wk[l], Hkv * d, H, xn, k);
-      orc_gemv(w->wv[l], Hkv * d, H, xn, v);
+      gemv_w(w->wq[l], q8 ? &q8->wq[l] : NULL, Hq * d, H, xn, q);
+      gemv_w(w->wk[l], q8 ? &q8->wk[l] : NULL, Hkv * d, H, xn, k);
+      gemv_w(w->wv[l], q8 ? &q8->wv[l] : NULL, Hkv * d, H, xn, v);
       for (int h = 0; h < Hq; h++) orc_rope(q + (size_t)h * d, d, P, cfg->rope_theta);
       for (int g = 0; g < Hkv; g++) orc_rope(k + (size_t)g * d, d, P, cfg->rope_theta);
       for (int g = 0; g < Hkv; g++) {
@@ -306,11 +357,23 @@ int orc_decode_step(const orc_config* cfg, const orc_weights* w, uint16_t* const
                       cache_row(vc[l], cfg, b, g, 0), P + 1, d, att + (size_t)h * d);
       }
       /* OP_O_PROJ_RES */
-      orc_gemv(w->wo[l], H, Hq * d, att, y);
+      gemv_w(w->wo[l], q8 ? &q8->wo[l] : NULL, H, Hq * d, att, y);
       for (int i = 0; i < H; i++) x[i] += y[i];
       /* OP_RMS_UP_GATE + OP_DOWN_RES (dense) or router + experts (MoE) */
       orc_rmsnorm(x, w->mlp_norm[l], H, cfg->rms_eps, xn);
-      if (!moe) {
+      if (!moe && q8) {
+        /* the same MLP with the int8 gate, up and down matrices */
+        const int F = cfg->ffn;
+        double* gq = (double*)malloc(sizeof(double) * (size_t)F);
+        double* uq = (double*)malloc(sizeof(double) * (size_t)F);
+        gemv_w(NULL, &q8->w_gate[l], F, H, xn, gq);
+        gemv_w(NULL, &q8->w_up[l], F, H, xn, uq);
+        for (int c = 0; c < F; c++) gq[c] = orc_silu(gq[c]) * uq[c];
+        gemv_w(NULL, &q8->w_down[l], H, F, gq, y);
+        free(gq);
+        free(uq);
+        for (int i = 0; i < H; i++) x[i] += y[i];
+      } else if (!moe) {
         orc_swiglu(w->w_gate[l], w->w_up[l], w->w_down[l], cfg->ffn, H, xn, y);
         for (int i = 0; i < H; i++) x[i] += y[i];
       } else {
@@ -349,7 +412,7 @@ int orc_decode_step(const orc_config* cfg, const orc_weights* w, uint16_t* const
     }
     /* OP_RMS_LM_HEAD */
     orc_rmsnorm(x, w->final_norm, H, cfg->rms_eps, xn);
-    orc_gemv(w->lm_head, V, H, xn, logits + (size_t)b * V);
+    gemv_w(w->lm_head, q8 ? &q8->lm_head : NULL, V, H, xn, logits + (size_t)b * V);
     argmax[b] = orc_argmax(logits + (size_t)b * V, V);
   }
   free(x);

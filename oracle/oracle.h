@@ -19,8 +19,9 @@
  * Arithmetic: every value is a double; bf16 inputs are widened exactly.  The
  * only rounding the oracle does on purpose is the bf16 rounding (round to
  * nearest, ties to even, directly from double) of the K and V rows it appends
- * to the cache, because the cache is bf16.  No blocking, fusion or
- * reordering: dot products accumulate in index order.
+ * to the cache, because the cache is bf16, and, for int8 weights, the fp32
+ * divisions that decide each code (orc_quantize_rows_int8).  No blocking,
+ * fusion or reordering: dot products accumulate in index order.
  *
  * Pins (tests/test_oracle_pins.py): bf16 widening/rounding on printed bit
  * patterns, RMSNorm closed forms, RoPE identity at p=0 / norm preservation /
@@ -29,7 +30,11 @@
  * merge equals the unsplit softmax, GEMV against numpy float64 matmul,
  * SiLU closed forms, router top-k against a stable numpy argsort and E=1,k=1
  * MoE equal to the dense MLP, argmax first-index ties, and the whole tiny
- * decoder against an independent numpy formulation.
+ * decoder against an independent numpy formulation.  int8: worked rows of
+ * the quantiser (ties to even, the clamp, a zero row), its half-step error
+ * bound, the int8 GEMV against numpy on the dequantised matrix, and the
+ * int8 decoder equal to the bf16 decoder on weights the quantiser
+ * reproduces exactly.
  */
 #ifndef MK_ORACLE_H
 #define MK_ORACLE_H
@@ -68,7 +73,32 @@ typedef struct {
   const uint16_t* const* sh_gate;   /* MoE shared: [shared_ffn][hidden] */
   const uint16_t* const* sh_up;     /* MoE shared: [shared_ffn][hidden] */
   const uint16_t* const* sh_down;   /* MoE shared: [hidden][shared_ffn] */
+  const struct orc_q8* q8;          /* NULL: bf16 weights; else int8 (below) */
 } orc_weights;
+
+/* int8 weights (the "INT8 experts" of "Gemma 4 TPU megakernel", section
+ * "What's next", applied to every streamed matrix of a dense model): a
+ * matrix is codes q[rows][cols] (int8) and one scale s[r] (fp32) per row,
+ * standing for the weights w[r][k] = q[r][k] * s[r].                    */
+typedef struct {
+  const int8_t* codes;  /* [rows][cols] */
+  const float* scales;  /* [rows] */
+} orc_qmat;
+
+/* With q8 set, orc_decode_step takes these matrices (per-layer arrays of
+ * n_layers) in place of the bf16 wq, wk, wv, wo, w_gate, w_up, w_down and
+ * lm_head; the embedding gather, norms and KV cache stay bf16.  Dense
+ * models only.                                                           */
+typedef struct orc_q8 {
+  const orc_qmat* wq;
+  const orc_qmat* wk;
+  const orc_qmat* wv;
+  const orc_qmat* wo;
+  const orc_qmat* w_gate;
+  const orc_qmat* w_up;
+  const orc_qmat* w_down;
+  orc_qmat lm_head;
+} orc_q8;
 
 /* bf16 <-> double */
 double orc_bf16_to_f64(uint16_t h);
@@ -83,6 +113,19 @@ void orc_rope(double* v, int d, int pos, double theta);
 
 /* y[r] = sum_k W[r][k] x[k] for a bf16 row-major W[rows][cols]. */
 void orc_gemv(const uint16_t* W, int rows, int cols, const double* x, double* y);
+
+/* Symmetric per-row int8 quantisation of a bf16 W[rows][cols]: with m the
+ * largest |W[r][k]| of row r, s[r] = m / 127 and q[r][k] = W[r][k] / s[r]
+ * rounded to the nearest integer, ties to even, then clamped to
+ * [-127, 127]; both divisions are single-precision (fp32) and correctly
+ * rounded, because the decision of an integer code is taken in the
+ * precision the device takes it in.  A row of zeros: s = 0, codes 0.      */
+void orc_quantize_rows_int8(const uint16_t* W, int rows, int cols, int8_t* codes, float* scales);
+
+/* y[r] = sum_k (q[r][k] * s[r]) x[k]: the plain GEMV of the dequantised
+ * weights (each q * s is exact in double).                                */
+void orc_gemv_q8(const int8_t* codes, const float* scales, int rows, int cols, const double* x,
+                 double* y);
 
 /* Softmax attention of one query q[d] over n_pos cache rows K,V [n_pos][d]
  * (bf16), scale 1/sqrt(d).                                              */

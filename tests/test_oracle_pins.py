@@ -277,3 +277,121 @@ def test_oracle_rejects_bad_arguments():
         om.step(kc, vc, [cfg["vocab"]], [16])
     with pytest.raises(ValueError):
         om.step(kc, vc, [1], [cfg["max_seq"]])
+
+
+# ------------------------------------------------------------------- int8 ----
+# Per-row int8 weights ("Gemma 4 TPU megakernel", "What's next": INT8
+# weights).  Reading: s = max|w| / 127, q = round-half-even(w / s), in fp32.
+def _bf16_rows(rows):
+    a = np.array(rows, np.float32).view(np.uint32)
+    assert np.all((a & 0xFFFF) == 0), "values must be exact in bf16"
+    return (a >> 16).astype(np.uint16)
+
+
+def test_int8_quantiser_worked_rows():
+    W = _bf16_rows([[127, -63.5, 0.5, 1.5, -2.5, 0, 64, -127],  # s = 1: ties go to even
+                    [0, 0, 0, 0, 0, 0, 0, 0],                   # zero row: s = 0
+                    [254, 3, 5, 7, -3, -5, -7, 1],              # s = 2: 1.5, 2.5, 3.5, 0.5
+                    [-0.25, 0.125, 0, 0, 0, 0, 0, 0.0078125]])  # negative maximum
+    q, s = oracle.quantize_rows_int8(W)
+    assert s.tolist() == [1.0, 0.0, 2.0, np.float32(0.25) / np.float32(127)]
+    assert q[0].tolist() == [127, -64, 0, 2, -2, 0, 64, -127]
+    assert q[1].tolist() == [0] * 8
+    assert q[2].tolist() == [127, 2, 2, 4, -2, -2, -4, 0]
+    # row 3: -0.25 is the largest magnitude -> -127; 0.125 / s = 63.5 -> 64 (even);
+    # 2^-7 / s = 3.96875 -> 4
+    assert q[3].tolist() == [-127, 64, 0, 0, 0, 0, 0, 4]
+
+
+def test_int8_quantiser_error_bound_and_extremes():
+    W = rand_bits((40, 300), std=0.02)
+    W[3] = 0  # a zero row
+    q, s = oracle.quantize_rows_int8(W)
+    w = bn.widen(W)
+    for r in range(W.shape[0]):
+        if not np.any(w[r]):
+            assert s[r] == 0 and not np.any(q[r])
+            continue
+        assert np.max(np.abs(q[r])) == 127  # the largest magnitude maps to +-127
+        err = np.abs(w[r] - q[r].astype(np.float64) * np.float64(s[r]))
+        # half a step, plus the fp32 rounding of s and of w / s (|w / s| <= 127)
+        assert np.all(err <= np.float64(s[r]) * (0.5 + 2.0 ** -16))
+        assert np.all(np.sign(q[r]) == np.sign(np.where(np.abs(w[r]) < s[r] / 2, 0, w[r])))
+
+
+def test_int8_gemv_matches_numpy_on_dequantised_weights():
+    rng = np.random.default_rng(9)
+    q = rng.integers(-127, 128, size=(37, 160)).astype(np.int8)
+    s = rng.uniform(1e-4, 1e-2, size=37).astype(np.float32)
+    x = rng.standard_normal(160)
+    y = oracle.gemv_q8(q, s, x)
+    ref = (q.astype(np.float64) * s.astype(np.float64)[:, None]) @ x
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-14)
+    # one row, one column: q * s * x
+    assert oracle.gemv_q8(np.array([[-3]], np.int8), np.array([0.5], np.float32), [2.0])[0] == -3.0
+
+
+def _exact_int8_weights(cfg, seed):
+    """bf16 weights that per-row int8 quantisation reproduces exactly: each row
+    is q * 2^-e with integer q in [-127, 127] (one entry at +-127) and e in 9..12."""
+    W = synth.make_weights(cfg, seed)
+    rng = np.random.default_rng(seed + 3)
+
+    def exact(t):
+        rows, cols = t.shape
+        q = rng.integers(-127, 128, size=(rows, cols))
+        q[np.arange(rows), rng.integers(0, cols, rows)] = 127 * rng.choice([-1, 1], rows)
+        e = rng.integers(9, 13, size=rows)
+        return torch.tensor(q * np.exp2(-e.astype(np.float64))[:, None],
+                            dtype=torch.float32).to(torch.bfloat16)
+
+    W["embed"] = exact(W["embed"])
+    for lw in W["layers"]:
+        for n in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down"):
+            lw[n] = exact(lw[n])
+    return W
+
+
+def _oracle_steps(cfg, W, int8, steps=3, seed=0):
+    lengths = synth.make_lengths(cfg, seed)
+    ks, vs = synth.make_kv(cfg, lengths, seed)
+    ko = [oracle._bits(t).copy() for t in ks]
+    vo = [oracle._bits(t).copy() for t in vs]
+    om = oracle.OracleModel(cfg, W, int8=int8)
+    toks, pos, out = synth.make_tokens(cfg, seed), list(lengths), []
+    for _ in range(steps):
+        lo, ao, _, _ = om.step(ko, vo, toks, pos)
+        out.append(lo)
+        toks = [int(a) for a in ao]
+        pos = [p + 1 for p in pos]
+    return out
+
+
+def test_int8_decoder_equals_bf16_decoder_on_exactly_quantisable_weights():
+    cfg = synth.with_cache(synth.custom(n_layers=2, hidden=128, n_q_heads=4, n_kv_heads=2,
+                                        head_dim=32, ffn=96, vocab=300, batch=2,
+                                        prefill=(3, 9), steps=3))
+    W = _exact_int8_weights(cfg, 11)
+    a = _oracle_steps(cfg, W, int8=False)
+    b = _oracle_steps(cfg, W, int8=True)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+def test_int8_decoder_differs_by_the_quantisation_error_only():
+    cfg = synth.with_cache(synth.custom(n_layers=2, hidden=128, n_q_heads=4, n_kv_heads=2,
+                                        head_dim=32, ffn=96, vocab=300, steps=2,
+                                        prefill=(5, 5)))
+    W = synth.make_weights(cfg, 13)
+    a = _oracle_steps(cfg, W, int8=False, steps=1)[0]
+    b = _oracle_steps(cfg, W, int8=True, steps=1)[0]
+    d = np.max(np.abs(a - b)) / np.std(a)
+    assert 0 < d < 0.1  # the int8 path is taken, and ~1 % weight noise stays small
+
+
+def test_int8_oracle_refuses_moe():
+    cfg = synth.with_cache(synth.custom(n_layers=1, hidden=128, n_q_heads=4, n_kv_heads=2,
+                                        head_dim=32, ffn=0, vocab=200, tied=False, n_experts=4,
+                                        top_k=2, expert_ffn=32, shared_ffn=0, prefill=(2, 2)))
+    with pytest.raises(AssertionError):
+        oracle.OracleModel(cfg, synth.make_weights(cfg, 0), int8=True)
