@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--pollers", type=int, default=None,
                     help="warps polling each dependency counter (library default if unset)")
     ap.add_argument("--poll-stagger", type=int, default=0, help="ns between pollers (with --pollers)")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "int8"],
+                    help="streamed weight format (int8: per-row int8 codes + fp32 scales)")
     ap.add_argument("--paged", type=int, default=0,
                     help="paged KV cache with blocks of this many rows (0: contiguous)")
     ap.add_argument("--ring-depth", type=int, default=None,
@@ -86,7 +88,9 @@ def workload_desc(cfg):
            f"F{cfg['shared_ffn']}" if cfg["n_experts"] else f"SwiGLU F{cfg['ffn']}")
     return (f"{cfg['name']}: {cfg['n_layers']}L H{cfg['hidden']} {cfg['n_q_heads']}q/"
             f"{cfg['n_kv_heads']}kv d{cfg['head_dim']} {mlp} V{cfg['vocab']}"
-            f"{' tied' if cfg['tied'] else ''}, bf16 weights, batch {cfg['batch']}, {kv}"
+            f"{' tied' if cfg['tied'] else ''}, "
+            f"{'int8 weights (per-row fp32 scales)' if cfg.get('int8') else 'bf16 weights'}, "
+            f"batch {cfg['batch']}, {kv}"
             f"{' in blocks of %d rows (paged)' % cfg['kv_pages'] if cfg.get('kv_pages') else ''}, "
             f"{cfg['steps']} greedy steps")
 
@@ -184,7 +188,7 @@ def cpu_baseline(cfg, W, ks, vs, lengths, tokens, budget_s=20.0):
     steps of the same workload (at least one step)."""
     import oracle
     t0 = time.perf_counter()
-    om = oracle.OracleModel(cfg, W)
+    om = oracle.OracleModel(cfg, W, int8=bool(cfg.get("int8")))
     ko = [oracle._bits(t.cpu()).copy() for t in ks]
     vo = [oracle._bits(t.cpu()).copy() for t in vs]
     prep = time.perf_counter() - t0
@@ -219,7 +223,7 @@ def run_reference(args, cfg):
     W = synth.make_weights(cfg, args.seed, "cpu")
     lengths = synth.make_lengths(cfg, args.seed)
     ks, vs = synth.make_kv(cfg, lengths, args.seed, "cpu")
-    om = oracle.OracleModel(cfg, W)
+    om = oracle.OracleModel(cfg, W, int8=bool(cfg.get("int8")))
     ko = [oracle._bits(t).copy() for t in ks]
     vo = [oracle._bits(t).copy() for t in vs]
     tokens = synth.make_tokens(cfg, args.seed)
@@ -243,7 +247,8 @@ def run_reference(args, cfg):
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "tok/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / k * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 (int8 weights)" if cfg.get("int8") else "f64",
         "data": "synthetic", "config": {"workload": workload_desc(cfg)},
         "cpu_baseline": {"value": val, "unit": "tok/s", "cores": oracle.get_threads(),
                          "kind": "oracle",
@@ -259,6 +264,8 @@ def main():
     import synth
     base = synth.CONFIGS[args.config]
     cfg = synth.with_cache(base)
+    if args.weights == "int8":
+        cfg = dict(cfg, int8=True)
     if args.impl == "reference":
         run_reference(args, cfg)
         return
@@ -280,11 +287,12 @@ def main():
     torch.cuda.synchronize()
     if args.paged:  # the same rows in shuffled blocks of a pool, through a block table
         pk, pv, table = synth.paged_pools(ks, vs, args.paged, args.seed)
-        dec = Decoder(cfg, W, pk, pv, max_batch=B, max_seq=cfg["max_seq"])
+        dec = Decoder(cfg, W, pk, pv, max_batch=B, max_seq=cfg["max_seq"],
+                      weight_format=args.weights)
         dec.set_kv_pages(args.paged, table)
         cfg = dict(cfg, kv_pages=args.paged)
     else:
-        dec = Decoder(cfg, W, ks, vs)
+        dec = Decoder(cfg, W, ks, vs, weight_format=args.weights)
     # the library holds its own packed copy: keep only a host copy (for the CPU
     # baseline) and free the device one
     want_cpu = rank == 0 and ws == 1 and not args.no_cpu_baseline
@@ -378,14 +386,16 @@ def main():
     spl = ns if ns else 1  # steps per launch
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak,
-            "traffic": traffic_record(args.config, spl),
+            "traffic": traffic_record(args.config + ("+int8" if args.weights == "int8" else ""),
+                                      spl),
             "peak_source": peak_kind, "algorithmic_bytes_per_launch": alg * spl,
             "kernel": "mk::mk_decode_kernel (persistent, %d step(s) per launch)" % spl}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 weights x f32" if args.weights == "int8" else "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "batch": B, "prefill": list(cfg["prefill"]),
                    "decode_window": window, "parallelism": f"replicas x{ws}",
                    "l2": "inputs larger than L2 (%.2f GB of weights streamed per step)"

@@ -20,6 +20,7 @@ MK_ERR_NOT_READY = -6
 MK_ERR_DEVICE = -7
 MK_ERR_SCRATCH = -8
 MK_ABL_STREAM, MK_ABL_GRAPH, MK_ABL_PDL = 0, 1, 2
+MK_WEIGHTS_BF16, MK_WEIGHTS_INT8 = 0, 1
 
 OP_NAMES = {0: "HALT", 1: "QKV", 2: "ATTN", 3: "OPROJ", 4: "MLP", 5: "LMHEAD", 6: "ROUTER", 8: "MLP_UP", 9: "MLP_DOWN",
             7: "NOP"}
@@ -80,6 +81,10 @@ _lib = None
 SIGNATURES = {
     "mk_create": (C.c_int, [C.POINTER(mk_model_desc), C.POINTER(mk_weights), C.POINTER(mk_kv),
                             C.POINTER(C.c_void_p)]),
+    "mk_create_ex": (C.c_int, [C.POINTER(mk_model_desc), C.POINTER(mk_weights), C.POINTER(mk_kv),
+                               C.c_int, C.POINTER(C.c_void_p)]),
+    "mk_quantize_rows_int8": (C.c_int, [C.c_void_p, C.c_long, C.c_int, C.c_void_p, C.c_void_p,
+                                        C.c_void_p]),
     "mk_build_schedule": (C.c_int, [C.c_void_p, C.c_int, C.c_int]),
     "mk_decode_step": (C.c_int, [C.c_void_p] * 6),
     "mk_decode_steps": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
@@ -146,6 +151,18 @@ def mk_create(desc: mk_model_desc, weights: mk_weights, kv: mk_kv) -> int:
     h = C.c_void_p()
     _check(lib().mk_create(C.byref(desc), C.byref(weights), C.byref(kv), C.byref(h)), "mk_create")
     return h.value
+
+
+def mk_create_ex(desc: mk_model_desc, weights: mk_weights, kv: mk_kv, weight_format: int) -> int:
+    h = C.c_void_p()
+    _check(lib().mk_create_ex(C.byref(desc), C.byref(weights), C.byref(kv), weight_format,
+                              C.byref(h)), "mk_create_ex")
+    return h.value
+
+
+def mk_quantize_rows_int8(d_w, rows: int, cols: int, d_codes, d_scales, stream=None):
+    _check(lib().mk_quantize_rows_int8(d_w, rows, cols, d_codes, d_scales, stream),
+           "mk_quantize_rows_int8")
 
 
 def mk_build_schedule(h, batch: int, max_ctx: int):

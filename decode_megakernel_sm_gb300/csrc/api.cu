@@ -3,6 +3,7 @@
 // host-buffer step, the per-phase ablation launcher and error reporting.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <map>
@@ -23,11 +24,19 @@ cudaError_t pack_rows(uint16_t* dst, const void* src, long rows, int H, cudaStre
 cudaError_t pack_down_tiles(uint16_t* dst, const void* src, int H, int F, cudaStream_t s);
 cudaError_t pack_transpose(uint16_t* dst, const void* src, int R, int C, int batch,
                            cudaStream_t s);
+cudaError_t quantize_rows_int8(int8_t* codes, float* scales, const void* w, long rows, int cols,
+                               cudaStream_t s);
+cudaError_t pack_qkv_scales(float* dst, const float* sq, const float* sk, const float* sv, int Hkv,
+                            int HPG, int D, cudaStream_t s);
+cudaError_t interleave_scales(float* dst, const float* a, const float* b, int n, cudaStream_t s);
+cudaError_t pack_wo_i8(void* dst, const void* wo_codes, int H, int Hq, cudaStream_t s);
+cudaError_t bias_codes(void* p, size_t bytes, cudaStream_t s);
 
 extern const Variant variant_h256_d64_g2_b1;
 extern const Variant variant_h2048_d64_g4_b1;
 extern const Variant variant_h2048_d64_g4_b8;
 extern const Variant variant_h2048_d128_g4_b1;
+extern const Variant variant_h2048_d64_g4_b1_w8;
 }  // namespace mk
 
 using namespace mk;
@@ -100,6 +109,8 @@ struct mk_handle {
   std::vector<LayerPtrs> layers_h;
   LayerPtrs* layers_d = nullptr;
   const uint16_t *embed = nullptr, *lm_head = nullptr, *final_norm = nullptr;
+  int wfmt = MK_WEIGHTS_BF16;
+  const float* lm_scale = nullptr;  // int8 weights
   float* rope = nullptr;
   // schedule and scratch
   int batch = 0, max_ctx = 0;
@@ -138,13 +149,14 @@ struct mk_handle {
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-static const Variant* pick_variant(const mk_model_desc& d) {
+static const Variant* pick_variant(const mk_model_desc& d, int wb) {
   const Variant* all[] = {&variant_h256_d64_g2_b1, &variant_h2048_d64_g4_b1,
-                          &variant_h2048_d64_g4_b8, &variant_h2048_d128_g4_b1};
+                          &variant_h2048_d64_g4_b8, &variant_h2048_d128_g4_b1,
+                          &variant_h2048_d64_g4_b1_w8};
   const int HPG = d.n_q_heads / d.n_kv_heads;
   const Variant* best = nullptr;
   for (const Variant* v : all) {
-    if (v->H != d.hidden || v->D != d.head_dim || v->HPG != HPG) continue;
+    if (v->H != d.hidden || v->D != d.head_dim || v->HPG != HPG || v->WB != wb) continue;
     if (v->NB < d.max_batch) continue;
     if (!best || v->NB < best->NB) best = v;
   }
@@ -217,10 +229,10 @@ static int size_ring(mk_handle* h, int stage_bytes) {
   int ns = 0;
   const int cap = h->max_stages > 0 ? h->max_stages : MAX_STAGES;
   for (int n = 2; n <= cap; n++)
-    if (smem_layout(n, stage_bytes, h->var->NB, d.hidden, d.head_dim, HPG, K).total <= optin)
+    if (smem_layout(n, stage_bytes, h->var->NB, d.hidden, d.head_dim, HPG, K, h->var->WB).total <= optin)
       ns = n;
   if (ns < 2) return MK_ERR_UNSUPPORTED;
-  const int bytes = smem_layout(ns, stage_bytes, h->var->NB, d.hidden, d.head_dim, HPG, K).total;
+  const int bytes = smem_layout(ns, stage_bytes, h->var->NB, d.hidden, d.head_dim, HPG, K, h->var->WB).total;
   CK(cudaFuncSetAttribute(h->var->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
   int per_sm = 0;
   CK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, h->var->kernel, NTHREADS, bytes));
@@ -231,13 +243,20 @@ static int size_ring(mk_handle* h, int stage_bytes) {
   return MK_OK;
 }
 
+static int pack_int8(mk_handle* h, const mk_weights* w, const mk_kv* kv, cudaStream_t s);
+
 static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv,
-                       mk_handle* h) {
+                       mk_handle* h, int wfmt) {
   const mk_model_desc& d = *desc;
   h->d = d;
   int rc = plan_shape_ok(d);
   if (rc) return rc;
-  h->var = pick_variant(d);
+  if (wfmt != MK_WEIGHTS_BF16 && wfmt != MK_WEIGHTS_INT8) return MK_ERR_INVALID_ARG;
+  // int8 weights: dense batch-1 shapes with the split MLP and 64-dim heads
+  if (wfmt == MK_WEIGHTS_INT8 && (!mlp_split(d) || d.ffn % 16 || d.head_dim != 64))
+    return MK_ERR_UNSUPPORTED;
+  h->wfmt = wfmt;
+  h->var = pick_variant(d, wfmt == MK_WEIGHTS_INT8 ? 1 : 2);
   if (!h->var) return MK_ERR_UNSUPPORTED;
   const int L = d.n_layers, H = d.hidden, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
   const int D = d.head_dim, HPG = Hq / Hkv;
@@ -267,6 +286,9 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
         (!okp(w->sh_gate[l]) || !okp(w->sh_up[l]) || !okp(w->sh_down[l])))
       return MK_ERR_INVALID_ARG;
   }
+  // int8 weights: a 4-stage ring by default (fewer copies in flight shorten
+  // the dependency hops; half the bytes per row keep the bodies fed)
+  if (wfmt == MK_WEIGHTS_INT8) h->max_stages = 4;
   // ---- device
   CK(cudaGetDevice(&h->dev));
   CK(cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, h->dev));
@@ -276,7 +298,11 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
   }
   CK(cudaStreamCreateWithFlags(&h->own, cudaStreamNonBlocking));
   CK(cudaMallocHost(&h->h_err, 4 * sizeof(int)));
-
+  cudaStream_t s = h->own;
+  if (wfmt == MK_WEIGHTS_INT8) {
+    rc = pack_int8(h, w, kv, s);
+    if (rc) return rc;
+  } else {
   // ---- packed weight buffer
   const LayerSizes ls = layer_sizes(d);
   const size_t V = d.vocab;
@@ -293,7 +319,6 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
     p += al256(elems * 2);
     return r;
   };
-  cudaStream_t s = h->own;
   h->layers_h.resize(L);
   for (int l = 0; l < L; l++) {
     LayerPtrs& lp = h->layers_h[l];
@@ -358,6 +383,7 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
   uint16_t* fn = take(H);
   CK(cudaMemcpyAsync(fn, w->final_norm, (size_t)H * 2, cudaMemcpyDeviceToDevice, s));
   h->final_norm = fn;
+  }  // bf16 weights
   CK(cudaMalloc(&h->layers_d, sizeof(LayerPtrs) * L));
   CK(cudaMemcpyAsync(h->layers_d, h->layers_h.data(), sizeof(LayerPtrs) * L,
                      cudaMemcpyHostToDevice, s));
@@ -376,14 +402,114 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
   return MK_OK;
 }
 
-extern "C" int mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv,
-                         mk_handle** out) {
+// int8 packing: every streamed matrix quantised per row (quantize_rows_int8),
+// then laid out like its bf16 counterpart with 16-code chunks, codes stored
+// biased by 128.  The
+// embedding stays bf16 for the token gather; the LM head (the embedding
+// when tied) gets its own int8 copy.
+static int pack_int8(mk_handle* h, const mk_weights* w, const mk_kv* kv, cudaStream_t s) {
+  const mk_model_desc& d = h->d;
+  const int L = d.n_layers, H = d.hidden, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
+  const int D = d.head_dim, HPG = Hq / Hkv, F = d.ffn;
+  const size_t V = d.vocab, R = (size_t)Hkv * (HPG + 2) * D;
+  const size_t per_layer = 2 * al256((size_t)H * 2) + al256(R * H) + al256((size_t)Hq * D * H) +
+                           al256(2 * (size_t)F * H) + al256((size_t)F * H) + al256(R * 4) +
+                           2 * al256((size_t)H * 4) + al256(2 * (size_t)F * 4);
+  const size_t total = per_layer * L + al256(V * H * 2) + al256(V * H) + al256(V * 4) + al256(H * 2);
+  CK(cudaMalloc(&h->packed, total));
+  h->packed_bytes = total;
+  // codes and scales of the matrices being packed (the largest: QKV, gate +
+  // up, or the LM head)
+  const size_t tcodes = std::max(std::max(R * H, 2 * (size_t)F * H), V * H);
+  const size_t tscales = std::max(std::max(R, 2 * (size_t)F), V);
+  struct Tmp {
+    void* p = nullptr;
+    ~Tmp() {
+      if (p) cudaFree(p);
+    }
+  } tmp;
+  CK(cudaMalloc(&tmp.p, al256(tcodes) + tscales * 4));
+  int8_t* tc = (int8_t*)tmp.p;
+  float* ts = (float*)((char*)tmp.p + al256(tcodes));
+  char* p = (char*)h->packed;
+  auto take = [&](size_t bytes) {
+    char* r = p;
+    p += al256(bytes);
+    return r;
+  };
+  h->layers_h.resize(L);
+  for (int l = 0; l < L; l++) {
+    LayerPtrs& lp = h->layers_h[l];
+    std::memset(&lp, 0, sizeof lp);
+    uint16_t* an = (uint16_t*)take((size_t)H * 2);
+    uint16_t* mn = (uint16_t*)take((size_t)H * 2);
+    char* qkv = take(R * H);
+    char* wo = take((size_t)Hq * D * H);
+    char* gu = take(2 * (size_t)F * H);
+    char* dn = take((size_t)F * H);
+    float* sqkv = (float*)take(R * 4);
+    float* so = (float*)take((size_t)H * 4);
+    float* sd = (float*)take((size_t)H * 4);
+    float* sgu = (float*)take(2 * (size_t)F * 4);
+    CK(cudaMemcpyAsync(an, w->attn_norm[l], (size_t)H * 2, cudaMemcpyDeviceToDevice, s));
+    CK(cudaMemcpyAsync(mn, w->mlp_norm[l], (size_t)H * 2, cudaMemcpyDeviceToDevice, s));
+    // QKV: q, k, v codes side by side, then the bf16 packer on 2-code units
+    const size_t nq = (size_t)Hq * D, nk = (size_t)Hkv * D;
+    CK(quantize_rows_int8(tc, ts, w->wq[l], (long)nq, H, s));
+    CK(quantize_rows_int8(tc + nq * H, ts + nq, w->wk[l], (long)nk, H, s));
+    CK(quantize_rows_int8(tc + (nq + nk) * H, ts + nq + nk, w->wv[l], (long)nk, H, s));
+    CK(pack_qkv((uint16_t*)qkv, tc, tc + nq * H, tc + (nq + nk) * H, H / 2, Hkv, HPG, D, s));
+    CK(pack_qkv_scales(sqkv, ts, ts + nq, ts + nq + nk, Hkv, HPG, D, s));
+    CK(quantize_rows_int8(tc, so, w->wo[l], H, Hq * D, s));
+    CK(pack_wo_i8(wo, tc, H, Hq, s));
+    CK(quantize_rows_int8(tc, ts, w->w_gate[l], F, H, s));
+    CK(quantize_rows_int8(tc + (size_t)F * H, ts + F, w->w_up[l], F, H, s));
+    CK(pack_interleave((uint16_t*)gu, tc, tc + (size_t)F * H, F, H / 2, s));
+    CK(interleave_scales(sgu, ts, ts + F, F, s));
+    CK(quantize_rows_int8((int8_t*)dn, sd, w->w_down[l], H, F, s));  // rows as they are
+    // the kernel reads codes biased by 128
+    CK(bias_codes(qkv, R * H, s));
+    CK(bias_codes(wo, (size_t)Hq * D * H, s));
+    CK(bias_codes(gu, 2 * (size_t)F * H, s));
+    CK(bias_codes(dn, (size_t)F * H, s));
+    lp.attn_norm = an;
+    lp.mlp_norm = mn;
+    lp.wqkv = (const uint16_t*)qkv;
+    lp.wo = (const uint16_t*)wo;
+    lp.wgu = (const uint16_t*)gu;
+    lp.wdT = (const uint16_t*)dn;
+    lp.sqkv = sqkv;
+    lp.so = so;
+    lp.sgu = sgu;
+    lp.sd = sd;
+    lp.kc = (uint16_t*)kv->k[l];
+    lp.vc = (uint16_t*)kv->v[l];
+  }
+  uint16_t* emb = (uint16_t*)take(V * H * 2);
+  CK(pack_rows(emb, w->embed, (long)V, H, s));
+  h->embed = emb;
+  char* lm = take(V * H);
+  float* lms = (float*)take(V * 4);
+  CK(quantize_rows_int8(tc, lms, d.tied_lm_head ? w->embed : w->lm_head, (long)V, H, s));
+  CK(pack_rows((uint16_t*)lm, tc, (long)V, H / 2, s));
+  CK(bias_codes(lm, V * H, s));
+  h->lm_head = (const uint16_t*)lm;
+  h->lm_scale = lms;
+  uint16_t* fn = (uint16_t*)take((size_t)H * 2);
+  CK(cudaMemcpyAsync(fn, w->final_norm, (size_t)H * 2, cudaMemcpyDeviceToDevice, s));
+  h->final_norm = fn;
+  CK(cudaStreamSynchronize(s));  // before the temporary codes are freed
+  return MK_OK;
+}
+
+static int create_checked(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv,
+                          int wfmt, mk_handle** out) {
   if (!out) return MK_ERR_INVALID_ARG;
   *out = nullptr;
   if (!desc) return MK_ERR_INVALID_ARG;
   mk_handle* h = new (std::nothrow) mk_handle();
   if (!h) return MK_ERR_INVALID_ARG;
-  const int rc = create_impl(desc, w, kv, h);
+  const int rc = create_impl(desc, w, kv, h, wfmt);
   if (rc != MK_OK) {
     free_all(h);
     cudaGetLastError();
@@ -393,13 +519,31 @@ extern "C" int mk_create(const mk_model_desc* desc, const mk_weights* w, const m
   return MK_OK;
 }
 
+extern "C" int mk_create_ex(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv,
+                            int weight_format, mk_handle** out) {
+  return create_checked(desc, w, kv, weight_format, out);
+}
+
+extern "C" int mk_quantize_rows_int8(const void* d_w, long rows, int cols, int8_t* d_codes,
+                                     float* d_scales, void* stream) {
+  if (rows < 0 || cols <= 0 || (rows > 0 && (!d_w || !d_codes || !d_scales)))
+    return MK_ERR_INVALID_ARG;
+  CK(quantize_rows_int8(d_codes, d_scales, d_w, rows, cols, (cudaStream_t)stream));
+  return MK_OK;
+}
+
+extern "C" int mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv,
+                         mk_handle** out) {
+  return create_checked(desc, w, kv, MK_WEIGHTS_BF16, out);
+}
+
 // ------------------------------------------------------------- schedule ----
 extern "C" int mk_build_schedule(mk_handle* h, int batch, int max_ctx) {
   if (!h) return MK_ERR_INVALID_ARG;
   CK(cudaStreamSynchronize(h->own));
   free_schedule(h);
   PlanOut p;
-  int rc = plan_build(h->d, batch, max_ctx, h->n_sm, p, h->hold_mask);
+  int rc = plan_build(h->d, batch, max_ctx, h->n_sm, p, h->hold_mask, h->var->WB);
   if (rc) return rc;
   if (plan_verify(h->d, batch, p)) return MK_ERR_SCHEDULE;
   if (plan_check(p.q.data(), h->n_sm, p.max_pc, p.n_ctr)) return MK_ERR_SCHEDULE;
@@ -443,6 +587,7 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.sched = h->sched;
   g.layers = h->layers_d;
   g.embed = h->embed;
+  g.lm_scale = h->lm_scale;
   g.lm_head = h->lm_head;
   g.final_norm = h->final_norm;
   g.rope = h->rope;

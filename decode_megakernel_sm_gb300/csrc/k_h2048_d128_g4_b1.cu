@@ -3,6 +3,6 @@
 #include "megakernel.cuh"
 
 namespace mk {
-extern const Variant variant_h2048_d128_g4_b1 = {2048, 128, 4, 1,
-                                              (const void*)&mk_decode_kernel<2048, 128, 4, 1>};
+extern const Variant variant_h2048_d128_g4_b1 = {2048, 128, 4, 1, 2,
+                                              (const void*)&mk_decode_kernel<2048, 128, 4, 1, 2>};
 }  // namespace mk

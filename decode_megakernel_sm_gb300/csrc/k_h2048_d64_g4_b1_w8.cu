@@ -1,0 +1,8 @@
+// One compiled instantiation of the decode interpreter: hidden 2048, head_dim 64,
+// 4 query heads per kv head, batch capacity 1, int8 weights (one fp32 scale per row).
+#include "megakernel.cuh"
+
+namespace mk {
+extern const Variant variant_h2048_d64_g4_b1_w8 = {
+    2048, 64, 4, 1, 1, (const void*)&mk_decode_kernel<2048, 64, 4, 1, 1>};
+}  // namespace mk

@@ -3,6 +3,6 @@
 #include "megakernel.cuh"
 
 namespace mk {
-extern const Variant variant_h2048_d64_g4_b8 = {2048, 64, 4, 8,
-                                              (const void*)&mk_decode_kernel<2048, 64, 4, 8>};
+extern const Variant variant_h2048_d64_g4_b8 = {2048, 64, 4, 8, 2,
+                                              (const void*)&mk_decode_kernel<2048, 64, 4, 8, 2>};
 }  // namespace mk

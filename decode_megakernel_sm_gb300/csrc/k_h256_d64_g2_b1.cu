@@ -3,6 +3,6 @@
 #include "megakernel.cuh"
 
 namespace mk {
-extern const Variant variant_h256_d64_g2_b1 = {256, 64, 2, 1,
-                                              (const void*)&mk_decode_kernel<256, 64, 2, 1>};
+extern const Variant variant_h256_d64_g2_b1 = {256, 64, 2, 1, 2,
+                                              (const void*)&mk_decode_kernel<256, 64, 2, 1, 2>};
 }  // namespace mk

@@ -20,7 +20,7 @@
 
 namespace mk {
 
-template <int HT, int D, int HPG, int NB>
+template <int HT, int D, int HPG, int NB, int WB>
 struct Ctx {
   float* xn;    // [NB][HT] normalised activation of the current instruction
   float* yrow;  // [NB][MAX_ROWS] row outputs / attention merge scratch
@@ -28,6 +28,7 @@ struct Ctx {
   float* mpart; // NB > 1: [NCW][MMA_FLUSH][NB] per-warp partial sums of the batched GEMV
   float* attn;  // [NB][D] reduced attention output of one head
   float* red;   // reduction scratch
+  float* sc;    // int8 weights: row scales of the current O-proj / LM-head instruction [HT]
   int* tok;     // [NB]
   int* pos;     // [NB]
   int* topk;    // [NB][K] routed expert ids
@@ -50,8 +51,8 @@ struct Ctx {
 // The dependency wait of one instruction: thread 0 spins on the counter,
 // then all consumer warps meet; false if the grid has failed.  Every op
 // calls it exactly once, after issuing its dependency-free loads.
-template <int HT, int D, int HPG, int NB>
-MK_DEV bool dep_wait(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool dep_wait(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
   // the first lanes of n_pollers warps poll the counter, staggered (flag[3]:
   // key of the instruction whose counter was seen; flag[4]: key of a failed
   // wait).  A met counter means complete inputs; errors elsewhere in the
@@ -97,23 +98,24 @@ MK_DEV float xres_sum(const Globals& g, uint32_t ep, int j, int b, int r) {
 // The weight / cache byte ranges an instruction streams, in ring order.
 // The producer issues exactly these copies; the consumers consume exactly
 // these stages.  Returns the number of segments (0..2).
-template <int HT, int D>
+template <int HT, int D, int WB>
 MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int* topk, Seg* s) {
-  constexpr uint32_t ROW = HT * 2;
+  // WB bytes per weight: 2 (bf16) or 1 (int8 codes, dense batch-1 shapes only)
+  constexpr uint32_t ROW = HT * WB;
   const uint32_t SBY = (uint32_t)g.stage_bytes;
   const uint32_t RPS = SBY / ROW;
   const LayerPtrs* Lp = g.layers + (I.op == OP_LMHEAD ? 0 : I.layer);
   const uint32_t n = I.r1 - I.r0;
   switch (I.op) {
     case OP_QKV:
-      s[0] = {(const unsigned char*)(Lp->wqkv + (size_t)I.r0 * HT), nullptr, ROW, n, RPS, I.r0};
+      s[0] = {(const unsigned char*)Lp->wqkv + (size_t)I.r0 * ROW, nullptr, ROW, n, RPS, I.r0};
       return 1;
     case OP_OPROJ: {
       // rows of Wo; with staged partials (heads of 128+ dims), first head
       // I.g's split-KV partials of every sequence, copied in by the consumers
       // once attention is done (one stage)
-      const Seg wo = {(const unsigned char*)(Lp->wo + ((size_t)I.g * HT + I.r0) * D), nullptr,
-                      D * 2, n, SBY / (D * 2)};
+      const Seg wo = {(const unsigned char*)Lp->wo + ((size_t)I.g * HT + I.r0) * D * WB, nullptr,
+                      D * WB, n, SBY / (D * WB)};
       if constexpr (D >= 128) {
         if (g.part_staged) {
           const uint32_t pb = (uint32_t)(g.B * g.splits * part_stride(D) * 4);
@@ -150,10 +152,10 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
       return 2;
     }
     case OP_LMHEAD:
-      s[0] = {(const unsigned char*)(g.lm_head + (size_t)I.r0 * HT), nullptr, ROW, n, RPS, I.r0};
+      s[0] = {(const unsigned char*)g.lm_head + (size_t)I.r0 * ROW, nullptr, ROW, n, RPS, I.r0};
       return 1;
     case OP_MLP_UP:
-      s[0] = {(const unsigned char*)(Lp->wgu + (size_t)I.r0 * 2 * HT), nullptr, ROW, 2 * n, RPS,
+      s[0] = {(const unsigned char*)Lp->wgu + (size_t)I.r0 * 2 * ROW, nullptr, ROW, 2 * n, RPS,
               2 * I.r0};
       return 1;
     case OP_MLP_DOWN:
@@ -167,8 +169,8 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
         return 1;
       }
       // rows of the row-major [H][F] down projection
-      s[0] = {(const unsigned char*)(Lp->wdT + (size_t)I.r0 * g.F), nullptr, (uint32_t)g.F * 2, n,
-              SBY / ((uint32_t)g.F * 2)};
+      s[0] = {(const unsigned char*)Lp->wdT + (size_t)I.r0 * g.F * WB, nullptr, (uint32_t)g.F * WB,
+              n, SBY / ((uint32_t)g.F * WB)};
       return 1;
     case OP_ATTN: {
       // slice s of S over positions [0, P]: [s*C/S, (s+1)*C/S), C = P + 1.
@@ -221,8 +223,8 @@ MK_DEV void norm_gain(NormGain<HT>& ng, const uint16_t* gain, int tid) {
 // Pass 3 turns every 16-column k-tile (512 bytes, k-major) into its 32 lanes'
 // fragments in place: lane 4g + t holds bf16 hi / lo of sequence g at
 // columns 2t, 2t+1 and 2t+8, 2t+9.
-template <int HT, int D, int HPG, int NB>
-MK_DEV bool norm_apply_batched(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j,
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool norm_apply_batched(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, int j,
                                const uint16_t* gain) {
   static_assert(NB == 8, "k-tile blocks of 16 columns x 8 sequences");
   constexpr int KPT = (HT + NCT - 1) / NCT;  // columns per thread
@@ -329,8 +331,8 @@ MK_DEV bool norm_apply_batched(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j,
   return true;
 }
 
-template <int HT, int D, int HPG, int NB>
-MK_DEV bool norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const NormGain<HT>& ng) {
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool norm_apply(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, int j, const NormGain<HT>& ng) {
   if constexpr (NB > 1) {
     return norm_apply_batched(c, g, j, ng.src);
   } else {
@@ -441,22 +443,37 @@ MK_DEV bool norm_apply(Ctx<HT, D, HPG, NB>& c, const Globals& g, int j, const No
 }
 
 // ----------------------------------------------------------------- GEMV ----
-// Lane l of a warp owns columns {it*256 + l*8 + k}; for NB == 1 its slice of
-// xn lives in registers.
-template <int HT>
+// Lane l of a warp owns the columns of its 16-byte chunks of a row: bf16
+// rows {it*256 + l*8 + k}, int8 rows {it*512 + l*16 + k}; for NB == 1 its
+// slice of xn lives in registers.
+template <int HT, int WB>
 MK_DEV void load_xr(const float* xn, int lane, float (&xr)[HT / 32]) {
+  if constexpr (WB == 1) {
 #pragma unroll
-  for (int it = 0; it < HT / 256; it++) {
-    const float4* p = (const float4*)(xn + it * 256 + lane * 8);
-    const float4 a = p[0], b = p[1];
-    xr[it * 8 + 0] = a.x; xr[it * 8 + 1] = a.y; xr[it * 8 + 2] = a.z; xr[it * 8 + 3] = a.w;
-    xr[it * 8 + 4] = b.x; xr[it * 8 + 5] = b.y; xr[it * 8 + 6] = b.z; xr[it * 8 + 7] = b.w;
+    for (int it = 0; it < HT / 512; it++) {
+      const float4* p = (const float4*)(xn + it * 512 + lane * 16);
+#pragma unroll
+      for (int q = 0; q < 4; q++) {
+        const float4 a = p[q];
+        xr[it * 16 + 4 * q] = a.x; xr[it * 16 + 4 * q + 1] = a.y;
+        xr[it * 16 + 4 * q + 2] = a.z; xr[it * 16 + 4 * q + 3] = a.w;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int it = 0; it < HT / 256; it++) {
+      const float4* p = (const float4*)(xn + it * 256 + lane * 8);
+      const float4 a = p[0], b = p[1];
+      xr[it * 8 + 0] = a.x; xr[it * 8 + 1] = a.y; xr[it * 8 + 2] = a.z; xr[it * 8 + 3] = a.w;
+      xr[it * 8 + 4] = b.x; xr[it * 8 + 5] = b.y; xr[it * 8 + 6] = b.z; xr[it * 8 + 7] = b.w;
+    }
   }
 }
 
-// Partial dot of one bf16 row (in shared memory) with the activation(s); the
-// caller reduces across the warp.
-template <int HT, int NB>
+// Partial dot of one row (in shared memory) with the activation(s); the
+// caller reduces across the warp.  int8 rows give the dot with the codes
+// (the caller applies the row's scale).
+template <int HT, int NB, int WB>
 MK_DEV void row_dot(const unsigned char* row, const float (&xr)[HT / 32], const float* xn,
                     int lane, int key, float (&acc)[NB]) {
   // the row is chunk-swizzled: this lane's chunk it*32 + lane sits at slot
@@ -464,7 +481,25 @@ MK_DEV void row_dot(const unsigned char* row, const float (&xr)[HT / 32], const 
   const uint4* w4 = (const uint4*)row;
   const int sl = lane ^ key;
   static_assert(NB == 1, "batched variants use the tensor-core GEMV");
-  {
+  if constexpr (WB == 1) {
+    // eight chains (element e of a word pair), two per packed FMA
+    float2 a[4];
+#pragma unroll
+    for (int k = 0; k < 4; k++) a[k] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int it = 0; it < HT / 512; it++) {
+      const uint4 w = w4[it * 32 + sl];
+      const float* x = xr + it * 16;
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int q = 0; q < 4; q++)
+#pragma unroll
+        for (int e = 0; e < 4; e += 2)
+          a[((4 * q + e) & 7) >> 1] = ffma2(i8_pair(ws[q], e), make_float2(x[4 * q + e], x[4 * q + e + 1]),
+                                           a[((4 * q + e) & 7) >> 1]);
+    }
+    acc[0] = ((a[0].x + a[0].y) + (a[1].x + a[1].y)) + ((a[2].x + a[2].y) + (a[3].x + a[3].y));
+  } else {
     // eight independent chains (one per element of a 16-byte chunk): the
     // dependent-FMA depth is HT/256 instead of HT/64
     float a[8];
@@ -487,8 +522,8 @@ MK_DEV void row_dot(const unsigned char* row, const float (&xr)[HT / 32], const 
 // Stream the rows of one segment through the ring; warp w computes rows
 // w, w + NCW, ... of each stage and hands (row index, per-sequence dot) to
 // fn on every lane.  Returns false if a wait gave up.
-template <int HT, int D, int HPG, int NB, class Fn>
-MK_DEV bool gemv_rows(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s,
+template <int HT, int D, int HPG, int NB, int WB, class Fn>
+MK_DEV bool gemv_rows(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Seg& s,
                       const float (&xr)[HT / 32], Fn&& fn) {
   float pend = 0.f;  // NB == 1: this lane's partial of the row not yet reduced
   int prow = -1;
@@ -504,13 +539,13 @@ MK_DEV bool gemv_rows(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s,
         // the previous row's cross-lane sum is issued in the same block as
         // this row's loads and FMAs, so its shuffle latency hides behind them
         float prev[1] = {warp_sum(pend)};
-        row_dot<HT, NB>(st + (size_t)r * HT * 2, xr, c.xn, c.lane, (int)((s.row0 + u0 + r) & 7u),
+        row_dot<HT, NB, WB>(st + (size_t)r * HT * WB, xr, c.xn, c.lane, (int)((s.row0 + u0 + r) & 7u),
                         acc);
         if (prow >= 0) fn((uint32_t)prow, prev);
         pend = acc[0];
         prow = (int)(u0 + r);
       } else {
-        row_dot<HT, NB>(st + (size_t)r * HT * 2, xr, c.xn, c.lane, (int)((s.row0 + u0 + r) & 7u),
+        row_dot<HT, NB, WB>(st + (size_t)r * HT * WB, xr, c.xn, c.lane, (int)((s.row0 + u0 + r) & 7u),
                         acc);
 #pragma unroll
         for (int b = 0; b < NB; b++) acc[b] = warp_sum(acc[b]);
@@ -541,8 +576,8 @@ MK_DEV bool gemv_rows(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s,
 // y) receives each output once.  Every warp runs the same loop and barriers;
 // a warp whose ring wait gave up stops touching the ring (it neither reads
 // nor releases stages) and the failure is broadcast, so all return alike.
-template <int HT, int D, int HPG, int NB, class Fe>
-MK_DEV bool gemv_rows_mma(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s, Fe&& fe) {
+template <int HT, int D, int HPG, int NB, int WB, class Fe>
+MK_DEV bool gemv_rows_mma(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Seg& s, Fe&& fe) {
   static_assert(NB > 1 && NB <= 8, "one m16n8k16 A tile holds up to 8 sequences");
   static_assert(NCT % NB == 0 && (NB & (NB - 1)) == 0, "a thread's outputs share one sequence");
   static_assert(MAX_STAGE_BYTES / (HT * 2) <= MMA_FLUSH, "a stage's rows fit one flush window");
@@ -610,8 +645,8 @@ MK_DEV bool gemv_rows_mma(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s
 // The GEMV of the row-dotted matrices: fe(row, b, y) is called exactly once
 // per output.  Batch 1 runs on the FP32 pipes (lane 0 of the row's warp
 // calls fe); batched variants run on the tensor cores.
-template <int HT, int D, int HPG, int NB, class Fe>
-MK_DEV bool gemv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Seg& s,
+template <int HT, int D, int HPG, int NB, int WB, class Fe>
+MK_DEV bool gemv(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Seg& s,
                  const float (&xr)[HT / 32], Fe&& fe) {
   if constexpr (NB > 1) {
     return gemv_rows_mma(c, g, s, fe);
@@ -631,8 +666,8 @@ namespace mk {
 // Rows [r0, r1) of the layer's packed QKV matrix, all inside kv head I.g's
 // group [q heads of the group][k][v]; inside a head, packed rows 2t and 2t+1
 // hold head dims t and t + D/2, so each rotary pair is produced by one SM.
-template <int HT, int D, int HPG, int NB>
-MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
   static_assert(MAX_ROWS <= 2 * NCT, "one rotary pair per thread");
   const LayerPtrs& Lp = g.layers[I.layer];
   const bool cached = (I.flags & F_NORM_CACHED) != 0;
@@ -645,7 +680,9 @@ MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   const uint32_t i = 2u * (uint32_t)c.tid;
   int hs = 0, t = 0;
   float2 cs[NB];
+  float2 rsc = make_float2(1.f, 1.f);  // int8: the pair's row scales
   if (i < n) {
+    if constexpr (WB == 1) rsc = *(const float2*)(Lp.sqkv + I.r0 + i);  // r0, i even
     const int lr = (int)(I.r0 + i) - (int)I.g * GR;
     hs = lr / D;
     t = (lr % D) >> 1;
@@ -658,9 +695,9 @@ MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   if (!cached && !norm_apply(c, g, 2 * I.layer, ng)) return false;
   c.mark(g, 0);
   float xr[HT / 32];
-  if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
+  if constexpr (NB == 1) load_xr<HT, WB>(c.xn, c.lane, xr);
   Seg s[2];
-  get_segs<HT, D>(g, I, c.pos, c.topk, s);
+  get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
   float* yrow = c.yrow;
   const int lane = c.lane;
   gemv(c, g, s[0], xr, [&](uint32_t r, int b, float y) { yrow[b * MAX_ROWS + r] = y; });
@@ -671,6 +708,10 @@ MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
     for (int b = 0; b < NB; b++) {
       if (b >= g.B) break;
       float y0 = yrow[b * MAX_ROWS + i], y1 = yrow[b * MAX_ROWS + i + 1];
+      if constexpr (WB == 1) {
+        y0 *= rsc.x;
+        y1 *= rsc.y;
+      }
       const int P = c.pos[b];
       if (hs <= HPG) {  // q heads and k: rotate (t, t + D/2) by P * theta^(-2t/D)
         const float a = y0 * cs[b].x - y1 * cs[b].y;
@@ -708,8 +749,8 @@ MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
 // and finally the CTA merge their states.
 constexpr float NEG_BIG = -1e30f;
 
-template <int HT, int D, int HPG, int NB>
-MK_DEV bool op_attn(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool op_attn(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
   constexpr int LPR = D / 8, SPW = 32 / LPR;
   const int slot = c.lane / LPR, dsl = c.lane % LPR;
   const int b = I.b, P = c.pos[b];
@@ -771,7 +812,7 @@ MK_DEV bool op_attn(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   };
   c.mark(g, 0);
   Seg s[2];
-  get_segs<HT, D>(g, I, c.pos, c.topk, s);
+  get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
   for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
     const uint32_t n = min(s[0].ups, s[0].n - u0);
     if (!c.ring.acquire(g)) break;
@@ -878,15 +919,22 @@ MK_DEV void merge_heads(C& c, const Globals& g, const float* pm, const float* pl
 // o = sum o_s 2^(m_s - M) / L), then rows [r0, r1) of Wo[:, h*D:(h+1)*D]
 // (packed [Hq][H][D]) are applied and accumulated into x_{2l+1} with float
 // atomics; the head-0 instructions also add the residual x_{2l}.
-template <int HT, int D, int HPG, int NB>
-MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
   constexpr int LPR = D / 8, SPW = 32 / LPR;
   constexpr int SG = (NCT / (NB * D)) > 0 ? NCT / (NB * D) : 1;  // slice groups per (b, dim)
   const int slot = c.lane / LPR, dsl = c.lane % LPR;
   const int h = I.g, l = I.layer;
   const int S = g.splits;
   constexpr int PS = part_stride(D);  // partial record stride
-  if (!dep_wait(c, g, I)) return false;
+  if constexpr (WB == 1) {
+    // int8: the Wo rows' scales, copied in while the wait runs
+    const float* so = g.layers[l].so + I.r0;
+    for (int t = c.tid; t < (int)(I.r1 - I.r0); t += NCT) cp_async4(c.sc + t, so + t);
+  }
+  const bool waited = dep_wait(c, g, I);
+  if constexpr (WB == 1) cp_async_wait_all();
+  if (!waited) return false;
   Seg s[2];
   bool staged = false;
   float* pm = c.yrow;                    // [NB][SG][D] partial max
@@ -900,7 +948,7 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
     // overlap them
     staged = g.part_staged != 0;
     if (staged) {
-      get_segs<HT, D>(g, I, c.pos, c.topk, s);
+      get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
       if (c.tid == 0) {
         asm volatile("fence.proxy.async.global;" ::: "memory");  // written by generic stores
         const uint64_t pol = policy_evict_normal();
@@ -1004,7 +1052,7 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   c.mark(g, 0);
   consumer_bar();
   if (c.flag[2]) return false;
-  if (!staged) get_segs<HT, D>(g, I, c.pos, c.topk, s);
+  if (!staged) get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
   const Seg& wseg = s[staged ? 1 : 0];  // the Wo rows
   const uint4 zero = make_uint4(0, 0, 0, 0);
   const int nr = (int)(I.r1 - I.r0);
@@ -1037,12 +1085,36 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
         const uint32_t j = blk * 32 + (uint32_t)c.lane;
         const bool valid = j < n;
         const uint32_t row = I.r0 + u0 + j;
-        const unsigned char* rp = st + (size_t)j * D * 2;
+        const unsigned char* rp = st + (size_t)j * D * WB;
         float a[8];
 #pragma unroll
         for (int e = 0; e < 8; e++) a[e] = 0.f;
+        if constexpr (WB == 1) {
+          // int8 rows of 64 codes, 4 chunks; chunk k of row r sits at slot
+          // k ^ ((r >> 1) & 3): 8 consecutive rows (two per 128 bytes) hit 8
+          // different bank groups
+          static_assert(D == 64 && REG, "int8 Wo rows hold 64 codes");
+          float2 a2[4];
 #pragma unroll
-        for (int k = 0; k < CPR; k++) {
+          for (int e = 0; e < 4; e++) a2[e] = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int k = 0; k < D / 16; k++) {
+            const uint4 w = valid ? *(const uint4*)(rp + ((k ^ ((row >> 1) & 3u)) * 16)) : zero;
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 16; e += 2)
+              a2[(e & 7) >> 1] = ffma2(i8_pair(ws[e >> 2], e & 3),
+                                       make_float2(av[k * 16 + e], av[k * 16 + e + 1]),
+                                       a2[(e & 7) >> 1]);
+          }
+#pragma unroll
+          for (int e = 0; e < 4; e++) {
+            a[2 * e] = a2[e].x;
+            a[2 * e + 1] = a2[e].y;
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < (WB == 1 ? 0 : CPR); k++) {
           const uint4 w = valid ? *(const uint4*)(rp + ((k ^ (row & 7u)) * 16)) : zero;
           float wf[8];
           unpack8(w, wf);
@@ -1060,6 +1132,7 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
         }
         if (valid) {
           float v = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+          if constexpr (WB == 1) v *= c.sc[row - I.r0];
           if (resid) v += xr_s[row - I.r0];
           red_add_f32(dst + row, v);
         }
@@ -1129,17 +1202,17 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
 }
 
 // ------------------------------------------------- OP_ROUTER (MoE only) ----
-template <int HT, int D, int HPG, int NB>
-MK_DEV bool op_router(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool op_router(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
   const LayerPtrs& Lp = g.layers[I.layer];
   NormGain<HT> ng;
   norm_gain(ng, Lp.mlp_norm, c.tid);
   if (!dep_wait(c, g, I)) return false;
   if (!norm_apply(c, g, 2 * I.layer + 1, ng)) return false;
   float xr[HT / 32];
-  if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
+  if constexpr (NB == 1) load_xr<HT, WB>(c.xn, c.lane, xr);
   Seg s[2];
-  get_segs<HT, D>(g, I, c.pos, c.topk, s);
+  get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
   float* rl = g.rlog + (size_t)I.layer * g.B * g.E + I.r0;
   const int E = g.E;
   gemv(c, g, s[0], xr, [&](uint32_t r, int b, float y) { rl[(size_t)b * E + r] = y; });
@@ -1198,8 +1271,8 @@ MK_DEV bool op_router(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
 // row per column) with float4 atomics; the instruction also adds x_{2l+1}
 // for its residual rows.  MoE: routed slices scale h by the slot's router
 // weight and read expert topk[slot]'s rows; shared slices use weight 1.
-template <int HT, int D, int HPG, int NB>
-MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
   const int l = I.layer;
   const LayerPtrs& Lp = g.layers[l];
   const bool routed = g.E > 0 && !(I.flags & F_SHARED);
@@ -1219,9 +1292,9 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
   }
   const float scale = routed ? c.topw[I.g] : 1.f;
   float xr[HT / 32];
-  if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
+  if constexpr (NB == 1) load_xr<HT, WB>(c.xn, c.lane, xr);
   Seg s[2];
-  get_segs<HT, D>(g, I, c.pos, c.topk, s);
+  get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
   float* yrow = c.yrow;
   const int lane = c.lane;
   gemv(c, g, s[0], xr, [&](uint32_t r, int b, float y) { yrow[b * MAX_ROWS + r] = y; });
@@ -1292,20 +1365,27 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
 // ------------------------------------- OP_MLP_UP (gate/up column slice) ----
 // h_c = SiLU(gate_c . xn) * (up_c . xn) for the slice's FFN columns, written
 // to the layer's h vector in global memory for the down instructions.
-template <int HT, int D, int HPG, int NB>
-MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
   const int l = I.layer;
   const LayerPtrs& Lp = g.layers[l];
   const bool cached = (I.flags & F_NORM_CACHED) != 0;
   NormGain<HT> ng;
   if (!cached) norm_gain(ng, Lp.mlp_norm, c.tid);
+  // int8: the gate / up row scales of this thread's FFN column (NB == 1:
+  // one column per thread)
+  float2 usc = make_float2(1.f, 1.f);
+  if constexpr (WB == 1) {
+    static_assert(NB == 1 && MAX_COLS <= NCT, "one column per thread");
+    if (c.tid < (int)(I.r1 - I.r0)) usc = *(const float2*)(Lp.sgu + 2 * (I.r0 + c.tid));
+  }
   if (!dep_wait(c, g, I)) return false;
   if (!cached && !norm_apply(c, g, 2 * l + 1, ng)) return false;
   c.mark(g, 0);
   float xr[HT / 32];
-  if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
+  if constexpr (NB == 1) load_xr<HT, WB>(c.xn, c.lane, xr);
   Seg s[2];
-  get_segs<HT, D>(g, I, c.pos, c.topk, s);
+  get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
   float* yrow = c.yrow;
   const int lane = c.lane;
   gemv(c, g, s[0], xr, [&](uint32_t r, int b, float y) { yrow[b * MAX_ROWS + r] = y; });
@@ -1343,7 +1423,11 @@ MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
     for (int t = c.tid; t < NB * ncol; t += NCT) {
       const int b = t / ncol, j = t % ncol;
       if (b < g.B) {
-        const float gt = yrow[b * MAX_ROWS + 2 * j], up = yrow[b * MAX_ROWS + 2 * j + 1];
+        float gt = yrow[b * MAX_ROWS + 2 * j], up = yrow[b * MAX_ROWS + 2 * j + 1];
+        if constexpr (WB == 1) {
+          gt *= usc.x;
+          up *= usc.y;
+        }
         g.hglob[((size_t)l * g.B + b) * g.F + I.r0 + j] = (gt / (1.f + expf(-gt))) * up;
       }
     }
@@ -1357,8 +1441,8 @@ MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
 // its 16-byte chunks of h in registers and dots them with the same chunks of
 // every down row streamed through the ring; per-warp partials meet in shared
 // memory.  Plain stores: no atomics, no other SM touches these rows.
-template <int HT, int D, int HPG, int NB>
-MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
   if constexpr (NB != 1) {
     // Batched (8 sequences): BD_ROWS rows.  Each ring stage holds, per
     // chunk of BD_KC columns, the rows' weight unit (lower half, chunk
@@ -1386,7 +1470,7 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I
     const uint32_t roff = (li + 8u * (mi >> 1)) * (BD_KC * 2u);
     float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
     Seg s[2];
-    get_segs<HT, D>(g, I, c.pos, c.topk, s);
+    get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
     const uint32_t SB = (uint32_t)g.stage_bytes;
     bool bad = false;
     for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
@@ -1430,23 +1514,25 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I
     consumer_bar();
     return true;
   } else {
-    constexpr int CPT = (DOWN_ROW_MAX / 16 + NCT - 1) / NCT;  // h chunks per thread
-    const int l = I.layer, F = g.F, nch = F / 8;
+    // a 16-byte chunk of a down row covers CW columns (8 bf16 or 16 int8)
+    constexpr int CW = 16 / WB;
+    constexpr int CPT = (DOWN_ROW_MAX / 2 / CW + NCT - 1) / NCT;  // h chunks per thread (F <= 8192)
+    const int l = I.layer, F = g.F, nch = F / CW;
     const int nrows = (int)(I.r1 - I.r0);
+    float dsc = 1.f;  // int8: this thread's output row scale
+    if constexpr (WB == 1)
+      if (c.tid < nrows) dsc = __ldg(g.layers[l].sd + I.r0 + c.tid);
     if (!dep_wait(c, g, I)) return false;
-    float h[CPT][8];
+    float h[CPT][CW];
     const float* hp = g.hglob + (size_t)l * F;
 #pragma unroll
     for (int q = 0; q < CPT; q++) {
       const int k = c.tid + q * NCT;
-      if (k < nch) {
-        const float4 a = __ldcg((const float4*)(hp + (size_t)k * 8));
-        const float4 b = __ldcg((const float4*)(hp + (size_t)k * 8) + 1);
-        h[q][0] = a.x; h[q][1] = a.y; h[q][2] = a.z; h[q][3] = a.w;
-        h[q][4] = b.x; h[q][5] = b.y; h[q][6] = b.z; h[q][7] = b.w;
-      } else {
 #pragma unroll
-        for (int e = 0; e < 8; e++) h[q][e] = 0.f;
+      for (int e4 = 0; e4 < CW / 4; e4++) {
+        const float4 a = k < nch ? __ldcg((const float4*)(hp + (size_t)k * CW) + e4)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        h[q][4 * e4] = a.x; h[q][4 * e4 + 1] = a.y; h[q][4 * e4 + 2] = a.z; h[q][4 * e4 + 3] = a.w;
       }
     }
     const float res = c.tid < nrows ? xres_sum(g, c.epoch, 2 * l + 1, 0, (int)I.r0 + c.tid) : 0.f;
@@ -1456,7 +1542,7 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I
     float pend = 0.f;
     int prow = -1;
     Seg s[2];
-    get_segs<HT, D>(g, I, c.pos, c.topk, s);
+    get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
     for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
       const uint32_t n = min(s[0].ups, s[0].n - u0);
       if (!c.ring.acquire(g)) break;
@@ -1467,13 +1553,24 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I
 #pragma unroll
         for (int q = 0; q < CPT; q++) {
           const int k = c.tid + q * NCT;
-          float w[8];
-          unpack8(k < nch ? *(const uint4*)(st + (size_t)j * F * 2 + (size_t)k * 16) : zero, w);
+          const uint4 wv = k < nch ? *(const uint4*)(st + (size_t)j * F * WB + (size_t)k * 16) : zero;
           float a0 = 0.f, a1 = 0.f;
+          if constexpr (WB == 1) {
+            const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+            float2 a01 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            a0 = fmaf(w[e], h[q][e], a0);
-            a1 = fmaf(w[e + 1], h[q][e + 1], a1);
+            for (int e = 0; e < 16; e += 2)
+              a01 = ffma2(i8_pair(ws[e >> 2], e & 3), make_float2(h[q][e], h[q][e + 1]), a01);
+            a0 = a01.x;
+            a1 = a01.y;
+          } else {
+            float w[8];
+            unpack8(wv, w);
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              a0 = fmaf(w[e], h[q][e], a0);
+              a1 = fmaf(w[e + 1], h[q][e + 1], a1);
+            }
           }
           a[q] = a0 + a1;
         }
@@ -1496,6 +1593,7 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I
       float y = 0.f;
 #pragma unroll
       for (int w = 0; w < NCW; w++) y += part[w * MAX_DOWN_ROWS + c.tid];
+      if constexpr (WB == 1) y *= dsc;
       st_tag(g.xt + (size_t)l * g.B * g.H + I.r0 + c.tid, res + y, c.epoch);
     }
     consumer_bar();
@@ -1506,8 +1604,8 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I
 // ------------------------------------ OP_LMHEAD (final norm + head rows) ----
 // Logits rows [r0, r1) and this slice's (max, first index); the slice that
 // arrives last on the argmax counter reduces all slices into argmax[b].
-template <int HT, int D, int HPG, int NB>
-MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) {
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
   if (g.zero_next) {
     // this slice's share of the next step's residual buffers (the other
     // parity): every step of this and earlier launches that read them is
@@ -1520,13 +1618,17 @@ MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   }
   NormGain<HT> ng;
   norm_gain(ng, g.final_norm, c.tid);
-  if (!dep_wait(c, g, I)) return false;
+  if constexpr (WB == 1)  // int8: the rows' scales (at most HT rows), copied in while the wait runs
+    for (int t = c.tid; t < (int)(I.r1 - I.r0); t += NCT) cp_async4(c.sc + t, g.lm_scale + I.r0 + t);
+  const bool waited = dep_wait(c, g, I);
+  if constexpr (WB == 1) cp_async_wait_all();
+  if (!waited) return false;
   if (!norm_apply(c, g, 2 * g.L, ng)) return false;
   c.mark(g, 0);
   float xr[HT / 32];
-  if constexpr (NB == 1) load_xr<HT>(c.xn, c.lane, xr);
+  if constexpr (NB == 1) load_xr<HT, WB>(c.xn, c.lane, xr);
   Seg s[2];
-  get_segs<HT, D>(g, I, c.pos, c.topk, s);
+  get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
   // each thread only ever sees one sequence, b = tid % NB (both GEMV paths);
   // it keeps that sequence's best (value, lowest row) of this slice
   float best = -INFINITY;
@@ -1534,7 +1636,9 @@ MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB>& c, const Globals& g, const Instr& I) 
   const int lane = c.lane, B = g.B, V = g.V;
   float* logits = g.logits;
   const uint32_t r0 = I.r0;
+  const float* rsc = c.sc;
   gemv(c, g, s[0], xr, [&](uint32_t r, int b, float y) {
+    if constexpr (WB == 1) y *= rsc[r];
     const int row = (int)(r0 + r);
     logits[(size_t)b * V + row] = y;
     if (y > best || (y == best && row < bidx)) {
@@ -1636,7 +1740,7 @@ MK_DEV bool selected(const Globals& g, const Instr& I) {
 // prefetches are per-line LSU prefetches spread over the producer warp's 32
 // lanes (the TMA engine stays free for the ring copies); every lane runs the
 // cursor in lockstep.
-template <int HT, int D, int NB>
+template <int HT, int D, int NB, int WB>
 struct L2Cursor {
   int pc = 0, k = 0, nseg = 0;
   uint32_t u0 = 0;
@@ -1678,7 +1782,7 @@ struct L2Cursor {
           }
           pos[I.b] = P;
         }
-        nseg = get_segs<HT, D>(g, I, pos, ptopk, s);
+        nseg = get_segs<HT, D, WB>(g, I, pos, ptopk, s);
         k = 0;
         u0 = 0;
         pc++;
@@ -1712,7 +1816,7 @@ struct L2Cursor {
 // instruction issues its later stages only once the consumers have finished
 // the instructions before it.  On any error it stops issuing and waits for
 // its copies in flight before the CTA may exit.
-template <int HT, int D, int HPG, int NB>
+template <int HT, int D, int HPG, int NB, int WB>
 MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint32_t empty0,
                      int* ppos, int* ptopk, float* ptopw, const int* done, int lane) {
   const uint64_t pol_w = policy_evict_first();
@@ -1726,7 +1830,7 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
   int routed_layer = -1;
   int seq = 0;  // instructions of this launch before the current one (consumer order)
   unsigned long long issued_bytes = 0;
-  L2Cursor<HT, D, NB> l2;
+  L2Cursor<HT, D, NB, WB> l2;
   int t = 0;               // step of this launch: the queue runs once per step
   uint32_t ep = g.epoch;   // its epoch
   bool step_ready = true;  // this step's copies may read rows written by earlier steps
@@ -1784,7 +1888,7 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
     }
     __syncwarp();
     Seg s[2];
-    const int nseg = get_segs<HT, D>(g, I, ppos, ptopk, s);
+    const int nseg = get_segs<HT, D, WB>(g, I, ppos, ptopk, s);
     const int my_seq = seq++;
     // a held instruction: stages from hold_k on wait until the consumers
     // have finished (and signalled) every earlier instruction of this launch
@@ -1978,10 +2082,10 @@ drain:
   }
 }
 
-template <int HT, int D, int HPG, int NB>
+template <int HT, int D, int HPG, int NB, int WB>
 __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_constant__ Globals g) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  const SmemLayout Ls = smem_layout(g.n_stages, g.stage_bytes, NB, HT, D, HPG, g.K);
+  const SmemLayout Ls = smem_layout(g.n_stages, g.stage_bytes, NB, HT, D, HPG, g.K, WB);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t full0 = smem_u32(smem + Ls.full), empty0 = smem_u32(smem + Ls.empty);
   const int KM = g.K > 0 ? g.K : 1;
@@ -2007,20 +2111,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
   __syncthreads();
 
   if (warp == NCW) {
-    producer<HT, D, HPG, NB>(g, smem + Ls.ring, full0, empty0, ppos, ptopk, ptopw, misc + 1,
+    producer<HT, D, HPG, NB, WB>(g, smem + Ls.ring, full0, empty0, ppos, ptopk, ptopw, misc + 1,
                              lane);
     return;
   }
 
   // ---- consumers
   if (g.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
-  Ctx<HT, D, HPG, NB> c;
+  Ctx<HT, D, HPG, NB, WB> c;
   c.xn = (float*)(smem + Ls.xn);
   c.yrow = (float*)(smem + Ls.yrow);
   c.hbuf = (float*)(smem + Ls.hbuf);
   c.mpart = (float*)(smem + Ls.mpart);
   c.attn = (float*)(smem + Ls.attn);
   c.red = (float*)(smem + Ls.red);
+  c.sc = WB == 1 ? (float*)(smem + Ls.sc) : nullptr;
   c.tok = tok;
   c.pos = pos;
   c.topk = topk;

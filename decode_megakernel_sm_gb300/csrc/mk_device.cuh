@@ -178,6 +178,45 @@ MK_DEV void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// 4-byte asynchronous global -> shared copy (the LSU path, not the bulk-copy
+// engine); cp_async_wait_all waits for this thread's copies.
+MK_DEV void cp_async4(float* sdst, const float* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(sdst)), "l"(gsrc)
+               : "memory");
+}
+MK_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Two fp32 lanes in one 64-bit register, and the packed f32x2 arithmetic of
+// sm_100+ (two IEEE fp32 operations per instruction, each rounded as the
+// scalar one).
+MK_DEV unsigned long long f2_bits(float2 v) {
+  return ((unsigned long long)__float_as_uint(v.y) << 32) | __float_as_uint(v.x);
+}
+MK_DEV float2 bits_f2(unsigned long long u) {
+  return make_float2(__uint_as_float((uint32_t)u), __uint_as_float((uint32_t)(u >> 32)));
+}
+MK_DEV float2 ffma2(float2 a, float2 b, float2 c) {  // a * b + c
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+  return bits_f2(d);
+}
+MK_DEV float2 fadd2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
+
+// int8 weight codes, stored biased by 128 (byte u = q + 128, 1..255).  Byte
+// k of a word as the low mantissa byte of 2^23 (bits 0x4B0000uu) is exactly
+// 2^23 + u; subtracting 2^23 + 128 leaves q exactly.  i8_pair gives codes
+// k, k + 1 of a word: two byte permutes and one packed add.
+MK_DEV float2 i8_pair(uint32_t biased, int k) {
+  const float2 m = make_float2(
+      __uint_as_float(__byte_perm(biased, 0x4B000000u, 0x7440u | (uint32_t)k)),
+      __uint_as_float(__byte_perm(biased, 0x4B000000u, 0x7440u | (uint32_t)(k + 1))));
+  return fadd2(m, make_float2(-8388736.f, -8388736.f));
+}
+
 MK_DEV void unpack8(const uint4& w, float* f) {
   f[0] = bf_lo(w.x); f[1] = bf_hi(w.x);
   f[2] = bf_lo(w.y); f[3] = bf_hi(w.y);

@@ -169,6 +169,14 @@ struct LayerPtrs {
   const uint16_t* sh_dT;      // MoE:   [Fs][H]
   uint16_t* kc;               // caller cache [maxB][Hkv][max_seq][D]
   uint16_t* vc;
+  // int8 weights (dense batch 1): wqkv, wo, wgu, wdT then hold int8 codes,
+  // biased by 128 (byte q + 128), in the same layouts (Wo: chunk k of row r
+  // at slot k ^ ((r >> 1) & 3)), and these fp32 scales, one per packed row,
+  // multiply each row's dot product
+  const float* sqkv;          // [Hkv][(HPG+2)*D], packed row order
+  const float* so;            // [H]: Wo output row r (shared by every head's piece)
+  const float* sgu;           // [F][2]: gate row c, up row c
+  const float* sd;            // [H]: down output row
 };
 
 // A value that one writer produces once per step, with that step's tag
@@ -183,7 +191,8 @@ struct Globals {
   const Instr* sched;
   const LayerPtrs* layers;
   const uint16_t* embed;
-  const uint16_t* lm_head;
+  const uint16_t* lm_head;    // int8 weights: biased int8 codes [V][H], scales lm_scale [V]
+  const float* lm_scale;
   const uint16_t* final_norm;
   const float* rope;       // [max_seq][D/2][2] (cos, sin)
   float* xbuf;             // [2][2L][kc][B][H] residual stream x_1 .. x_2L, kc partial copies
@@ -236,11 +245,12 @@ struct Globals {
 
 // Shared-memory layout (bytes from the dynamic shared memory base).
 struct SmemLayout {
-  int ring, full, empty, xn, yrow, hbuf, attn, red, misc, mpart, total;
+  int ring, full, empty, xn, yrow, hbuf, attn, red, misc, mpart, sc, total;
 };
 
+// WB: bytes per weight (2 bf16, 1 int8; int8 adds the row-scale region sc)
 MK_HD inline SmemLayout smem_layout(int n_stages, int stage_bytes, int NB, int H, int D, int HPG,
-                                     int K) {
+                                     int K, int WB) {
   SmemLayout s;
   int o = 0;
   s.ring = o;   o += n_stages * stage_bytes;
@@ -258,14 +268,15 @@ MK_HD inline SmemLayout smem_layout(int n_stages, int stage_bytes, int NB, int H
   s.misc = o;   o += 4 * (8 + 3 * NB + 4 * NB * (K > 0 ? K : 1));
   o = (o + 15) / 16 * 16;
   s.mpart = o;  o += NB > 1 ? 4 * NCW * MMA_FLUSH * NB : 0;  // batched GEMV partial sums
+  s.sc = o;     o += WB == 1 ? 4 * H : 0;  // row scales of one O-proj / LM-head instruction
   s.total = (o + 127) / 128 * 128;
   return s;
 }
 
 // One compiled instantiation of the interpreter.
 struct Variant {
-  int H, D, HPG, NB;
-  const void* kernel;  // host stub of mk_decode_kernel<H, D, HPG, NB>
+  int H, D, HPG, NB, WB;  // WB: bytes per weight, 2 (bf16) or 1 (int8 codes)
+  const void* kernel;     // host stub of mk_decode_kernel<H, D, HPG, NB, WB>
 };
 
 // A built schedule: queues [n_sm][max_pc] (HALT-padded) and their statistics.
@@ -275,8 +286,9 @@ struct PlanOut {
   double max_sm_bytes = 0, mean_sm_bytes = 0, weight_bytes = 0;
 };
 int plan_shape_ok(const mk_model_desc& d);
+// wb: bytes per weight of the packed matrices (2 bf16, 1 int8)
 int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& out,
-               unsigned hold_mask = DEFAULT_HOLD);
+               unsigned hold_mask = DEFAULT_HOLD, int wb = 2);
 int plan_verify(const mk_model_desc& d, int B, const PlanOut& p);
 int plan_check(const Instr* q, int n_sm, int max_pc, int n_ctr);
 

@@ -18,6 +18,15 @@
 //         2..8 sequences, F a multiple of 512: units of 16 rows x 512 columns,
 //         16-byte chunk q of unit row i at slot q ^ (i & 7);
 //         otherwise [F][H], transposed (one contiguous row per FFN column)
+//
+// int8 weights (dense batch-1 shapes): every matrix is first quantised per
+// row (quantize_rows_kernel), then the codes take the same layouts with
+// 16-byte chunks of 16 codes (a row of H codes is H / 16 chunks, swizzled
+// the same way), except Wo, whose 64-code head rows are 4 chunks: chunk c of
+// row r sits at slot c ^ ((r >> 1) & 3).  The packed codes are stored
+// biased by 128 (byte q + 128; bias_codes), which the kernel's decode
+// expects.  The fp32 row scales follow their rows (QKV: packed row order;
+// gate/up: interleaved).
 #include <cuda_runtime.h>
 
 #include "mk_internal.h"
@@ -140,6 +149,121 @@ cudaError_t pack_transpose(uint16_t* dst, const void* src, int R, int C, int bat
   if (R <= 0 || C <= 0 || batch <= 0) return cudaSuccess;
   dim3 grid((C + 31) / 32, (R + 31) / 32, batch);
   transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(dst, (const uint16_t*)src, R, C);
+  return cudaGetLastError();
+}
+
+// Symmetric per-row int8 quantisation of a bf16 matrix [rows][cols], the
+// "INT8 experts" of the Gemma 4 TPU megakernel page ("What's next") applied
+// to every streamed matrix: with m = max_k |w[r][k]|, the scale is
+// s = m / 127 and the code q = round-half-even(w / s) in [-127, 127], both
+// divisions correctly rounded in fp32 (a zero row: s = 0, codes 0), so that
+// w ~ q * s.  One block per row.
+__global__ void quantize_rows_kernel(int8_t* __restrict__ codes, float* __restrict__ scales,
+                                     const uint16_t* __restrict__ w, int cols) {
+  __shared__ float red[32];
+  const size_t r = blockIdx.x;
+  const uint16_t* src = w + r * (size_t)cols;
+  float m = 0.f;
+  for (int k = threadIdx.x; k < cols; k += blockDim.x)
+    m = fmaxf(m, fabsf(__uint_as_float((uint32_t)src[k] << 16)));
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (threadIdx.x == 0) red[0] = m;
+  }
+  __syncthreads();
+  const float s = red[0] > 0.f ? __fdiv_rn(red[0], 127.f) : 0.f;
+  int8_t* dst = codes + r * (size_t)cols;
+  for (int k = threadIdx.x; k < cols; k += blockDim.x) {
+    int q = 0;
+    if (s > 0.f) {
+      q = __float2int_rn(__fdiv_rn(__uint_as_float((uint32_t)src[k] << 16), s));
+      q = min(127, max(-127, q));
+    }
+    dst[k] = (int8_t)q;
+  }
+  if (threadIdx.x == 0) scales[r] = s;
+}
+
+cudaError_t quantize_rows_int8(int8_t* codes, float* scales, const void* w, long rows, int cols,
+                               cudaStream_t s) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  quantize_rows_kernel<<<(unsigned)rows, 256, 0, s>>>(codes, scales, (const uint16_t*)w, cols);
+  return cudaGetLastError();
+}
+
+// Row scales of the packed QKV rows (the row order of pack_qkv_kernel).
+__global__ void pack_qkv_scales_kernel(float* __restrict__ dst, const float* __restrict__ sq,
+                                       const float* __restrict__ sk, const float* __restrict__ sv,
+                                       int HPG, int D, int n) {
+  const int p = blockIdx.x * blockDim.x + threadIdx.x;
+  if (p >= n) return;
+  const int GR = (HPG + 2) * D;
+  const int g = p / GR, lr = p % GR, hs = lr / D, e = lr % D;
+  const int dim = (e & 1) ? (e >> 1) + D / 2 : (e >> 1);
+  dst[p] = hs < HPG ? sq[(g * HPG + hs) * D + dim] : hs == HPG ? sk[g * D + dim] : sv[g * D + dim];
+}
+
+cudaError_t pack_qkv_scales(float* dst, const float* sq, const float* sk, const float* sv, int Hkv,
+                            int HPG, int D, cudaStream_t s) {
+  const int n = Hkv * (HPG + 2) * D;
+  pack_qkv_scales_kernel<<<(n + 255) / 256, 256, 0, s>>>(dst, sq, sk, sv, HPG, D, n);
+  return cudaGetLastError();
+}
+
+// dst[2c] = a[c], dst[2c + 1] = b[c]: gate / up row scales.
+__global__ void interleave_scales_kernel(float* __restrict__ dst, const float* __restrict__ a,
+                                         const float* __restrict__ b, int n) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c < n) {
+    dst[2 * c] = a[c];
+    dst[2 * c + 1] = b[c];
+  }
+}
+
+cudaError_t interleave_scales(float* dst, const float* a, const float* b, int n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  interleave_scales_kernel<<<(n + 255) / 256, 256, 0, s>>>(dst, a, b, n);
+  return cudaGetLastError();
+}
+
+// int8 Wo codes [H][Hq*64] -> [Hq][H][64]: chunk c of head row r at slot
+// c ^ ((r >> 1) & 3) (4 chunks of 16 codes per row).
+__global__ void pack_wo_i8_kernel(uint4* __restrict__ dst, const uint4* __restrict__ wo, int H,
+                                  int Hq) {
+  const size_t total = (size_t)Hq * H * 4;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t slot = i % 4, hr = i / 4;
+    const size_t r = hr % H, h = hr / H;
+    dst[i] = wo[(r * Hq + h) * 4 + (slot ^ ((r >> 1) & 3))];
+  }
+}
+
+cudaError_t pack_wo_i8(void* dst, const void* wo_codes, int H, int Hq, cudaStream_t s) {
+  pack_wo_i8_kernel<<<2048, 256, 0, s>>>((uint4*)dst, (const uint4*)wo_codes, H, Hq);
+  return cudaGetLastError();
+}
+
+// Two's complement int8 codes -> biased bytes q + 128 (flip each top bit), in place.
+__global__ void bias_codes_kernel(uint4* __restrict__ p, size_t n) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    uint4 v = p[i];
+    v.x ^= 0x80808080u;
+    v.y ^= 0x80808080u;
+    v.z ^= 0x80808080u;
+    v.w ^= 0x80808080u;
+    p[i] = v;
+  }
+}
+
+cudaError_t bias_codes(void* p, size_t bytes, cudaStream_t s) {
+  if (bytes == 0) return cudaSuccess;
+  bias_codes_kernel<<<2048, 256, 0, s>>>((uint4*)p, bytes / 16);
   return cudaGetLastError();
 }
 

@@ -43,11 +43,15 @@ int plan_shape_ok(const mk_model_desc& d) {
 }
 
 int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& out,
-               unsigned hold_mask) {
+               unsigned hold_mask, int wb) {
   int rc = plan_shape_ok(d);
   if (rc) return rc;
   if (B <= 0 || B > d.max_batch || max_ctx <= 0 || max_ctx > d.max_seq || n_sm <= 0)
     return MK_ERR_INVALID_ARG;
+  if (wb != 1 && wb != 2) return MK_ERR_INVALID_ARG;
+  // int8 weights: an LM-head instruction's row scales fit the kernel's
+  // hidden-sized scale buffer
+  if (wb == 1 && ((long)d.vocab + n_sm - 1) / n_sm > d.hidden) return MK_ERR_UNSUPPORTED;
   const int L = d.n_layers, H = d.hidden, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
   const int D = d.head_dim, HPG = Hq / Hkv, V = d.vocab;
   const bool moe = d.n_experts > 0;
@@ -113,7 +117,7 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
         if (l > 0 && mlp_split(d)) I.flags |= F_TAG_WAIT;
         I.sig_ctr = cm.qkv(l, (int)g);
         qs[i].push_back(I);
-        bytes[i] += (double)(e - a) * H * 2;
+        bytes[i] += (double)(e - a) * H * wb;
         first = false;
         a = e;
       }
@@ -159,7 +163,7 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
         I.wait_ctr = cm.attn(l, (int)(h / HPG));
         I.sig_ctr = cm.oproj(l);
         qs[i].push_back(I);
-        bytes[i] += (double)(e - a) * D * 2;
+        bytes[i] += (double)(e - a) * D * wb;
         a = e;
       }
     }
@@ -204,7 +208,7 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
           I.wait_ctr = cm.oproj(l);
           I.sig_ctr = cm.mlp_up(l);
           qs[i].push_back(I);
-          bytes[i] += (double)(e - a) * H * 4;
+          bytes[i] += (double)(e - a) * H * 2 * wb;
           first = false;
           a = e;
         }
@@ -223,7 +227,7 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
           I.wait_ctr = cm.mlp_up(l);
           I.sig_ctr = cm.mlp(l);
           qs[i].push_back(I);
-          bytes[i] += (double)(e - a) * F * 2;
+          bytes[i] += (double)(e - a) * F * wb;
           a = e;
         }
       }
@@ -302,7 +306,7 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
     if (mlp_split(d)) I.flags |= F_TAG_WAIT;
     I.aux = (uint32_t)n_lm++;
     qs[i].push_back(I);
-    bytes[i] += (double)(b - a) * H * 2;
+    bytes[i] += (double)(b - a) * H * wb;
   }
 
   // ---- hold marks: the first instruction of each run of a held op on an SM
@@ -356,9 +360,12 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
   out.max_sm_bytes = m;
   out.mean_sm_bytes = sum / n_sm;
   const double router_rows = moe ? (double)d.n_experts : 0.0;
-  out.weight_bytes = (double)L * ((double)R * H * 2 + (double)Hq * D * H * 2 +
-                                  router_rows * H * 2 + (double)Fv * H * 6 + 2.0 * H * 2) +
-                     (double)V * H * 2 + (double)H * 2;
+  // weights read per step (int8: codes plus one fp32 scale per row; the
+  // norm gains stay bf16)
+  out.weight_bytes = (double)L * ((double)R * H * wb + (double)Hq * D * H * wb +
+                                  router_rows * H * wb + (double)Fv * H * 3 * wb + 2.0 * H * 2) +
+                     (double)V * H * wb + (double)H * 2;
+  if (wb == 1) out.weight_bytes += 4.0 * ((double)L * ((double)R + 2.0 * H + 2.0 * Fv) + V);
   return MK_OK;
 }
 

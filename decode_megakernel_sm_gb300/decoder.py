@@ -46,9 +46,12 @@ class Decoder:
     weights: dict as produced by ``synth.make_weights`` (bf16, [out][in]);
     kcache / vcache: per-layer bf16 tensors [max_batch][Hkv][max_seq][head_dim]."""
 
-    def __init__(self, cfg: dict, weights: dict, kcache, vcache, max_batch=None, max_seq=None):
+    def __init__(self, cfg: dict, weights: dict, kcache, vcache, max_batch=None, max_seq=None,
+                 weight_format: str = "bf16"):
         """kcache / vcache may also be paged pools [n_blocks][Hkv][block][head_dim]:
-        then pass max_batch and max_seq, and call set_kv_pages before the first step."""
+        then pass max_batch and max_seq, and call set_kv_pages before the first step.
+        weight_format "int8": the library quantises every streamed matrix per row
+        (mk_create_ex with MK_WEIGHTS_INT8)."""
         if max_batch is None or max_seq is None:
             max_batch, _, max_seq, _ = kcache[0].shape
         self.cfg = cfg
@@ -72,7 +75,9 @@ class Decoder:
         self._arrays += [ka, va]
         kv = L.mk_kv(C.cast(ka, C.POINTER(C.c_void_p)), C.cast(va, C.POINTER(C.c_void_p)))
         self.kcache, self.vcache = kcache, vcache  # the library writes row P in place
-        self.h = L.mk_create(self.desc, w, kv)
+        fmt = {"bf16": L.MK_WEIGHTS_BF16, "int8": L.MK_WEIGHTS_INT8}[weight_format]
+        self.weight_format = weight_format
+        self.h = L.mk_create_ex(self.desc, w, kv, fmt)
         self.batch = 0
 
     # -- schedule ---------------------------------------------------------

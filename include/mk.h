@@ -105,6 +105,39 @@ typedef struct {
  * On error *out is NULL and nothing is leaked.                            */
 int mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv, mk_handle** out);
 
+/* Weight formats of mk_create_ex. */
+#define MK_WEIGHTS_BF16 0 /* as mk_create */
+#define MK_WEIGHTS_INT8 1 /* int8 codes with one fp32 scale per row           */
+
+/* mk_create with a choice of streamed weight format (the survey's "INT8 /
+ * FP8 weights" next step; "Gemma 4 TPU megakernel", section "What's next":
+ * the same kernel reaches a higher rate with INT8 experts, because decode is
+ * bound by the weight bytes it reads).  The caller still passes bf16 weights.
+ * MK_WEIGHTS_INT8 quantises every streamed matrix on the device, row by row,
+ * exactly as mk_quantize_rows_int8 does: QKV, O-projection, gate, up, down
+ * and the LM head (with a tied head, an int8 copy of the embedding; the
+ * token gather still reads the bf16 embedding).  Norm gains and the KV cache
+ * stay bf16.  The step then computes y[r] = s[r] * sum_k q[r][k] * x[k] for
+ * every such matrix; everything else is as with bf16 weights.
+ * An int8 handle starts with a ring of at most 4 stages (mk_set_ring_depth
+ * changes it).  Supported: dense models with batch capacity 1 (max_batch ==
+ * 1), hidden 2048, head_dim 64, 4 query heads per kv head, ffn a multiple
+ * of 16 and at most 8192, vocab at most hidden x (SM count);
+ * MK_ERR_UNSUPPORTED otherwise.  Errors and ownership as mk_create.       */
+int mk_create_ex(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv,
+                 int weight_format, mk_handle** out);
+
+/* The row quantiser of MK_WEIGHTS_INT8, on its own.  d_w: device bf16
+ * [rows][cols]; d_codes: device int8 [rows][cols]; d_scales: device fp32
+ * [rows] (all caller-owned).  Per row: m = max |w|, s = m / 127, q =
+ * round-half-even(w / s) clamped to [-127, 127], both divisions correctly
+ * rounded in fp32; a row of zeros gets s = 0 and codes 0.  Weights must be
+ * finite.  Asynchronous on `stream` (a cudaStream_t, NULL: the default
+ * stream).  MK_ERR_INVALID_ARG for negative rows, cols <= 0 or NULL
+ * pointers; MK_ERR_CUDA if the launch fails.                              */
+int mk_quantize_rows_int8(const void* d_w, long rows, int cols, int8_t* d_codes, float* d_scales,
+                          void* stream);
+
 /* Paged KV cache (the survey's "paged KV cache" next step; the blocks of
  * vLLM-style serving).  From the next step on, kv->k[l] / kv->v[l] given to
  * mk_create point at pools [n_blocks][n_kv_heads][block][head_dim] (bf16,

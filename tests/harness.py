@@ -28,7 +28,7 @@ ROUTE_TIE = 1e-4
 class Run:
     def __init__(self, cfg: dict, seed: int = 0, max_ctx: int | None = None,
                  stage_bytes: int | None = None, hold: tuple | None = None,
-                 paged: int | None = None):
+                 paged: int | None = None, int8: bool = False):
         cfg = cfg if "max_seq" in cfg else synth.with_cache(cfg)
         self.cfg = cfg
         self.W = synth.make_weights(cfg, seed, "cuda")
@@ -37,7 +37,10 @@ class Run:
         torch.cuda.synchronize()
         self.ko = [oracle._bits(t.cpu()).copy() for t in self.ks]
         self.vo = [oracle._bits(t.cpu()).copy() for t in self.vs]
-        self.om = oracle.OracleModel(cfg, self.W)
+        # int8: each side quantises the same bf16 weights itself (the library
+        # on the device, the oracle on the host)
+        self.om = oracle.OracleModel(cfg, self.W, int8=int8)
+        fmt = "int8" if int8 else "bf16"
         self.paged = paged
         if paged:
             # the same rows in pools of `paged`-row blocks, at shuffled block
@@ -45,10 +48,10 @@ class Run:
             B, Hkv, S, D = self.ks[0].shape
             pk, pv, self.table = synth.paged_pools(self.ks, self.vs, paged, seed)
             self.pk, self.pv = pk, pv
-            self.dec = Decoder(cfg, self.W, pk, pv, max_batch=B, max_seq=S)
+            self.dec = Decoder(cfg, self.W, pk, pv, max_batch=B, max_seq=S, weight_format=fmt)
             self.dec.set_kv_pages(paged, self.table)
         else:
-            self.dec = Decoder(cfg, self.W, self.ks, self.vs)
+            self.dec = Decoder(cfg, self.W, self.ks, self.vs, weight_format=fmt)
         if stage_bytes is not None:
             self.dec.set_stage_bytes(stage_bytes)
         if hold is not None:
