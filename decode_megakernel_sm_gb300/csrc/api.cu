@@ -244,6 +244,7 @@ static int size_ring(mk_handle* h, int stage_bytes) {
 }
 
 static int pack_int8(mk_handle* h, const mk_weights* w, const mk_kv* kv, cudaStream_t s);
+static int pack_bf16(mk_handle* h, const mk_weights* w, const mk_kv* kv, cudaStream_t s);
 
 static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv,
                        mk_handle* h, int wfmt) {
@@ -258,8 +259,7 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
   h->wfmt = wfmt;
   h->var = pick_variant(d, wfmt == MK_WEIGHTS_INT8 ? 1 : 2);
   if (!h->var) return MK_ERR_UNSUPPORTED;
-  const int L = d.n_layers, H = d.hidden, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
-  const int D = d.head_dim, HPG = Hq / Hkv;
+  const int L = d.n_layers, D = d.head_dim;
   const bool moe = d.n_experts > 0;
   // ---- argument checks (pointers present and 16-byte aligned)
   if (!w || !kv || !kv->k || !kv->v || !w->embed || !w->final_norm || !w->attn_norm || !w->wq ||
@@ -303,7 +303,33 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
     rc = pack_int8(h, w, kv, s);
     if (rc) return rc;
   } else {
-  // ---- packed weight buffer
+    rc = pack_bf16(h, w, kv, s);
+    if (rc) return rc;
+  }
+  CK(cudaMalloc(&h->layers_d, sizeof(LayerPtrs) * L));
+  CK(cudaMemcpyAsync(h->layers_d, h->layers_h.data(), sizeof(LayerPtrs) * L,
+                     cudaMemcpyHostToDevice, s));
+  // rotary table: angle p * theta^(-2t/D) evaluated in double, stored fp32
+  std::vector<float> rope((size_t)d.max_seq * D);
+  for (int pp = 0; pp < d.max_seq; pp++)
+    for (int t = 0; t < D / 2; t++) {
+      const double ang = (double)pp * std::pow((double)d.rope_theta, -2.0 * t / (double)D);
+      rope[((size_t)pp * (D / 2) + t) * 2 + 0] = (float)std::cos(ang);
+      rope[((size_t)pp * (D / 2) + t) * 2 + 1] = (float)std::sin(ang);
+    }
+  CK(cudaMalloc(&h->rope, rope.size() * sizeof(float)));
+  CK(cudaMemcpyAsync(h->rope, rope.data(), rope.size() * sizeof(float), cudaMemcpyHostToDevice,
+                     s));
+  CK(cudaStreamSynchronize(s));
+  return MK_OK;
+}
+
+// bf16 packing: every matrix re-laid out for the ring (the layouts in pack.cu).
+static int pack_bf16(mk_handle* h, const mk_weights* w, const mk_kv* kv, cudaStream_t s) {
+  const mk_model_desc& d = h->d;
+  const int L = d.n_layers, H = d.hidden, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
+  const int D = d.head_dim, HPG = Hq / Hkv;
+  const bool moe = d.n_experts > 0;
   const LayerSizes ls = layer_sizes(d);
   const size_t V = d.vocab;
   size_t per_layer = 0;
@@ -383,22 +409,6 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
   uint16_t* fn = take(H);
   CK(cudaMemcpyAsync(fn, w->final_norm, (size_t)H * 2, cudaMemcpyDeviceToDevice, s));
   h->final_norm = fn;
-  }  // bf16 weights
-  CK(cudaMalloc(&h->layers_d, sizeof(LayerPtrs) * L));
-  CK(cudaMemcpyAsync(h->layers_d, h->layers_h.data(), sizeof(LayerPtrs) * L,
-                     cudaMemcpyHostToDevice, s));
-  // rotary table: angle p * theta^(-2t/D) evaluated in double, stored fp32
-  std::vector<float> rope((size_t)d.max_seq * D);
-  for (int pp = 0; pp < d.max_seq; pp++)
-    for (int t = 0; t < D / 2; t++) {
-      const double ang = (double)pp * std::pow((double)d.rope_theta, -2.0 * t / (double)D);
-      rope[((size_t)pp * (D / 2) + t) * 2 + 0] = (float)std::cos(ang);
-      rope[((size_t)pp * (D / 2) + t) * 2 + 1] = (float)std::sin(ang);
-    }
-  CK(cudaMalloc(&h->rope, rope.size() * sizeof(float)));
-  CK(cudaMemcpyAsync(h->rope, rope.data(), rope.size() * sizeof(float), cudaMemcpyHostToDevice,
-                     s));
-  CK(cudaStreamSynchronize(s));
   return MK_OK;
 }
 
