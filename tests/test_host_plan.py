@@ -245,3 +245,29 @@ def test_default_hold_marks_gate_up_and_down():
         for k, I in enumerate(run):
             first = k > 0 and (run[k - 1].op != I.op or run[k - 1].layer != I.layer)
             assert bool(I.flags & 8) == (first and I.op in (8, 9)), (sm, k, I.op)
+
+
+# ---- int8 weights: argument checks taken before any CUDA call
+def test_create_ex_refuses_bad_format_and_unsupported_int8_shapes():
+    lib = L.lib()
+    zero_w, zero_kv = L.mk_weights(), L.mk_kv()
+    h = C.c_void_p()
+    _, d = desc("llama1b_1k")
+    assert lib.mk_create_ex(C.byref(d), C.byref(zero_w), C.byref(zero_kv), 7,
+                            C.byref(h)) == L.MK_ERR_INVALID_ARG
+    assert h.value is None
+    for name, over in (("llama1b_b8", {}), ("moe", {}), ("llama1b_1k", {"ffn": 2056}),
+                       ("llama1b_1k", {"head_dim": 128, "n_q_heads": 16})):
+        _, d = desc(name, **over)
+        assert lib.mk_create_ex(C.byref(d), C.byref(zero_w), C.byref(zero_kv),
+                                L.MK_WEIGHTS_INT8, C.byref(h)) == L.MK_ERR_UNSUPPORTED, name
+
+
+def test_quantize_rows_refuses_bad_arguments():
+    lib = L.lib()
+    p = C.c_void_p(16)  # never dereferenced: the checks come first
+    assert lib.mk_quantize_rows_int8(p, -1, 8, p, p, None) == L.MK_ERR_INVALID_ARG
+    assert lib.mk_quantize_rows_int8(p, 4, 0, p, p, None) == L.MK_ERR_INVALID_ARG
+    assert lib.mk_quantize_rows_int8(None, 4, 8, p, p, None) == L.MK_ERR_INVALID_ARG
+    assert lib.mk_quantize_rows_int8(p, 4, 8, None, p, None) == L.MK_ERR_INVALID_ARG
+    assert lib.mk_quantize_rows_int8(p, 4, 8, p, None, None) == L.MK_ERR_INVALID_ARG
