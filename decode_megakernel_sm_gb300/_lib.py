@@ -103,6 +103,7 @@ SIGNATURES = {
     "mk_set_stage_bytes": (C.c_int, [C.c_void_p, C.c_int]),
     "mk_set_ring_depth": (C.c_int, [C.c_void_p, C.c_int]),
     "mk_set_kv_pages": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_int]),
+    "mk_set_race_stress": (C.c_int, [C.c_void_p, C.c_uint, C.c_uint, C.c_int]),
     "mk_set_poll_policy": (C.c_int, [C.c_void_p, C.c_int, C.c_uint]),
     "mk_set_hold_policy": (C.c_int, [C.c_void_p, C.c_uint, C.c_uint64]),
     "mk_get_trace": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.c_size_t]),
@@ -234,6 +235,11 @@ def mk_set_residual_copies(h, copies: int):
 
 def mk_set_poll_policy(h, pollers: int, stagger_ns: int):
     _check(lib().mk_set_poll_policy(h, int(pollers), int(stagger_ns)), "mk_set_poll_policy")
+
+
+def mk_set_race_stress(h, max_delay_ns: int, seed: int, permute_queues: bool):
+    _check(lib().mk_set_race_stress(h, int(max_delay_ns), int(seed), int(bool(permute_queues))),
+           "mk_set_race_stress")
 
 
 def mk_set_kv_pages(h, block: int, n_blocks: int, d_table, table_stride: int):

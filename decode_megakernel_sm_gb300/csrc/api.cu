@@ -104,6 +104,8 @@ struct mk_handle {
   int max_stages = 0;  // 0: as many as fit
   int kv_block = 0, kv_blocks = 0, kv_stride = 0;  // paged KV cache (0: contiguous)
   const int32_t* kv_table = nullptr;
+  unsigned stress_ns = 0, stress_seed = 0;  // race stress (0: off)
+  int* qperm = nullptr;                     // device queue permutation, or nullptr
   void* packed = nullptr;
   size_t packed_bytes = 0;
   std::vector<LayerPtrs> layers_h;
@@ -185,6 +187,7 @@ static void free_all(mk_handle* h) {
   if (h->packed) cudaFree(h->packed);
   if (h->layers_d) cudaFree(h->layers_d);
   if (h->rope) cudaFree(h->rope);
+  if (h->qperm) cudaFree(h->qperm);
   if (h->h_err) cudaFreeHost(h->h_err);
   if (h->own) cudaStreamDestroy(h->own);
   delete h;
@@ -650,6 +653,9 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.kv_blocks = h->kv_blocks;
   g.kv_table = h->kv_table;
   g.kv_stride = h->kv_stride;
+  g.stress_ns = h->stress_ns;
+  g.stress_seed = h->stress_seed;
+  g.qperm = h->qperm;
   g.n_steps = 1;
   g.n_lm = h->plan.n_lm;
   g.sel_key = -1;
@@ -918,6 +924,36 @@ extern "C" int mk_set_poll_policy(mk_handle* h, int pollers, unsigned stagger_ns
   if (!h || pollers < 1 || pollers > NCW || stagger_ns > 100000u) return MK_ERR_INVALID_ARG;
   h->n_pollers = pollers;
   h->poll_stagger_ns = stagger_ns;
+  for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
+  h->graphs.clear();
+  return MK_OK;
+}
+
+extern "C" int mk_set_race_stress(mk_handle* h, unsigned max_delay_ns, unsigned seed,
+                                  int permute_queues) {
+  if (!h || max_delay_ns > 100000u || (permute_queues != 0 && permute_queues != 1))
+    return MK_ERR_INVALID_ARG;
+  CK(cudaStreamSynchronize(h->own));
+  if (h->qperm) {
+    CK(cudaFree(h->qperm));
+    h->qperm = nullptr;
+  }
+  if (permute_queues) {
+    // a seeded Fisher-Yates shuffle of the queues over the CTAs
+    std::vector<int> perm(h->n_sm);
+    for (int i = 0; i < h->n_sm; i++) perm[i] = i;
+    uint64_t x = 0x9E3779B97F4A7C15ull ^ seed;
+    for (int i = h->n_sm - 1; i > 0; i--) {
+      x ^= x << 13;
+      x ^= x >> 7;
+      x ^= x << 17;
+      std::swap(perm[i], perm[(int)(x % (uint64_t)(i + 1))]);
+    }
+    CK(cudaMalloc(&h->qperm, perm.size() * sizeof(int)));
+    CK(cudaMemcpy(h->qperm, perm.data(), perm.size() * sizeof(int), cudaMemcpyHostToDevice));
+  }
+  h->stress_ns = max_delay_ns;
+  h->stress_seed = seed;
   for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
   h->graphs.clear();
   return MK_OK;

@@ -1758,7 +1758,7 @@ struct L2Cursor {
           done = true;
           return;
         }
-        const Instr I = load_instr(g, blockIdx.x, pc);
+        const Instr I = load_instr(g, queue_id(g), pc);
         if (I.op == OP_HALT) {
           done = true;
           return;
@@ -1831,12 +1831,13 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
   int seq = 0;  // instructions of this launch before the current one (consumer order)
   unsigned long long issued_bytes = 0;
   L2Cursor<HT, D, NB, WB> l2;
+  const int qid = queue_id(g);
   int t = 0;               // step of this launch: the queue runs once per step
   uint32_t ep = g.epoch;   // its epoch
   bool step_ready = true;  // this step's copies may read rows written by earlier steps
   for (int pc = 0;; pc++) {
     Instr I;
-    if (pc < g.max_pc) I = load_instr(g, blockIdx.x, pc);
+    if (pc < g.max_pc) I = load_instr(g, qid, pc);
     if (pc >= g.max_pc || I.op == OP_HALT) {
       if (++t >= g.n_steps) break;
       pc = -1;
@@ -1846,6 +1847,10 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
       continue;
     }
     if (I.op == OP_NOP || !selected(g, I)) continue;
+    if (g.stress_ns) {
+      if (lane == 0) stress_delay(g, qid, pc, t, 0x5EEDu);
+      __syncwarp();
+    }
     // every branch below is warp-uniform: lane 0 decides, the warp follows
     // (errors elsewhere in the grid are seen in the bounded waits below)
     const bool routed = I.op == OP_MLP && g.E > 0 && !(I.flags & F_SHARED);
@@ -1930,7 +1935,7 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
           stage_of(wi, stg, p);
           if (__shfl_sync(0xFFFFFFFFu, mbar_try(empty0 + 8u * stg, p ^ 1u), 0)) {
             if (lane == 0) {
-              if (g.trace && wi == 0) g.trace[((size_t)blockIdx.x * g.max_pc + pc) * 8] = gtimer();
+              if (g.trace && wi == 0) g.trace[((size_t)qid * g.max_pc + pc) * 8] = gtimer();
               const uint32_t u0 = wi * S.ups, bytes = min(S.ups, S.n - u0) * S.unit;
               mbar_expect_tx(full0 + 8u * stg, 2u * bytes);
               issue(wi, S.src, 0, pol_w);
@@ -2027,7 +2032,7 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
         }
         if (lane == 0) {
           if (g.trace && k == 0 && u0 == 0)
-            g.trace[((size_t)blockIdx.x * g.max_pc + pc) * 8] = gtimer();
+            g.trace[((size_t)qid * g.max_pc + pc) * 8] = gtimer();
           const uint32_t bytes = n * s[k].unit;
           const uint32_t full = full0 + 8u * st;
           const uint32_t dst = ring_s + (uint32_t)st * (uint32_t)g.stage_bytes;
@@ -2140,6 +2145,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
   c.tm[0] = c.tm[1] = 0;
 
   int finished = 0;
+  const int qid = queue_id(g);
   for (int step = 0; step < g.n_steps; step++) {
     c.step = step;
     c.epoch = g.epoch + (uint32_t)step;
@@ -2165,13 +2171,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
     if (step == 0 && g.pdl && tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     consumer_bar();  // everyone has read *flag before it is reused
 
-    Instr next = load_instr(g, blockIdx.x, 0);
+    Instr next = load_instr(g, qid, 0);
     for (int pc = 0; pc < g.max_pc; pc++) {
       const Instr I = next;
       if (I.op == OP_HALT) break;
-      if (pc + 1 < g.max_pc) next = load_instr(g, blockIdx.x, pc + 1);
+      if (pc + 1 < g.max_pc) next = load_instr(g, qid, pc + 1);
       if (I.op == OP_NOP || !selected(g, I)) continue;
       c.pc = pc;
+      // race stress: thread 0 starts late; the op's dependency wait holds the rest
+      if (g.stress_ns && tid == 0) stress_delay(g, qid, pc, step, 0xC0DEu);
       bool ok;
       switch (I.op) {
         case OP_QKV: ok = op_qkv(c, g, I); break;
@@ -2190,7 +2198,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
       if (!ok) return;
       if (tid == 0) {
         if (g.trace) {
-          unsigned long long* t = g.trace + ((size_t)blockIdx.x * g.max_pc + pc) * 8;
+          unsigned long long* t = g.trace + ((size_t)qid * g.max_pc + pc) * 8;
           t[1] = c.tw0;
           t[2] = c.tw1;
           t[3] = c.tm[0];
@@ -2205,7 +2213,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
           else
             red_release(g.ctr + I.sig_ctr, 1u);
         }
-        if (g.trace) g.trace[((size_t)blockIdx.x * g.max_pc + pc) * 8 + 7] = gtimer();
+        if (g.trace) g.trace[((size_t)qid * g.max_pc + pc) * 8 + 7] = gtimer();
         *(volatile int*)(misc + 1) = ++finished;
       }
     }

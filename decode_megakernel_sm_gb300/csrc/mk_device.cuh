@@ -232,6 +232,20 @@ MK_DEV float warp_sum(float v) {
 
 MK_DEV int peek_err(const Globals& g) { return *(volatile const int*)g.err; }
 
+// The queue this CTA runs (a permutation of the CTAs under race stress).
+MK_DEV int queue_id(const Globals& g) { return g.qperm ? __ldg(g.qperm + blockIdx.x) : (int)blockIdx.x; }
+
+// Race stress: sleep a pseudo-random time below g.stress_ns, a function of
+// (queue, pc, step, seed, side).  Only timing changes: no wait is skipped.
+MK_DEV void stress_delay(const Globals& g, int q, int pc, int step, uint32_t side) {
+  uint32_t h = (uint32_t)q * 0x9E3779B1u ^ (uint32_t)pc * 0x85EBCA6Bu ^
+               (uint32_t)step * 0xC2B2AE35u ^ g.stress_seed ^ side;
+  h ^= h >> 15;
+  h *= 0x2C1B3C6Du;
+  h ^= h >> 12;
+  __nanosleep(h % g.stress_ns);
+}
+
 MK_DEV void set_err(const Globals& g, int code, int pc, int op) {
   if (atomicCAS(g.err, 0, code) == 0) {
     g.err[1] = (int)blockIdx.x;

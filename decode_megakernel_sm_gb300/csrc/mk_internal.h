@@ -232,6 +232,11 @@ struct Globals {
   const int* kv_table;      //   kv_table[b * kv_stride + j]
   int kv_stride;
   int n_steps;              // greedy decode steps in this launch (1: one step)
+  // race stress (mk_set_race_stress; off: 0 / nullptr): a hashed delay below
+  // stress_ns before each instruction, on the producer and the consumers,
+  // and queue qperm[blockIdx.x] run by CTA blockIdx.x
+  uint32_t stress_ns, stress_seed;
+  const int* qperm;
   int n_lm;
   int sel_key;             // -1: run every instruction; else only key == sel_key (ablation)
   int zero_next;           // the LM head slices zero the next step's residual buffers (the

@@ -114,6 +114,12 @@ class Decoder:
         L.mk_set_kv_pages(self.h, block, n_blocks, _ptr(table, torch.int32), table.shape[1])
         self._kv_table = table  # kept alive: the kernel reads it every step
 
+    def set_race_stress(self, max_delay_ns: int, seed: int = 0, permute_queues: bool = True):
+        """Test aid: random delays before every instruction and a random
+        queue-to-CTA permutation; results must not change (0 delay and no
+        permutation: off)."""
+        L.mk_set_race_stress(self.h, max_delay_ns, seed, permute_queues)
+
     def set_ring_depth(self, max_stages: int):
         """At most max_stages ring stages (0: as many as fit)."""
         L.mk_set_ring_depth(self.h, max_stages)

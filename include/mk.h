@@ -155,6 +155,19 @@ int mk_quantize_rows_int8(const void* d_w, long rows, int cols, int8_t* d_codes,
 int mk_set_kv_pages(mk_handle* h, int block, int n_blocks, const int32_t* d_table,
                     int table_stride);
 
+/* Race stress for tests (the survey's race-stress test level; the hazard is
+ * the missing fence that "Megakernels: Deleting the Kernel Boundary",
+ * section "Correctness without the free barrier", warns of).  With
+ * max_delay_ns > 0 the producer warp and consumer thread 0 of every CTA
+ * sleep a pseudo-random time below max_delay_ns (a function of queue, pc,
+ * step and seed) before each instruction; with permute_queues = 1 the CTAs
+ * run the queues in a seeded random permutation.  Only timing and placement
+ * change: every wait, fence and signal stays, so results must be those of
+ * an unstressed step.  max_delay_ns <= 100000; (0, *, 0) turns it off.
+ * Synchronises the handle's stream; drops cached ablation graphs.
+ * MK_ERR_INVALID_ARG for out-of-range arguments.                          */
+int mk_set_race_stress(mk_handle* h, unsigned max_delay_ns, unsigned seed, int permute_queues);
+
 /* Build the per-SM instruction queues for `batch` sequences whose positions
  * will stay below `max_ctx` (<= max_seq): splits every projection into
  * byte-balanced row ranges, one split-KV attention work item per

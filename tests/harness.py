@@ -28,7 +28,7 @@ ROUTE_TIE = 1e-4
 class Run:
     def __init__(self, cfg: dict, seed: int = 0, max_ctx: int | None = None,
                  stage_bytes: int | None = None, hold: tuple | None = None,
-                 paged: int | None = None, int8: bool = False):
+                 paged: int | None = None, int8: bool = False, stress: tuple | None = None):
         cfg = cfg if "max_seq" in cfg else synth.with_cache(cfg)
         self.cfg = cfg
         self.W = synth.make_weights(cfg, seed, "cuda")
@@ -54,6 +54,8 @@ class Run:
             self.dec = Decoder(cfg, self.W, self.ks, self.vs, weight_format=fmt)
         if stage_bytes is not None:
             self.dec.set_stage_bytes(stage_bytes)
+        if stress is not None:  # (max delay ns, seed, permute queues)
+            self.dec.set_race_stress(*stress)
         if hold is not None:
             self.dec.set_hold_policy(*hold)
         self.B = cfg["batch"]
