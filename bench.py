@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--pollers", type=int, default=None,
                     help="warps polling each dependency counter (library default if unset)")
     ap.add_argument("--poll-stagger", type=int, default=0, help="ns between pollers (with --pollers)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="sequences per step (default: the workload's own; at most its batch capacity)")
     ap.add_argument("--weights", default="bf16", choices=["bf16", "int8"],
                     help="streamed weight format (int8: per-row int8 codes + fp32 scales)")
     ap.add_argument("--paged", type=int, default=0,
@@ -266,6 +268,8 @@ def main():
     cfg = synth.with_cache(base)
     if args.weights == "int8":
         cfg = dict(cfg, int8=True)
+    if args.batch is not None:
+        cfg = dict(cfg, batch=args.batch)
     if args.impl == "reference":
         run_reference(args, cfg)
         return
