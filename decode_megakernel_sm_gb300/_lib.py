@@ -104,6 +104,7 @@ SIGNATURES = {
     "mk_set_ring_depth": (C.c_int, [C.c_void_p, C.c_int]),
     "mk_set_kv_pages": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_int]),
     "mk_set_race_stress": (C.c_int, [C.c_void_p, C.c_uint, C.c_uint, C.c_int]),
+    "mk_debug_read": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_size_t]),
     "mk_set_poll_policy": (C.c_int, [C.c_void_p, C.c_int, C.c_uint]),
     "mk_set_hold_policy": (C.c_int, [C.c_void_p, C.c_uint, C.c_uint64]),
     "mk_get_trace": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.c_size_t]),
@@ -235,6 +236,15 @@ def mk_set_residual_copies(h, copies: int):
 
 def mk_set_poll_policy(h, pollers: int, stagger_ns: int):
     _check(lib().mk_set_poll_policy(h, int(pollers), int(stagger_ns)), "mk_set_poll_policy")
+
+
+MK_DBG_Q, MK_DBG_X, MK_DBG_H = 0, 1, 2
+
+
+def mk_debug_read(h, what: int, layer: int, out) -> None:
+    """out: a C-contiguous float32 numpy array of the intermediate's size."""
+    _check(lib().mk_debug_read(h, int(what), int(layer), out.ctypes.data_as(C.c_void_p),
+                               out.size), "mk_debug_read")
 
 
 def mk_set_race_stress(h, max_delay_ns: int, seed: int, permute_queues: bool):

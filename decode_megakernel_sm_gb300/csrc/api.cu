@@ -929,6 +929,53 @@ extern "C" int mk_set_poll_policy(mk_handle* h, int pollers, unsigned stagger_ns
   return MK_OK;
 }
 
+extern "C" int mk_debug_read(mk_handle* h, int what, int layer, float* out, size_t n) {
+  if (!h || !out) return MK_ERR_INVALID_ARG;
+  if (!h->scratch || h->batch <= 0 || h->epoch == 0) return MK_ERR_NOT_READY;
+  const mk_model_desc& d = h->d;
+  const size_t B = h->batch, L = d.n_layers, H = d.hidden, F = d.ffn > 0 ? d.ffn : 0;
+  const size_t HqD = (size_t)d.n_q_heads * d.head_dim;
+  CK(cudaDeviceSynchronize());  // the step may have run on any stream
+  switch (what) {
+    case MK_DBG_Q: {
+      if (layer < 0 || (size_t)layer >= L || n < B * HqD) return MK_ERR_INVALID_ARG;
+      CK(cudaMemcpy(out, h->sc.qbuf + (size_t)layer * B * HqD, B * HqD * 4,
+                    cudaMemcpyDeviceToHost));
+      return MK_OK;
+    }
+    case MK_DBG_X: {
+      if (layer < 1 || (size_t)layer > 2 * L || n < B * H) return MK_ERR_INVALID_ARG;
+      const size_t j = (size_t)layer;
+      if (j % 2 == 0 && mlp_split(d)) {  // x_{2l+2} as the down rows' tagged words
+        std::vector<TagWord> t(B * H);
+        CK(cudaMemcpy(t.data(), h->sc.xt + (j / 2 - 1) * B * H, t.size() * sizeof(TagWord),
+                      cudaMemcpyDeviceToHost));
+        for (size_t i = 0; i < t.size(); i++) std::memcpy(out + i, &t[i].bits, 4);
+        return MK_OK;
+      }
+      // the step's parity, summed over the partial copies
+      const size_t kc = (size_t)h->kc, par = h->epoch & 1u;
+      std::vector<float> v(kc * B * H);
+      CK(cudaMemcpy(v.data(), h->sc.xbuf + ((par * 2 * L + (j - 1)) * kc) * B * H, v.size() * 4,
+                    cudaMemcpyDeviceToHost));
+      for (size_t i = 0; i < B * H; i++) {
+        float s = 0.f;
+        for (size_t c = 0; c < kc; c++) s += v[c * B * H + i];
+        out[i] = s;
+      }
+      return MK_OK;
+    }
+    case MK_DBG_H: {
+      if (!mlp_split(d)) return MK_ERR_UNSUPPORTED;
+      if (layer < 0 || (size_t)layer >= L || n < B * F) return MK_ERR_INVALID_ARG;
+      CK(cudaMemcpy(out, h->sc.hglob + (size_t)layer * B * F, B * F * 4, cudaMemcpyDeviceToHost));
+      return MK_OK;
+    }
+    default:
+      return MK_ERR_INVALID_ARG;
+  }
+}
+
 extern "C" int mk_set_race_stress(mk_handle* h, unsigned max_delay_ns, unsigned seed,
                                   int permute_queues) {
   if (!h || max_delay_ns > 100000u || (permute_queues != 0 && permute_queues != 1))

@@ -114,6 +114,18 @@ class Decoder:
         L.mk_set_kv_pages(self.h, block, n_blocks, _ptr(table, torch.int32), table.shape[1])
         self._kv_table = table  # kept alive: the kernel reads it every step
 
+    def debug_read(self, what: str, layer: int):
+        """An intermediate of the most recent step as a float32 numpy array:
+        "q" [batch][Hq*d] of layer `layer`, "x" [batch][H] the residual x_layer
+        (1 .. 2L), "h" [batch][F] of layer `layer` (dense batch 1)."""
+        import numpy as np
+        c = self.cfg
+        width = {"q": c["n_q_heads"] * c["head_dim"], "x": c["hidden"], "h": c["ffn"]}[what]
+        out = np.empty((self.batch, width), np.float32)
+        L.mk_debug_read(self.h, {"q": L.MK_DBG_Q, "x": L.MK_DBG_X, "h": L.MK_DBG_H}[what], layer,
+                        out)
+        return out
+
     def set_race_stress(self, max_delay_ns: int, seed: int = 0, permute_queues: bool = True):
         """Test aid: random delays before every instruction and a random
         queue-to-CTA permutation; results must not change (0 delay and no

@@ -155,6 +155,23 @@ int mk_quantize_rows_int8(const void* d_w, long rows, int cols, int8_t* d_codes,
 int mk_set_kv_pages(mk_handle* h, int block, int n_blocks, const int32_t* d_table,
                     int table_stride);
 
+/* Diagnostics: an intermediate of the handle's most recent step
+ * (mk_decode_step, mk_decode_step_host, or the last step of
+ * mk_decode_steps; not the no-allocation call), copied to host memory as
+ * fp32, for per-phase checks against a reference:
+ *   MK_DBG_Q: the queries of layer `layer` after RoPE, [batch][n_q_heads][head_dim];
+ *   MK_DBG_X: the residual x_j for j = `layer` in [1, 2 n_layers]: x_{2l+1}
+ *             after layer l's O-projection, x_{2l+2} after its MLP, [batch][hidden];
+ *   MK_DBG_H: SiLU(gate) * up of layer `layer`, [batch][ffn] (dense batch 1
+ *             only; MK_ERR_UNSUPPORTED otherwise).
+ * n: capacity of out in floats.  Synchronises the device.
+ * MK_ERR_NOT_READY before the first step; MK_ERR_INVALID_ARG for a bad
+ * selector, layer or capacity.                                            */
+#define MK_DBG_Q 0
+#define MK_DBG_X 1
+#define MK_DBG_H 2
+int mk_debug_read(mk_handle* h, int what, int layer, float* out, size_t n);
+
 /* Race stress for tests (the survey's race-stress test level; the hazard is
  * the missing fence that "Megakernels: Deleting the Kernel Boundary",
  * section "Correctness without the free barrier", warns of).  With

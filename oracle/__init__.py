@@ -93,6 +93,11 @@ def lib():
             L.orc_argmax.argtypes = [dp, C.c_int]
             L.orc_quantize_rows_int8.argtypes = [u16p, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
             L.orc_gemv_q8.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, dp, dp]
+            L.orc_decode_step_trace.restype = C.c_int
+            L.orc_decode_step_trace.argtypes = [C.POINTER(OrcConfig), C.POINTER(OrcWeights),
+                                                C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
+                                                C.c_int, ip, ip, dp, ip, ip, dp, ip, ip, dp, dp,
+                                                dp]
             L.orc_decode_step.restype = C.c_int
             L.orc_decode_step.argtypes = [C.POINTER(OrcConfig), C.POINTER(OrcWeights),
                                           C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
@@ -301,9 +306,13 @@ class OracleModel:
         self._keep.append(a)
         return a
 
-    def step(self, kc, vc, tokens, positions, forced_routes=None, forced_mask=None):
+    def step(self, kc, vc, tokens, positions, forced_routes=None, forced_mask=None,
+             trace=None):
         """kc/vc: lists (per layer) of uint16 arrays [B][Hkv][max_seq][d], updated in
-        place.  Returns (logits [B][V] float64, argmax [B] int32, route_ids, margins)."""
+        place.  Returns (logits [B][V] float64, argmax [B] int32, route_ids, margins).
+        trace: a dict that receives the intermediates q [L][B][Hq*d] (after RoPE),
+        x [2L][B][H] (residual after each O-projection and each MLP) and, for dense
+        models, h [L][B][F]."""
         cfg = self.cfg
         B = len(tokens)
         L = cfg["n_layers"]
@@ -318,11 +327,24 @@ class OracleModel:
         rmg = np.zeros((L, B)) if moe else None
         fr = None if forced_routes is None else np.ascontiguousarray(forced_routes, np.int32)
         fm = None if forced_mask is None else np.ascontiguousarray(forced_mask, np.int32)
-        rc = lib().orc_decode_step(
-            C.byref(self.c), C.byref(self.w), C.cast(kp, C.POINTER(C.c_void_p)),
-            C.cast(vp, C.POINTER(C.c_void_p)), B, _ip(tok), _ip(pos), _dp(logits), _ip(am),
-            None if rid is None else _ip(rid), None if rmg is None else _dp(rmg),
-            None if fr is None else _ip(fr), None if fm is None else _ip(fm))
+        if trace is not None:
+            H, Hq, d = cfg["hidden"], cfg["n_q_heads"], cfg["head_dim"]
+            tq = np.zeros((L, B, Hq * d))
+            tx = np.zeros((2 * L, B, H))
+            th = np.zeros((L, B, max(cfg.get("ffn", 0), 1)))
+            rc = lib().orc_decode_step_trace(
+                C.byref(self.c), C.byref(self.w), C.cast(kp, C.POINTER(C.c_void_p)),
+                C.cast(vp, C.POINTER(C.c_void_p)), B, _ip(tok), _ip(pos), _dp(logits), _ip(am),
+                None if rid is None else _ip(rid), None if rmg is None else _dp(rmg),
+                None if fr is None else _ip(fr), None if fm is None else _ip(fm), _dp(tq),
+                _dp(tx), _dp(th) if not moe else None)
+            trace.update(q=tq, x=tx, h=None if moe else th)
+        else:
+            rc = lib().orc_decode_step(
+                C.byref(self.c), C.byref(self.w), C.cast(kp, C.POINTER(C.c_void_p)),
+                C.cast(vp, C.POINTER(C.c_void_p)), B, _ip(tok), _ip(pos), _dp(logits), _ip(am),
+                None if rid is None else _ip(rid), None if rmg is None else _dp(rmg),
+                None if fr is None else _ip(fr), None if fm is None else _ip(fm))
         if rc != 0:
             raise ValueError("oracle: invalid argument")
         return logits, am, rid, rmg

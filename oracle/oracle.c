@@ -222,17 +222,24 @@ void orc_attention_merge(int n_parts, const double* m, const double* l, const do
 /* [MK] "SiLU": a * sigmoid(a). */
 double orc_silu(double a) { return a / (1.0 + exp(-a)); }
 
-/* [MK] "up and gate projections, SiLU, down projection". */
-void orc_swiglu(const uint16_t* wg, const uint16_t* wu, const uint16_t* wd, int F, int H,
-                const double* xn, double* y) {
+/* [MK] "up and gate projections, SiLU, down projection"; h (may be NULL)
+ * receives silu(Wg xn) * (Wu xn). */
+void orc_swiglu_h(const uint16_t* wg, const uint16_t* wu, const uint16_t* wd, int F, int H,
+                  const double* xn, double* y, double* h) {
   double* g = (double*)malloc(sizeof(double) * (size_t)F);
   double* u = (double*)malloc(sizeof(double) * (size_t)F);
   orc_gemv(wg, F, H, xn, g);
   orc_gemv(wu, F, H, xn, u);
   for (int c = 0; c < F; c++) g[c] = orc_silu(g[c]) * u[c];
+  if (h) memcpy(h, g, sizeof(double) * (size_t)F);
   orc_gemv(wd, H, F, g, y);
   free(g);
   free(u);
+}
+
+void orc_swiglu(const uint16_t* wg, const uint16_t* wu, const uint16_t* wd, int F, int H,
+                const double* xn, double* y) {
+  orc_swiglu_h(wg, wu, wd, F, H, xn, y, NULL);
 }
 
 /* [G4] component "Router".  Reading: softmax over all router logits, the
@@ -305,6 +312,15 @@ int orc_decode_step(const orc_config* cfg, const orc_weights* w, uint16_t* const
                     uint16_t* const* vc, int B, const int* tokens, const int* positions,
                     double* logits, int* argmax, int* route_ids, double* route_margin,
                     const int* forced_routes, const int* forced_mask) {
+  return orc_decode_step_trace(cfg, w, kc, vc, B, tokens, positions, logits, argmax, route_ids,
+                               route_margin, forced_routes, forced_mask, NULL, NULL, NULL);
+}
+
+int orc_decode_step_trace(const orc_config* cfg, const orc_weights* w, uint16_t* const* kc,
+                          uint16_t* const* vc, int B, const int* tokens, const int* positions,
+                          double* logits, int* argmax, int* route_ids, double* route_margin,
+                          const int* forced_routes, const int* forced_mask, double* tq,
+                          double* tx, double* th) {
   const int H = cfg->hidden, Hq = cfg->n_q_heads, Hkv = cfg->n_kv_heads, d = cfg->head_dim;
   const int L = cfg->n_layers, V = cfg->vocab;
   if (B <= 0 || H <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || (d % 2) || (Hq % Hkv)) return -1;
@@ -342,6 +358,7 @@ int orc_decode_step(const orc_config* cfg, const orc_weights* w, uint16_t* const
       gemv_w(w->wv[l], q8 ? &q8->wv[l] : NULL, Hkv * d, H, xn, v);
       for (int h = 0; h < Hq; h++) orc_rope(q + (size_t)h * d, d, P, cfg->rope_theta);
       for (int g = 0; g < Hkv; g++) orc_rope(k + (size_t)g * d, d, P, cfg->rope_theta);
+      if (tq) memcpy(tq + ((size_t)l * B + b) * Hq * d, q, sizeof(double) * (size_t)Hq * d);
       for (int g = 0; g < Hkv; g++) {
         uint16_t* kr = cache_row(kc[l], cfg, b, g, P);
         uint16_t* vr = cache_row(vc[l], cfg, b, g, P);
@@ -359,6 +376,7 @@ int orc_decode_step(const orc_config* cfg, const orc_weights* w, uint16_t* const
       /* OP_O_PROJ_RES */
       gemv_w(w->wo[l], q8 ? &q8->wo[l] : NULL, H, Hq * d, att, y);
       for (int i = 0; i < H; i++) x[i] += y[i];
+      if (tx) memcpy(tx + ((size_t)(2 * l) * B + b) * H, x, sizeof(double) * (size_t)H);
       /* OP_RMS_UP_GATE + OP_DOWN_RES (dense) or router + experts (MoE) */
       orc_rmsnorm(x, w->mlp_norm[l], H, cfg->rms_eps, xn);
       if (!moe && q8) {
@@ -369,12 +387,14 @@ int orc_decode_step(const orc_config* cfg, const orc_weights* w, uint16_t* const
         gemv_w(NULL, &q8->w_gate[l], F, H, xn, gq);
         gemv_w(NULL, &q8->w_up[l], F, H, xn, uq);
         for (int c = 0; c < F; c++) gq[c] = orc_silu(gq[c]) * uq[c];
+        if (th) memcpy(th + ((size_t)l * B + b) * F, gq, sizeof(double) * (size_t)F);
         gemv_w(NULL, &q8->w_down[l], H, F, gq, y);
         free(gq);
         free(uq);
         for (int i = 0; i < H; i++) x[i] += y[i];
       } else if (!moe) {
-        orc_swiglu(w->w_gate[l], w->w_up[l], w->w_down[l], cfg->ffn, H, xn, y);
+        orc_swiglu_h(w->w_gate[l], w->w_up[l], w->w_down[l], cfg->ffn, H, xn, y,
+                     th ? th + ((size_t)l * B + b) * cfg->ffn : NULL);
         for (int i = 0; i < H; i++) x[i] += y[i];
       } else {
         const int E = cfg->n_experts, K = cfg->top_k, Fe = cfg->expert_ffn;
@@ -409,6 +429,7 @@ int orc_decode_step(const orc_config* cfg, const orc_weights* w, uint16_t* const
         }
         for (int i = 0; i < H; i++) x[i] += y[i];
       }
+      if (tx) memcpy(tx + ((size_t)(2 * l + 1) * B + b) * H, x, sizeof(double) * (size_t)H);
     }
     /* OP_RMS_LM_HEAD */
     orc_rmsnorm(x, w->final_norm, H, cfg->rms_eps, xn);

@@ -172,6 +172,21 @@ int orc_decode_step(const orc_config* cfg, const orc_weights* w, uint16_t* const
                     double* logits, int* argmax, int* route_ids, double* route_margin,
                     const int* forced_routes, const int* forced_mask);
 
+/* orc_decode_step that also records its intermediates (each may be NULL):
+ * tq [n_layers][B][n_q_heads*head_dim] the queries after RoPE; tx
+ * [2*n_layers][B][hidden] the residual after each O-projection (2l) and
+ * after each MLP (2l+1); th [n_layers][B][ffn] SiLU(gate)*up (dense). The
+ * arithmetic is that of orc_decode_step.                                  */
+int orc_decode_step_trace(const orc_config* cfg, const orc_weights* w, uint16_t* const* kc,
+                          uint16_t* const* vc, int B, const int* tokens, const int* positions,
+                          double* logits, int* argmax, int* route_ids, double* route_margin,
+                          const int* forced_routes, const int* forced_mask, double* tq,
+                          double* tx, double* th);
+
+/* orc_swiglu, also writing h = silu(Wg xn) * (Wu xn) when h != NULL. */
+void orc_swiglu_h(const uint16_t* wg, const uint16_t* wu, const uint16_t* wd, int F, int H,
+                  const double* xn, double* y, double* h);
+
 void orc_set_threads(int n);
 int orc_get_threads(void);
 
