@@ -395,3 +395,49 @@ def test_int8_oracle_refuses_moe():
                                         top_k=2, expert_ffn=32, shared_ffn=0, prefill=(2, 2)))
     with pytest.raises(AssertionError):
         oracle.OracleModel(cfg, synth.make_weights(cfg, 0), int8=True)
+
+
+# ------------------------------------------------------- traced decode step ----
+def test_traced_step_equals_untraced_and_feeds_the_logits():
+    cfg = synth.with_cache(synth.custom(n_layers=2, hidden=128, n_q_heads=4, n_kv_heads=2,
+                                        head_dim=32, ffn=96, vocab=300, batch=2,
+                                        prefill=(3, 9), steps=2))
+    W = synth.make_weights(cfg, 21)
+    lengths = synth.make_lengths(cfg, 21)
+    ks, vs = synth.make_kv(cfg, lengths, 21)
+    toks = synth.make_tokens(cfg, 21)
+    om = oracle.OracleModel(cfg, W)
+    runs = []
+    for trace in (None, {}):
+        ko = [oracle._bits(t).copy() for t in ks]
+        vo = [oracle._bits(t).copy() for t in vs]
+        runs.append((om.step(ko, vo, toks, list(lengths), trace=trace), trace, ko))
+    (a, _, ka), (b, tr, kb) = runs
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    assert all(np.array_equal(x, y) for x, y in zip(ka, kb))
+    L, H = cfg["n_layers"], cfg["hidden"]
+    assert tr["q"].shape == (L, 2, cfg["n_q_heads"] * cfg["head_dim"])
+    assert tr["x"].shape == (2 * L, 2, H) and tr["h"].shape == (L, 2, cfg["ffn"])
+    # the last residual, normed and multiplied by the (tied) head in numpy,
+    # gives the logits
+    Wf = bn.weights_f64(W)
+    for s in range(2):
+        x = tr["x"][-1, s]
+        g = bn.widen(oracle._bits(W["final_norm"]))
+        xn = x / np.sqrt(np.mean(x * x) + cfg["rms_eps"]) * g
+        assert np.allclose(Wf["embed"] @ xn, b[0][s], rtol=1e-12, atol=1e-12)
+
+
+def test_traced_mlp_output_is_the_residual_step():
+    # x after the MLP minus x after the O-projection is Wd h for the traced h
+    cfg = synth.with_cache(synth.custom(n_layers=2, hidden=128, n_q_heads=4, n_kv_heads=2,
+                                        head_dim=32, ffn=96, vocab=300, prefill=(5, 5)))
+    W = synth.make_weights(cfg, 23)
+    ks, vs = synth.make_kv(cfg, [5], 23)
+    tr = {}
+    oracle.OracleModel(cfg, W).step([oracle._bits(t).copy() for t in ks],
+                                    [oracle._bits(t).copy() for t in vs], [7], [5], trace=tr)
+    Wf = bn.weights_f64(W)
+    for l in range(cfg["n_layers"]):
+        d = tr["x"][2 * l + 1, 0] - tr["x"][2 * l, 0]
+        assert np.allclose(Wf["layers"][l]["w_down"] @ tr["h"][l, 0], d, rtol=1e-9, atol=1e-12)
