@@ -83,6 +83,19 @@ def dist_env():
     return ws, rank, local
 
 
+def job_rate(elapsed_s, units_per_rank, ws, device):
+    """The slowest rank's elapsed time (max over ranks) and the whole job's
+    rate: all ranks' units over that time.  Every rank runs the same units
+    (weak scaling); ws == 1 needs no process group."""
+    import torch
+    t = torch.tensor([float(elapsed_s)], dtype=torch.float64, device=device)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    slowest = float(t.item())
+    return slowest, ws * units_per_rank / slowest
+
+
 def workload_desc(cfg):
     lo, hi = cfg["prefill"]
     kv = f"KV prefill {lo}" if lo == hi else f"KV prefill U[{lo},{hi}]"
@@ -374,12 +387,9 @@ def main():
     st = dec.sync_status(stream)
     if st != 0:
         raise SystemExit(f"device status {st} in the timed region")
-    el = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(el, op=dist.ReduceOp.MAX)
-    ms_max = float(el.item())
+    el_s, value = job_rate(ms / 1e3, args.steps * B, ws, dev)
+    ms_max = el_s * 1e3
     ms_step = ms_max / args.steps
-    value = ws * args.steps * B / (ms_max / 1e3)
 
     # roofline of the (only) kernel: algorithmic bytes / average launch time
     per_step = [step_bytes(cfg, [lengths[b] + (t % window) for b in range(B)],
@@ -459,10 +469,8 @@ def main():
             if stt != 0:
                 raise SystemExit(f"host step status {stt}")
             htok.copy_(ham)
-        el2 = torch.tensor([time.perf_counter() - t0], dtype=torch.float64, device=dev)
-        if ws > 1:
-            dist.all_reduce(el2, op=dist.ReduceOp.MAX)
-        line["e2e"] = {"value": ws * n * B / float(el2.item()), "unit": "tok/s",
+        _, e2e_rate = job_rate(time.perf_counter() - t0, n * B, ws, dev)
+        line["e2e"] = {"value": e2e_rate, "unit": "tok/s",
                        "h2d_bytes_per_step": 2 * B * 4, "d2h_bytes_per_step": B * V * 4 + B * 4,
                        "steps": n}
 
