@@ -7,8 +7,10 @@ LM head, bf16 weights ~N(0, 0.02) from a seed, bf16 KV cache prefilled with
 device-to-device and writes cache row 1024 + (t mod 128), so the timed steps
 cycle over the 128-step decode window of the workload.  A step is one pass
 of the persistent kernel over the whole forward pass; by default one launch
-runs 16 such steps back to back (mk_decode_steps: each step decodes the
-previous step's argmax on the device), --multi-step 0 launches once per step.
+runs up to 16 such steps back to back (mk_decode_steps: each step decodes the
+previous step's argmax on the device; the launch size divides --steps), and
+--multi-step 0 launches once per step.  Besides the mean, the line gives the
+median and p10 / p90 of the per-step time of every launch.
 The end-to-end figure goes through the host-buffer call, one step per call.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
@@ -48,7 +50,8 @@ def parse():
     ap.add_argument("--ablation", action="store_true", help="also time the per-phase launches")
     ap.add_argument("--multi-step", type=int, default=None,
                     help="greedy steps per launch (mk_decode_steps); 0: one launch per step; "
-                         "default 16 when it divides the decode window and --steps")
+                         "default: the largest of 16, 8, 4, 2 that divides both the decode "
+                         "window and --steps (else one launch per step)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--l2-ahead", type=int, default=None,
                     help="bytes each SM warms in L2 ahead of its ring (library default if unset)")
@@ -139,17 +142,29 @@ def measured_peak():
 
 
 def traffic_record(config, steps_per_launch=1):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources with this many steps per launch."""
+    """DRAM bytes per launch of `steps_per_launch` steps from the committed ncu
+    summary (profiles/traffic.json), if it was taken on the current kernel
+    sources: the capture of launches of that size when there is one, else a
+    capture of another launch size of the same workload scaled by its steps
+    (the step-to-step L2 reuse is a few MB of a 2.5 GB step).  Returns
+    (bytes, how) or (None, reason)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         j = json.load(open(p))
-        e = j.get(config if steps_per_launch == 1 else f"{config}@{steps_per_launch}")
-        if e and e.get("kernel_src_sha") == kernel_src_hash():
-            return float(e["dram_bytes_per_launch"])
     except Exception:
-        pass
-    return None
+        return None, "no profiles/traffic.json"
+    src = kernel_src_hash()
+    exact = j.get(config if steps_per_launch == 1 else f"{config}@{steps_per_launch}")
+    if exact and exact.get("kernel_src_sha") == src:
+        return float(exact["dram_bytes_per_launch"]), f"ncu, launches of {steps_per_launch} step(s)"
+    for key, e in sorted(j.items()):
+        if key.split("@")[0] != config or e.get("kernel_src_sha") != src:
+            continue
+        spl = int(key.split("@")[1]) if "@" in key else 1
+        per_step = float(e["dram_bytes_per_launch"]) / spl
+        return per_step * steps_per_launch, (f"ncu, launches of {spl} step(s), scaled to "
+                                             f"{steps_per_launch}")
+    return None, "no capture on this kernel source"
 
 
 class ClockSampler:
@@ -338,19 +353,23 @@ def main():
     logits = torch.empty((B, V), dtype=torch.float32, device=dev)
 
     ns = args.multi_step
-    if ns is None:
-        ns = 16 if window % 16 == 0 and args.steps % 16 == 0 else 0
+    if ns is None:  # the longest launch (<= 16 steps) that divides the window and --steps
+        ns = next((k for k in (16, 8, 4, 2) if window % k == 0 and args.steps % k == 0), 0)
     if ns:
         if ns < 1 or window % ns or args.steps % ns:
             raise SystemExit(f"--multi-step {ns} must divide the decode window ({window}) "
                              f"and --steps ({args.steps})")
         am_ms = [torch.empty((ns, B), dtype=torch.int32, device=dev) for _ in range(2)]
 
-    def run(n, fn=None):
+    def run(n, fn=None, marks=None):
+        """n steps; with `marks`, an event is recorded after every launch."""
         if ns and fn is None:  # launches of ns steps, each fed the last argmax of the one before
             for k in range((n + ns - 1) // ns):
                 tok = tok0 if k == 0 else am_ms[(k - 1) % 2][ns - 1]
                 dec.steps(tok, pos_table[(k * ns) % window], ns, logits, am_ms[k % 2], stream)
+                if marks is not None:
+                    marks.append(torch.cuda.Event(enable_timing=True))
+                    marks[-1].record(stream)
             return
         for t in range(n):
             tok = tok0 if t == 0 else am[(t - 1) % 2]
@@ -358,6 +377,9 @@ def main():
                 dec.step(tok, pos_table[t % window], logits, am[t % 2], stream)
             else:
                 fn(tok, pos_table[t % window], logits, am[t % 2])
+            if marks is not None:
+                marks.append(torch.cuda.Event(enable_timing=True))
+                marks[-1].record(stream)
 
     def barrier():
         if ws > 1:
@@ -378,11 +400,16 @@ def main():
     time.sleep(0.15)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
+    marks = []
     e0.record(stream)
-    run(args.steps)
+    run(args.steps, marks=marks)
     e1.record(stream)
     barrier()
     ms = e0.elapsed_time(e1)
+    # per-step time of every launch (launch time / its steps): median, p10, p90
+    spl_ = ns if ns else 1
+    per = [a.elapsed_time(b) / spl_ for a, b in zip([e0] + marks[:-1], marks)]
+    qs = np.quantile(np.array(per), [0.1, 0.5, 0.9]) if per else [None] * 3
     ck = clocks.stop()
     st = dec.sync_status(stream)
     if st != 0:
@@ -398,16 +425,22 @@ def main():
     peak, peak_kind = measured_peak()
     achieved = alg / (ms / args.steps / 1e3) / 1e9
     spl = ns if ns else 1  # steps per launch
+    traffic, traffic_how = traffic_record(
+        args.config + ("+int8" if args.weights == "int8" else "") +
+        (f"+b{B}" if args.batch is not None else "") +
+        (f"+paged{args.paged}" if args.paged else ""), spl)
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak,
-            "traffic": traffic_record(args.config + ("+int8" if args.weights == "int8" else ""),
-                                      spl),
+            "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_how,
+            "traffic_over_algorithmic": (traffic / (alg * spl)) if traffic else None,
             "peak_source": peak_kind, "algorithmic_bytes_per_launch": alg * spl,
             "kernel": "mk::mk_decode_kernel (persistent, %d step(s) per launch)" % spl}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": ms_step,
+        "ms_per_step_dist": {"p10": float(qs[0]), "median": float(qs[1]), "p90": float(qs[2]),
+                             "over": f"{len(per)} launches of {spl_} step(s)"},
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "int8 weights x f32" if args.weights == "int8" else "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "batch": B, "prefill": list(cfg["prefill"]),
@@ -437,6 +470,11 @@ def main():
                 abl[name] = None
         line["ablation_ms_per_step"] = abl
         line["ablation_launches_per_step"] = info["ablation_launches"]
+        # what each extra launch costs beyond the megakernel's step time: launch,
+        # drain and refill of the pipeline at every (layer, phase) boundary
+        line["ablation_overhead_us_per_launch"] = {
+            k: (None if v is None else (v - ms_step) * 1e3 / info["ablation_launches"])
+            for k, v in abl.items()}
 
     if args.trace:
         from decode_megakernel_sm_gb300.trace import chrome_trace, summarize

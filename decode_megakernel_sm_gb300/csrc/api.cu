@@ -53,7 +53,7 @@ struct Scratch {
   uint32_t* ctr;
   float* hglob;             // SiLU(gate)*up (split MLP)
   TagWord* xt;              // tagged block: x_{2l+2} (split MLP)
-  size_t xbuf_bytes, ctr_bytes, tag_bytes, total;
+  size_t xbuf_bytes, ctr_bytes, err_bytes, tag_bytes, total;
 };
 
 static size_t al256(size_t n) { return (n + 255) / 256 * 256; }
@@ -76,6 +76,7 @@ static Scratch carve_scratch(const mk_model_desc& d, size_t B, size_t kc, size_t
   Scratch s{};
   s.xbuf_bytes = sx;
   s.ctr_bytes = sc;
+  s.err_bytes = se;
   s.tag_bytes = sxt;
   s.total = sx + sq + sp + sr + 2 * sl + sc + se + 2 * sroute + sh + sxt;
   if (!base) return s;
@@ -121,7 +122,15 @@ struct mk_handle {
   void* scratch = nullptr;
   size_t scratch_bytes = 0;
   Scratch sc{};
-  std::vector<int> abl_keys;  // ablation launches (keys that own instructions)
+  // ablation: one launch per (layer, phase) key that owns instructions, each
+  // over compacted queues holding only that key's instructions
+  struct AblLaunch {
+    size_t off;   // first record of its queues in abl_sched
+    int n_q;      // queues (= CTAs of the launch): the SMs that own such instructions
+    int max_pc;   // records per queue, HALT included
+  };
+  std::vector<AblLaunch> abl;
+  Instr* abl_sched = nullptr;
   uint32_t epoch = 0;
   unsigned long long timeout_ns = 2000000000ull;
   int n_pollers = 1;
@@ -172,8 +181,11 @@ static void free_schedule(mk_handle* h) {
   for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
   h->graphs.clear();
   if (h->sched) cudaFree(h->sched);
+  if (h->abl_sched) cudaFree(h->abl_sched);
   if (h->scratch) cudaFree(h->scratch);
   h->sched = nullptr;
+  h->abl_sched = nullptr;
+  h->abl.clear();
   h->scratch = nullptr;
   if (h->d_tok) cudaFree(h->d_tok);
   h->d_tok = h->d_pos = h->d_am = nullptr;
@@ -576,14 +588,43 @@ extern "C" int mk_build_schedule(mk_handle* h, int batch, int max_ctx) {
   h->d_pos = (int32_t*)((char*)h->d_tok + al256(B * 4));
   h->d_am = (int32_t*)((char*)h->d_pos + al256(B * 4));
   h->d_logits = (float*)((char*)h->d_am + al256(B * 4));
-  std::vector<char> has(L * N_PHASES + 1, 0);
-  for (const Instr& I : p.q) {
-    if (I.op == OP_HALT || I.op == OP_NOP) continue;
-    has[I.op == OP_LMHEAD ? L * N_PHASES : I.layer * N_PHASES + phase_of(I.op)] = 1;
+  // ablation queues: for every (layer, phase) key in step order, each SM's
+  // instructions of that key alone (in queue order), one queue per SM that
+  // owns any, HALT-padded -- so a launch walks only its own work
+  {
+    auto key_of = [&](const Instr& I) {
+      return I.op == OP_LMHEAD ? L * N_PHASES : (size_t)I.layer * N_PHASES + phase_of(I.op);
+    };
+    Instr halt;
+    std::memset(&halt, 0, sizeof halt);
+    halt.op = OP_HALT;
+    std::vector<Instr> flat;
+    for (size_t k = 0; k < L * N_PHASES + 1; k++) {
+      std::vector<std::vector<Instr>> qs;
+      for (int sm = 0; sm < h->n_sm; sm++) {
+        std::vector<Instr> q;
+        for (int pc = 0; pc < p.max_pc; pc++) {
+          const Instr& I = p.q[(size_t)sm * p.max_pc + pc];
+          if (I.op == OP_HALT) break;
+          if (I.op != OP_NOP && key_of(I) == k) q.push_back(I);
+        }
+        if (!q.empty()) qs.push_back(std::move(q));
+      }
+      if (qs.empty()) continue;
+      size_t mx = 0;
+      for (auto& q : qs) mx = std::max(mx, q.size());
+      mk_handle::AblLaunch a{flat.size(), (int)qs.size(), (int)mx + 1};
+      for (auto& q : qs) {
+        q.resize(mx + 1, halt);
+        flat.insert(flat.end(), q.begin(), q.end());
+      }
+      h->abl.push_back(a);
+    }
+    CK(cudaMalloc(&h->abl_sched, flat.size() * sizeof(Instr)));
+    CK(cudaMemcpyAsync(h->abl_sched, flat.data(), flat.size() * sizeof(Instr),
+                       cudaMemcpyHostToDevice, h->own));
+    CK(cudaStreamSynchronize(h->own));  // before `flat` goes out of scope
   }
-  h->abl_keys.clear();
-  for (size_t k = 0; k < has.size(); k++)
-    if (has[k]) h->abl_keys.push_back((int)k);
   h->plan = std::move(p);
   h->batch = batch;
   h->max_ctx = max_ctx;
@@ -658,7 +699,6 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.qperm = h->qperm;
   g.n_steps = 1;
   g.n_lm = h->plan.n_lm;
-  g.sel_key = -1;
   g.trace = h->trace;
   g.l2_ahead = h->l2_ahead;
   g.hold_early = h->hold_early;
@@ -701,7 +741,7 @@ static void reset_after_error(mk_handle* h) {
   cudaMemset(h->sc.ctr, 0, h->sc.ctr_bytes);
   cudaMemset(h->sc.xbuf, 0, h->sc.xbuf_bytes);
   cudaMemset(h->sc.xt, 0, h->sc.tag_bytes);  // the next step is epoch 1 again
-  cudaMemset(h->sc.err, 0, 4 * sizeof(int));
+  cudaMemset(h->sc.err, 0, h->sc.err_bytes);
   cudaDeviceSynchronize();
   h->epoch = 0;
 }
@@ -739,15 +779,21 @@ extern "C" int mk_decode_step_host(mk_handle* h, const int32_t* h_tokens,
 }
 
 // ------------------------------------------------------------- ablation ----
+// One launch per (layer, phase), each over its own compacted queues and with
+// one CTA per queue.  Tracing and the race-stress queue permutation index the
+// full schedule, so neither applies here (stress delays still do).
 static cudaError_t launch_phases(mk_handle* h, Globals g, cudaStream_t s, bool pdl) {
-  for (size_t i = 0; i < h->abl_keys.size(); i++) {
-    g.sel_key = h->abl_keys[i];
+  g.trace = nullptr;
+  g.qperm = nullptr;
+  for (const mk_handle::AblLaunch& a : h->abl) {
+    g.sched = h->abl_sched + a.off;
+    g.max_pc = a.max_pc;
     g.pdl = pdl ? 1 : 0;
     void* args[] = {&g};
     cudaError_t e;
     if (pdl) {
       cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(h->n_sm);
+      cfg.gridDim = dim3(a.n_q);
       cfg.blockDim = dim3(NTHREADS);
       cfg.dynamicSmemBytes = (size_t)h->smem_bytes;
       cfg.stream = s;
@@ -758,7 +804,7 @@ static cudaError_t launch_phases(mk_handle* h, Globals g, cudaStream_t s, bool p
       cfg.numAttrs = 1;
       e = cudaLaunchKernelExC(&cfg, h->var->kernel, args);
     } else {
-      e = cudaLaunchKernel(h->var->kernel, dim3(h->n_sm), dim3(NTHREADS), args,
+      e = cudaLaunchKernel(h->var->kernel, dim3(a.n_q), dim3(NTHREADS), args,
                            (size_t)h->smem_bytes, s);
     }
     if (e != cudaSuccess) return e;
@@ -899,11 +945,14 @@ extern "C" int mk_decode_step_noalloc(mk_handle* h, const int32_t* d_tokens,
   g.err = sc.err;
   g.xt = sc.xt;
   g.hglob = sc.hglob;
+  g.routes = sc.routes;    // MoE routing of this call, in the array as well
+  g.rweight = sc.rweight;
   // the array keeps the previous call's contents: clear what must start at
   // zero (residual accumulators of both parities, counters, error word, step
   // tags) and run the step as epoch 1
   CK(cudaMemsetAsync(g.xbuf, 0, sc.xbuf_bytes, s));
-  CK(cudaMemsetAsync(g.ctr, 0, sc.ctr_bytes + 256, s));
+  CK(cudaMemsetAsync(g.ctr, 0, sc.ctr_bytes, s));
+  CK(cudaMemsetAsync(g.err, 0, sc.err_bytes, s));
   CK(cudaMemsetAsync(g.xt, 0, sc.tag_bytes, s));
   g.epoch = 1;
   g.zero_next = 0;
@@ -1082,7 +1131,7 @@ extern "C" int mk_get_info(const mk_handle* h, mk_info* out) {
   out->n_counters = h->plan.n_ctr;
   out->attn_splits = h->plan.splits;
   out->launches_per_step = 1;
-  out->ablation_launches = (int)h->abl_keys.size();
+  out->ablation_launches = (int)h->abl.size();
   out->batch = h->batch;
   out->max_ctx = h->max_ctx;
   out->packed_bytes = h->packed_bytes;

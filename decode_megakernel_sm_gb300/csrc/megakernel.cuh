@@ -1725,12 +1725,6 @@ MK_DEV Instr load_instr(const Globals& g, int sm, int pc) {
   return I;
 }
 
-MK_DEV bool selected(const Globals& g, const Instr& I) {
-  if (g.sel_key < 0) return true;
-  const int key = I.op == OP_LMHEAD ? g.L * N_PHASES : I.layer * N_PHASES + phase_of(I.op);
-  return key == g.sel_key;
-}
-
 // Second cursor of the producer: walks the same chunk sequence as the ring
 // cursor.  Only while the ring is full (the consumers are waiting on a
 // dependency and the producer is blocked) does it warm L2 with the chunks
@@ -1763,7 +1757,7 @@ struct L2Cursor {
           done = true;
           return;
         }
-        if (I.op == OP_NOP || !selected(g, I)) {
+        if (I.op == OP_NOP) {
           pc++;
           continue;
         }
@@ -1846,7 +1840,7 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
       step_ready = false;
       continue;
     }
-    if (I.op == OP_NOP || !selected(g, I)) continue;
+    if (I.op == OP_NOP) continue;
     if (g.stress_ns) {
       if (lane == 0) stress_delay(g, qid, pc, t, 0x5EEDu);
       __syncwarp();
@@ -2176,7 +2170,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
       const Instr I = next;
       if (I.op == OP_HALT) break;
       if (pc + 1 < g.max_pc) next = load_instr(g, qid, pc + 1);
-      if (I.op == OP_NOP || !selected(g, I)) continue;
+      if (I.op == OP_NOP) continue;
       c.pc = pc;
       // race stress: thread 0 starts late; the op's dependency wait holds the rest
       if (g.stress_ns && tid == 0) stress_delay(g, qid, pc, step, 0xC0DEu);

@@ -33,8 +33,9 @@ enum Op : uint8_t {
   OP_MLP_DOWN = 9,  // down-projection rows over the whole h + residual (split MLP)
 };
 
-// Ablation phases: one launch per (layer, phase).  No instruction waits on a
-// counter signalled by an instruction of its own phase.
+// Ablation phases: one launch per (layer, phase), each over queues that hold
+// only that phase's instructions.  No instruction waits on a counter
+// signalled by an instruction of its own phase.
 enum Phase : int {
   PH_QKV = 0, PH_ATTN = 1, PH_OPROJ = 2, PH_ROUTER = 3, PH_MLP = 4, PH_DOWN = 5, N_PHASES = 6
 };
@@ -238,7 +239,6 @@ struct Globals {
   uint32_t stress_ns, stress_seed;
   const int* qperm;
   int n_lm;
-  int sel_key;             // -1: run every instruction; else only key == sel_key (ablation)
   int zero_next;           // the LM head slices zero the next step's residual buffers (the
                            // other parity, epoch + 1 & 1) while they wait for their input
   int pdl;                 // ablation with programmatic dependent launch

@@ -102,6 +102,16 @@ typedef struct {
 /* Create a handle on the current CUDA device: validates the shape, selects
  * the compiled kernel variant (MK_ERR_UNSUPPORTED if none), copies and packs
  * the weights on the device (synchronous), allocates counters and scratch.
+ * Passage: "Megakernels: Deleting the Kernel Boundary to Win Back
+ * Microseconds", opening paragraph (batch-1 decode reads every weight once
+ * per forward pass, so the packed weights are laid out for one contiguous
+ * stream per instruction) and section "Correctness without the free
+ * barrier", last paragraph (weights prefetched into paged shared memory:
+ * here a bulk-copy ring, which is why every matrix is re-laid out).
+ * Ownership: the caller keeps its weights (read only during the call) and
+ * its KV cache (must outlive the handle); the library owns the packed copy.
+ * Errors: MK_ERR_INVALID_ARG for a NULL or non-16-byte-aligned pointer or an
+ * inconsistent shape, MK_ERR_UNSUPPORTED, MK_ERR_CUDA.
  * On error *out is NULL and nothing is leaked.                            */
 int mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv, mk_handle** out);
 
@@ -109,8 +119,8 @@ int mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv, m
 #define MK_WEIGHTS_BF16 0 /* as mk_create */
 #define MK_WEIGHTS_INT8 1 /* int8 codes with one fp32 scale per row           */
 
-/* mk_create with a choice of streamed weight format (the survey's "INT8 /
- * FP8 weights" next step; "Gemma 4 TPU megakernel", section "What's next":
+/* mk_create with a choice of streamed weight format (int8 weight
+ * streaming; "Gemma 4 TPU megakernel", section "What's next":
  * the same kernel reaches a higher rate with INT8 experts, because decode is
  * bound by the weight bytes it reads).  The caller still passes bf16 weights.
  * MK_WEIGHTS_INT8 quantises every streamed matrix on the device, row by row,
@@ -138,7 +148,7 @@ int mk_create_ex(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv
 int mk_quantize_rows_int8(const void* d_w, long rows, int cols, int8_t* d_codes, float* d_scales,
                           void* stream);
 
-/* Paged KV cache (the survey's "paged KV cache" next step; the blocks of
+/* Paged KV cache (long-context decode over a block-table cache; the blocks of
  * vLLM-style serving).  From the next step on, kv->k[l] / kv->v[l] given to
  * mk_create point at pools [n_blocks][n_kv_heads][block][head_dim] (bf16,
  * 16-byte aligned), and cache row p of sequence b lives in block
@@ -172,7 +182,7 @@ int mk_set_kv_pages(mk_handle* h, int block, int n_blocks, const int32_t* d_tabl
 #define MK_DBG_H 2
 int mk_debug_read(mk_handle* h, int what, int layer, float* out, size_t n);
 
-/* Race stress for tests (the survey's race-stress test level; the hazard is
+/* Race stress for tests (a stress level for the counter protocol; the hazard is
  * the missing fence that "Megakernels: Deleting the Kernel Boundary",
  * section "Correctness without the free barrier", warns of).  With
  * max_delay_ns > 0 the producer warp and consumer thread 0 of every CTA
@@ -190,10 +200,28 @@ int mk_set_race_stress(mk_handle* h, unsigned max_delay_ns, unsigned seed, int p
  * byte-balanced row ranges, one split-KV attention work item per
  * (sequence, kv head, split), assigns counter ids and targets, checks the
  * queues for deadlock and coverage on the host (MK_ERR_SCHEDULE), uploads
- * them and zeroes the counters.  Synchronous.  Must precede any step.     */
+ * them and zeroes the counters.  Synchronous.  Must precede any step.
+ * Passage: "Megakernels: Deleting the Kernel Boundary to Win Back
+ * Microseconds", section "One launch, one interpreter" (the per-SM
+ * instruction schedule is computed on the host ahead of time and reused for
+ * many forward passes) and section "Correctness without the free barrier"
+ * (a counter array in global memory, zeroed before the launch, replaces the
+ * kernel boundaries); the byte balance answers the wave-quantisation tail of
+ * section "Where the microseconds go".
+ * Errors: MK_ERR_INVALID_ARG (batch outside [1, max_batch], max_ctx outside
+ * [1, max_seq]), MK_ERR_UNSUPPORTED, MK_ERR_SCHEDULE, MK_ERR_CUDA; the
+ * previous schedule is dropped in every case.                             */
 int mk_build_schedule(mk_handle* h, int batch, int max_ctx);
 
 /* One decode step, asynchronous on `stream`, one kernel launch.
+ * Passage: "Megakernels: Deleting the Kernel Boundary to Win Back
+ * Microseconds", section "One launch, one interpreter" (one persistent
+ * kernel, one block per SM, runs the whole forward pass: RMSNorm + QKV +
+ * RoPE, attention and its reduce, O-projection + residual, RMSNorm + gate/up
+ * + SiLU, down + residual, final RMSNorm + LM head) and the page's opening
+ * paragraph (a token per pass; here the argmax of the logits).
+ * All buffers are caller-owned device memory; the library writes d_logits,
+ * d_argmax and cache row P of every layer.
  *   d_tokens    [batch] int32: token fed at this step (may alias the d_argmax
  *               of the previous step);
  *   d_positions [batch] int32: P, the cache row written by this step; each
@@ -258,6 +286,9 @@ int mk_decode_step_ablation(mk_handle* h, int mode, const int32_t* d_tokens,
  * have a schedule (built earlier, by a caller that could allocate).
  *   d_status (may be NULL): [1] int32 device output that receives the step's
  *            device status (MK_OK, MK_ERR_TIMEOUT, MK_ERR_INVALID_ARG, ...).
+ * Everything the step writes besides the caller's outputs and KV cache
+ * (MoE routing included) stays in the array, so mk_get_routes and
+ * mk_debug_read keep reporting the handle's own most recent step.
  * Returns MK_ERR_SCRATCH, with nothing launched, if the handle's schedule
  * needs more than 16 MiB of scratch.  Each call clears the parts of the
  * array that must start at zero, on `stream`, before its launch; all calls
@@ -271,7 +302,14 @@ int mk_decode_step_noalloc(mk_handle* h, const int32_t* d_tokens, const int32_t*
 
 /* Wait for `stream` and return the device error word (MK_OK if none).  A
  * non-OK result also resets the counters and scratch so that the next step
- * starts clean (the KV rows written by the failed step are unspecified).  */
+ * starts clean (the KV rows written by the failed step are unspecified).
+ * Passage: "Megakernels: Deleting the Kernel Boundary to Win Back
+ * Microseconds", section "Correctness without the free barrier": the
+ * consumer there spins until a counter reaches its target; here every such
+ * wait is bounded in time, and a wait that runs out, or a bad input, sets
+ * the error word this call reads instead of hanging the GPU.
+ * Errors: MK_ERR_INVALID_ARG (NULL handle), MK_ERR_CUDA (the stream failed),
+ * or the device status itself (MK_ERR_TIMEOUT, MK_ERR_INVALID_ARG, ...).  */
 int mk_sync_status(mk_handle* h, void* stream);
 
 /* Limit, in nanoseconds, of every device-side wait (default 2 s). */
@@ -354,7 +392,11 @@ int mk_get_info(const mk_handle* h, mk_info* out);
 /* MoE only: the expert ids the router chose at the most recent step,
  * [n_layers][top_k] int32 in selection order (largest router logit first,
  * lower id first on ties; "Gemma 4 TPU megakernel", section "Megakernels
- * for Gemma 4", component "Router").  Waits for the device.  n = capacity. */
+ * for Gemma 4", component "Router").  Waits for the device.  n = capacity.
+ * "Most recent step" means the handle's own steps (mk_decode_step, the
+ * host-buffer step, the last step of mk_decode_steps, the ablation): a
+ * mk_decode_step_noalloc call keeps its routing in the library's fixed
+ * array, so this call does not see it.                                     */
 int mk_get_routes(mk_handle* h, int32_t* out, size_t n);
 
 /* Replace instruction `pc` of SM `sm` by a no-op that neither waits nor
@@ -379,7 +421,16 @@ int mk_debug_drop_instruction(mk_handle* h, int sm, int pc);
 int mk_set_trace(mk_handle* h, int on);
 int mk_get_trace(mk_handle* h, uint64_t* out, size_t n);
 
+/* Release everything the library owns for the handle (packed weights,
+ * schedule, scratch, streams), after waiting for the handle's own stream.
+ * The pages have no counterpart: it ends the life cycle that mk_create
+ * starts.  The caller's weights, KV cache and buffers are untouched.
+ * MK_ERR_INVALID_ARG for a NULL handle.                                    */
 int mk_destroy(mk_handle* h);
+
+/* A static, NUL-terminated English description of a status code (never
+ * NULL; "unknown status" for codes this library does not define).  No
+ * counterpart in the pages: the library's own error reporting.             */
 const char* mk_status_string(int status);
 
 /* ---- host-only planning (no GPU needed) ---------------------------------

@@ -45,6 +45,12 @@ def test_intermediates_llama1b():
     _check(synth.CONFIGS["llama1b_1k"], 103)
 
 
+def test_intermediates_llama1b_b8_full_config():
+    # the full batch-8 workload (16 layers, lengths U[512, 2048]): q and every
+    # residual of every sequence
+    _check(synth.CONFIGS["llama1b_b8"], 109)
+
+
 @pytest.mark.parametrize("ffn", [2048, 3000])
 def test_intermediates_batch8(ffn):
     # ffn 2048: the batched split MLP; 3000: fused MLP slices with atomics

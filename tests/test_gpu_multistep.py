@@ -29,8 +29,12 @@ def test_multistep_dense_against_oracle():
 
 
 def test_multistep_llama1b_against_oracle():
+    # one launch of 16 greedy steps (the bench's launch), every step's argmax
+    # against the teacher-forced oracle, the last logits and all 16 appended
+    # K/V rows of every layer; then a second launch continues the sequence
     r = Run(synth.CONFIGS["llama1b_1k"], seed=4)
     try:
+        r.multi_step(16)
         r.multi_step(4)
     finally:
         r.close()

@@ -161,6 +161,16 @@ def test_llama1b_8k_parity():
     run_steps(synth.CONFIGS["llama1b_8k"], 2, seed=1)
 
 
+def test_llama1b_b8_full_config_parity():
+    # the full batch-8 workload: 16 layers, vocab 128256, eight sequences
+    # with their own cache lengths drawn from U[512, 2048]; every step's
+    # logits, argmax and appended K/V rows of every sequence against the
+    # oracle
+    cfg = synth.CONFIGS["llama1b_b8"]
+    worst = run_steps(cfg, 3, seed=0)
+    print(f"llama1b_b8 worst max|dlogit|/std = {worst:.2e}")
+
+
 def _moe_small_cfg():
     # MoE variant (hidden 2048, head_dim 128, 4 q heads per kv head) at a reduced
     # size: 16 experts, top-4, shared expert, ragged FFN widths

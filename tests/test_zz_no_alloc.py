@@ -1,13 +1,17 @@
-"""The decode step that allocates nothing, checked against the regular step.
+"""The decode step that allocates nothing, checked against the regular step and
+against the oracle.
 
 Callers that may not allocate device memory while they decode -- because an
 outside allocator or a fixed budget owns the device memory, or because the
 decoding thread must stay off the synchronising cudaMalloc/cudaFree paths --
 use mk_decode_step_noalloc, whose scratch is a fixed array inside the library.
-These tests call it through the C ABI and compare it with mk_decode_step on
-the same inputs, two calls in a row, with the tolerance of the parity tests.
-This file is collected last so that a run stopping at the first failure has
-already run every other test.
+These tests call it through the C ABI on the same inputs as mk_decode_step,
+two calls in a row, and hold both results to the parity tests' tolerance:
+the no-allocation logits against the regular step's and against the oracle
+teacher-forced on the same tokens.  The shapes cover batch 1 (small and
+Llama-1B), a small MoE (its routing lives in the fixed array too) and a
+batch-8 shape with the batched MLP.  This file is collected last so that a
+run stopping at the first failure has already run every other test.
 """
 import ctypes as C
 
@@ -21,6 +25,20 @@ from tests.harness import Run
 
 pytestmark = pytest.mark.gpu
 
+CASES = {
+    "tiny": synth.CONFIGS["tiny"],
+    "llama1b_1k": synth.CONFIGS["llama1b_1k"],
+    # 16 experts, top-4, a shared expert, ragged widths
+    "moe_small": synth.custom(n_layers=3, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=128,
+                              ffn=0, vocab=3001, tied=False, n_experts=16, top_k=4,
+                              expert_ffn=200, shared_ffn=500, rope_theta=5e5, prefill=(70, 70),
+                              steps=4),
+    # eight sequences, ragged lengths, the batched split MLP (h as fragments)
+    "batch8": synth.custom(n_layers=2, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=64,
+                           ffn=2048, vocab=5000, batch=8, prefill=(0, 300), steps=4,
+                           rope_theta=5e5),
+}
+
 
 def _noalloc(r, logits, am, status):
     stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
@@ -33,9 +51,16 @@ def _noalloc(r, logits, am, status):
     return logits.cpu().numpy().astype(np.float64), am.cpu().numpy()
 
 
-@pytest.mark.parametrize("name", ["tiny", "llama1b_1k"])
-def test_noalloc_step_matches_regular_step_on_two_calls(name):
-    r = Run(synth.CONFIGS[name], seed=13)
+def _oracle(r):
+    if r.cfg.get("n_experts", 0) > 0:  # routing near-ties follow the regular step's routes
+        return r._oracle_moe_step()
+    lo, ao, _, _ = r.om.step(r.ko, r.vo, r.tokens, r.pos)
+    return lo, ao
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_noalloc_step_matches_regular_step_and_oracle_on_two_calls(name):
+    r = Run(CASES[name], seed=13)
     try:
         V = r.cfg["vocab"]
         logits = torch.full((r.B, V), float("nan"), dtype=torch.float32, device="cuda")
@@ -43,8 +68,11 @@ def test_noalloc_step_matches_regular_step_on_two_calls(name):
         status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
         for _ in range(2):
             lg_ref, am_ref = r.gpu_step("mega")       # the existing entry point
+            lo, ao = _oracle(r)                        # same tokens and positions
+            r.check(lg_ref, am_ref, lo, ao)
             lg, a = _noalloc(r, logits, am, status)   # same inputs, same cache row P
-            r.check(lg, a, lg_ref, am_ref)
+            r.check(lg, a, lg_ref, am_ref)            # against the regular step
+            r.check(lg, a, lo, ao)                    # and against the oracle
             r.tokens = [int(x) for x in am_ref]
             r.pos = [p + 1 for p in r.pos]
     finally:
