@@ -237,8 +237,6 @@ static int size_ring(mk_handle* h, int stage_bytes) {
   const mk_model_desc& d = h->d;
   const int K = d.n_experts > 0 ? d.top_k : 0;
   const int HPG = d.n_q_heads / d.n_kv_heads;
-  // batched split down: a stage carries a weight unit and its h fragments
-  if (mlp_split_batched(d) && stage_bytes < 2 * BD_ROWS * BD_KC * 2) return MK_ERR_UNSUPPORTED;
   int optin = 0;
   CK(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->dev));
   int ns = 0;

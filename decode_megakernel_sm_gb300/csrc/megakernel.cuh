@@ -160,12 +160,9 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
       return 1;
     case OP_MLP_DOWN:
       if (g.bsplit) {
-        // BD_ROWS rows; per chunk of BD_KC columns, the weight unit (lower
-        // half of a stage) and that chunk's h fragments (upper half)
-        const uint32_t nkc = (uint32_t)g.F / BD_KC, unit = BD_ROWS * BD_KC * 2u;
-        s[0] = {(const unsigned char*)(Lp->wdT + (size_t)(I.r0 / BD_ROWS) * nkc * BD_ROWS * BD_KC),
-                (const unsigned char*)g.hglob + (size_t)I.layer * (g.F / 16) * 512, unit, nkc,
-                (SBY / 2) / unit};
+        // the run [r0, r1) of chunk-major weight units (BD_ROWS x BD_KC, 16 KB)
+        const uint32_t unit = BD_ROWS * BD_KC * 2u;
+        s[0] = {(const unsigned char*)Lp->wdT + (size_t)I.r0 * unit, nullptr, unit, n, SBY / unit};
         return 1;
       }
       // rows of the row-major [H][F] down projection
@@ -197,21 +194,29 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
 // x_j (j = 0: the embedding row of the token).  The gain slice of each
 // thread is loaded before the dependency wait (norm_gain), the rest after
 // it (norm_apply).  All consumer threads.
-template <int HT>
+template <int HT, int NB>
 struct NormGain {
   static constexpr int GROUPS = HT / 8;
   static constexpr int GPT = (GROUPS + NCT - 1) / NCT;
-  uint4 w[GPT];  // 8 packed bf16 gains per 8-column group
-  const uint16_t* src;  // the gain vector (batched variants read it per column)
+  static constexpr int KPT = (HT + NCT - 1) / NCT;  // batched: columns tid + q * NCT
+  uint4 w[NB == 1 ? GPT : 1];    // batch 1: 8 packed bf16 gains per 8-column group
+  float gw[NB == 1 ? 1 : KPT];   // batched: this thread's columns' gains
 };
 
-template <int HT>
-MK_DEV void norm_gain(NormGain<HT>& ng, const uint16_t* gain, int tid) {
-  ng.src = gain;
+template <int HT, int NB>
+MK_DEV void norm_gain(NormGain<HT, NB>& ng, const uint16_t* gain, int tid) {
+  if constexpr (NB == 1) {
 #pragma unroll
-  for (int q = 0; q < NormGain<HT>::GPT; q++) {
-    const int gi = tid + q * NCT;
-    if (gi < NormGain<HT>::GROUPS) ng.w[q] = __ldg((const uint4*)gain + gi);
+    for (int q = 0; q < NormGain<HT, NB>::GPT; q++) {
+      const int gi = tid + q * NCT;
+      if (gi < NormGain<HT, NB>::GROUPS) ng.w[q] = __ldg((const uint4*)gain + gi);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < NormGain<HT, NB>::KPT; q++) {
+      const int k = tid + q * NCT;
+      ng.gw[q] = k < HT ? bf1(__ldg(gain + k)) : 0.f;
+    }
   }
 }
 
@@ -225,10 +230,12 @@ MK_DEV void norm_gain(NormGain<HT>& ng, const uint16_t* gain, int tid) {
 // columns 2t, 2t+1 and 2t+8, 2t+9.
 template <int HT, int D, int HPG, int NB, int WB>
 MK_DEV bool norm_apply_batched(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, int j,
-                               const uint16_t* gain) {
+                               const NormGain<HT, NB>& ng) {
   static_assert(NB == 8, "k-tile blocks of 16 columns x 8 sequences");
   constexpr int KPT = (HT + NCT - 1) / NCT;  // columns per thread
-  constexpr int CH = 5;                      // columns whose loads are in flight together
+  // every load of the pass in flight at once: under a streaming ring each L2
+  // round trip costs microseconds, so the pass takes one
+  constexpr int CH = KPT;
   float ss[NB];
 #pragma unroll
   for (int b = 0; b < NB; b++) ss[b] = 0.f;
@@ -283,12 +290,7 @@ MK_DEV bool norm_apply_batched(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, int
       }
     }
   }
-  float gw[KPT];
-#pragma unroll
-  for (int q = 0; q < KPT; q++) {
-    const int k = c.tid + q * NCT;
-    gw[q] = k < HT ? bf1(__ldg(gain + k)) : 0.f;
-  }
+  const float* gw = ng.gw;  // loaded before the dependency wait
 #pragma unroll
   for (int b = 0; b < NB; b++) {
     const float t = warp_sum(ss[b]);
@@ -332,11 +334,12 @@ MK_DEV bool norm_apply_batched(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, int
 }
 
 template <int HT, int D, int HPG, int NB, int WB>
-MK_DEV bool norm_apply(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, int j, const NormGain<HT>& ng) {
+MK_DEV bool norm_apply(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, int j,
+                       const NormGain<HT, NB>& ng) {
   if constexpr (NB > 1) {
-    return norm_apply_batched(c, g, j, ng.src);
+    return norm_apply_batched(c, g, j, ng);
   } else {
-  constexpr int GROUPS = NormGain<HT>::GROUPS, GPT = NormGain<HT>::GPT;
+  constexpr int GROUPS = NormGain<HT, NB>::GROUPS, GPT = NormGain<HT, NB>::GPT;
   // split MLP: x_{2l+2} (j even, j > 0) arrives as tagged words from the
   // down rows' owners; each thread polls its own 8-element groups
   const bool tagged = g.xtag && j > 0 && (j & 1) == 0;
@@ -671,7 +674,7 @@ MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I)
   static_assert(MAX_ROWS <= 2 * NCT, "one rotary pair per thread");
   const LayerPtrs& Lp = g.layers[I.layer];
   const bool cached = (I.flags & F_NORM_CACHED) != 0;
-  NormGain<HT> ng;
+  NormGain<HT, NB> ng;
   if (!cached) norm_gain(ng, Lp.attn_norm, c.tid);
   // this thread's rotary pair: head slot hs, dims (t, t + D/2), and its
   // cos/sin at P -- none of it depends on the wait
@@ -921,9 +924,7 @@ MK_DEV void merge_heads(C& c, const Globals& g, const float* pm, const float* pl
 // atomics; the head-0 instructions also add the residual x_{2l}.
 template <int HT, int D, int HPG, int NB, int WB>
 MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
-  constexpr int LPR = D / 8, SPW = 32 / LPR;
   constexpr int SG = (NCT / (NB * D)) > 0 ? NCT / (NB * D) : 1;  // slice groups per (b, dim)
-  const int slot = c.lane / LPR, dsl = c.lane % LPR;
   const int h = I.g, l = I.layer;
   const int S = g.splits;
   constexpr int PS = part_stride(D);  // partial record stride
@@ -1141,60 +1142,64 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& 
       c.ring.release(c.lane);
     }
   } else {
-  float a[NB][8];
+    // Batched (8 sequences): y[b][row] = Wo_h[row] . attn_h[b] on the tensor
+    // cores, mma.sync m16n8k16 with f32 accumulators.  A = the head's
+    // attention output as the batched GEMV holds activations (rows 0-7 the
+    // bf16 high parts of the 8 sequences, rows 8-15 the bf16 remainders, so
+    // the sum of the two halves keeps about 16 mantissa bits), built once in
+    // registers for the D / 16 k-tiles; B = 8 Wo rows per n-tile, loaded with
+    // ldmatrix from the chunk-swizzled stage (chunk k of row r at slot
+    // k ^ (r & 7): the 8 row reads of a matrix hit 8 bank groups).  Lane
+    // 4g + t ends with sequence g's outputs of rows 2t, 2t + 1 of the n-tile
+    // and adds them into x_{2l+1} with one 8-byte reduction (the planner cuts
+    // batched O-projection rows at multiples of 8, so the pair is aligned).
+    static_assert(NB == 8 && D == 64, "fragments of 8 sequences, 4 k-tiles");
+    constexpr int KT = D / 16;
+    const int gq = c.lane >> 2, tq = c.lane & 3;
+    uint32_t af[KT][4];
 #pragma unroll
-  for (int b = 0; b < NB; b++)
-#pragma unroll
-    for (int j = 0; j < 8; j++) a[b][j] = c.attn[b * D + dsl * 8 + j];
-  for (uint32_t u0 = 0; u0 < wseg.n; u0 += wseg.ups) {
-    const uint32_t n = min(wseg.ups, wseg.n - u0);
-    if (!c.ring.acquire(g)) break;
-    const unsigned char* st = c.ring.stage_ptr();
-    // two passes of SPW rows per iteration: independent loads, FMA chains
-    // and shuffles, so each warp keeps two rows' latencies in flight
-    constexpr uint32_t STEP = NCW * SPW;
-    for (uint32_t jb = (uint32_t)c.warp * SPW; jb < n; jb += 2 * STEP) {
-      float y[2][NB];
-#pragma unroll
-      for (int p = 0; p < 2; p++) {
-        const uint32_t j = jb + p * STEP + slot;
-        const uint32_t key = (I.r0 + u0 + j) & 7u;  // chunk swizzle of this row
-        float wf[8];
-        unpack8(j < n ? *(const uint4*)(st + (size_t)j * D * 2 + ((dsl ^ key) * 16)) : zero, wf);
-#pragma unroll
-        for (int b = 0; b < NB; b++) {
-          float v0 = 0.f, v1 = 0.f;
-#pragma unroll
-          for (int k = 0; k < 8; k += 2) {
-            v0 = fmaf(a[b][k], wf[k], v0);
-            v1 = fmaf(a[b][k + 1], wf[k + 1], v1);
-          }
-          y[p][b] = v0 + v1;
-        }
-      }
-#pragma unroll
-      for (int off = LPR / 2; off > 0; off >>= 1)
-#pragma unroll
-        for (int p = 0; p < 2; p++)
-#pragma unroll
-          for (int b = 0; b < NB; b++) y[p][b] += __shfl_xor_sync(0xFFFFFFFFu, y[p][b], off);
-      if (dsl == 0) {
-#pragma unroll
-        for (int p = 0; p < 2; p++) {
-          const uint32_t j = jb + p * STEP + slot;
-          if (j < n) {
-            const int r = (int)(I.r0 + u0 + j);
-            for (int b = 0; b < g.B && b < NB; b++) {
-              float v = y[p][b];
-              if (resid) v += xr_s[b * nr + (r - (int)I.r0)];
-              red_add_f32(xres_mine(g, c.epoch, 2 * l + 1, b) + r, v);
-            }
-          }
-        }
-      }
+    for (int kt = 0; kt < KT; kt++) {
+      const float* ap = c.attn + gq * D + kt * 16 + 2 * tq;
+      split2(ap[0], ap[1], af[kt][0], af[kt][1]);
+      split2(ap[8], ap[9], af[kt][2], af[kt][3]);
     }
-    c.ring.release(c.lane);
-  }
+    const bool live = gq < g.B;
+    float* dst = xres_mine(g, c.epoch, 2 * l + 1, live ? gq : 0);
+    const uint32_t li = (uint32_t)c.lane & 7u, mi = (uint32_t)c.lane >> 3;
+    uint32_t tc = 0;  // 8-row tiles of earlier stages (round-robin offset)
+    for (uint32_t u0 = 0; u0 < wseg.n; u0 += wseg.ups) {
+      const uint32_t n = min(wseg.ups, wseg.n - u0);
+      if (!c.ring.acquire(g)) break;
+      const uint32_t sbase = smem_u32(c.ring.stage_ptr());
+      const uint32_t nt = (n + 7) / 8;
+      for (uint32_t t = (uint32_t)(c.warp + NCW - (int)(tc % NCW)) % NCW; t < nt; t += NCW) {
+        // rows past the stage's last repeat row 8t (their outputs are dropped)
+        const uint32_t rr = t * 8 + li < n ? t * 8 + li : t * 8;
+        const uint32_t key = (I.r0 + u0 + rr) & 7u;
+        const uint32_t ra = sbase + rr * (uint32_t)(D * 2);
+        uint32_t b[8];
+        ldsm_x4(ra + ((mi ^ key) << 4), b[0], b[1], b[2], b[3]);
+        ldsm_x4(ra + (((mi + 4u) ^ key) << 4), b[4], b[5], b[6], b[7]);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kt = 0; kt < KT; kt++) mma_16816(d, af[kt], b[2 * kt], b[2 * kt + 1]);
+        const uint32_t r = t * 8 + 2u * (uint32_t)tq;  // stage row of this lane's pair
+        if (live && r < n) {
+          const int row = (int)(I.r0 + u0 + r);
+          float v0 = d[0] + d[2], v1 = d[1] + d[3];
+          if (resid) {
+            v0 += xr_s[gq * nr + (row - (int)I.r0)];
+            if (r + 1 < n) v1 += xr_s[gq * nr + (row + 1 - (int)I.r0)];
+          }
+          if (r + 1 < n)
+            red_add_v2f32(dst + row, v0, v1);
+          else
+            red_add_f32(dst + row, v0);
+        }
+      }
+      tc += nt;
+      c.ring.release(c.lane);
+    }
   }
   c.mark(g, 1);
   consumer_bar();
@@ -1205,7 +1210,7 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& 
 template <int HT, int D, int HPG, int NB, int WB>
 MK_DEV bool op_router(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
   const LayerPtrs& Lp = g.layers[I.layer];
-  NormGain<HT> ng;
+  NormGain<HT, NB> ng;
   norm_gain(ng, Lp.mlp_norm, c.tid);
   if (!dep_wait(c, g, I)) return false;
   if (!norm_apply(c, g, 2 * I.layer + 1, ng)) return false;
@@ -1277,7 +1282,7 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I)
   const LayerPtrs& Lp = g.layers[l];
   const bool routed = g.E > 0 && !(I.flags & F_SHARED);
   const bool cached = (I.flags & F_NORM_CACHED) != 0;
-  NormGain<HT> ng;
+  NormGain<HT, NB> ng;
   if (!cached) norm_gain(ng, Lp.mlp_norm, c.tid);
   if (!dep_wait(c, g, I)) return false;
   if (!cached && !norm_apply(c, g, 2 * l + 1, ng)) return false;
@@ -1370,7 +1375,7 @@ MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr&
   const int l = I.layer;
   const LayerPtrs& Lp = g.layers[l];
   const bool cached = (I.flags & F_NORM_CACHED) != 0;
-  NormGain<HT> ng;
+  NormGain<HT, NB> ng;
   if (!cached) norm_gain(ng, Lp.mlp_norm, c.tid);
   // int8: the gate / up row scales of this thread's FFN column (NB == 1:
   // one column per thread)
@@ -1417,8 +1422,6 @@ MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr&
       split2(hp[8], hp[9], f.z, f.w);
       hf[it] = f;
     }
-    // the down instructions copy these fragments with the bulk-copy engine
-    asm volatile("fence.proxy.async.global;" ::: "memory");
   } else {
     for (int t = c.tid; t < NB * ncol; t += NCT) {
       const int b = t / ncol, j = t % ncol;
@@ -1444,74 +1447,95 @@ MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr&
 template <int HT, int D, int HPG, int NB, int WB>
 MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
   if constexpr (NB != 1) {
-    // Batched (8 sequences): BD_ROWS rows.  Each ring stage holds, per
-    // chunk of BD_KC columns, the rows' weight unit (lower half, chunk
-    // q of unit row i at slot q ^ (i & 7)) and the chunk's h fragments
-    // (upper half) as the gate/up slices wrote them.  Tensor cores: A = h
-    // (rows 0-7 the hi parts of 8 sequences, rows 8-15 the lo parts), B =
-    // 8 weight rows (ldmatrix); a chunk's BD_KC / 16 k-tiles are split over
-    // the warps.  Per-warp partial sums meet in shared memory at the end;
-    // each row has one writer (plain stores).
+    // Batched (8 sequences): a run [r0, r1) of chunk-major units (chunk q,
+    // row block rb) = unit q * NRB + rb, spanning chunks q0 and at most q0 + 1.
+    // After the gate/up counter the consumers copy those chunks' h fragments
+    // (A fragments as the gate/up slices wrote them: rows 0-7 the hi parts of
+    // 8 sequences, rows 8-15 the lo parts) into shared memory with cp.async,
+    // and the residual rows of any chunk-0 unit; the units' weights stream
+    // through the ring (chunk q' of unit row i at slot q' ^ (i & 7)).  Warp
+    // w takes the run's units w, w + NCW, ... whole: 32 k-tiles, B = 8
+    // weight rows by ldmatrix, two accumulators for rows 0-7 and 8-15, so no
+    // cross-warp sum is needed.  Each lane then adds sequence g's outputs of
+    // two row pairs into x_{2l+2} with 8-byte float reductions.
     static_assert(NB == 8, "fragments of 8 sequences");
     constexpr int KT = BD_KC / 16;                        // k-tiles per chunk
     constexpr uint32_t UNIT = BD_ROWS * BD_KC * 2u;       // bytes of a weight unit
+    constexpr int RES_MAX = BD_MAX_UNITS * BD_ROWS * NB;  // residual values of chunk-0 units
+    static_assert(2 * KT * 32 * 16 + RES_MAX * 4 <= NB * HT * 4, "h + residual fit xn");
     const int l = I.layer;
+    const uint32_t NRB = (uint32_t)g.H / BD_ROWS;
+    const uint32_t u0 = I.r0, u1 = I.r1, q0 = u0 / NRB;
+    const uint32_t nq = (u1 - 1) / NRB - q0 + 1;  // 1 or 2 chunks of h
     if (!dep_wait(c, g, I)) return false;
-    float* res = c.yrow;  // [BD_ROWS][NB] residual rows x_{2l+1}
-    for (int t = c.tid; t < BD_ROWS * NB; t += NCT) {
-      const int r = t / NB, b = t % NB;
-      res[t] = b < g.B ? xres_sum(g, c.epoch, 2 * l + 1, b, (int)I.r0 + r) : 0.f;
+    uint4* hs = (uint4*)c.xn;                      // [nq][KT][32 lanes] A fragments
+    float* res = c.xn + 2 * KT * 32 * 4;           // [units of chunk 0][BD_ROWS][NB]
+    {
+      const uint4* src = (const uint4*)g.hglob + ((size_t)l * (g.F / 16) + (size_t)q0 * KT) * 32;
+      for (int i = c.tid; i < (int)(nq * KT * 32); i += NCT) cp_async16(hs + i, src + i);
+      // chunk-0 units add the residual x_{2l+1} of their rows
+      const int n0 = q0 == 0 ? (int)(min(u1, NRB) - u0) : 0;
+      for (int t = c.tid; t < n0 * BD_ROWS * NB; t += NCT) {
+        const int j = t / (BD_ROWS * NB), r = (t / NB) % BD_ROWS, b = t % NB;
+        res[t] = b < g.B ? xres_sum(g, c.epoch, 2 * l + 1, b, (int)(u0 + j) * BD_ROWS + r) : 0.f;
+      }
+      cp_async_wait_all();
     }
+    consumer_bar();
     c.mark(g, 0);
-    const int kt0 = c.warp * KT / NCW, kt1 = (c.warp + 1) * KT / NCW;
     const int gq = c.lane >> 2, tq = c.lane & 3;
     // ldmatrix lanes: matrix m = lane / 8 is rows 8 (m / 2) .. +7, k half m % 2
     const uint32_t li = (uint32_t)c.lane & 7u, mi = (uint32_t)c.lane >> 3;
     const uint32_t roff = (li + 8u * (mi >> 1)) * (BD_KC * 2u);
-    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+    const bool live = gq < g.B;
+    float* dst = xres_mine(g, c.epoch, 2 * l + 2, live ? gq : 0);
     Seg s[2];
     get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
-    const uint32_t SB = (uint32_t)g.stage_bytes;
     bool bad = false;
-    for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
-      const uint32_t n = min(s[0].ups, s[0].n - u0);
-      if (!bad && !c.ring.acquire(g)) bad = true;
-      if (bad) continue;
+    for (uint32_t v0 = 0; v0 < s[0].n; v0 += s[0].ups) {
+      const uint32_t n = min(s[0].ups, s[0].n - v0);
+      if (!c.ring.acquire(g)) {
+        bad = true;
+        break;
+      }
       const uint32_t wb = smem_u32(c.ring.stage_ptr());
-      const unsigned char* hb = c.ring.stage_ptr() + SB / 2 + c.lane * 16;
       for (uint32_t j = 0; j < n; j++) {
+        const uint32_t u = u0 + v0 + j;
+        if ((int)((v0 + j) % NCW) != c.warp) continue;
+        const uint32_t q = u / NRB, rb = u % NRB;
+        const uint4* af = hs + (size_t)(q - q0) * KT * 32 + c.lane;
         const uint32_t wu = wb + j * UNIT + roff;
-        for (int kt = kt0; kt < kt1; kt++) {
-          const uint4 af = *(const uint4*)(hb + j * UNIT + kt * 512);
-          const uint32_t a[4] = {af.x, af.y, af.z, af.w};
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int kt = 0; kt < KT; kt++) {
+          const uint4 fa = af[kt * 32];
+          const uint32_t a[4] = {fa.x, fa.y, fa.z, fa.w};
           uint32_t b0, b1, b2, b3;
           ldsm_x4(wu + ((((uint32_t)(2 * kt) + (mi & 1u)) ^ li) << 4), b0, b1, b2, b3);
           mma_16816(d0, a, b0, b1);
           mma_16816(d1, a, b2, b3);
         }
+        if (live) {
+          // rows 2t, 2t + 1 (d0) and 8 + 2t, 9 + 2t (d1) of the unit, sequence gq
+          float v[4] = {d0[0] + d0[2], d0[1] + d0[3], d1[0] + d1[2], d1[1] + d1[3]};
+          if (q == 0) {
+            const float* rr = res + (size_t)(u - u0) * BD_ROWS * NB + gq;
+            v[0] += rr[(2 * tq) * NB];
+            v[1] += rr[(2 * tq + 1) * NB];
+            v[2] += rr[(8 + 2 * tq) * NB];
+            v[3] += rr[(9 + 2 * tq) * NB];
+          }
+          const int row = (int)rb * BD_ROWS + 2 * tq;
+          red_add_v2f32(dst + row, v[0], v[1]);
+          red_add_v2f32(dst + row + 8, v[2], v[3]);
+        }
       }
       c.ring.release(c.lane);
     }
     c.mark(g, 1);
-    float* part = c.xn;  // [NCW][BD_ROWS][NB]: hi + lo sums of rows 2tq, 2tq+1 (+8)
-    {
-      float* pw = part + (size_t)c.warp * BD_ROWS * NB + gq;
-      pw[(2 * tq) * NB] = d0[0] + d0[2];
-      pw[(2 * tq + 1) * NB] = d0[1] + d0[3];
-      pw[(8 + 2 * tq) * NB] = d1[0] + d1[2];
-      pw[(9 + 2 * tq) * NB] = d1[1] + d1[3];
-    }
     if (bad) c.flag[2] = 1;
     consumer_bar();
     if (c.flag[2]) return false;
-    for (int t = c.tid; t < BD_ROWS * NB; t += NCT) {
-      const int r = t / NB, b = t % NB;
-      float y = 0.f;
-#pragma unroll
-      for (int w = 0; w < NCW; w++) y += part[(size_t)w * BD_ROWS * NB + t];
-      if (b < g.B) xres(g, c.epoch, 2 * l + 2, b, 0)[I.r0 + r] = res[t] + y;
-    }
-    consumer_bar();
     return true;
   } else {
     // a 16-byte chunk of a down row covers CW columns (8 bf16 or 16 int8)
@@ -1616,7 +1640,7 @@ MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr&
     float* nx = g.xbuf + (size_t)((c.epoch + 1u) & 1u) * total;
     for (size_t i = a + c.tid; i < e; i += NCT) nx[i] = 0.f;
   }
-  NormGain<HT> ng;
+  NormGain<HT, NB> ng;
   norm_gain(ng, g.final_norm, c.tid);
   if constexpr (WB == 1)  // int8: the rows' scales (at most HT rows), copied in while the wait runs
     for (int t = c.tid; t < (int)(I.r1 - I.r0); t += NCT) cp_async4(c.sc + t, g.lm_scale + I.r0 + t);
@@ -1895,90 +1919,6 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
         (I.flags & F_HOLD) ? (uint32_t)(g.hold_early / (unsigned)g.stage_bytes) : 0xFFFFFFFFu;
     auto held_back = [&]() { return *(volatile const int*)done < my_seq; };
     uint32_t nst_i = 0;  // stages of this instruction issued so far
-    if (I.op == OP_MLP_DOWN && g.bsplit) {
-      // Each stage's weight unit is copied as soon as the stage is free; its
-      // h fragments, written by other SMs' gate/up slices, follow once the
-      // gate/up counter shows them complete.  The stage's full barrier
-      // expects both halves from the first arming on.
-      const Seg& S = s[0];
-      const uint32_t SB = (uint32_t)g.stage_bytes;
-      const uint32_t nst = (S.n + S.ups - 1) / S.ups;
-      uint32_t wi = 0, hi = 0;  // stages whose weights / h fragments are issued
-      bool dep = false;
-      int bad = 0;
-      const uint64_t t0 = gtimer();
-      auto stage_of = [&](uint32_t j, uint32_t& stg, uint32_t& p) {
-        const uint32_t a = (uint32_t)st + j;
-        stg = a % (uint32_t)ns;
-        p = par ^ ((a / (uint32_t)ns) & 1u);
-      };
-      auto issue = [&](uint32_t j, const unsigned char* src, uint32_t off, uint64_t pol) {
-        uint32_t stg, p;
-        stage_of(j, stg, p);
-        const uint32_t u0 = j * S.ups, bytes = min(S.ups, S.n - u0) * S.unit;
-        bulk_g2s(ring_s + stg * SB + off, src + (size_t)u0 * S.unit, bytes, full0 + 8u * stg, pol);
-      };
-      auto issue_h = [&](uint32_t j) {
-        if (lane == 0) issue(j, S.src2, SB / 2, pol_kv);
-      };
-      for (uint32_t it = 1; hi < nst; it++) {
-        bool moved = false;
-        const bool wfree = wi < hold_k || !__shfl_sync(0xFFFFFFFFu, held_back(), 0);
-        if (wi < nst && wi < hi + (uint32_t)ns && wfree) {
-          uint32_t stg, p;
-          stage_of(wi, stg, p);
-          if (__shfl_sync(0xFFFFFFFFu, mbar_try(empty0 + 8u * stg, p ^ 1u), 0)) {
-            if (lane == 0) {
-              if (g.trace && wi == 0) g.trace[((size_t)qid * g.max_pc + pc) * 8] = gtimer();
-              const uint32_t u0 = wi * S.ups, bytes = min(S.ups, S.n - u0) * S.unit;
-              mbar_expect_tx(full0 + 8u * stg, 2u * bytes);
-              issue(wi, S.src, 0, pol_w);
-            }
-            wi++;
-            moved = true;
-          }
-        }
-        if (!dep) {
-          int ok = 0;
-          if (lane == 0) {
-            ok = (int32_t)(ld_acquire(g.ctr + I.wait_ctr) - ep * I.wait_cnt) >= 0;
-            // the fragments were written through the generic proxy
-            if (ok) asm volatile("fence.proxy.async.global;" ::: "memory");
-          }
-          dep = __shfl_sync(0xFFFFFFFFu, ok, 0);
-        }
-        if (dep && hi < wi) {
-          issue_h(hi++);
-          moved = true;
-        }
-        if (!moved && (it & 63) == 0) {
-          if (lane == 0) {
-            if (peek_err(g)) {
-              bad = 1;
-            } else if (gtimer() - t0 > g.timeout_ns) {
-              set_err(g, MK_ERR_TIMEOUT, pc, I.op);
-              bad = 1;
-            }
-          }
-          bad = __shfl_sync(0xFFFFFFFFu, bad, 0);
-          if (bad) break;
-        }
-        __syncwarp();
-      }
-      // on failure, complete the armed stages with whatever the fragment
-      // buffer holds (the step has failed) so that every copy can be drained
-      while (hi < wi) issue_h(hi++);
-      __syncwarp();
-      issued += wi;
-      issued_bytes += 2ull * S.n * S.unit;
-      for (uint32_t j = 0; j < wi; j++)
-        if (++st == ns) {
-          st = 0;
-          par ^= 1u;
-        }
-      if (bad) goto drain;
-      continue;
-    }
     for (int k = 0; k < nseg; k++) {
       for (uint32_t u0 = 0; u0 < s[k].n; u0 += s[k].ups) {
         const uint32_t n = min(s[k].ups, s[k].n - u0);

@@ -92,6 +92,10 @@ MK_DEV void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
+MK_DEV void red_add_v2f32(float* p, float a, float b) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(a), "f"(b) : "memory");
+}
+
 MK_DEV void red_add_v4f32(float* p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
                "f"(d)
@@ -182,6 +186,10 @@ MK_DEV void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32
 // engine); cp_async_wait_all waits for this thread's copies.
 MK_DEV void cp_async4(float* sdst, const float* gsrc) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(sdst)), "l"(gsrc)
+               : "memory");
+}
+MK_DEV void cp_async16(void* sdst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sdst)), "l"(gsrc)
                : "memory");
 }
 MK_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }

@@ -140,12 +140,16 @@ constexpr int MMA_FLUSH = 32;        // batched GEMV: rows per cross-warp sum of
 // row-split down projection over the whole h) when one down row fits a ring
 // stage; otherwise one fused op per FFN column slice with float atomics.
 // Batched split MLP (dense, 2..8 sequences): gate/up column slices (multiples
-// of 16 columns) write h in tensor-core A-fragment form; a down instruction
-// owns BD_ROWS rows and streams, per chunk of BD_KC columns, that chunk's h
-// fragments (16 KB) next to its weight unit of BD_ROWS x BD_KC (16 KB), so
-// no SM reduces into another's rows.  Needs ring stages of at least 32 KB.
+// of 16 columns) write h in tensor-core A-fragment form; the down projection
+// is cut into units of BD_ROWS rows x BD_KC columns (16 KB), numbered
+// chunk-major, and a down instruction takes a run of at most BD_MAX_UNITS
+// consecutive units that spans at most two chunks.  It loads those chunks'
+// h fragments (16 KB each) once, streams its units through the ring and adds
+// each unit's partial rows into the residual with float reductions (the
+// chunk-0 units also add x_{2l+1}).
 constexpr int BD_KC = 512;
 constexpr int BD_ROWS = 16;
+constexpr int BD_MAX_UNITS = 32;
 MK_HD inline bool mlp_split_batched(const mk_model_desc& d) {
   return d.n_experts == 0 && d.max_batch > 1 && d.max_batch <= 8 && d.ffn % BD_KC == 0 &&
          d.hidden % BD_ROWS == 0;

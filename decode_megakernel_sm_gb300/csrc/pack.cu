@@ -15,8 +15,9 @@
 //                              different shared-memory bank groups
 //   gate/up [F][2][H]          gate row c, then up row c
 //   down  dense batch 1: [H][F] as given (one contiguous row per output row);
-//         2..8 sequences, F a multiple of 512: units of 16 rows x 512 columns,
-//         16-byte chunk q of unit row i at slot q ^ (i & 7);
+//         2..8 sequences, F a multiple of 512: units of 16 rows x 512 columns
+//         in chunk-major order (unit kc * (H / 16) + row block), 16-byte
+//         chunk q of unit row i at slot q ^ (i & 7);
 //         otherwise [F][H], transposed (one contiguous row per FFN column)
 //
 // int8 weights (dense batch-1 shapes): every matrix is first quantised per
@@ -116,20 +117,24 @@ cudaError_t pack_interleave(uint16_t* dst, const void* a, const void* b, long ro
 // Down projection [H][F] as units of BD_ROWS rows x BD_KC columns, unit
 // (rb, kc) at ((rb * (F / BD_KC) + kc) * BD_ROWS) rows of BD_KC; inside a
 // unit, 16-byte chunk q of unit row i sits at slot q ^ (i & 7).
-__global__ void pack_down_tiles_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int F) {
-  const int nkc = F / BD_KC, cpr = BD_KC / 8;
+// Units of BD_ROWS rows x BD_KC columns in chunk-major order: unit
+// (chunk kc, row block rb) is unit kc * (H / BD_ROWS) + rb, so a run of
+// consecutive units covers consecutive row blocks of one or two chunks.
+__global__ void pack_down_tiles_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int H,
+                                       int F) {
+  const int nkc = F / BD_KC, cpr = BD_KC / 8, nrb = H / BD_ROWS;
   const size_t r = blockIdx.x / nkc;
   const int kc = (int)(blockIdx.x % nkc);
   const size_t rb = r / BD_ROWS;
   const int i = (int)(r % BD_ROWS);
-  uint4* d = dst + ((rb * nkc + kc) * BD_ROWS + i) * cpr;
+  uint4* d = dst + (((size_t)kc * nrb + rb) * BD_ROWS + i) * cpr;
   const uint4* sr = src + r * (F / 8) + (size_t)kc * cpr;
   for (int q = threadIdx.x; q < cpr; q += blockDim.x) d[q ^ (i & 7)] = sr[q];
 }
 
 cudaError_t pack_down_tiles(uint16_t* dst, const void* src, int H, int F, cudaStream_t s) {
   pack_down_tiles_kernel<<<(unsigned)((size_t)H * (F / BD_KC)), 128, 0, s>>>(
-      (uint4*)dst, (const uint4*)src, F);
+      (uint4*)dst, (const uint4*)src, H, F);
   return cudaGetLastError();
 }
 

@@ -138,7 +138,10 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
     }
     // ---- O-projection: with at least one SM per query head every SM takes
     // rows of a single head; otherwise the (head, row) space is cut evenly.
+    // (the batched variants' tensor-core O-projection takes 8-row tiles and
+    // adds row pairs with 8-byte reductions: cut at multiples of 8 rows)
     const long OR = (long)Hq * H;
+    const int oal = d.max_batch > 1 ? 8 : 1;
     for (int i = 0; i < n_sm; i++) {
       long a, b;
       if (n_sm >= Hq) {
@@ -146,11 +149,11 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
         const long s0 = ((long)h * n_sm + Hq - 1) / Hq;
         const long s1 = ((long)(h + 1) * n_sm + Hq - 1) / Hq;
         const int m = (int)(s1 - s0), k = (int)(i - s0);
-        a = (long)h * H + cut(H, m, k, 1);
-        b = (long)h * H + (k == m - 1 ? H : cut(H, m, k + 1, 1));
+        a = (long)h * H + cut(H, m, k, oal);
+        b = (long)h * H + (k == m - 1 ? H : cut(H, m, k + 1, oal));
       } else {
-        a = cut(OR, n_sm, i, 1);
-        b = (i == n_sm - 1) ? OR : cut(OR, n_sm, i + 1, 1);
+        a = cut(OR, n_sm, i, oal);
+        b = (i == n_sm - 1) ? OR : cut(OR, n_sm, i + 1, oal);
       }
       while (a < b) {
         long h = a / H;
@@ -191,10 +194,10 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
     }
     // ---- split MLP (dense, batch 1): gate/up column slices, then down rows
     if (mlp_split(d) || mlp_split_batched(d)) {
-      // batched: gate/up slices in whole 16-column k-tiles of h, down rows in
-      // units of BD_ROWS rows
+      // batched: gate/up slices in whole 16-column k-tiles of h, down runs of
+      // (row block, column chunk) units
       const bool bat = mlp_split_batched(d);
-      const long F = d.ffn, cu = bat ? 16 : 1, ru = bat ? BD_ROWS : 1;
+      const long F = d.ffn, cu = bat ? 16 : 1;
       for (int i = 0; i < n_sm; i++) {
         long a = cut(F / cu, n_sm, i, 1) * cu;
         long b = (i == n_sm - 1) ? F : cut(F / cu, n_sm, i + 1, 1) * cu;
@@ -213,11 +216,15 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
           a = e;
         }
       }
+      // batch 1: rows [r0, r1) of x_{2l+2}, one owner per row; batched: a
+      // run [r0, r1) of chunk-major down units (r0 / NRB is the first chunk)
+      const long NRB = H / BD_ROWS, NU = bat ? NRB * (F / BD_KC) : H;
       for (int i = 0; i < n_sm; i++) {
-        long a = cut(H / ru, n_sm, i, 1) * ru;
-        long b = (i == n_sm - 1) ? H : cut(H / ru, n_sm, i + 1, 1) * ru;
+        long a = cut(NU, n_sm, i, 1);
+        long b = (i == n_sm - 1) ? NU : cut(NU, n_sm, i + 1, 1);
         while (a < b) {
-          const long e = std::min(b, a + (bat ? (long)BD_ROWS : (long)MAX_DOWN_ROWS));
+          long e = std::min(b, a + (bat ? (long)BD_MAX_UNITS : (long)MAX_DOWN_ROWS));
+          if (bat) e = std::min(e, (a / NRB + 2) * NRB);  // at most two chunks of h
           Instr I = mk(OP_MLP_DOWN, l);
           I.r0 = (uint32_t)a;
           I.r1 = (uint32_t)e;
@@ -227,7 +234,7 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
           I.wait_ctr = cm.mlp_up(l);
           I.sig_ctr = cm.mlp(l);
           qs[i].push_back(I);
-          bytes[i] += (double)(e - a) * F * wb;
+          bytes[i] += bat ? (double)(e - a) * BD_ROWS * BD_KC * 2 : (double)(e - a) * F * wb;
           a = e;
         }
       }
@@ -385,6 +392,8 @@ int plan_verify(const mk_model_desc& d, int B, const PlanOut& p) {
   std::vector<uint8_t> qkv((size_t)L * R, 0), att((size_t)L * B * Hkv * S, 0);
   std::vector<uint8_t> op((size_t)L * Hq * H, 0), mlp((size_t)L * Fv, 0), res((size_t)L * H, 0);
   std::vector<uint8_t> rt((size_t)L * (moe ? d.n_experts : 1), 0), lm(V, 0), slot(p.n_lm, 0);
+  // batched split MLP: down units (row block, column chunk)
+  std::vector<uint8_t> dunit(mlp_split_batched(d) ? (size_t)L * (H / BD_ROWS) * (d.ffn / BD_KC) : 0, 0);
   auto mark = [](std::vector<uint8_t>& v, size_t i) {
     if (i >= v.size() || v[i]) return false;
     v[i] = 1;
@@ -470,11 +479,22 @@ int plan_verify(const mk_model_desc& d, int B, const PlanOut& p) {
           if (!mark(mlp, (size_t)l * Fv + c)) return 24;
         break;
       case OP_MLP_DOWN:
-        if (!(mlp_split(d) || mlp_split_batched(d)) || l >= L || I.r0 >= I.r1 || (int)I.r1 > H ||
-            I.r1 - I.r0 > (uint32_t)MAX_DOWN_ROWS)
-          return 25;
-        if (mlp_split_batched(d) && ((I.r0 % BD_ROWS) || I.r1 - I.r0 != (uint32_t)BD_ROWS))
-          return 25;
+        if (!(mlp_split(d) || mlp_split_batched(d)) || l >= L || I.r0 >= I.r1) return 25;
+        if (mlp_split_batched(d)) {
+          // a run of chunk-major units spanning at most two chunks; the
+          // chunk-0 units add the residual rows of their row blocks
+          const uint32_t nrb = (uint32_t)(H / BD_ROWS), nu = nrb * (uint32_t)(d.ffn / BD_KC);
+          if (I.r1 > nu || I.r1 - I.r0 > (uint32_t)BD_MAX_UNITS || (I.r1 - 1) / nrb > I.r0 / nrb + 1)
+            return 25;
+          for (uint32_t u = I.r0; u < I.r1; u++) {
+            if (!mark(dunit, (size_t)l * nu + u)) return 26;
+            if (u < nrb)
+              for (uint32_t r = u * BD_ROWS; r < (u + 1) * BD_ROWS; r++)
+                if (!mark(res, (size_t)l * H + r)) return 26;
+          }
+          break;
+        }
+        if ((int)I.r1 > H || I.r1 - I.r0 > (uint32_t)MAX_DOWN_ROWS) return 25;
         for (uint32_t r = I.r0; r < I.r1; r++)
           if (!mark(res, (size_t)l * H + r)) return 26;
         break;
@@ -488,7 +508,7 @@ int plan_verify(const mk_model_desc& d, int B, const PlanOut& p) {
         return 20;
     }
   }
-  for (auto* v : {&qkv, &att, &op, &mlp, &res, &lm, &slot})
+  for (auto* v : {&qkv, &att, &op, &mlp, &res, &lm, &slot, &dunit})
     for (uint8_t x : *v)
       if (!x) return 21;
   if (moe)

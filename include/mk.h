@@ -328,10 +328,7 @@ int mk_set_l2_prefetch(mk_handle* h, uint64_t bytes_ahead);
  * stage; smaller stages give a deeper ring.  Results do not depend on it.
  * Call between steps (not while a step is in flight on another stream);
  * drops the cached ablation graphs.  MK_ERR_INVALID_ARG for other sizes,
- * MK_ERR_UNSUPPORTED if two stages no longer fit, or for 16384 on a handle
- * with 2..8 sequences and an FFN of whole 512-column chunks, whose down
- * stages carry 16 KB of weights next to 16 KB of activations (the old size
- * is kept).                                                                */
+ * MK_ERR_UNSUPPORTED if two stages no longer fit (the old size is kept).   */
 int mk_set_stage_bytes(mk_handle* h, int stage_bytes);
 
 /* At most `max_stages` ring stages (2..16; 0, the default: as many as the

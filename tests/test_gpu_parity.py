@@ -140,15 +140,17 @@ def test_batched_split_mlp_stage_sizes(sb):
     run_steps(_bsplit_cfg(8), 3, seed=19, stage_bytes=sb)
 
 
-def test_batched_split_mlp_refuses_16k_stages():
-    r = Run(_bsplit_cfg(8), seed=2)
-    try:
-        with pytest.raises(MkError) as e:
-            r.dec.set_stage_bytes(16384)
-        assert e.value.status == MK_ERR_UNSUPPORTED
-        r.step()  # the old stage size is kept
-    finally:
-        r.close()
+def test_batched_split_mlp_16k_stages():
+    # one 16 KB down unit per stage
+    run_steps(_bsplit_cfg(8), 3, seed=2, stage_bytes=16384)
+
+
+def test_batched_split_mlp_ragged_ffn_chunks():
+    # FFN of 3 chunks of 512 and a short vocabulary: down runs that start and
+    # end inside chunks, two-chunk runs, and every SM's share under one chunk
+    cfg = synth.custom(n_layers=2, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=64,
+                       ffn=1536, vocab=3000, batch=8, prefill=(5, 400), steps=3, rope_theta=5e5)
+    run_steps(cfg, 3, seed=29)
 
 
 def test_llama1b_1k_parity():

@@ -227,10 +227,19 @@ def test_batched_split_mlp_cuts_whole_tiles():
     st, q = L.mk_plan(d, cfg["batch"], cfg["max_seq"], 152)
     ops = [q[i] for i in range(152 * st["max_pc"]) if q[i].op in (8, 9)]
     assert all(I.r0 % 16 == 0 and I.r1 % 16 == 0 for I in ops if I.op == 8)
-    # down instructions own exactly 16 rows (one weight unit per column chunk)
+    # down instructions: runs of chunk-major (row block, 512-column chunk)
+    # units, at most 32 units and two chunks each, covering every unit of a
+    # layer exactly once, with every SM's share within one unit of the mean
     down = [I for I in ops if I.op == 9]
-    assert all(I.r0 % 16 == 0 and I.r1 - I.r0 == 16 for I in down)
-    assert sorted(I.r0 for I in down if I.layer == 0) == list(range(0, cfg["hidden"], 16))
+    nrb, nkc = cfg["hidden"] // 16, cfg["ffn"] // 512
+    units = sorted(u for I in down if I.layer == 0 for u in range(I.r0, I.r1))
+    assert units == list(range(nrb * nkc))
+    assert all(I.r1 - I.r0 <= 32 and (I.r1 - 1) // nrb <= I.r0 // nrb + 1 for I in down)
+    per_sm = [sum(q[sm * st["max_pc"] + k].r1 - q[sm * st["max_pc"] + k].r0
+                  for k in range(st["max_pc"])
+                  if q[sm * st["max_pc"] + k].op == 9 and q[sm * st["max_pc"] + k].layer == 0)
+              for sm in range(152)]
+    assert max(per_sm) - min(per_sm) <= 1
     assert not any(I.flags & (16 | 32) for I in ops)  # no tagged hops at batch > 1
 
 
