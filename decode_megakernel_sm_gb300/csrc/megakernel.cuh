@@ -199,8 +199,9 @@ struct NormGain {
   static constexpr int GROUPS = HT / 8;
   static constexpr int GPT = (GROUPS + NCT - 1) / NCT;
   static constexpr int KPT = (HT + NCT - 1) / NCT;  // batched: columns tid + q * NCT
-  uint4 w[NB == 1 ? GPT : 1];    // batch 1: 8 packed bf16 gains per 8-column group
-  float gw[NB == 1 ? 1 : KPT];   // batched: this thread's columns' gains
+  uint4 w[NB == 1 ? GPT : 1];       // batch 1: 8 packed bf16 gains per 8-column group
+  uint16_t gw[NB == 1 ? 1 : KPT];   // batched: this thread's columns' bf16 gains (widened
+                                    // at use, so the loads do not stall the wait)
 };
 
 template <int HT, int NB>
@@ -215,7 +216,7 @@ MK_DEV void norm_gain(NormGain<HT, NB>& ng, const uint16_t* gain, int tid) {
 #pragma unroll
     for (int q = 0; q < NormGain<HT, NB>::KPT; q++) {
       const int k = tid + q * NCT;
-      ng.gw[q] = k < HT ? bf1(__ldg(gain + k)) : 0.f;
+      ng.gw[q] = k < HT ? __ldg(gain + k) : (uint16_t)0;
     }
   }
 }
@@ -290,7 +291,9 @@ MK_DEV bool norm_apply_batched(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, int
       }
     }
   }
-  const float* gw = ng.gw;  // loaded before the dependency wait
+  float gw[KPT];  // loaded before the dependency wait
+#pragma unroll
+  for (int q = 0; q < KPT; q++) gw[q] = bf1(ng.gw[q]);
 #pragma unroll
   for (int b = 0; b < NB; b++) {
     const float t = warp_sum(ss[b]);
