@@ -1314,15 +1314,19 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I)
     c.hbuf[b * MAX_COLS + j] = scale * (gt / (1.f + expf(-gt))) * up;
   }
   consumer_bar();
-  constexpr int NG = HT / 8;                   // 8-row groups of the output
-  constexpr int GPT = (NG + NCT - 1) / NCT;    // groups per consumer thread
-  float acc[GPT][NB][8];
+  // Down columns as an axpy over the output in 4-row quads (8 bytes of a
+  // transposed down row): HT / 4 quads over the consumer threads, so the
+  // busiest thread holds ceil(HT / 4 / NCT) quads (12 rows at H = 2048)
+  // rather than two 8-row groups; one 16-byte reduction per quad.
+  constexpr int NQ = HT / 4;                   // 4-row quads of the output
+  constexpr int QPT = (NQ + NCT - 1) / NCT;    // quads per consumer thread (at most)
+  float acc[QPT][NB][4];
 #pragma unroll
-  for (int q = 0; q < GPT; q++)
+  for (int q = 0; q < QPT; q++)
 #pragma unroll
     for (int b = 0; b < NB; b++)
 #pragma unroll
-      for (int k = 0; k < 8; k++) acc[q][b][k] = 0.f;
+      for (int k = 0; k < 4; k++) acc[q][b][k] = 0.f;
   for (uint32_t u0 = 0; u0 < s[1].n; u0 += s[1].ups) {
     const uint32_t n = min(s[1].ups, s[1].n - u0);
     if (!c.ring.acquire(g)) break;
@@ -1332,15 +1336,15 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I)
 #pragma unroll
       for (int b = 0; b < NB; b++) hv[b] = c.hbuf[b * MAX_COLS + u0 + j];
 #pragma unroll
-      for (int q = 0; q < GPT; q++) {
+      for (int q = 0; q < QPT; q++) {
         const int k = c.tid + q * NCT;
-        if (k < NG) {
-          float wf[8];
-          unpack8(*(const uint4*)(st + (size_t)j * HT * 2 + k * 16), wf);
+        if (k < NQ) {
+          const uint2 w = *(const uint2*)(st + (size_t)j * HT * 2 + k * 8);
+          const float wf[4] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y)};
 #pragma unroll
           for (int b = 0; b < NB; b++)
 #pragma unroll
-            for (int e = 0; e < 8; e++) acc[q][b][e] = fmaf(hv[b], wf[e], acc[q][b][e]);
+            for (int e = 0; e < 4; e++) acc[q][b][e] = fmaf(hv[b], wf[e], acc[q][b][e]);
         }
       }
     }
@@ -1349,20 +1353,18 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I)
   c.mark(g, 1);
   const int rs0 = (int)(I.aux & 0xFFFFu), rs1 = (int)(I.aux >> 16);
 #pragma unroll
-  for (int q = 0; q < GPT; q++) {
+  for (int q = 0; q < QPT; q++) {
     const int k = c.tid + q * NCT;
-    if (k < NG) {
-      const int r0 = k * 8;
+    if (k < NQ) {
+      const int r0 = k * 4;
       for (int b = 0; b < g.B && b < NB; b++) {
-        float v[8];
+        float v[4];
 #pragma unroll
-        for (int e = 0; e < 8; e++) {
+        for (int e = 0; e < 4; e++) {
           v[e] = acc[q][b][e];
           if (r0 + e >= rs0 && r0 + e < rs1) v[e] += xres_sum(g, c.epoch, 2 * l + 1, b, r0 + e);
         }
-        float* dst = xres_mine(g, c.epoch, 2 * l + 2, b) + r0;
-        red_add_v4f32(dst, v[0], v[1], v[2], v[3]);
-        red_add_v4f32(dst + 4, v[4], v[5], v[6], v[7]);
+        red_add_v4f32(xres_mine(g, c.epoch, 2 * l + 2, b) + r0, v[0], v[1], v[2], v[3]);
       }
     }
   }
