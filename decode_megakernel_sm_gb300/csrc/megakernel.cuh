@@ -816,20 +816,66 @@ MK_DEV bool op_attn(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I
       }
     }
   };
+  // Two positions per slot and pass (j and j + NCW * SPW): their scores,
+  // shuffles and exponentials are independent chains, so each hides the
+  // other's latency, and one running-max update covers both.  An absent
+  // position scores -inf and contributes 2^-inf = 0.
+  auto process2 = [&](const uint4& ka, const uint4& va, bool oka, const uint4& kb,
+                      const uint4& vb, bool okb) {
+    float kfa[8], kfb[8], sa[HPG], sb[HPG];
+    unpack8(ka, kfa);
+    unpack8(kb, kfb);
+#pragma unroll
+    for (int h = 0; h < HPG; h++) {
+      float a = 0.f, b = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; j++) {
+        a = fmaf(q[h][j], kfa[j], a);
+        b = fmaf(q[h][j], kfb[j], b);
+      }
+      sa[h] = a;
+      sb[h] = b;
+    }
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1)
+#pragma unroll
+      for (int h = 0; h < HPG; h++) {
+        sa[h] += __shfl_xor_sync(0xFFFFFFFFu, sa[h], off);
+        sb[h] += __shfl_xor_sync(0xFFFFFFFFu, sb[h], off);
+      }
+    float vfa[8], vfb[8];
+    unpack8(va, vfa);
+    unpack8(vb, vfb);
+#pragma unroll
+    for (int h = 0; h < HPG; h++) {
+      const float xa = oka ? sa[h] : -INFINITY, xb = okb ? sb[h] : -INFINITY;
+      const float mn = fmaxf(m[h], fmaxf(xa, xb));
+      const float cr = exp2f(m[h] - mn), pa = exp2f(xa - mn), pb = exp2f(xb - mn);
+      l[h] = fmaf(l[h], cr, pa + pb);
+#pragma unroll
+      for (int j = 0; j < 8; j++) o[h][j] = fmaf(o[h][j], cr, fmaf(pa, vfa[j], pb * vfb[j]));
+      m[h] = mn;
+    }
+  };
   c.mark(g, 0);
   Seg s[2];
   get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
+  constexpr uint32_t STEP = NCW * SPW;  // positions per pass of all warps' slots
   for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
     const uint32_t n = min(s[0].ups, s[0].n - u0);
     if (!c.ring.acquire(g)) break;
     const unsigned char* st = c.ring.stage_ptr();
-    for (uint32_t jb = (uint32_t)c.warp * SPW; jb < n; jb += NCW * SPW) {
-      const uint32_t j = jb + slot;
-      const bool valid = j < n;
-      const uint4 kw = valid ? *(const uint4*)(st + (size_t)j * D * 2 + dsl * 16) : zero;
-      const uint4 vw =
-          valid ? *(const uint4*)(st + c.ring.sb / 2 + (size_t)j * D * 2 + dsl * 16) : zero;
-      process(kw, vw, valid);
+    const unsigned char* vs = st + c.ring.sb / 2;
+    for (uint32_t jb = (uint32_t)c.warp * SPW; jb < n; jb += 2 * STEP) {
+      const uint32_t ja = jb + slot, jc = ja + STEP;
+      const bool oka = ja < n, okb = jc < n;
+      const size_t oa = (size_t)ja * D * 2 + dsl * 16, ob = (size_t)jc * D * 2 + dsl * 16;
+      const uint4 ka = oka ? *(const uint4*)(st + oa) : zero, va = oka ? *(const uint4*)(vs + oa) : zero;
+      const uint4 kb = okb ? *(const uint4*)(st + ob) : zero, vb = okb ? *(const uint4*)(vs + ob) : zero;
+      if (jb + STEP < n)
+        process2(ka, va, oka, kb, vb, okb);
+      else
+        process(ka, va, oka);  // (warp-uniform: no slot of this pass has a second position)
     }
     c.ring.release(c.lane);
   }
