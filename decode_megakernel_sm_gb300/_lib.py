@@ -19,6 +19,7 @@ MK_ERR_TIMEOUT = -5
 MK_ERR_NOT_READY = -6
 MK_ERR_DEVICE = -7
 MK_ERR_SCRATCH = -8
+MK_ERR_BOUNDS = -9
 MK_ABL_STREAM, MK_ABL_GRAPH, MK_ABL_PDL = 0, 1, 2
 MK_WEIGHTS_BF16, MK_WEIGHTS_INT8 = 0, 1
 
@@ -117,14 +118,15 @@ SIGNATURES = {
 
 
 def lib():
-    """Load libmk.so (building it in-tree first if it is missing or stale)."""
+    """Load libmk.so (building it in-tree first if it is missing or stale); with
+    MK_LIB=bounds in the environment, the bounds-checked libmk_bounds.so."""
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.LIB
+            path = _build.LIB_BOUNDS if os.environ.get("MK_LIB") == "bounds" else _build.LIB
             if not _build.up_to_date():
                 try:
-                    path = _build.build()
+                    _build.build()
                 except Exception as e:  # no silent fallback: the CUDA path is the product
                     raise RuntimeError(f"libmk.so is missing and could not be built: {e}") from e
             L = C.CDLL(path)

@@ -33,10 +33,12 @@ cudaError_t pack_wo_i8(void* dst, const void* wo_codes, int H, int Hq, cudaStrea
 cudaError_t bias_codes(void* p, size_t bytes, cudaStream_t s);
 
 extern const Variant variant_h256_d64_g2_b1;
+#ifndef MK_BOUNDS
 extern const Variant variant_h2048_d64_g4_b1;
 extern const Variant variant_h2048_d64_g4_b8;
 extern const Variant variant_h2048_d128_g4_b1;
 extern const Variant variant_h2048_d64_g4_b1_w8;
+#endif
 }  // namespace mk
 
 using namespace mk;
@@ -54,6 +56,7 @@ struct Scratch {
   float* hglob;             // SiLU(gate)*up (split MLP)
   TagWord* xt;              // tagged block: x_{2l+2} (split MLP)
   size_t xbuf_bytes, ctr_bytes, err_bytes, tag_bytes, total;
+  size_t n_q, n_part, n_h, n_xt, n_lm;  // element counts (bounds checks)
 };
 
 static size_t al256(size_t n) { return (n + 255) / 256 * 256; }
@@ -78,6 +81,11 @@ static Scratch carve_scratch(const mk_model_desc& d, size_t B, size_t kc, size_t
   s.ctr_bytes = sc;
   s.err_bytes = se;
   s.tag_bytes = sxt;
+  s.n_q = sq / 4;
+  s.n_part = sp / 4;
+  s.n_h = sh / 4;
+  s.n_xt = sxt / 8;
+  s.n_lm = sl / 4;
   s.total = sx + sq + sp + sr + 2 * sl + sc + se + 2 * sroute + sh + sxt;
   if (!base) return s;
   char* q = base;
@@ -161,9 +169,14 @@ struct mk_handle {
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 static const Variant* pick_variant(const mk_model_desc& d, int wb) {
+#ifdef MK_BOUNDS
+  // the bounds-checked library carries the small variant only
+  const Variant* all[] = {&variant_h256_d64_g2_b1};
+#else
   const Variant* all[] = {&variant_h256_d64_g2_b1, &variant_h2048_d64_g4_b1,
                           &variant_h2048_d64_g4_b8, &variant_h2048_d128_g4_b1,
                           &variant_h2048_d64_g4_b1_w8};
+#endif
   const int HPG = d.n_q_heads / d.n_kv_heads;
   const Variant* best = nullptr;
   for (const Variant* v : all) {
@@ -700,6 +713,18 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.trace = h->trace;
   g.l2_ahead = h->l2_ahead;
   g.hold_early = h->hold_early;
+  g.sc_lo = (const unsigned char*)h->scratch;
+  g.sc_bytes = h->scratch_bytes;
+  g.pk_lo = (const unsigned char*)h->packed;
+  g.pk_bytes = h->packed_bytes;
+  g.kv_elems = h->kv_block ? (size_t)h->kv_blocks * d.n_kv_heads * h->kv_block * d.head_dim
+                           : (size_t)d.max_batch * d.n_kv_heads * d.max_seq * d.head_dim;
+  g.n_xbuf = h->sc.xbuf_bytes / 4;
+  g.n_q = h->sc.n_q;
+  g.n_part = h->sc.n_part;
+  g.n_h = h->sc.n_h;
+  g.n_xt = h->sc.n_xt;
+  g.n_lmv = h->sc.n_lm;
   return g;
 }
 
@@ -945,6 +970,8 @@ extern "C" int mk_decode_step_noalloc(mk_handle* h, const int32_t* d_tokens,
   g.hglob = sc.hglob;
   g.routes = sc.routes;    // MoE routing of this call, in the array as well
   g.rweight = sc.rweight;
+  g.sc_lo = (const unsigned char*)base;
+  g.sc_bytes = need;
   // the array keeps the previous call's contents: clear what must start at
   // zero (residual accumulators of both parities, counters, error word, step
   // tags) and run the step as epoch 1
@@ -1209,6 +1236,8 @@ extern "C" const char* mk_status_string(int status) {
     case MK_ERR_DEVICE: return "device reported an internal inconsistency";
     case MK_ERR_SCRATCH:
       return "workload needs more scratch than the 16 MiB no-allocation array holds";
+    case MK_ERR_BOUNDS:
+      return "bounds-checked build: an access fell outside its buffer";
     default: return "unknown status";
   }
 }

@@ -189,6 +189,15 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
   }
 }
 
+// Units of a segment in the stage that starts at unit u0, checked in the
+// bounds build against the room the stage (or its half) has for them: a
+// violation records MK_ERR_BOUNDS and the consumer reads none of them.
+MK_DEV uint32_t stage_units(const Globals& g, const Seg& sg, uint32_t u0, uint32_t room, int pc,
+                            int op) {
+  const uint32_t n = min(sg.ups, sg.n - u0);
+  return MK_IN(g, n * sg.unit <= room, pc, op) ? n : 0u;
+}
+
 // ---------------------------------------------------------------- norms ----
 // xn[b][k] = x[b][k] * rsqrt(mean(x^2) + eps) * gain[k] for the residual
 // x_j (j = 0: the embedding row of the token).  The gain slice of each
@@ -343,17 +352,27 @@ MK_DEV bool norm_apply(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, int j,
     return norm_apply_batched(c, g, j, ng);
   } else {
   constexpr int GROUPS = NormGain<HT, NB>::GROUPS, GPT = NormGain<HT, NB>::GPT;
+  bool ok = true;
+  // bounds build: the residual vector must lie inside its buffer, else the
+  // instruction fails (and reads x_1 meanwhile, which does)
+  if (j > 0 && !MK_IN(g,
+                      (g.xtag && (j & 1) == 0)
+                          ? (size_t)(j / 2) * g.B * HT <= g.n_xt
+                          : (size_t)(xres(g, c.epoch, j, g.B - 1, g.kc - 1) - g.xbuf) + HT <= g.n_xbuf,
+                      c.pc, -1)) {
+    ok = false;
+    j = 1;
+  }
   // split MLP: x_{2l+2} (j even, j > 0) arrives as tagged words from the
   // down rows' owners; each thread polls its own 8-element groups
   const bool tagged = g.xtag && j > 0 && (j & 1) == 0;
-  bool ok = true;
   if constexpr (NB == 1) {
     if (tagged) {  // this thread's groups, polled together straight into xn
       uint32_t valid = 0;
 #pragma unroll
       for (int q = 0; q < GPT; q++)
         if (c.tid + q * NCT < GROUPS) valid |= 1u << q;
-      ok = poll_tag_groups_to<GPT, 4>(g, g.xt + (size_t)(j / 2 - 1) * HT + 8 * c.tid,
+      ok = ok && poll_tag_groups_to<GPT, 4>(g, g.xt + (size_t)(j / 2 - 1) * HT + 8 * c.tid,
                                       (size_t)NCT * 8, valid, c.epoch, c.xn + 8 * c.tid, NCT * 8,
                                       c.pc, OP_QKV);
     }
@@ -534,7 +553,7 @@ MK_DEV bool gemv_rows(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Seg& s
   float pend = 0.f;  // NB == 1: this lane's partial of the row not yet reduced
   int prow = -1;
   for (uint32_t u0 = 0; u0 < s.n; u0 += s.ups) {
-    const uint32_t n = min(s.ups, s.n - u0);
+    const uint32_t n = stage_units(g, s, u0, (uint32_t)g.stage_bytes, c.pc, -1);
     if (!c.ring.acquire(g)) return false;
     const unsigned char* st = c.ring.stage_ptr();
     // segment row u0 + r goes to warp (u0 + r) mod NCW, so a short segment
@@ -599,7 +618,7 @@ MK_DEV bool gemv_rows_mma(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Se
   uint32_t prow0 = 0, pending = 0;  // rows held in part since the last flush
   const uint32_t li = (uint32_t)c.lane & 7u, lm = (uint32_t)c.lane >> 3;
   for (uint32_t u0 = 0; u0 < s.n; u0 += s.ups) {
-    const uint32_t n = min(s.ups, s.n - u0);
+    const uint32_t n = stage_units(g, s, u0, (uint32_t)g.stage_bytes, c.pc, -1);
     if (!bad && !c.ring.acquire(g)) bad = true;
     if (!bad) {
       const uint32_t sbase = smem_u32(c.ring.stage_ptr());
@@ -726,14 +745,17 @@ MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I)
         y1 = bb;
       }
       if (hs < HPG) {
-        float* q = g.qbuf + (((size_t)I.layer * g.B + b) * g.Hq + (size_t)I.g * HPG + hs) * D;
-        q[t] = y0;
-        q[t + D / 2] = y1;
+        const size_t qo = (((size_t)I.layer * g.B + b) * g.Hq + (size_t)I.g * HPG + hs) * D;
+        if (MK_IN(g, qo + D <= g.n_q, c.pc, I.op)) {
+          float* q = g.qbuf + qo;
+          q[t] = y0;
+          q[t + D / 2] = y1;
+        }
       } else {
         const long long off = kv_row(g, b, I.g, P);
         if (off < 0) {
           set_err(g, MK_ERR_INVALID_ARG, c.pc, I.op);  // a block outside the pool
-        } else {
+        } else if (MK_IN(g, (size_t)off + D <= g.kv_elems, c.pc, I.op)) {
           uint16_t* row = (hs == HPG ? Lp.kc : Lp.vc) + off;
           row[t] = to_bf16(y0);
           row[t + D / 2] = to_bf16(y1);
@@ -768,7 +790,8 @@ MK_DEV bool op_attn(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I
   uint4 kP = zero, vP = zero;
   if (last && slot == 0) {
     const long long off = kv_row(g, b, I.g, P);
-    if (off >= 0) {  // (a bad block was reported by the append)
+    if (off >= 0 && MK_IN(g, (size_t)off + D <= g.kv_elems, c.pc, I.op)) {  // (a bad block was
+                                                                            // reported by the append)
       kP = __ldcg((const uint4*)(Lp.kc + off + dsl * 8));
       vP = __ldcg((const uint4*)(Lp.vc + off + dsl * 8));
     }
@@ -777,10 +800,8 @@ MK_DEV bool op_attn(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I
   float q[HPG][8], m[HPG], l[HPG], o[HPG][8];
 #pragma unroll
   for (int h = 0; h < HPG; h++) {
-    const float4* qp = (const float4*)(g.qbuf +
-                                       (((size_t)I.layer * g.B + b) * g.Hq + (size_t)I.g * HPG + h) *
-                                           D +
-                                       dsl * 8);
+    const size_t qo = (((size_t)I.layer * g.B + b) * g.Hq + (size_t)I.g * HPG + h) * D + dsl * 8;
+    const float4* qp = (const float4*)(g.qbuf + (MK_IN(g, qo + 8 <= g.n_q, c.pc, I.op) ? qo : 0));
     const float4 a0 = __ldcg(qp), a1 = __ldcg(qp + 1);
     q[h][0] = a0.x * QS; q[h][1] = a0.y * QS; q[h][2] = a0.z * QS; q[h][3] = a0.w * QS;
     q[h][4] = a1.x * QS; q[h][5] = a1.y * QS; q[h][6] = a1.z * QS; q[h][7] = a1.w * QS;
@@ -862,7 +883,7 @@ MK_DEV bool op_attn(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I
   get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
   constexpr uint32_t STEP = NCW * SPW;  // positions per pass of all warps' slots
   for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
-    const uint32_t n = min(s[0].ups, s[0].n - u0);
+    const uint32_t n = stage_units(g, s[0], u0, (uint32_t)g.stage_bytes / 2, c.pc, OP_ATTN);
     if (!c.ring.acquire(g)) break;
     const unsigned char* st = c.ring.stage_ptr();
     const unsigned char* vs = st + c.ring.sb / 2;
@@ -926,12 +947,15 @@ MK_DEV bool op_attn(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I
       Ls = fmaf(p[D + 1], f, Ls);
       O = fmaf(p[dim], f, O);
     }
-    float* dst = g.part + ((((size_t)I.layer * g.B + b) * g.Hq + (size_t)I.g * HPG + h) * g.splits +
-                           I.r0) * part_stride(D);
-    dst[dim] = O;
-    if (dim == 0) {
-      dst[D] = M;
-      dst[D + 1] = Ls;
+    const size_t po = ((((size_t)I.layer * g.B + b) * g.Hq + (size_t)I.g * HPG + h) * g.splits +
+                       I.r0) * part_stride(D);
+    if (MK_IN(g, po + D + 2 <= g.n_part, c.pc, I.op)) {
+      float* dst = g.part + po;
+      dst[dim] = O;
+      if (dim == 0) {
+        dst[D] = M;
+        dst[D + 1] = Ls;
+      }
     }
   }
   consumer_bar();
@@ -1016,7 +1040,8 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& 
     for (int it = c.tid; it < NB * SG * D; it += NCT) {
       const int dim = it % D, sg = (it / D) % SG, b = it / (D * SG);
       float M = NEG_BIG, Ls = 0.f, O = 0.f;
-      if (b < g.B) {
+      if (b < g.B && MK_IN(g, (((size_t)l * g.B + b) * g.Hq + h + 1) * S * PS <= g.n_part, c.pc,
+                           I.op)) {
         const float* base = g.part + (((size_t)l * g.B + b) * g.Hq + h) * S * PS;
 #pragma unroll 4
         for (int s2 = sg; s2 < S; s2 += SG) {
@@ -1046,9 +1071,9 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& 
       for (int t = c.tid; t < NB * nr; t += NCT) {
         const int b = t / nr, r = t % nr;
         float v = 0.f;
-        if (b < g.B) {
-          const TagWord* p = g.xt + ((size_t)(l - 1) * g.B + b) * g.H + I.r0 + r;
-          if (!poll_tag1(g, p, c.epoch, v, c.pc, I.op)) okr = false;
+        const size_t xo = ((size_t)(l - 1) * g.B + b) * g.H + I.r0 + r;
+        if (b < g.B && MK_IN(g, xo < g.n_xt, c.pc, I.op)) {
+          if (!poll_tag1(g, g.xt + xo, c.epoch, v, c.pc, I.op)) okr = false;
         }
         xr_s[t] = v;
       }
@@ -1126,7 +1151,7 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& 
     float* dst = xres_mine(g, c.epoch, 2 * l + 1, 0);
     uint32_t bc = 0;  // 32-row blocks of earlier stages (round-robin offset)
     for (uint32_t u0 = 0; u0 < wseg.n; u0 += wseg.ups) {
-      const uint32_t n = min(wseg.ups, wseg.n - u0);
+      const uint32_t n = stage_units(g, wseg, u0, (uint32_t)g.stage_bytes, c.pc, OP_OPROJ);
       if (!c.ring.acquire(g)) break;
       const unsigned char* st = c.ring.stage_ptr();
       const uint32_t nblk = (n + 31) / 32;
@@ -1180,7 +1205,7 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& 
 #pragma unroll
           for (int e = 0; e < 8; e++) a[e] = fmaf(wf[e], xv[e], a[e]);
         }
-        if (valid) {
+        if (valid && MK_IN(g, (size_t)(dst - g.xbuf) + row < g.n_xbuf, c.pc, I.op)) {
           float v = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
           if constexpr (WB == 1) v *= c.sc[row - I.r0];
           if (resid) v += xr_s[row - I.r0];
@@ -1217,7 +1242,7 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& 
     const uint32_t li = (uint32_t)c.lane & 7u, mi = (uint32_t)c.lane >> 3;
     uint32_t tc = 0;  // 8-row tiles of earlier stages (round-robin offset)
     for (uint32_t u0 = 0; u0 < wseg.n; u0 += wseg.ups) {
-      const uint32_t n = min(wseg.ups, wseg.n - u0);
+      const uint32_t n = stage_units(g, wseg, u0, (uint32_t)g.stage_bytes, c.pc, OP_OPROJ);
       if (!c.ring.acquire(g)) break;
       const uint32_t sbase = smem_u32(c.ring.stage_ptr());
       const uint32_t nt = (n + 7) / 8;
@@ -1233,7 +1258,8 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& 
 #pragma unroll
         for (int kt = 0; kt < KT; kt++) mma_16816(d, af[kt], b[2 * kt], b[2 * kt + 1]);
         const uint32_t r = t * 8 + 2u * (uint32_t)tq;  // stage row of this lane's pair
-        if (live && r < n) {
+        if (live && r < n &&
+            MK_IN(g, (size_t)(dst - g.xbuf) + I.r0 + u0 + r + 2 <= g.n_xbuf, c.pc, I.op)) {
           const int row = (int)(I.r0 + u0 + r);
           float v0 = d[0] + d[2], v1 = d[1] + d[3];
           if (resid) {
@@ -1374,7 +1400,7 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I)
 #pragma unroll
       for (int k = 0; k < 4; k++) acc[q][b][k] = 0.f;
   for (uint32_t u0 = 0; u0 < s[1].n; u0 += s[1].ups) {
-    const uint32_t n = min(s[1].ups, s[1].n - u0);
+    const uint32_t n = stage_units(g, s[1], u0, (uint32_t)g.stage_bytes, c.pc, OP_MLP);
     if (!c.ring.acquire(g)) break;
     const unsigned char* st = c.ring.stage_ptr();
     for (uint32_t j = 0; j < n; j++) {
@@ -1482,7 +1508,8 @@ MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr&
           gt *= usc.x;
           up *= usc.y;
         }
-        g.hglob[((size_t)l * g.B + b) * g.F + I.r0 + j] = (gt / (1.f + expf(-gt))) * up;
+        const size_t ho = ((size_t)l * g.B + b) * g.F + I.r0 + j;
+        if (MK_IN(g, ho < g.n_h, c.pc, I.op)) g.hglob[ho] = (gt / (1.f + expf(-gt))) * up;
       }
     }
   }
@@ -1544,7 +1571,7 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Inst
     get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
     bool bad = false;
     for (uint32_t v0 = 0; v0 < s[0].n; v0 += s[0].ups) {
-      const uint32_t n = min(s[0].ups, s[0].n - v0);
+      const uint32_t n = stage_units(g, s[0], v0, (uint32_t)g.stage_bytes, c.pc, OP_MLP_DOWN);
       if (!c.ring.acquire(g)) {
         bad = true;
         break;
@@ -1599,7 +1626,9 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Inst
       if (c.tid < nrows) dsc = __ldg(g.layers[l].sd + I.r0 + c.tid);
     if (!dep_wait(c, g, I)) return false;
     float h[CPT][CW];
-    const float* hp = g.hglob + (size_t)l * F;
+    // (the whole row of h this layer's down rows read)
+    const float* hp =
+        g.hglob + (MK_IN(g, ((size_t)l + 1) * F <= g.n_h, c.pc, I.op) ? (size_t)l * F : 0);
 #pragma unroll
     for (int q = 0; q < CPT; q++) {
       const int k = c.tid + q * NCT;
@@ -1619,7 +1648,7 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Inst
     Seg s[2];
     get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
     for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
-      const uint32_t n = min(s[0].ups, s[0].n - u0);
+      const uint32_t n = stage_units(g, s[0], u0, (uint32_t)g.stage_bytes, c.pc, OP_MLP_DOWN);
       if (!c.ring.acquire(g)) break;
       const unsigned char* st = c.ring.stage_ptr();
       for (uint32_t j = 0; j < n; j++) {
@@ -1669,7 +1698,8 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Inst
 #pragma unroll
       for (int w = 0; w < NCW; w++) y += part[w * MAX_DOWN_ROWS + c.tid];
       if constexpr (WB == 1) y *= dsc;
-      st_tag(g.xt + (size_t)l * g.B * g.H + I.r0 + c.tid, res + y, c.epoch);
+      const size_t xo = (size_t)l * g.B * g.H + I.r0 + c.tid;
+      if (MK_IN(g, xo < g.n_xt, c.pc, I.op)) st_tag(g.xt + xo, res + y, c.epoch);
     }
     consumer_bar();
     return true;
@@ -1689,7 +1719,8 @@ MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr&
     const size_t total = (size_t)2 * g.L * g.kc * g.B * g.H;
     const size_t a = total * I.aux / (size_t)g.n_lm, e = total * (I.aux + 1) / (size_t)g.n_lm;
     float* nx = g.xbuf + (size_t)((c.epoch + 1u) & 1u) * total;
-    for (size_t i = a + c.tid; i < e; i += NCT) nx[i] = 0.f;
+    if (MK_IN(g, 2 * total <= g.n_xbuf, c.pc, I.op))
+      for (size_t i = a + c.tid; i < e; i += NCT) nx[i] = 0.f;
   }
   NormGain<HT, NB> ng;
   norm_gain(ng, g.final_norm, c.tid);
@@ -1712,10 +1743,11 @@ MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr&
   float* logits = g.logits;
   const uint32_t r0 = I.r0;
   const float* rsc = c.sc;
+  const int pcI = c.pc;
   gemv(c, g, s[0], xr, [&](uint32_t r, int b, float y) {
     if constexpr (WB == 1) y *= rsc[r];
     const int row = (int)(r0 + r);
-    logits[(size_t)b * V + row] = y;
+    if (MK_IN(g, row < V, pcI, OP_LMHEAD)) logits[(size_t)b * V + row] = y;
     if (y > best || (y == best && row < bidx)) {
       best = y;
       bidx = row;
@@ -1740,7 +1772,7 @@ MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr&
   }
   consumer_bar();
   if (c.warp != 0) return true;
-  if (lane == 0) {
+  if (lane == 0 && MK_IN(g, ((size_t)I.aux + 1) * B <= g.n_lmv, c.pc, I.op)) {
     for (int b = 0; b < B && b < NB; b++) {
       float v = -INFINITY;
       int ix = 0x7FFFFFFF;
@@ -1877,6 +1909,23 @@ struct L2Cursor {
     }
   }
 };
+
+// The source of a bulk copy, checked in the bounds build: it must lie in the
+// packed weights, the scratch or the instruction's layer of K / V cache;
+// otherwise MK_ERR_BOUNDS is recorded and the copy reads the first bytes of
+// the packed weights instead, so the stage still completes (the step has
+// failed by then).
+MK_DEV const unsigned char* copy_src(const Globals& g, const Instr& I, const unsigned char* p,
+                                     uint32_t bytes, int pc) {
+#ifdef MK_BOUNDS
+  const LayerPtrs* Lp = g.layers + (I.op == OP_LMHEAD ? 0 : I.layer);
+  const size_t kvb = g.kv_elems * 2;
+  const bool ok = span_in(p, bytes, g.pk_lo, g.pk_bytes) || span_in(p, bytes, g.sc_lo, g.sc_bytes) ||
+                  span_in(p, bytes, Lp->kc, kvb) || span_in(p, bytes, Lp->vc, kvb);
+  if (!MK_IN(g, ok, pc, I.op)) return g.pk_lo;
+#endif
+  return p;
+}
 
 // Producer warp: walks the queue and streams every instruction's segments
 // into the ring (lane 0 issues).  It waits for free stages, and besides:
@@ -2015,6 +2064,14 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
             }
           }
         }
+#ifdef MK_BOUNDS
+        {  // the stage (or each half) must hold what the segment puts there
+          const uint32_t room = s[k].src2 ? (uint32_t)g.stage_bytes / 2 : (uint32_t)g.stage_bytes;
+          int bad = 0;
+          if (lane == 0 && !MK_IN(g, n * s[k].unit <= room, pc, I.op)) bad = 1;
+          if (__shfl_sync(0xFFFFFFFFu, bad, 0)) goto drain;
+        }
+#endif
         if (lane == 0) {
           if (g.trace && k == 0 && u0 == 0)
             g.trace[((size_t)qid * g.max_pc + pc) * 8] = gtimer();
@@ -2039,16 +2096,20 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
               }
               const uint32_t pb = (uint32_t)(re - r) * (uint32_t)(D * 2);
               const uint32_t at = (uint32_t)(r - p0) * (uint32_t)(D * 2);
-              bulk_g2s(dst + at, Lp->kc + off, pb, full, pol_kv);
-              bulk_g2s(dst + (uint32_t)g.stage_bytes / 2 + at, Lp->vc + off, pb, full, pol_kv);
+              bulk_g2s(dst + at, copy_src(g, I, (const unsigned char*)(Lp->kc + off), pb, pc), pb, full,
+                       pol_kv);
+              bulk_g2s(dst + (uint32_t)g.stage_bytes / 2 + at,
+                       copy_src(g, I, (const unsigned char*)(Lp->vc + off), pb, pc), pb, full, pol_kv);
               r = re;
             }
           } else if (s[k].src2) {
-            bulk_g2s(dst, s[k].src + (size_t)u0 * s[k].unit, bytes, full, pol_kv);
-            bulk_g2s(dst + (uint32_t)g.stage_bytes / 2, s[k].src2 + (size_t)u0 * s[k].unit, bytes, full,
+            bulk_g2s(dst, copy_src(g, I, s[k].src + (size_t)u0 * s[k].unit, bytes, pc), bytes, full,
                      pol_kv);
+            bulk_g2s(dst + (uint32_t)g.stage_bytes / 2,
+                     copy_src(g, I, s[k].src2 + (size_t)u0 * s[k].unit, bytes, pc), bytes, full, pol_kv);
           } else {
-            bulk_g2s(dst, s[k].src + (size_t)u0 * s[k].unit, bytes, full, pol_w);
+            bulk_g2s(dst, copy_src(g, I, s[k].src + (size_t)u0 * s[k].unit, bytes, pc), bytes, full,
+                     pol_w);
           }
         }
         issued_bytes += (s[k].src2 ? 2ull : 1ull) * n * s[k].unit;

@@ -262,6 +262,28 @@ MK_DEV void set_err(const Globals& g, int code, int pc, int op) {
   }
 }
 
+// ---- bounds-checked build -------------------------------------------------
+// With MK_BOUNDS defined (the libmk_bounds.so build), MK_IN(g, cond, pc, op)
+// checks an access before it happens: a violation records MK_ERR_BOUNDS (with
+// the SM, pc and op) in the error word, and the caller skips the access, so
+// nothing traps and no out-of-range address is ever touched.  Without it the
+// check is the constant true and compiles away.
+#ifdef MK_BOUNDS
+MK_DEV bool mk_in(const Globals& g, bool ok, int pc, int op) {
+  if (!ok) set_err(g, MK_ERR_BOUNDS, pc, op);
+  return ok;
+}
+#define MK_IN(g, cond, pc, op) mk_in((g), (cond), (pc), (op))
+#else
+#define MK_IN(g, cond, pc, op) true
+#endif
+
+// [p, p + bytes) inside [lo, lo + n)
+MK_DEV bool span_in(const void* p, size_t bytes, const void* lo, size_t n) {
+  const unsigned char *a = (const unsigned char*)p, *b = (const unsigned char*)lo;
+  return a >= b && a + bytes <= b + n;
+}
+
 // ---- KV cache rows -------------------------------------------------------
 // Element offset of cache row p of (sequence b, kv head h): contiguous
 // [B][Hkv][max_seq][D], or paged -- block kv_table[b][p / blk] of the pool

@@ -250,6 +250,15 @@ struct Globals {
   unsigned long long l2_ahead;  // bytes of the SM's stream warmed in L2 ahead of the ring (0: off)
   unsigned hold_early;          // bytes of a held instruction's copies issued before the
                                 // consumers finish the previous instruction (whole stages)
+  // extents, for the bounds-checked build (MK_BOUNDS): the library's scratch
+  // and packed-weight allocations, one layer's K (or V) cache, and the
+  // element counts of the scratch buffers the ops index
+  const unsigned char* sc_lo;
+  size_t sc_bytes;
+  const unsigned char* pk_lo;
+  size_t pk_bytes;
+  size_t kv_elems;              // bf16 elements of one layer's K (or V) cache or pool
+  size_t n_xbuf, n_q, n_part, n_h, n_xt, n_lmv;  // n_lmv: lm_val / lm_idx elements
 };
 
 // Shared-memory layout (bytes from the dynamic shared memory base).

@@ -38,6 +38,7 @@ extern "C" {
 #define MK_ERR_NOT_READY (-6)   /* mk_build_schedule has not succeeded yet         */
 #define MK_ERR_DEVICE (-7)      /* device reported an internal inconsistency       */
 #define MK_ERR_SCRATCH (-8)     /* scratch need exceeds the fixed no-allocation array */
+#define MK_ERR_BOUNDS (-9)      /* bounds-checked build only: an access fell outside its buffer */
 
 typedef struct mk_handle mk_handle;
 

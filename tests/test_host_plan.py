@@ -30,8 +30,21 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(lib, n), n
 
 
+def test_bounds_library_exports_every_declared_symbol():
+    # the bounds-checked build (MK_BOUNDS: the small variant with every
+    # checked access guarded) has the same C ABI
+    from decode_megakernel_sm_gb300 import build as B
+    L.lib()  # builds both libraries when either is stale
+    lib = C.CDLL(B.LIB_BOUNDS)
+    for n in sorted(declared_symbols()):
+        assert hasattr(lib, n), n
+    f = lib.mk_status_string
+    f.restype, f.argtypes = C.c_char_p, [C.c_int]
+    assert b"bounds" in f(L.MK_ERR_BOUNDS)
+
+
 def test_status_strings():
-    for s in range(0, -8, -1):
+    for s in range(0, -10, -1):
         assert L.mk_status_string(s) not in ("", "unknown status")
     assert L.mk_status_string(-99) == "unknown status"
 
