@@ -157,10 +157,14 @@ def traffic_record(config, steps_per_launch=1):
     exact = j.get(config if steps_per_launch == 1 else f"{config}@{steps_per_launch}")
     if exact and exact.get("kernel_src_sha") == src:
         return float(exact["dram_bytes_per_launch"]), f"ncu, launches of {steps_per_launch} step(s)"
-    for key, e in sorted(j.items()):
+    near = []  # captures of other launch sizes, nearest size first
+    for key, e in j.items():
         if key.split("@")[0] != config or e.get("kernel_src_sha") != src:
             continue
         spl = int(key.split("@")[1]) if "@" in key else 1
+        near.append((abs(spl - steps_per_launch), -spl, spl, e))
+    if near:
+        _, _, spl, e = min(near, key=lambda x: x[:2])
         per_step = float(e["dram_bytes_per_launch"]) / spl
         return per_step * steps_per_launch, (f"ncu, launches of {spl} step(s), scaled to "
                                              f"{steps_per_launch}")
