@@ -35,7 +35,8 @@ struct Ctx {
   float* topw;  // [NB][K] routed expert weights
   int* flag;    // [0] bad launch input, [2] a tagged-input poll failed, [3] / [4] key of
                 // the instruction whose counter was seen / whose wait failed
-                // (both shared by the consumer warps; [1] belongs to the producer)
+                // (both shared by the consumer warps; [1] belongs to the producer),
+                // [5] a router's arrival count
   Ring ring;
   int tid, warp, lane;
   int pc;
@@ -1330,7 +1331,10 @@ MK_DEV bool op_router(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr&
   // logits above logit i, equal ones with a lower id counting as above.
   // Weights are the probabilities renormalised over the K chosen,
   // exp(l - l_max) / sum.  Batch 1 (sequence 0).
-  int* arrived = c.flag + 3;
+  // (its own slot: flag[3] holds the dependency-wait key of the instruction
+  // whose counter was seen, and an arrival count equal to the next
+  // instruction's key would let that instruction skip its wait)
+  int* arrived = c.flag + 5;
   if (c.tid == 0)
     *arrived = (int)atom_add_acq_rel(g.ctr + CtrMap{g.Hkv, g.L}.router_arrive(I.layer), 1u);
   consumer_bar();

@@ -204,6 +204,16 @@ def test_moe_split_mlp_parity(shared):
     run_steps(_moe_split_cfg(shared), 4, seed=25)
 
 
+def test_moe_fused_mlp_without_shared_expert():
+    # no shared expert, expert width 204 (not whole 16-byte chunks): fused
+    # slices, and every SM's first MLP instruction waits on the router.  The
+    # routers' arrival counts once shared a word with the dependency wait's
+    # seen-key, so an instruction whose key equalled an arrival count skipped
+    # its wait on the routing; this shape hit that
+    cfg = dict(_moe_split_cfg(0), expert_ffn=204)
+    run_steps(cfg, 4, seed=25)
+
+
 def test_moe_split_mlp_held():
     # every op held, no early stage: the gathered down rows wait for the
     # routing and for the gate/up slices' signal
