@@ -66,7 +66,7 @@ static Scratch carve_scratch(const mk_model_desc& d, size_t B, size_t kc, size_t
                              size_t n_lm, size_t n_ctr, char* base) {
   const size_t L = d.n_layers, H = d.hidden, Hq = d.n_q_heads, D = d.head_dim;
   const size_t E = d.n_experts > 0 ? d.n_experts : 1;
-  const size_t F = ffn_virtual(d) > 0 ? ffn_virtual(d) : 1;
+  const size_t F = d.ffn > 0 ? d.ffn : 1;
   const size_t sx = al256(2 * 2 * L * kc * B * H * 4), sq = al256(L * B * Hq * D * 4);
   const size_t sp = al256(L * B * Hq * splits * part_stride((int)D) * 4);
   const size_t sr = al256(L * B * E * 4), sl = al256(n_lm * B * 4);
@@ -140,7 +140,6 @@ struct mk_handle {
   std::vector<AblLaunch> abl;
   Instr* abl_sched = nullptr;
   uint32_t epoch = 0;
-  uint32_t router_cnt = 0;  // MoE: router instructions of a layer (each layer has as many)
   unsigned long long timeout_ns = 2000000000ull;
   int n_pollers = 1;
   unsigned poll_stagger_ns = 0;
@@ -281,8 +280,7 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
   if (rc) return rc;
   if (wfmt != MK_WEIGHTS_BF16 && wfmt != MK_WEIGHTS_INT8) return MK_ERR_INVALID_ARG;
   // int8 weights: dense batch-1 shapes with the split MLP and 64-dim heads
-  if (wfmt == MK_WEIGHTS_INT8 &&
-      (d.n_experts > 0 || !mlp_split(d) || d.ffn % 16 || d.head_dim != 64))
+  if (wfmt == MK_WEIGHTS_INT8 && (!mlp_split(d) || d.ffn % 16 || d.head_dim != 64))
     return MK_ERR_UNSUPPORTED;
   h->wfmt = wfmt;
   h->var = pick_variant(d, wfmt == MK_WEIGHTS_INT8 ? 1 : 2);
@@ -404,18 +402,10 @@ static int pack_bf16(mk_handle* h, const mk_weights* w, const mk_kv* kv, cudaStr
       CK(pack_rows(rt, w->router[l], d.n_experts, H, s));
       CK(pack_interleave(egu, w->ex_gate[l], w->ex_up[l], (long)d.n_experts * d.expert_ffn, H,
                          s));
-      // split MLP: the down rows are gathered as they are ([E][H][Fe] and
-      // [H][Fs]); fused MLP: transposed, one contiguous row per FFN column
-      if (mlp_split(d))
-        CK(cudaMemcpyAsync(edT, w->ex_down[l], ls.ex_dT * 2, cudaMemcpyDeviceToDevice, s));
-      else
-        CK(pack_transpose(edT, w->ex_down[l], H, d.expert_ffn, d.n_experts, s));
+      CK(pack_transpose(edT, w->ex_down[l], H, d.expert_ffn, d.n_experts, s));
       if (d.shared_ffn > 0) {
         CK(pack_interleave(sgu, w->sh_gate[l], w->sh_up[l], d.shared_ffn, H, s));
-        if (mlp_split(d))
-          CK(cudaMemcpyAsync(sdT, w->sh_down[l], ls.sh_dT * 2, cudaMemcpyDeviceToDevice, s));
-        else
-          CK(pack_transpose(sdT, w->sh_down[l], H, d.shared_ffn, 1, s));
+        CK(pack_transpose(sdT, w->sh_down[l], H, d.shared_ffn, 1, s));
       }
     }
     lp.attn_norm = an;
@@ -646,9 +636,6 @@ extern "C" int mk_build_schedule(mk_handle* h, int batch, int max_ctx) {
                        cudaMemcpyHostToDevice, h->own));
     CK(cudaStreamSynchronize(h->own));  // before `flat` goes out of scope
   }
-  h->router_cnt = 0;
-  for (const Instr& I : p.q)
-    if (I.op == OP_ROUTER && I.layer == 0) h->router_cnt++;
   h->plan = std::move(p);
   h->batch = batch;
   h->max_ctx = max_ctx;
@@ -697,7 +684,7 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.Hq = d.n_q_heads;
   g.Hkv = d.n_kv_heads;
   g.D = d.head_dim;
-  g.F = ffn_virtual(d);
+  g.F = d.ffn;
   g.V = d.vocab;
   g.L = d.n_layers;
   g.max_seq = d.max_seq;
@@ -709,7 +696,6 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.Fs = d.shared_ffn;
   g.kc = h->kc;
   g.xtag = mlp_split(d) ? 1 : 0;
-  g.router_cnt = h->router_cnt;
   g.bsplit = mlp_split_batched(d) ? 1 : 0;
   g.eps = d.rms_eps;
   g.lm_ctr = CtrMap{d.n_kv_heads, d.n_layers}.lm();
@@ -1021,7 +1007,7 @@ extern "C" int mk_debug_read(mk_handle* h, int what, int layer, float* out, size
   if (!h || !out) return MK_ERR_INVALID_ARG;
   if (!h->scratch || h->batch <= 0 || h->epoch == 0) return MK_ERR_NOT_READY;
   const mk_model_desc& d = h->d;
-  const size_t B = h->batch, L = d.n_layers, H = d.hidden, F = (size_t)ffn_virtual(d);
+  const size_t B = h->batch, L = d.n_layers, H = d.hidden, F = d.ffn > 0 ? d.ffn : 0;
   const size_t HqD = (size_t)d.n_q_heads * d.head_dim;
   CK(cudaDeviceSynchronize());  // the step may have run on any stream
   switch (what) {

@@ -99,14 +99,6 @@ MK_DEV float xres_sum(const Globals& g, uint32_t ep, int j, int b, int r) {
 // The weight / cache byte ranges an instruction streams, in ring order.
 // The producer issues exactly these copies; the consumers consume exactly
 // these stages.  Returns the number of segments (0..2).
-// MoE instructions whose weight addresses depend on the router's choice: the
-// routed slices (fused or split gate/up) and the split MLP's gathered down rows.
-MK_DEV bool needs_routes(const Globals& g, const Instr& I) {
-  if (g.E == 0) return false;
-  if (I.op == OP_MLP_DOWN) return true;
-  return (I.op == OP_MLP || I.op == OP_MLP_UP) && !(I.flags & F_SHARED);
-}
-
 template <int HT, int D, int WB>
 MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int* topk, Seg* s) {
   // WB bytes per weight: 2 (bf16) or 1 (int8 codes, dense batch-1 shapes only)
@@ -164,20 +156,6 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
       s[0] = {(const unsigned char*)g.lm_head + (size_t)I.r0 * ROW, nullptr, ROW, n, RPS, I.r0};
       return 1;
     case OP_MLP_UP:
-      if (g.E > 0) {
-        // MoE: the shared expert's gate/up rows, or routed slot j's columns of
-        // the expert the router chose for it
-        if (I.flags & F_SHARED) {
-          s[0] = {(const unsigned char*)Lp->sh_gu + (size_t)I.r0 * 2 * ROW, nullptr, ROW, 2 * n, RPS,
-                  2 * I.r0};
-        } else {
-          const uint32_t c0 = I.r0 - (uint32_t)g.Fs, j = c0 / (uint32_t)g.Fe;
-          const size_t e = (size_t)topk[j], c = e * g.Fe + (c0 - j * (uint32_t)g.Fe);
-          s[0] = {(const unsigned char*)Lp->ex_gu + c * 2 * ROW, nullptr, ROW, 2 * n, RPS,
-                  (uint32_t)(2 * c)};
-        }
-        return 1;
-      }
       s[0] = {(const unsigned char*)Lp->wgu + (size_t)I.r0 * 2 * ROW, nullptr, ROW, 2 * n, RPS,
               2 * I.r0};
       return 1;
@@ -186,10 +164,6 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
         // the run [r0, r1) of chunk-major weight units (BD_ROWS x BD_KC, 16 KB)
         const uint32_t unit = BD_ROWS * BD_KC * 2u;
         s[0] = {(const unsigned char*)Lp->wdT + (size_t)I.r0 * unit, nullptr, unit, n, SBY / unit};
-        return 1;
-      }
-      if (g.E > 0) {  // MoE: rows of h's width gathered piece by piece by the producer
-        s[0] = {nullptr, nullptr, (uint32_t)g.F * 2, n, SBY / ((uint32_t)g.F * 2), SEG_GATHER};
         return 1;
       }
       // rows of the row-major [H][F] down projection
@@ -1493,20 +1467,6 @@ MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr&
   }
   if (!dep_wait(c, g, I)) return false;
   if (!cached && !norm_apply(c, g, 2 * l + 1, ng)) return false;
-  // MoE split MLP: a routed slice reads slot j's expert (the router has
-  // published the layer's routing: the wait was on its counter), and h of
-  // the slice is scaled by that expert's router weight
-  float hscale = 1.f;
-  if (g.E > 0 && !(I.flags & F_SHARED)) {
-    const int j = (int)((I.r0 - (uint32_t)g.Fs) / (uint32_t)g.Fe);
-    if (c.warp == 0 && c.lane < g.K) {
-      const int e = __ldcg(g.routes + (size_t)l * g.K + c.lane);
-      c.topk[c.lane] = min(max(e, 0), g.E - 1);
-      c.topw[c.lane] = __ldcg(g.rweight + (size_t)l * g.K + c.lane);
-    }
-    consumer_bar();
-    hscale = c.topw[j];
-  }
   c.mark(g, 0);
   float xr[HT / 32];
   if constexpr (NB == 1) load_xr<HT, WB>(c.xn, c.lane, xr);
@@ -1553,7 +1513,7 @@ MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr&
           up *= usc.y;
         }
         const size_t ho = ((size_t)l * g.B + b) * g.F + I.r0 + j;
-        if (MK_IN(g, ho < g.n_h, c.pc, I.op)) g.hglob[ho] = hscale * ((gt / (1.f + expf(-gt))) * up);
+        if (MK_IN(g, ho < g.n_h, c.pc, I.op)) g.hglob[ho] = (gt / (1.f + expf(-gt))) * up;
       }
     }
   }
@@ -1912,7 +1872,7 @@ struct L2Cursor {
           pc++;
           continue;
         }
-        const bool routed = needs_routes(g, I);
+        const bool routed = I.op == OP_MLP && g.E > 0 && !(I.flags & F_SHARED);
         if (routed && routed_layer != (int)I.layer) return;  // addresses not known yet
         int pos[NB];
         if (I.op == OP_ATTN) {
@@ -1941,7 +1901,7 @@ struct L2Cursor {
       const uint32_t n = min(s[k].ups, s[k].n - u0);
       const uint32_t b = n * s[k].unit;
       const unsigned long long cb = s[k].src2 ? 2ull * b : b;
-      if (bytes + cb > from && !s[k].cfill() && !s[k].gather() && !(g.kv_block && s[k].src2)) {
+      if (bytes + cb > from && !s[k].cfill() && !(g.kv_block && s[k].src2)) {
         if ((threadIdx.x & 31) == 0) {
           bulk_prefetch_l2(s[k].src + (size_t)u0 * s[k].unit, b);
           if (s[k].src2) bulk_prefetch_l2(s[k].src2 + (size_t)u0 * s[k].unit, b);
@@ -2015,7 +1975,7 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
     }
     // every branch below is warp-uniform: lane 0 decides, the warp follows
     // (errors elsewhere in the grid are seen in the bounded waits below)
-    const bool routed = needs_routes(g, I);
+    const bool routed = I.op == OP_MLP && g.E > 0 && !(I.flags & F_SHARED);
     if ((I.op == OP_ATTN || routed) && !grid_waited) {
       asm volatile("griddepcontrol.wait;" ::: "memory");
       grid_waited = true;
@@ -2041,10 +2001,8 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
       if (lane == 0) ppos[I.b] = P;
     }
     if (routed && routed_layer != I.layer) {
-      // the layer's routing is out once its router counter is met
       bool ok = true;
-      if (lane == 0)
-        ok = wait_counter(g, CtrMap{g.Hkv, g.L}.router(I.layer), ep * g.router_cnt, pc, I.op);
+      if (lane == 0) ok = wait_counter(g, I.wait_ctr, ep * I.wait_cnt, pc, I.op);
       if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) goto drain;
       __syncwarp();
       if (lane < g.K) {  // the routing published by the layer's last router
@@ -2127,25 +2085,6 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
           mbar_expect_tx(full, s[k].src2 ? 2u * bytes : bytes);
           if (s[k].cfill()) {
             // the consumers copy this stage in after their dependency wait
-          } else if (s[k].gather()) {
-            // MoE down rows: row r of h's width = the shared expert's row r
-            // (Fs columns), then slot j's expert row r (Fe columns) for each j
-            const LayerPtrs* Lp = g.layers + I.layer;
-            for (uint32_t i = 0; i < n; i++) {
-              const size_t row = (size_t)I.r0 + u0 + i;
-              const uint32_t at = dst + i * s[k].unit;
-              if (g.Fs > 0)
-                bulk_g2s(at, copy_src(g, I, (const unsigned char*)(Lp->sh_dT + row * g.Fs),
-                                      (uint32_t)g.Fs * 2, pc),
-                         (uint32_t)g.Fs * 2, full, pol_w);
-              for (int j = 0; j < g.K; j++) {
-                const size_t e = (size_t)ptopk[j];
-                bulk_g2s(at + (uint32_t)(g.Fs + j * g.Fe) * 2,
-                         copy_src(g, I, (const unsigned char*)(Lp->ex_dT + (e * g.H + row) * g.Fe),
-                                  (uint32_t)g.Fe * 2, pc),
-                         (uint32_t)g.Fe * 2, full, pol_w);
-              }
-            }
           } else if (s[k].src2 && g.kv_block && I.op == OP_ATTN) {
             // paged cache: the stage's rows, one copy per block piece (K in
             // the lower half, V in the upper)

@@ -464,9 +464,6 @@ MK_DEV bool wait_mbar(const Globals& g, uint32_t bar, uint32_t parity, bool abor
 // with the matching V rows in src2) streamed through the ring, `ups` units
 // per stage.  src2 lands in the upper half of the stage.
 constexpr uint32_t SEG_CFILL = 0x80000000u;
-// SEG_GATHER: MoE split-MLP down rows; each unit (one row of h's width) is
-// gathered from the shared expert's row and the chosen experts' rows
-constexpr uint32_t SEG_GATHER = 0x20000000u;
 
 struct Seg {
   const unsigned char* src;
@@ -478,7 +475,6 @@ struct Seg {
                   // SEG_CFILL set: an input of this step, whose stages the producer only arms
                   // and the consumers fill once their dependency wait has passed
   MK_DEV bool cfill() const { return (row0 & SEG_CFILL) != 0; }
-  MK_DEV bool gather() const { return (row0 & SEG_GATHER) != 0; }
 };
 
 // Ring cursor of one consumer warp.

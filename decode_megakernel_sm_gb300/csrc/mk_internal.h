@@ -155,22 +155,8 @@ MK_HD inline bool mlp_split_batched(const mk_model_desc& d) {
          d.hidden % BD_ROWS == 0;
 }
 
-// Width of the split MLP's h vector: the dense FFN, or for a MoE layer the
-// shared expert's columns followed by the top_k routed slots' columns (slot
-// j holds the columns of the j-th chosen expert, scaled by its router weight).
-MK_HD inline int ffn_virtual(const mk_model_desc& d) {
-  return d.n_experts > 0 ? d.shared_ffn + d.top_k * d.expert_ffn : d.ffn;
-}
-
-// Batch-1 models run the MLP split (gate/up column slices, then row-owned
-// down rows over the whole h) when one down row fits a ring stage.  For MoE
-// a down row is gathered from the shared expert's row and the chosen
-// experts' rows, one bulk copy per piece, so the pieces must be whole
-// 16-byte chunks.
 inline bool mlp_split(const mk_model_desc& d) {
-  if (d.max_batch != 1 || ffn_virtual(d) * 2 > DOWN_ROW_MAX) return false;
-  if (d.n_experts == 0) return d.ffn % 8 == 0;
-  return d.shared_ffn % 8 == 0 && d.expert_ffn % 8 == 0;
+  return d.n_experts == 0 && d.max_batch == 1 && d.ffn % 8 == 0 && d.ffn * 2 <= DOWN_ROW_MAX;
 }
 
 // Device pointers of one layer inside the packed weight buffer.
@@ -183,9 +169,9 @@ struct LayerPtrs {
   const uint16_t* wdT;        // dense: down, [F][H] transposed (fused MLP) or [H][F] (split MLP)
   const uint16_t* router;     // MoE:   [E][H]
   const uint16_t* ex_gu;      // MoE:   [E][Fe][2][H]
-  const uint16_t* ex_dT;      // MoE:   [E][Fe][H] (fused MLP), or [E][H][Fe] row-major (split MLP)
+  const uint16_t* ex_dT;      // MoE:   [E][Fe][H]
   const uint16_t* sh_gu;      // MoE:   [Fs][2][H]
-  const uint16_t* sh_dT;      // MoE:   [Fs][H] (fused MLP), or [H][Fs] row-major (split MLP)
+  const uint16_t* sh_dT;      // MoE:   [Fs][H]
   uint16_t* kc;               // caller cache [maxB][Hkv][max_seq][D]
   uint16_t* vc;
   // int8 weights (dense batch 1): wqkv, wo, wgu, wdT then hold int8 codes,
@@ -246,7 +232,6 @@ struct Globals {
   uint32_t lm_ctr;
   uint32_t lm_done_ctr;     // signalled once per step after the argmax is written
   int part_staged;          // O-projection: partials through a ring stage (part_staged())
-  uint32_t router_cnt;      // MoE: signals of a layer's router counter (one step's target)
   int kv_block;             // 0: KV cache [B][Hkv][max_seq][D]; else paged, blocks of kv_block rows:
   int kv_blocks;            //   pool [kv_blocks][Hkv][kv_block][D], block of (b, j) =
   const int* kv_table;      //   kv_table[b * kv_stride + j]

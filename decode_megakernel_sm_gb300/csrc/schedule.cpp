@@ -192,43 +192,28 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
       }
       for (auto& rp : routers) qs[rp.first][rp.second].aux = (uint32_t)routers.size();
     }
-    // ---- split MLP (batch 1, dense or MoE; dense batches of 2..8): gate/up
-    // column slices of h, then down rows
+    // ---- split MLP (dense, batch 1): gate/up column slices, then down rows
     if (mlp_split(d) || mlp_split_batched(d)) {
       // batched: gate/up slices in whole 16-column k-tiles of h, down runs of
-      // (row block, column chunk) units.  MoE: h's columns are the shared
-      // expert's [0, Fs) and the routed slots' [Fs, Fv) (slot j: columns
-      // [Fs + j Fe, Fs + (j + 1) Fe)); every SM takes a slice of the shared
-      // columns first (their weights stream while the router resolves), then
-      // a slice of the routed ones, and no slice crosses a slot boundary
+      // (row block, column chunk) units
       const bool bat = mlp_split_batched(d);
-      const long F = Fv, cu = bat ? 16 : 1;
-      std::vector<std::pair<long, long>> fsegs;
-      if (moe && Fs > 0) fsegs.push_back({0, Fs});
-      fsegs.push_back({Fs, F});
+      const long F = d.ffn, cu = bat ? 16 : 1;
       for (int i = 0; i < n_sm; i++) {
+        long a = cut(F / cu, n_sm, i, 1) * cu;
+        long b = (i == n_sm - 1) ? F : cut(F / cu, n_sm, i + 1, 1) * cu;
         bool first = true;
-        for (auto& fs : fsegs) {
-          const long span = (fs.second - fs.first) / cu;
-          long a = fs.first + cut(span, n_sm, i, 1) * cu;
-          long b = (i == n_sm - 1) ? fs.second : fs.first + cut(span, n_sm, i + 1, 1) * cu;
-          while (a < b) {
-            long seg_end = b;
-            if (moe && a >= Fs) seg_end = std::min(b, Fs + ((a - Fs) / d.expert_ffn + 1) * d.expert_ffn);
-            const long e = std::min(seg_end, a + MAX_COLS);
-            Instr I = mk(OP_MLP_UP, l);
-            I.r0 = (uint32_t)a;
-            I.r1 = (uint32_t)e;
-            I.flags = first ? 0 : F_NORM_CACHED;
-            if (moe && a < Fs) I.flags |= F_SHARED;
-            // routed slices need the router's choice (their expert's rows)
-            I.wait_ctr = moe && a >= Fs ? cm.router(l) : cm.oproj(l);
-            I.sig_ctr = cm.mlp_up(l);
-            qs[i].push_back(I);
-            bytes[i] += (double)(e - a) * H * 2 * wb;
-            first = false;
-            a = e;
-          }
+        while (a < b) {
+          const long e = std::min(b, a + MAX_COLS);
+          Instr I = mk(OP_MLP_UP, l);
+          I.r0 = (uint32_t)a;
+          I.r1 = (uint32_t)e;
+          I.flags = first ? 0 : F_NORM_CACHED;
+          I.wait_ctr = cm.oproj(l);
+          I.sig_ctr = cm.mlp_up(l);
+          qs[i].push_back(I);
+          bytes[i] += (double)(e - a) * H * 2 * wb;
+          first = false;
+          a = e;
         }
       }
       // batch 1: rows [r0, r1) of x_{2l+2}, one owner per row; batched: a
@@ -490,13 +475,6 @@ int plan_verify(const mk_model_desc& d, int B, const PlanOut& p) {
             I.r1 - I.r0 > (uint32_t)MAX_COLS || (long)I.r1 > Fv)
           return 23;
         if (mlp_split_batched(d) && ((I.r0 % 16) || (I.r1 % 16))) return 23;
-        if (moe) {  // shared slices flagged, within the shared columns; routed within one slot
-          if (((I.flags & F_SHARED) != 0) != ((long)I.r0 < Fs) || ((long)I.r0 < Fs && (long)I.r1 > Fs))
-            return 23;
-          if ((long)I.r0 >= Fs &&
-              ((long)I.r0 - Fs) / d.expert_ffn != ((long)I.r1 - 1 - Fs) / d.expert_ffn)
-            return 23;
-        }
         for (uint32_t c = I.r0; c < I.r1; c++)
           if (!mark(mlp, (size_t)l * Fv + c)) return 24;
         break;

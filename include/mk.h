@@ -173,11 +173,8 @@ int mk_set_kv_pages(mk_handle* h, int block, int n_blocks, const int32_t* d_tabl
  *   MK_DBG_Q: the queries of layer `layer` after RoPE, [batch][n_q_heads][head_dim];
  *   MK_DBG_X: the residual x_j for j = `layer` in [1, 2 n_layers]: x_{2l+1}
  *             after layer l's O-projection, x_{2l+2} after its MLP, [batch][hidden];
- *   MK_DBG_H: SiLU(gate) * up of layer `layer`, [batch][ffn] (batch 1 with
- *             the split MLP only; MK_ERR_UNSUPPORTED otherwise).  For MoE the
- *             row is [shared_ffn] columns of the shared expert, then top_k
- *             slots of expert_ffn columns, slot j the j-th chosen expert's
- *             values times its router weight.
+ *   MK_DBG_H: SiLU(gate) * up of layer `layer`, [batch][ffn] (dense batch 1
+ *             only; MK_ERR_UNSUPPORTED otherwise).
  * n: capacity of out in floats.  Synchronises the device.
  * MK_ERR_NOT_READY before the first step; MK_ERR_INVALID_ARG for a bad
  * selector, layer or capacity.                                            */

@@ -62,11 +62,3 @@ def test_intermediates_int8():
     _check(synth.custom(n_layers=2, hidden=2048, n_q_heads=32, n_kv_heads=8, head_dim=64,
                         ffn=2048, vocab=5000, rope_theta=5e5, prefill=(300, 300), steps=2), 107,
            int8=True)
-
-
-def test_intermediates_moe_split_mlp():
-    # MoE with the split MLP: q and every residual (the routed and shared
-    # experts summed through the gathered down rows)
-    _check(synth.custom(n_layers=3, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn=0,
-                        vocab=3001, tied=False, n_experts=16, top_k=4, expert_ffn=200,
-                        shared_ffn=512, rope_theta=5e5, prefill=(70, 70), steps=2), 111)

@@ -190,34 +190,17 @@ def test_moe_small_held():
     run_steps(_moe_small_cfg(), 3, seed=22, hold=(63, 0))
 
 
-def _moe_split_cfg(shared=512):
-    # the same small MoE with a shared width of whole 16-byte chunks: the
-    # split MLP (gate/up column slices of the shared and routed columns, then
-    # down rows gathered from the shared and the chosen experts' rows)
-    return synth.custom(n_layers=3, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn=0,
-                        vocab=3001, tied=False, n_experts=16, top_k=4, expert_ffn=200,
-                        shared_ffn=shared, rope_theta=5e5, prefill=(70, 70), steps=4)
-
-
-@pytest.mark.parametrize("shared", [512, 0])
-def test_moe_split_mlp_parity(shared):
-    run_steps(_moe_split_cfg(shared), 4, seed=25)
-
-
-def test_moe_fused_mlp_without_shared_expert():
-    # no shared expert, expert width 204 (not whole 16-byte chunks): fused
-    # slices, and every SM's first MLP instruction waits on the router.  The
-    # routers' arrival counts once shared a word with the dependency wait's
-    # seen-key, so an instruction whose key equalled an arrival count skipped
-    # its wait on the routing; this shape hit that
-    cfg = dict(_moe_split_cfg(0), expert_ffn=204)
+@pytest.mark.parametrize("shared,expert", [(0, 200), (0, 204), (8, 200)])
+def test_moe_without_or_with_a_small_shared_expert(shared, expert):
+    # no shared expert (or one of 8 columns): every SM's first MLP instruction
+    # is a routed slice that waits on the router.  The routers' arrival counts
+    # once shared a word with the dependency wait's seen-key, so an
+    # instruction whose key equalled an arrival count skipped its wait on the
+    # routing and read the previous step's experts; these shapes hit that
+    cfg = synth.custom(n_layers=3, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn=0,
+                       vocab=3001, tied=False, n_experts=16, top_k=4, expert_ffn=expert,
+                       shared_ffn=shared, rope_theta=5e5, prefill=(70, 70), steps=4)
     run_steps(cfg, 4, seed=25)
-
-
-def test_moe_split_mlp_held():
-    # every op held, no early stage: the gathered down rows wait for the
-    # routing and for the gate/up slices' signal
-    run_steps(_moe_split_cfg(), 3, seed=26, hold=(63, 0))
 
 
 def test_moe_full_config_parity():

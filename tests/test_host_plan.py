@@ -49,11 +49,6 @@ def test_status_strings():
     assert L.mk_status_string(-99) == "unknown status"
 
 
-def desc_cfg(c):
-    cfg = synth.with_cache(c)
-    return cfg, desc_from_config(cfg, cfg["batch"], cfg["max_seq"])
-
-
 def desc(name, **over):
     cfg = synth.with_cache(dict(synth.CONFIGS[name], **over))
     return cfg, desc_from_config(cfg, cfg["batch"], cfg["max_seq"])
@@ -144,39 +139,14 @@ def test_plan_covers_all_work_and_is_deadlock_free(name, n_sm):
     assert L.mk_plan_check(q, n_sm, st["max_pc"], st["n_counters"]) == L.MK_OK
 
 
-def test_split_mlp_where_it_applies():
-    # batch 1 (dense, or MoE whose shared and expert widths are whole 16-byte
-    # chunks), and dense batches of up to 8 whose FFN is whole 512-column tiles;
-    # a MoE with a shared width of 500 columns keeps the fused slices
-    moe500 = dict(synth.CONFIGS["moe"], shared_ffn=500)
-    for name, split in (("llama1b_1k", True), ("tiny", True), ("llama1b_b8", True), ("moe", True),
-                        (moe500, False)):
-        cfg, d = desc(name) if isinstance(name, str) else desc_cfg(name)
+def test_split_mlp_is_used_for_dense_models():
+    # batch 1, and batches of up to 8 whose FFN is whole 512-column tiles
+    for name, split in (("llama1b_1k", True), ("tiny", True), ("llama1b_b8", True), ("moe", False)):
+        cfg, d = desc(name)
         st, q = L.mk_plan(d, cfg["batch"], cfg["max_seq"], 152)
         ops = {q[i].op for i in range(152 * st["max_pc"])}
         assert (8 in ops and 9 in ops and 4 not in ops) == split, name
         assert (4 in ops) == (not split), name
-
-
-def test_moe_split_mlp_slices():
-    # every SM's gate/up slices: shared columns first (flagged, waiting on the
-    # O-projection), then routed columns inside one slot (waiting on the
-    # router); the down rows are relaxed-signalled tagged rows
-    cfg, d = desc("moe")
-    st, q = L.mk_plan(d, 1, cfg["max_seq"], 152)
-    Fs, Fe, K = cfg["shared_ffn"], cfg["expert_ffn"], cfg["top_k"]
-    ups = [q[i] for i in range(152 * st["max_pc"]) if q[i].op == 8 and q[i].layer == 3]
-    cols = sorted(c for I in ups for c in range(I.r0, I.r1))
-    assert cols == list(range(Fs + K * Fe))
-    F_SHARED = 4
-    for I in ups:
-        shared = I.r0 < Fs
-        assert bool(I.flags & F_SHARED) == shared and (not shared or I.r1 <= Fs)
-        if not shared:
-            assert (I.r0 - Fs) // Fe == (I.r1 - 1 - Fs) // Fe
-    waits = {bool(I.flags & F_SHARED): I.wait_ctr for I in ups}
-    assert waits[True] != waits[False]
-    assert all(q[i].flags & 32 for i in range(152 * st["max_pc"]) if q[i].op == 9)
 
 
 def test_llama1b_plan_is_byte_balanced():

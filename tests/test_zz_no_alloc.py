@@ -9,9 +9,8 @@ These tests call it through the C ABI on the same inputs as mk_decode_step,
 two calls in a row, and hold both results to the parity tests' tolerance:
 the no-allocation logits against the regular step's and against the oracle
 teacher-forced on the same tokens.  The shapes cover batch 1 (small and
-Llama-1B), a small MoE with fused MLP slices and one with the split MLP
-(its routing lives in the fixed array too) and a batch-8 shape with the
-batched MLP.  This file is collected last so that a
+Llama-1B), a small MoE (its routing lives in the fixed array too) and a
+batch-8 shape with the batched MLP.  This file is collected last so that a
 run stopping at the first failure has already run every other test.
 """
 import ctypes as C
@@ -33,11 +32,6 @@ CASES = {
     "moe_small": synth.custom(n_layers=3, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=128,
                               ffn=0, vocab=3001, tied=False, n_experts=16, top_k=4,
                               expert_ffn=200, shared_ffn=500, rope_theta=5e5, prefill=(70, 70),
-                              steps=4),
-    # the same with a shared width of whole 16-byte chunks: the MoE split MLP
-    "moe_split": synth.custom(n_layers=3, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=128,
-                              ffn=0, vocab=3001, tied=False, n_experts=16, top_k=4,
-                              expert_ffn=200, shared_ffn=512, rope_theta=5e5, prefill=(70, 70),
                               steps=4),
     # eight sequences, ragged lengths, the batched split MLP (h as fragments)
     "batch8": synth.custom(n_layers=2, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=64,
