@@ -31,11 +31,13 @@ cudaError_t pack_qkv_scales(float* dst, const float* sq, const float* sk, const 
 cudaError_t interleave_scales(float* dst, const float* a, const float* b, int n, cudaStream_t s);
 cudaError_t pack_wo_i8(void* dst, const void* wo_codes, int H, int Hq, cudaStream_t s);
 cudaError_t bias_codes(void* p, size_t bytes, cudaStream_t s);
+cudaError_t pack_kchunk(uint16_t* dst, const uint16_t* src, long R, int K, cudaStream_t s);
 
 extern const Variant variant_h256_d64_g2_b1;
 #ifndef MK_BOUNDS
 extern const Variant variant_h2048_d64_g4_b1;
 extern const Variant variant_h2048_d64_g4_b8;
+extern const Variant variant_h2048_d64_g4_b32;
 extern const Variant variant_h2048_d128_g4_b1;
 extern const Variant variant_h2048_d64_g4_b1_w8;
 #endif
@@ -55,6 +57,7 @@ struct Scratch {
   uint32_t* ctr;
   float* hglob;             // SiLU(gate)*up (split MLP)
   TagWord* xt;              // tagged block: x_{2l+2} (split MLP)
+  unsigned char* act;       // wide batch: the three normalised operands
   size_t xbuf_bytes, ctr_bytes, err_bytes, tag_bytes, total;
   size_t n_q, n_part, n_h, n_xt, n_lm;  // element counts (bounds checks)
 };
@@ -73,9 +76,15 @@ static Scratch carve_scratch(const mk_model_desc& d, size_t B, size_t kc, size_t
   const size_t sc = al256(n_ctr * 4), se = 256;
   const size_t sroute = al256(L * (size_t)(d.top_k > 0 ? d.top_k : 1) * 4);  // ids, then weights
   // h: batch-1 split [L][B][F] floats; batched split [L][F/16][32] A-fragment
-  // words of 16 bytes (8 sequences x 4 bytes per column)
+  // words of 16 bytes (8 sequences x 4 bytes per column); wide batch one
+  // operand buffer [F/64][2 Bp][64] bf16 (every layer reuses it).  The wide
+  // normalised operands: three buffers [H/64][2 Bp][64] bf16.
+  const bool wide = wide_path(d);
+  const size_t Bp = (size_t)wide_bp((int)B);
   const size_t hB = mlp_split_batched(d) ? 8 : B;
-  const size_t sxt = al256(L * B * H * 8), sh = al256(L * hB * F * 4);
+  const size_t sxt = al256(L * B * H * 8);
+  const size_t sh = wide ? al256(F * 2 * Bp * 2) : al256(L * hB * F * 4);
+  const size_t sa = wide ? al256(3 * H * 2 * Bp * 2) : 0;
   Scratch s{};
   s.xbuf_bytes = sx;
   s.ctr_bytes = sc;
@@ -86,7 +95,7 @@ static Scratch carve_scratch(const mk_model_desc& d, size_t B, size_t kc, size_t
   s.n_h = sh / 4;
   s.n_xt = sxt / 8;
   s.n_lm = sl / 4;
-  s.total = sx + sq + sp + sr + 2 * sl + sc + se + 2 * sroute + sh + sxt;
+  s.total = sx + sq + sp + sr + 2 * sl + sc + se + 2 * sroute + sh + sxt + sa;
   if (!base) return s;
   char* q = base;
   s.xbuf = (float*)q; q += sx;
@@ -100,7 +109,8 @@ static Scratch carve_scratch(const mk_model_desc& d, size_t B, size_t kc, size_t
   s.routes = (int*)q; q += sroute;
   s.rweight = (float*)q; q += sroute;
   s.hglob = (float*)q; q += sh;
-  s.xt = (TagWord*)q;
+  s.xt = (TagWord*)q; q += sxt;
+  s.act = sa ? (unsigned char*)q : nullptr;
   return s;
 }
 
@@ -175,7 +185,7 @@ static const Variant* pick_variant(const mk_model_desc& d, int wb) {
 #else
   const Variant* all[] = {&variant_h256_d64_g2_b1, &variant_h2048_d64_g4_b1,
                           &variant_h2048_d64_g4_b8, &variant_h2048_d128_g4_b1,
-                          &variant_h2048_d64_g4_b1_w8};
+                          &variant_h2048_d64_g4_b1_w8, &variant_h2048_d64_g4_b32};
 #endif
   const int HPG = d.n_q_heads / d.n_kv_heads;
   const Variant* best = nullptr;
@@ -283,6 +293,11 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
   if (wfmt == MK_WEIGHTS_INT8 && (!mlp_split(d) || d.ffn % 16 || d.head_dim != 64))
     return MK_ERR_UNSUPPORTED;
   h->wfmt = wfmt;
+  // wide batch (9 .. 32 sequences): dense FFN in whole 64-column chunks,
+  // 64-dim heads, bf16 weights
+  if (d.max_batch > 8 && (d.n_experts > 0 || d.max_batch > WIDE_NB || d.ffn % WIDE_KC ||
+                          d.hidden % WIDE_KC || d.head_dim != WIDE_KC || wfmt != MK_WEIGHTS_BF16))
+    return MK_ERR_UNSUPPORTED;
   h->var = pick_variant(d, wfmt == MK_WEIGHTS_INT8 ? 1 : 2);
   if (!h->var) return MK_ERR_UNSUPPORTED;
   const int L = d.n_layers, D = d.head_dim;
@@ -358,11 +373,32 @@ static int pack_bf16(mk_handle* h, const mk_weights* w, const mk_kv* kv, cudaStr
   const bool moe = d.n_experts > 0;
   const LayerSizes ls = layer_sizes(d);
   const size_t V = d.vocab;
+  // wide batch: every streamed matrix but Wo K-chunk-major ([K/64][R8][64],
+  // pack_kchunk) from its standard packed form, staged in `tmp`
+  const bool wide = wide_path(d);
+  const size_t V8 = (V + 7) / 8 * 8;
   size_t per_layer = 0;
   for (size_t e : {ls.norm, ls.norm, ls.qkv, ls.wo, ls.gu, ls.dT, ls.router, ls.ex_gu, ls.ex_dT,
                    ls.sh_gu, ls.sh_dT})
     per_layer += al256(e * 2);
-  const size_t total = per_layer * L + al256(V * H * 2) * (d.tied_lm_head ? 1 : 2) + al256(H * 2);
+  const size_t lm_bytes = wide ? al256(V8 * H * 2) : al256(V * H * 2);
+  const size_t total =
+      per_layer * L + al256(V * H * 2) + (d.tied_lm_head && !wide ? 0 : lm_bytes) + al256(H * 2);
+  uint16_t* tmp = nullptr;
+  if (wide) {
+    const size_t mx = std::max({ls.qkv, ls.gu, ls.dT, V * (size_t)H});
+    CK(cudaMalloc(&tmp, mx * 2));
+  }
+  struct TmpFree {
+    uint16_t* p;
+    cudaStream_t s;
+    ~TmpFree() {
+      if (p) {
+        cudaStreamSynchronize(s);
+        cudaFree(p);
+      }
+    }
+  } tmp_free{tmp, s};
   CK(cudaMalloc(&h->packed, total));
   h->packed_bytes = total;
   char* p = (char*)h->packed;
@@ -388,9 +424,20 @@ static int pack_bf16(mk_handle* h, const mk_weights* w, const mk_kv* kv, cudaStr
     uint16_t* sdT = take(ls.sh_dT);
     CK(cudaMemcpyAsync(an, w->attn_norm[l], ls.norm * 2, cudaMemcpyDeviceToDevice, s));
     CK(cudaMemcpyAsync(mn, w->mlp_norm[l], ls.norm * 2, cudaMemcpyDeviceToDevice, s));
-    CK(pack_qkv(qkv, w->wq[l], w->wk[l], w->wv[l], H, Hkv, HPG, D, s));
     CK(pack_wo(wo, w->wo[l], H, Hq, D, s));
-    if (!moe) {
+    if (wide) {
+      CK(pack_qkv(tmp, w->wq[l], w->wk[l], w->wv[l], H, Hkv, HPG, D, s));
+      CK(pack_kchunk(qkv, tmp, (long)Hkv * (HPG + 2) * D, H, s));
+      CK(pack_interleave(tmp, w->w_gate[l], w->w_up[l], d.ffn, H, s));
+      CK(pack_kchunk(gu, tmp, 2L * d.ffn, H, s));
+      CK(pack_rows(tmp, w->w_down[l], H, d.ffn, s));
+      CK(pack_kchunk(dT, tmp, H, d.ffn, s));
+    } else {
+      CK(pack_qkv(qkv, w->wq[l], w->wk[l], w->wv[l], H, Hkv, HPG, D, s));
+    }
+    if (wide) {
+      // packed above
+    } else if (!moe) {
       CK(pack_interleave(gu, w->w_gate[l], w->w_up[l], d.ffn, H, s));
       if (mlp_split(d))  // the down rows are streamed as they are
         CK(cudaMemcpyAsync(dT, w->w_down[l], ls.dT * 2, cudaMemcpyDeviceToDevice, s));
@@ -425,7 +472,12 @@ static int pack_bf16(mk_handle* h, const mk_weights* w, const mk_kv* kv, cudaStr
   uint16_t* emb = take(V * H);
   CK(pack_rows(emb, w->embed, (long)V, H, s));
   h->embed = emb;
-  if (d.tied_lm_head) {
+  if (wide) {  // its own K-chunk-major copy, tied or not
+    uint16_t* lm = take(V8 * H);
+    CK(pack_rows(tmp, d.tied_lm_head ? w->embed : w->lm_head, (long)V, H, s));
+    CK(pack_kchunk(lm, tmp, (long)V, H, s));
+    h->lm_head = lm;
+  } else if (d.tied_lm_head) {
     h->lm_head = emb;
   } else {
     uint16_t* lm = take(V * H);
@@ -603,14 +655,13 @@ extern "C" int mk_build_schedule(mk_handle* h, int batch, int max_ctx) {
   // instructions of that key alone (in queue order), one queue per SM that
   // owns any, HALT-padded -- so a launch walks only its own work
   {
-    auto key_of = [&](const Instr& I) {
-      return I.op == OP_LMHEAD ? L * N_PHASES : (size_t)I.layer * N_PHASES + phase_of(I.op);
-    };
+    // (the LM head and the final norm carry layer L)
+    auto key_of = [&](const Instr& I) { return (size_t)I.layer * N_PHASES + phase_of(I); };
     Instr halt;
     std::memset(&halt, 0, sizeof halt);
     halt.op = OP_HALT;
     std::vector<Instr> flat;
-    for (size_t k = 0; k < L * N_PHASES + 1; k++) {
+    for (size_t k = 0; k < (L + 1) * N_PHASES; k++) {
       std::vector<std::vector<Instr>> qs;
       for (int sm = 0; sm < h->n_sm; sm++) {
         std::vector<Instr> q;
@@ -662,6 +713,8 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.rlog = h->sc.rlog;
   g.xt = h->sc.xt;
   g.hglob = h->sc.hglob;
+  g.act = h->sc.act;
+  g.Bp = wide_bp(h->batch);
   g.routes = h->sc.routes;
   g.rweight = h->sc.rweight;
   g.lm_val = h->sc.lm_val;
@@ -1119,6 +1172,9 @@ extern "C" int mk_set_stage_bytes(mk_handle* h, int stage_bytes) {
   if (!h || stage_bytes < STAGE_UNIT || stage_bytes > MAX_STAGE_BYTES ||
       stage_bytes % STAGE_UNIT != 0)
     return MK_ERR_INVALID_ARG;
+  // wide batch: a stage holds a 128-row K chunk of weights (16 KB) and the
+  // operand's chunk (up to 8 KB)
+  if (h->var->NB > 8 && stage_bytes < 2 * STAGE_UNIT) return MK_ERR_UNSUPPORTED;
   const int old = h->stage_bytes;
   const int st = size_ring(h, stage_bytes);
   if (st != MK_OK) {

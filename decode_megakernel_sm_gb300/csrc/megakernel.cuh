@@ -44,6 +44,10 @@ struct Ctx {
   uint32_t epoch;   // g.epoch + step: counter targets, tags, residual parity
   unsigned long long tw0, tw1;  // trace: wait start / end (thread 0)
   unsigned long long tm[2];     // trace: after the prologue phase, after the ring loop
+  // wide batch: tensor-memory base, MMA-done mbarrier (shared address) and
+  // the parity of its next phase, the O-projection's operand tile
+  uint32_t tmem, mma_bar, mma_par;
+  unsigned char* actile;
   MK_DEV void mark(const Globals& g, int k) {
     if (g.trace && tid == 0) tm[k] = gtimer();
   }
@@ -99,7 +103,7 @@ MK_DEV float xres_sum(const Globals& g, uint32_t ep, int j, int b, int r) {
 // The weight / cache byte ranges an instruction streams, in ring order.
 // The producer issues exactly these copies; the consumers consume exactly
 // these stages.  Returns the number of segments (0..2).
-template <int HT, int D, int WB>
+template <int HT, int D, int WB, int NB>
 MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int* topk, Seg* s) {
   // WB bytes per weight: 2 (bf16) or 1 (int8 codes, dense batch-1 shapes only)
   constexpr uint32_t ROW = HT * WB;
@@ -107,6 +111,51 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
   const uint32_t RPS = SBY / ROW;
   const LayerPtrs* Lp = g.layers + (I.op == OP_LMHEAD ? 0 : I.layer);
   const uint32_t n = I.r1 - I.r0;
+  if constexpr (NB > 8) {
+    // wide batch: K chunks of the instruction's rows (K-chunk-major packed
+    // matrices, [K / 64][R8][64] with R8 = R rounded up to 8 rows) next to
+    // the operand's chunks; QKV / gate-up / LM head take every chunk of
+    // their normalised operand, a down instruction the chunks [b, g) of h
+    if (I.op == OP_QKV || I.op == OP_MLP_UP || I.op == OP_MLP_DOWN || I.op == OP_LMHEAD) {
+      const uint32_t ab = 2u * (uint32_t)g.Bp * 128u;
+      const size_t abuf = (size_t)(HT / WIDE_KC) * ab;
+      const unsigned char* w;
+      const unsigned char* a;
+      uint32_t R, r0, rows, k0 = 0, nk = HT / WIDE_KC;
+      if (I.op == OP_QKV) {
+        w = (const unsigned char*)Lp->wqkv;
+        a = g.act;
+        R = (uint32_t)(g.Hq + 2 * g.Hkv) * D;
+        r0 = I.r0;
+        rows = n;
+      } else if (I.op == OP_MLP_UP) {
+        w = (const unsigned char*)Lp->wgu;
+        a = g.act + abuf;
+        R = 2u * (uint32_t)g.F;
+        r0 = 2u * I.r0;
+        rows = 2u * n;
+      } else if (I.op == OP_MLP_DOWN) {
+        w = (const unsigned char*)Lp->wdT;
+        a = (const unsigned char*)g.hglob;
+        R = (uint32_t)g.H;
+        r0 = I.r0;
+        rows = n;
+        k0 = I.b;
+        nk = (uint32_t)I.g - I.b;
+      } else {
+        w = (const unsigned char*)g.lm_head;
+        a = g.act + 2 * abuf;
+        R = (uint32_t)g.V;
+        r0 = I.r0;
+        rows = n;
+      }
+      const uint32_t R8 = (R + 7u) / 8u * 8u, unit = (rows + 7u) / 8u * 8u * 128u;
+      s[0] = {w + ((size_t)k0 * R8 + r0) * 128u, a + (size_t)k0 * ab, unit, nk, SBY / (unit + ab),
+              SEG_WIDE, R8 * 128u, ab};
+      return 1;
+    }
+    if (I.op == OP_NORM) return 0;
+  }
   switch (I.op) {
     case OP_QKV:
       s[0] = {(const unsigned char*)Lp->wqkv + (size_t)I.r0 * ROW, nullptr, ROW, n, RPS, I.r0};
@@ -723,7 +772,7 @@ MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I)
   float xr[HT / 32];
   if constexpr (NB == 1) load_xr<HT, WB>(c.xn, c.lane, xr);
   Seg s[2];
-  get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
+  get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
   float* yrow = c.yrow;
   const int lane = c.lane;
   gemv(c, g, s[0], xr, [&](uint32_t r, int b, float y) { yrow[b * MAX_ROWS + r] = y; });
@@ -881,7 +930,7 @@ MK_DEV bool op_attn(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I
   };
   c.mark(g, 0);
   Seg s[2];
-  get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
+  get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
   constexpr uint32_t STEP = NCW * SPW;  // positions per pass of all warps' slots
   for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
     const uint32_t n = stage_units(g, s[0], u0, (uint32_t)g.stage_bytes / 2, c.pc, OP_ATTN);
@@ -1023,7 +1072,7 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& 
     // overlap them
     staged = g.part_staged != 0;
     if (staged) {
-      get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
+      get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
       if (c.tid == 0) {
         asm volatile("fence.proxy.async.global;" ::: "memory");  // written by generic stores
         const uint64_t pol = policy_evict_normal();
@@ -1128,7 +1177,7 @@ MK_DEV bool op_oproj(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& 
   c.mark(g, 0);
   consumer_bar();
   if (c.flag[2]) return false;
-  if (!staged) get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
+  if (!staged) get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
   const Seg& wseg = s[staged ? 1 : 0];  // the Wo rows
   const uint4 zero = make_uint4(0, 0, 0, 0);
   const int nr = (int)(I.r1 - I.r0);
@@ -1293,7 +1342,7 @@ MK_DEV bool op_router(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr&
   float xr[HT / 32];
   if constexpr (NB == 1) load_xr<HT, WB>(c.xn, c.lane, xr);
   Seg s[2];
-  get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
+  get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
   float* rl = g.rlog + (size_t)I.layer * g.B * g.E + I.r0;
   const int E = g.E;
   gemv(c, g, s[0], xr, [&](uint32_t r, int b, float y) { rl[(size_t)b * E + r] = y; });
@@ -1378,7 +1427,7 @@ MK_DEV bool op_mlp(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I)
   float xr[HT / 32];
   if constexpr (NB == 1) load_xr<HT, WB>(c.xn, c.lane, xr);
   Seg s[2];
-  get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
+  get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
   float* yrow = c.yrow;
   const int lane = c.lane;
   gemv(c, g, s[0], xr, [&](uint32_t r, int b, float y) { yrow[b * MAX_ROWS + r] = y; });
@@ -1471,7 +1520,7 @@ MK_DEV bool op_mlp_up(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr&
   float xr[HT / 32];
   if constexpr (NB == 1) load_xr<HT, WB>(c.xn, c.lane, xr);
   Seg s[2];
-  get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
+  get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
   float* yrow = c.yrow;
   const int lane = c.lane;
   gemv(c, g, s[0], xr, [&](uint32_t r, int b, float y) { yrow[b * MAX_ROWS + r] = y; });
@@ -1572,7 +1621,7 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Inst
     const bool live = gq < g.B;
     float* dst = xres_mine(g, c.epoch, 2 * l + 2, live ? gq : 0);
     Seg s[2];
-    get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
+    get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
     bool bad = false;
     for (uint32_t v0 = 0; v0 < s[0].n; v0 += s[0].ups) {
       const uint32_t n = stage_units(g, s[0], v0, (uint32_t)g.stage_bytes, c.pc, OP_MLP_DOWN);
@@ -1650,7 +1699,7 @@ MK_DEV bool op_mlp_down(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Inst
     float pend = 0.f;
     int prow = -1;
     Seg s[2];
-    get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
+    get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
     for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
       const uint32_t n = stage_units(g, s[0], u0, (uint32_t)g.stage_bytes, c.pc, OP_MLP_DOWN);
       if (!c.ring.acquire(g)) break;
@@ -1738,7 +1787,7 @@ MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr&
   float xr[HT / 32];
   if constexpr (NB == 1) load_xr<HT, WB>(c.xn, c.lane, xr);
   Seg s[2];
-  get_segs<HT, D, WB>(g, I, c.pos, c.topk, s);
+  get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
   // each thread only ever sees one sequence, b = tid % NB (both GEMV paths);
   // it keeps that sequence's best (value, lowest row) of this slice
   float best = -INFINITY;
@@ -1792,11 +1841,21 @@ MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr&
       g.lm_idx[(size_t)I.aux * B + b] = ix;
     }
   }
+  lm_reduce(c, g);
+  return true;
+}
+
+// The LM-head slices' last step (consumer warp 0, once its slice's (max,
+// index) per sequence is written): count this slice in; the slice that
+// arrives last reduces all slices into argmax[b] and signals the step done.
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV void lm_reduce(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g) {
+  const int lane = c.lane, B = g.B;
   uint32_t old = 0;
   if (lane == 0) old = atom_add_acq_rel(g.ctr + g.lm_ctr, 1u);
   old = __shfl_sync(0xFFFFFFFFu, old, 0);
   __syncwarp();
-  if (old != c.epoch * (uint32_t)g.n_lm - 1u) return true;
+  if (old != c.epoch * (uint32_t)g.n_lm - 1u) return;
   for (int b = 0; b < B && b < NB; b++) {
     float v = -INFINITY;
     int ix = 0x7FFFFFFF;
@@ -1823,8 +1882,13 @@ MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr&
   // launch starts the next step behind this signal
   __syncwarp();
   if (lane == 0) red_release(g.ctr + g.lm_done_ctr, 1u);
-  return true;
 }
+
+}  // namespace mk
+
+#include "megakernel_wide.cuh"
+
+namespace mk {
 
 // ------------------------------------------------------------ interpreter ----
 MK_DEV Instr load_instr(const Globals& g, int sm, int pc) {
@@ -1887,7 +1951,7 @@ struct L2Cursor {
           }
           pos[I.b] = P;
         }
-        nseg = get_segs<HT, D, WB>(g, I, pos, ptopk, s);
+        nseg = get_segs<HT, D, WB, NB>(g, I, pos, ptopk, s);
         k = 0;
         u0 = 0;
         pc++;
@@ -1900,8 +1964,9 @@ struct L2Cursor {
       }
       const uint32_t n = min(s[k].ups, s[k].n - u0);
       const uint32_t b = n * s[k].unit;
-      const unsigned long long cb = s[k].src2 ? 2ull * b : b;
-      if (bytes + cb > from && !s[k].cfill() && !(g.kv_block && s[k].src2)) {
+      const unsigned long long cb = s[k].wide() ? (unsigned long long)n * (s[k].unit + s[k].unit2)
+                                                : (s[k].src2 ? 2ull * b : b);
+      if (bytes + cb > from && !s[k].cfill() && !s[k].wide() && !(g.kv_block && s[k].src2)) {
         if ((threadIdx.x & 31) == 0) {
           bulk_prefetch_l2(s[k].src + (size_t)u0 * s[k].unit, b);
           if (s[k].src2) bulk_prefetch_l2(s[k].src2 + (size_t)u0 * s[k].unit, b);
@@ -2015,8 +2080,21 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
     }
     __syncwarp();
     Seg s[2];
-    const int nseg = get_segs<HT, D, WB>(g, I, ppos, ptopk, s);
+    const int nseg = get_segs<HT, D, WB, NB>(g, I, ppos, ptopk, s);
     const int my_seq = seq++;
+    if constexpr (NB > 8) {
+      // wide batch: the operand pieces are this step's input, written with
+      // generic stores by other SMs -- wait for the dependency, then order
+      // those stores before the bulk copies that read them
+      if (nseg > 0 && s[0].wide() && I.wait_ctr != NO_CTR) {
+        bool ok = true;
+        if (lane == 0) {
+          ok = wait_counter(g, I.wait_ctr, ep * I.wait_cnt, pc, I.op);
+          if (ok) asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) goto drain;
+      }
+    }
     // a held instruction: stages from hold_k on wait until the consumers
     // have finished (and signalled) every earlier instruction of this launch
     const uint32_t hold_k =
@@ -2071,8 +2149,10 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
 #ifdef MK_BOUNDS
         {  // the stage (or each half) must hold what the segment puts there
           const uint32_t room = s[k].src2 ? (uint32_t)g.stage_bytes / 2 : (uint32_t)g.stage_bytes;
+          const bool fits = s[k].wide() ? n * (s[k].unit + s[k].unit2) <= (uint32_t)g.stage_bytes
+                                        : n * s[k].unit <= room;
           int bad = 0;
-          if (lane == 0 && !MK_IN(g, n * s[k].unit <= room, pc, I.op)) bad = 1;
+          if (lane == 0 && !MK_IN(g, fits, pc, I.op)) bad = 1;
           if (__shfl_sync(0xFFFFFFFFu, bad, 0)) goto drain;
         }
 #endif
@@ -2082,8 +2162,24 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
           const uint32_t bytes = n * s[k].unit;
           const uint32_t full = full0 + 8u * st;
           const uint32_t dst = ring_s + (uint32_t)st * (uint32_t)g.stage_bytes;
-          mbar_expect_tx(full, s[k].src2 ? 2u * bytes : bytes);
-          if (s[k].cfill()) {
+          if (s[k].wide()) {
+            // (wide variant only) chunk j: its weight piece at j * unit, its
+            // operand piece at ups * unit + j * unit2
+            mbar_expect_tx(full, n * (s[k].unit + s[k].unit2));
+            for (uint32_t j = 0; j < n; j++) {
+              bulk_g2s(dst + j * s[k].unit,
+                       copy_src(g, I, s[k].src + (size_t)(u0 + j) * s[k].pitch, s[k].unit, pc),
+                       s[k].unit, full, pol_w);
+              bulk_g2s(dst + s[k].ups * s[k].unit + j * s[k].unit2,
+                       copy_src(g, I, s[k].src2 + (size_t)(u0 + j) * s[k].unit2, s[k].unit2, pc),
+                       s[k].unit2, full, pol_kv);
+            }
+          } else {
+            mbar_expect_tx(full, s[k].src2 ? 2u * bytes : bytes);
+          }
+          if (s[k].wide()) {
+            // issued above
+          } else if (s[k].cfill()) {
             // the consumers copy this stage in after their dependency wait
           } else if (s[k].src2 && g.kv_block && I.op == OP_ATTN) {
             // paged cache: the stage's rows, one copy per block piece (K in
@@ -2116,7 +2212,8 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
                      pol_w);
           }
         }
-        issued_bytes += (s[k].src2 ? 2ull : 1ull) * n * s[k].unit;
+        issued_bytes += s[k].wide() ? (unsigned long long)n * (s[k].unit + s[k].unit2)
+                                    : (s[k].src2 ? 2ull : 1ull) * n * s[k].unit;
         __syncwarp();
         issued++;
         if (++st == ns) {
@@ -2136,6 +2233,9 @@ drain:
     wait_mbar(g, full0 + 8u * (j % (uint32_t)ns), (j / (uint32_t)ns) & 1u, false);
   }
 }
+
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV void consumer_steps(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, int* misc);
 
 template <int HT, int D, int HPG, int NB, int WB>
 __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_constant__ Globals g) {
@@ -2158,6 +2258,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
       mbar_init(full0 + 8u * s, 1u);
       mbar_init(empty0 + 8u * s, (uint32_t)NCW);
     }
+    if constexpr (NB > 8) mbar_init(smem_u32(smem + Ls.tcw + 8), 1u);  // MMA done
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *flag = 0;
     misc[1] = 0;  // instructions the consumers have finished (read by the producer)
@@ -2193,7 +2294,45 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
   c.flag = flag;
   c.tw0 = c.tw1 = 0;
   c.tm[0] = c.tm[1] = 0;
+  c.tmem = c.mma_bar = c.mma_par = 0;
+  c.actile = nullptr;
+  if constexpr (NB > 8) {
+    // wide batch: the accumulators' tensor memory, held for the whole kernel
+    c.actile = smem + Ls.actile;
+    c.mma_bar = smem_u32(smem + Ls.tcw + 8);
+    if (warp == 0) tmem_alloc(smem_u32(smem + Ls.tcw), (uint32_t)WIDE_TMEM_COLS);
+    tc_fence_before();
+    consumer_bar();
+    tc_fence_after();
+    c.tmem = *(volatile uint32_t*)(smem + Ls.tcw);
+  }
+  consumer_steps(c, g, misc);
+  if constexpr (NB > 8) {
+    // every exit: once the MMAs issued so far have completed (a commit with
+    // none outstanding arrives at once), warp 0 frees the tensor memory
+    tc_fence_before();
+    consumer_bar();
+    if (warp == 0) {
+      if (lane == 0) {
+        tc_commit(c.mma_bar);
+        wait_mbar(g, c.mma_bar, c.mma_par, false);
+      }
+      __syncwarp();
+      tc_fence_after();
+      tmem_dealloc(c.tmem, (uint32_t)WIDE_TMEM_COLS);
+    }
+  }
+}
 
+// The consumer warps' work: every step of the launch, every instruction of
+// the CTA's queue, in order.  Returns on completion or on the first failure
+// (the error word is set by then).
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV void consumer_steps(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, int* misc) {
+  const int tid = c.tid;
+  int* flag = c.flag;
+  int* tok = c.tok;
+  int* pos = c.pos;
   int finished = 0;
   const int qid = queue_id(g);
   for (int step = 0; step < g.n_steps; step++) {
@@ -2231,19 +2370,35 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
       // race stress: thread 0 starts late; the op's dependency wait holds the rest
       if (g.stress_ns && tid == 0) stress_delay(g, qid, pc, step, 0xC0DEu);
       bool ok;
-      switch (I.op) {
-        case OP_QKV: ok = op_qkv(c, g, I); break;
-        case OP_ATTN: ok = op_attn(c, g, I); break;
-        case OP_OPROJ: ok = op_oproj(c, g, I); break;
-        case OP_ROUTER: ok = op_router(c, g, I); break;
-        case OP_MLP: ok = op_mlp(c, g, I); break;
-        case OP_MLP_UP: ok = op_mlp_up(c, g, I); break;
-        case OP_MLP_DOWN: ok = op_mlp_down(c, g, I); break;
-        case OP_LMHEAD: ok = op_lmhead(c, g, I); break;
-        default:
-          if (tid == 0) set_err(g, MK_ERR_DEVICE, pc, I.op);
-          ok = false;
-          break;
+      if constexpr (NB > 8) {
+        switch (I.op) {
+          case OP_NORM: ok = op_norm_wide(c, g, I); break;
+          case OP_QKV: ok = op_qkv_wide(c, g, I); break;
+          case OP_ATTN: ok = op_attn(c, g, I); break;
+          case OP_OPROJ: ok = op_oproj_wide(c, g, I); break;
+          case OP_MLP_UP: ok = op_mlp_up_wide(c, g, I); break;
+          case OP_MLP_DOWN: ok = op_mlp_down_wide(c, g, I); break;
+          case OP_LMHEAD: ok = op_lmhead_wide(c, g, I); break;
+          default:
+            if (tid == 0) set_err(g, MK_ERR_DEVICE, pc, I.op);
+            ok = false;
+            break;
+        }
+      } else {
+        switch (I.op) {
+          case OP_QKV: ok = op_qkv(c, g, I); break;
+          case OP_ATTN: ok = op_attn(c, g, I); break;
+          case OP_OPROJ: ok = op_oproj(c, g, I); break;
+          case OP_ROUTER: ok = op_router(c, g, I); break;
+          case OP_MLP: ok = op_mlp(c, g, I); break;
+          case OP_MLP_UP: ok = op_mlp_up(c, g, I); break;
+          case OP_MLP_DOWN: ok = op_mlp_down(c, g, I); break;
+          case OP_LMHEAD: ok = op_lmhead(c, g, I); break;
+          default:
+            if (tid == 0) set_err(g, MK_ERR_DEVICE, pc, I.op);
+            ok = false;
+            break;
+        }
       }
       if (!ok) return;
       if (tid == 0) {

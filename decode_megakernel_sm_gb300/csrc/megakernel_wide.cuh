@@ -1,0 +1,457 @@
+// megakernel_wide.cuh -- op bodies of the wide-batch variant (9 .. 32
+// sequences), included by megakernel.cuh.
+//
+// Every contraction runs on the fifth-generation tensor cores: one elected
+// thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> f32) with A = 128
+// weight rows of a ring stage and B = the activation operand, 2 Bp rows: the
+// bf16 high part of sequence b's activation in row 2b and the bf16 remainder
+// in row 2b + 1, so that the two products together keep about 16 mantissa
+// bits of the activation ("Megakernels in LLM Inference When Fusion
+// Actually Wins", sections "Core Tradeoff" and "When Megakernels Win": the
+// batch range where the contraction turns from a GEMV into a skinny GEMM).
+// The accumulator lives in tensor memory (256 columns allocated once per CTA
+// for the life of the kernel); consumer warps 0-3 read it back with
+// tcgen05.ld, one accumulator row (one weight row) per thread, and add the
+// high and low columns of each sequence.
+//
+// A stage is released to the producer by a tcgen05.commit on its empty
+// barrier (warp 0's arrival), which fires once the MMAs have read it; the
+// other consumer warps arrive as usual.  The accumulator is complete when a
+// second commit, on the CTA's MMA-done barrier, fires.
+#pragma once
+#include "mk_tc.cuh"
+
+namespace mk {
+
+// bf16 high part and remainder of x (x = hi + lo to about 16 mantissa bits).
+MK_DEV void split_hl8(const float (&x)[8], uint4& hi, uint4& lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; i++) split2(x[2 * i], x[2 * i + 1], h[i], l[i]);
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Byte offset of (operand row, column k) in an operand buffer of K chunks:
+// chunk k / 64 is a tile of 2 Bp rows x 64 columns (ab bytes).
+MK_DEV size_t opnd_off(uint32_t ab, uint32_t row, uint32_t k) {
+  return (size_t)(k / WIDE_KC) * ab + sw128_off(row, k % WIDE_KC);
+}
+
+// Wait for the MMAs committed so far on the MMA-done barrier (all consumer
+// threads; bounded).  False if the wait gave up.
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool wide_mma_wait(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g) {
+  const bool ok = wait_mbar(g, c.mma_bar, c.mma_par, true);
+  c.mma_par ^= 1u;
+  tc_fence_after();
+  return ok;
+}
+
+// Stream a wide segment through the ring into the accumulator at column 0:
+// chunk by chunk, D (+)= W_chunk (128 rows from the weight piece) x
+// operand_chunk^T.  Rows past the piece's own read the bytes that follow it
+// (the rest of the stage, or the shared memory after the ring); their
+// outputs are never read.  All consumer warps call; false (on every thread)
+// if a ring wait gave up.
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool wide_mma_stream(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Seg& s) {
+  const uint32_t N = s.unit2 / 128u;
+  const uint32_t idesc = idesc_bf16(128, (int)N);
+  bool bad = false, first = true;
+  for (uint32_t u0 = 0; u0 < s.n; u0 += s.ups) {
+    uint32_t n = min(s.ups, s.n - u0);
+    if (!MK_IN(g, n * (s.unit + s.unit2) <= (uint32_t)g.stage_bytes, c.pc, -1)) n = 0;
+    if (!bad && !c.ring.acquire(g)) bad = true;
+    if (bad) continue;
+    if (c.warp == 0) {
+      if (c.lane == 0) {
+        tc_fence_after();
+        const uint32_t sb = smem_u32(c.ring.stage_ptr());
+        for (uint32_t j = 0; j < n; j++) {
+          const uint32_t wa = sb + j * s.unit, aa = sb + s.ups * s.unit + j * s.unit2;
+#pragma unroll
+          for (uint32_t k = 0; k < 4; k++)
+            tc_mma_bf16(c.tmem, sw128_desc(wa + 32u * k), sw128_desc(aa + 32u * k), idesc,
+                        !first || k > 0);
+          first = false;
+        }
+        tc_commit(c.ring.empty_bar());  // warp 0's arrival, once the MMAs have read the stage
+      }
+      __syncwarp();
+      c.ring.advance();
+    } else {
+      c.ring.release(c.lane);
+    }
+  }
+  if (bad) c.flag[2] = 1;
+  consumer_bar();
+  if (c.flag[2]) return false;
+  if (c.tid == 0) tc_commit(c.mma_bar);
+  return wide_mma_wait(c, g);
+}
+
+// Read accumulator tile t back (rows 128 t .. 128 t + 127 of the
+// instruction, N = 2 Bp columns at column t * N) into yrow[b][m], b < Bp, m
+// < 128: consumer warp w < 4 reads lanes 32 w .. 32 w + 31 and adds each
+// sequence's high and low columns.  Ends with the tensor-memory reads ordered
+// before a CTA barrier, after which yrow is complete (and the next MMAs may
+// overwrite the accumulator).
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV void wide_tile_out(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, uint32_t N, int t) {
+  static_assert(NB <= 32, "64 accumulator columns per tile");
+  if (c.warp < 4) {
+    float* y = c.yrow + 32 * c.warp + c.lane;
+    for (uint32_t q = 0; 16u * q < N; q++) {  // 16 columns: sequences 8q .. 8q + 7
+      float v[16];
+      tmem_ld16(c.tmem + ((uint32_t)(32 * c.warp) << 16) + (uint32_t)t * N + 16u * q, v);
+#pragma unroll
+      for (int e = 0; e < 8; e++) y[(8 * q + e) * WIDE_ROWS] = v[2 * e] + v[2 * e + 1];
+    }
+  }
+  tc_fence_before();
+  consumer_bar();
+}
+
+// ------------------------------------------- OP_NORM (operand of a GEMV) ----
+// Sequences [r0, r1) of x_j -> rows 2b, 2b + 1 of operand buffer I.g (0: the
+// QKV input, x_{2l} with the attention-norm gain; 1: the MLP input, x_{2l+1}
+// with the MLP-norm gain; 2: the LM head's input, x_{2L} with the final
+// gain).  Sequences b >= B (up to Bp) get zero rows.
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool op_norm_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
+  constexpr int GROUPS = HT / 8, GPT = (GROUPS + NCT - 1) / NCT;
+  const int which = I.g, l = I.layer;
+  const int j = which == 0 ? 2 * l : which == 1 ? 2 * l + 1 : 2 * g.L;
+  const uint16_t* gain = which == 2 ? g.final_norm
+                                    : (which == 0 ? g.layers[l].attn_norm : g.layers[l].mlp_norm);
+  uint4 gw[GPT];
+#pragma unroll
+  for (int q = 0; q < GPT; q++) {
+    const int gi = c.tid + q * NCT;
+    gw[q] = gi < GROUPS ? __ldg((const uint4*)gain + gi) : make_uint4(0, 0, 0, 0);
+  }
+  if (!dep_wait(c, g, I)) return false;
+  const uint32_t ab = 2u * (uint32_t)g.Bp * 128u;
+  unsigned char* out = g.act + (size_t)which * (HT / WIDE_KC) * ab;
+  for (int b = (int)I.r0; b < (int)I.r1; b++) {
+    float v[GPT][8];
+    float ss = 0.f;
+#pragma unroll
+    for (int q = 0; q < GPT; q++) {
+      const int gi = c.tid + q * NCT;
+#pragma unroll
+      for (int e = 0; e < 8; e++) v[q][e] = 0.f;
+      if (gi >= GROUPS || b >= g.B) continue;
+      if (j == 0) {  // embedding rows are chunk-swizzled by token id
+        const int tk = c.tok[b];
+        unpack8(__ldg((const uint4*)(g.embed + (size_t)tk * HT) + (gi ^ (tk & 7))), v[q]);
+      } else {
+        for (int cp = 0; cp < g.kc; cp++) {
+          const float4* p = (const float4*)xres(g, c.epoch, j, b, cp) + 2 * gi;
+          const float4 a0 = __ldcg(p), a1 = __ldcg(p + 1);
+          v[q][0] += a0.x; v[q][1] += a0.y; v[q][2] += a0.z; v[q][3] += a0.w;
+          v[q][4] += a1.x; v[q][5] += a1.y; v[q][6] += a1.z; v[q][7] += a1.w;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 8; e++) ss = fmaf(v[q][e], v[q][e], ss);
+    }
+    ss = warp_sum(ss);
+    if (c.lane == 0) c.red[c.warp] = ss;
+    consumer_bar();
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < NCW; w++) t += c.red[w];
+    const float rs = rsqrtf(t / (float)HT + g.eps);
+#pragma unroll
+    for (int q = 0; q < GPT; q++) {
+      const int gi = c.tid + q * NCT;
+      if (gi >= GROUPS) continue;
+      float gf[8], x[8];
+      unpack8(gw[q], gf);
+#pragma unroll
+      for (int e = 0; e < 8; e++) x[e] = b < g.B ? v[q][e] * rs * gf[e] : 0.f;
+      uint4 hi, lo;
+      split_hl8(x, hi, lo);
+      *(uint4*)(out + opnd_off(ab, 2u * b, 8u * gi)) = hi;
+      *(uint4*)(out + opnd_off(ab, 2u * b + 1u, 8u * gi)) = lo;
+    }
+    consumer_bar();  // c.red is reused by the next sequence
+  }
+  return true;
+}
+
+// ------------------------------------------------- OP_QKV (wide batch) ----
+// Rows [r0, r1) (at most 128, starting on a multiple of 8) of kv head I.g's
+// packed QKV rows; then RoPE on the (t, t + D/2) pairs of q and k, q to the
+// query buffer, k and v appended to the cache at each sequence's position.
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool op_qkv_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
+  const LayerPtrs& Lp = g.layers[I.layer];
+  if (!dep_wait(c, g, I)) return false;
+  c.mark(g, 0);
+  Seg s[2];
+  get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
+  if (!wide_mma_stream(c, g, s[0])) return false;
+  c.mark(g, 1);
+  const uint32_t n = I.r1 - I.r0;
+  float* yrow = c.yrow;  // [NB][WIDE_ROWS]
+  wide_tile_out(c, g, s[0].unit2 / 128u, 0);
+  constexpr int GR = (HPG + 2) * D;
+  const int np = (int)n / 2;
+  for (int it = c.tid; it < np * g.B; it += NCT) {
+    const int b = it / np, i = 2 * (it % np);
+    float y0 = yrow[b * WIDE_ROWS + i], y1 = yrow[b * WIDE_ROWS + i + 1];
+    const int lr = (int)(I.r0 + i) - (int)I.g * GR;
+    const int hs = lr / D, t = (lr % D) >> 1;
+    const int P = c.pos[b];
+    if (hs <= HPG) {  // q heads and k: rotate (t, t + D/2) by P * theta^(-2t/D)
+      const float2 cs = ((const float2*)g.rope)[(size_t)P * (D / 2) + t];
+      const float a = y0 * cs.x - y1 * cs.y;
+      const float bb = y0 * cs.y + y1 * cs.x;
+      y0 = a;
+      y1 = bb;
+    }
+    if (hs < HPG) {
+      const size_t qo = (((size_t)I.layer * g.B + b) * g.Hq + (size_t)I.g * HPG + hs) * D;
+      if (MK_IN(g, qo + D <= g.n_q, c.pc, I.op)) {
+        float* q = g.qbuf + qo;
+        q[t] = y0;
+        q[t + D / 2] = y1;
+      }
+    } else {
+      const long long off = kv_row(g, b, I.g, P);
+      if (off < 0) {
+        set_err(g, MK_ERR_INVALID_ARG, c.pc, I.op);
+      } else if (MK_IN(g, (size_t)off + D <= g.kv_elems, c.pc, I.op)) {
+        uint16_t* row = (hs == HPG ? Lp.kc : Lp.vc) + off;
+        row[t] = to_bf16(y0);
+        row[t + D / 2] = to_bf16(y1);
+      }
+    }
+  }
+  consumer_bar();
+  return true;
+}
+
+// --------------------------------------------- OP_OPROJ (wide batch) ----
+// Head I.g's split-KV partials merged for every sequence, the merged output
+// written as the MMA's operand tile in shared memory, then rows [r0, r1)
+// (at most 512: up to four M tiles, the accumulators side by side in tensor
+// memory) of Wo[:, h*D:(h+1)*D] applied and added into x_{2l+1} with float
+// reductions; head-0 instructions also add x_{2l}.
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool op_oproj_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
+  static_assert(D == WIDE_KC, "one head is one K chunk");
+  const int h = I.g, l = I.layer, S = g.splits;
+  constexpr int PS = part_stride(D);
+  if (!dep_wait(c, g, I)) return false;
+  for (int it = c.tid; it < NB * D; it += NCT) {
+    const int dim = it % D, b = it / D;
+    float M = NEG_BIG, Ls = 0.f, O = 0.f;
+    if (b < g.B && MK_IN(g, (((size_t)l * g.B + b) * g.Hq + h + 1) * S * PS <= g.n_part, c.pc,
+                         I.op)) {
+      const float* base = g.part + (((size_t)l * g.B + b) * g.Hq + h) * S * PS;
+      for (int s2 = 0; s2 < S; s2++) {
+        const float* p = base + (size_t)s2 * PS;
+        const float ms = __ldcg(p + D), ls = __ldcg(p + D + 1), os = __ldcg(p + dim);
+        const float mn = fmaxf(M, ms);
+        const float fa = exp2f(M - mn), fb = exp2f(ms - mn);
+        Ls = Ls * fa + ls * fb;
+        O = O * fa + os * fb;
+        M = mn;
+      }
+    }
+    c.attn[b * D + dim] = b < g.B ? O / Ls : 0.f;
+  }
+  consumer_bar();
+  // the operand tile: rows 2b (high) and 2b + 1 (remainder) of the head's
+  // output, 64 columns, swizzled
+  for (int it = c.tid; it < g.Bp * (D / 8); it += NCT) {
+    const int b = it / (D / 8), j = it % (D / 8);
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; e++) x[e] = c.attn[b * D + 8 * j + e];
+    uint4 hi, lo;
+    split_hl8(x, hi, lo);
+    *(uint4*)(c.actile + sw128_off(2u * b, 8u * j)) = hi;
+    *(uint4*)(c.actile + sw128_off(2u * b + 1u, 8u * j)) = lo;
+  }
+  fence_async_smem();
+  consumer_bar();
+  c.mark(g, 0);
+  Seg s[2];
+  get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
+  const Seg& ws = s[0];  // Wo rows, 128 bytes each; a stage holds whole 128-row tiles
+  const uint32_t N = 2u * (uint32_t)g.Bp;
+  const uint32_t idesc = idesc_bf16(128, (int)N);
+  const uint32_t at = smem_u32(c.actile);
+  bool bad = false;
+  for (uint32_t u0 = 0; u0 < ws.n; u0 += ws.ups) {
+    const uint32_t n = stage_units(g, ws, u0, (uint32_t)g.stage_bytes, c.pc, OP_OPROJ);
+    if (!bad && !c.ring.acquire(g)) bad = true;
+    if (bad) continue;
+    if (c.warp == 0) {
+      if (c.lane == 0) {
+        tc_fence_after();
+        const uint32_t sb = smem_u32(c.ring.stage_ptr());
+        for (uint32_t t = 0; t * 128u < n; t++) {
+          const uint32_t col = ((u0 + 128u * t) / 128u) * N;
+#pragma unroll
+          for (uint32_t k = 0; k < 4; k++)
+            tc_mma_bf16(c.tmem + col, sw128_desc(sb + t * 16384u + 32u * k),
+                        sw128_desc(at + 32u * k), idesc, k > 0);
+        }
+        tc_commit(c.ring.empty_bar());
+      }
+      __syncwarp();
+      c.ring.advance();
+    } else {
+      c.ring.release(c.lane);
+    }
+  }
+  if (bad) c.flag[2] = 1;
+  consumer_bar();
+  if (c.flag[2]) return false;
+  if (c.tid == 0) tc_commit(c.mma_bar);
+  if (!wide_mma_wait(c, g)) return false;
+  c.mark(g, 1);
+  const int nr = (int)(I.r1 - I.r0);
+  const bool resid = (I.flags & F_RESIDUAL) != 0;
+  for (int t = 0; t * 128 < nr; t++) {
+    wide_tile_out(c, g, N, t);
+    const int mt = min(128, nr - 128 * t);
+    for (int it = c.tid; it < g.B * mt; it += NCT) {
+      const int b = it / mt, m = it % mt;
+      const int row = (int)I.r0 + 128 * t + m;
+      float y = c.yrow[b * WIDE_ROWS + m];
+      if (resid) y += x_in(g, c.epoch, 2 * l, c.tok, b, row);
+      float* dst = xres_mine(g, c.epoch, 2 * l + 1, b);
+      if (MK_IN(g, (size_t)(dst - g.xbuf) + row < g.n_xbuf, c.pc, I.op)) red_add_f32(dst + row, y);
+    }
+    consumer_bar();  // yrow is reused by the next tile
+  }
+  return true;
+}
+
+// ---------------------------------------------- OP_MLP_UP (wide batch) ----
+// FFN columns [r0, r1) (at most 64, starting on a multiple of 4): gate and up
+// rows 2c, 2c + 1, then h = SiLU(gate) * up written into h's operand buffer
+// (rows 2b, 2b + 1 of the column's chunk).
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool op_mlp_up_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
+  if (!dep_wait(c, g, I)) return false;
+  c.mark(g, 0);
+  Seg s[2];
+  get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
+  if (!wide_mma_stream(c, g, s[0])) return false;
+  c.mark(g, 1);
+  const int ncol = (int)(I.r1 - I.r0);
+  float* yrow = c.yrow;  // [NB][WIDE_ROWS]
+  wide_tile_out(c, g, s[0].unit2 / 128u, 0);
+  const uint32_t ab = 2u * (uint32_t)g.Bp * 128u;
+  unsigned char* hb = (unsigned char*)g.hglob;
+  for (int it = c.tid; it < ncol * g.Bp; it += NCT) {
+    const int b = it / ncol, j = it % ncol;
+    float h = 0.f;
+    if (b < g.B) {
+      const float gt = yrow[b * WIDE_ROWS + 2 * j], up = yrow[b * WIDE_ROWS + 2 * j + 1];
+      h = (gt / (1.f + expf(-gt))) * up;
+    }
+    const uint16_t hi = to_bf16(h), lo = to_bf16(h - bf1(hi));
+    const uint32_t col = I.r0 + (uint32_t)j;
+    *(uint16_t*)(hb + opnd_off(ab, 2u * b, col)) = hi;
+    *(uint16_t*)(hb + opnd_off(ab, 2u * b + 1u, col)) = lo;
+  }
+  consumer_bar();
+  return true;
+}
+
+// -------------------------------------------- OP_MLP_DOWN (wide batch) ----
+// Rows [r0, r1) (at most 128, starting on a multiple of 8) of x_{2l+2} over
+// the FFN chunks [b, g) of h, added with float reductions; the instructions
+// of chunk 0 also add the residual x_{2l+1}.
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool op_mlp_down_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
+  const int l = I.layer;
+  if (!dep_wait(c, g, I)) return false;
+  c.mark(g, 0);
+  Seg s[2];
+  get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
+  if (!wide_mma_stream(c, g, s[0])) return false;
+  c.mark(g, 1);
+  wide_tile_out(c, g, s[0].unit2 / 128u, 0);
+  const int n = (int)(I.r1 - I.r0);
+  for (int it = c.tid; it < g.B * n; it += NCT) {
+    const int b = it / n, m = it % n;
+    const int row = (int)I.r0 + m;
+    float y = c.yrow[b * WIDE_ROWS + m];
+    if (I.b == 0) y += xres_sum(g, c.epoch, 2 * l + 1, b, row);
+    float* dst = xres_mine(g, c.epoch, 2 * l + 2, b);
+    if (MK_IN(g, (size_t)(dst - g.xbuf) + row < g.n_xbuf, c.pc, I.op)) red_add_f32(dst + row, y);
+  }
+  consumer_bar();
+  return true;
+}
+
+// ----------------------------------------------- OP_LMHEAD (wide batch) ----
+// Rows [r0, r1) (at most 128) of the LM head over the final operand: the
+// logits, this slice's first maximum per sequence, and the last-arriver
+// argmax over all slices (lm_reduce).
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool op_lmhead_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
+  if (g.zero_next) {  // as in op_lmhead: this slice's share of the next step's residual buffers
+    const size_t total = (size_t)2 * g.L * g.kc * g.B * g.H;
+    const size_t a = total * I.aux / (size_t)g.n_lm, e = total * (I.aux + 1) / (size_t)g.n_lm;
+    float* nx = g.xbuf + (size_t)((c.epoch + 1u) & 1u) * total;
+    if (MK_IN(g, 2 * total <= g.n_xbuf, c.pc, I.op))
+      for (size_t i = a + c.tid; i < e; i += NCT) nx[i] = 0.f;
+  }
+  if (!dep_wait(c, g, I)) return false;
+  c.mark(g, 0);
+  Seg s[2];
+  get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
+  if (!wide_mma_stream(c, g, s[0])) return false;
+  c.mark(g, 1);
+  const int n = (int)(I.r1 - I.r0), B = g.B, V = g.V;
+  float* yrow = c.yrow;  // [NB][WIDE_ROWS]
+  wide_tile_out(c, g, s[0].unit2 / 128u, 0);
+  for (int it = c.tid; it < B * n; it += NCT) {
+    const int b = it / n, m = it % n;
+    const int row = (int)I.r0 + m;
+    if (MK_IN(g, row < V, c.pc, I.op)) g.logits[(size_t)b * V + row] = yrow[b * WIDE_ROWS + m];
+  }
+  // this slice's (max, lowest row) per sequence: warp w takes sequences
+  // w, w + NCW, ...
+  for (int b = c.warp; b < B; b += NCW) {
+    float best = -INFINITY;
+    int bidx = 0x7FFFFFFF;
+    for (int m = c.lane; m < n; m += 32) {
+      const float y = yrow[b * WIDE_ROWS + m];
+      if (y > best) {  // rows ascend along a lane: the first maximum wins
+        best = y;
+        bidx = (int)I.r0 + m;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bidx, o);
+      if (ov > best || (ov == best && oi < bidx)) {
+        best = ov;
+        bidx = oi;
+      }
+    }
+    if (c.lane == 0 && MK_IN(g, ((size_t)I.aux + 1) * B <= g.n_lmv, c.pc, I.op)) {
+      g.lm_val[(size_t)I.aux * B + b] = best;
+      g.lm_idx[(size_t)I.aux * B + b] = bidx;
+    }
+  }
+  consumer_bar();
+  if (c.warp != 0) return true;
+  lm_reduce(c, g);
+  return true;
+}
+
+}  // namespace mk

@@ -464,6 +464,13 @@ MK_DEV bool wait_mbar(const Globals& g, uint32_t bar, uint32_t parity, bool abor
 // with the matching V rows in src2) streamed through the ring, `ups` units
 // per stage.  src2 lands in the upper half of the stage.
 constexpr uint32_t SEG_CFILL = 0x80000000u;
+// A wide-batch segment: unit i (a K chunk) is a weight piece of `unit` bytes
+// at src + i * pitch and an operand piece of `unit2` bytes at src2 + i * unit2;
+// a stage holds `ups` chunks, the weight pieces first (unit apart), then the
+// operand pieces (unit2 apart, from offset ups * unit).  The operand is an
+// input of this step: the producer waits for the instruction's dependency
+// before it issues any of the segment's copies.
+constexpr uint32_t SEG_WIDE = 0x40000000u;
 
 struct Seg {
   const unsigned char* src;
@@ -474,7 +481,9 @@ struct Seg {
   uint32_t row0;  // swizzled GEMV matrices: index of the first row in its tensor (key = row & 7);
                   // SEG_CFILL set: an input of this step, whose stages the producer only arms
                   // and the consumers fill once their dependency wait has passed
+  uint32_t pitch = 0, unit2 = 0;  // SEG_WIDE segments only
   MK_DEV bool cfill() const { return (row0 & SEG_CFILL) != 0; }
+  MK_DEV bool wide() const { return (row0 & SEG_WIDE) != 0; }
 };
 
 // Ring cursor of one consumer warp.
@@ -508,11 +517,17 @@ struct Ring {
   MK_DEV void release(int lane) {
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8u * st);
+    advance();
+  }
+  // The cursor moves on without arriving: the warp's arrival comes from
+  // elsewhere (a tensor-core commit, once its MMAs have read the stage).
+  MK_DEV void advance() {
     if (++st == ns) {
       st = 0;
       par ^= 1u;
     }
   }
+  MK_DEV uint32_t empty_bar() const { return empty0 + 8u * st; }
 };
 
 }  // namespace mk

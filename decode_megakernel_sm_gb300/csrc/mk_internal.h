@@ -31,13 +31,17 @@ enum Op : uint8_t {
   OP_NOP = 7,     // does nothing (fault-injection stand-in)
   OP_MLP_UP = 8,  // RMSNorm + gate/up rows + SiLU*mul of an FFN column slice -> h (split MLP)
   OP_MLP_DOWN = 9,  // down-projection rows over the whole h + residual (split MLP)
+  OP_NORM = 10,     // wide batch: RMSNorm of a range of sequences -> tensor-core operand
 };
 
 // Ablation phases: one launch per (layer, phase), each over queues that hold
 // only that phase's instructions.  No instruction waits on a counter
-// signalled by an instruction of its own phase.
+// signalled by an instruction of its own phase.  (The wide-batch norms run
+// before QKV and before the MLP; the final norm and the LM head are keyed
+// to layer L.)
 enum Phase : int {
-  PH_QKV = 0, PH_ATTN = 1, PH_OPROJ = 2, PH_ROUTER = 3, PH_MLP = 4, PH_DOWN = 5, N_PHASES = 6
+  PH_NORM_A = 0, PH_QKV = 1, PH_ATTN = 2, PH_OPROJ = 3, PH_ROUTER = 4, PH_NORM_M = 5,
+  PH_MLP = 6, PH_DOWN = 7, N_PHASES = 8
 };
 
 enum Flag : uint8_t {
@@ -72,22 +76,24 @@ constexpr uint32_t NO_CTR = 0xFFFFFFFFu;
 using Instr = mk_instr;  // 32-byte record, layout fixed by mk.h
 static_assert(sizeof(Instr) == 32, "instruction record must be 32 bytes");
 
-MK_HD inline int phase_of(uint8_t op) {
-  switch (op) {
+MK_HD inline int phase_of(const Instr& I) {
+  switch (I.op) {
     case OP_QKV: return PH_QKV;
     case OP_ATTN: return PH_ATTN;
     case OP_OPROJ: return PH_OPROJ;
     case OP_ROUTER: return PH_ROUTER;
     case OP_MLP_DOWN: return PH_DOWN;
+    case OP_NORM: return I.g == 1 ? PH_NORM_M : PH_NORM_A;
     default: return PH_MLP;
   }
 }
 
 // Counter ids: per layer l, base l*stride:
-//   qkv[g] (g < Hkv), attn[g], oproj, mlp, router, mlp_up; then one argmax counter.
+//   qkv[g] (g < Hkv), attn[g], oproj, mlp, router, mlp_up, router arrivals,
+//   norm_a, norm_m; then the argmax counter, the step counter and norm_f.
 struct CtrMap {
   int Hkv, L;
-  MK_HD int stride() const { return 2 * Hkv + 5; }
+  MK_HD int stride() const { return 2 * Hkv + 7; }
   MK_HD uint32_t qkv(int l, int g) const { return (uint32_t)(l * stride() + g); }
   MK_HD uint32_t attn(int l, int g) const { return (uint32_t)(l * stride() + Hkv + g); }
   MK_HD uint32_t oproj(int l) const { return (uint32_t)(l * stride() + 2 * Hkv); }
@@ -101,7 +107,12 @@ struct CtrMap {
   // one signal per step, by the LM head's last arriver once the step's
   // argmax is written: a multi-step launch starts step t + 1 behind it
   MK_HD uint32_t lm_done() const { return (uint32_t)(L * stride() + 1); }
-  MK_HD int count() const { return L * stride() + 2; }
+  // wide batch: the normalised operand of QKV / of the MLP of layer l, and of
+  // the LM head, is complete
+  MK_HD uint32_t norm_a(int l) const { return (uint32_t)(l * stride() + 2 * Hkv + 5); }
+  MK_HD uint32_t norm_m(int l) const { return (uint32_t)(l * stride() + 2 * Hkv + 6); }
+  MK_HD uint32_t norm_f() const { return (uint32_t)(L * stride() + 2); }
+  MK_HD int count() const { return L * stride() + 3; }
 };
 
 // Kernel-shape constants.
@@ -158,6 +169,27 @@ MK_HD inline bool mlp_split_batched(const mk_model_desc& d) {
 inline bool mlp_split(const mk_model_desc& d) {
   return d.n_experts == 0 && d.max_batch == 1 && d.ffn % 8 == 0 && d.ffn * 2 <= DOWN_ROW_MAX;
 }
+
+// Wide batch (9 .. WIDE_NB sequences, dense FFN, 64-dim heads).  Every
+// contraction runs on the fifth-generation tensor cores: tcgen05.mma with
+// M = 128 weight rows (A, from the ring) and N = 2 * Bp activation rows (B:
+// the bf16 high and low parts of each sequence's activation, rows 2b and
+// 2b + 1, Bp = the batch rounded up to 8), the f32 accumulator in tensor
+// memory.  Both operands are K-major tiles of 64 columns in the 128-byte
+// swizzle.  The normalised activations are written once per step and norm
+// point by OP_NORM instructions, into operand buffers in that layout; the
+// QKV, gate/up, down and LM-head instructions stream them through the ring
+// K chunk by K chunk next to their weights.  The O-projection builds its
+// operand (one head's attention output) in shared memory.
+constexpr int WIDE_NB = 32;          // batch capacity of the wide variant
+constexpr int WIDE_KC = 64;          // columns of one K chunk (a 128-byte row of bf16)
+constexpr int WIDE_ROWS = 128;       // weight rows of one streamed instruction (the MMA's M)
+constexpr int WIDE_OROWS = 512;      // rows of one O-projection instruction (four M tiles)
+constexpr int WIDE_TMEM_COLS = 256;  // tensor-memory columns a CTA allocates
+MK_HD inline bool wide_path(const mk_model_desc& d) {
+  return d.n_experts == 0 && d.max_batch > 8;
+}
+MK_HD inline int wide_bp(int B) { return (B + 7) / 8 * 8; }
 
 // Device pointers of one layer inside the packed weight buffer.
 struct LayerPtrs {
@@ -259,11 +291,16 @@ struct Globals {
   size_t pk_bytes;
   size_t kv_elems;              // bf16 elements of one layer's K (or V) cache or pool
   size_t n_xbuf, n_q, n_part, n_h, n_xt, n_lmv;  // n_lmv: lm_val / lm_idx elements
+  // wide batch: the three normalised operands (attention input, MLP input,
+  // final), each [H / 64][2 Bp][64] bf16 in the swizzled K-major layout; h
+  // (in hglob) is [F / 64][2 Bp][64] likewise
+  unsigned char* act;
+  int Bp;                  // batch rounded up to 8 (the operand holds 2 Bp rows)
 };
 
 // Shared-memory layout (bytes from the dynamic shared memory base).
 struct SmemLayout {
-  int ring, full, empty, xn, yrow, hbuf, attn, red, misc, mpart, sc, total;
+  int ring, full, empty, xn, yrow, hbuf, attn, red, misc, mpart, sc, actile, tcw, total;
 };
 
 // WB: bytes per weight (2 bf16, 1 int8; int8 adds the row-scale region sc)
@@ -275,6 +312,30 @@ MK_HD inline SmemLayout smem_layout(int n_stages, int stage_bytes, int NB, int H
   s.full = o;   o += 8 * n_stages;
   s.empty = o;  o += 8 * n_stages;
   o = (o + 15) / 16 * 16;
+  if (NB > 8) {
+    // wide batch: no normalised vector in shared memory (it is an operand
+    // buffer in global memory); the M = 128 MMAs read up to 16 KB from the
+    // start of a weight piece, so at least that much shared memory follows
+    // the ring (yrow comes first)
+    s.xn = o;
+    s.yrow = o;
+    const int yb = 4 * NB * WIDE_ROWS, pb = 4 * 3 * NB * D, ab = 4 * NCW * HPG * (D + 2);
+    int m = yb > pb ? yb : pb;
+    m = m > ab ? m : ab;
+    m = m > 16384 ? m : 16384;
+    o += (m + 15) / 16 * 16;
+    s.hbuf = o;
+    s.attn = o;   o += 4 * NB * D;
+    s.red = o;    o += 4 * 2 * NCW * NB + 16;
+    s.misc = o;   o += 4 * (8 + 3 * NB + 4 * NB);
+    o = (o + 1023) / 1024 * 1024;
+    s.actile = o; o += 2 * NB * 128;  // the O-projection's operand: 2 NB rows x 64 bf16
+    s.tcw = o;    o += 16;            // tensor-memory base address, MMA-done mbarrier
+    s.mpart = o;
+    s.sc = o;
+    s.total = (o + 127) / 128 * 128;
+    return s;
+  }
   s.xn = o;     o += 4 * NB * H;
   s.yrow = o;
   int yb = 4 * NB * MAX_ROWS;
@@ -287,6 +348,7 @@ MK_HD inline SmemLayout smem_layout(int n_stages, int stage_bytes, int NB, int H
   o = (o + 15) / 16 * 16;
   s.mpart = o;  o += NB > 1 ? 4 * NCW * MMA_FLUSH * NB : 0;  // batched GEMV partial sums
   s.sc = o;     o += WB == 1 ? 4 * H : 0;  // row scales of one O-proj / LM-head instruction
+  s.actile = s.tcw = o;
   s.total = (o + 127) / 128 * 128;
   return s;
 }

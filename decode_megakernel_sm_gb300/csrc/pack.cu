@@ -272,4 +272,30 @@ cudaError_t bias_codes(void* p, size_t bytes, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Wide batch: the K-chunk-major re-layout of a chunk-swizzled row-major
+// matrix [R][K] (16-byte chunk i of row p at slot i ^ (p & 7), as the
+// packers above write it): dst[kc][p] = the 128 bytes of columns
+// [64 kc, 64 kc + 64) of row p, for kc < K / 64 and p < R8 (R rounded up to
+// 8 rows; rows past R are zero).  A row's swizzle only permutes the low three
+// bits of the chunk index, so inside each 128-byte piece chunk j of row p
+// already sits at slot j ^ (p & 7): the tensor cores' 128-byte swizzle of a
+// K-major operand tile whose 8-row atoms start at rows that are multiples of 8.
+__global__ void pack_kchunk_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, long R,
+                                   long R8, int nk) {
+  const size_t total = (size_t)nk * R8 * 8;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t e = i % 8, pr = i / 8;
+    const size_t p = pr % R8, kc = pr / R8;
+    dst[i] = p < (size_t)R ? src[(p * nk + kc) * 8 + e] : make_uint4(0, 0, 0, 0);
+  }
+}
+
+cudaError_t pack_kchunk(uint16_t* dst, const uint16_t* src, long R, int K, cudaStream_t s) {
+  if (R <= 0 || K <= 0 || K % 64) return cudaErrorInvalidValue;
+  pack_kchunk_kernel<<<4096, 256, 0, s>>>((uint4*)dst, (const uint4*)src, R, (R + 7) / 8 * 8,
+                                          K / 64);
+  return cudaGetLastError();
+}
+
 }  // namespace mk

@@ -42,6 +42,330 @@ int plan_shape_ok(const mk_model_desc& d) {
   return MK_OK;
 }
 
+// The common end of a plan: hold marks, counter targets, the flattened
+// HALT-padded queues and their statistics (all but weight_bytes).
+static void finish_plan(std::vector<std::vector<Instr>>& qs, const std::vector<double>& bytes,
+                        const CtrMap& cm, unsigned hold_mask, int S, int n_lm, PlanOut& out) {
+  const int n_sm = (int)qs.size();
+  Instr halt;
+  std::memset(&halt, 0, sizeof halt);
+  halt.op = OP_HALT;
+  halt.wait_ctr = NO_CTR;
+  halt.sig_ctr = NO_CTR;
+  // ---- hold marks: the first instruction of each run of a held op on an SM
+  auto hold_bit = [](uint8_t op) -> unsigned {
+    switch (op) {
+      case OP_QKV: return HOLD_QKV;
+      case OP_ATTN: return HOLD_ATTN;
+      case OP_OPROJ: return HOLD_OPROJ;
+      case OP_MLP: case OP_MLP_UP: case OP_ROUTER: return HOLD_MLP;
+      case OP_MLP_DOWN: return HOLD_DOWN;
+      case OP_LMHEAD: return HOLD_LM;
+      default: return 0;
+    }
+  };
+  for (auto& q : qs)
+    for (size_t k = 1; k < q.size(); k++)
+      if ((hold_mask & hold_bit(q[k].op)) &&
+          (q[k - 1].op != q[k].op || q[k - 1].layer != q[k].layer))
+        q[k].flags |= F_HOLD;
+
+  // ---- counter targets: a wait is for every signal of its counter
+  const int n_ctr = cm.count();
+  std::vector<uint32_t> cnt(n_ctr, 0);
+  for (auto& q : qs)
+    for (auto& I : q)
+      if (I.sig_ctr != NO_CTR) cnt[I.sig_ctr]++;
+  for (auto& q : qs)
+    for (auto& I : q) {
+      if (I.wait_ctr != NO_CTR) I.wait_cnt = cnt[I.wait_ctr];
+    }
+
+  // ---- flatten, HALT-padded
+  size_t mx = 0, total = 0;
+  for (auto& q : qs) {
+    mx = std::max(mx, q.size());
+    total += q.size();
+  }
+  out.max_pc = (int)mx + 1;
+  out.q.assign((size_t)n_sm * out.max_pc, halt);
+  for (int i = 0; i < n_sm; i++)
+    std::copy(qs[i].begin(), qs[i].end(), out.q.begin() + (size_t)i * out.max_pc);
+  out.n_ctr = n_ctr;
+  out.splits = S;
+  out.n_lm = n_lm;
+  out.n_instr = (int)total;
+  double sum = 0, m = 0;
+  for (double v : bytes) {
+    sum += v;
+    m = std::max(m, v);
+  }
+  out.max_sm_bytes = m;
+  out.mean_sm_bytes = sum / n_sm;
+}
+
+// ---------------------------------------------------------- wide batch ----
+// 9 .. 32 sequences ("Megakernels in LLM Inference When Fusion Actually
+// Wins", sections "Core Tradeoff" and "When Megakernels Win": the batch range
+// where one fused launch meets skinny GEMMs).  Per layer:
+//   NORM (attention input) -> QKV rows -> attention items -> O-proj rows ->
+//   NORM (MLP input) -> gate/up columns -> down (row block, FFN chunks),
+// then the final NORM and the LM head rows.  The norms are one instruction
+// per sequence (padded to Bp = B rounded up to 8), spread over the SMs; every
+// GEMV instruction holds at most 128 weight rows (the MMA's M; O-projection:
+// up to 512, four tiles) starting on a multiple of 8 (the operand atoms).
+static int plan_build_wide(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& out,
+                           unsigned hold_mask) {
+  const int L = d.n_layers, H = d.hidden, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
+  const int D = d.head_dim, HPG = Hq / Hkv, V = d.vocab;
+  const long F = d.ffn;
+  if (d.n_experts > 0 || B > WIDE_NB || D != WIDE_KC || H % WIDE_KC || F % WIDE_KC)
+    return MK_ERR_UNSUPPORTED;
+  const int GR = (HPG + 2) * D;
+  const long R = (long)Hkv * GR;
+  const int Bp = wide_bp(B);
+  CtrMap cm{Hkv, L};
+  int S = std::max(1, n_sm / (B * Hkv));
+  S = std::min(S, std::max(1, max_ctx / 16));
+  S = std::min(S, STAGE_UNIT / (B * part_stride(D) * 4));
+  if (S < 1) return MK_ERR_UNSUPPORTED;
+  const int n_items = B * Hkv * S;
+  std::vector<std::vector<Instr>> qs(n_sm);
+  std::vector<double> bytes(n_sm, 0.0);
+  auto mk = [](uint8_t op, int layer) {
+    Instr I;
+    std::memset(&I, 0, sizeof I);
+    I.op = op;
+    I.layer = (uint16_t)layer;
+    I.wait_ctr = NO_CTR;
+    I.sig_ctr = NO_CTR;
+    return I;
+  };
+  const double ab = 2.0 * Bp * 128;  // operand bytes of one K chunk
+  auto norms = [&](int layer, int which, uint32_t wait, uint32_t sig) {
+    for (int b = 0; b < Bp; b++) {
+      Instr I = mk(OP_NORM, layer);
+      I.g = (uint16_t)which;
+      I.r0 = (uint32_t)b;
+      I.r1 = (uint32_t)b + 1;
+      I.wait_ctr = wait;
+      I.sig_ctr = sig;
+      qs[(size_t)((long)b * n_sm / Bp)].push_back(I);
+    }
+  };
+  int n_lm = 0;
+  for (int l = 0; l < L; l++) {
+    norms(l, 0, l > 0 ? cm.mlp(l - 1) : NO_CTR, cm.norm_a(l));
+    // ---- QKV rows: per kv head group, cut at multiples of 8 rows
+    for (int i = 0; i < n_sm; i++) {
+      long a, b;
+      if (n_sm >= Hkv) {
+        const int g = (int)((long)i * Hkv / n_sm);
+        const long s0 = ((long)g * n_sm + Hkv - 1) / Hkv;
+        const long s1 = ((long)(g + 1) * n_sm + Hkv - 1) / Hkv;
+        const int m = (int)(s1 - s0), k = (int)(i - s0);
+        a = (long)g * GR + cut(GR, m, k, 8);
+        b = (long)g * GR + (k == m - 1 ? GR : cut(GR, m, k + 1, 8));
+      } else {
+        a = cut(R, n_sm, i, 8);
+        b = (i == n_sm - 1) ? R : cut(R, n_sm, i + 1, 8);
+      }
+      while (a < b) {
+        const long g = a / GR;
+        const long e = std::min(std::min(b, (g + 1) * GR), a + (long)WIDE_ROWS);
+        Instr I = mk(OP_QKV, l);
+        I.g = (uint16_t)g;
+        I.r0 = (uint32_t)a;
+        I.r1 = (uint32_t)e;
+        I.wait_ctr = cm.norm_a(l);
+        I.sig_ctr = cm.qkv(l, (int)g);
+        qs[i].push_back(I);
+        bytes[i] += (double)(e - a) * H * 2 + (double)(H / WIDE_KC) * ab;
+        a = e;
+      }
+    }
+    // ---- attention items (as in plan_build)
+    for (int k = 0; k < n_items; k++) {
+      const int sm = (int)((long)k * n_sm / n_items);
+      Instr I = mk(OP_ATTN, l);
+      I.b = (uint16_t)(k / (Hkv * S));
+      I.g = (uint16_t)((k / S) % Hkv);
+      I.r0 = (uint32_t)(k % S);
+      I.r1 = (uint32_t)S;
+      I.wait_ctr = cm.qkv(l, I.g);
+      I.sig_ctr = cm.attn(l, I.g);
+      qs[sm].push_back(I);
+      bytes[sm] += (double)max_ctx / S * D * 4;
+    }
+    // ---- O-projection rows (multiples of 8, at most WIDE_OROWS each)
+    const long OR = (long)Hq * H;
+    for (int i = 0; i < n_sm; i++) {
+      long a, b;
+      if (n_sm >= Hq) {
+        const int h = (int)((long)i * Hq / n_sm);
+        const long s0 = ((long)h * n_sm + Hq - 1) / Hq;
+        const long s1 = ((long)(h + 1) * n_sm + Hq - 1) / Hq;
+        const int m = (int)(s1 - s0), k = (int)(i - s0);
+        a = (long)h * H + cut(H, m, k, 8);
+        b = (long)h * H + (k == m - 1 ? H : cut(H, m, k + 1, 8));
+      } else {
+        a = cut(OR, n_sm, i, 8);
+        b = (i == n_sm - 1) ? OR : cut(OR, n_sm, i + 1, 8);
+      }
+      while (a < b) {
+        const long h = a / H;
+        const long e = std::min(std::min(b, (h + 1) * H), a + (long)WIDE_OROWS);
+        Instr I = mk(OP_OPROJ, l);
+        I.g = (uint16_t)h;
+        I.r0 = (uint32_t)(a - h * H);
+        I.r1 = (uint32_t)(e - h * H);
+        I.flags = h == 0 ? F_RESIDUAL : 0;
+        I.wait_ctr = cm.attn(l, (int)(h / HPG));
+        I.sig_ctr = cm.oproj(l);
+        qs[i].push_back(I);
+        bytes[i] += (double)(e - a) * D * 2;
+        a = e;
+      }
+    }
+    norms(l, 1, cm.oproj(l), cm.norm_m(l));
+    // ---- gate/up columns: multiples of 4 (8 interleaved rows), at most 64
+    for (int i = 0; i < n_sm; i++) {
+      long a = cut(F / 4, n_sm, i, 1) * 4;
+      const long b = (i == n_sm - 1) ? F : cut(F / 4, n_sm, i + 1, 1) * 4;
+      while (a < b) {
+        const long e = std::min(b, a + (long)WIDE_ROWS / 2);
+        Instr I = mk(OP_MLP_UP, l);
+        I.r0 = (uint32_t)a;
+        I.r1 = (uint32_t)e;
+        I.wait_ctr = cm.norm_m(l);
+        I.sig_ctr = cm.mlp_up(l);
+        qs[i].push_back(I);
+        bytes[i] += (double)(e - a) * 2 * H * 2 + (double)(H / WIDE_KC) * ab;
+        a = e;
+      }
+    }
+    // ---- down: cells (row block of 128 rows, 64-column FFN chunk), row-block
+    // major; each SM takes a contiguous run, one instruction per row block
+    const long nrb = (H + WIDE_ROWS - 1) / WIDE_ROWS, nch = F / WIDE_KC, ncell = nrb * nch;
+    for (int i = 0; i < n_sm; i++) {
+      long a = cut(ncell, n_sm, i, 1);
+      const long b = (i == n_sm - 1) ? ncell : cut(ncell, n_sm, i + 1, 1);
+      while (a < b) {
+        const long rb = a / nch;
+        const long e = std::min(b, (rb + 1) * nch);
+        Instr I = mk(OP_MLP_DOWN, l);
+        I.r0 = (uint32_t)(rb * WIDE_ROWS);
+        I.r1 = (uint32_t)std::min((long)H, (rb + 1) * WIDE_ROWS);
+        I.b = (uint16_t)(a - rb * nch);
+        I.g = (uint16_t)(e - rb * nch);
+        I.wait_ctr = cm.mlp_up(l);
+        I.sig_ctr = cm.mlp(l);
+        qs[i].push_back(I);
+        bytes[i] += (double)(e - a) * ((double)(I.r1 - I.r0) * WIDE_KC * 2 + ab);
+        a = e;
+      }
+    }
+  }
+  norms(L, 2, cm.mlp(L - 1), cm.norm_f());
+  // ---- LM head rows: multiples of 8, at most 128 per instruction
+  for (int i = 0; i < n_sm; i++) {
+    long a = cut(V, n_sm, i, 8);
+    const long b = (i == n_sm - 1) ? V : cut(V, n_sm, i + 1, 8);
+    while (a < b) {
+      const long e = std::min(b, a + (long)WIDE_ROWS);
+      Instr I = mk(OP_LMHEAD, L);
+      I.r0 = (uint32_t)a;
+      I.r1 = (uint32_t)e;
+      I.wait_ctr = cm.norm_f();
+      I.aux = (uint32_t)n_lm++;
+      qs[i].push_back(I);
+      bytes[i] += (double)(e - a) * H * 2 + (double)(H / WIDE_KC) * ab;
+      a = e;
+    }
+  }
+  finish_plan(qs, bytes, cm, hold_mask, S, n_lm, out);
+  out.weight_bytes = (double)L * ((double)R * H * 2 + (double)Hq * D * H * 2 + (double)F * H * 6 +
+                                  2.0 * H * 2) +
+                     (double)V * H * 2 + (double)H * 2;
+  return MK_OK;
+}
+
+// Coverage check of a wide plan (plan_verify's counterpart).
+static int plan_verify_wide(const mk_model_desc& d, int B, const PlanOut& p) {
+  const int L = d.n_layers, H = d.hidden, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
+  const int D = d.head_dim, HPG = Hq / Hkv, V = d.vocab, GR = (HPG + 2) * D;
+  const long R = (long)Hkv * GR, F = d.ffn, nch = F / WIDE_KC;
+  const int S = p.splits, Bp = wide_bp(B);
+  std::vector<uint8_t> qkv((size_t)L * R, 0), att((size_t)L * B * Hkv * S, 0);
+  std::vector<uint8_t> op((size_t)L * Hq * H, 0), up((size_t)L * F, 0);
+  std::vector<uint8_t> dn((size_t)L * H * nch, 0), lm(V, 0), slot(p.n_lm, 0);
+  std::vector<uint8_t> nrm((size_t)(2 * L + 1) * Bp, 0);
+  auto mark = [](std::vector<uint8_t>& v, size_t i) {
+    if (i >= v.size() || v[i]) return false;
+    v[i] = 1;
+    return true;
+  };
+  for (const Instr& I : p.q) {
+    const int l = I.layer;
+    if (I.op != OP_HALT && (I.flags & (F_TAG_WAIT | F_RELAXED_SIG))) return 29;
+    switch (I.op) {
+      case OP_HALT: break;
+      case OP_NORM:
+        if (I.g > 2 || (I.g == 2) != (l == L) || l > L || I.r1 != I.r0 + 1 || (int)I.r0 >= Bp)
+          return 40;
+        if (!mark(nrm, (size_t)(I.g == 2 ? 2 * L : 2 * l + I.g) * Bp + I.r0)) return 41;
+        break;
+      case OP_QKV:
+        if (l >= L || I.r0 >= I.r1 || I.r1 > R || I.r1 - I.r0 > (uint32_t)WIDE_ROWS) return 1;
+        if (I.r0 / GR != I.g || (I.r1 - 1) / GR != I.g || (I.r0 % 8) || (I.r1 % 2)) return 2;
+        for (uint32_t r = I.r0; r < I.r1; r++)
+          if (!mark(qkv, (size_t)l * R + r)) return 3;
+        break;
+      case OP_ATTN:
+        if (l >= L || I.b >= B || I.g >= Hkv || (int)I.r1 != S || (int)I.r0 >= S) return 4;
+        if (!mark(att, (((size_t)l * B + I.b) * Hkv + I.g) * S + I.r0)) return 5;
+        break;
+      case OP_OPROJ:
+        if (l >= L || I.g >= Hq || I.r0 >= I.r1 || (int)I.r1 > H || (I.r0 % 8) ||
+            I.r1 - I.r0 > (uint32_t)WIDE_OROWS)
+          return 6;
+        if (((I.flags & F_RESIDUAL) != 0) != (I.g == 0)) return 7;
+        for (uint32_t r = I.r0; r < I.r1; r++)
+          if (!mark(op, ((size_t)l * Hq + I.g) * H + r)) return 8;
+        break;
+      case OP_MLP_UP:
+        if (l >= L || I.r0 >= I.r1 || (long)I.r1 > F || (I.r0 % 4) ||
+            2 * (I.r1 - I.r0) > (uint32_t)WIDE_ROWS)
+          return 23;
+        for (uint32_t c = I.r0; c < I.r1; c++)
+          if (!mark(up, (size_t)l * F + c)) return 24;
+        break;
+      case OP_MLP_DOWN:
+        if (l >= L || I.r0 >= I.r1 || (int)I.r1 > H || (I.r0 % 8) ||
+            I.r1 - I.r0 > (uint32_t)WIDE_ROWS || I.b >= I.g || (long)I.g > nch)
+          return 25;
+        for (uint32_t r = I.r0; r < I.r1; r++)
+          for (uint32_t k = I.b; k < I.g; k++)
+            if (!mark(dn, ((size_t)l * H + r) * nch + k)) return 26;
+        break;
+      case OP_LMHEAD:
+        if (I.r0 >= I.r1 || (int)I.r1 > V || (I.r0 % 8) || I.r1 - I.r0 > (uint32_t)WIDE_ROWS ||
+            (int)I.aux >= p.n_lm)
+          return 17;
+        if (!mark(slot, I.aux)) return 18;
+        for (uint32_t r = I.r0; r < I.r1; r++)
+          if (!mark(lm, r)) return 19;
+        break;
+      default:
+        return 20;
+    }
+  }
+  for (auto* v : {&qkv, &att, &op, &up, &dn, &lm, &slot, &nrm})
+    for (uint8_t x : *v)
+      if (!x) return 21;
+  return 0;
+}
+
 int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& out,
                unsigned hold_mask, int wb) {
   int rc = plan_shape_ok(d);
@@ -49,6 +373,8 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
   if (B <= 0 || B > d.max_batch || max_ctx <= 0 || max_ctx > d.max_seq || n_sm <= 0)
     return MK_ERR_INVALID_ARG;
   if (wb != 1 && wb != 2) return MK_ERR_INVALID_ARG;
+  if (wide_path(d)) return wb == 2 ? plan_build_wide(d, B, max_ctx, n_sm, out, hold_mask)
+                                   : MK_ERR_UNSUPPORTED;
   // int8 weights: an LM-head instruction's row scales fit the kernel's
   // hidden-sized scale buffer
   if (wb == 1 && ((long)d.vocab + n_sm - 1) / n_sm > d.hidden) return MK_ERR_UNSUPPORTED;
@@ -316,56 +642,7 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
     bytes[i] += (double)(b - a) * H * wb;
   }
 
-  // ---- hold marks: the first instruction of each run of a held op on an SM
-  auto hold_bit = [](uint8_t op) -> unsigned {
-    switch (op) {
-      case OP_QKV: return HOLD_QKV;
-      case OP_ATTN: return HOLD_ATTN;
-      case OP_OPROJ: return HOLD_OPROJ;
-      case OP_MLP: case OP_MLP_UP: case OP_ROUTER: return HOLD_MLP;
-      case OP_MLP_DOWN: return HOLD_DOWN;
-      case OP_LMHEAD: return HOLD_LM;
-      default: return 0;
-    }
-  };
-  for (auto& q : qs)
-    for (size_t k = 1; k < q.size(); k++)
-      if ((hold_mask & hold_bit(q[k].op)) &&
-          (q[k - 1].op != q[k].op || q[k - 1].layer != q[k].layer))
-        q[k].flags |= F_HOLD;
-
-  // ---- counter targets: a wait is for every signal of its counter
-  const int n_ctr = cm.count();
-  std::vector<uint32_t> cnt(n_ctr, 0);
-  for (auto& q : qs)
-    for (auto& I : q)
-      if (I.sig_ctr != NO_CTR) cnt[I.sig_ctr]++;
-  for (auto& q : qs)
-    for (auto& I : q) {
-      if (I.wait_ctr != NO_CTR) I.wait_cnt = cnt[I.wait_ctr];
-    }
-
-  // ---- flatten, HALT-padded
-  size_t mx = 0, total = 0;
-  for (auto& q : qs) {
-    mx = std::max(mx, q.size());
-    total += q.size();
-  }
-  out.max_pc = (int)mx + 1;
-  out.q.assign((size_t)n_sm * out.max_pc, mk(OP_HALT, 0));
-  for (int i = 0; i < n_sm; i++)
-    std::copy(qs[i].begin(), qs[i].end(), out.q.begin() + (size_t)i * out.max_pc);
-  out.n_ctr = n_ctr;
-  out.splits = S;
-  out.n_lm = n_lm;
-  out.n_instr = (int)total;
-  double sum = 0, m = 0;
-  for (double v : bytes) {
-    sum += v;
-    m = std::max(m, v);
-  }
-  out.max_sm_bytes = m;
-  out.mean_sm_bytes = sum / n_sm;
+  finish_plan(qs, bytes, cm, hold_mask, S, n_lm, out);
   const double router_rows = moe ? (double)d.n_experts : 0.0;
   // weights read per step (int8: codes plus one fp32 scale per row; the
   // norm gains stay bf16)
@@ -381,6 +658,7 @@ int plan_build(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& ou
 // group / pair / size limits the kernel relies on, and every residual row is
 // added exactly once per layer.
 int plan_verify(const mk_model_desc& d, int B, const PlanOut& p) {
+  if (wide_path(d)) return plan_verify_wide(d, B, p);
   const int L = d.n_layers, H = d.hidden, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
   const int D = d.head_dim, HPG = Hq / Hkv, V = d.vocab, GR = (HPG + 2) * D;
   const bool moe = d.n_experts > 0;
