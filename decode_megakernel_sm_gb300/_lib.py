@@ -23,7 +23,7 @@ MK_ERR_BOUNDS = -9
 MK_ABL_STREAM, MK_ABL_GRAPH, MK_ABL_PDL = 0, 1, 2
 MK_WEIGHTS_BF16, MK_WEIGHTS_INT8 = 0, 1
 
-OP_NAMES = {0: "HALT", 1: "QKV", 2: "ATTN", 3: "OPROJ", 4: "MLP", 5: "LMHEAD", 6: "ROUTER", 8: "MLP_UP", 9: "MLP_DOWN",
+OP_NAMES = {0: "HALT", 1: "QKV", 2: "ATTN", 3: "OPROJ", 4: "MLP", 5: "LMHEAD", 6: "ROUTER", 8: "MLP_UP", 9: "MLP_DOWN", 10: "NORM",
             7: "NOP"}
 
 

@@ -78,13 +78,14 @@ static Scratch carve_scratch(const mk_model_desc& d, size_t B, size_t kc, size_t
   // h: batch-1 split [L][B][F] floats; batched split [L][F/16][32] A-fragment
   // words of 16 bytes (8 sequences x 4 bytes per column); wide batch one
   // operand buffer [F/64][2 Bp][64] bf16 (every layer reuses it).  The wide
-  // normalised operands: three buffers [H/64][2 Bp][64] bf16.
+  // normalised operands: three buffers [H/64][2 Bp][64] bf16, then the merged
+  // attention outputs [Hq][2 Bp][64].
   const bool wide = wide_path(d);
   const size_t Bp = (size_t)wide_bp((int)B);
   const size_t hB = mlp_split_batched(d) ? 8 : B;
   const size_t sxt = al256(L * B * H * 8);
   const size_t sh = wide ? al256(F * 2 * Bp * 2) : al256(L * hB * F * 4);
-  const size_t sa = wide ? al256(3 * H * 2 * Bp * 2) : 0;
+  const size_t sa = wide ? al256((3 * H + Hq * D) * 2 * Bp * 2) : 0;
   Scratch s{};
   s.xbuf_bytes = sx;
   s.ctr_bytes = sc;
@@ -715,6 +716,7 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.hglob = h->sc.hglob;
   g.act = h->sc.act;
   g.Bp = wide_bp(h->batch);
+  g.arr_ctr = (uint32_t)CtrMap{d.n_kv_heads, d.n_layers}.count();
   g.routes = h->sc.routes;
   g.rweight = h->sc.rweight;
   g.lm_val = h->sc.lm_val;

@@ -36,7 +36,8 @@ struct Ctx {
   int* flag;    // [0] bad launch input, [2] a tagged-input poll failed, [3] / [4] key of
                 // the instruction whose counter was seen / whose wait failed
                 // (both shared by the consumer warps; [1] belongs to the producer),
-                // [5] a router's arrival count
+                // [5] a router's arrival count, [6] wide batch: this attention
+                // item arrived last for its (sequence, kv head)
   Ring ring;
   int tid, warp, lane;
   int pc;
@@ -45,9 +46,8 @@ struct Ctx {
   unsigned long long tw0, tw1;  // trace: wait start / end (thread 0)
   unsigned long long tm[2];     // trace: after the prologue phase, after the ring loop
   // wide batch: tensor-memory base, MMA-done mbarrier (shared address) and
-  // the parity of its next phase, the O-projection's operand tile
+  // the parity of its next phase
   uint32_t tmem, mma_bar, mma_par;
-  unsigned char* actile;
   MK_DEV void mark(const Globals& g, int k) {
     if (g.trace && tid == 0) tm[k] = gtimer();
   }
@@ -151,7 +151,20 @@ MK_DEV int get_segs(const Globals& g, const Instr& I, const int* pos, const int*
       }
       const uint32_t R8 = (R + 7u) / 8u * 8u, unit = (rows + 7u) / 8u * 8u * 128u;
       s[0] = {w + ((size_t)k0 * R8 + r0) * 128u, a + (size_t)k0 * ab, unit, nk, SBY / (unit + ab),
-              SEG_WIDE, R8 * 128u, ab};
+              seg_wide_tag(R8 * 128u, ab)};
+      return 1;
+    }
+    if (I.op == OP_OPROJ) {
+      // rows [r0, r1) of Wo for each of kv group I.g's query heads (one K
+      // chunk per head, [Hq][H][64] packed, H rows apart), next to those
+      // heads' merged attention outputs (the fourth operand buffer, one
+      // chunk per query head)
+      const uint32_t ab = 2u * (uint32_t)g.Bp * 128u;
+      const uint32_t unit = (n + 7u) / 8u * 8u * 128u;
+      const int hpg = g.Hq / g.Hkv;
+      s[0] = {(const unsigned char*)Lp->wo + ((size_t)I.g * hpg * HT + I.r0) * 128u,
+              g.act + (3 * (size_t)(HT / WIDE_KC) + (size_t)I.g * hpg) * ab, unit, (uint32_t)hpg,
+              SBY / (unit + ab), seg_wide_tag((uint32_t)HT * 128u, ab)};
       return 1;
     }
     if (I.op == OP_NORM) return 0;
@@ -828,6 +841,9 @@ MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I)
 constexpr float NEG_BIG = -1e30f;
 
 template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool attn_merge_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I);
+
+template <int HT, int D, int HPG, int NB, int WB>
 MK_DEV bool op_attn(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
   constexpr int LPR = D / 8, SPW = 32 / LPR;
   const int slot = c.lane / LPR, dsl = c.lane % LPR;
@@ -1009,6 +1025,7 @@ MK_DEV bool op_attn(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I
     }
   }
   consumer_bar();
+  if constexpr (NB > 8) return attn_merge_wide(c, g, I);
   return true;
 }
 
@@ -1964,9 +1981,10 @@ struct L2Cursor {
       }
       const uint32_t n = min(s[k].ups, s[k].n - u0);
       const uint32_t b = n * s[k].unit;
-      const unsigned long long cb = s[k].wide() ? (unsigned long long)n * (s[k].unit + s[k].unit2)
-                                                : (s[k].src2 ? 2ull * b : b);
-      if (bytes + cb > from && !s[k].cfill() && !s[k].wide() && !(g.kv_block && s[k].src2)) {
+      const bool wseg = NB > 8 && s[k].wide();
+      const unsigned long long cb = wseg ? (unsigned long long)n * (s[k].unit + s[k].unit2())
+                                         : (s[k].src2 ? 2ull * b : b);
+      if (bytes + cb > from && !s[k].cfill() && !wseg && !(g.kv_block && s[k].src2)) {
         if ((threadIdx.x & 31) == 0) {
           bulk_prefetch_l2(s[k].src + (size_t)u0 * s[k].unit, b);
           if (s[k].src2) bulk_prefetch_l2(s[k].src2 + (size_t)u0 * s[k].unit, b);
@@ -2086,7 +2104,7 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
       // wide batch: the operand pieces are this step's input, written with
       // generic stores by other SMs -- wait for the dependency, then order
       // those stores before the bulk copies that read them
-      if (nseg > 0 && s[0].wide() && I.wait_ctr != NO_CTR) {
+      if (nseg > 0 && s[0].wide() && s[0].unit2() && I.wait_ctr != NO_CTR) {
         bool ok = true;
         if (lane == 0) {
           ok = wait_counter(g, I.wait_ctr, ep * I.wait_cnt, pc, I.op);
@@ -2149,8 +2167,9 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
 #ifdef MK_BOUNDS
         {  // the stage (or each half) must hold what the segment puts there
           const uint32_t room = s[k].src2 ? (uint32_t)g.stage_bytes / 2 : (uint32_t)g.stage_bytes;
-          const bool fits = s[k].wide() ? n * (s[k].unit + s[k].unit2) <= (uint32_t)g.stage_bytes
-                                        : n * s[k].unit <= room;
+          const bool fits = (NB > 8 && s[k].wide())
+                                ? n * (s[k].unit + s[k].unit2()) <= (uint32_t)g.stage_bytes
+                                : n * s[k].unit <= room;
           int bad = 0;
           if (lane == 0 && !MK_IN(g, fits, pc, I.op)) bad = 1;
           if (__shfl_sync(0xFFFFFFFFu, bad, 0)) goto drain;
@@ -2162,22 +2181,25 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
           const uint32_t bytes = n * s[k].unit;
           const uint32_t full = full0 + 8u * st;
           const uint32_t dst = ring_s + (uint32_t)st * (uint32_t)g.stage_bytes;
-          if (s[k].wide()) {
-            // (wide variant only) chunk j: its weight piece at j * unit, its
-            // operand piece at ups * unit + j * unit2
-            mbar_expect_tx(full, n * (s[k].unit + s[k].unit2));
+          const bool wseg = NB > 8 && s[k].wide();
+          if (wseg) {
+            // chunk j: its weight piece at j * unit, its operand piece (if
+            // the operand is streamed; unit2 > 0) at ups * unit + j * unit2
+            const uint32_t u2 = s[k].unit2();
+            mbar_expect_tx(full, n * (s[k].unit + u2));
             for (uint32_t j = 0; j < n; j++) {
               bulk_g2s(dst + j * s[k].unit,
-                       copy_src(g, I, s[k].src + (size_t)(u0 + j) * s[k].pitch, s[k].unit, pc),
+                       copy_src(g, I, s[k].src + (size_t)(u0 + j) * s[k].pitch(), s[k].unit, pc),
                        s[k].unit, full, pol_w);
-              bulk_g2s(dst + s[k].ups * s[k].unit + j * s[k].unit2,
-                       copy_src(g, I, s[k].src2 + (size_t)(u0 + j) * s[k].unit2, s[k].unit2, pc),
-                       s[k].unit2, full, pol_kv);
+              if (u2)
+                bulk_g2s(dst + s[k].ups * s[k].unit + j * u2,
+                         copy_src(g, I, s[k].src2 + (size_t)(u0 + j) * u2, u2, pc), u2, full,
+                         pol_kv);
             }
           } else {
             mbar_expect_tx(full, s[k].src2 ? 2u * bytes : bytes);
           }
-          if (s[k].wide()) {
+          if (wseg) {
             // issued above
           } else if (s[k].cfill()) {
             // the consumers copy this stage in after their dependency wait
@@ -2212,8 +2234,8 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
                      pol_w);
           }
         }
-        issued_bytes += s[k].wide() ? (unsigned long long)n * (s[k].unit + s[k].unit2)
-                                    : (s[k].src2 ? 2ull : 1ull) * n * s[k].unit;
+        issued_bytes += (NB > 8 && s[k].wide()) ? (unsigned long long)n * (s[k].unit + s[k].unit2())
+                                                 : (s[k].src2 ? 2ull : 1ull) * n * s[k].unit;
         __syncwarp();
         issued++;
         if (++st == ns) {
@@ -2295,10 +2317,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
   c.tw0 = c.tw1 = 0;
   c.tm[0] = c.tm[1] = 0;
   c.tmem = c.mma_bar = c.mma_par = 0;
-  c.actile = nullptr;
   if constexpr (NB > 8) {
     // wide batch: the accumulators' tensor memory, held for the whole kernel
-    c.actile = smem + Ls.actile;
     c.mma_bar = smem_u32(smem + Ls.tcw + 8);
     if (warp == 0) tmem_alloc(smem_u32(smem + Ls.tcw), (uint32_t)WIDE_TMEM_COLS);
     tc_fence_before();

@@ -9,7 +9,7 @@
 // bits of the activation ("Megakernels in LLM Inference When Fusion
 // Actually Wins", sections "Core Tradeoff" and "When Megakernels Win": the
 // batch range where the contraction turns from a GEMV into a skinny GEMM).
-// The accumulator lives in tensor memory (256 columns allocated once per CTA
+// The accumulator lives in tensor memory (64 columns allocated once per CTA
 // for the life of the kernel); consumer warps 0-3 read it back with
 // tcgen05.ld, one accumulator row (one weight row) per thread, and add the
 // high and low columns of each sequence.
@@ -56,12 +56,12 @@ MK_DEV bool wide_mma_wait(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g) {
 // if a ring wait gave up.
 template <int HT, int D, int HPG, int NB, int WB>
 MK_DEV bool wide_mma_stream(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Seg& s) {
-  const uint32_t N = s.unit2 / 128u;
+  const uint32_t N = s.unit2() / 128u;
   const uint32_t idesc = idesc_bf16(128, (int)N);
   bool bad = false, first = true;
   for (uint32_t u0 = 0; u0 < s.n; u0 += s.ups) {
     uint32_t n = min(s.ups, s.n - u0);
-    if (!MK_IN(g, n * (s.unit + s.unit2) <= (uint32_t)g.stage_bytes, c.pc, -1)) n = 0;
+    if (!MK_IN(g, n * (s.unit + s.unit2()) <= (uint32_t)g.stage_bytes, c.pc, -1)) n = 0;
     if (!bad && !c.ring.acquire(g)) bad = true;
     if (bad) continue;
     if (c.warp == 0) {
@@ -69,7 +69,7 @@ MK_DEV bool wide_mma_stream(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const 
         tc_fence_after();
         const uint32_t sb = smem_u32(c.ring.stage_ptr());
         for (uint32_t j = 0; j < n; j++) {
-          const uint32_t wa = sb + j * s.unit, aa = sb + s.ups * s.unit + j * s.unit2;
+          const uint32_t wa = sb + j * s.unit, aa = sb + s.ups * s.unit + j * s.unit2();
 #pragma unroll
           for (uint32_t k = 0; k < 4; k++)
             tc_mma_bf16(c.tmem, sw128_desc(wa + 32u * k), sw128_desc(aa + 32u * k), idesc,
@@ -91,20 +91,19 @@ MK_DEV bool wide_mma_stream(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const 
   return wide_mma_wait(c, g);
 }
 
-// Read accumulator tile t back (rows 128 t .. 128 t + 127 of the
-// instruction, N = 2 Bp columns at column t * N) into yrow[b][m], b < Bp, m
-// < 128: consumer warp w < 4 reads lanes 32 w .. 32 w + 31 and adds each
-// sequence's high and low columns.  Ends with the tensor-memory reads ordered
-// before a CTA barrier, after which yrow is complete (and the next MMAs may
-// overwrite the accumulator).
+// Read the accumulator back (128 weight rows, N = 2 Bp columns) into
+// yrow[b][m], b < Bp, m < 128: consumer warp w < 4 reads lanes 32 w ..
+// 32 w + 31 and adds each sequence's high and low columns.  Ends with the
+// tensor-memory reads ordered before a CTA barrier, after which yrow is
+// complete (and the next MMAs may overwrite the accumulator).
 template <int HT, int D, int HPG, int NB, int WB>
-MK_DEV void wide_tile_out(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, uint32_t N, int t) {
+MK_DEV void wide_tile_out(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, uint32_t N) {
   static_assert(NB <= 32, "64 accumulator columns per tile");
   if (c.warp < 4) {
     float* y = c.yrow + 32 * c.warp + c.lane;
     for (uint32_t q = 0; 16u * q < N; q++) {  // 16 columns: sequences 8q .. 8q + 7
       float v[16];
-      tmem_ld16(c.tmem + ((uint32_t)(32 * c.warp) << 16) + (uint32_t)t * N + 16u * q, v);
+      tmem_ld16(c.tmem + ((uint32_t)(32 * c.warp) << 16) + 16u * q, v);
 #pragma unroll
       for (int e = 0; e < 8; e++) y[(8 * q + e) * WIDE_ROWS] = v[2 * e] + v[2 * e + 1];
     }
@@ -197,7 +196,7 @@ MK_DEV bool op_qkv_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Inst
   c.mark(g, 1);
   const uint32_t n = I.r1 - I.r0;
   float* yrow = c.yrow;  // [NB][WIDE_ROWS]
-  wide_tile_out(c, g, s[0].unit2 / 128u, 0);
+  wide_tile_out(c, g, s[0].unit2() / 128u);
   constexpr int GR = (HPG + 2) * D;
   const int np = (int)n / 2;
   for (int it = c.tid; it < np * g.B; it += NCT) {
@@ -235,26 +234,35 @@ MK_DEV bool op_qkv_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Inst
   return true;
 }
 
-// --------------------------------------------- OP_OPROJ (wide batch) ----
-// Head I.g's split-KV partials merged for every sequence, the merged output
-// written as the MMA's operand tile in shared memory, then rows [r0, r1)
-// (at most 512: up to four M tiles, the accumulators side by side in tensor
-// memory) of Wo[:, h*D:(h+1)*D] applied and added into x_{2l+1} with float
-// reductions; head-0 instructions also add x_{2l}.
+// ------------------------------------- attention merge (wide batch) ----
+// After an attention item has written its partial (o, m, l) records: count
+// the item in for its (layer, sequence, kv head); the item that arrives last
+// merges the S slices of each of the group's query heads (M = max m_s,
+// L = sum l_s 2^(m_s - M), o = sum o_s 2^(m_s - M) / L) and writes the heads'
+// outputs, bf16 high part and remainder, as rows 2b, 2b + 1 of their chunks
+// of the O-projection's operand buffer.  Its completion signal (a release)
+// follows, so a met attention counter means merged outputs.
 template <int HT, int D, int HPG, int NB, int WB>
-MK_DEV bool op_oproj_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
-  static_assert(D == WIDE_KC, "one head is one K chunk");
-  const int h = I.g, l = I.layer, S = g.splits;
+MK_DEV bool attn_merge_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
+  const int b = I.b, S = (int)I.r1;
   constexpr int PS = part_stride(D);
-  if (!dep_wait(c, g, I)) return false;
-  for (int it = c.tid; it < NB * D; it += NCT) {
-    const int dim = it % D, b = it / D;
+  if (c.tid == 0) {
+    uint32_t* arr = g.ctr + g.arr_ctr + ((size_t)I.layer * g.B + b) * g.Hkv + I.g;
+    const uint32_t old = atom_add_acq_rel(arr, 1u);
+    c.flag[6] = old == c.epoch * (uint32_t)S - 1u;
+  }
+  consumer_bar();
+  const bool last = c.flag[6] != 0;
+  if (!last) return true;
+  const uint32_t ab = 2u * (uint32_t)g.Bp * 128u;
+  unsigned char* out = g.act + 3 * (size_t)(HT / WIDE_KC) * ab;
+  for (int t = c.tid; t < HPG * D; t += NCT) {
+    const int h = t / D, dim = t % D, hq = I.g * HPG + h;
+    const size_t r = (((size_t)I.layer * g.B + b) * g.Hq + hq) * S;
     float M = NEG_BIG, Ls = 0.f, O = 0.f;
-    if (b < g.B && MK_IN(g, (((size_t)l * g.B + b) * g.Hq + h + 1) * S * PS <= g.n_part, c.pc,
-                         I.op)) {
-      const float* base = g.part + (((size_t)l * g.B + b) * g.Hq + h) * S * PS;
+    if (MK_IN(g, (r + S) * PS <= g.n_part, c.pc, I.op)) {
       for (int s2 = 0; s2 < S; s2++) {
-        const float* p = base + (size_t)s2 * PS;
+        const float* p = g.part + (r + s2) * PS;
         const float ms = __ldcg(p + D), ls = __ldcg(p + D + 1), os = __ldcg(p + dim);
         const float mn = fmaxf(M, ms);
         const float fa = exp2f(M - mn), fb = exp2f(ms - mn);
@@ -263,75 +271,43 @@ MK_DEV bool op_oproj_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const In
         M = mn;
       }
     }
-    c.attn[b * D + dim] = b < g.B ? O / Ls : 0.f;
+    const float x = O / Ls;
+    const uint16_t hi = to_bf16(x), lo = to_bf16(x - bf1(hi));
+    *(uint16_t*)(out + opnd_off(ab, 2u * b, (uint32_t)(hq * D + dim))) = hi;
+    *(uint16_t*)(out + opnd_off(ab, 2u * b + 1u, (uint32_t)(hq * D + dim))) = lo;
   }
   consumer_bar();
-  // the operand tile: rows 2b (high) and 2b + 1 (remainder) of the head's
-  // output, 64 columns, swizzled
-  for (int it = c.tid; it < g.Bp * (D / 8); it += NCT) {
-    const int b = it / (D / 8), j = it % (D / 8);
-    float x[8];
-#pragma unroll
-    for (int e = 0; e < 8; e++) x[e] = c.attn[b * D + 8 * j + e];
-    uint4 hi, lo;
-    split_hl8(x, hi, lo);
-    *(uint4*)(c.actile + sw128_off(2u * b, 8u * j)) = hi;
-    *(uint4*)(c.actile + sw128_off(2u * b + 1u, 8u * j)) = lo;
-  }
-  fence_async_smem();
-  consumer_bar();
+  return true;
+}
+
+// --------------------------------------------- OP_OPROJ (wide batch) ----
+// Rows [r0, r1) (at most 128, from a multiple of 8) of Wo over kv group I.g's
+// HPG * D columns, against the group's merged attention outputs (streamed
+// with the weights, one K chunk per query head), added into x_{2l+1} with
+// float reductions: one contribution per group and element rather than one
+// per head.  The group-0 instructions also add x_{2l}.
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool op_oproj_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
+  static_assert(D == WIDE_KC, "one head is one K chunk");
+  const int l = I.layer;
+  if (!dep_wait(c, g, I)) return false;
   c.mark(g, 0);
   Seg s[2];
   get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
-  const Seg& ws = s[0];  // Wo rows, 128 bytes each; a stage holds whole 128-row tiles
-  const uint32_t N = 2u * (uint32_t)g.Bp;
-  const uint32_t idesc = idesc_bf16(128, (int)N);
-  const uint32_t at = smem_u32(c.actile);
-  bool bad = false;
-  for (uint32_t u0 = 0; u0 < ws.n; u0 += ws.ups) {
-    const uint32_t n = stage_units(g, ws, u0, (uint32_t)g.stage_bytes, c.pc, OP_OPROJ);
-    if (!bad && !c.ring.acquire(g)) bad = true;
-    if (bad) continue;
-    if (c.warp == 0) {
-      if (c.lane == 0) {
-        tc_fence_after();
-        const uint32_t sb = smem_u32(c.ring.stage_ptr());
-        for (uint32_t t = 0; t * 128u < n; t++) {
-          const uint32_t col = ((u0 + 128u * t) / 128u) * N;
-#pragma unroll
-          for (uint32_t k = 0; k < 4; k++)
-            tc_mma_bf16(c.tmem + col, sw128_desc(sb + t * 16384u + 32u * k),
-                        sw128_desc(at + 32u * k), idesc, k > 0);
-        }
-        tc_commit(c.ring.empty_bar());
-      }
-      __syncwarp();
-      c.ring.advance();
-    } else {
-      c.ring.release(c.lane);
-    }
-  }
-  if (bad) c.flag[2] = 1;
-  consumer_bar();
-  if (c.flag[2]) return false;
-  if (c.tid == 0) tc_commit(c.mma_bar);
-  if (!wide_mma_wait(c, g)) return false;
+  if (!wide_mma_stream(c, g, s[0])) return false;
   c.mark(g, 1);
+  wide_tile_out(c, g, s[0].unit2() / 128u);
   const int nr = (int)(I.r1 - I.r0);
   const bool resid = (I.flags & F_RESIDUAL) != 0;
-  for (int t = 0; t * 128 < nr; t++) {
-    wide_tile_out(c, g, N, t);
-    const int mt = min(128, nr - 128 * t);
-    for (int it = c.tid; it < g.B * mt; it += NCT) {
-      const int b = it / mt, m = it % mt;
-      const int row = (int)I.r0 + 128 * t + m;
-      float y = c.yrow[b * WIDE_ROWS + m];
-      if (resid) y += x_in(g, c.epoch, 2 * l, c.tok, b, row);
-      float* dst = xres_mine(g, c.epoch, 2 * l + 1, b);
-      if (MK_IN(g, (size_t)(dst - g.xbuf) + row < g.n_xbuf, c.pc, I.op)) red_add_f32(dst + row, y);
-    }
-    consumer_bar();  // yrow is reused by the next tile
+  for (int it = c.tid; it < g.B * nr; it += NCT) {
+    const int b = it / nr, m = it % nr;
+    const int row = (int)I.r0 + m;
+    float y = c.yrow[b * WIDE_ROWS + m];
+    if (resid) y += x_in(g, c.epoch, 2 * l, c.tok, b, row);
+    float* dst = xres_mine(g, c.epoch, 2 * l + 1, b);
+    if (MK_IN(g, (size_t)(dst - g.xbuf) + row < g.n_xbuf, c.pc, I.op)) red_add_f32(dst + row, y);
   }
+  consumer_bar();
   return true;
 }
 
@@ -349,7 +325,7 @@ MK_DEV bool op_mlp_up_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const I
   c.mark(g, 1);
   const int ncol = (int)(I.r1 - I.r0);
   float* yrow = c.yrow;  // [NB][WIDE_ROWS]
-  wide_tile_out(c, g, s[0].unit2 / 128u, 0);
+  wide_tile_out(c, g, s[0].unit2() / 128u);
   const uint32_t ab = 2u * (uint32_t)g.Bp * 128u;
   unsigned char* hb = (unsigned char*)g.hglob;
   for (int it = c.tid; it < ncol * g.Bp; it += NCT) {
@@ -381,7 +357,7 @@ MK_DEV bool op_mlp_down_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const
   get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
   if (!wide_mma_stream(c, g, s[0])) return false;
   c.mark(g, 1);
-  wide_tile_out(c, g, s[0].unit2 / 128u, 0);
+  wide_tile_out(c, g, s[0].unit2() / 128u);
   const int n = (int)(I.r1 - I.r0);
   for (int it = c.tid; it < g.B * n; it += NCT) {
     const int b = it / n, m = it % n;
@@ -416,7 +392,7 @@ MK_DEV bool op_lmhead_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const I
   c.mark(g, 1);
   const int n = (int)(I.r1 - I.r0), B = g.B, V = g.V;
   float* yrow = c.yrow;  // [NB][WIDE_ROWS]
-  wide_tile_out(c, g, s[0].unit2 / 128u, 0);
+  wide_tile_out(c, g, s[0].unit2() / 128u);
   for (int it = c.tid; it < B * n; it += NCT) {
     const int b = it / n, m = it % n;
     const int row = (int)I.r0 + m;

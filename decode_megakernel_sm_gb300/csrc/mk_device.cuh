@@ -469,8 +469,12 @@ constexpr uint32_t SEG_CFILL = 0x80000000u;
 // a stage holds `ups` chunks, the weight pieces first (unit apart), then the
 // operand pieces (unit2 apart, from offset ups * unit).  The operand is an
 // input of this step: the producer waits for the instruction's dependency
-// before it issues any of the segment's copies.
+// before it issues any of the segment's copies.  row0 carries the flag, the
+// pitch in 128-byte rows in bits [8, 30) and unit2 / 128 in bits [0, 8).
 constexpr uint32_t SEG_WIDE = 0x40000000u;
+MK_HD inline uint32_t seg_wide_tag(uint32_t pitch, uint32_t unit2) {
+  return SEG_WIDE | ((pitch / 128u) << 8) | (unit2 / 128u);
+}
 
 struct Seg {
   const unsigned char* src;
@@ -481,9 +485,10 @@ struct Seg {
   uint32_t row0;  // swizzled GEMV matrices: index of the first row in its tensor (key = row & 7);
                   // SEG_CFILL set: an input of this step, whose stages the producer only arms
                   // and the consumers fill once their dependency wait has passed
-  uint32_t pitch = 0, unit2 = 0;  // SEG_WIDE segments only
   MK_DEV bool cfill() const { return (row0 & SEG_CFILL) != 0; }
   MK_DEV bool wide() const { return (row0 & SEG_WIDE) != 0; }
+  MK_DEV uint32_t pitch() const { return ((row0 & 0x3FFFFFFFu) >> 8) * 128u; }
+  MK_DEV uint32_t unit2() const { return (row0 & 0xFFu) * 128u; }
 };
 
 // Ring cursor of one consumer warp.

@@ -89,11 +89,12 @@ MK_HD inline int phase_of(const Instr& I) {
 }
 
 // Counter ids: per layer l, base l*stride:
-//   qkv[g] (g < Hkv), attn[g], oproj, mlp, router, mlp_up, router arrivals,
-//   norm_a, norm_m; then the argmax counter, the step counter and norm_f.
+//   qkv[g] (g < Hkv), attn[g], oproj, mlp, router, mlp_up, router arrivals;
+//   then the argmax counter, the step counter, and (wide batch) norm_a and
+//   norm_m of every layer and norm_f.
 struct CtrMap {
   int Hkv, L;
-  MK_HD int stride() const { return 2 * Hkv + 7; }
+  MK_HD int stride() const { return 2 * Hkv + 5; }
   MK_HD uint32_t qkv(int l, int g) const { return (uint32_t)(l * stride() + g); }
   MK_HD uint32_t attn(int l, int g) const { return (uint32_t)(l * stride() + Hkv + g); }
   MK_HD uint32_t oproj(int l) const { return (uint32_t)(l * stride() + 2 * Hkv); }
@@ -109,10 +110,10 @@ struct CtrMap {
   MK_HD uint32_t lm_done() const { return (uint32_t)(L * stride() + 1); }
   // wide batch: the normalised operand of QKV / of the MLP of layer l, and of
   // the LM head, is complete
-  MK_HD uint32_t norm_a(int l) const { return (uint32_t)(l * stride() + 2 * Hkv + 5); }
-  MK_HD uint32_t norm_m(int l) const { return (uint32_t)(l * stride() + 2 * Hkv + 6); }
-  MK_HD uint32_t norm_f() const { return (uint32_t)(L * stride() + 2); }
-  MK_HD int count() const { return L * stride() + 3; }
+  MK_HD uint32_t norm_a(int l) const { return (uint32_t)(L * stride() + 2 + 2 * l); }
+  MK_HD uint32_t norm_m(int l) const { return (uint32_t)(L * stride() + 3 + 2 * l); }
+  MK_HD uint32_t norm_f() const { return (uint32_t)(L * stride() + 2 + 2 * L); }
+  MK_HD int count() const { return L * stride() + 3 + 2 * L; }
 };
 
 // Kernel-shape constants.
@@ -179,13 +180,14 @@ inline bool mlp_split(const mk_model_desc& d) {
 // swizzle.  The normalised activations are written once per step and norm
 // point by OP_NORM instructions, into operand buffers in that layout; the
 // QKV, gate/up, down and LM-head instructions stream them through the ring
-// K chunk by K chunk next to their weights.  The O-projection builds its
-// operand (one head's attention output) in shared memory.
+// K chunk by K chunk next to their weights.  The attention items that finish
+// a (sequence, kv head) last merge its split-KV slices into a fourth operand
+// buffer, which the O-projection (one kv group's query heads, one K chunk
+// per head) streams the same way.
 constexpr int WIDE_NB = 32;          // batch capacity of the wide variant
 constexpr int WIDE_KC = 64;          // columns of one K chunk (a 128-byte row of bf16)
-constexpr int WIDE_ROWS = 128;       // weight rows of one streamed instruction (the MMA's M)
-constexpr int WIDE_OROWS = 512;      // rows of one O-projection instruction (four M tiles)
-constexpr int WIDE_TMEM_COLS = 256;  // tensor-memory columns a CTA allocates
+constexpr int WIDE_ROWS = 128;       // weight rows of one instruction (the MMA's M)
+constexpr int WIDE_TMEM_COLS = 64;   // tensor-memory columns a CTA allocates (N <= 2 * 32)
 MK_HD inline bool wide_path(const mk_model_desc& d) {
   return d.n_experts == 0 && d.max_batch > 8;
 }
@@ -294,13 +296,14 @@ struct Globals {
   // wide batch: the three normalised operands (attention input, MLP input,
   // final), each [H / 64][2 Bp][64] bf16 in the swizzled K-major layout; h
   // (in hglob) is [F / 64][2 Bp][64] likewise
-  unsigned char* act;
+  unsigned char* act;      // (then a fourth, [Hq][2 Bp][64]: the merged attention outputs)
   int Bp;                  // batch rounded up to 8 (the operand holds 2 Bp rows)
+  uint32_t arr_ctr;        // first of the [L][B][Hkv] attention-arrival counters
 };
 
 // Shared-memory layout (bytes from the dynamic shared memory base).
 struct SmemLayout {
-  int ring, full, empty, xn, yrow, hbuf, attn, red, misc, mpart, sc, actile, tcw, total;
+  int ring, full, empty, xn, yrow, hbuf, attn, red, misc, mpart, sc, tcw, total;
 };
 
 // WB: bytes per weight (2 bf16, 1 int8; int8 adds the row-scale region sc)
@@ -319,18 +322,15 @@ MK_HD inline SmemLayout smem_layout(int n_stages, int stage_bytes, int NB, int H
     // the ring (yrow comes first)
     s.xn = o;
     s.yrow = o;
-    const int yb = 4 * NB * WIDE_ROWS, pb = 4 * 3 * NB * D, ab = 4 * NCW * HPG * (D + 2);
-    int m = yb > pb ? yb : pb;
-    m = m > ab ? m : ab;
+    const int yb = 4 * NB * WIDE_ROWS, ab = 4 * NCW * HPG * (D + 2);
+    int m = yb > ab ? yb : ab;
     m = m > 16384 ? m : 16384;
     o += (m + 15) / 16 * 16;
     s.hbuf = o;
-    s.attn = o;   o += 4 * NB * D;
+    s.attn = o;
     s.red = o;    o += 4 * 2 * NCW * NB + 16;
     s.misc = o;   o += 4 * (8 + 3 * NB + 4 * NB);
-    o = (o + 1023) / 1024 * 1024;
-    s.actile = o; o += 2 * NB * 128;  // the O-projection's operand: 2 NB rows x 64 bf16
-    s.tcw = o;    o += 16;            // tensor-memory base address, MMA-done mbarrier
+    s.tcw = o;    o += 16;  // tensor-memory base address, MMA-done mbarrier
     s.mpart = o;
     s.sc = o;
     s.total = (o + 127) / 128 * 128;
@@ -348,7 +348,7 @@ MK_HD inline SmemLayout smem_layout(int n_stages, int stage_bytes, int NB, int H
   o = (o + 15) / 16 * 16;
   s.mpart = o;  o += NB > 1 ? 4 * NCW * MMA_FLUSH * NB : 0;  // batched GEMV partial sums
   s.sc = o;     o += WB == 1 ? 4 * H : 0;  // row scales of one O-proj / LM-head instruction
-  s.actile = s.tcw = o;
+  s.tcw = o;
   s.total = (o + 127) / 128 * 128;
   return s;
 }

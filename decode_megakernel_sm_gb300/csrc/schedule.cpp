@@ -112,8 +112,9 @@ static void finish_plan(std::vector<std::vector<Instr>>& qs, const std::vector<d
 //   NORM (MLP input) -> gate/up columns -> down (row block, FFN chunks),
 // then the final NORM and the LM head rows.  The norms are one instruction
 // per sequence (padded to Bp = B rounded up to 8), spread over the SMs; every
-// GEMV instruction holds at most 128 weight rows (the MMA's M; O-projection:
-// up to 512, four tiles) starting on a multiple of 8 (the operand atoms).
+// GEMV instruction holds at most 128 weight rows (the MMA's M) starting on a
+// multiple of 8 (the operand atoms); an O-projection instruction covers all
+// query heads of one kv group (one K chunk per head).
 static int plan_build_wide(const mk_model_desc& d, int B, int max_ctx, int n_sm, PlanOut& out,
                            unsigned hold_mask) {
   const int L = d.n_layers, H = d.hidden, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
@@ -125,10 +126,12 @@ static int plan_build_wide(const mk_model_desc& d, int B, int max_ctx, int n_sm,
   const long R = (long)Hkv * GR;
   const int Bp = wide_bp(B);
   CtrMap cm{Hkv, L};
-  int S = std::max(1, n_sm / (B * Hkv));
+  // split-KV: about three items per SM (at least two slices per sequence and
+  // kv head, at least 16 positions per slice at max_ctx), dealt out slice-
+  // major and round-robin, so that each SM's items come from different
+  // sequences and their lengths average out
+  int S = std::max(2, (3 * n_sm + B * Hkv - 1) / (B * Hkv));
   S = std::min(S, std::max(1, max_ctx / 16));
-  S = std::min(S, STAGE_UNIT / (B * part_stride(D) * 4));
-  if (S < 1) return MK_ERR_UNSUPPORTED;
   const int n_items = B * Hkv * S;
   std::vector<std::vector<Instr>> qs(n_sm);
   std::vector<double> bytes(n_sm, 0.0);
@@ -184,47 +187,55 @@ static int plan_build_wide(const mk_model_desc& d, int B, int max_ctx, int n_sm,
         a = e;
       }
     }
-    // ---- attention items (as in plan_build)
+    // ---- attention items: item k = slice k / (B Hkv) of pair k % (B Hkv)
     for (int k = 0; k < n_items; k++) {
-      const int sm = (int)((long)k * n_sm / n_items);
+      const int sm = k % n_sm, pr = k % (B * Hkv);
       Instr I = mk(OP_ATTN, l);
-      I.b = (uint16_t)(k / (Hkv * S));
-      I.g = (uint16_t)((k / S) % Hkv);
-      I.r0 = (uint32_t)(k % S);
+      I.b = (uint16_t)(pr / Hkv);
+      I.g = (uint16_t)(pr % Hkv);
+      I.r0 = (uint32_t)(k / (B * Hkv));
       I.r1 = (uint32_t)S;
       I.wait_ctr = cm.qkv(l, I.g);
       I.sig_ctr = cm.attn(l, I.g);
       qs[sm].push_back(I);
       bytes[sm] += (double)max_ctx / S * D * 4;
     }
-    // ---- O-projection rows (multiples of 8, at most WIDE_OROWS each)
-    const long OR = (long)Hq * H;
+    // ---- O-projection: per kv group, its query heads' Wo columns for a row
+    // range (multiples of 8, at most 128 rows); the SMs split evenly over
+    // the groups
     for (int i = 0; i < n_sm; i++) {
+      int g;
       long a, b;
-      if (n_sm >= Hq) {
-        const int h = (int)((long)i * Hq / n_sm);
-        const long s0 = ((long)h * n_sm + Hq - 1) / Hq;
-        const long s1 = ((long)(h + 1) * n_sm + Hq - 1) / Hq;
+      if (n_sm >= Hkv) {
+        g = (int)((long)i * Hkv / n_sm);
+        const long s0 = ((long)g * n_sm + Hkv - 1) / Hkv;
+        const long s1 = ((long)(g + 1) * n_sm + Hkv - 1) / Hkv;
         const int m = (int)(s1 - s0), k = (int)(i - s0);
-        a = (long)h * H + cut(H, m, k, 8);
-        b = (long)h * H + (k == m - 1 ? H : cut(H, m, k + 1, 8));
-      } else {
-        a = cut(OR, n_sm, i, 8);
-        b = (i == n_sm - 1) ? OR : cut(OR, n_sm, i + 1, 8);
+        a = cut(H, m, k, 8);
+        b = k == m - 1 ? H : cut(H, m, k + 1, 8);
+      } else {  // fewer SMs than groups: SM i takes whole groups
+        g = -1;
+        a = b = 0;
       }
-      while (a < b) {
-        const long h = a / H;
-        const long e = std::min(std::min(b, (h + 1) * H), a + (long)WIDE_OROWS);
-        Instr I = mk(OP_OPROJ, l);
-        I.g = (uint16_t)h;
-        I.r0 = (uint32_t)(a - h * H);
-        I.r1 = (uint32_t)(e - h * H);
-        I.flags = h == 0 ? F_RESIDUAL : 0;
-        I.wait_ctr = cm.attn(l, (int)(h / HPG));
-        I.sig_ctr = cm.oproj(l);
-        qs[i].push_back(I);
-        bytes[i] += (double)(e - a) * D * 2;
-        a = e;
+      auto push = [&](int grp, long a0, long b0) {
+        while (a0 < b0) {
+          const long e = std::min(b0, a0 + (long)WIDE_ROWS);
+          Instr I = mk(OP_OPROJ, l);
+          I.g = (uint16_t)grp;
+          I.r0 = (uint32_t)a0;
+          I.r1 = (uint32_t)e;
+          I.flags = grp == 0 ? F_RESIDUAL : 0;
+          I.wait_ctr = cm.attn(l, grp);
+          I.sig_ctr = cm.oproj(l);
+          qs[i].push_back(I);
+          bytes[i] += (double)(e - a0) * HPG * D * 2 + HPG * ab;
+          a0 = e;
+        }
+      };
+      if (g >= 0) {
+        push(g, a, b);
+      } else {
+        for (int grp = i; grp < Hkv; grp += n_sm) push(grp, 0, H);
       }
     }
     norms(l, 1, cm.oproj(l), cm.norm_m(l));
@@ -284,6 +295,7 @@ static int plan_build_wide(const mk_model_desc& d, int B, int max_ctx, int n_sm,
     }
   }
   finish_plan(qs, bytes, cm, hold_mask, S, n_lm, out);
+  out.n_ctr += L * B * Hkv;  // the attention-arrival counters (after cm's)
   out.weight_bytes = (double)L * ((double)R * H * 2 + (double)Hq * D * H * 2 + (double)F * H * 6 +
                                   2.0 * H * 2) +
                      (double)V * H * 2 + (double)H * 2;
@@ -325,13 +337,14 @@ static int plan_verify_wide(const mk_model_desc& d, int B, const PlanOut& p) {
         if (l >= L || I.b >= B || I.g >= Hkv || (int)I.r1 != S || (int)I.r0 >= S) return 4;
         if (!mark(att, (((size_t)l * B + I.b) * Hkv + I.g) * S + I.r0)) return 5;
         break;
-      case OP_OPROJ:
-        if (l >= L || I.g >= Hq || I.r0 >= I.r1 || (int)I.r1 > H || (I.r0 % 8) ||
-            I.r1 - I.r0 > (uint32_t)WIDE_OROWS)
+      case OP_OPROJ:  // a kv group's query heads
+        if (l >= L || I.g >= Hkv || I.r0 >= I.r1 || (int)I.r1 > H || (I.r0 % 8) ||
+            I.r1 - I.r0 > (uint32_t)WIDE_ROWS)
           return 6;
         if (((I.flags & F_RESIDUAL) != 0) != (I.g == 0)) return 7;
-        for (uint32_t r = I.r0; r < I.r1; r++)
-          if (!mark(op, ((size_t)l * Hq + I.g) * H + r)) return 8;
+        for (int hh = 0; hh < HPG; hh++)
+          for (uint32_t r = I.r0; r < I.r1; r++)
+            if (!mark(op, ((size_t)l * Hq + (size_t)I.g * HPG + hh) * H + r)) return 8;
         break;
       case OP_MLP_UP:
         if (l >= L || I.r0 >= I.r1 || (long)I.r1 > F || (I.r0 % 4) ||
