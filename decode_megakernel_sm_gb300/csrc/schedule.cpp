@@ -255,25 +255,30 @@ static int plan_build_wide(const mk_model_desc& d, int B, int max_ctx, int n_sm,
         a = e;
       }
     }
-    // ---- down: cells (row block of 128 rows, 64-column FFN chunk), row-block
-    // major; each SM takes a contiguous run, one instruction per row block
-    const long nrb = (H + WIDE_ROWS - 1) / WIDE_ROWS, nch = F / WIDE_KC, ncell = nrb * nch;
+    // ---- down: per 128-row block of x, its FFN chunks cut into K ranges,
+    // the SMs split evenly over the row blocks (one instruction per SM, so
+    // one epilogue of reductions each)
+    const long nrb = (H + WIDE_ROWS - 1) / WIDE_ROWS, nch = F / WIDE_KC;
+    auto push_down = [&](int i, long rb, long k0, long k1) {
+      if (k0 >= k1) return;
+      Instr I = mk(OP_MLP_DOWN, l);
+      I.r0 = (uint32_t)(rb * WIDE_ROWS);
+      I.r1 = (uint32_t)std::min((long)H, (rb + 1) * WIDE_ROWS);
+      I.b = (uint16_t)k0;
+      I.g = (uint16_t)k1;
+      I.wait_ctr = cm.mlp_up(l);
+      I.sig_ctr = cm.mlp(l);
+      qs[i].push_back(I);
+      bytes[i] += (double)(k1 - k0) * ((double)(I.r1 - I.r0) * WIDE_KC * 2 + ab);
+    };
     for (int i = 0; i < n_sm; i++) {
-      long a = cut(ncell, n_sm, i, 1);
-      const long b = (i == n_sm - 1) ? ncell : cut(ncell, n_sm, i + 1, 1);
-      while (a < b) {
-        const long rb = a / nch;
-        const long e = std::min(b, (rb + 1) * nch);
-        Instr I = mk(OP_MLP_DOWN, l);
-        I.r0 = (uint32_t)(rb * WIDE_ROWS);
-        I.r1 = (uint32_t)std::min((long)H, (rb + 1) * WIDE_ROWS);
-        I.b = (uint16_t)(a - rb * nch);
-        I.g = (uint16_t)(e - rb * nch);
-        I.wait_ctr = cm.mlp_up(l);
-        I.sig_ctr = cm.mlp(l);
-        qs[i].push_back(I);
-        bytes[i] += (double)(e - a) * ((double)(I.r1 - I.r0) * WIDE_KC * 2 + ab);
-        a = e;
+      if (n_sm >= nrb) {
+        const long rb = (long)i * nrb / n_sm;
+        const long s0 = (rb * n_sm + nrb - 1) / nrb, s1 = ((rb + 1) * n_sm + nrb - 1) / nrb;
+        const int m = (int)(s1 - s0), k = (int)(i - s0);
+        push_down(i, rb, cut(nch, m, k, 1), k == m - 1 ? nch : cut(nch, m, k + 1, 1));
+      } else {  // fewer SMs than row blocks: SM i takes whole row blocks
+        for (long rb = i; rb < nrb; rb += n_sm) push_down(i, rb, 0, nch);
       }
     }
   }
