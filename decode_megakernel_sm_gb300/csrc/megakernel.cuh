@@ -37,7 +37,8 @@ struct Ctx {
                 // the instruction whose counter was seen / whose wait failed
                 // (both shared by the consumer warps; [1] belongs to the producer),
                 // [5] a router's arrival count, [6] wide batch: this attention
-                // item arrived last for its (sequence, kv head)
+                // item arrived last for its (sequence, kv head), [7] this LM-head
+                // slice arrived last
   Ring ring;
   int tid, warp, lane;
   int pc;
@@ -1841,8 +1842,7 @@ MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr&
     ri[c.warp * NB + lane] = bidx;
   }
   consumer_bar();
-  if (c.warp != 0) return true;
-  if (lane == 0 && MK_IN(g, ((size_t)I.aux + 1) * B <= g.n_lmv, c.pc, I.op)) {
+  if (c.tid == 0 && MK_IN(g, ((size_t)I.aux + 1) * B <= g.n_lmv, c.pc, I.op)) {
     for (int b = 0; b < B && b < NB; b++) {
       float v = -INFINITY;
       int ix = 0x7FFFFFFF;
@@ -1862,27 +1862,37 @@ MK_DEV bool op_lmhead(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr&
   return true;
 }
 
-// The LM-head slices' last step (consumer warp 0, once its slice's (max,
-// index) per sequence is written): count this slice in; the slice that
-// arrives last reduces all slices into argmax[b] and signals the step done.
+// The LM-head slices' last step (all consumer threads, once this slice's
+// (max, first index) per sequence is in lm_val / lm_idx): count the slice in;
+// the CTA whose slice arrives last reduces all slices into argmax[b], one
+// sequence per warp with four slices' loads in flight per lane, and signals
+// the step done.
 template <int HT, int D, int HPG, int NB, int WB>
 MK_DEV void lm_reduce(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g) {
   const int lane = c.lane, B = g.B;
-  uint32_t old = 0;
-  if (lane == 0) old = atom_add_acq_rel(g.ctr + g.lm_ctr, 1u);
-  old = __shfl_sync(0xFFFFFFFFu, old, 0);
-  __syncwarp();
-  if (old != c.epoch * (uint32_t)g.n_lm - 1u) return;
-  for (int b = 0; b < B && b < NB; b++) {
+  consumer_bar();  // every slice value this CTA writes is written
+  if (c.tid == 0)
+    c.flag[7] = atom_add_acq_rel(g.ctr + g.lm_ctr, 1u) == c.epoch * (uint32_t)g.n_lm - 1u;
+  consumer_bar();
+  if (!c.flag[7]) return;
+  for (int b = c.warp; b < B && b < NB; b += NCW) {
     float v = -INFINITY;
     int ix = 0x7FFFFFFF;
-    for (int k = lane; k < g.n_lm; k += 32) {
-      const float ov = __ldcg(g.lm_val + (size_t)k * B + b);
-      const int oi = __ldcg(g.lm_idx + (size_t)k * B + b);
-      if (ov > v || (ov == v && oi < ix)) {
-        v = ov;
-        ix = oi;
+    for (int k0 = lane; k0 < g.n_lm; k0 += 4 * 32) {
+      float ov[4];
+      int oi[4];
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int k = k0 + 32 * u;
+        ov[u] = k < g.n_lm ? __ldcg(g.lm_val + (size_t)k * B + b) : -INFINITY;
+        oi[u] = k < g.n_lm ? __ldcg(g.lm_idx + (size_t)k * B + b) : 0x7FFFFFFF;
       }
+#pragma unroll
+      for (int u = 0; u < 4; u++)
+        if (ov[u] > v || (ov[u] == v && oi[u] < ix)) {
+          v = ov[u];
+          ix = oi[u];
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -1897,8 +1907,8 @@ MK_DEV void lm_reduce(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g) {
   }
   // every SM is done with this step once its argmax is out: a multi-step
   // launch starts the next step behind this signal
-  __syncwarp();
-  if (lane == 0) red_release(g.ctr + g.lm_done_ctr, 1u);
+  consumer_bar();
+  if (c.tid == 0) red_release(g.ctr + g.lm_done_ctr, 1u);
 }
 
 }  // namespace mk

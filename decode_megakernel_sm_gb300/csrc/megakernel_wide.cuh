@@ -373,11 +373,16 @@ MK_DEV bool op_mlp_down_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const
 
 // ----------------------------------------------- OP_LMHEAD (wide batch) ----
 // Rows [r0, r1) (at most 128) of the LM head over the final operand: the
-// logits, this slice's first maximum per sequence, and the last-arriver
-// argmax over all slices (lm_reduce).
+// logits and, per sequence, the first maximum of the rows, folded into the
+// SM's running (max, lowest row) in shared memory.  An SM's LM-head
+// instructions form one slice (aux): the first of them (I.b bit 0) starts the
+// running maxima and zeroes the slice's share of the next step's residual
+// buffers, the last (bit 1) writes the slice's values and joins the
+// last-arriver argmax over all slices (lm_reduce).
 template <int HT, int D, int HPG, int NB, int WB>
 MK_DEV bool op_lmhead_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
-  if (g.zero_next) {  // as in op_lmhead: this slice's share of the next step's residual buffers
+  const bool first = (I.b & 1) != 0, last = (I.b & 2) != 0;
+  if (g.zero_next && first) {  // as in op_lmhead, once per slice
     const size_t total = (size_t)2 * g.L * g.kc * g.B * g.H;
     const size_t a = total * I.aux / (size_t)g.n_lm, e = total * (I.aux + 1) / (size_t)g.n_lm;
     float* nx = g.xbuf + (size_t)((c.epoch + 1u) & 1u) * total;
@@ -398,8 +403,10 @@ MK_DEV bool op_lmhead_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const I
     const int row = (int)I.r0 + m;
     if (MK_IN(g, row < V, c.pc, I.op)) g.logits[(size_t)b * V + row] = yrow[b * WIDE_ROWS + m];
   }
-  // this slice's (max, lowest row) per sequence: warp w takes sequences
-  // w, w + NCW, ...
+  // this instruction's (max, lowest row) per sequence, folded into the SM's
+  // running values: warp w takes sequences w, w + NCW, ...
+  float* runv = c.red + 2 * NCW * NB + 4;
+  int* runi = (int*)(runv + NB);
   for (int b = c.warp; b < B; b += NCW) {
     float best = -INFINITY;
     int bidx = 0x7FFFFFFF;
@@ -419,14 +426,21 @@ MK_DEV bool op_lmhead_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const I
         bidx = oi;
       }
     }
-    if (c.lane == 0 && MK_IN(g, ((size_t)I.aux + 1) * B <= g.n_lmv, c.pc, I.op)) {
-      g.lm_val[(size_t)I.aux * B + b] = best;
-      g.lm_idx[(size_t)I.aux * B + b] = bidx;
+    if (c.lane == 0) {
+      if (!first && (runv[b] > best || (runv[b] == best && runi[b] < bidx))) {
+        best = runv[b];
+        bidx = runi[b];
+      }
+      runv[b] = best;
+      runi[b] = bidx;
+      if (last && MK_IN(g, ((size_t)I.aux + 1) * B <= g.n_lmv, c.pc, I.op)) {
+        g.lm_val[(size_t)I.aux * B + b] = best;
+        g.lm_idx[(size_t)I.aux * B + b] = bidx;
+      }
     }
   }
   consumer_bar();
-  if (c.warp != 0) return true;
-  lm_reduce(c, g);
+  if (last) lm_reduce(c, g);
   return true;
 }
 

@@ -328,7 +328,7 @@ MK_HD inline SmemLayout smem_layout(int n_stages, int stage_bytes, int NB, int H
     o += (m + 15) / 16 * 16;
     s.hbuf = o;
     s.attn = o;
-    s.red = o;    o += 4 * 2 * NCW * NB + 16;
+    s.red = o;    o += 4 * 2 * NCW * NB + 16 + 4 * 2 * NB;  // + an LM-head slice's running maxima
     s.misc = o;   o += 4 * (8 + 3 * NB + 4 * NB);
     s.tcw = o;    o += 16;  // tensor-memory base address, MMA-done mbarrier
     s.mpart = o;

@@ -283,21 +283,28 @@ static int plan_build_wide(const mk_model_desc& d, int B, int max_ctx, int n_sm,
     }
   }
   norms(L, 2, cm.mlp(L - 1), cm.norm_f());
-  // ---- LM head rows: multiples of 8, at most 128 per instruction
+  // ---- LM head rows: multiples of 8, at most 128 per instruction; an SM's
+  // instructions are one argmax slice (aux), the first (b bit 0) and last
+  // (bit 1) of them marked
   for (int i = 0; i < n_sm; i++) {
     long a = cut(V, n_sm, i, 8);
     const long b = (i == n_sm - 1) ? V : cut(V, n_sm, i + 1, 8);
+    if (a >= b) continue;
+    const size_t k0 = qs[i].size();
     while (a < b) {
       const long e = std::min(b, a + (long)WIDE_ROWS);
       Instr I = mk(OP_LMHEAD, L);
       I.r0 = (uint32_t)a;
       I.r1 = (uint32_t)e;
       I.wait_ctr = cm.norm_f();
-      I.aux = (uint32_t)n_lm++;
+      I.aux = (uint32_t)n_lm;
       qs[i].push_back(I);
       bytes[i] += (double)(e - a) * H * 2 + (double)(H / WIDE_KC) * ab;
       a = e;
     }
+    qs[i][k0].b |= 1;
+    qs[i].back().b |= 2;
+    n_lm++;
   }
   finish_plan(qs, bytes, cm, hold_mask, S, n_lm, out);
   out.n_ctr += L * B * Hkv;  // the attention-arrival counters (after cm's)
@@ -368,9 +375,9 @@ static int plan_verify_wide(const mk_model_desc& d, int B, const PlanOut& p) {
         break;
       case OP_LMHEAD:
         if (I.r0 >= I.r1 || (int)I.r1 > V || (I.r0 % 8) || I.r1 - I.r0 > (uint32_t)WIDE_ROWS ||
-            (int)I.aux >= p.n_lm)
+            (int)I.aux >= p.n_lm || I.b > 3)
           return 17;
-        if (!mark(slot, I.aux)) return 18;
+        if ((I.b & 2) && !mark(slot, I.aux)) return 18;  // one last instruction per slice
         for (uint32_t r = I.r0; r < I.r1; r++)
           if (!mark(lm, r)) return 19;
         break;
