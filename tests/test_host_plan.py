@@ -293,3 +293,107 @@ def test_quantize_rows_refuses_bad_arguments():
     assert lib.mk_quantize_rows_int8(None, 4, 8, p, p, None) == L.MK_ERR_INVALID_ARG
     assert lib.mk_quantize_rows_int8(p, 4, 8, None, p, None) == L.MK_ERR_INVALID_ARG
     assert lib.mk_quantize_rows_int8(p, 4, 8, p, None, None) == L.MK_ERR_INVALID_ARG
+
+
+def wide_coverage(cfg, q, n_sm, max_pc, splits):
+    """The wide-batch plan (9..32 sequences), re-derived in Python: every norm
+    row, QKV row, attention item, O-projection (head, row), FFN column, down
+    (row, 64-column chunk) and LM-head row exactly once, within the tile
+    limits the tensor-core bodies rely on (at most 128 weight rows per
+    instruction, starting on a multiple of 8), and the LM-head slices: one
+    per SM, its instructions consecutive, the first and the last marked."""
+    Lc, H, Hq, Hkv, D = cfg["n_layers"], cfg["hidden"], cfg["n_q_heads"], cfg["n_kv_heads"], \
+        cfg["head_dim"]
+    B, F, V = cfg["batch"], cfg["ffn"], cfg["vocab"]
+    HPG, Bp = Hq // Hkv, (B + 7) // 8 * 8
+    R = Hkv * (HPG + 2) * D
+    seen = {k: set() for k in ("norm", "qkv", "attn", "oproj", "up", "down", "lm")}
+    slices = {}
+    for s in range(n_sm):
+        lm_run = []
+        for i in range(max_pc):
+            I = q[s * max_pc + i]
+            if I.op == 0:
+                break
+            rows = I.r1 - I.r0
+            if I.op == 10:
+                key = (I.layer, I.g, I.r0)
+                assert key not in seen["norm"] and rows == 1 and I.r0 < Bp
+                seen["norm"].add(key)
+            elif I.op == 1:
+                assert I.r0 % 8 == 0 and 0 < rows <= 128
+                for r in range(I.r0, I.r1):
+                    assert (I.layer, r) not in seen["qkv"]
+                    seen["qkv"].add((I.layer, r))
+            elif I.op == 2:
+                key = (I.layer, I.b, I.g, I.r0)
+                assert key not in seen["attn"] and I.r1 == splits
+                seen["attn"].add(key)
+            elif I.op == 3:  # a kv group's heads
+                assert I.r0 % 8 == 0 and 0 < rows <= 128 and I.g < Hkv
+                assert bool(I.flags & 1) == (I.g == 0)
+                for h in range(I.g * HPG, (I.g + 1) * HPG):
+                    for r in range(I.r0, I.r1):
+                        assert (I.layer, h, r) not in seen["oproj"]
+                        seen["oproj"].add((I.layer, h, r))
+            elif I.op == 8:
+                assert I.r0 % 4 == 0 and 0 < 2 * rows <= 128
+                for c in range(I.r0, I.r1):
+                    assert (I.layer, c) not in seen["up"]
+                    seen["up"].add((I.layer, c))
+            elif I.op == 9:  # rows x FFN chunks [b, g)
+                assert I.r0 % 8 == 0 and 0 < rows <= 128 and I.b < I.g <= F // 64
+                for r in range(I.r0, I.r1):
+                    for k in range(I.b, I.g):
+                        assert (I.layer, r, k) not in seen["down"]
+                        seen["down"].add((I.layer, r, k))
+            elif I.op == 5:
+                assert I.r0 % 8 == 0 and 0 < rows <= 128
+                lm_run.append((i, I))
+                for r in range(I.r0, I.r1):
+                    assert r not in seen["lm"]
+                    seen["lm"].add(r)
+            else:
+                raise AssertionError(f"op {I.op} in a wide plan")
+        if lm_run:
+            idx = [i for i, _ in lm_run]
+            assert idx == list(range(idx[0], idx[0] + len(idx)))  # consecutive
+            assert len({I.aux for _, I in lm_run}) == 1
+            assert [I.b for _, I in lm_run] == ([3] if len(lm_run) == 1 else
+                                               [1] + [0] * (len(lm_run) - 2) + [2])
+            assert lm_run[0][1].aux not in slices
+            slices[lm_run[0][1].aux] = s
+    assert len(seen["norm"]) == (2 * Lc + 1) * Bp
+    assert len(seen["qkv"]) == Lc * R
+    assert len(seen["attn"]) == Lc * B * Hkv * splits
+    assert len(seen["oproj"]) == Lc * Hq * H
+    assert len(seen["up"]) == Lc * F
+    assert len(seen["down"]) == Lc * H * (F // 64)
+    assert len(seen["lm"]) == V
+    assert sorted(slices) == list(range(len(slices)))
+
+
+@pytest.mark.parametrize("batch", [9, 16, 32])
+@pytest.mark.parametrize("n_sm", [1, 7, 148, 152])
+def test_wide_plan_covers_all_work_and_is_deadlock_free(batch, n_sm):
+    cfg, d = desc("llama1b_b8", batch=batch)
+    st, q = L.mk_plan(d, batch, cfg["max_seq"], n_sm)
+    assert st["attn_splits"] >= 2
+    wide_coverage(cfg, q, n_sm, st["max_pc"], st["attn_splits"])
+    assert st["n_lm"] == min(n_sm, cfg["vocab"] // 8)
+    assert L.mk_plan_check(q, n_sm, st["max_pc"], st["n_counters"]) == L.MK_OK
+
+
+def test_wide_plan_ragged_shape():
+    # 17 FFN chunks, a vocabulary that is not a multiple of 8, 13 sequences
+    cfg, d = desc("llama1b_b8", batch=13, n_layers=3, ffn=1088, vocab=5001)
+    st, q = L.mk_plan(d, 13, cfg["max_seq"], 152)
+    wide_coverage(cfg, q, 152, st["max_pc"], st["attn_splits"])
+    assert L.mk_plan_check(q, 152, st["max_pc"], st["n_counters"]) == L.MK_OK
+
+
+def test_wide_shapes_outside_the_variant_are_refused():
+    # the wide variant needs a dense FFN of whole 64-column chunks
+    cfg, d = desc("llama1b_b8", batch=16, ffn=1000)
+    with pytest.raises(L.MkError):
+        L.mk_plan(d, 16, cfg["max_seq"], 152)
