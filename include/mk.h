@@ -111,8 +111,16 @@ typedef struct {
  * here a bulk-copy ring, which is why every matrix is re-laid out).
  * Ownership: the caller keeps its weights (read only during the call) and
  * its KV cache (must outlive the handle); the library owns the packed copy.
+ * Batch capacity: max_batch 1 (the batch-1 variants), 2..8 (the batched
+ * variant) or 9..32 (the wide-batch variant: every contraction on the
+ * tcgen05 tensor cores with the accumulator in tensor memory; dense FFN of
+ * whole 64-column chunks, hidden size a multiple of 64, 64-dim heads, bf16
+ * weights -- "Megakernels in LLM Inference When Fusion Actually Wins",
+ * sections "Core Tradeoff" and "When Megakernels Win", the batch range up
+ * to 32 where the crossover lies).
  * Errors: MK_ERR_INVALID_ARG for a NULL or non-16-byte-aligned pointer or an
- * inconsistent shape, MK_ERR_UNSUPPORTED, MK_ERR_CUDA.
+ * inconsistent shape, MK_ERR_UNSUPPORTED (no compiled variant, or a wide
+ * batch outside the conditions above), MK_ERR_CUDA.
  * On error *out is NULL and nothing is leaked.                            */
 int mk_create(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv, mk_handle** out);
 
@@ -329,7 +337,9 @@ int mk_set_l2_prefetch(mk_handle* h, uint64_t bytes_ahead);
  * stage; smaller stages give a deeper ring.  Results do not depend on it.
  * Call between steps (not while a step is in flight on another stream);
  * drops the cached ablation graphs.  MK_ERR_INVALID_ARG for other sizes,
- * MK_ERR_UNSUPPORTED if two stages no longer fit (the old size is kept).   */
+ * MK_ERR_UNSUPPORTED if two stages no longer fit, or for 16384 on a
+ * wide-batch handle (a stage holds a 128-row weight chunk and its operand
+ * chunk); the old size is kept.                                            */
 int mk_set_stage_bytes(mk_handle* h, int stage_bytes);
 
 /* At most `max_stages` ring stages (2..16; 0, the default: as many as the
@@ -437,7 +447,12 @@ const char* mk_status_string(int status);
  *   op, flags (u8), layer (u16), b, g (u16), r0, r1, wait_ctr, wait_cnt,
  *   sig_ctr, aux (u32).  op: 0 HALT, 1 QKV, 2 ATTN, 3 OPROJ, 4 MLP (fused
  *   column slice), 5 LMHEAD, 6 ROUTER, 7 NOP, 8 MLP_UP (gate/up column
- *   slice), 9 MLP_DOWN (down rows).  wait_ctr / sig_ctr 0xFFFFFFFF: none.  */
+ *   slice), 9 MLP_DOWN (down rows), 10 NORM (wide batch: RMSNorm of the
+ *   sequences [r0, r1) into the tensor-core operand g: 0 attention input,
+ *   1 MLP input, 2 LM-head input).  Wide-batch MLP_DOWN: rows [r0, r1) over
+ *   the 64-column FFN chunks [b, g); wide-batch OPROJ: kv group g's query
+ *   heads; wide-batch LMHEAD: b bit 0 / bit 1 mark the first / last
+ *   instruction of an SM's slice aux.  wait_ctr / sig_ctr 0xFFFFFFFF: none. */
 typedef struct {
   uint8_t op, flags;
   uint16_t layer;
