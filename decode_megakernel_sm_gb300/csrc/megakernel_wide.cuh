@@ -234,6 +234,29 @@ MK_DEV bool op_qkv_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Inst
   return true;
 }
 
+// The rows [r0, r1) of yrow (one per weight row; r0 and r1 - r0 multiples of
+// 8) added into the residual x_out with 16-byte float reductions, four rows
+// of one sequence each; with `resid`, the instruction also adds x_in of its
+// rows (the residual input of the phase).
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV void wide_residual_add(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I,
+                              int j_in, int j_out, bool resid) {
+  const int n4 = (int)(I.r1 - I.r0) / 4;
+  for (int it = c.tid; it < g.B * n4; it += NCT) {
+    const int b = it / n4, m = 4 * (it % n4);
+    const int row = (int)I.r0 + m;
+    const float* y = c.yrow + b * WIDE_ROWS + m;
+    float v[4] = {y[0], y[1], y[2], y[3]};
+    if (resid)
+#pragma unroll
+      for (int e = 0; e < 4; e++) v[e] += x_in(g, c.epoch, j_in, c.tok, b, row + e);
+    float* dst = xres_mine(g, c.epoch, j_out, b);
+    if (MK_IN(g, (size_t)(dst - g.xbuf) + row + 4 <= g.n_xbuf, c.pc, I.op))
+      red_add_v4f32(dst + row, v[0], v[1], v[2], v[3]);
+  }
+  consumer_bar();
+}
+
 // ------------------------------------- attention merge (wide batch) ----
 // After an attention item has written its partial (o, m, l) records: count
 // the item in for its (layer, sequence, kv head); the item that arrives last
@@ -297,17 +320,7 @@ MK_DEV bool op_oproj_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const In
   if (!wide_mma_stream(c, g, s[0])) return false;
   c.mark(g, 1);
   wide_tile_out(c, g, s[0].unit2() / 128u);
-  const int nr = (int)(I.r1 - I.r0);
-  const bool resid = (I.flags & F_RESIDUAL) != 0;
-  for (int it = c.tid; it < g.B * nr; it += NCT) {
-    const int b = it / nr, m = it % nr;
-    const int row = (int)I.r0 + m;
-    float y = c.yrow[b * WIDE_ROWS + m];
-    if (resid) y += x_in(g, c.epoch, 2 * l, c.tok, b, row);
-    float* dst = xres_mine(g, c.epoch, 2 * l + 1, b);
-    if (MK_IN(g, (size_t)(dst - g.xbuf) + row < g.n_xbuf, c.pc, I.op)) red_add_f32(dst + row, y);
-  }
-  consumer_bar();
+  wide_residual_add(c, g, I, 2 * l, 2 * l + 1, (I.flags & F_RESIDUAL) != 0);
   return true;
 }
 
@@ -358,16 +371,7 @@ MK_DEV bool op_mlp_down_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const
   if (!wide_mma_stream(c, g, s[0])) return false;
   c.mark(g, 1);
   wide_tile_out(c, g, s[0].unit2() / 128u);
-  const int n = (int)(I.r1 - I.r0);
-  for (int it = c.tid; it < g.B * n; it += NCT) {
-    const int b = it / n, m = it % n;
-    const int row = (int)I.r0 + m;
-    float y = c.yrow[b * WIDE_ROWS + m];
-    if (I.b == 0) y += xres_sum(g, c.epoch, 2 * l + 1, b, row);
-    float* dst = xres_mine(g, c.epoch, 2 * l + 2, b);
-    if (MK_IN(g, (size_t)(dst - g.xbuf) + row < g.n_xbuf, c.pc, I.op)) red_add_f32(dst + row, y);
-  }
-  consumer_bar();
+  wide_residual_add(c, g, I, 2 * l + 1, 2 * l + 2, I.b == 0);
   return true;
 }
 
