@@ -1,6 +1,8 @@
 // api.cu -- the C ABI of libmk.so (declared in include/mk.h): handle life
 // cycle, weight packing, schedule upload, the one-launch decode step, the
 // host-buffer step, the per-phase ablation launcher and error reporting.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -134,6 +136,9 @@ struct mk_handle {
   int wfmt = MK_WEIGHTS_BF16;
   const float* lm_scale = nullptr;  // int8 weights
   float* rope = nullptr;
+  // batched variants: per layer, tensor maps of the K and V caches (tiled
+  // TMA loads for the tensor-core attention), or nullptr
+  void* tmaps = nullptr;
   // schedule and scratch
   int batch = 0, max_ctx = 0;
   PlanOut plan;
@@ -223,6 +228,7 @@ static void free_all(mk_handle* h) {
   if (h->packed) cudaFree(h->packed);
   if (h->layers_d) cudaFree(h->layers_d);
   if (h->rope) cudaFree(h->rope);
+  if (h->tmaps) cudaFree(h->tmaps);
   if (h->qperm) cudaFree(h->qperm);
   if (h->h_err) cudaFreeHost(h->h_err);
   if (h->own) cudaStreamDestroy(h->own);
@@ -282,6 +288,43 @@ static int size_ring(mk_handle* h, int stage_bytes) {
 
 static int pack_int8(mk_handle* h, const mk_weights* w, const mk_kv* kv, cudaStream_t s);
 static int pack_bf16(mk_handle* h, const mk_weights* w, const mk_kv* kv, cudaStream_t s);
+
+// Tensor maps of every layer's K and V cache for the tensor-core attention
+// of the batched variants (64-dim heads, 2 or 4 query heads per kv head): the
+// cache [max_batch][Hkv][max_seq][64] as a 2-D bf16 tensor of
+// max_batch * Hkv * max_seq rows, loaded in boxes of 64 rows x 64 columns in
+// the 128-byte swizzle.  Other shapes get none (the CUDA-core attention).
+static int make_kv_tmaps(mk_handle* h, const mk_kv* kv) {
+  const mk_model_desc& d = h->d;
+  const int HPG = d.n_q_heads / d.n_kv_heads;
+  if (h->var->NB == 1 || d.head_dim != 64 || (HPG != 2 && HPG != 4)) return MK_OK;
+  static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  if (!enc) {
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", (void**)&enc, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !enc) {
+      enc = nullptr;
+      return MK_ERR_CUDA;
+    }
+  }
+  const int L = d.n_layers;
+  std::vector<CUtensorMap> maps(2 * (size_t)L);
+  const cuuint64_t dims[2] = {64, (cuuint64_t)d.max_batch * d.n_kv_heads * d.max_seq};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {64, 64}, es[2] = {1, 1};
+  for (int l = 0; l < L; l++)
+    for (int kvi = 0; kvi < 2; kvi++) {
+      void* base = kvi == 0 ? kv->k[l] : kv->v[l];
+      if (enc(&maps[2 * l + kvi], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return MK_ERR_CUDA;
+    }
+  CK(cudaMalloc(&h->tmaps, maps.size() * sizeof(CUtensorMap)));
+  CK(cudaMemcpy(h->tmaps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice));
+  return MK_OK;
+}
 
 static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_kv* kv,
                        mk_handle* h, int wfmt) {
@@ -360,6 +403,10 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
       rope[((size_t)pp * (D / 2) + t) * 2 + 1] = (float)std::sin(ang);
     }
   CK(cudaMalloc(&h->rope, rope.size() * sizeof(float)));
+  {
+    const int rc2 = make_kv_tmaps(h, kv);
+    if (rc2 != MK_OK) return rc2;
+  }
   CK(cudaMemcpyAsync(h->rope, rope.data(), rope.size() * sizeof(float), cudaMemcpyHostToDevice,
                      s));
   CK(cudaStreamSynchronize(s));
@@ -715,6 +762,7 @@ static Globals make_globals(const mk_handle* h, const int32_t* tok, const int32_
   g.xt = h->sc.xt;
   g.hglob = h->sc.hglob;
   g.act = h->sc.act;
+  g.tmaps = h->kv_block ? nullptr : h->tmaps;  // (a paged cache: the CUDA-core attention)
   g.Bp = wide_bp(h->batch);
   g.arr_ctr = (uint32_t)CtrMap{d.n_kv_heads, d.n_layers}.count();
   g.routes = h->sc.routes;

@@ -16,9 +16,18 @@
 // Template parameters: HT hidden size, D head dim, HPG query heads per kv
 // head, NB batch capacity of the compiled variant (rows b >= B are masked).
 #pragma once
+#include "attn_tc.cuh"
 #include "mk_device.cuh"
 
 namespace mk {
+
+// The batched variants with 64-dim heads and 2 or 4 query heads per kv head
+// run attention on the tensor cores over TMA-swizzled K / V tiles (when the
+// cache is contiguous; a paged cache keeps the CUDA-core body).
+template <int D, int HPG, int NB>
+MK_HD constexpr bool attn_tc_path() {
+  return NB > 1 && D == 64 && (HPG == 2 || HPG == 4);
+}
 
 template <int HT, int D, int HPG, int NB, int WB>
 struct Ctx {
@@ -839,13 +848,132 @@ MK_DEV bool op_qkv(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I)
 // through the ring K-half / V-half per stage; every slot of LPR lanes handles
 // one position at a time with an online-softmax update, then slots, warps
 // and finally the CTA merge their states.
-constexpr float NEG_BIG = -1e30f;
 
 template <int HT, int D, int HPG, int NB, int WB>
 MK_DEV bool attn_merge_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I);
 
+// The end of an attention item: every warp has put its per-head state (o,
+// m, l) into sc = yrow [NCW][HPG][D + 2]; merge the warps and write the
+// item's partial record (o, m, l of each head) for the O-projection (or, wide
+// batch, for the last arriving item's merge).
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool attn_cta_merge(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
+  const int b = I.b;
+  const float* sc = c.yrow;
+  consumer_bar();
+  for (int t = c.tid; t < HPG * D; t += NCT) {
+    const int h = t / D, dim = t % D;
+    float M = NEG_BIG;
+#pragma unroll
+    for (int w = 0; w < NCW; w++) M = fmaxf(M, sc[(w * HPG + h) * (D + 2) + D]);
+    float Ls = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < NCW; w++) {
+      const float* p = sc + (w * HPG + h) * (D + 2);
+      const float f = exp2f(p[D] - M);
+      Ls = fmaf(p[D + 1], f, Ls);
+      O = fmaf(p[dim], f, O);
+    }
+    const size_t po = ((((size_t)I.layer * g.B + b) * g.Hq + (size_t)I.g * HPG + h) * g.splits +
+                       I.r0) * part_stride(D);
+    if (MK_IN(g, po + D + 2 <= g.n_part, c.pc, I.op)) {
+      float* dst = g.part + po;
+      dst[dim] = O;
+      if (dim == 0) {
+        dst[D] = M;
+        dst[D + 1] = Ls;
+      }
+    }
+  }
+  consumer_bar();
+  if constexpr (NB > 8) return attn_merge_wide(c, g, I);
+  return true;
+}
+
+// Attention item (b, kv group g, slice) on the tensor cores (attn_tc.cuh):
+// the K / V stages arrive as swizzled TMA tiles; each warp takes 16-position
+// chunks of every stage (rotating with the stage, so that the short last
+// chunk moves between warps), and warp 0 of the item's last slice also runs
+// row P from a zero-padded 16-row tile.  The V rows past a stage's last
+// position in its last chunk are zeroed first (those rows may hold anything).
+template <int HT, int D, int HPG, int NB, int WB>
+MK_DEV bool op_attn_tc(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
+  const int b = I.b, P = c.pos[b];
+  const LayerPtrs& Lp = g.layers[I.layer];
+  const bool last = I.r0 + 1 == I.r1 && c.warp == 0;
+  if (!dep_wait(c, g, I)) return false;
+  constexpr float QS = 0.125f * 1.4426950408889634f;  // log2(e) / sqrt(64)
+  AttnTC<HPG> st;
+  {
+    const size_t qo = (((size_t)I.layer * g.B + b) * g.Hq + (size_t)I.g * HPG) * D;
+    st.init(g.qbuf + (MK_IN(g, qo + HPG * D <= g.n_q, c.pc, I.op) ? qo : 0), QS, c.lane);
+  }
+  c.mark(g, 0);
+  Seg s[2];
+  get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
+  uint32_t rot = 0;  // chunks of earlier stages (round-robin offset)
+  for (uint32_t u0 = 0; u0 < s[0].n; u0 += s[0].ups) {
+    const uint32_t n = stage_units(g, s[0], u0, (uint32_t)g.stage_bytes / 2, c.pc, OP_ATTN);
+    if (!c.ring.acquire(g)) {
+      c.flag[2] = 1;
+      break;
+    }
+    const uint32_t kt = smem_u32(c.ring.stage_ptr()), vt = kt + c.ring.sb / 2;
+    const uint32_t nch = (n + 15u) / 16u;
+    for (uint32_t ch = (uint32_t)(c.warp + NCW - (int)(rot % NCW)) % NCW; ch < nch; ch += NCW) {
+      const int nv = (int)min(16u, n - 16u * ch);
+      if (nv < 16) {  // zero V rows nv .. 15 of this chunk (generic stores, then a proxy fence
+                      // before the stage goes back to the bulk-copy engine)
+        unsigned char* vr = (unsigned char*)c.ring.stage_ptr() + c.ring.sb / 2 +
+                            (size_t)(16u * ch + (uint32_t)nv) * 128u;
+        for (int i = c.lane; i < (16 - nv) * 8; i += 32) ((uint4*)vr)[i] = make_uint4(0, 0, 0, 0);
+        __syncwarp();
+      }
+      st.chunk(kt, vt, 16u * ch, nv, c.lane);
+      if (nv < 16) fence_async_smem();
+    }
+    rot += nch;
+    c.ring.release(c.lane);
+  }
+  if (last) {
+    // row P in a 16-row tile (1024-byte aligned, inside xn, free during
+    // attention): rows 1..15 zero, row 0 unswizzled
+    unsigned char* mt = (unsigned char*)(((uintptr_t)c.xn + 1023) & ~(uintptr_t)1023);
+    for (int i = c.lane; i < 256; i += 32) ((uint4*)mt)[i] = make_uint4(0, 0, 0, 0);
+    __syncwarp();
+    const long long off = kv_row(g, b, I.g, P);
+    if (c.lane < 16 && off >= 0 && MK_IN(g, (size_t)off + D <= g.kv_elems, c.pc, I.op)) {
+      const uint16_t* src = (c.lane < 8 ? Lp.kc : Lp.vc) + off + (c.lane & 7) * 8;
+      ((uint4*)(mt + (c.lane < 8 ? 0 : 2048)))[c.lane & 7] = __ldcg((const uint4*)src);
+    }
+    __syncwarp();
+    st.chunk(smem_u32(mt), smem_u32(mt) + 2048u, 0u, 1, c.lane);
+  }
+  st.finish();
+  c.mark(g, 1);
+  consumer_bar();  // (every warp is past its last use of xn's tile and of the ring)
+  if (c.flag[2]) return false;
+  float* sc = c.yrow;  // [NCW][HPG][D + 2]
+  const int gq = c.lane >> 2, tq = c.lane & 3;
+  if (gq < HPG) {
+    float* p = sc + ((size_t)c.warp * HPG + gq) * (D + 2);
+#pragma unroll
+    for (int dt = 0; dt < 8; dt++) {
+      p[8 * dt + 2 * tq] = st.o[dt][0];
+      p[8 * dt + 2 * tq + 1] = st.o[dt][1];
+    }
+    if (tq == 0) {
+      p[D] = st.m;
+      p[D + 1] = st.l;
+    }
+  }
+  return attn_cta_merge(c, g, I);
+}
+
 template <int HT, int D, int HPG, int NB, int WB>
 MK_DEV bool op_attn(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
+  if constexpr (attn_tc_path<D, HPG, NB>())
+    if (g.tmaps && !g.kv_block) return op_attn_tc(c, g, I);
   constexpr int LPR = D / 8, SPW = 32 / LPR;
   const int slot = c.lane / LPR, dsl = c.lane % LPR;
   const int b = I.b, P = c.pos[b];
@@ -1000,34 +1128,7 @@ MK_DEV bool op_attn(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I
       }
     }
   }
-  consumer_bar();
-  for (int t = c.tid; t < HPG * D; t += NCT) {
-    const int h = t / D, dim = t % D;
-    float M = NEG_BIG;
-#pragma unroll
-    for (int w = 0; w < NCW; w++) M = fmaxf(M, sc[(w * HPG + h) * (D + 2) + D]);
-    float Ls = 0.f, O = 0.f;
-#pragma unroll
-    for (int w = 0; w < NCW; w++) {
-      const float* p = sc + (w * HPG + h) * (D + 2);
-      const float f = exp2f(p[D] - M);
-      Ls = fmaf(p[D + 1], f, Ls);
-      O = fmaf(p[dim], f, O);
-    }
-    const size_t po = ((((size_t)I.layer * g.B + b) * g.Hq + (size_t)I.g * HPG + h) * g.splits +
-                       I.r0) * part_stride(D);
-    if (MK_IN(g, po + D + 2 <= g.n_part, c.pc, I.op)) {
-      float* dst = g.part + po;
-      dst[dim] = O;
-      if (dim == 0) {
-        dst[D] = M;
-        dst[D + 1] = Ls;
-      }
-    }
-  }
-  consumer_bar();
-  if constexpr (NB > 8) return attn_merge_wide(c, g, I);
-  return true;
+  return attn_cta_merge(c, g, I);
 }
 
 // Residual input x_j[b][r] (j = 0: the embedding row of the token).
@@ -2206,10 +2307,24 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
                          copy_src(g, I, s[k].src2 + (size_t)(u0 + j) * u2, u2, pc), u2, full,
                          pol_kv);
             }
+          } else if (attn_tc_path<D, HPG, NB>() && g.tmaps && I.op == OP_ATTN && !g.kv_block) {
+            // tensor-core attention: the K and V rows as tiled TMA boxes of
+            // 64 rows in the 128-byte swizzle (the box past the item's last
+            // row loads neighbouring rows, or zeros past the cache's end)
+            const uint32_t nbox = (n + 63u) / 64u;
+            mbar_expect_tx(full, 2u * nbox * 8192u);
+            const LayerPtrs* Lp = g.layers + I.layer;
+            const int row = (int)((s[k].src - (const unsigned char*)Lp->kc) / 128) + (int)u0;
+            const unsigned char* tm = (const unsigned char*)g.tmaps + (size_t)I.layer * 256;
+            for (uint32_t x = 0; x < nbox; x++) {
+              tma_load_2d(dst + 8192u * x, tm, 0, row + 64 * (int)x, full, pol_kv);
+              tma_load_2d(dst + (uint32_t)g.stage_bytes / 2 + 8192u * x, tm + 128, 0,
+                          row + 64 * (int)x, full, pol_kv);
+            }
           } else {
             mbar_expect_tx(full, s[k].src2 ? 2u * bytes : bytes);
           }
-          if (wseg) {
+          if (wseg || (attn_tc_path<D, HPG, NB>() && g.tmaps && I.op == OP_ATTN && !g.kv_block)) {
             // issued above
           } else if (s[k].cfill()) {
             // the consumers copy this stage in after their dependency wait

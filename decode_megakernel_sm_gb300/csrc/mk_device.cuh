@@ -22,10 +22,20 @@ namespace mk {
 
 MK_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+// Start value of a running softmax maximum (finite, so that max - start
+// never forms inf - inf).
+constexpr float NEG_BIG = -1e30f;
+
 MK_DEV uint64_t gtimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// Generic-proxy shared-memory stores ordered before later async-proxy
+// accesses of the same bytes (tensor-core operand reads, bulk-copy writes).
+MK_DEV void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 MK_DEV void mbar_init(uint32_t bar, uint32_t count) {

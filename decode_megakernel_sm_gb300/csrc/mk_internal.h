@@ -299,6 +299,9 @@ struct Globals {
   unsigned char* act;      // (then a fourth, [Hq][2 Bp][64]: the merged attention outputs)
   int Bp;                  // batch rounded up to 8 (the operand holds 2 Bp rows)
   uint32_t arr_ctr;        // first of the [L][B][Hkv] attention-arrival counters
+  // batched variants: [L][K, V] tensor maps (128 bytes each) of the contiguous
+  // K / V caches for the tensor-core attention; nullptr: the CUDA-core body
+  const void* tmaps;
 };
 
 // Shared-memory layout (bytes from the dynamic shared memory base).

@@ -82,11 +82,6 @@ MK_DEV void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Generic-proxy shared-memory stores made visible to the tensor core's reads.
-MK_DEV void fence_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Sixteen consecutive f32 columns of this thread's tensor-memory lane: warp w
 // of a warpgroup reads lanes 32 (w % 4) .. + 31, so taddr carries that lane
 // base in its upper half.  The load and its wait sit in one asm statement, so
