@@ -17,6 +17,7 @@
 // head, NB batch capacity of the compiled variant (rows b >= B are masked).
 #pragma once
 #include "attn_tc.cuh"
+#include "mk_tc.cuh"
 #include "mk_device.cuh"
 
 namespace mk {
@@ -873,6 +874,21 @@ MK_DEV bool attn_cta_merge(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const I
       const float f = exp2f(p[D] - M);
       Ls = fmaf(p[D + 1], f, Ls);
       O = fmaf(p[dim], f, O);
+    }
+    if constexpr (NB > 8) {
+      if (g.splits == 1) {
+        // wide batch, one slice per (sequence, kv head): the item's output
+        // goes straight into the O-projection's operand (bf16 high part and
+        // remainder, rows 2b, 2b + 1 of the head's chunk)
+        const uint32_t ab = 2u * (uint32_t)g.Bp * 128u;
+        const uint32_t col = (uint32_t)((I.g * HPG + h) * D + dim);
+        unsigned char* out = g.act + 3 * (size_t)(HT / WIDE_KC) * ab + (size_t)(col / WIDE_KC) * ab;
+        const float x = O / Ls;
+        const uint16_t hi = to_bf16(x), lo = to_bf16(x - bf1(hi));
+        *(uint16_t*)(out + sw128_off(2u * b, col % WIDE_KC)) = hi;
+        *(uint16_t*)(out + sw128_off(2u * b + 1u, col % WIDE_KC)) = lo;
+        continue;
+      }
     }
     const size_t po = ((((size_t)I.layer * g.B + b) * g.Hq + (size_t)I.g * HPG + h) * g.splits +
                        I.r0) * part_stride(D);

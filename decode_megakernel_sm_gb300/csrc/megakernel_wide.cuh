@@ -269,6 +269,7 @@ template <int HT, int D, int HPG, int NB, int WB>
 MK_DEV bool attn_merge_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Instr& I) {
   const int b = I.b, S = (int)I.r1;
   constexpr int PS = part_stride(D);
+  if (S == 1) return true;  // (a whole-sequence item wrote its outputs itself: attn_cta_merge)
   if (c.tid == 0) {
     uint32_t* arr = g.ctr + g.arr_ctr + ((size_t)I.layer * g.B + b) * g.Hkv + I.g;
     const uint32_t old = atom_add_acq_rel(arr, 1u);
