@@ -126,12 +126,13 @@ static int plan_build_wide(const mk_model_desc& d, int B, int max_ctx, int n_sm,
   const long R = (long)Hkv * GR;
   const int Bp = wide_bp(B);
   CtrMap cm{Hkv, L};
-  // split-KV: whole sequences when there are at least as many (sequence, kv
-  // head) pairs as SMs (no merge, no arrival count); otherwise about three
-  // items per SM (at least 16 positions per slice at max_ctx).  Items are
-  // dealt out slice-major and round-robin, so that each SM's items come from
-  // different sequences and their lengths average out.
-  int S = B * Hkv >= n_sm ? 1 : std::max(2, (3 * n_sm + B * Hkv - 1) / (B * Hkv));
+  // split-KV: whole sequences once the (sequence, kv head) pairs number a
+  // quarter of the SMs or more (no merge, no arrival count: on the tensor
+  // cores a whole 2K-position sequence is a few microseconds, less than the
+  // merge costs); otherwise about three items per SM (at least 16 positions
+  // per slice at max_ctx).  Items are dealt out slice-major and round-robin,
+  // so that each SM's items come from different sequences.
+  int S = 4 * B * Hkv >= n_sm ? 1 : std::max(2, (3 * n_sm + B * Hkv - 1) / (B * Hkv));
   S = std::min(S, std::max(1, max_ctx / 16));
   const int n_items = B * Hkv * S;
   std::vector<std::vector<Instr>> qs(n_sm);
