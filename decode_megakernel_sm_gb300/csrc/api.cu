@@ -198,6 +198,7 @@ static const Variant* pick_variant(const mk_model_desc& d, int wb) {
   for (const Variant* v : all) {
     if (v->H != d.hidden || v->D != d.head_dim || v->HPG != HPG || v->WB != wb) continue;
     if (v->NB < d.max_batch) continue;
+    if (wide_path(d) != (v->NB == WIDE_NB)) continue;  // the wide variant exactly on its path
     if (!best || v->NB < best->NB) best = v;
   }
   if (best && d.n_experts > 0 && best->NB != 1) return nullptr;  // MoE routing is per token
@@ -337,11 +338,12 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
   if (wfmt == MK_WEIGHTS_INT8 && (!mlp_split(d) || d.ffn % 16 || d.head_dim != 64))
     return MK_ERR_UNSUPPORTED;
   h->wfmt = wfmt;
-  // wide batch (9 .. 32 sequences): dense FFN in whole 64-column chunks,
-  // 64-dim heads, bf16 weights
+  // wide batch (8 .. 32 sequences, see wide_path): dense FFN in whole
+  // 64-column chunks, 64-dim heads, bf16 weights
   if (d.max_batch > 8 && (d.n_experts > 0 || d.max_batch > WIDE_NB || d.ffn % WIDE_KC ||
-                          d.hidden % WIDE_KC || d.head_dim != WIDE_KC || wfmt != MK_WEIGHTS_BF16))
+                          d.hidden % WIDE_KC || d.head_dim != WIDE_KC))
     return MK_ERR_UNSUPPORTED;
+  if (wide_path(d) && wfmt != MK_WEIGHTS_BF16) return MK_ERR_UNSUPPORTED;
   h->var = pick_variant(d, wfmt == MK_WEIGHTS_INT8 ? 1 : 2);
   if (!h->var) return MK_ERR_UNSUPPORTED;
   const int L = d.n_layers, D = d.head_dim;

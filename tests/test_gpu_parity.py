@@ -125,11 +125,12 @@ def _bsplit_cfg(batch):
                         rope_theta=5e5)
 
 
-@pytest.mark.parametrize("batch", [8, 5])
+@pytest.mark.parametrize("batch", [7, 5])
 def test_batched_split_mlp(batch):
-    # batch > 1 with an FFN of whole 512-column chunks: gate/up slices write h
-    # as tensor-core fragments, 16-row down units stream them next to their
-    # weights (batch 5: padded rows)
+    # batch 2..7 with an FFN of whole 512-column chunks (the batch-8 variant;
+    # at 8 sequences the wide one takes over): gate/up slices write h as
+    # tensor-core fragments, 16-row down units stream them next to their
+    # weights (padded rows past the batch)
     run_steps(_bsplit_cfg(batch), 3, seed=17)
 
 
@@ -137,19 +138,19 @@ def test_batched_split_mlp(batch):
 def test_batched_split_mlp_stage_sizes(sb):
     # 48 KiB: one weight unit + its fragments per stage (8 KB idle per
     # half); 64 KiB: two of each
-    run_steps(_bsplit_cfg(8), 3, seed=19, stage_bytes=sb)
+    run_steps(_bsplit_cfg(7), 3, seed=19, stage_bytes=sb)
 
 
 def test_batched_split_mlp_16k_stages():
     # one 16 KB down unit per stage
-    run_steps(_bsplit_cfg(8), 3, seed=2, stage_bytes=16384)
+    run_steps(_bsplit_cfg(7), 3, seed=2, stage_bytes=16384)
 
 
 def test_batched_split_mlp_ragged_ffn_chunks():
     # FFN of 3 chunks of 512 and a short vocabulary: down runs that start and
     # end inside chunks, two-chunk runs, and every SM's share under one chunk
     cfg = synth.custom(n_layers=2, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=64,
-                       ffn=1536, vocab=3000, batch=8, prefill=(5, 400), steps=3, rope_theta=5e5)
+                       ffn=1536, vocab=3000, batch=6, prefill=(5, 400), steps=3, rope_theta=5e5)
     run_steps(cfg, 3, seed=29)
 
 

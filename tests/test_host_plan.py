@@ -135,7 +135,10 @@ def test_plan_covers_all_work_and_is_deadlock_free(name, n_sm):
     cfg, d = desc(name)
     st, q = L.mk_plan(d, cfg["batch"], cfg["max_seq"], n_sm)
     assert st["n_sm"] == n_sm
-    independent_coverage(cfg, q, n_sm, st["max_pc"], st["attn_splits"])
+    if is_wide(cfg):
+        wide_coverage(cfg, q, n_sm, st["max_pc"], st["attn_splits"])
+    else:
+        independent_coverage(cfg, q, n_sm, st["max_pc"], st["attn_splits"])
     assert L.mk_plan_check(q, n_sm, st["max_pc"], st["n_counters"]) == L.MK_OK
 
 
@@ -236,7 +239,8 @@ def test_checker_rejects_plain_wait_on_relaxed_signals():
 
 
 def test_batched_split_mlp_cuts_whole_tiles():
-    cfg, d = desc("llama1b_b8")
+    # 7 sequences: the batch-8 variant (at 8 the wide variant takes this shape)
+    cfg, d = desc("llama1b_b8", batch=7)
     st, q = L.mk_plan(d, cfg["batch"], cfg["max_seq"], 152)
     ops = [q[i] for i in range(152 * st["max_pc"]) if q[i].op in (8, 9)]
     assert all(I.r0 % 16 == 0 and I.r1 % 16 == 0 for I in ops if I.op == 8)
@@ -293,6 +297,13 @@ def test_quantize_rows_refuses_bad_arguments():
     assert lib.mk_quantize_rows_int8(None, 4, 8, p, p, None) == L.MK_ERR_INVALID_ARG
     assert lib.mk_quantize_rows_int8(p, 4, 8, None, p, None) == L.MK_ERR_INVALID_ARG
     assert lib.mk_quantize_rows_int8(p, 4, 8, p, None, None) == L.MK_ERR_INVALID_ARG
+
+
+def is_wide(cfg):
+    # the wide-batch (tcgen05) variant's plan: 9..32 sequences, or 8 on a shape it takes
+    b, dense = cfg["batch"], cfg["n_experts"] == 0
+    return dense and (b > 8 or (b == 8 and cfg["ffn"] % 64 == 0 and cfg["hidden"] % 64 == 0 and
+                                cfg["head_dim"] == 64 and cfg["n_q_heads"] == 4 * cfg["n_kv_heads"]))
 
 
 def wide_coverage(cfg, q, n_sm, max_pc, splits):
