@@ -1075,6 +1075,7 @@ extern "C" int mk_decode_step_noalloc(mk_handle* h, const int32_t* d_tokens,
   g.hglob = sc.hglob;
   g.routes = sc.routes;    // MoE routing of this call, in the array as well
   g.rweight = sc.rweight;
+  g.act = sc.act;          // wide batch: the tensor-core operands, likewise
   g.sc_lo = (const unsigned char*)base;
   g.sc_bytes = need;
   // the array keeps the previous call's contents: clear what must start at

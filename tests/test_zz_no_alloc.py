@@ -9,9 +9,11 @@ These tests call it through the C ABI on the same inputs as mk_decode_step,
 two calls in a row, and hold both results to the parity tests' tolerance:
 the no-allocation logits against the regular step's and against the oracle
 teacher-forced on the same tokens.  The shapes cover batch 1 (small and
-Llama-1B), a small MoE (its routing lives in the fixed array too) and a
-batch-8 shape with the batched MLP.  This file is collected last so that a
-run stopping at the first failure has already run every other test.
+Llama-1B), a small MoE (its routing lives in the fixed array too), 5
+sequences on the batched variant (h as tensor-core fragments) and 8 on the
+wide tcgen05 variant (its operand buffers and attention arrival counters
+live in the fixed array too).  This file is collected last so that a run
+stopping at the first failure has already run every other test.
 """
 import ctypes as C
 
@@ -33,7 +35,11 @@ CASES = {
                               ffn=0, vocab=3001, tied=False, n_experts=16, top_k=4,
                               expert_ffn=200, shared_ffn=500, rope_theta=5e5, prefill=(70, 70),
                               steps=4),
-    # eight sequences, ragged lengths, the batched split MLP (h as fragments)
+    # five sequences, ragged lengths, the batched split MLP (h as fragments)
+    "batch5": synth.custom(n_layers=2, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=64,
+                           ffn=2048, vocab=5000, batch=5, prefill=(0, 300), steps=4,
+                           rope_theta=5e5),
+    # eight sequences: the wide tcgen05 variant
     "batch8": synth.custom(n_layers=2, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=64,
                            ffn=2048, vocab=5000, batch=8, prefill=(0, 300), steps=4,
                            rope_theta=5e5),
