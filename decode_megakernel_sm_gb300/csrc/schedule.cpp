@@ -126,13 +126,16 @@ static int plan_build_wide(const mk_model_desc& d, int B, int max_ctx, int n_sm,
   const long R = (long)Hkv * GR;
   const int Bp = wide_bp(B);
   CtrMap cm{Hkv, L};
-  // split-KV: whole sequences once the (sequence, kv head) pairs number a
-  // quarter of the SMs or more (no merge, no arrival count: on the tensor
-  // cores a whole 2K-position sequence is a few microseconds, less than the
-  // merge costs); otherwise about three items per SM (at least 16 positions
-  // per slice at max_ctx).  Items are dealt out slice-major and round-robin,
-  // so that each SM's items come from different sequences.
-  int S = 4 * B * Hkv >= n_sm ? 1 : std::max(2, (3 * n_sm + B * Hkv - 1) / (B * Hkv));
+  // split-KV: whole sequences once the (sequence, kv head) pairs number half
+  // the SMs or more (no merge, no arrival count: on the tensor cores a whole
+  // 2K-position sequence costs less than the merge); below that, enough
+  // slices for the items to fill about half the SMs, at least two (measured
+  // at 8 sequences x 8 kv heads: 1, 2, 3 slices give 1.074, 1.037, 1.121 ms
+  // per step; at 16 and 32 sequences one slice is best), and at least 16
+  // positions per slice at max_ctx.  Items are dealt out slice-major and
+  // round-robin, so that each SM's items come from different sequences.
+  const int pairs = B * Hkv;
+  int S = 2 * pairs >= n_sm ? 1 : std::max(2, n_sm / (2 * pairs));
   S = std::min(S, std::max(1, max_ctx / 16));
   const int n_items = B * Hkv * S;
   std::vector<std::vector<Instr>> qs(n_sm);

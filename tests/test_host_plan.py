@@ -389,8 +389,8 @@ def wide_coverage(cfg, q, n_sm, max_pc, splits):
 def test_wide_plan_covers_all_work_and_is_deadlock_free(batch, n_sm):
     cfg, d = desc("llama1b_b8", batch=batch)
     st, q = L.mk_plan(d, batch, cfg["max_seq"], n_sm)
-    # whole sequences once the (sequence, kv head) pairs number a quarter of the SMs
-    assert (st["attn_splits"] == 1) == (4 * batch * cfg["n_kv_heads"] >= n_sm)
+    # whole sequences once the (sequence, kv head) pairs number half the SMs
+    assert (st["attn_splits"] == 1) == (2 * batch * cfg["n_kv_heads"] >= n_sm)
     wide_coverage(cfg, q, n_sm, st["max_pc"], st["attn_splits"])
     assert st["n_lm"] == min(n_sm, cfg["vocab"] // 8)
     assert L.mk_plan_check(q, n_sm, st["max_pc"], st["n_counters"]) == L.MK_OK
