@@ -376,6 +376,7 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
   // int8 weights: a 4-stage ring by default (fewer copies in flight shorten
   // the dependency hops; half the bytes per row keep the bodies fed)
   if (wfmt == MK_WEIGHTS_INT8) h->max_stages = 4;
+  if (h->var->NB > 8) h->stage_bytes = WIDE_STAGE_BYTES;
   // ---- device
   CK(cudaGetDevice(&h->dev));
   CK(cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, h->dev));

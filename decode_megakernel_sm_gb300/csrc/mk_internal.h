@@ -126,6 +126,11 @@ constexpr int NTHREADS = NCT + 32;   // + one producer warp
 constexpr int STAGE_UNIT = 16384;
 constexpr int MAX_STAGE_BYTES = 65536;
 constexpr int DEFAULT_STAGE_BYTES = 32768;
+// The wide-batch variant's default: its consumer issues a tensor-core MMA per
+// 16-deep K step of a chunk plus a commit per stage, and bigger stages hold
+// more chunks per stage and per ring (a 128-row chunk with its operand takes
+// 18-24 KB, so 32 KB stages leave a quarter to half of each unused).
+constexpr int WIDE_STAGE_BYTES = 65536;
 constexpr int MAX_STAGES = 16;
 constexpr int DOWN_ROW_MAX = 16384;  // bytes of one down row (F <= 8192) in the split MLP
 constexpr int MAX_ROWS = 256;        // rows of one QKV / gate-up / router instruction

@@ -11,7 +11,7 @@ one attention item per (sequence, kv head) (pairs at least half the SMs) and
 split-KV slices merged by the last arriver (fewer pairs),
 an FFN with an odd number of 64-column chunks and a vocabulary that is not a
 multiple of 8 (the LM head's last instruction reads zero-padded rows), ring
-stages of 48 and 64 KB (16 KB is refused), several steps per launch, the multi-launch ablation,
+stages of 32, 48 and 64 KB (the default; 16 KB is refused), several steps per launch, the multi-launch ablation,
 and the full Llama-1B shape at 32 sequences.
 """
 import numpy as np
@@ -60,7 +60,17 @@ def test_wide_ragged_ffn_vocab_and_batch():
     run_steps(cfg, 3, seed=7)
 
 
-@pytest.mark.parametrize("sb", [49152, 65536])
+def test_wide_default_stage_size():
+    # 64 KB stages unless the caller asks otherwise
+    r = Run(small(16), seed=5)
+    try:
+        info = r.dec.info()
+        assert info["stage_bytes"] == 65536 and info["n_stages"] >= 2
+    finally:
+        r.close()
+
+
+@pytest.mark.parametrize("sb", [32768, 49152])
 def test_wide_stage_sizes(sb):
     run_steps(small(24), 2, seed=sb % 97, stage_bytes=sb)
 
