@@ -8,7 +8,8 @@ maximum of its own logits, and the appended K/V rows within one bf16 ulp.
 The shapes cover batches that fill 8-sequence groups exactly (16, 32) and
 ones that do not (9, 13: zero operand rows up to the next multiple of 8),
 one attention item per (sequence, kv head) (pairs at least half the SMs) and
-split-KV slices merged by the last arriver (fewer pairs),
+split-KV slices merged by the last arriver (fewer pairs), cache lengths of
+0..2 rows (slices with no cached rows),
 an FFN with an odd number of 64-column chunks and a vocabulary that is not a
 multiple of 8 (the LM head's last instruction reads zero-padded rows), ring
 stages of 32, 48 and 64 KB (the default; 16 KB is refused), several steps per launch, the multi-launch ablation,
@@ -45,6 +46,13 @@ def run_steps(cfg, steps, seed=0, **kw):
 def test_wide_parity(batch):
     worst = run_steps(small(batch), 3, seed=batch)
     print(f"batch {batch} worst max|dlogit|/std = {worst:.2e}")
+
+
+def test_wide_short_sequences():
+    # cache lengths 0..2 with 4 slices per (sequence, kv head): most attention
+    # items have no cached rows (only the last slice's row P)
+    worst = run_steps(small(9, prefill=(0, 2)), 3, seed=11)
+    print(f"batch 9, lengths 0..2 worst max|dlogit|/std = {worst:.2e}")
 
 
 def test_wide_whole_sequence_attention_items():
