@@ -2421,7 +2421,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
       mbar_init(full0 + 8u * s, 1u);
       mbar_init(empty0 + 8u * s, (uint32_t)NCW);
     }
-    if constexpr (NB > 8) mbar_init(smem_u32(smem + Ls.tcw + 8), 1u);  // MMA done
+    if constexpr (NB > 8) mbar_init(smem_u32(smem + Ls.tcw + 8), (uint32_t)WIDE_NI);  // MMA done
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *flag = 0;
     misc[1] = 0;  // instructions the consumers have finished (read by the producer)
@@ -2469,15 +2469,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
   }
   consumer_steps(c, g, misc);
   if constexpr (NB > 8) {
-    // every exit: once the MMAs issued so far have completed (a commit with
-    // none outstanding arrives at once), warp 0 frees the tensor memory
+    // every exit: once the MMAs issued so far have completed (each issuing
+    // warp commits; a commit with none outstanding arrives at once), warp 0
+    // frees the tensor memory
     tc_fence_before();
     consumer_bar();
+    if (warp < WIDE_NI && lane == 0) tc_commit(c.mma_bar);
     if (warp == 0) {
-      if (lane == 0) {
-        tc_commit(c.mma_bar);
-        wait_mbar(g, c.mma_bar, c.mma_par, false);
-      }
+      if (lane == 0) wait_mbar(g, c.mma_bar, c.mma_par, false);
       __syncwarp();
       tc_fence_after();
       tmem_dealloc(c.tmem, (uint32_t)WIDE_TMEM_COLS);

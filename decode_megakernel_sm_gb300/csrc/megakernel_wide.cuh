@@ -48,35 +48,41 @@ MK_DEV bool wide_mma_wait(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g) {
   return ok;
 }
 
-// Stream a wide segment through the ring into the accumulator at column 0:
-// chunk by chunk, D (+)= W_chunk (128 rows from the weight piece) x
-// operand_chunk^T.  Rows past the piece's own read the bytes that follow it
-// (the rest of the stage, or the shared memory after the ring); their
-// outputs are never read.  All consumer warps call; false (on every thread)
-// if a ring wait gave up.
+// Stream a wide segment through the ring into the accumulators: chunk by
+// chunk, D_w (+)= W_chunk (128 rows from the weight piece) x operand_chunk^T,
+// where consumer warp w < WIDE_NI issues (lane 0) the MMAs of chunks i with
+// i % WIDE_NI == w into its own accumulator at column 64 w and releases each
+// stage with a commit once its MMAs have read it; wide_tile_out sums the
+// accumulators.  Rows past the piece's own read the bytes that follow it (the
+// rest of the stage, or the shared memory after the ring); their outputs are
+// never read.  All consumer warps call; false (on every thread) if a ring
+// wait gave up.
 template <int HT, int D, int HPG, int NB, int WB>
 MK_DEV bool wide_mma_stream(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Seg& s) {
   const uint32_t N = s.unit2() / 128u;
   const uint32_t idesc = idesc_bf16(128, (int)N);
-  bool bad = false, first = true;
+  const uint32_t NI = (uint32_t)WIDE_NI;
+  bool bad = false, first = true;  // first: this warp's accumulator not written yet
   for (uint32_t u0 = 0; u0 < s.n; u0 += s.ups) {
     uint32_t n = min(s.ups, s.n - u0);
     if (!MK_IN(g, n * (s.unit + s.unit2()) <= (uint32_t)g.stage_bytes, c.pc, -1)) n = 0;
     if (!bad && !c.ring.acquire(g)) bad = true;
     if (bad) continue;
-    if (c.warp == 0) {
+    if ((uint32_t)c.warp < NI) {
+      // warp w: the stage's chunks u0 + j with (u0 + j) % NI == w
       if (c.lane == 0) {
         tc_fence_after();
         const uint32_t sb = smem_u32(c.ring.stage_ptr());
-        for (uint32_t j = 0; j < n; j++) {
+        const uint32_t acc = c.tmem + 64u * (uint32_t)c.warp;
+        for (uint32_t j = ((uint32_t)c.warp + NI - u0 % NI) % NI; j < n; j += NI) {
           const uint32_t wa = sb + j * s.unit, aa = sb + s.ups * s.unit + j * s.unit2();
 #pragma unroll
           for (uint32_t k = 0; k < 4; k++)
-            tc_mma_bf16(c.tmem, sw128_desc(wa + 32u * k), sw128_desc(aa + 32u * k), idesc,
+            tc_mma_bf16(acc, sw128_desc(wa + 32u * k), sw128_desc(aa + 32u * k), idesc,
                         !first || k > 0);
           first = false;
         }
-        tc_commit(c.ring.empty_bar());  // warp 0's arrival, once the MMAs have read the stage
+        tc_commit(c.ring.empty_bar());  // the warp's arrival, once its MMAs have read the stage
       }
       __syncwarp();
       c.ring.advance();
@@ -87,23 +93,33 @@ MK_DEV bool wide_mma_stream(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const 
   if (bad) c.flag[2] = 1;
   consumer_bar();
   if (c.flag[2]) return false;
-  if (c.tid == 0) tc_commit(c.mma_bar);
+  if ((uint32_t)c.warp < NI && c.lane == 0) tc_commit(c.mma_bar);  // WIDE_NI arrivals
   return wide_mma_wait(c, g);
 }
 
-// Read the accumulator back (128 weight rows, N = 2 Bp columns) into
-// yrow[b][m], b < Bp, m < 128: consumer warp w < 4 reads lanes 32 w ..
-// 32 w + 31 and adds each sequence's high and low columns.  Ends with the
+// Accumulators a segment writes: one per issuing warp that has a chunk.
+MK_DEV uint32_t wide_nacc(const Seg& s) { return min((uint32_t)WIDE_NI, s.n); }
+
+// Read the accumulators back (128 weight rows, N = 2 Bp columns each; nacc
+// of them written, wide_nacc) into yrow[b][m], b < Bp, m < 128: consumer warp
+// w < 4 reads lanes 32 w .. 32 w + 31, sums the accumulators and adds each
+// sequence's high and low columns.  Ends with the
 // tensor-memory reads ordered before a CTA barrier, after which yrow is
 // complete (and the next MMAs may overwrite the accumulator).
 template <int HT, int D, int HPG, int NB, int WB>
-MK_DEV void wide_tile_out(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, uint32_t N) {
+MK_DEV void wide_tile_out(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, uint32_t N, uint32_t nacc) {
   static_assert(NB <= 32, "64 accumulator columns per tile");
   if (c.warp < 4) {
     float* y = c.yrow + 32 * c.warp + c.lane;
     for (uint32_t q = 0; 16u * q < N; q++) {  // 16 columns: sequences 8q .. 8q + 7
-      float v[16];
-      tmem_ld16(c.tmem + ((uint32_t)(32 * c.warp) << 16) + 16u * q, v);
+      float v[16], w[16];
+      const uint32_t ta = c.tmem + ((uint32_t)(32 * c.warp) << 16) + 16u * q;
+      tmem_ld16(ta, v);
+      for (uint32_t a = 1; a < nacc; a++) {  // the other issuers' accumulators
+        tmem_ld16(ta + 64u * a, w);
+#pragma unroll
+        for (int e = 0; e < 16; e++) v[e] += w[e];
+      }
 #pragma unroll
       for (int e = 0; e < 8; e++) y[(8 * q + e) * WIDE_ROWS] = v[2 * e] + v[2 * e + 1];
     }
@@ -196,7 +212,7 @@ MK_DEV bool op_qkv_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const Inst
   c.mark(g, 1);
   const uint32_t n = I.r1 - I.r0;
   float* yrow = c.yrow;  // [NB][WIDE_ROWS]
-  wide_tile_out(c, g, s[0].unit2() / 128u);
+  wide_tile_out(c, g, s[0].unit2() / 128u, wide_nacc(s[0]));
   constexpr int GR = (HPG + 2) * D;
   const int np = (int)n / 2;
   for (int it = c.tid; it < np * g.B; it += NCT) {
@@ -320,7 +336,7 @@ MK_DEV bool op_oproj_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const In
   get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
   if (!wide_mma_stream(c, g, s[0])) return false;
   c.mark(g, 1);
-  wide_tile_out(c, g, s[0].unit2() / 128u);
+  wide_tile_out(c, g, s[0].unit2() / 128u, wide_nacc(s[0]));
   wide_residual_add(c, g, I, 2 * l, 2 * l + 1, (I.flags & F_RESIDUAL) != 0);
   return true;
 }
@@ -339,7 +355,7 @@ MK_DEV bool op_mlp_up_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const I
   c.mark(g, 1);
   const int ncol = (int)(I.r1 - I.r0);
   float* yrow = c.yrow;  // [NB][WIDE_ROWS]
-  wide_tile_out(c, g, s[0].unit2() / 128u);
+  wide_tile_out(c, g, s[0].unit2() / 128u, wide_nacc(s[0]));
   const uint32_t ab = 2u * (uint32_t)g.Bp * 128u;
   unsigned char* hb = (unsigned char*)g.hglob;
   for (int it = c.tid; it < ncol * g.Bp; it += NCT) {
@@ -371,7 +387,7 @@ MK_DEV bool op_mlp_down_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const
   get_segs<HT, D, WB, NB>(g, I, c.pos, c.topk, s);
   if (!wide_mma_stream(c, g, s[0])) return false;
   c.mark(g, 1);
-  wide_tile_out(c, g, s[0].unit2() / 128u);
+  wide_tile_out(c, g, s[0].unit2() / 128u, wide_nacc(s[0]));
   wide_residual_add(c, g, I, 2 * l + 1, 2 * l + 2, I.b == 0);
   return true;
 }
@@ -402,7 +418,7 @@ MK_DEV bool op_lmhead_wide(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g, const I
   c.mark(g, 1);
   const int n = (int)(I.r1 - I.r0), B = g.B, V = g.V;
   float* yrow = c.yrow;  // [NB][WIDE_ROWS]
-  wide_tile_out(c, g, s[0].unit2() / 128u);
+  wide_tile_out(c, g, s[0].unit2() / 128u, wide_nacc(s[0]));
   for (int it = c.tid; it < B * n; it += NCT) {
     const int b = it / n, m = it % n;
     const int row = (int)I.r0 + m;

@@ -180,7 +180,16 @@ constexpr int MMA_FLUSH = 32;        // batched GEMV: rows per cross-warp sum of
 constexpr int WIDE_NB = 32;          // batch capacity of the wide variant
 constexpr int WIDE_KC = 64;          // columns of one K chunk (a 128-byte row of bf16)
 constexpr int WIDE_ROWS = 128;       // weight rows of one instruction (the MMA's M)
-constexpr int WIDE_TMEM_COLS = 64;   // tensor-memory columns a CTA allocates (N <= 2 * 32)
+// Consumer warps 0 .. WIDE_NI - 1 each issue the MMAs of every WIDE_NI-th K
+// chunk into an accumulator of their own (64 columns apart): one thread
+// issues a tcgen05.mma about every 40 ns whatever its shape, so the issue
+// rate, not the tensor pipe, bounds a GEMV with a handful of operand rows
+// (measured at 8 / 16 / 32 sequences, 1 / 2 / 4 / 7 issuers: 0.993 / 0.952 /
+// 0.937 / 0.938, 1.111 / 1.076 / 1.053 / 1.061, 1.451 / 1.404 / 1.397 /
+// 1.408 ms per step).
+constexpr int WIDE_NI = 4;
+// tensor-memory columns a CTA allocates (a power of two >= 32)
+constexpr int WIDE_TMEM_COLS = WIDE_NI <= 1 ? 64 : WIDE_NI <= 2 ? 128 : WIDE_NI <= 4 ? 256 : 512;
 // Used from 9 sequences on, and at 8 when the shape allows it (measured: at
 // 8 sequences the wide variant's step is 7 % shorter than the batched one's).
 MK_HD inline bool wide_path(const mk_model_desc& d) {
