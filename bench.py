@@ -72,6 +72,9 @@ def parse():
                     help="at most this many ring stages (library default if unset)")
     ap.add_argument("--hold-early", type=int, default=128 << 10,
                     help="bytes of a held instruction's copies issued early (with --hold)")
+    ap.add_argument("--batched-variant", type=int, default=0, choices=[0, 1],
+                    help="2..8 sequences: 0 the tcgen05 wide-batch kernel where the shape allows "
+                         "it (default), 1 the warp-level mma.sync batched kernel")
     ap.add_argument("--stage-bytes", type=int, default=None,
                     help="ring stage size in bytes (default: the library's)")
     ap.add_argument("--trace", default=None,
@@ -302,6 +305,8 @@ def main():
         cfg = dict(cfg, int8=True)
     if args.batch is not None:
         cfg = dict(cfg, batch=args.batch)
+    if args.batched_variant:
+        cfg = dict(cfg, batched_variant=1)
     if args.impl == "reference":
         run_reference(args, cfg)
         return
@@ -432,6 +437,7 @@ def main():
     traffic, traffic_how = traffic_record(
         args.config + ("+int8" if args.weights == "int8" else "") +
         (f"+b{B}" if args.batch is not None else "") +
+        ("+mma" if args.batched_variant else "") +
         (f"+paged{args.paged}" if args.paged else ""), spl)
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_how,
@@ -454,7 +460,8 @@ def main():
         "gpu_launches": args.steps // ns if ns else args.steps, "roofline": roof, "clocks": ck,
         "kernel": {"n_sm": info["n_sm"], "ring_stages": info["n_stages"],
                    "stage_bytes": info["stage_bytes"], "instructions": info["n_instr"],
-                   "attn_splits": info["attn_splits"]},
+                   "attn_splits": info["attn_splits"],
+                   "batched_variant": int(cfg.get("batched_variant", 0))},
     }
 
     if args.ablation:

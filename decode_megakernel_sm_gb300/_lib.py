@@ -32,7 +32,8 @@ class mk_model_desc(C.Structure):
                                         "head_dim", "ffn", "vocab")] + \
                [("rms_eps", C.c_float), ("rope_theta", C.c_float)] + \
                [(n, C.c_int) for n in ("tied_lm_head", "n_experts", "top_k", "expert_ffn",
-                                        "shared_ffn", "max_batch", "max_seq")]
+                                        "shared_ffn", "max_batch", "max_seq",
+                                        "batched_variant")]
 
 
 WEIGHT_LISTS = ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down",

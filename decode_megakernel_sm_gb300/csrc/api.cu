@@ -338,7 +338,7 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
   if (wfmt == MK_WEIGHTS_INT8 && (!mlp_split(d) || d.ffn % 16 || d.head_dim != 64))
     return MK_ERR_UNSUPPORTED;
   h->wfmt = wfmt;
-  // wide batch (8 .. 32 sequences, see wide_path): dense FFN in whole
+  // wide batch (2 .. 32 sequences, see wide_path): dense FFN in whole
   // 64-column chunks, 64-dim heads, bf16 weights
   if (d.max_batch > 8 && (d.n_experts > 0 || d.max_batch > WIDE_NB || d.ffn % WIDE_KC ||
                           d.hidden % WIDE_KC || d.head_dim != WIDE_KC))

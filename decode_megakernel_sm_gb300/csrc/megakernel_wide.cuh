@@ -1,8 +1,9 @@
-// megakernel_wide.cuh -- op bodies of the wide-batch variant (9 .. 32
-// sequences), included by megakernel.cuh.
+// megakernel_wide.cuh -- op bodies of the wide-batch variant (2 .. 32
+// sequences on the shapes it takes, see wide_path), included by
+// megakernel.cuh.
 //
-// Every contraction runs on the fifth-generation tensor cores: one elected
-// thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> f32) with A = 128
+// Every contraction runs on the fifth-generation tensor cores: elected
+// threads issue tcgen05.mma (kind::f16, bf16 x bf16 -> f32) with A = 128
 // weight rows of a ring stage and B = the activation operand, 2 Bp rows: the
 // bf16 high part of sequence b's activation in row 2b and the bf16 remainder
 // in row 2b + 1, so that the two products together keep about 16 mantissa

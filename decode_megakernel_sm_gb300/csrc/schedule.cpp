@@ -32,6 +32,7 @@ int plan_shape_ok(const mk_model_desc& d) {
   if (d.n_experts < 0 || d.top_k < 0 || d.expert_ffn < 0 || d.shared_ffn < 0 || d.ffn < 0)
     return MK_ERR_INVALID_ARG;
   if (d.n_experts == 0 && d.ffn <= 0) return MK_ERR_INVALID_ARG;
+  if (d.batched_variant != 0 && d.batched_variant != 1) return MK_ERR_INVALID_ARG;
   if (d.n_experts > 0 && (d.top_k <= 0 || d.top_k > d.n_experts || d.expert_ffn <= 0))
     return MK_ERR_INVALID_ARG;
   if (d.hidden % 256 || d.hidden > 16384) return MK_ERR_UNSUPPORTED;
@@ -105,7 +106,7 @@ static void finish_plan(std::vector<std::vector<Instr>>& qs, const std::vector<d
 }
 
 // ---------------------------------------------------------- wide batch ----
-// 9 .. 32 sequences ("Megakernels in LLM Inference When Fusion Actually
+// 2 .. 32 sequences on the shapes of wide_path ("Megakernels in LLM Inference When Fusion Actually
 // Wins", sections "Core Tradeoff" and "When Megakernels Win": the batch range
 // where one fused launch meets skinny GEMMs).  Per layer:
 //   NORM (attention input) -> QKV rows -> attention items -> O-proj rows ->

@@ -19,6 +19,7 @@ def desc_from_config(cfg: dict, max_batch: int, max_seq: int) -> L.mk_model_desc
     d.tied_lm_head = 1 if cfg.get("tied", True) else 0
     d.max_batch = int(max_batch)
     d.max_seq = int(max_seq)
+    d.batched_variant = int(cfg.get("batched_variant", 0))
     return d
 
 

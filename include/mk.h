@@ -47,13 +47,21 @@ typedef struct mk_handle mk_handle;
  * per token, plus an always-on shared expert of width shared_ffn (0: none).
  * "Gemma 4 TPU megakernel", section "Megakernels for Gemma 4", lists the
  * router / experts / shared MLP components of that MoE step.  Supported:
- * n_experts <= 256, top_k <= 16 (MK_ERR_UNSUPPORTED otherwise).          */
+ * n_experts <= 256, top_k <= 16 (MK_ERR_UNSUPPORTED otherwise).
+ * batched_variant picks the kernel for max_batch 2..8 on a dense shape with
+ * 64-dim heads, four query heads per kv head and hidden / ffn multiples of
+ * 64: 0 (default) the wide-batch variant (every contraction on tcgen05 with
+ * tensor-memory accumulators; measured 13-20 % faster per step at 2, 4 and
+ * 7 sequences), 1 the batched variant (warp-level mma.sync).  Other shapes
+ * and max_batch 9..32 ignore it (the wide-batch variant).  "Megakernels in LLM Inference When Fusion
+ * Actually Wins", section "Core Tradeoff", frames the batch ranges.        */
 typedef struct {
   int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
   float rms_eps, rope_theta;
   int tied_lm_head;                 /* 1: the LM head is the embedding matrix */
   int n_experts, top_k, expert_ffn, shared_ffn;
   int max_batch, max_seq;           /* KV cache capacity (rows per kv head)   */
+  int batched_variant;              /* 2..8 sequences: 0 tcgen05, 1 mma.sync  */
 } mk_model_desc;
 
 /* Weight pointers (device, bf16).  Per-layer fields are HOST arrays of
@@ -111,13 +119,14 @@ typedef struct {
  * here a bulk-copy ring, which is why every matrix is re-laid out).
  * Ownership: the caller keeps its weights (read only during the call) and
  * its KV cache (must outlive the handle); the library owns the packed copy.
- * Batch capacity: max_batch 1 (the batch-1 variants), 2..8 (the batched
- * variant) or 9..32 (the wide-batch variant: every contraction on the
- * tcgen05 tensor cores with the accumulator in tensor memory; dense FFN of
- * whole 64-column chunks, hidden size a multiple of 64, 64-dim heads, bf16
- * weights -- "Megakernels in LLM Inference When Fusion Actually Wins",
- * sections "Core Tradeoff" and "When Megakernels Win", the batch range up
- * to 32 where the crossover lies).
+ * Batch capacity: max_batch 1 (the batch-1 variants), 2..32 (the wide-batch
+ * variant: every contraction on the tcgen05 tensor cores with the
+ * accumulator in tensor memory; dense FFN of whole 64-column chunks, hidden
+ * size a multiple of 64, 64-dim heads, bf16 weights -- "Megakernels in LLM
+ * Inference When Fusion Actually Wins", sections "Core Tradeoff" and "When
+ * Megakernels Win", the batch range up to 32 where the crossover lies) or
+ * 2..8 (the batched variant, warp-level mma.sync: other shapes, or
+ * batched_variant 1).
  * Errors: MK_ERR_INVALID_ARG for a NULL or non-16-byte-aligned pointer or an
  * inconsistent shape, MK_ERR_UNSUPPORTED (no compiled variant, or a wide
  * batch outside the conditions above), MK_ERR_CUDA.

@@ -120,15 +120,17 @@ def test_batch8_variant_ragged_lengths():
 
 
 def _bsplit_cfg(batch):
+    # the batched (mma.sync) variant, which the descriptor asks for: this
+    # shape would run on the wide-batch variant by default
     return synth.custom(n_layers=2, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=64,
                         ffn=2048, vocab=5000, batch=batch, prefill=(0, 300), steps=3,
-                        rope_theta=5e5)
+                        rope_theta=5e5, batched_variant=1)
 
 
-@pytest.mark.parametrize("batch", [7, 5])
+@pytest.mark.parametrize("batch", [7, 5, 8])
 def test_batched_split_mlp(batch):
-    # batch 2..7 with an FFN of whole 512-column chunks (the batch-8 variant;
-    # at 8 sequences the wide one takes over): gate/up slices write h as
+    # batch 2..8 with an FFN of whole 512-column chunks on the batched
+    # variant: gate/up slices write h as
     # tensor-core fragments, 16-row down units stream them next to their
     # weights (padded rows past the batch)
     run_steps(_bsplit_cfg(batch), 3, seed=17)
@@ -150,7 +152,8 @@ def test_batched_split_mlp_ragged_ffn_chunks():
     # FFN of 3 chunks of 512 and a short vocabulary: down runs that start and
     # end inside chunks, two-chunk runs, and every SM's share under one chunk
     cfg = synth.custom(n_layers=2, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=64,
-                       ffn=1536, vocab=3000, batch=6, prefill=(5, 400), steps=3, rope_theta=5e5)
+                       ffn=1536, vocab=3000, batch=6, prefill=(5, 400), steps=3, rope_theta=5e5,
+                       batched_variant=1)
     run_steps(cfg, 3, seed=29)
 
 

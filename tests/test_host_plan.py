@@ -239,8 +239,8 @@ def test_checker_rejects_plain_wait_on_relaxed_signals():
 
 
 def test_batched_split_mlp_cuts_whole_tiles():
-    # 7 sequences: the batch-8 variant (at 8 the wide variant takes this shape)
-    cfg, d = desc("llama1b_b8", batch=7)
+    # 7 sequences on the batched (mma.sync) variant, asked for by the descriptor
+    cfg, d = desc("llama1b_b8", batch=7, batched_variant=1)
     st, q = L.mk_plan(d, cfg["batch"], cfg["max_seq"], 152)
     ops = [q[i] for i in range(152 * st["max_pc"]) if q[i].op in (8, 9)]
     assert all(I.r0 % 16 == 0 and I.r1 % 16 == 0 for I in ops if I.op == 8)
@@ -300,14 +300,16 @@ def test_quantize_rows_refuses_bad_arguments():
 
 
 def is_wide(cfg):
-    # the wide-batch (tcgen05) variant's plan: 9..32 sequences, or 8 on a shape it takes
+    # the wide-batch (tcgen05) variant's plan: 9..32 sequences, or 2..8 on a
+    # shape it takes unless the batched (mma.sync) variant is asked for
     b, dense = cfg["batch"], cfg["n_experts"] == 0
-    return dense and (b > 8 or (b == 8 and cfg["ffn"] % 64 == 0 and cfg["hidden"] % 64 == 0 and
-                                cfg["head_dim"] == 64 and cfg["n_q_heads"] == 4 * cfg["n_kv_heads"]))
+    shape = (cfg["ffn"] % 64 == 0 and cfg["hidden"] % 64 == 0 and cfg["head_dim"] == 64 and
+             cfg["n_q_heads"] == 4 * cfg["n_kv_heads"])
+    return dense and (b > 8 or (b >= 2 and shape and not cfg.get("batched_variant", 0)))
 
 
 def wide_coverage(cfg, q, n_sm, max_pc, splits):
-    """The wide-batch plan (9..32 sequences), re-derived in Python: every norm
+    """The wide-batch plan (2..32 sequences), re-derived in Python: every norm
     row, QKV row, attention item, O-projection (head, row), FFN column, down
     (row, 64-column chunk) and LM-head row exactly once, within the tile
     limits the tensor-core bodies rely on (at most 128 weight rows per
@@ -384,7 +386,7 @@ def wide_coverage(cfg, q, n_sm, max_pc, splits):
     assert sorted(slices) == list(range(len(slices)))
 
 
-@pytest.mark.parametrize("batch", [9, 16, 32])
+@pytest.mark.parametrize("batch", [2, 7, 9, 16, 32])
 @pytest.mark.parametrize("n_sm", [1, 7, 148, 152])
 def test_wide_plan_covers_all_work_and_is_deadlock_free(batch, n_sm):
     cfg, d = desc("llama1b_b8", batch=batch)

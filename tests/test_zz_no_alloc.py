@@ -35,10 +35,11 @@ CASES = {
                               ffn=0, vocab=3001, tied=False, n_experts=16, top_k=4,
                               expert_ffn=200, shared_ffn=500, rope_theta=5e5, prefill=(70, 70),
                               steps=4),
-    # five sequences, ragged lengths, the batched split MLP (h as fragments)
+    # five sequences, ragged lengths, the batched variant's split MLP (h as
+    # fragments), which the descriptor asks for
     "batch5": synth.custom(n_layers=2, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=64,
                            ffn=2048, vocab=5000, batch=5, prefill=(0, 300), steps=4,
-                           rope_theta=5e5),
+                           rope_theta=5e5, batched_variant=1),
     # eight sequences: the wide tcgen05 variant
     "batch8": synth.custom(n_layers=2, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=64,
                            ffn=2048, vocab=5000, batch=8, prefill=(0, 300), steps=4,
