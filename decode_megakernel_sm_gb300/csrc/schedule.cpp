@@ -127,16 +127,17 @@ static int plan_build_wide(const mk_model_desc& d, int B, int max_ctx, int n_sm,
   const long R = (long)Hkv * GR;
   const int Bp = wide_bp(B);
   CtrMap cm{Hkv, L};
-  // split-KV: whole sequences once the (sequence, kv head) pairs number half
-  // the SMs or more (no merge, no arrival count: on the tensor cores a whole
-  // 2K-position sequence costs less than the merge); below that, enough
-  // slices for the items to fill about half the SMs, at least two (measured
-  // at 8 sequences x 8 kv heads: 1, 2, 3 slices give 1.074, 1.037, 1.121 ms
-  // per step; at 16 and 32 sequences one slice is best), and at least 16
-  // positions per slice at max_ctx.  Items are dealt out slice-major and
-  // round-robin, so that each SM's items come from different sequences.
+  // split-KV: as many slices per (sequence, kv head) pair as keep the items
+  // at one per SM (an SM's second item doubles the phase; whole sequences
+  // once the pairs number the SMs), at most 4 (each slice adds to the
+  // merge), at least 16 positions per slice at max_ctx.  Measured per step
+  // with 8 kv heads (ms, slices 1 / 2 / 3 / 4): 4 sequences 0.898 / 0.882 /
+  // 0.873 / 0.861, 8 sequences 0.955 / 0.940 / 1.020 / 0.984, 12 sequences
+  // 1.022 / 1.127 / 1.086 / 1.132; 2 sequences with 4 / 6 / 9 slices 0.837 /
+  // 0.844 / 0.848.  Items are dealt out slice-major and round-robin, so that
+  // each SM's items come from different sequences.
   const int pairs = B * Hkv;
-  int S = 2 * pairs >= n_sm ? 1 : std::max(2, n_sm / (2 * pairs));
+  int S = std::min(4, std::max(1, n_sm / pairs));
   S = std::min(S, std::max(1, max_ctx / 16));
   const int n_items = B * Hkv * S;
   std::vector<std::vector<Instr>> qs(n_sm);

@@ -7,9 +7,9 @@ wherever the oracle's top-2 margin exceeds 5e-2, the GPU argmax the first
 maximum of its own logits, and the appended K/V rows within one bf16 ulp.
 The shapes cover batches that fill 8-sequence groups exactly (16, 32) and
 ones that do not (2, 5, 9, 13: zero operand rows up to the next multiple of 8),
-one attention item per (sequence, kv head) (pairs at least half the SMs) and
-split-KV slices merged by the last arriver (fewer pairs), cache lengths of
-0..2 rows (slices with no cached rows),
+one attention item per (sequence, kv head) (pairs at least as many as the
+SMs) and split-KV slices merged by the last arriver (fewer pairs), cache
+lengths of 0..2 rows (slices with no cached rows),
 an FFN with an odd number of 64-column chunks and a vocabulary that is not a
 multiple of 8 (the LM head's last instruction reads zero-padded rows), ring
 stages of 32, 48 and 64 KB (the default; 16 KB is refused), several steps per launch, the multi-launch ablation,
