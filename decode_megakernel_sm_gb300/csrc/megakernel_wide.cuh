@@ -10,15 +10,18 @@
 // bits of the activation ("Megakernels in LLM Inference When Fusion
 // Actually Wins", sections "Core Tradeoff" and "When Megakernels Win": the
 // batch range where the contraction turns from a GEMV into a skinny GEMM).
-// The accumulator lives in tensor memory (64 columns allocated once per CTA
-// for the life of the kernel); consumer warps 0-3 read it back with
-// tcgen05.ld, one accumulator row (one weight row) per thread, and add the
-// high and low columns of each sequence.
+// Consumer warps 0 .. WIDE_NI - 1 each issue the MMAs of every WIDE_NI-th K
+// chunk into an accumulator of their own in tensor memory (64 columns each,
+// allocated once per CTA for the life of the kernel); consumer warps 0-3 read
+// them back with tcgen05.ld, one accumulator row (one weight row) per
+// thread, sum the accumulators and add the high and low columns of each
+// sequence.
 //
-// A stage is released to the producer by a tcgen05.commit on its empty
-// barrier (warp 0's arrival), which fires once the MMAs have read it; the
-// other consumer warps arrive as usual.  The accumulator is complete when a
-// second commit, on the CTA's MMA-done barrier, fires.
+// A stage is released to the producer by a tcgen05.commit of each issuing
+// warp on its empty barrier (that warp's arrival), which fires once the
+// warp's MMAs have read it; the other consumer warps arrive as usual.  The
+// accumulators are complete when each issuing warp's commit on the CTA's
+// MMA-done barrier has fired.
 #pragma once
 #include "mk_tc.cuh"
 

@@ -56,7 +56,7 @@ MK_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                : "memory");
 }
 
-// D[tmem] (+)= A[adesc] * B[bdesc]^T, M x N x 16, issued by one thread.
+// D[tmem] (+)= A[adesc] * B[bdesc]^T, M x N x 16, issued by the calling thread.
 MK_DEV void tc_mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                         bool accumulate) {
   asm volatile(
