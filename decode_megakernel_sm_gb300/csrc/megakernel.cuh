@@ -2310,19 +2310,18 @@ MK_DEV void producer(const Globals& g, unsigned char* ring, uint32_t full0, uint
           const uint32_t dst = ring_s + (uint32_t)st * (uint32_t)g.stage_bytes;
           const bool wseg = NB > 8 && s[k].wide();
           if (wseg) {
-            // chunk j: its weight piece at j * unit, its operand piece (if
-            // the operand is streamed; unit2 > 0) at ups * unit + j * unit2
+            // chunk j: its weight piece at j * unit; the stage's operand
+            // pieces (if the operand is streamed; unit2 > 0) are contiguous
+            // at both ends, one copy to ups * unit
             const uint32_t u2 = s[k].unit2();
             mbar_expect_tx(full, n * (s[k].unit + u2));
-            for (uint32_t j = 0; j < n; j++) {
+            if (u2)
+              bulk_g2s(dst + s[k].ups * s[k].unit,
+                       copy_src(g, I, s[k].src2 + (size_t)u0 * u2, n * u2, pc), n * u2, full, pol_kv);
+            for (uint32_t j = 0; j < n; j++)
               bulk_g2s(dst + j * s[k].unit,
                        copy_src(g, I, s[k].src + (size_t)(u0 + j) * s[k].pitch(), s[k].unit, pc),
                        s[k].unit, full, pol_w);
-              if (u2)
-                bulk_g2s(dst + s[k].ups * s[k].unit + j * u2,
-                         copy_src(g, I, s[k].src2 + (size_t)(u0 + j) * u2, u2, pc), u2, full,
-                         pol_kv);
-            }
           } else if (attn_tc_path<D, HPG, NB>() && g.tmaps && I.op == OP_ATTN && !g.kv_block) {
             // tensor-core attention: the K and V rows as tiled TMA boxes of
             // 64 rows in the 128-byte swizzle (the box past the item's last
