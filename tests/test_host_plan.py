@@ -210,6 +210,22 @@ def test_plan_rejects_bad_arguments():
     with pytest.raises(L.MkError) as e:
         L.mk_plan(d2, 1, 64, 8)
     assert e.value.status == L.MK_ERR_UNSUPPORTED
+    _, d3 = desc("tiny", batched_variant=2)  # 0 or 1 only
+    with pytest.raises(L.MkError) as e:
+        L.mk_plan(d3, 1, 64, 8)
+    assert e.value.status == L.MK_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("variant", [0, 1])
+def test_batched_variant_picks_the_plan(variant):
+    # 2..8 sequences on a shape the wide variant takes: its plan (NORM
+    # instructions, tensor-core tiles) unless the descriptor asks for the
+    # batched mma.sync variant (whole-tile split MLP, no NORM instructions)
+    cfg, d = desc("llama1b_b8", batch=4, batched_variant=variant)
+    st, q = L.mk_plan(d, 4, cfg["max_seq"], 152)
+    ops = {q[i].op for i in range(152 * st["max_pc"])}
+    assert (10 in ops) == (variant == 0)
+    assert is_wide(cfg) == (variant == 0)
 
 
 def test_split_mlp_residual_hop_is_tagged():
