@@ -59,3 +59,19 @@ def test_stress_int8_paged():
         r.step()
     finally:
         r.close()
+
+
+@pytest.mark.parametrize("variant", [0, 1])
+def test_stress_batch5_split_attention(variant):
+    # 5 sequences: the wide variant, whose attention runs 4 split-KV slices per
+    # (sequence, kv head) merged by the last arriving item (0), or the batched
+    # mma.sync variant (1); one step, then a multi-step launch
+    cfg = synth.custom(n_layers=2, hidden=2048, n_q_heads=8, n_kv_heads=2, head_dim=64, ffn=2048,
+                       vocab=5000, batch=5, prefill=(0, 300), steps=5, rope_theta=5e5,
+                       batched_variant=variant)
+    r = Run(cfg, seed=99 + variant, stress=(4000, 9 + variant, True))
+    try:
+        r.step()
+        r.multi_step(2)
+    finally:
+        r.close()
