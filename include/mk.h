@@ -51,7 +51,7 @@ typedef struct mk_handle mk_handle;
  * batched_variant picks the kernel for max_batch 2..8 on a dense shape with
  * 64-dim heads, four query heads per kv head and hidden / ffn multiples of
  * 64: 0 (default) the wide-batch variant (every contraction on tcgen05 with
- * tensor-memory accumulators; measured 13-20 % faster per step at 2, 4 and
+ * tensor-memory accumulators; measured 14-21 % faster per step at 2, 4 and
  * 7 sequences), 1 the batched variant (warp-level mma.sync).  Other shapes
  * and max_batch 9..32 ignore it (the wide-batch variant).  "Megakernels in LLM Inference When Fusion
  * Actually Wins", section "Core Tradeoff", frames the batch ranges.        */
