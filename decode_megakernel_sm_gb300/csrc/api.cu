@@ -377,11 +377,16 @@ static int create_impl(const mk_model_desc* desc, const mk_weights* w, const mk_
   // the dependency hops; half the bytes per row keep the bodies fed)
   if (wfmt == MK_WEIGHTS_INT8) h->max_stages = 4;
   if (h->var->NB > 8) h->stage_bytes = WIDE_STAGE_BYTES;
+  if (h->var->NB == 1 && wfmt != MK_WEIGHTS_INT8) h->stage_bytes = BATCH1_STAGE_BYTES;
   // ---- device
   CK(cudaGetDevice(&h->dev));
   CK(cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, h->dev));
   {
-    const int st = size_ring(h, h->stage_bytes);
+    int st = size_ring(h, h->stage_bytes);
+    // a one-sequence shape whose fixed buffers leave no room for two 64 KB
+    // stages takes the general default
+    if (st == MK_ERR_UNSUPPORTED && h->var->NB == 1 && h->stage_bytes > DEFAULT_STAGE_BYTES)
+      st = size_ring(h, DEFAULT_STAGE_BYTES);
     if (st != MK_OK) return st;
   }
   CK(cudaStreamCreateWithFlags(&h->own, cudaStreamNonBlocking));

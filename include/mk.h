@@ -340,8 +340,9 @@ int mk_set_wait_timeout(mk_handle* h, uint64_t ns);
 int mk_set_l2_prefetch(mk_handle* h, uint64_t bytes_ahead);
 
 /* Bytes per shared-memory ring stage: 16384, 32768, 49152 or 65536
- * (default 32768; 65536 on a wide-batch handle, whose consumer pays a
- * tensor-core commit per stage).  The ring holds as many stages (2..16) as the device's
+ * (default 65536 on a one-sequence bf16 handle where two such stages fit,
+ * and on a wide-batch handle, whose consumer pays a tensor-core commit per
+ * stage; 32768 on int8 and on batched mma.sync handles).  The ring holds as many stages (2..16) as the device's
  * opt-in shared memory allows next to the kernel's fixed buffers.  Bigger
  * stages hold more weight rows, so every consumer warp has rows in each
  * stage; smaller stages give a deeper ring.  Results do not depend on it.

@@ -59,7 +59,9 @@ def run_steps(cfg, steps, seed, **kw):
 def test_int8_decode_against_oracle():
     r = Run(_cfg(), 71, int8=True)
     try:
-        assert r.dec.info()["n_stages"] == 4  # the int8 default ring depth
+        info = r.dec.info()
+        assert info["n_stages"] == 4  # the int8 default ring depth
+        assert info["stage_bytes"] == 32768
         for _ in range(3):
             r.step()
     finally:

@@ -31,10 +31,21 @@ def test_ragged_small_shape_parity():
     run_steps(cfg, 4, seed=3)
 
 
-@pytest.mark.parametrize("sb", [16384, 49152, 65536])
+def test_batch1_default_stage_size():
+    # one bf16 sequence: 64 KB stages unless the caller asks otherwise
+    r = Run(synth.CONFIGS["tiny"], seed=5)
+    try:
+        info = r.dec.info()
+        assert info["stage_bytes"] == 65536 and info["n_stages"] >= 2
+        r.step()
+    finally:
+        r.close()
+
+
+@pytest.mark.parametrize("sb", [16384, 32768, 49152])
 def test_ring_stage_sizes(sb):
-    # the same ragged shape with every larger stage size: more rows, more
-    # cache positions and more down rows per stage, results unchanged
+    # the same ragged shape with every stage size besides the 64 KB default:
+    # fewer rows, cache positions and down rows per stage, results unchanged
     cfg = synth.custom(n_layers=3, n_q_heads=6, n_kv_heads=3, ffn=1000, vocab=999,
                        prefill=(300, 300), steps=3)
     run_steps(cfg, 3, seed=9, stage_bytes=sb)
@@ -85,8 +96,9 @@ def test_staged_partials_many_slices():
     run_steps(cfg, 2, seed=42, stage_bytes=16384)
 
 
-def test_llama1b_large_stages():
-    r = Run(synth.CONFIGS["llama1b_1k"], seed=3, stage_bytes=65536)
+def test_llama1b_32k_stages():
+    # the bench shape with half-size stages (a deeper ring of 8-row stages)
+    r = Run(synth.CONFIGS["llama1b_1k"], seed=3, stage_bytes=32768)
     try:
         r.step()
         r.step()
@@ -141,6 +153,16 @@ def test_batched_split_mlp_stage_sizes(sb):
     # 48 KiB: one weight unit + its fragments per stage (8 KB idle per
     # half); 64 KiB: two of each
     run_steps(_bsplit_cfg(7), 3, seed=19, stage_bytes=sb)
+
+
+def test_batched_default_stage_size():
+    # the batched variant keeps 32 KB stages by default
+    r = Run(_bsplit_cfg(5), seed=23)
+    try:
+        assert r.dec.info()["stage_bytes"] == 32768
+        r.step()
+    finally:
+        r.close()
 
 
 def test_batched_split_mlp_16k_stages():
