@@ -43,10 +43,13 @@ MK_DEV size_t opnd_off(uint32_t ab, uint32_t row, uint32_t k) {
 }
 
 // Wait for the MMAs committed so far on the MMA-done barrier (all consumer
-// threads; bounded).  False if the wait gave up.
+// threads; bounded).  False if the wait gave up.  The wait does not give up
+// on an error elsewhere in the grid: the committed MMAs complete regardless,
+// so every thread returns the same value and the warps leave the op together
+// (the next dependency wait sees the error).
 template <int HT, int D, int HPG, int NB, int WB>
 MK_DEV bool wide_mma_wait(Ctx<HT, D, HPG, NB, WB>& c, const Globals& g) {
-  const bool ok = wait_mbar(g, c.mma_bar, c.mma_par, true);
+  const bool ok = wait_mbar(g, c.mma_bar, c.mma_par, false);
   c.mma_par ^= 1u;
   tc_fence_after();
   return ok;

@@ -13,13 +13,14 @@ lengths of 0..2 rows (slices with no cached rows),
 an FFN with an odd number of 64-column chunks and a vocabulary that is not a
 multiple of 8 (the LM head's last instruction reads zero-padded rows), ring
 stages of 32, 48 and 64 KB (the default; 16 KB is refused), several steps per launch, the multi-launch ablation,
+a launch that times out on a dropped instruction and the steps after it,
 and the full Llama-1B shape at 32 sequences.
 """
 import numpy as np
 import pytest
 
 import synth
-from decode_megakernel_sm_gb300 import MK_ERR_UNSUPPORTED, MkError
+from decode_megakernel_sm_gb300 import MK_ERR_TIMEOUT, MK_ERR_UNSUPPORTED, MkError
 from tests.harness import Run
 
 pytestmark = pytest.mark.gpu
@@ -91,6 +92,23 @@ def test_wide_refuses_16k_stages():
             r.dec.set_stage_bytes(16384)
         assert e.value.status == MK_ERR_UNSUPPORTED
         r.step()  # the handle keeps its ring
+    finally:
+        r.close()
+
+
+def test_wide_missing_producer_times_out_and_recovers():
+    # SM 0's first instruction (the layer-0 norm of sequence 0) never signals:
+    # every QKV instruction's wait runs out, the launch ends with a timeout
+    # status (its tensor memory freed), and the rebuilt schedule decodes again
+    r = Run(small(16), seed=3)
+    try:
+        r.dec.set_wait_timeout(50_000_000)  # 50 ms
+        r.dec.drop_instruction(0, 0)
+        r.dec.step(r.d_tok, r.d_pos, r.d_logits, r.d_am)
+        assert r.dec.sync_status() == MK_ERR_TIMEOUT
+        r.dec.build_schedule(r.B, r.max_ctx)  # restores the dropped instruction
+        r.step()
+        r.step()
     finally:
         r.close()
 
